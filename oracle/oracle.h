@@ -1,0 +1,95 @@
+/*
+ * Flint-shaped sparse MoE layer: plain fp64 CPU oracle.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This is the slow, obviously-correct definition that the
+ * CUDA path is checked against.  Only the test suite, the package smoke check and the
+ * benchmark's CPU-baseline / reference leg may load it; the product library never does,
+ * and it shares no code, header or constant table with the CUDA sources.
+ *
+ * What it computes (sources: the Recursive Flint serving-kit post, section "The
+ * architecture, from the config", and the news article "Recursive opens Flint, a 40B
+ * coding model with 2.5B active", section "What runs on each token"):
+ *   - every MoE layer has 256 routed experts, 6 chosen per token, and one shared
+ *     expert that runs on every token; expert width 512, shared width 1024, hidden 2048;
+ *   - router scores are sigmoids of the router logits, and the chosen experts' weights
+ *     are those scores normalised over the chosen set (not a softmax).
+ * Readings where the pages are silent (each one is listed in the design notes):
+ *   - experts are SwiGLU MLPs: E(x) = (silu(x Wg) * (x Wu)) Wd, silu(z) = z / (1 + e^-z);
+ *   - an optional per-expert router bias is added to the logit before the sigmoid and is
+ *     used both for selection and for the gate values; routed scaling factor is 1;
+ *   - ties in score are broken by the lower expert index, for membership and for order;
+ *     the chosen experts are listed in (score descending, index ascending) order;
+ *   - y = shared(x) + sum_j g_j E_{sel_j}(x).
+ * Everything is evaluated in IEEE double with no rounding of intermediates; bf16 inputs
+ * are widened exactly.
+ */
+#ifndef FLINT_MOE_ORACLE_H
+#define FLINT_MOE_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct {
+  int H;                          /* hidden size */
+  int E;                          /* routed experts */
+  int k;                          /* experts chosen per token */
+  int I;                          /* routed expert width */
+  int Is;                         /* shared expert width */
+  const uint16_t* w_router;       /* bf16 bits [H][E] */
+  const float* router_bias;       /* [E] or NULL */
+  const uint16_t* const* w_gate;  /* E pointers, each bf16 [H][I]; NULL = not supplied */
+  const uint16_t* const* w_up;    /* E pointers, each bf16 [H][I] */
+  const uint16_t* const* w_down;  /* E pointers, each bf16 [I][H] */
+  const uint16_t* ws_gate;        /* bf16 [H][Is] */
+  const uint16_t* ws_up;          /* bf16 [H][Is] */
+  const uint16_t* ws_down;        /* bf16 [Is][H] */
+} oracle_layer;
+
+/* Error codes (0 = ok). */
+#define ORACLE_OK 0
+#define ORACLE_EINVAL 1
+#define ORACLE_EMISSING_EXPERT 2
+
+double oracle_bf16_to_f64(uint16_t bits);
+
+/* logits[t][e] = sum_h x[t][h] Wr[h][e] + b[e];  s[t][e] = 1 / (1 + exp(-logits)). */
+int oracle_router(const double* x, int T, int H, int E, const uint16_t* w_router,
+                  const float* bias, double* logits, double* scores);
+
+/* One token: the first k experts in (score desc, index asc) order, their normalised
+ * gates, and gaps[j] = s_(j) - s_(j+1) for j = 0..k-1 (gaps[k-1] is the k-th minus the
+ * (k+1)-th score, or +inf when k == E). */
+int oracle_select(const double* scores, int E, int k, int32_t* idx, double* gates, double* gaps);
+
+/* One SwiGLU MLP on one row: out = (silu(x Wg) * (x Wu)) Wd.  Wg, Wu: [H][I]; Wd: [I][H].
+ * hbuf: scratch of I doubles. */
+void oracle_swiglu(const double* x, int H, int I, const uint16_t* wg, const uint16_t* wu,
+                   const uint16_t* wd, double* out, double* hbuf);
+
+/* The whole layer on T rows of x ([T][H], double).  y: [T][H].  Optional outputs (may be
+ * NULL): idx [T][k], gates [T][k], gaps [T][k], scores [T][E]. */
+int oracle_moe_forward(const oracle_layer* L, const double* x, int T, double* y,
+                       int32_t* idx, double* gates, double* gaps, double* scores);
+
+/* Same layer with the chosen experts given (idx [T][k]) instead of selected: gates are the
+ * fp64 scores of the given experts normalised over them.  Used to re-evaluate tokens whose
+ * top-k is decided by a near tie. */
+int oracle_moe_forward_given(const oracle_layer* L, const double* x, int T, const int32_t* idx,
+                             double* y);
+
+/* Stable counting sort of the (token, slot) pairs by expert.  idx: [T][k].
+ * counts[E]; offsets[E+1] (exclusive scan); perm[T*k]: sorted row -> pair t*k+j;
+ * inv[T*k]: pair -> sorted row.  Pairs of one expert keep (t, j) order. */
+int oracle_permute(const int32_t* idx, int T, int k, int E, int32_t* counts, int32_t* offsets,
+                   int32_t* perm, int32_t* inv);
+
+/* r[t] = x[t] / sqrt(mean_h x[t][h]^2 + eps)  (unit weight). */
+void oracle_rmsnorm(const double* x, int T, int H, double eps, double* r);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,180 @@
+"""Seeded synthetic inputs for the Flint-shaped MoE layer.
+
+This module is shared by the fp64 oracle side (tests, CPU baseline) and the CUDA
+side (tests, bench).  It holds no arithmetic of the MoE method itself: it only
+draws numbers.  Every value is a pure function of (seed, tag, element index), so
+any slice of any tensor can be regenerated without generating the rest, and the
+device twin (``synth/gen.cu``) produces bit-identical arrays on the GPU.
+
+Generator (the same on host and device):
+
+* stream: splitmix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number
+  generators", OOPSLA 2014).  The per-tensor state is
+  ``key = mix64(mix64(seed + GOLDEN) ^ (tag * TAGMUL))``; element ``i`` consumes
+  outputs ``2i+1`` and ``2i+2`` of the stream started at ``key``, i.e.
+  ``z_j = mix64(key + j * GOLDEN)`` (all arithmetic mod 2**64).
+* normal deviate: Box--Muller (Box and Muller, 1958),
+  ``u1 = ((z1 >> 11) + 1) * 2**-53`` in (0, 1], ``u2 = (z2 >> 11) * 2**-53`` in
+  [0, 1), ``n = sqrt(-2 ln u1) * cos(2*pi*u2)`` in float64.
+* value: ``float32(sigma * n)`` (round to nearest), then bfloat16 by
+  round-to-nearest-even on the float32 bits.
+
+Host and device use different libm ``log``/``cos``; a last-bit difference in
+float64 changes the bf16 result only when it straddles a rounding boundary, a
+chance of order 2**-45 per element.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import numpy as np
+
+GOLDEN = 0x9E3779B97F4A7C15
+TAGMUL = 0xD1B54A32D192ED03
+M1 = 0xBF58476D1CE4E5B9
+M2 = 0x94D049BB133111EB
+TWO_PI = 6.283185307179586  # the float64 nearest to 2*pi, used verbatim on both sides
+
+# Tensor tags.  The layer index of a stacked model is folded into the seed.
+TAG_X = 1
+TAG_ROUTER = 2
+TAG_BIAS = 3
+TAG_GATE = 4
+TAG_UP = 5
+TAG_DOWN = 6
+TAG_SGATE = 7
+TAG_SUP = 8
+TAG_SDOWN = 9
+TAG_PERM = 10
+
+_MASK = (1 << 64) - 1
+
+
+def mix64_int(z: int) -> int:
+    """splitmix64 output function on a Python int (reference scalar form)."""
+    z &= _MASK
+    z = ((z ^ (z >> 30)) * M1) & _MASK
+    z = ((z ^ (z >> 27)) * M2) & _MASK
+    return z ^ (z >> 31)
+
+
+def tensor_key(seed: int, tag: int) -> int:
+    return mix64_int(mix64_int((seed + GOLDEN) & _MASK) ^ ((tag * TAGMUL) & _MASK))
+
+
+def _mix64(z: np.ndarray) -> np.ndarray:
+    z = (z ^ (z >> np.uint64(30))) * np.uint64(M1)
+    z = (z ^ (z >> np.uint64(27))) * np.uint64(M2)
+    return z ^ (z >> np.uint64(31))
+
+
+def f32_to_bf16_bits(v: np.ndarray) -> np.ndarray:
+    """float32 -> bfloat16 bits, round to nearest even (inputs are finite)."""
+    b = np.ascontiguousarray(v, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    b = b + np.uint64(0x7FFF) + ((b >> np.uint64(16)) & np.uint64(1))
+    return (b >> np.uint64(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def normal_bf16_at(seed: int, tag: int, idx, sigma: float) -> np.ndarray:
+    """bf16 bits of elements ``idx`` (any int array) of tensor (seed, tag)."""
+    with np.errstate(over="ignore"):
+        idx = np.asarray(idx, dtype=np.uint64)
+        key = np.uint64(tensor_key(seed, tag))
+        g = np.uint64(GOLDEN)
+        z1 = _mix64(key + (np.uint64(2) * idx + np.uint64(1)) * g)
+        z2 = _mix64(key + (np.uint64(2) * idx + np.uint64(2)) * g)
+    u1 = ((z1 >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)
+    u2 = (z2 >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+    n = np.sqrt(-2.0 * np.log(u1)) * np.cos(TWO_PI * u2)
+    return f32_to_bf16_bits((float(sigma) * n).astype(np.float32))
+
+
+def normal_bf16(seed: int, tag: int, n: int, sigma: float, start: int = 0,
+                chunk: int = 1 << 22) -> np.ndarray:
+    """bf16 bits of elements [start, start+n) of tensor (seed, tag)."""
+    out = np.empty(n, dtype=np.uint16)
+    for c0 in range(0, n, chunk):
+        c1 = min(n, c0 + chunk)
+        out[c0:c1] = normal_bf16_at(seed, tag, np.arange(start + c0, start + c1, dtype=np.uint64), sigma)
+    return out
+
+
+def permutation(seed: int, n: int) -> np.ndarray:
+    """A seeded permutation of range(n): argsort of splitmix64 draws (ties by index)."""
+    with np.errstate(over="ignore"):
+        key = np.uint64(tensor_key(seed, TAG_PERM))
+        z = _mix64(key + (np.arange(n, dtype=np.uint64) + np.uint64(1)) * np.uint64(GOLDEN))
+    return np.argsort(z, kind="stable").astype(np.int64)
+
+
+# --------------------------------------------------------------------------------------
+# Device twin (synth/gen.cu -> synth/libsynth.so).  Only data generation lives there.
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+
+def lib_path() -> str:
+    return os.path.join(_HERE, "libsynth.so")
+
+
+def build(verbose: bool = False) -> str:
+    import subprocess
+    src = os.path.join(_HERE, "gen.cu")
+    out = lib_path()
+    cmd = ["nvcc", "-O3", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",
+           "-Xcompiler", "-fPIC", "-shared", "-o", out, src]
+    if verbose:
+        print(" ".join(cmd))
+    subprocess.check_call(cmd)
+    return out
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"synth device generator not built: {path} (run __graft_entry__.build())")
+        _LIB = ctypes.CDLL(path)
+        _LIB.synth_normal_bf16.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint64,
+                                           ctypes.c_uint64, ctypes.c_uint32, ctypes.c_double,
+                                           ctypes.c_void_p]
+        _LIB.synth_normal_bf16.restype = ctypes.c_int
+    return _LIB
+
+
+def device_normal_bf16(dst_ptr: int, n: int, seed: int, tag: int, sigma: float,
+                       start: int = 0, stream: int = 0) -> None:
+    """Fill ``n`` bf16 values at device pointer ``dst_ptr`` with elements
+    [start, start+n) of tensor (seed, tag); bit-identical to :func:`normal_bf16`."""
+    rc = _lib().synth_normal_bf16(ctypes.c_void_p(dst_ptr), n, start, seed & _MASK, tag,
+                                  float(sigma), ctypes.c_void_p(stream))
+    if rc != 0:
+        raise RuntimeError(f"synth_normal_bf16 failed with CUDA error {rc}")
+
+
+def torch_normal_bf16(shape, seed: int, tag: int, sigma: float, device="cuda", start: int = 0):
+    """A torch bf16 tensor of ``shape`` filled by the generator (device or host)."""
+    import torch
+    n = int(np.prod(shape))
+    if str(device).startswith("cuda"):
+        t = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        if n:
+            device_normal_bf16(t.data_ptr(), n, seed, tag, sigma, start,
+                               torch.cuda.current_stream(t.device).cuda_stream)
+        return t
+    bits = normal_bf16(seed, tag, n, sigma, start)
+    return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).reshape(shape)
+
+
+SIGMA_X = 1.0
+SIGMA_ROUTER = 1.0 / math.sqrt(2048.0)
+SIGMA_EXPERT = 0.02
+SIGMA_BIAS = math.sqrt(0.5)
