@@ -1,0 +1,358 @@
+"""Benchmark of the Flint MoE layer on B300 (one JSON line on stdout).
+
+Default workload: the decode sweep -- one Flint-shaped layer (seed-0 weights) run at
+T = 1, 2, 4, 8, 16, 32, 64 tokens (x ~ N(0,1) bf16, seed 1000+T).  One step is one forward
+at every T of the sweep (127 tokens); L2 is flushed (a 512 MB write) before every forward,
+outside the timed spans; each forward is timed with CUDA events on its stream.  value =
+tokens of all ranks / max over ranks of the summed forward times.
+
+Other workloads (--workload): single (T=16, seed 0), prefill (T=8192, router bias
+~N(0, 0.5)), stack (47 pre-norm residual layers, T=256), adversarial (T=16384, +8/-8 bias
+with tied router columns).
+
+Multi-GPU (torchrun, one rank per GPU): independent replicas, no collective on the data
+path; ranks only meet at the timing barriers.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+SWEEP = (1, 2, 4, 8, 16, 32, 64)
+METRIC = "MoE-layer tokens/s on 1 B300; HBM GB/s (decode) / tensor TFLOPS (prefill) vs peak"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=p["hbm_gbs"], bf16_tflops=p["bf16_tflops"],
+                    bf16_tflops_sustained=p.get("bf16_tflops_sustained"), source="measured")
+    return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"])
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return dict(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=max(smax) if smax else None,
+                    reasons=sorted(reasons), samples=len(sm))
+
+
+def dist_setup():
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import synth
+    import sparse_moe_layer_15_b300 as fm
+    from sparse_moe_layer_15_b300 import accounting as acc
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(max(4 * l2, 512 << 20), dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    w = synth.flint_weights(seed=0, device=dev)
+    layer = fm.FlintMoE(w, max_tokens=max(SWEEP))
+    xs = {T: synth.torch_normal_bf16((T, fm.HIDDEN), 1000 + T, synth.TAG_X, 1.0, device=dev) for T in SWEEP}
+    ys = {T: torch.empty_like(xs[T]) for T in SWEEP}
+    idx = {T: torch.empty((T, fm.TOP_K), dtype=torch.int32, device=dev) for T in SWEEP}
+    gw = {T: torch.empty((T, fm.TOP_K), dtype=torch.float32, device=dev) for T in SWEEP}
+    ev = {T: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for T in SWEEP}
+
+    def step(times):
+        for T in SWEEP:
+            flush()
+            a, b = ev[T]
+            a.record(stream)
+            layer.forward(xs[T], y=ys[T], topk_idx=idx[T], topk_w=gw[T])
+            b.record(stream)
+        torch.cuda.synchronize()
+        for T in SWEEP:
+            times[T].append(ev[T][0].elapsed_time(ev[T][1]))
+
+    warm = {T: [] for T in SWEEP}
+    for _ in range(args.warmup):
+        step(warm)
+    if layer.poll_device_status() != 0:
+        raise RuntimeError("device status error during warm-up")
+    # touched experts per T (for the algorithmic bytes)
+    U = {}
+    for T in SWEEP:
+        _, _, c = layer.route(xs[T])
+        torch.cuda.synchronize()
+        U[T] = int((c > 0).sum().item())
+
+    times = {T: [] for T in SWEEP}
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall = time.perf_counter()
+    for _ in range(args.steps):
+        step(times)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    barrier(world)
+    if layer.poll_device_status() != 0:
+        raise RuntimeError("device status error in the timed region")
+
+    ms_step_local = sum(statistics.mean(times[T]) for T in SWEEP)
+    ms_step = max_over_ranks(ms_step_local, world)
+    tokens_step = sum(SWEEP)
+    value = world * tokens_step / (ms_step * 1e-3)
+
+    sweep = {}
+    for T in SWEEP:
+        med = statistics.median(times[T])
+        b = acc.algorithmic_bytes(U[T], T)
+        sweep[str(T)] = dict(us=round(med * 1e3, 2), tokens_per_s=round(T / (med * 1e-3), 1), touched_experts=U[T],
+                             alg_bytes=b, gbs=round(b / (med * 1e-3) / 1e9, 1),
+                             hbm_frac=round(b / (med * 1e-3) / 1e9 / peaks["hbm_gbs"], 4))
+
+    # per-kernel times (second pass with kernel events; same workload, same flushes)
+    layer.enable_kernel_timing(True)
+    kt = {}
+    for _ in range(max(3, min(args.steps, 10))):
+        for T in SWEEP:
+            flush()
+            layer.forward(xs[T], y=ys[T], topk_idx=idx[T], topk_w=gw[T])
+            for name, ms in layer.kernel_times():
+                kt.setdefault(name, {}).setdefault(T, []).append(ms)
+    layer.enable_kernel_timing(False)
+    kernels = {}
+    for name, per_t in kt.items():
+        kernels[name] = {str(T): round(statistics.median(v) * 1e3, 2) for T, v in per_t.items()}
+    # dominant kernel: largest summed time over the sweep
+    dom = max(kt, key=lambda n: sum(statistics.mean(v) for v in kt[n].values()))
+
+    def kernel_bytes(name, T):
+        u = U[T]
+        if name.startswith("stream_k1"):
+            return 2 * (fm.HIDDEN * fm.N_EXPERTS + 2 * fm.HIDDEN * fm.SHARED_INTER) + 2 * fm.HIDDEN * T
+        if name.startswith("stream_k2"):
+            return 2 * (u * 2 * fm.HIDDEN * fm.EXPERT_INTER + fm.SHARED_INTER * fm.HIDDEN)
+        if name.startswith("stream_k3"):
+            return 2 * (u * fm.EXPERT_INTER * fm.HIDDEN) + 2 * fm.HIDDEN * T
+        return 2 * 2 * fm.HIDDEN * T
+
+    dom_bytes = sum(kernel_bytes(dom, T) for T in SWEEP) / len(SWEEP)
+    dom_ms = sum(statistics.mean(kt[dom][T]) for T in SWEEP) / len(SWEEP)
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    roofline = dict(bound="hbm", kernel=dom, achieved=round(achieved, 1), peak=peaks["hbm_gbs"], unit="GB/s",
+                    frac=round(achieved / peaks["hbm_gbs"], 4), traffic=None,
+                    peak_source=peaks["source"], note="per-launch mean over the sweep's T values")
+
+    # end to end through the C ABI with host buffers (H2D of x and D2H of y inside the span)
+    xh = {T: xs[T].cpu().pin_memory() for T in SWEEP}
+    yh = {T: torch.empty_like(xh[T]).pin_memory() for T in SWEEP}
+    e2e_t = {T: [] for T in SWEEP}
+    for it in range(args.warmup + args.steps):
+        for T in SWEEP:
+            flush()
+            a, b = ev[T]
+            a.record(stream)
+            layer.forward_host(xh[T], yh[T])
+            b.record(stream)
+        torch.cuda.synchronize()
+        if it >= args.warmup:
+            for T in SWEEP:
+                e2e_t[T].append(ev[T][0].elapsed_time(ev[T][1]))
+    e2e_ms = max_over_ranks(sum(statistics.mean(e2e_t[T]) for T in SWEEP), world)
+    e2e = dict(value=round(world * tokens_step / (e2e_ms * 1e-3), 1), unit="tokens/s",
+               h2d_bytes_per_step=2 * fm.HIDDEN * tokens_step, d2h_bytes_per_step=2 * fm.HIDDEN * tokens_step)
+
+    out = dict(metric=METRIC, value=round(value, 1), unit="tokens/s", n_gpus=world, steps=args.steps,
+               warmup=args.warmup, ms_per_step=round(ms_step, 4), higher_is_better=True, scaling="weak",
+               vs_baseline=None, dtype="bf16", data="synthetic",
+               config=dict(workload="decode sweep: one Flint MoE layer (H2048 E256 top6 I512 shared1024), "
+                                    "T=1,2,4,8,16,32,64 per step",
+                           tokens_per_step=tokens_step, parallelism=f"replicas x{world}",
+                           l2="flushed (512 MB write) before every forward"),
+               sweep=sweep, kernels_us=kernels, roofline=roofline, e2e=e2e,
+               gpu_launches=args.steps * len(SWEEP) * 3, clocks=clk, wall_s=round(wall, 3))
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, xs, budget_s=args.cpu_budget)
+    layer.close()
+    return out
+
+
+# ----------------------------------------------------------------------------- oracle timing
+
+def cpu_baseline(w, xs, budget_s=20.0, sample=(1, 2, 4, 8)):
+    """The fp64 oracle (single thread) on the first tokens of the sweep, until the budget."""
+    import oracle
+    from tests import parity
+
+    layer = parity.oracle_layer(w)
+    n_tok = 0
+    t0 = time.perf_counter()
+    done = []
+    for T in sample:
+        x64 = oracle.bf16_to_f64(parity.to_np_bf16(xs[T]))
+        oracle.forward(layer, x64, nthreads=1)
+        n_tok += T
+        done.append(T)
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return dict(value=round(n_tok / dt, 3), unit="tokens/s", cores=1, kind="oracle",
+                sample=f"decode-sweep forwards at T={done} ({n_tok} tokens), fp64, one thread")
+
+
+def run_reference(args, rank, world, local):
+    """--impl reference: the fp64 CPU oracle as the reference arm (rank 0 only)."""
+    import torch
+
+    import synth
+    import oracle
+    from tests import parity
+
+    sample = (1, 2, 4, 8)
+    w = synth.flint_weights(seed=0, device="cuda" if torch.cuda.is_available() else "cpu")
+    layer = parity.oracle_layer(w)
+    xin = {T: oracle.bf16_to_f64(parity.to_np_bf16(synth.torch_normal_bf16((T, 2048), 1000 + T, synth.TAG_X, 1.0,
+                                                                          device="cpu"))) for T in sample}
+
+    def step():
+        for T in sample:
+            oracle.forward(layer, xin[T], nthreads=1)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    tok = sum(sample) * args.steps
+    v = tok / dt
+    return dict(metric=METRIC, value=round(v, 3), unit="tokens/s", n_gpus=world, steps=args.steps,
+                warmup=args.warmup, ms_per_step=round(dt / args.steps * 1e3, 3), higher_is_better=True,
+                scaling="weak", vs_baseline=None, dtype="f64", data="synthetic", impl="reference",
+                config=dict(workload="decode sweep: one Flint MoE layer (H2048 E256 top6 I512 shared1024); "
+                                     "reference step = the T=1,2,4,8 forwards (15 tokens)",
+                            tokens_per_step=sum(sample), parallelism="rank 0 only"),
+                cpu_baseline=dict(value=round(v, 3), unit="tokens/s", cores=1, kind="oracle",
+                                  sample="decode-sweep forwards at T=1,2,4,8 per step, fp64, one thread"),
+                e2e=dict(value=round(v, 3), unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world, local)), flush=True)
+        return
+    out = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,137 @@
+/*
+ * flint_moe — one Flint-shaped sparse mixture-of-experts layer on an sm_103a GPU (B300).
+ *
+ * The layer (Recursive Flint serving-kit post, section "The architecture, from the config";
+ * news article "Recursive opens Flint, a 40B coding model with 2.5B active", section "What
+ * runs on each token"): hidden size 2048; 256 routed experts, 6 chosen per token by sigmoid
+ * router scores normalised over the chosen set ("normalized top-k, not softmax routing");
+ * routed expert width 512; one shared expert of width 1024 that runs on every token.
+ * Readings taken where the pages are silent: every expert is a SwiGLU MLP
+ * E(x) = (silu(x Wg) * (x Wu)) Wd; an optional per-expert router bias is added to the logit
+ * before the sigmoid and counts for both selection and gates; ties in score go to the lower
+ * expert index; y = shared(x) + sum_j g_j E_{e_j}(x).
+ *
+ * Conventions for every call below:
+ *   - All tensor pointers are caller-owned DEVICE memory unless the name ends in _host.
+ *     The library never copies, repacks or frees them; weights are borrowed for the
+ *     lifetime of the handle.
+ *   - bf16 tensors are passed as `const void*` (IEEE bfloat16, row-major, densely packed,
+ *     16-byte aligned base).  Matrices use the math orientation y = x W.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  route / forward make no host synchronisation and no allocation.
+ *   - Argument errors are returned synchronously and nothing is enqueued.
+ *   - Errors detected on the device (a bounded wait that ran out, an index out of range)
+ *     are recorded in a status word inside the workspace; they are sticky until read by
+ *     flint_moe_poll_device_status.
+ *   - A handle may be used from one stream at a time.  Results are bitwise deterministic
+ *     for identical inputs (no floating-point atomics).
+ *   - The only supported shape is the Flint layer's (hidden 2048, 256 experts, top-6,
+ *     widths 512 / 1024); any other returns FLINT_MOE_ERR_UNSUPPORTED, as does a device
+ *     that is not compute capability 10.3 (the serving kit likewise refuses configurations
+ *     it cannot run correctly rather than degrade: serving-kit post, section "What isn't
+ *     validated, and what the kit refuses to do").
+ */
+#ifndef FLINT_MOE_H
+#define FLINT_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct flint_moe_s* flint_moe_t;
+typedef struct CUstream_st* flint_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  FLINT_MOE_OK = 0,
+  FLINT_MOE_ERR_INVALID_ARG = 1,    /* NULL / misaligned pointer, T out of range, ...   */
+  FLINT_MOE_ERR_UNSUPPORTED = 2,    /* shape, flags or device not supported              */
+  FLINT_MOE_ERR_WORKSPACE = 3,      /* workspace missing, misaligned or too small        */
+  FLINT_MOE_ERR_CUDA = 4,           /* a CUDA runtime call failed                         */
+  FLINT_MOE_ERR_DEVICE_TIMEOUT = 5, /* a bounded device-side wait ran out                 */
+  FLINT_MOE_ERR_DEVICE_BOUNDS = 6   /* a device-side index check failed                   */
+} flint_moe_status;
+
+/* config.flags */
+#define FLINT_MOE_FLAG_PRE_RMSNORM 0x1u /* route and run the experts on r = x / rms(x)     */
+#define FLINT_MOE_FLAG_RESIDUAL 0x2u    /* y = x + MoE(...) (y may alias x)                 */
+
+typedef struct {
+  int hidden;       /* must be 2048 */
+  int n_experts;    /* must be 256 */
+  int top_k;        /* must be 6 */
+  int expert_inter; /* must be 512 */
+  int shared_inter; /* must be 1024 */
+  int max_tokens;   /* largest T any call on this handle will pass; 1..65536 */
+  unsigned flags;   /* FLINT_MOE_FLAG_* */
+  float rms_eps;    /* RMSNorm epsilon (used with FLINT_MOE_FLAG_PRE_RMSNORM), > 0 */
+} flint_moe_config;
+
+typedef struct {
+  const void* w_router;     /* bf16 [hidden][n_experts]                            */
+  const float* router_bias; /* fp32 [n_experts], or NULL for no bias                */
+  const void* w_gate;       /* bf16 [n_experts][hidden][expert_inter]              */
+  const void* w_up;         /* bf16 [n_experts][hidden][expert_inter]              */
+  const void* w_down;       /* bf16 [n_experts][expert_inter][hidden]              */
+  const void* ws_gate;      /* bf16 [hidden][shared_inter]                         */
+  const void* ws_up;        /* bf16 [hidden][shared_inter]                         */
+  const void* ws_down;      /* bf16 [shared_inter][hidden]                         */
+} flint_moe_weights;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* flint_moe_status_string(flint_moe_status s);
+
+/* Bytes of device workspace a handle created with `cfg` needs (written to *bytes).
+ * The caller allocates it (256-byte aligned) and keeps it alive until flint_moe_destroy. */
+flint_moe_status flint_moe_workspace_bytes(const flint_moe_config* cfg, size_t* bytes);
+
+/* Validates the configuration, the device (compute capability 10.3), pointer alignment
+ * (16 bytes) and the workspace size; builds the TMA descriptors of the weights; zeroes
+ * the workspace's counters and status word (a synchronous cudaMemset on the current
+ * device).  On success *out receives a handle owning only host-side state. */
+flint_moe_status flint_moe_create(const flint_moe_config* cfg, const flint_moe_weights* w,
+                                  void* workspace, size_t workspace_bytes, flint_moe_t* out);
+
+/* Router scoring, normalised top-k and the expert permutation only.
+ *   x        bf16 [T][hidden] (the layer input; with PRE_RMSNORM the routing uses rms(x))
+ *   topk_idx int32 [T][top_k]: chosen experts, score descending, lower index first on ties
+ *   topk_w   fp32 [T][top_k]: their normalised gates
+ *   counts   int32 [n_experts] tokens per expert, or NULL
+ * 1 <= T <= max_tokens. */
+flint_moe_status flint_moe_route(flint_moe_t h, const void* x, int T, int32_t* topk_idx,
+                                 float* topk_w, int32_t* counts, flint_stream_t stream);
+
+/* The whole layer: y bf16 [T][hidden] = shared(x') + sum_j g_j E_{e_j}(x') with x' = x, or
+ * rms(x) under PRE_RMSNORM; plus x under RESIDUAL (then y may alias x).  topk_idx / topk_w
+ * (same layout as flint_moe_route) receive the routing when not NULL.  1 <= T <= max_tokens. */
+flint_moe_status flint_moe_forward(flint_moe_t h, const void* x, int T, void* y,
+                                   int32_t* topk_idx, float* topk_w, flint_stream_t stream);
+
+/* flint_moe_forward on HOST buffers: x_host and y_host are host memory (pinned for
+ * asynchronous copies; pageable works but the copies then synchronise).  The input is
+ * copied into the workspace, the layer runs, the output is copied back, all on `stream`;
+ * the call returns once the work is enqueued (synchronise `stream` before reading y_host). */
+flint_moe_status flint_moe_forward_host(flint_moe_t h, const void* x_host, int T, void* y_host,
+                                        flint_stream_t stream);
+
+/* Synchronises `stream`, then returns and clears the device status word
+ * (FLINT_MOE_OK, FLINT_MOE_ERR_DEVICE_TIMEOUT or FLINT_MOE_ERR_DEVICE_BOUNDS). */
+flint_moe_status flint_moe_poll_device_status(flint_moe_t h, flint_stream_t stream);
+
+/* Kernel timing for profiling.  With enable != 0, later forward calls record a CUDA event
+ * pair around every kernel they launch (this serialises kernels that would otherwise
+ * overlap).  flint_moe_kernel_times synchronises on the last forward's events and writes up
+ * to `cap` entries: names[i] (static strings) and ms[i]; *n receives the count. */
+flint_moe_status flint_moe_enable_kernel_timing(flint_moe_t h, int enable);
+flint_moe_status flint_moe_kernel_times(flint_moe_t h, const char** names, float* ms, int cap,
+                                        int* n);
+
+/* Releases the handle's host state.  Does not touch the workspace or the weights. */
+flint_moe_status flint_moe_destroy(flint_moe_t h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FLINT_MOE_H */

@@ -1,0 +1,194 @@
+"""Python binding of the flint_moe C ABI (include/flint_moe.h).
+
+Argument marshalling only: every step of the layer runs in the CUDA kernels of
+``libflint_moe.so``.  PyTorch supplies device memory and streams.  There is no fallback:
+if the library is missing or the device is not an sm_103 GPU, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_NAME = "libflint_moe.so"
+
+HIDDEN, N_EXPERTS, TOP_K, EXPERT_INTER, SHARED_INTER = 2048, 256, 6, 512, 1024
+FLAG_PRE_RMSNORM = 0x1
+FLAG_RESIDUAL = 0x2
+
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "cuda error",
+          5: "device timeout", 6: "device bounds"}
+
+# Every entry point declared in include/flint_moe.h.
+EXPORTS = ("flint_moe_status_string", "flint_moe_workspace_bytes", "flint_moe_create", "flint_moe_route",
+           "flint_moe_forward", "flint_moe_forward_host", "flint_moe_poll_device_status",
+           "flint_moe_enable_kernel_timing", "flint_moe_kernel_times", "flint_moe_destroy")
+
+
+class FlintMoEError(RuntimeError):
+    def __init__(self, code, what):
+        self.code = code
+        super().__init__(f"{what}: {STATUS.get(code, code)}")
+
+
+class _Config(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int), ("n_experts", ctypes.c_int), ("top_k", ctypes.c_int),
+                ("expert_inter", ctypes.c_int), ("shared_inter", ctypes.c_int), ("max_tokens", ctypes.c_int),
+                ("flags", ctypes.c_uint), ("rms_eps", ctypes.c_float)]
+
+
+class _Weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("w_router", "router_bias", "w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down")]
+
+
+_LIB = None
+
+
+def lib_path() -> str:
+    return os.path.join(_HERE, LIB_NAME)
+
+
+def load_library():
+    """Load libflint_moe.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build() "
+                           "(python -m sparse_moe_layer_15_b300.build)")
+    L = ctypes.CDLL(path)
+    P, I32 = ctypes.c_void_p, ctypes.c_int
+    L.flint_moe_status_string.argtypes = [I32]
+    L.flint_moe_status_string.restype = ctypes.c_char_p
+    L.flint_moe_workspace_bytes.argtypes = [ctypes.POINTER(_Config), ctypes.POINTER(ctypes.c_size_t)]
+    L.flint_moe_create.argtypes = [ctypes.POINTER(_Config), ctypes.POINTER(_Weights), P, ctypes.c_size_t,
+                                   ctypes.POINTER(P)]
+    L.flint_moe_route.argtypes = [P, P, I32, P, P, P, P]
+    L.flint_moe_forward.argtypes = [P, P, I32, P, P, P, P]
+    L.flint_moe_forward_host.argtypes = [P, P, I32, P, P]
+    L.flint_moe_poll_device_status.argtypes = [P, P]
+    L.flint_moe_enable_kernel_timing.argtypes = [P, I32]
+    L.flint_moe_kernel_times.argtypes = [P, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float), I32,
+                                         ctypes.POINTER(I32)]
+    L.flint_moe_destroy.argtypes = [P]
+    for name in EXPORTS:
+        if name != "flint_moe_status_string":
+            getattr(L, name).restype = I32
+    _LIB = L
+    return L
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise FlintMoEError(rc, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def workspace_bytes(max_tokens: int, flags: int = 0, rms_eps: float = 1e-6) -> int:
+    L = load_library()
+    cfg = _Config(HIDDEN, N_EXPERTS, TOP_K, EXPERT_INTER, SHARED_INTER, max_tokens, flags, rms_eps)
+    n = ctypes.c_size_t(0)
+    _check(L.flint_moe_workspace_bytes(ctypes.byref(cfg), ctypes.byref(n)), "flint_moe_workspace_bytes")
+    return n.value
+
+
+class FlintMoE:
+    """One Flint MoE layer bound to borrowed bf16 device weights.
+
+    ``weights``: dict with torch CUDA tensors ``w_router`` [2048,256], ``w_gate``/``w_up``
+    [256,2048,512], ``w_down`` [256,512,2048], ``ws_gate``/``ws_up`` [2048,1024],
+    ``ws_down`` [1024,2048] (bf16, contiguous) and optionally ``router_bias`` [256] fp32.
+    The tensors must stay alive as long as the layer."""
+
+    def __init__(self, weights: dict, max_tokens: int, flags: int = 0, rms_eps: float = 1e-6,
+                 workspace=None):
+        import torch
+        self._L = load_library()
+        self.max_tokens = int(max_tokens)
+        self.flags = int(flags)
+        self._weights = weights  # keep the borrowed tensors alive
+        for k, v in weights.items():
+            if v is not None and not v.is_contiguous():
+                raise ValueError(f"{k} must be contiguous")
+        self._cfg = _Config(HIDDEN, N_EXPERTS, TOP_K, EXPERT_INTER, SHARED_INTER, self.max_tokens, self.flags,
+                            float(rms_eps))
+        self._w = _Weights(*[(weights[n].data_ptr() if weights.get(n) is not None else None)
+                             for n, _ in _Weights._fields_])
+        nbytes = ctypes.c_size_t(0)
+        _check(self._L.flint_moe_workspace_bytes(ctypes.byref(self._cfg), ctypes.byref(nbytes)),
+               "flint_moe_workspace_bytes")
+        dev = weights["w_router"].device
+        if workspace is None:
+            workspace = torch.empty(nbytes.value, dtype=torch.uint8, device=dev)
+        self.workspace = workspace
+        h = ctypes.c_void_p()
+        _check(self._L.flint_moe_create(ctypes.byref(self._cfg), ctypes.byref(self._w),
+                                        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                                        ctypes.byref(h)), "flint_moe_create")
+        self._h = h
+
+    def route(self, x, topk_idx=None, topk_w=None, counts=None, stream=None):
+        import torch
+        T = x.shape[0]
+        if topk_idx is None:
+            topk_idx = torch.empty((T, TOP_K), dtype=torch.int32, device=x.device)
+        if topk_w is None:
+            topk_w = torch.empty((T, TOP_K), dtype=torch.float32, device=x.device)
+        if counts is None:
+            counts = torch.empty((N_EXPERTS,), dtype=torch.int32, device=x.device)
+        _check(self._L.flint_moe_route(self._h, _ptr(x), T, _ptr(topk_idx), _ptr(topk_w), _ptr(counts),
+                                       _stream_ptr(stream)), "flint_moe_route")
+        return topk_idx, topk_w, counts
+
+    def forward(self, x, y=None, topk_idx=None, topk_w=None, stream=None):
+        import torch
+        T = x.shape[0]
+        if y is None:
+            y = torch.empty_like(x)
+        _check(self._L.flint_moe_forward(self._h, _ptr(x), T, _ptr(y), _ptr(topk_idx), _ptr(topk_w),
+                                         _stream_ptr(stream)), "flint_moe_forward")
+        return y
+
+    def forward_host(self, x_host, y_host, stream=None):
+        """x_host, y_host: CPU (ideally pinned) bf16 tensors [T, 2048]."""
+        T = x_host.shape[0]
+        _check(self._L.flint_moe_forward_host(self._h, ctypes.c_void_p(x_host.data_ptr()), T,
+                                              ctypes.c_void_p(y_host.data_ptr()), _stream_ptr(stream)),
+               "flint_moe_forward_host")
+        return y_host
+
+    def poll_device_status(self, stream=None):
+        return self._L.flint_moe_poll_device_status(self._h, _stream_ptr(stream))
+
+    def enable_kernel_timing(self, on=True):
+        _check(self._L.flint_moe_enable_kernel_timing(self._h, 1 if on else 0), "flint_moe_enable_kernel_timing")
+
+    def kernel_times(self):
+        cap = 16
+        names = (ctypes.c_char_p * cap)()
+        ms = (ctypes.c_float * cap)()
+        n = ctypes.c_int(0)
+        _check(self._L.flint_moe_kernel_times(self._h, names, ms, cap, ctypes.byref(n)), "flint_moe_kernel_times")
+        return [(names[i].decode(), float(ms[i])) for i in range(n.value)]
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._L.flint_moe_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

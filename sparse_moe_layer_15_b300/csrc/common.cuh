@@ -1,0 +1,192 @@
+// Shared device helpers of the Flint MoE kernels: layer constants, workspace view,
+// inline-PTX wrappers (mbarrier, TMA bulk / tensor copies, L2 bulk prefetch, programmatic
+// dependent launch) and bounded waits.  sm_103a only.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace flint {
+
+// ---- the only supported layer shape (Flint serving-kit post, "The architecture, from the
+// config": hidden 2048, 256 routed experts, 6 per token, widths 512 / 1024)
+constexpr int H = 2048;
+constexpr int E = 256;
+constexpr int K = 6;
+constexpr int I = 512;
+constexpr int IS = 1024;
+
+using bf16 = __nv_bfloat16;
+
+// ---- device status word bits
+constexpr uint32_t ST_TIMEOUT = 1u;
+constexpr uint32_t ST_BOUNDS = 2u;
+
+// A bounded wait gives up after this long and records ST_TIMEOUT.
+constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;  // 1 s
+
+// ---- launch-time parameters shared by every kernel of one forward call
+struct Params {
+  int T;                 // tokens in this call
+  unsigned flags;        // FLINT_MOE_FLAG_*
+  float rms_eps;
+  const bf16* x;         // layer input [T][H]
+  const bf16* xin;       // expert / router input: x, or rms(x) in xn
+  bf16* y;               // output [T][H]
+  const bf16* w_router;  // [H][E]
+  const float* router_bias;  // [E] or null
+  const bf16* w_gate;    // [E][H][I]
+  const bf16* w_up;      // [E][H][I]
+  const bf16* w_down;    // [E][I][H]
+  const bf16* ws_gate;   // [H][IS]
+  const bf16* ws_up;     // [H][IS]
+  const bf16* ws_down;   // [IS][H]
+  // workspace
+  uint32_t* status;      // [1]
+  uint32_t* tickets;     // see TicketLayout
+  int32_t* n_touched;    // [1]
+  int32_t* touched;      // [E]
+  int32_t* counts;       // [E]
+  int32_t* offsets;      // [E+1]
+  int32_t* perm;         // [T*K] sorted row -> pair (t*K + j)
+  int32_t* inv;          // [T*K] pair -> sorted row
+  int32_t* topk_idx;     // [T*K]
+  float* topk_w;         // [T*K]
+  bf16* xn;              // [T][H] rms-normalised input
+  bf16* h;               // [T*K][I] routed SwiGLU activations, expert-sorted rows
+  bf16* hs;              // [T][IS] shared SwiGLU activations
+  float* Y;              // [T*K][H] gated routed expert outputs (streaming path)
+  float* S;              // [T][H] shared expert output
+  float* P_gu;           // [GU_KS][T*K][2*I] routed gate/up split-K partials
+  float* P_sgu;          // [SGU_KS][T][2*IS] shared gate/up split-K partials
+  float* P_sd;           // [SD_KS][T][H] shared down split-K partials
+  // user-visible copies (may be null)
+  int32_t* out_idx;
+  float* out_w;
+  int32_t* out_counts;
+  unsigned long long prefetch_bytes_max;  // L2 prefetch budget for touched experts
+};
+
+// Ticket counters (uint32, zero between kernels: the last arriver resets its counter).
+struct TicketLayout {
+  static constexpr int router = 0;          // [1]
+  static constexpr int sgu = 16;            // [IS/64]
+  static constexpr int sd = sgu + IS / 64;  // [H/64]
+  static constexpr int dn = sd + H / 64;    // [H/64]
+  static constexpr int gu = dn + H / 64;    // [E][I/64]
+  static constexpr int total = gu + E * (I / 64);
+};
+
+// ------------------------------------------------------------------ small PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void record_status(uint32_t* status, uint32_t bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// Wait for phase `parity` of an mbarrier, giving up after WAIT_LIMIT_NS.  Returns false
+// (and records ST_TIMEOUT) when the limit ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+      record_status(status, ST_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// 1-D bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16), completing
+// `bytes` transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// 2-D tiled TMA load of box (x = inner coordinate, y = row) into shared memory.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Ask the memory system to bring `bytes` (multiple of 16) at `src` into L2.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Programmatic dependent launch: wait for the preceding grid's results / let the next
+// grid start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float* f) {
+  f[0] = __uint_as_float(v.x << 16);
+  f[1] = __uint_as_float(v.x & 0xFFFF0000u);
+  f[2] = __uint_as_float(v.y << 16);
+  f[3] = __uint_as_float(v.y & 0xFFFF0000u);
+  f[4] = __uint_as_float(v.z << 16);
+  f[5] = __uint_as_float(v.z & 0xFFFF0000u);
+  f[6] = __uint_as_float(v.w << 16);
+  f[7] = __uint_as_float(v.w & 0xFFFF0000u);
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
+
+__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
+
+}  // namespace flint

@@ -1,0 +1,381 @@
+// C-ABI of the Flint MoE layer: argument checks, workspace carving, TMA descriptors and the
+// launch sequence of each call.  Every step of the layer runs in the kernels included below.
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "../../include/flint_moe.h"
+#include "common.cuh"
+#include "stream_kernels.cuh"
+
+using namespace flint;
+
+namespace {
+
+constexpr int MAX_TOKENS_LIMIT = 65536;
+constexpr int MAX_EVENTS = 16;
+
+struct Layout {
+  size_t status, tickets, n_touched, touched, counts, offsets, perm, inv, topk_idx, topk_w;
+  size_t xn, xstage, ystage, h, hs, S, Y, P_gu, P_sgu, P_sd;
+  size_t total;
+};
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+Layout make_layout(int max_tokens) {
+  Layout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = align_up(off, 256);
+    off = o + bytes;
+    return o;
+  };
+  const size_t T = (size_t)max_tokens;
+  const size_t Ts = (size_t)(max_tokens < STREAM_MAX_T ? max_tokens : STREAM_MAX_T);
+  L.status = take(256);
+  L.tickets = take(sizeof(uint32_t) * TicketLayout::total);
+  L.n_touched = take(sizeof(int32_t));
+  L.touched = take(sizeof(int32_t) * E);
+  L.counts = take(sizeof(int32_t) * E);
+  L.offsets = take(sizeof(int32_t) * (E + 1));
+  L.perm = take(sizeof(int32_t) * T * K);
+  L.inv = take(sizeof(int32_t) * T * K);
+  L.topk_idx = take(sizeof(int32_t) * T * K);
+  L.topk_w = take(sizeof(float) * T * K);
+  L.xn = take(sizeof(uint16_t) * T * H);
+  L.xstage = take(sizeof(uint16_t) * T * H);
+  L.ystage = take(sizeof(uint16_t) * T * H);
+  L.h = take(sizeof(uint16_t) * T * K * I);
+  L.hs = take(sizeof(uint16_t) * T * IS);
+  L.S = take(sizeof(float) * T * H);
+  L.Y = take(sizeof(float) * Ts * K * H);
+  L.P_gu = take(sizeof(float) * GU_KS * Ts * K * 2 * I);
+  L.P_sgu = take(sizeof(float) * SGU_KS * STREAM_MAX_T * 2 * IS);
+  L.P_sd = take(sizeof(float) * SD_KS * STREAM_MAX_T * H);
+  L.total = align_up(off, 256);
+  return L;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// Row-major bf16 matrix [rows][cols] -> 2-D tensor map with a box of box_cols x box_rows.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+              uint32_t box_rows, CUtensorMapSwizzle swz) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+struct flint_moe_s {
+  flint_moe_config cfg;
+  flint_moe_weights w;
+  int device;
+  uint8_t* ws;
+  size_t ws_bytes;
+  Layout L;
+  StreamMaps smaps;
+  unsigned long long prefetch_max;
+  bool timing;
+  cudaEvent_t ev[2 * MAX_EVENTS];
+  const char* ev_name[MAX_EVENTS];
+  int n_ev;
+};
+
+namespace {
+
+flint_moe_status check_config(const flint_moe_config* c) {
+  if (!c) return FLINT_MOE_ERR_INVALID_ARG;
+  if (c->hidden != H || c->n_experts != E || c->top_k != K || c->expert_inter != I || c->shared_inter != IS)
+    return FLINT_MOE_ERR_UNSUPPORTED;
+  if (c->max_tokens < 1 || c->max_tokens > MAX_TOKENS_LIMIT) return FLINT_MOE_ERR_INVALID_ARG;
+  if (c->flags & ~(FLINT_MOE_FLAG_PRE_RMSNORM | FLINT_MOE_FLAG_RESIDUAL)) return FLINT_MOE_ERR_UNSUPPORTED;
+  if ((c->flags & FLINT_MOE_FLAG_PRE_RMSNORM) && !(c->rms_eps > 0.f)) return FLINT_MOE_ERR_INVALID_ARG;
+  return FLINT_MOE_OK;
+}
+
+Params make_params(flint_moe_t h, const void* x, int T, void* y, int32_t* out_idx, float* out_w,
+                   int32_t* out_counts) {
+  Params p{};
+  uint8_t* ws = h->ws;
+  const Layout& L = h->L;
+  p.T = T;
+  p.flags = h->cfg.flags;
+  p.rms_eps = h->cfg.rms_eps;
+  p.x = static_cast<const bf16*>(x);
+  p.xn = reinterpret_cast<bf16*>(ws + L.xn);
+  p.xin = (h->cfg.flags & FLINT_MOE_FLAG_PRE_RMSNORM) ? p.xn : p.x;
+  p.y = static_cast<bf16*>(y);
+  p.w_router = static_cast<const bf16*>(h->w.w_router);
+  p.router_bias = h->w.router_bias;
+  p.w_gate = static_cast<const bf16*>(h->w.w_gate);
+  p.w_up = static_cast<const bf16*>(h->w.w_up);
+  p.w_down = static_cast<const bf16*>(h->w.w_down);
+  p.ws_gate = static_cast<const bf16*>(h->w.ws_gate);
+  p.ws_up = static_cast<const bf16*>(h->w.ws_up);
+  p.ws_down = static_cast<const bf16*>(h->w.ws_down);
+  p.status = reinterpret_cast<uint32_t*>(ws + L.status);
+  p.tickets = reinterpret_cast<uint32_t*>(ws + L.tickets);
+  p.n_touched = reinterpret_cast<int32_t*>(ws + L.n_touched);
+  p.touched = reinterpret_cast<int32_t*>(ws + L.touched);
+  p.counts = reinterpret_cast<int32_t*>(ws + L.counts);
+  p.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+  p.perm = reinterpret_cast<int32_t*>(ws + L.perm);
+  p.inv = reinterpret_cast<int32_t*>(ws + L.inv);
+  p.topk_idx = reinterpret_cast<int32_t*>(ws + L.topk_idx);
+  p.topk_w = reinterpret_cast<float*>(ws + L.topk_w);
+  p.h = reinterpret_cast<bf16*>(ws + L.h);
+  p.hs = reinterpret_cast<bf16*>(ws + L.hs);
+  p.S = reinterpret_cast<float*>(ws + L.S);
+  p.Y = reinterpret_cast<float*>(ws + L.Y);
+  p.P_gu = reinterpret_cast<float*>(ws + L.P_gu);
+  p.P_sgu = reinterpret_cast<float*>(ws + L.P_sgu);
+  p.P_sd = reinterpret_cast<float*>(ws + L.P_sd);
+  p.out_idx = out_idx;
+  p.out_w = out_w;
+  p.out_counts = out_counts;
+  p.prefetch_bytes_max = h->prefetch_max;
+  return p;
+}
+
+template <class... KArgs, class... Args>
+cudaError_t launch(flint_moe_t h, const char* name, void (*kern)(KArgs...), unsigned grid, int smem,
+                   cudaStream_t st, Args&&... args) {
+  if (grid == 0) return cudaSuccess;
+  const bool rec = h->timing && h->n_ev < MAX_EVENTS;
+  if (rec) {
+    h->ev_name[h->n_ev] = name;
+    cudaEventRecord(h->ev[2 * h->n_ev], st);
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+  if (rec) {
+    cudaEventRecord(h->ev[2 * h->n_ev + 1], st);
+    h->n_ev++;
+  }
+  return e;
+}
+
+// The layer on T <= STREAM_MAX_T tokens (streaming path).
+flint_moe_status run_stream(flint_moe_t h, const Params& p, cudaStream_t st, bool full) {
+  const int T = p.T;
+  const int u_max = T * K < E ? T * K : E;
+  cudaError_t e = cudaSuccess;
+  if (h->cfg.flags & FLINT_MOE_FLAG_PRE_RMSNORM) e = launch(h, "rmsnorm", rmsnorm_kernel, T, 0, st, p);
+  if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  const int n_router = ((T + RT_TOK - 1) / RT_TOK) * RT_CL;
+  e = launch(h, "stream_k1_router_sharedgu", stream_k1, n_router + (full ? SGU_UNITS : 0), K1_SMEM, st, p,
+             h->smaps, n_router, full ? 1 : 0);
+  if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  if (!full) return FLINT_MOE_OK;
+  e = launch(h, "stream_k2_gateup_shareddown", stream_k2, u_max * GU_UPE + SD_UNITS, K2_SMEM, st, p, h->smaps,
+             u_max * GU_UPE);
+  if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  e = launch(h, "stream_k3_down_combine", stream_k3, u_max * DN_NCH, K3_SMEM, st, p, h->smaps);
+  if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  return FLINT_MOE_OK;
+}
+
+flint_moe_status check_call(flint_moe_t h, const void* x, int T) {
+  if (!h) return FLINT_MOE_ERR_INVALID_ARG;
+  if (!x || !aligned16(x)) return FLINT_MOE_ERR_INVALID_ARG;
+  if (T < 1 || T > h->cfg.max_tokens) return FLINT_MOE_ERR_INVALID_ARG;
+  if (T > STREAM_MAX_T) return FLINT_MOE_ERR_UNSUPPORTED;
+  return FLINT_MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* flint_moe_status_string(flint_moe_status s) {
+  switch (s) {
+    case FLINT_MOE_OK: return "ok";
+    case FLINT_MOE_ERR_INVALID_ARG: return "invalid argument";
+    case FLINT_MOE_ERR_UNSUPPORTED: return "unsupported shape, flags or device";
+    case FLINT_MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case FLINT_MOE_ERR_CUDA: return "CUDA runtime error";
+    case FLINT_MOE_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
+    case FLINT_MOE_ERR_DEVICE_BOUNDS: return "a device-side index check failed";
+  }
+  return "unknown status";
+}
+
+flint_moe_status flint_moe_workspace_bytes(const flint_moe_config* cfg, size_t* bytes) {
+  flint_moe_status s = check_config(cfg);
+  if (s != FLINT_MOE_OK) return s;
+  if (!bytes) return FLINT_MOE_ERR_INVALID_ARG;
+  *bytes = make_layout(cfg->max_tokens).total;
+  return FLINT_MOE_OK;
+}
+
+flint_moe_status flint_moe_create(const flint_moe_config* cfg, const flint_moe_weights* w, void* workspace,
+                                  size_t workspace_bytes, flint_moe_t* out) {
+  if (!out) return FLINT_MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  flint_moe_status s = check_config(cfg);
+  if (s != FLINT_MOE_OK) return s;
+  if (!w || !w->w_router || !w->w_gate || !w->w_up || !w->w_down || !w->ws_gate || !w->ws_up || !w->ws_down)
+    return FLINT_MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {w->w_router, w->w_gate, w->w_up, w->w_down, w->ws_gate, w->ws_up, w->ws_down};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return FLINT_MOE_ERR_INVALID_ARG;
+  if (w->router_bias && (reinterpret_cast<uintptr_t>(w->router_bias) & 3u)) return FLINT_MOE_ERR_INVALID_ARG;
+  Layout L = make_layout(cfg->max_tokens);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < L.total)
+    return FLINT_MOE_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return FLINT_MOE_ERR_CUDA;
+  if (major != 10 || minor != 3) return FLINT_MOE_ERR_UNSUPPORTED;
+
+  flint_moe_s* h = new (std::nothrow) flint_moe_s();
+  if (!h) return FLINT_MOE_ERR_CUDA;
+  h->cfg = *cfg;
+  h->w = *w;
+  h->device = dev;
+  h->ws = static_cast<uint8_t*>(workspace);
+  h->ws_bytes = workspace_bytes;
+  h->L = L;
+  h->prefetch_max = 64ull << 20;
+  if (const char* env = std::getenv("FLINT_MOE_PREFETCH_MB")) h->prefetch_max = std::strtoull(env, nullptr, 10) << 20;
+  h->timing = false;
+  h->n_ev = 0;
+  bool ok = make_map(&h->smaps.wg, w->w_gate, (uint64_t)E * H, I, 64, BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+            make_map(&h->smaps.wu, w->w_up, (uint64_t)E * H, I, 64, BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+            make_map(&h->smaps.wd, w->w_down, (uint64_t)E * I, H, 64, BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+            make_map(&h->smaps.wsg, w->ws_gate, H, IS, 64, BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+            make_map(&h->smaps.wsu, w->ws_up, H, IS, 64, BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+            make_map(&h->smaps.wsd, w->ws_down, IS, H, 64, BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (!ok) {
+    delete h;
+    return FLINT_MOE_ERR_CUDA;
+  }
+  cudaError_t e = cudaFuncSetAttribute(stream_k1, cudaFuncAttributeMaxDynamicSharedMemorySize, K1_SMEM);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(stream_k2, cudaFuncAttributeMaxDynamicSharedMemorySize, K2_SMEM);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(stream_k3, cudaFuncAttributeMaxDynamicSharedMemorySize, K3_SMEM);
+  if (e == cudaSuccess) e = cudaMemset(h->ws, 0, L.xn);  // status, tickets and routing scratch
+  for (int i = 0; i < 2 * MAX_EVENTS && e == cudaSuccess; ++i) e = cudaEventCreate(&h->ev[i]);
+  if (e != cudaSuccess) {
+    delete h;
+    return FLINT_MOE_ERR_CUDA;
+  }
+  *out = h;
+  return FLINT_MOE_OK;
+}
+
+flint_moe_status flint_moe_route(flint_moe_t h, const void* x, int T, int32_t* topk_idx, float* topk_w,
+                                 int32_t* counts, flint_stream_t stream) {
+  flint_moe_status s = check_call(h, x, T);
+  if (s != FLINT_MOE_OK) return s;
+  if (!topk_idx || !topk_w) return FLINT_MOE_ERR_INVALID_ARG;
+  h->n_ev = 0;
+  Params p = make_params(h, x, T, nullptr, topk_idx, topk_w, counts);
+  return run_stream(h, p, reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+flint_moe_status flint_moe_forward(flint_moe_t h, const void* x, int T, void* y, int32_t* topk_idx,
+                                   float* topk_w, flint_stream_t stream) {
+  flint_moe_status s = check_call(h, x, T);
+  if (s != FLINT_MOE_OK) return s;
+  if (!y || !aligned16(y)) return FLINT_MOE_ERR_INVALID_ARG;
+  h->n_ev = 0;
+  Params p = make_params(h, x, T, y, topk_idx, topk_w, nullptr);
+  return run_stream(h, p, reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+flint_moe_status flint_moe_forward_host(flint_moe_t h, const void* x_host, int T, void* y_host,
+                                        flint_stream_t stream) {
+  if (!h || !x_host || !y_host) return FLINT_MOE_ERR_INVALID_ARG;
+  if (T < 1 || T > h->cfg.max_tokens) return FLINT_MOE_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  void* xd = h->ws + h->L.xstage;
+  void* yd = h->ws + h->L.ystage;
+  const size_t bytes = (size_t)T * H * sizeof(uint16_t);
+  if (cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  flint_moe_status s = flint_moe_forward(h, xd, T, yd, nullptr, nullptr, stream);
+  if (s != FLINT_MOE_OK) return s;
+  if (cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  return FLINT_MOE_OK;
+}
+
+flint_moe_status flint_moe_poll_device_status(flint_moe_t h, flint_stream_t stream) {
+  if (!h) return FLINT_MOE_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, h->ws + h->L.status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FLINT_MOE_ERR_CUDA;
+  if (word == 0) return FLINT_MOE_OK;
+  // A device error may leave tickets mid-count: clear them with the status word.
+  if (cudaMemset(h->ws + h->L.status, 0, h->L.n_touched - h->L.status) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  return (word & ST_TIMEOUT) ? FLINT_MOE_ERR_DEVICE_TIMEOUT : FLINT_MOE_ERR_DEVICE_BOUNDS;
+}
+
+flint_moe_status flint_moe_enable_kernel_timing(flint_moe_t h, int enable) {
+  if (!h) return FLINT_MOE_ERR_INVALID_ARG;
+  h->timing = enable != 0;
+  h->n_ev = 0;
+  return FLINT_MOE_OK;
+}
+
+flint_moe_status flint_moe_kernel_times(flint_moe_t h, const char** names, float* ms, int cap, int* n) {
+  if (!h || !n || cap < 0 || (cap > 0 && (!names || !ms))) return FLINT_MOE_ERR_INVALID_ARG;
+  int m = h->n_ev < cap ? h->n_ev : cap;
+  for (int i = 0; i < m; ++i) {
+    if (cudaEventSynchronize(h->ev[2 * i + 1]) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, h->ev[2 * i], h->ev[2 * i + 1]) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+    names[i] = h->ev_name[i];
+    ms[i] = t;
+  }
+  *n = m;
+  return FLINT_MOE_OK;
+}
+
+flint_moe_status flint_moe_destroy(flint_moe_t h) {
+  if (!h) return FLINT_MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 2 * MAX_EVENTS; ++i)
+    if (h->ev[i]) cudaEventDestroy(h->ev[i]);
+  delete h;
+  return FLINT_MOE_OK;
+}
+
+}  // extern "C"

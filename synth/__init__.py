@@ -178,3 +178,75 @@ SIGMA_X = 1.0
 SIGMA_ROUTER = 1.0 / math.sqrt(2048.0)
 SIGMA_EXPERT = 0.02
 SIGMA_BIAS = math.sqrt(0.5)
+
+
+# --------------------------------------------------------------------------------------
+# Flint-layer input sets (weights and token rows), as used by the tests and the benchmark.
+
+LAYER_SHAPES = {
+    "w_router": (2048, 256),
+    "w_gate": (256, 2048, 512),
+    "w_up": (256, 2048, 512),
+    "w_down": (256, 512, 2048),
+    "ws_gate": (2048, 1024),
+    "ws_up": (2048, 1024),
+    "ws_down": (1024, 2048),
+}
+_LAYER_TAGS = {"w_router": (TAG_ROUTER, SIGMA_ROUTER), "w_gate": (TAG_GATE, SIGMA_EXPERT),
+               "w_up": (TAG_UP, SIGMA_EXPERT), "w_down": (TAG_DOWN, SIGMA_EXPERT),
+               "ws_gate": (TAG_SGATE, SIGMA_EXPERT), "ws_up": (TAG_SUP, SIGMA_EXPERT),
+               "ws_down": (TAG_SDOWN, SIGMA_EXPERT)}
+
+
+def flint_weights(seed: int, device="cuda", bias: str | None = None, bias_seed: int | None = None):
+    """One layer's weights, generated on ``device``: router ~N(0, 1/2048), expert and shared
+    matrices ~N(0, 0.02^2), all bf16.  ``bias``: None (no router bias), "normal" (fp32
+    bf16-valued ~N(0, 0.5), seed ``bias_seed``) or "adversarial" (see
+    :func:`adversarial_bias_and_router`)."""
+    import torch
+    w = {}
+    for name, shape in LAYER_SHAPES.items():
+        tag, sigma = _LAYER_TAGS[name]
+        w[name] = torch_normal_bf16(shape, seed, tag, sigma, device=device)
+    w["router_bias"] = None
+    if bias == "normal":
+        b = torch_normal_bf16((256,), seed if bias_seed is None else bias_seed, TAG_BIAS, SIGMA_BIAS, device=device)
+        w["router_bias"] = b.float().contiguous()
+    elif bias == "adversarial":
+        hot, cold, neutral = adversarial_sets(5 if bias_seed is None else bias_seed)
+        b = torch.zeros(256, dtype=torch.float32)
+        b[hot] = 8.0
+        b[cold] = -8.0
+        w["router_bias"] = b.to(device)
+        wr = w["w_router"]
+        # exact score ties: duplicated router columns with equal bias
+        wr[:, hot[1]] = wr[:, hot[0]]
+        wr[:, hot[3]] = wr[:, hot[2]]
+        wr[:, neutral[1]] = wr[:, neutral[0]]
+    elif bias is not None:
+        raise ValueError(bias)
+    return w
+
+
+def adversarial_sets(seed: int = 5):
+    """A seeded permutation of the 256 experts split into 8 hot, 200 cold, 48 neutral."""
+    pi = permutation(seed, 256)
+    return [int(v) for v in pi[:8]], [int(v) for v in pi[8:208]], [int(v) for v in pi[208:]]
+
+
+def weights_to_host(w, experts=None):
+    """uint16 numpy copies of a layer's weights (only ``experts`` of the routed ones, as a
+    dict, when given), plus the fp32 bias or None."""
+    out = {}
+    for name in ("w_router", "ws_gate", "ws_up", "ws_down"):
+        out[name] = w[name].contiguous().view(__import__("torch").int16).cpu().numpy().view(np.uint16)
+    for name in ("w_gate", "w_up", "w_down"):
+        t = w[name]
+        if experts is None:
+            out[name] = t.contiguous().view(__import__("torch").int16).cpu().numpy().view(np.uint16)
+        else:
+            out[name] = {int(e): t[int(e)].contiguous().view(__import__("torch").int16).cpu().numpy().view(np.uint16)
+                         for e in experts}
+    b = w.get("router_bias")
+    out["router_bias"] = None if b is None else b.detach().float().cpu().numpy()
+    return out

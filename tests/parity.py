@@ -1,0 +1,145 @@
+"""Parity rule between the CUDA layer and the fp64 oracle (test infrastructure).
+
+Routing: on every token whose oracle gap between the 6th and 7th score exceeds 1e-4 the GPU
+must choose the same expert set; inside the chosen list, the GPU order must equal the oracle
+order across every adjacent pair whose oracle gap exceeds 1e-4, and across every exact tie
+(where both sides must put the lower index first).  Tokens at or below the gap are exempt:
+their fp32 scores may legitimately pick the other near-tied expert; the oracle then
+re-evaluates them with the GPU's choice (gates = its fp64 scores renormalised).
+
+Outputs (bf16): max |y_gpu - y_ref| <= 2e-2 * max |y_ref| and
+sum |y_gpu - y_ref| / sum |y_ref| <= 5e-3 (relative L1).
+Gates: |g_gpu - g_ref| <= 2e-5 per chosen expert, and the GPU's gates sum to 1 within 1e-5.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import synth
+
+GAP = 1e-4
+MAX_ABS_REL = 2e-2
+REL_L1 = 5e-3
+GATE_TOL = 2e-5
+
+
+def to_np_bf16(t):
+    import torch
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def oracle_layer(w, experts=None):
+    hw = synth.weights_to_host(w, experts=experts)
+    return oracle.Layer(hw["w_router"], hw["w_gate"], hw["w_up"], hw["w_down"], hw["ws_gate"], hw["ws_up"],
+                        hw["ws_down"], router_bias=hw["router_bias"], k=6)
+
+
+def touched_experts(w, xin64, tokens):
+    """Experts the oracle's routing picks for these token rows, plus every expert whose score
+    is within twice the exemption gap of the 6th (so that a re-evaluation with the GPU's
+    choice of a near-tied expert finds its weights)."""
+    wr = to_np_bf16(w["w_router"])
+    b = None if w.get("router_bias") is None else w["router_bias"].detach().float().cpu().numpy()
+    _, s = oracle.router(xin64[tokens], wr, b)
+    idx, _, _ = oracle.select(s, 6)
+    need = set(idx.reshape(-1).tolist())
+    sixth = -np.sort(-s, axis=1)[:, 5]
+    for t in range(s.shape[0]):
+        need.update(np.nonzero(s[t] >= sixth[t] - 2 * GAP)[0].tolist())
+    return sorted(need)
+
+
+def oracle_reference(w, x, tokens, xin64=None, nthreads=8, residual=False, eps=None):
+    """Oracle outputs for the token rows ``tokens`` of x (bf16 torch tensor).  With ``eps``
+    the layer is pre-normed (x' = rms(x)) and, with ``residual``, y = x + MoE(x')."""
+    x64 = oracle.bf16_to_f64(to_np_bf16(x))
+    tokens = np.asarray(tokens, dtype=np.int64)
+    xin = x64 if eps is None else oracle.rmsnorm(x64, eps)
+    experts = touched_experts(w, xin, tokens)
+    layer = oracle_layer(w, experts=experts)
+    out = oracle.forward(layer, xin[tokens], nthreads=nthreads, want_scores=True)
+    if residual:
+        out["y"] = x64[tokens] + out["y"]
+    out["tokens"] = tokens
+    out["layer"] = layer
+    out["xin"] = xin[tokens]
+    out["xres"] = x64[tokens] if residual else None
+    return out
+
+
+def compare(ref, y, idx, gw, counts=None, full_T=None):
+    """Apply the parity rule to GPU results (torch tensors over all T rows) on ref's tokens."""
+    tokens = ref["tokens"]
+    y_g = oracle.bf16_to_f64(to_np_bf16(y))[tokens]
+    idx_g = idx.detach().cpu().numpy()[tokens]
+    w_g = gw.detach().cpu().numpy().astype(np.float64)[tokens]
+    idx_r, gaps, g_r, s_r = ref["idx"], ref["gaps"], ref["gates"], ref["scores"]
+    n = len(tokens)
+    exempt = gaps[:, 5] <= GAP
+    set_mismatch, order_err, tie_err = [], [], []
+    for i in range(n):
+        same_set = set(idx_g[i].tolist()) == set(idx_r[i].tolist())
+        if not same_set:
+            if not exempt[i]:
+                set_mismatch.append(int(tokens[i]))
+            continue
+        # segments of the ranked list separated by gaps > GAP must hold the same experts
+        a = 0
+        for j in range(6):
+            if j == 5 or gaps[i, j] > GAP:
+                if set(idx_g[i, a:j + 1].tolist()) != set(idx_r[i, a:j + 1].tolist()):
+                    order_err.append(int(tokens[i]))
+                    break
+                a = j + 1
+        for j in range(5):
+            if gaps[i, j] == 0.0 and (idx_g[i, j], idx_g[i, j + 1]) != (idx_r[i, j], idx_r[i, j + 1]):
+                tie_err.append(int(tokens[i]))
+    # re-evaluate exempt tokens whose set differs, with the GPU's choice
+    y_ref = ref["y"].copy()
+    reeval = [i for i in range(n) if set(idx_g[i].tolist()) != set(idx_r[i].tolist()) and exempt[i]]
+    missing = []
+    if reeval:
+        try:
+            yy = oracle.forward_given(ref["layer"], ref["xin"][reeval], idx_g[reeval])
+            if ref.get("xres") is not None:
+                yy = ref["xres"][reeval] + yy
+            y_ref[reeval] = yy
+        except RuntimeError:
+            missing = [int(tokens[i]) for i in reeval]
+    d = np.abs(y_g - y_ref)
+    ymax = float(np.max(np.abs(y_ref))) if y_ref.size else 0.0
+    max_rel = float(d.max() / ymax) if ymax > 0 else float(d.max())
+    rel_l1 = float(d.sum() / max(np.abs(y_ref).sum(), 1e-300))
+    # gates by expert id
+    gate_err = 0.0
+    for i in range(n):
+        sg = dict(zip(idx_g[i].tolist(), w_g[i].tolist()))
+        if set(sg) == set(idx_r[i].tolist()):
+            for e, g in zip(idx_r[i].tolist(), g_r[i].tolist()):
+                gate_err = max(gate_err, abs(sg[e] - g))
+        else:
+            sc = s_r[i, idx_g[i]]
+            for e, g in zip(idx_g[i].tolist(), (sc / sc.sum()).tolist()):
+                gate_err = max(gate_err, abs(sg[e] - g))
+    gate_sum_err = float(np.max(np.abs(w_g.sum(1) - 1.0))) if n else 0.0
+    rep = dict(n_tokens=n, n_exempt=int(exempt.sum()), set_mismatch=set_mismatch, order_err=order_err,
+               tie_err=tie_err, reevaluated=len(reeval), missing=missing, max_abs_err_rel=max_rel,
+               rel_l1=rel_l1, gate_err=gate_err, gate_sum_err=gate_sum_err,
+               routing_mismatch=len(set_mismatch) + len(order_err) + len(tie_err))
+    rep["ok"] = (not set_mismatch and not order_err and not tie_err and not missing and max_rel <= MAX_ABS_REL
+                 and rel_l1 <= REL_L1 and gate_err <= GATE_TOL and gate_sum_err <= 1e-5)
+    return rep
+
+
+def check_counts(ref_all, idx_gpu, counts_gpu):
+    """Counts: exactly the oracle's when no token is exempt; in general exactly the counts
+    of the GPU's own choices, which must agree with the oracle's on every non-exempt token
+    (checked by compare)."""
+    idx_g = idx_gpu.detach().cpu().numpy()
+    c_g = counts_gpu.detach().cpu().numpy()
+    own = np.bincount(idx_g.reshape(-1), minlength=256)
+    ok = np.array_equal(c_g, own)
+    if ref_all is not None and not (ref_all["gaps"][:, 5] <= GAP).any():
+        ok = ok and np.array_equal(c_g, np.bincount(ref_all["idx"].reshape(-1), minlength=256))
+    return ok

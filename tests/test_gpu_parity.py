@@ -1,0 +1,190 @@
+"""CUDA layer vs the fp64 oracle, through the C ABI, on the synthetic workloads.
+
+Sizes span several tiles and ragged tails; the parity rule is in tests/parity.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+import sparse_moe_layer_15_b300 as fm
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def w0():
+    """Single-layer weights, seed 0, no router bias."""
+    return synth.flint_weights(seed=0, device=DEV)
+
+
+@pytest.fixture(scope="module")
+def layer0(w0):
+    layer = fm.FlintMoE(w0, max_tokens=256)
+    yield layer
+    layer.close()
+
+
+def x_rows(T, seed):
+    return synth.torch_normal_bf16((T, fm.HIDDEN), seed, synth.TAG_X, 1.0, device=DEV)
+
+
+def run_forward(layer, x):
+    T = x.shape[0]
+    idx = torch.full((T, fm.TOP_K), -1, dtype=torch.int32, device=DEV)
+    gw = torch.zeros((T, fm.TOP_K), dtype=torch.float32, device=DEV)
+    y = layer.forward(x, topk_idx=idx, topk_w=gw)
+    torch.cuda.synchronize()
+    assert layer.poll_device_status() == 0
+    return y, idx, gw
+
+
+def assert_parity(rep):
+    assert rep["ok"], {k: v for k, v in rep.items() if k != "missing" or v}
+
+
+def test_single_layer_T16_seed0(w0, layer0):
+    x = x_rows(16, 0)
+    y, idx, gw = run_forward(layer0, x)
+    ref = parity.oracle_reference(w0, x, range(16))
+    rep = parity.compare(ref, y, idx, gw)
+    assert_parity(rep)
+    _, _, counts = layer0.route(x)
+    torch.cuda.synchronize()
+    assert parity.check_counts(ref, idx, counts)
+
+
+@pytest.mark.parametrize("T", [1, 2, 4, 8, 16, 32, 64])
+def test_decode_sweep(w0, layer0, T):
+    x = x_rows(T, 1000 + T)
+    y, idx, gw = run_forward(layer0, x)
+    ref = parity.oracle_reference(w0, x, range(T))
+    assert_parity(parity.compare(ref, y, idx, gw))
+
+
+@pytest.mark.parametrize("T", [3, 37, 256])
+def test_ragged_and_max_stream_sizes(w0, layer0, T):
+    x = x_rows(T, 77 + T)
+    y, idx, gw = run_forward(layer0, x)
+    tokens = range(T) if T <= 64 else sorted(set(np.linspace(0, T - 1, 48).astype(int).tolist()))
+    ref = parity.oracle_reference(w0, x, tokens)
+    assert_parity(parity.compare(ref, y, idx, gw))
+
+
+def test_route_matches_forward_routing_and_counts(w0, layer0):
+    x = x_rows(64, 5)
+    y, idx, gw = run_forward(layer0, x)
+    idx2, gw2, counts = layer0.route(x)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, idx2) and torch.equal(gw, gw2)
+    assert np.array_equal(counts.cpu().numpy(), np.bincount(idx.cpu().numpy().reshape(-1), minlength=256))
+
+
+def test_bitwise_deterministic_and_token_permutation(w0, layer0):
+    x = x_rows(48, 9)
+    y1, idx1, g1 = run_forward(layer0, x)
+    y2, idx2, g2 = run_forward(layer0, x)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    assert torch.equal(idx1, idx2) and torch.equal(g1, g2)
+    perm = torch.randperm(48, generator=torch.Generator().manual_seed(3)).to(DEV)
+    y3, idx3, g3 = run_forward(layer0, x[perm].contiguous())
+    assert torch.equal(y3.view(torch.int16), y1[perm].view(torch.int16))
+    assert torch.equal(idx3, idx1[perm])
+
+
+def test_zeroed_routed_weights_give_shared_expert_alone():
+    w = synth.flint_weights(seed=0, device=DEV)
+    x = x_rows(8, 11)
+    wd = dict(w)
+    wd["w_down"] = torch.zeros_like(w["w_down"])
+    wg = dict(w)
+    wg["w_gate"] = torch.zeros_like(w["w_gate"])
+    la, lb = fm.FlintMoE(wd, max_tokens=8), fm.FlintMoE(wg, max_tokens=8)
+    ya, _, _ = run_forward(la, x)
+    yb, _, _ = run_forward(lb, x)
+    assert torch.equal(ya.view(torch.int16), yb.view(torch.int16))
+    ref = parity.oracle_reference(wd, x, range(8))
+    d = np.abs(parity.oracle.bf16_to_f64(parity.to_np_bf16(ya)) - ref["y"])
+    assert d.max() <= 2e-2 * np.abs(ref["y"]).max()
+    la.close()
+    lb.close()
+
+
+def test_zero_input_gives_zero_and_lowest_experts():
+    w = synth.flint_weights(seed=0, device=DEV)
+    layer = fm.FlintMoE(w, max_tokens=4)
+    x = torch.zeros((4, fm.HIDDEN), dtype=torch.bfloat16, device=DEV)
+    y, idx, gw = run_forward(layer, x)
+    assert torch.all(y.float() == 0)
+    assert idx.cpu().tolist() == [[0, 1, 2, 3, 4, 5]] * 4
+    assert torch.all(gw == torch.tensor(1.0 / 6.0, dtype=torch.float32))
+    layer.close()
+
+
+def test_router_bias_zipf_like_small_T():
+    w = synth.flint_weights(seed=0, device=DEV, bias="normal", bias_seed=3)
+    layer = fm.FlintMoE(w, max_tokens=64)
+    x = x_rows(64, 3)
+    y, idx, gw = run_forward(layer, x)
+    ref = parity.oracle_reference(w, x, range(64))
+    assert_parity(parity.compare(ref, y, idx, gw))
+    layer.close()
+
+
+def test_adversarial_bias_with_exact_ties_small_T():
+    w = synth.flint_weights(seed=0, device=DEV, bias="adversarial", bias_seed=5)
+    hot, cold, neutral = synth.adversarial_sets(5)
+    layer = fm.FlintMoE(w, max_tokens=128)
+    x = x_rows(128, 5)
+    y, idx, gw = run_forward(layer, x)
+    ref = parity.oracle_reference(w, x, range(128))
+    rep = parity.compare(ref, y, idx, gw)
+    assert_parity(rep)
+    chosen = set(idx.cpu().numpy().reshape(-1).tolist())
+    assert not (chosen & set(cold))
+    # the duplicated hot columns tie exactly: when both are chosen, the lower index is first
+    a, b = sorted((hot[0], hot[1]))
+    rows = idx.cpu().numpy()
+    for r in rows:
+        r = r.tolist()
+        if a in r and b in r:
+            assert r.index(a) + 1 == r.index(b)
+    layer.close()
+
+
+def test_prenorm_residual_layer():
+    w = synth.flint_weights(seed=100, device=DEV)
+    layer = fm.FlintMoE(w, max_tokens=32, flags=fm.FLAG_PRE_RMSNORM | fm.FLAG_RESIDUAL, rms_eps=1e-6)
+    x = x_rows(32, 4)
+    y, idx, gw = run_forward(layer, x)
+    ref = parity.oracle_reference(w, x, range(32), eps=1e-6, residual=True)
+    assert_parity(parity.compare(ref, y, idx, gw))
+    # in place: y aliases x
+    x2 = x.clone()
+    layer.forward(x2, y=x2)
+    torch.cuda.synchronize()
+    assert torch.equal(x2.view(torch.int16), y.view(torch.int16))
+    layer.close()
+
+
+def test_forward_host_matches_device_forward(w0, layer0):
+    x = x_rows(16, 21)
+    y, _, _ = run_forward(layer0, x)
+    xh = x.cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    layer0.forward_host(xh, yh)
+    torch.cuda.synchronize()
+    assert torch.equal(yh.view(torch.int16), y.cpu().view(torch.int16))
+
+
+def test_argument_errors(layer0):
+    x = x_rows(4, 1)
+    with pytest.raises(fm.FlintMoEError) as e:
+        layer0.forward(x[:0])
+    assert e.value.code == 1
+    big = torch.empty((257, fm.HIDDEN), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(fm.FlintMoEError):
+        layer0.forward(big)
