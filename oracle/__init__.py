@@ -57,6 +57,8 @@ def _lib():
         L.oracle_permute.argtypes = [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P, _P]
         L.oracle_rmsnorm.argtypes = [_P, ctypes.c_int, ctypes.c_int, ctypes.c_double, _P]
         L.oracle_rmsnorm.restype = None
+        L.oracle_round_bf16.argtypes = [ctypes.c_double]
+        L.oracle_round_bf16.restype = ctypes.c_double
         L.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
         L.oracle_bf16_to_f64.restype = ctypes.c_double
         _LIB = L
@@ -235,10 +237,23 @@ def rmsnorm(x, eps):
     return r
 
 
+def round_bf16(v) -> np.ndarray:
+    """Elementwise rounding to the nearest bfloat16 value (ties to even), as float64."""
+    L = _lib()
+    a = _f64(v)
+    return np.vectorize(L.oracle_round_bf16, otypes=[np.float64])(a) if a.size else a
+
+
+def prenorm_input(x, eps):
+    """The MoE input of a pre-norm layer: rmsnorm(x), handed to the layer as a bf16
+    activation (rounded to bf16 like every tensor between the layer's steps)."""
+    return round_bf16(rmsnorm(x, eps))
+
+
 def prenorm_residual(layer: Layer, x, eps, nthreads: int = 1):
-    """y = x + MoE(rmsnorm(x)); returns dict(y, idx, gates, gaps, r)."""
+    """y = x + MoE(bf16(rmsnorm(x))); returns dict(y, idx, gates, gaps, r)."""
     x = _f64(x)
-    r = rmsnorm(x, eps)
+    r = prenorm_input(x, eps)
     out = forward(layer, r, nthreads=nthreads)
     out["y"] = x + out["y"]
     out["r"] = r

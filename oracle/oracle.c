@@ -242,6 +242,16 @@ int oracle_permute(const int32_t* idx, int T, int k, int E, int32_t* counts, int
   return ORACLE_OK;
 }
 
+/* Round to the nearest bfloat16 value, ties to even (normal range; the layer's values are
+ * far from bf16's subnormal and overflow limits). */
+double oracle_round_bf16(double v) {
+  if (v == 0.0 || !isfinite(v)) return v;
+  int e;
+  const double m = frexp(v, &e);       /* v = m * 2^e, 0.5 <= |m| < 1 */
+  const double q = nearbyint(m * 256.0); /* 8 significant bits; default mode: ties to even */
+  return ldexp(q, e - 8);
+}
+
 /* RMSNorm with a unit weight. */
 void oracle_rmsnorm(const double* x, int T, int H, double eps, double* r) {
   for (int t = 0; t < T; ++t) {

@@ -86,6 +86,9 @@ int oracle_moe_forward_given(const oracle_layer* L, const double* x, int T, cons
 int oracle_permute(const int32_t* idx, int T, int k, int E, int32_t* counts, int32_t* offsets,
                    int32_t* perm, int32_t* inv);
 
+/* v rounded to the nearest bfloat16 value (ties to even). */
+double oracle_round_bf16(double v);
+
 /* r[t] = x[t] / sqrt(mean_h x[t][h]^2 + eps)  (unit weight). */
 void oracle_rmsnorm(const double* x, int T, int H, double eps, double* r);
 

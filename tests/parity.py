@@ -55,7 +55,7 @@ def oracle_reference(w, x, tokens, xin64=None, nthreads=8, residual=False, eps=N
     the layer is pre-normed (x' = rms(x)) and, with ``residual``, y = x + MoE(x')."""
     x64 = oracle.bf16_to_f64(to_np_bf16(x))
     tokens = np.asarray(tokens, dtype=np.int64)
-    xin = x64 if eps is None else oracle.rmsnorm(x64, eps)
+    xin = x64 if eps is None else oracle.prenorm_input(x64, eps)
     experts = touched_experts(w, xin, tokens)
     layer = oracle_layer(w, experts=experts)
     out = oracle.forward(layer, xin[tokens], nthreads=nthreads, want_scores=True)

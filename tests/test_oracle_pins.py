@@ -323,11 +323,25 @@ def test_rmsnorm_closed_form_and_numpy():
     np.testing.assert_allclose(r, ref, rtol=1e-14)
 
 
+def test_round_bf16_matches_float32_rounding():
+    # Every float32 value rounds to bf16 in a single step, so the float32 bit trick of the
+    # generator (round to nearest even on the low 16 bits) is an independent check.
+    rng = np.random.default_rng(8)
+    v = np.concatenate([rng.normal(size=4000).astype(np.float32),
+                        np.array([1.00390625, 1.01171875, -2.5, 3.0e-3, 65504.0, 1e-20], np.float32)])
+    # half-way cases between bf16 neighbours: low 16 bits exactly 0x8000
+    halves = (rng.integers(0x3F00, 0x4100, size=200).astype(np.uint32) << 16) | np.uint32(0x8000)
+    v = np.concatenate([v, halves.view(np.float32)])
+    want = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(v)).astype(np.float64)
+    got = oracle.round_bf16(v.astype(np.float64))
+    assert np.array_equal(got, want)
+
+
 def test_prenorm_residual_composition():
     p = tiny_layer(seed=12)
     x = x_rows(4, 64, seed=13) * 3.0
     out = oracle.prenorm_residual(to_layer(p), x, 1e-6)
-    r = x / np.sqrt((x * x).mean(axis=1, keepdims=True) + 1e-6)
+    r = oracle.round_bf16(x / np.sqrt((x * x).mean(axis=1, keepdims=True) + 1e-6))
     y_bf, _, _ = brute_force(p, r)
     np.testing.assert_allclose(out["y"], x + y_bf, rtol=1e-11, atol=1e-12)
 
