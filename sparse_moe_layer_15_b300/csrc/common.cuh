@@ -44,10 +44,11 @@ struct Params {
   const bf16* ws_up;     // [H][IS]
   const bf16* ws_down;   // [IS][H]
   // workspace
-  uint32_t* status;      // [1]
-  uint32_t* tickets;     // see TicketLayout
-  int32_t* n_touched;    // [1]
-  int32_t* touched;      // [E]
+  uint32_t* status;      // [1] device status word (ST_* bits)
+  int32_t* n_touched;    // [1] experts with at least one token
+  int32_t* n_groups;     // [1] token groups (of up to 8 expert-sorted rows) over all experts
+  int32_t* touched;      // [E] touched experts, ascending
+  int32_t* tgp;          // [E+1] token-group prefix over the touched experts
   int32_t* counts;       // [E]
   int32_t* offsets;      // [E+1]
   int32_t* perm;         // [T*K] sorted row -> pair (t*K + j)
@@ -57,26 +58,23 @@ struct Params {
   bf16* xn;              // [T][H] rms-normalised input
   bf16* h;               // [T*K][I] routed SwiGLU activations, expert-sorted rows
   bf16* hs;              // [T][IS] shared SwiGLU activations
-  float* Y;              // [T*K][H] gated routed expert outputs (streaming path)
+  float* Y;              // [T*K][H] gated routed expert outputs
   float* S;              // [T][H] shared expert output
-  float* P_gu;           // [GU_KS][T*K][2*I] routed gate/up split-K partials
-  float* P_sgu;          // [SGU_KS][T][2*IS] shared gate/up split-K partials
-  float* P_sd;           // [SD_KS][T][H] shared down split-K partials
+  float* P_gu;           // split-item partial sums of the streaming path, per kind
+  float* P_sgu;
+  float* P_sd;
+  float* P_dn;
+  uint32_t* tk_router;   // [1] tickets (zero between kernels: the last arriver resets)
+  uint32_t* tk_gu;
+  uint32_t* tk_sgu;
+  uint32_t* tk_sd;
+  uint32_t* tk_dn;
+  uint32_t* tk_comb;     // [H/64]
   // user-visible copies (may be null)
   int32_t* out_idx;
   float* out_w;
   int32_t* out_counts;
-  unsigned long long prefetch_bytes_max;  // L2 prefetch budget for touched experts
-};
-
-// Ticket counters (uint32, zero between kernels: the last arriver resets its counter).
-struct TicketLayout {
-  static constexpr int router = 0;          // [1]
-  static constexpr int sgu = 16;            // [IS/64]
-  static constexpr int sd = sgu + IS / 64;  // [H/64]
-  static constexpr int dn = sd + H / 64;    // [H/64]
-  static constexpr int gu = dn + H / 64;    // [E][I/64]
-  static constexpr int total = gu + E * (I / 64);
+  unsigned long long prefetch_bytes_max;  // L2 prefetch budget for the touched down matrices
 };
 
 // ------------------------------------------------------------------ small PTX wrappers

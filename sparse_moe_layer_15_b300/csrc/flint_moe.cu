@@ -19,8 +19,10 @@ constexpr int MAX_TOKENS_LIMIT = 65536;
 constexpr int MAX_EVENTS = 16;
 
 struct Layout {
-  size_t status, tickets, n_touched, touched, counts, offsets, perm, inv, topk_idx, topk_w;
-  size_t xn, xstage, ystage, h, hs, S, Y, P_gu, P_sgu, P_sd;
+  // tickets first: [status, tickets) and [tickets, scalars) are cleared together after errors
+  size_t status, tk_router, tk_gu, tk_sgu, tk_sd, tk_dn, tk_comb;
+  size_t n_touched, n_groups, touched, tgp, counts, offsets, perm, inv, topk_idx, topk_w;
+  size_t xn, xstage, ystage, h, hs, S, Y, P_gu, P_sgu, P_sd, P_dn;
   size_t total;
 };
 
@@ -35,11 +37,20 @@ Layout make_layout(int max_tokens) {
     return o;
   };
   const size_t T = (size_t)max_tokens;
-  const size_t Ts = (size_t)(max_tokens < STREAM_MAX_T ? max_tokens : STREAM_MAX_T);
+  const int Ts = max_tokens < STREAM_MAX_T ? max_tokens : STREAM_MAX_T;
+  const size_t G = (size_t)max_groups(Ts);               // routed token groups
+  const size_t Gs = (size_t)(Ts + NT_MAX - 1) / NT_MAX;  // shared token groups
   L.status = take(256);
-  L.tickets = take(sizeof(uint32_t) * TicketLayout::total);
+  L.tk_router = take(sizeof(uint32_t));
+  L.tk_gu = take(sizeof(uint32_t) * G * GU_NCH);
+  L.tk_sgu = take(sizeof(uint32_t) * Gs * SGU_NCH);
+  L.tk_sd = take(sizeof(uint32_t) * Gs * OUT_NCH);
+  L.tk_dn = take(sizeof(uint32_t) * G * OUT_NCH);
+  L.tk_comb = take(sizeof(uint32_t) * OUT_NCH);
   L.n_touched = take(sizeof(int32_t));
+  L.n_groups = take(sizeof(int32_t));
   L.touched = take(sizeof(int32_t) * E);
+  L.tgp = take(sizeof(int32_t) * (E + 1));
   L.counts = take(sizeof(int32_t) * E);
   L.offsets = take(sizeof(int32_t) * (E + 1));
   L.perm = take(sizeof(int32_t) * T * K);
@@ -52,10 +63,11 @@ Layout make_layout(int max_tokens) {
   L.h = take(sizeof(uint16_t) * T * K * I);
   L.hs = take(sizeof(uint16_t) * T * IS);
   L.S = take(sizeof(float) * T * H);
-  L.Y = take(sizeof(float) * Ts * K * H);
-  L.P_gu = take(sizeof(float) * GU_KS * Ts * K * 2 * I);
-  L.P_sgu = take(sizeof(float) * SGU_KS * STREAM_MAX_T * 2 * IS);
-  L.P_sd = take(sizeof(float) * SD_KS * STREAM_MAX_T * H);
+  L.Y = take(sizeof(float) * (size_t)Ts * K * H);
+  L.P_gu = take(sizeof(float) * G * GU_NCH * GU_KB * NT_MAX * 128);
+  L.P_sgu = take(sizeof(float) * Gs * SGU_NCH * GU_KB * NT_MAX * 128);
+  L.P_sd = take(sizeof(float) * Gs * OUT_NCH * SD_KB * NT_MAX * 64);
+  L.P_dn = take(sizeof(float) * G * OUT_NCH * DN_KB * NT_MAX * 64);
   L.total = align_up(off, 256);
   return L;
 }
@@ -96,6 +108,7 @@ struct flint_moe_s {
   flint_moe_config cfg;
   flint_moe_weights w;
   int device;
+  int n_sm;
   uint8_t* ws;
   size_t ws_bytes;
   Layout L;
@@ -140,8 +153,15 @@ Params make_params(flint_moe_t h, const void* x, int T, void* y, int32_t* out_id
   p.ws_up = static_cast<const bf16*>(h->w.ws_up);
   p.ws_down = static_cast<const bf16*>(h->w.ws_down);
   p.status = reinterpret_cast<uint32_t*>(ws + L.status);
-  p.tickets = reinterpret_cast<uint32_t*>(ws + L.tickets);
+  p.tk_router = reinterpret_cast<uint32_t*>(ws + L.tk_router);
+  p.tk_gu = reinterpret_cast<uint32_t*>(ws + L.tk_gu);
+  p.tk_sgu = reinterpret_cast<uint32_t*>(ws + L.tk_sgu);
+  p.tk_sd = reinterpret_cast<uint32_t*>(ws + L.tk_sd);
+  p.tk_dn = reinterpret_cast<uint32_t*>(ws + L.tk_dn);
+  p.tk_comb = reinterpret_cast<uint32_t*>(ws + L.tk_comb);
   p.n_touched = reinterpret_cast<int32_t*>(ws + L.n_touched);
+  p.n_groups = reinterpret_cast<int32_t*>(ws + L.n_groups);
+  p.tgp = reinterpret_cast<int32_t*>(ws + L.tgp);
   p.touched = reinterpret_cast<int32_t*>(ws + L.touched);
   p.counts = reinterpret_cast<int32_t*>(ws + L.counts);
   p.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
@@ -156,6 +176,7 @@ Params make_params(flint_moe_t h, const void* x, int T, void* y, int32_t* out_id
   p.P_gu = reinterpret_cast<float*>(ws + L.P_gu);
   p.P_sgu = reinterpret_cast<float*>(ws + L.P_sgu);
   p.P_sd = reinterpret_cast<float*>(ws + L.P_sd);
+  p.P_dn = reinterpret_cast<float*>(ws + L.P_dn);
   p.out_idx = out_idx;
   p.out_w = out_w;
   p.out_counts = out_counts;
@@ -193,19 +214,19 @@ cudaError_t launch(flint_moe_t h, const char* name, void (*kern)(KArgs...), unsi
 // The layer on T <= STREAM_MAX_T tokens (streaming path).
 flint_moe_status run_stream(flint_moe_t h, const Params& p, cudaStream_t st, bool full) {
   const int T = p.T;
-  const int u_max = T * K < E ? T * K : E;
   cudaError_t e = cudaSuccess;
   if (h->cfg.flags & FLINT_MOE_FLAG_PRE_RMSNORM) e = launch(h, "rmsnorm", rmsnorm_kernel, T, 0, st, p);
   if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
   const int n_router = ((T + RT_TOK - 1) / RT_TOK) * RT_CL;
-  e = launch(h, "stream_k1_router_sharedgu", stream_k1, n_router + (full ? SGU_UNITS : 0), K1_SMEM, st, p,
-             h->smaps, n_router, full ? 1 : 0);
+  // persistent streaming CTAs of k1: one per SM, rounded up to whole clusters
+  const int n_stream = full ? (h->n_sm + RT_CL - 1) / RT_CL * RT_CL : 0;
+  e = launch(h, "stream_k1_router_sharedgu", stream_k1, n_router + n_stream, K1_SMEM, st, p, h->smaps, n_router,
+             n_stream);
   if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
   if (!full) return FLINT_MOE_OK;
-  e = launch(h, "stream_k2_gateup_shareddown", stream_k2, u_max * GU_UPE + SD_UNITS, K2_SMEM, st, p, h->smaps,
-             u_max * GU_UPE);
+  e = launch(h, "stream_k2_gateup_shareddown", stream_k2, h->n_sm, K23_SMEM, st, p, h->smaps);
   if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
-  e = launch(h, "stream_k3_down_combine", stream_k3, u_max * DN_NCH, K3_SMEM, st, p, h->smaps);
+  e = launch(h, "stream_k3_down_combine", stream_k3, h->n_sm, K23_SMEM, st, p, h->smaps);
   if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
   return FLINT_MOE_OK;
 }
@@ -274,23 +295,28 @@ flint_moe_status flint_moe_create(const flint_moe_config* cfg, const flint_moe_w
   h->ws = static_cast<uint8_t*>(workspace);
   h->ws_bytes = workspace_bytes;
   h->L = L;
-  h->prefetch_max = 64ull << 20;
+  h->prefetch_max = 40ull << 20;
   if (const char* env = std::getenv("FLINT_MOE_PREFETCH_MB")) h->prefetch_max = std::strtoull(env, nullptr, 10) << 20;
   h->timing = false;
   h->n_ev = 0;
-  bool ok = make_map(&h->smaps.wg, w->w_gate, (uint64_t)E * H, I, 64, BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-            make_map(&h->smaps.wu, w->w_up, (uint64_t)E * H, I, 64, BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-            make_map(&h->smaps.wd, w->w_down, (uint64_t)E * I, H, 64, BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-            make_map(&h->smaps.wsg, w->ws_gate, H, IS, 64, BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-            make_map(&h->smaps.wsu, w->ws_up, H, IS, 64, BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-            make_map(&h->smaps.wsd, w->ws_down, IS, H, 64, BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || h->n_sm < 1) {
+    delete h;
+    return FLINT_MOE_ERR_CUDA;
+  }
+  const auto none = CU_TENSOR_MAP_SWIZZLE_NONE;
+  bool ok = make_map(&h->smaps.wg, w->w_gate, (uint64_t)E * H, I, 64, GU_ROWS, none) &&
+            make_map(&h->smaps.wu, w->w_up, (uint64_t)E * H, I, 64, GU_ROWS, none) &&
+            make_map(&h->smaps.wd, w->w_down, (uint64_t)E * I, H, 64, DN_ROWS, none) &&
+            make_map(&h->smaps.wsg, w->ws_gate, H, IS, 64, GU_ROWS, none) &&
+            make_map(&h->smaps.wsu, w->ws_up, H, IS, 64, GU_ROWS, none) &&
+            make_map(&h->smaps.wsd, w->ws_down, IS, H, 64, DN_ROWS, none);
   if (!ok) {
     delete h;
     return FLINT_MOE_ERR_CUDA;
   }
   cudaError_t e = cudaFuncSetAttribute(stream_k1, cudaFuncAttributeMaxDynamicSharedMemorySize, K1_SMEM);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(stream_k2, cudaFuncAttributeMaxDynamicSharedMemorySize, K2_SMEM);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(stream_k3, cudaFuncAttributeMaxDynamicSharedMemorySize, K3_SMEM);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(stream_k2, cudaFuncAttributeMaxDynamicSharedMemorySize, K23_SMEM);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(stream_k3, cudaFuncAttributeMaxDynamicSharedMemorySize, K23_SMEM);
   if (e == cudaSuccess) e = cudaMemset(h->ws, 0, L.xn);  // status, tickets and routing scratch
   for (int i = 0; i < 2 * MAX_EVENTS && e == cudaSuccess; ++i) e = cudaEventCreate(&h->ev[i]);
   if (e != cudaSuccess) {

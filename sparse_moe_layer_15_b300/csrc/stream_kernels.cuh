@@ -1,20 +1,23 @@
 // Streaming (decode-size) path of the Flint MoE layer, T <= STREAM_MAX_T tokens.
 //
-// At decode sizes the layer is bound by reading weights: each touched expert's 6 MB and
-// the shared expert's 12 MB are read once, the arithmetic is tiny.  So every weight tile is
-// moved by one TMA copy into shared memory and consumed there by CUDA cores, and the work
-// is split into enough independent tiles (column chunks x K splits) to keep all SMs
-// streaming.  Split-K sums are reduced deterministically by the last tile of each chunk to
-// arrive (an integer ticket, no floating-point atomics).
+// At decode sizes the layer is bound by reading weights once: 6 MB per touched expert plus
+// 12 MB of shared expert and 1 MB of router.  Each phase therefore flattens its weight
+// traffic into a list of equal 32 KB blocks (64 output columns x 128 or 256 rows of one or
+// two matrices), gives every CTA of a one-per-SM persistent grid an equal contiguous range
+// of blocks, and streams them through a 4-stage TMA pipeline into shared memory, where CUDA
+// cores multiply them against the few token rows.  Consecutive blocks of the same output
+// columns accumulate in registers; a block range that splits an item across CTAs leaves a
+// partial sum, and the last CTA to finish the item (an integer ticket that also records which
+// partial slots exist) adds the partials in block order: deterministic, no float atomics.
 //
-//   stream_k1: router (8-CTA clusters, one cluster per 4 tokens; scores reduced over the
-//              cluster in distributed shared memory), top-6 + renormalisation, the
-//              expert permutation (last cluster), L2 prefetch of the touched experts;
-//              and, in other CTAs of the same grid, the shared expert's gate/up.
-//   stream_k2: routed gate/up with fused SiLU-mul (touched experts only) and the shared
-//              expert's down projection.
-//   stream_k3: routed down projection scaled by the gate, and the combine
-//              y = S + sum_j Y[inv(t, j)] in slot order (last tile of each column chunk).
+//   stream_k1: router (8-CTA clusters per 4 tokens, W_r slice by one bulk copy, scores summed
+//              over the cluster in distributed shared memory), top-6 + renormalisation and
+//              the expert permutation (last cluster); the shared expert's gate/up (SiLU-mul
+//              fused) in the persistent CTAs, which also prefetch the shared down matrix.
+//   stream_k2: routed gate/up (touched experts only, SiLU-mul fused) and the shared down
+//              projection; prefetches the touched experts' down matrices into L2 when they fit.
+//   stream_k3: routed down projection scaled by the gate; the last item of each 64-column
+//              chunk performs the combine y = S + sum_j Y[inv(t, j)] in slot order (+ x).
 #pragma once
 
 #include <cooperative_groups.h>
@@ -27,87 +30,71 @@ namespace cg = cooperative_groups;
 constexpr int NTHREADS = 256;
 constexpr int NWARPS = NTHREADS / 32;
 constexpr int STREAM_MAX_T = 256;
-constexpr int NT_MAX = 8;  // tokens per register block
+constexpr int NT_MAX = 8;  // token rows per register block (a "token group")
+constexpr int NSTAGE = 4;
+constexpr int BLK_BYTES = 32768;
+constexpr int GU_ROWS = 128;       // gate/up block: 128 rows x 64 columns of gate and of up
+constexpr int DN_ROWS = 256;       // down block: 256 rows x 64 columns
+constexpr int GU_KB = H / GU_ROWS;   // 16 blocks per gate/up item
+constexpr int SD_KB = IS / DN_ROWS;  // 4 blocks per shared-down item
+constexpr int DN_KB = I / DN_ROWS;   // 2 blocks per routed-down item
+constexpr int GU_NCH = I / 64;       // 8 column chunks of a routed expert's gate/up
+constexpr int SGU_NCH = IS / 64;     // 16 column chunks of the shared gate/up
+constexpr int OUT_NCH = H / 64;      // 32 column chunks of a down projection
 
-constexpr int RT_TOK = 4;                // tokens per router cluster
-constexpr int RT_CL = 8;                 // CTAs per router cluster (K split of H)
-constexpr int RT_KR = H / RT_CL;         // 256 router rows per CTA
-constexpr int SGU_KS = 8;                // shared gate/up: K splits
-constexpr int SGU_KR = H / SGU_KS;       // 256
-constexpr int SGU_NCH = IS / 64;         // 16 column chunks
-constexpr int SGU_UNITS = SGU_KS * SGU_NCH;
-constexpr int GU_KS = 8;                 // routed gate/up: K splits
-constexpr int GU_KR = H / GU_KS;         // 256
-constexpr int GU_NCH = I / 64;           // 8 column chunks
-constexpr int GU_UPE = GU_KS * GU_NCH;   // 64 tiles per expert
-constexpr int SD_KS = 4;                 // shared down: K splits
-constexpr int SD_KR = IS / SD_KS;        // 256
-constexpr int SD_NCH = H / 64;           // 32 column chunks
-constexpr int SD_UNITS = SD_KS * SD_NCH; // 128
-constexpr int DN_NCH = H / 64;           // routed down: 32 column chunks per expert, all I rows
-constexpr int BOX_ROWS = 256;            // rows per TMA box of a weight tile (64 columns wide)
+constexpr int RT_TOK = 4;         // tokens per router cluster
+constexpr int RT_CL = 8;          // CTAs per router cluster (K split of H)
+constexpr int RT_KR = H / RT_CL;  // 256 router rows per CTA (128 KB, one bulk copy pair)
 
-static_assert(SGU_UNITS % RT_CL == 0, "shared gate/up tiles must fill whole clusters");
+enum Kind : int { KIND_GU = 0, KIND_SGU = 1, KIND_SD = 2, KIND_DN = 3 };
 
 struct StreamMaps {
-  CUtensorMap wg;   // w_gate as [E*H][I]
-  CUtensorMap wu;   // w_up   as [E*H][I]
-  CUtensorMap wd;   // w_down as [E*I][H]
-  CUtensorMap wsg;  // [H][IS]
-  CUtensorMap wsu;  // [H][IS]
-  CUtensorMap wsd;  // [IS][H]
+  CUtensorMap wg;   // w_gate as [E*H][I], box 64 x 128
+  CUtensorMap wu;   // w_up   as [E*H][I], box 64 x 128
+  CUtensorMap wd;   // w_down as [E*I][H], box 64 x 256
+  CUtensorMap wsg;  // [H][IS], box 64 x 128
+  CUtensorMap wsu;  // [H][IS], box 64 x 128
+  CUtensorMap wsd;  // [IS][H], box 64 x 256
 };
+
+// Largest number of token groups (of NT_MAX expert-sorted rows) a call of T tokens can have.
+__host__ __device__ constexpr int max_groups(int T) {
+  const int pairs = T * K;
+  const int u = pairs < E ? pairs : E;
+  const int g = (pairs + NT_MAX - 1) / NT_MAX + u;
+  return g < pairs ? g : pairs;
+}
 
 // ---------------------------------------------------------------- shared-memory layouts
-constexpr int TILE_BYTES = BOX_ROWS * 64 * 2;  // 32 KB per TMA box
-
-struct SmemGU {  // gate/up tile (routed or shared): two KR x 64 tiles
-  static constexpr int tiles = 0;                                   // 2 * 32 KB
-  static constexpr int xs = tiles + 2 * TILE_BYTES;                 // [NT_MAX][256] f32
-  static constexpr int red = xs + NT_MAX * 256 * 4;                 // [8][NT_MAX][128] f32
+struct SmemST {  // persistent streaming CTA
+  static constexpr int stages = 0;                                  // NSTAGE x 32 KB
+  static constexpr int xs = stages + NSTAGE * BLK_BYTES;            // [NT_MAX][<=2048] bf16
+  static constexpr int red = xs + NT_MAX * H * 2;                   // [8][NT_MAX][128] f32
   static constexpr int out = red + NWARPS * NT_MAX * 128 * 4;       // [NT_MAX][128] f32
-  static constexpr int bar = out + NT_MAX * 128 * 4;                // mbarrier
-  static constexpr int flag = bar + 16;
-  static constexpr int bytes = flag + 16;
-};
-struct SmemSD {  // shared down tile: one 256 x 64 tile
-  static constexpr int tiles = 0;
-  static constexpr int xs = tiles + TILE_BYTES;
-  static constexpr int red = xs + NT_MAX * 256 * 4;
-  static constexpr int out = red + NWARPS * NT_MAX * 64 * 4;
-  static constexpr int bar = out + NT_MAX * 64 * 4;
-  static constexpr int flag = bar + 16;
-  static constexpr int bytes = flag + 16;
-};
-struct SmemDN {  // routed down tile: one 512 x 64 tile (two boxes)
-  static constexpr int tiles = 0;
-  static constexpr int xs = tiles + 2 * TILE_BYTES;                 // [NT_MAX][512] f32
-  static constexpr int red = xs + NT_MAX * 512 * 4;
-  static constexpr int out = red + NWARPS * NT_MAX * 64 * 4;
-  static constexpr int bar = out + NT_MAX * 64 * 4;
-  static constexpr int flag = bar + 16;
-  static constexpr int bytes = flag + 16;
+  static constexpr int bars = out + NT_MAX * 128 * 4;               // NSTAGE mbarriers
+  static constexpr int misc = bars + 8 * NSTAGE;                    // item broadcast, flags
+  static constexpr int bytes = misc + 128;
 };
 struct SmemRT {  // router CTA + the permutation
-  static constexpr int xs = 0;                                      // [RT_TOK][256] f32
+  static constexpr int wr = 0;                                      // [256][256] bf16
+  static constexpr int xs = wr + RT_KR * E * 2;                     // [RT_TOK][256] f32
   static constexpr int red = xs + RT_TOK * RT_KR * 4;               // [8][RT_TOK][256] f32
   static constexpr int part = red + NWARPS * RT_TOK * E * 4;        // [RT_TOK][256] f32
   static constexpr int scores = part + RT_TOK * E * 4;              // [RT_TOK][256] f32
-  static constexpr int flag = scores + RT_TOK * E * 4;
+  static constexpr int bar = scores + RT_TOK * E * 4;
+  static constexpr int flag = bar + 16;
   static constexpr int bytes = flag + 16;
   // permutation scratch aliases `red` (used only after the router is done)
-  static constexpr int s_cnt = red;                 // [E] int
-  static constexpr int s_off = s_cnt + E * 4;       // [E+1] int (+pad)
-  static constexpr int s_fill = s_off + (E + 4) * 4;// [E] int
-  static constexpr int s_wcnt = s_fill + E * 4;     // [8][E] int
-  static constexpr int s_wsum = s_wcnt + NWARPS * E * 4;  // [2][8] int
+  static constexpr int s_cnt = red;                  // [E] int
+  static constexpr int s_fill = s_cnt + E * 4;       // [E] int
+  static constexpr int s_wcnt = s_fill + E * 4;      // [8][E] int
+  static constexpr int s_wsum = s_wcnt + NWARPS * E * 4;  // [3][8] int + totals
 };
-static_assert(SmemRT::s_wsum + 64 <= SmemRT::part, "permutation scratch must fit in the router buffer");
+static_assert(SmemRT::s_wsum + 128 <= SmemRT::part, "permutation scratch must fit in the router buffer");
 
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
-constexpr int K1_SMEM = cmax(SmemGU::bytes, SmemRT::bytes) + 1024;
-constexpr int K2_SMEM = cmax(SmemGU::bytes, SmemSD::bytes) + 1024;
-constexpr int K3_SMEM = SmemDN::bytes + 1024;
+constexpr int K1_SMEM = cmax(SmemST::bytes, SmemRT::bytes) + 1024;
+constexpr int K23_SMEM = SmemST::bytes + 1024;
 
 __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
   uint32_t a = smem_u32(raw);
@@ -115,34 +102,179 @@ __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
   return raw + pad;
 }
 
-// ---------------------------------------------------------------- tile multiply-accumulate
-// out[t][m*64 + c] = sum over the KR rows r of xs[t][r] * tile_m[r][c], for NT staged input
-// rows and NM weight tiles (each KR x 64 bf16, row-major, in shared memory).  Each lane
-// accumulates 8 columns of one row in four, rows ascending; the four row lanes are summed by
-// a fixed shuffle tree, the eight warps in warp order: the result is bitwise reproducible.
+// ---------------------------------------------------------------- tickets
+// Arrive after this CTA's global writes with `add` (nblk in the low 8 bits plus one bit per
+// partial slot); returns in every thread the counter value after the add when this CTA
+// completed the item (low byte == KB), or 0.  The last arriver resets the counter.
+__device__ __forceinline__ uint32_t ticket_add(uint32_t* ticket, uint32_t add, uint32_t KB, int* s_word) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t now = atomicAdd(ticket, add) + add;
+    const bool last = (now & 0xFFu) == KB;
+    if (last) atomicExch(ticket, 0u);
+    *s_word = last ? int(now) : 0;
+  }
+  __syncthreads();
+  const uint32_t v = uint32_t(*s_word);
+  if (v) __threadfence();
+  return v;
+}
+
+__device__ __forceinline__ bool ticket_last(uint32_t* ticket, uint32_t total, int* s_word) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t old = atomicAdd(ticket, 1u);
+    const bool last = (old == total - 1);
+    if (last) atomicExch(ticket, 0u);
+    *s_word = last ? 1 : 0;
+  }
+  __syncthreads();
+  const bool last = *s_word != 0;
+  if (last) __threadfence();
+  return last;
+}
+
+// ---------------------------------------------------------------- work items
+struct Item {
+  int kind;
+  int idx;   // item index within its kind
+  int e;     // routed expert, or -1 for the shared expert
+  int row0;  // first row: expert-sorted row (routed) or token (shared)
+  int nt;    // rows in this token group (1..NT_MAX)
+  int c;     // 64-column chunk
+  int KB;    // blocks per item
+};
+
+// largest u in [0, n) with tgp[u] <= gi
+__device__ __forceinline__ int find_group_owner(const int32_t* tgp, int n, int gi) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldcg(tgp + mid) <= gi)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ Item decode_item(const Params& p, int kind, int idx) {
+  Item it;
+  it.kind = kind;
+  it.idx = idx;
+  if (kind == KIND_GU || kind == KIND_DN) {
+    const int nch = kind == KIND_GU ? GU_NCH : OUT_NCH;
+    const int gi = idx / nch;
+    it.c = idx % nch;
+    const int U = __ldcg(p.n_touched);
+    const int u = find_group_owner(p.tgp, U, gi);
+    const int tg = gi - __ldcg(p.tgp + u);
+    it.e = __ldcg(p.touched + u);
+    const int n = __ldcg(p.counts + it.e);
+    it.row0 = __ldcg(p.offsets + it.e) + tg * NT_MAX;
+    it.nt = min(NT_MAX, n - tg * NT_MAX);
+    it.KB = kind == KIND_GU ? GU_KB : DN_KB;
+  } else {
+    const int nch = kind == KIND_SGU ? SGU_NCH : OUT_NCH;
+    const int tg = idx / nch;
+    it.c = idx % nch;
+    it.e = -1;
+    it.row0 = tg * NT_MAX;
+    it.nt = min(NT_MAX, p.T - tg * NT_MAX);
+    it.KB = kind == KIND_SGU ? GU_KB : SD_KB;
+  }
+  return it;
+}
+
+// The blocks of one kernel: [0, n_first) of kind k_first, then [n_first, n_total) of k_second.
+struct BlockList {
+  int k_first, k_second;
+  int n_first, n_total;
+  int kb_first, kb_second;
+};
+
+__device__ __forceinline__ void block_kind(const BlockList& L, int b, int& kind, int& idx, int& kb) {
+  if (b < L.n_first) {
+    kind = L.k_first;
+    idx = b / L.kb_first;
+    kb = b % L.kb_first;
+  } else {
+    kind = L.k_second;
+    const int r = b - L.n_first;
+    idx = r / L.kb_second;
+    kb = r % L.kb_second;
+  }
+}
+
+__device__ void issue_block(const Params& p, const StreamMaps& maps, const BlockList& L, int b, uint8_t* stage,
+                            uint64_t* bar) {
+  int kind, idx, kb;
+  block_kind(L, b, kind, idx, kb);
+  const Item it = decode_item(p, kind, idx);
+  mbar_arrive_expect_tx(bar, BLK_BYTES);
+  const int x = it.c * 64;
+  switch (kind) {
+    case KIND_GU:
+      tma_load_2d(stage, &maps.wg, x, it.e * H + kb * GU_ROWS, bar);
+      tma_load_2d(stage + BLK_BYTES / 2, &maps.wu, x, it.e * H + kb * GU_ROWS, bar);
+      break;
+    case KIND_SGU:
+      tma_load_2d(stage, &maps.wsg, x, kb * GU_ROWS, bar);
+      tma_load_2d(stage + BLK_BYTES / 2, &maps.wsu, x, kb * GU_ROWS, bar);
+      break;
+    case KIND_SD:
+      tma_load_2d(stage, &maps.wsd, x, kb * DN_ROWS, bar);
+      break;
+    default:
+      tma_load_2d(stage, &maps.wd, x, it.e * I + kb * DN_ROWS, bar);
+      break;
+  }
+}
+
+// ---------------------------------------------------------------- the per-CTA stream
+struct Stream {
+  const Params* p;
+  const StreamMaps* maps;
+  BlockList L;
+  int b0, nb;  // this CTA's block range
+  uint8_t* sm;
+  uint64_t* bars;
+  int* misc;   // [0..7]: item broadcast; [8]: flags
+};
+
+// Wait for stage `st` of block number j: thread 0 waits (bounded); the others observe the
+// already-completed phase.  Uniform result across the CTA.
+__device__ __forceinline__ bool wait_stage(Stream& S, int j) {
+  const int st = j % NSTAGE;
+  const uint32_t par = uint32_t(j / NSTAGE) & 1u;
+  int* ok = S.misc + 8;
+  if (threadIdx.x == 0) *ok = mbar_wait_bounded(S.bars + st, par, S.p->status) ? 1 : 0;
+  __syncthreads();
+  if (!*ok) return false;
+  while (!mbar_try_wait(S.bars + st, par)) {
+  }
+  return true;
+}
+
+// acc[t][m][q] += sum over rows r of block `stg` of xs[t][k0 + r] * tile_m[r][ch*8 + q].
+// Lane = (row quarter rsub, 16-byte column chunk ch); warps own contiguous row ranges.
 template <int NT, int NM, int KR>
-__device__ __forceinline__ void mac_block(const bf16* __restrict__ wt, const float* __restrict__ xs,
-                                          float* __restrict__ red, float* __restrict__ out) {
+__device__ __forceinline__ void mac_block(float (&acc)[NT][NM][8], const bf16* __restrict__ stg,
+                                          const bf16* __restrict__ xs, int xlen, int k0) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int rsub = lane >> 3, ch = lane & 7;
-  constexpr int RPW = KR / NWARPS;  // rows per warp
-  float acc[NT][NM][8];
-#pragma unroll
-  for (int t = 0; t < NT; ++t)
-#pragma unroll
-    for (int m = 0; m < NM; ++m)
-#pragma unroll
-      for (int q = 0; q < 8; ++q) acc[t][m][q] = 0.f;
-
+  constexpr int RPW = KR / NWARPS;
 #pragma unroll 4
   for (int i = 0; i < RPW / 4; ++i) {
     const int r = warp * RPW + i * 4 + rsub;
     float xv[NT];
 #pragma unroll
-    for (int t = 0; t < NT; ++t) xv[t] = xs[t * KR + r];
+    for (int t = 0; t < NT; ++t) xv[t] = __bfloat162float(xs[t * xlen + k0 + r]);
 #pragma unroll
     for (int m = 0; m < NM; ++m) {
-      const uint4 w = *reinterpret_cast<const uint4*>(wt + (size_t)m * KR * 64 + r * 64 + ch * 8);
+      const uint4 w = *reinterpret_cast<const uint4*>(stg + (size_t)m * KR * 64 + r * 64 + ch * 8);
       float wf[8];
       bf16x8_to_f32(w, wf);
 #pragma unroll
@@ -151,6 +283,13 @@ __device__ __forceinline__ void mac_block(const bf16* __restrict__ wt, const flo
         for (int q = 0; q < 8; ++q) acc[t][m][q] = fmaf(xv[t], wf[q], acc[t][m][q]);
     }
   }
+}
+
+// Sum acc over the row lanes (fixed shuffle tree) and the warps (warp order) into out[t][m*64+c].
+template <int NT, int NM>
+__device__ __forceinline__ void reduce_acc(float (&acc)[NT][NM][8], float* red, float* out) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int rsub = lane >> 3, ch = lane & 7;
 #pragma unroll
   for (int t = 0; t < NT; ++t)
 #pragma unroll
@@ -172,160 +311,309 @@ __device__ __forceinline__ void mac_block(const bf16* __restrict__ wt, const flo
   __syncthreads();
 }
 
-// Runs mac_block over `ntok` input rows in register blocks of up to NT_MAX tokens.
-//   stage(xs, t0, nt, ntb): fill xs[t][r] (t < ntb, zero rows beyond nt), KR floats per row
-//   store(out, t0, nt):     consume out[t][NM*64] for t < nt
-template <int NM, int KR, class Stage, class Store>
-__device__ __forceinline__ void mac_tokens(const bf16* wt, float* xs, float* red, float* out, int ntok,
-                                           Stage stage, Store store) {
-  for (int t0 = 0; t0 < ntok; t0 += NT_MAX) {
-    const int nt = min(NT_MAX, ntok - t0);
-    const int ntb = nt <= 1 ? 1 : nt <= 2 ? 2 : nt <= 4 ? 4 : 8;
-    stage(xs, t0, nt, ntb);
-    __syncthreads();
-    switch (ntb) {
-      case 1: mac_block<1, NM, KR>(wt, xs, red, out); break;
-      case 2: mac_block<2, NM, KR>(wt, xs, red, out); break;
-      case 4: mac_block<4, NM, KR>(wt, xs, red, out); break;
-      default: mac_block<8, NM, KR>(wt, xs, red, out); break;
-    }
-    store(out, t0, nt);
-    __syncthreads();
+__device__ __forceinline__ float* partial_slot(const Params& p, const Item& it, int slot) {
+  switch (it.kind) {
+    case KIND_GU: return p.P_gu + ((size_t)it.idx * GU_KB + slot) * (NT_MAX * 128);
+    case KIND_SGU: return p.P_sgu + ((size_t)it.idx * GU_KB + slot) * (NT_MAX * 128);
+    case KIND_SD: return p.P_sd + ((size_t)it.idx * SD_KB + slot) * (NT_MAX * 64);
+    default: return p.P_dn + ((size_t)it.idx * DN_KB + slot) * (NT_MAX * 64);
   }
 }
 
-// xs[t][r] = float(src_row(t)[k0 + r]) for r < KR, rows t < nt; zero for nt <= t < ntb.
-template <int KR, class RowPtr>
-__device__ __forceinline__ void stage_rows(float* xs, int nt, int ntb, int k0, RowPtr row_ptr) {
-  constexpr int CPR = KR / 8;  // 16-byte chunks per row
-  for (int c = threadIdx.x; c < ntb * CPR; c += NTHREADS) {
-    const int t = c / CPR, q = c % CPR;
-    float f[8];
-    if (t < nt) {
-      const uint4 v = *reinterpret_cast<const uint4*>(row_ptr(t) + k0 + q * 8);
-      bf16x8_to_f32(v, f);
-    } else {
+__device__ __forceinline__ uint32_t* item_ticket(const Params& p, const Item& it) {
+  switch (it.kind) {
+    case KIND_GU: return p.tk_gu + it.idx;
+    case KIND_SGU: return p.tk_sgu + it.idx;
+    case KIND_SD: return p.tk_sd + it.idx;
+    default: return p.tk_dn + it.idx;
+  }
+}
+
+// Final values of an item (fp32 sums [nt][ncol] in `vals`, row stride ncol) -> outputs.
+__device__ void item_epilogue(const Params& p, const Item& it, const float* vals, int* s_word) {
+  const int nt = it.nt, c = it.c;
+  if (it.kind == KIND_GU || it.kind == KIND_SGU) {
+    bf16* dst = it.kind == KIND_GU ? p.h : p.hs;
+    const int ld = it.kind == KIND_GU ? I : IS;
+    for (int q = threadIdx.x; q < nt * 64; q += NTHREADS) {
+      const int t = q / 64, j = q % 64;
+      const float g = vals[t * 128 + j], u = vals[t * 128 + 64 + j];
+      dst[(size_t)(it.row0 + t) * ld + c * 64 + j] = __float2bfloat16_rn(silu_f32(g) * u);
+    }
+    return;
+  }
+  if (it.kind == KIND_SD) {
+    for (int q = threadIdx.x; q < nt * 64; q += NTHREADS) {
+      const int t = q / 64, j = q % 64;
+      p.S[(size_t)(it.row0 + t) * H + c * 64 + j] = vals[t * 64 + j];
+    }
+    return;
+  }
+  // routed down: gated rows, then the combine of column chunk c once every group is in
+  for (int q = threadIdx.x; q < nt * 64; q += NTHREADS) {
+    const int t = q / 64, j = q % 64;
+    const int row = it.row0 + t;
+    const float g = __ldcg(p.topk_w + __ldcg(p.perm + row));
+    p.Y[(size_t)row * H + c * 64 + j] = g * vals[t * 64 + j];
+  }
+  const int groups = __ldcg(p.n_groups);
+  if (!ticket_last(p.tk_comb + c, uint32_t(groups), s_word)) return;
+  const bool residual = (p.flags & 2u) != 0;
+  for (int q = threadIdx.x; q < p.T * 64; q += NTHREADS) {
+    const int t = q / 64, j = q % 64;
+    const int col = c * 64 + j;
+    float v = __ldcg(p.S + (size_t)t * H + col);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) f[j] = 0.f;
-    }
-    float4* d = reinterpret_cast<float4*>(xs + t * KR + q * 8);
-    d[0] = make_float4(f[0], f[1], f[2], f[3]);
-    d[1] = make_float4(f[4], f[5], f[6], f[7]);
+    for (int k = 0; k < K; ++k) v += __ldcg(p.Y + (size_t)__ldcg(p.inv + t * K + k) * H + col);
+    if (residual) v += __bfloat162float(p.x[(size_t)t * H + col]);
+    p.y[(size_t)t * H + col] = __float2bfloat16_rn(v);
   }
 }
 
-// Arrive on a ticket after this CTA's global writes; returns (in every thread) whether this
-// CTA is the last of `total` arrivals, and if so resets the ticket for the next use.
-__device__ __forceinline__ bool ticket_arrive(uint32_t* ticket, uint32_t total, int* s_flag) {
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const uint32_t old = atomicAdd(ticket, 1u);
-    const bool last = (old == total - 1);
-    if (last) atomicExch(ticket, 0u);
-    *s_flag = last ? 1 : 0;
+// One segment: blocks [kb_start, kb_start + nblk) of item `it`, consumed as CTA blocks
+// j .. j + nblk - 1.  Returns false on a device timeout.
+template <int NT, int NM, int KR>
+__device__ bool run_segment(Stream& S, const Item& it, int kb_start, int nblk, int& j) {
+  const Params& p = *S.p;
+  bf16* xs = reinterpret_cast<bf16*>(S.sm + SmemST::xs);
+  float* red = reinterpret_cast<float*>(S.sm + SmemST::red);
+  float* out = reinterpret_cast<float*>(S.sm + SmemST::out);
+  // stage the token group's input rows (bf16) for the whole item
+  const int xlen = it.kind == KIND_SD ? IS : it.kind == KIND_DN ? I : H;
+  const int cpr = xlen / 8;
+  for (int q = threadIdx.x; q < NT * cpr; q += NTHREADS) {
+    const int t = q / cpr, k8 = q % cpr;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (t < it.nt) {
+      const bf16* src;
+      if (it.kind == KIND_GU) {
+        const int tok = __ldcg(p.perm + it.row0 + t) / K;
+        src = p.xin + (size_t)tok * H;
+      } else if (it.kind == KIND_SGU) {
+        src = p.xin + (size_t)(it.row0 + t) * H;
+      } else if (it.kind == KIND_SD) {
+        src = p.hs + (size_t)(it.row0 + t) * IS;
+      } else {
+        src = p.h + (size_t)(it.row0 + t) * I;
+      }
+      v = __ldcg(reinterpret_cast<const uint4*>(src) + k8);
+    }
+    *reinterpret_cast<uint4*>(xs + t * xlen + k8 * 8) = v;
   }
   __syncthreads();
-  const bool last = *s_flag != 0;
-  if (last) __threadfence();
-  return last;
+  float acc[NT][NM][8];
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+#pragma unroll
+    for (int m = 0; m < NM; ++m)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[t][m][q] = 0.f;
+  for (int q = 0; q < nblk; ++q, ++j) {
+    if (!wait_stage(S, j)) return false;
+    const int st = j % NSTAGE;
+    mac_block<NT, NM, KR>(acc, reinterpret_cast<const bf16*>(S.sm + SmemST::stages + st * BLK_BYTES), xs, xlen,
+                          (kb_start + q) * KR);
+    __syncthreads();  // every thread is done with this stage
+    if (threadIdx.x == 0 && j + NSTAGE < S.nb)
+      issue_block(p, *S.maps, S.L, S.b0 + j + NSTAGE, S.sm + SmemST::stages + st * BLK_BYTES, S.bars + st);
+  }
+  reduce_acc<NT, NM>(acc, red, out);
+  constexpr int ncol = NM * 64;
+  if (kb_start == 0 && nblk == it.KB) {
+    item_epilogue(p, it, out, S.misc + 9);
+    __syncthreads();
+    return true;
+  }
+  float* P = partial_slot(p, it, kb_start);
+  for (int q = threadIdx.x; q < it.nt * ncol; q += NTHREADS) P[q] = out[q];
+  const uint32_t v = ticket_add(item_ticket(p, it), uint32_t(nblk) | (1u << (8 + kb_start)), uint32_t(it.KB),
+                                S.misc + 10);
+  if (v) {
+    // last arriver: add the partial slots in block order
+    const uint32_t mask = v >> 8;
+    for (int q = threadIdx.x; q < it.nt * ncol; q += NTHREADS) {
+      float s = 0.f;
+      for (int sl = 0; sl < it.KB; ++sl)
+        if (mask & (1u << sl)) s += __ldcg(partial_slot(p, it, sl) + q);
+      out[q] = s;
+    }
+    __syncthreads();
+    item_epilogue(p, it, out, S.misc + 9);
+  }
+  __syncthreads();
+  return true;
+}
+
+template <int NM, int KR>
+__device__ __forceinline__ bool run_segment_nt(Stream& S, const Item& it, int kb, int nblk, int& j) {
+  if (it.nt <= 1) return run_segment<1, NM, KR>(S, it, kb, nblk, j);
+  if (it.nt <= 2) return run_segment<2, NM, KR>(S, it, kb, nblk, j);
+  if (it.nt <= 4) return run_segment<4, NM, KR>(S, it, kb, nblk, j);
+  return run_segment<8, NM, KR>(S, it, kb, nblk, j);
+}
+
+// Persistent stream over blocks [0, n_total) of L, split evenly over `nctas` CTAs (this is
+// CTA `g`).  All threads of the CTA call it.
+__device__ void stream_blocks(const Params& p, const StreamMaps& maps, const BlockList& L, int g, int nctas,
+                              uint8_t* sm) {
+  Stream S;
+  S.p = &p;
+  S.maps = &maps;
+  S.L = L;
+  S.sm = sm;
+  S.bars = reinterpret_cast<uint64_t*>(sm + SmemST::bars);
+  S.misc = reinterpret_cast<int*>(sm + SmemST::misc);
+  const long long N = L.n_total;
+  S.b0 = int(N * g / nctas);
+  const int b1 = int(N * (g + 1) / nctas);
+  S.nb = b1 - S.b0;
+  if (S.nb <= 0) return;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTAGE; ++s) mbar_init(S.bars + s, 1);
+    fence_mbar_init();
+    for (int s = 0; s < NSTAGE && s < S.nb; ++s)
+      issue_block(p, maps, L, S.b0 + s, sm + SmemST::stages + s * BLK_BYTES, S.bars + s);
+  }
+  __syncthreads();
+  int j = 0;
+  while (j < S.nb) {
+    int kind, idx, kb;
+    block_kind(L, S.b0 + j, kind, idx, kb);
+    if (threadIdx.x == 0) {
+      const Item it = decode_item(p, kind, idx);
+      int* m = S.misc;
+      m[0] = it.e;
+      m[1] = it.row0;
+      m[2] = it.nt;
+      m[3] = it.c;
+      m[4] = it.KB;
+    }
+    __syncthreads();
+    Item it;
+    it.kind = kind;
+    it.idx = idx;
+    it.e = S.misc[0];
+    it.row0 = S.misc[1];
+    it.nt = S.misc[2];
+    it.c = S.misc[3];
+    it.KB = S.misc[4];
+    __syncthreads();
+    const int nblk = min(it.KB - kb, S.nb - j);
+    bool ok;
+    if (kind == KIND_GU || kind == KIND_SGU)
+      ok = run_segment_nt<2, GU_ROWS>(S, it, kb, nblk, j);
+    else
+      ok = run_segment_nt<1, DN_ROWS>(S, it, kb, nblk, j);
+    if (!ok) return;
+  }
+}
+
+// Spread a bulk L2 prefetch of `bytes` (multiple of 16) at `base` over `nctas` CTAs.
+__device__ __forceinline__ void prefetch_share(const void* base, size_t bytes, int g, int nctas) {
+  const size_t per = ((bytes / nctas) + 15) & ~size_t(15);
+  const size_t a = per * g;
+  if (a >= bytes) return;
+  size_t n = per < bytes - a ? per : bytes - a;
+  const uint8_t* src = static_cast<const uint8_t*>(base) + a;
+  while (n) {
+    const uint32_t c = n > 65536 ? 65536u : uint32_t(n);
+    prefetch_l2_bulk(src, c);
+    src += c;
+    n -= c;
+  }
 }
 
 // ================================================================ K1: router + shared gate/up
 __device__ void router_cluster(const Params& p, uint8_t* sm, int cl, int rank);
 __device__ void permute_small(const Params& p, uint8_t* sm);
 
-__device__ void shared_gate_up_tile(const Params& p, const StreamMaps& maps, uint8_t* sm, int unit) {
-  const int c = unit % SGU_NCH, s = unit / SGU_NCH;
-  const int col0 = c * 64, k0 = s * SGU_KR;
-  bf16* tiles = reinterpret_cast<bf16*>(sm + SmemGU::tiles);
-  float* xs = reinterpret_cast<float*>(sm + SmemGU::xs);
-  float* red = reinterpret_cast<float*>(sm + SmemGU::red);
-  float* out = reinterpret_cast<float*>(sm + SmemGU::out);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + SmemGU::bar);
-  int* flag = reinterpret_cast<int*>(sm + SmemGU::flag);
-  if (threadIdx.x == 0) {
-    mbar_init(bar, 1);
-    fence_mbar_init();
-    mbar_arrive_expect_tx(bar, 2 * TILE_BYTES);
-    tma_load_2d(tiles, &maps.wsg, col0, k0, bar);
-    tma_load_2d(tiles + BOX_ROWS * 64, &maps.wsu, col0, k0, bar);
-  }
-  pdl_wait();
-  __syncthreads();
-  if (!mbar_wait_bounded(bar, 0, p.status)) return;
-  const int T = p.T;
-  mac_tokens<2, SGU_KR>(
-      tiles, xs, red, out, T,
-      [&](float* xsb, int t0, int nt, int ntb) {
-        stage_rows<SGU_KR>(xsb, nt, ntb, k0, [&](int t) { return p.xin + (size_t)(t0 + t) * H; });
-      },
-      [&](const float* o, int t0, int nt) {
-        for (int q = threadIdx.x; q < nt * 128; q += NTHREADS) {
-          const int t = q / 128, j = q % 128;
-          p.P_sgu[((size_t)s * STREAM_MAX_T + t0 + t) * (2 * IS) + c * 128 + j] = o[q];
-        }
-      });
-  if (!ticket_arrive(p.tickets + TicketLayout::sgu + c, SGU_KS, flag)) return;
-  for (int q = threadIdx.x; q < T * 64; q += NTHREADS) {
-    const int t = q / 64, j = q % 64;
-    float g = 0.f, u = 0.f;
-    for (int ss = 0; ss < SGU_KS; ++ss) {
-      const float* P = p.P_sgu + ((size_t)ss * STREAM_MAX_T + t) * (2 * IS) + c * 128;
-      g += __ldcg(P + j);
-      u += __ldcg(P + 64 + j);
-    }
-    p.hs[(size_t)t * IS + col0 + j] = __float2bfloat16_rn(silu_f32(g) * u);
-  }
-}
-
 __global__ void __cluster_dims__(RT_CL, 1, 1) __launch_bounds__(NTHREADS)
-    stream_k1(const __grid_constant__ Params p, const __grid_constant__ StreamMaps maps, int n_router_ctas, int with_shared) {
+    stream_k1(const __grid_constant__ Params p, const __grid_constant__ StreamMaps maps, int n_router_ctas,
+              int n_stream_ctas) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = aligned_smem(smem_raw);
   pdl_launch_dependents();
   if ((int)blockIdx.x < n_router_ctas) {
-    pdl_wait();
     router_cluster(p, sm, blockIdx.x / RT_CL, blockIdx.x % RT_CL);
-  } else if (with_shared) {
-    shared_gate_up_tile(p, maps, sm, blockIdx.x - n_router_ctas);
+    return;
   }
+  const int g = blockIdx.x - n_router_ctas;
+  // the shared down matrix is read by the next kernel: start bringing it into L2
+  prefetch_share(p.ws_down, (size_t)IS * H * 2, g, n_stream_ctas);
+  pdl_wait();
+  const int ntg = (p.T + NT_MAX - 1) / NT_MAX;
+  BlockList L;
+  L.k_first = KIND_SGU;
+  L.k_second = KIND_SGU;
+  L.kb_first = L.kb_second = GU_KB;
+  L.n_first = L.n_total = ntg * SGU_NCH * GU_KB;
+  stream_blocks(p, maps, L, g, n_stream_ctas, sm);
 }
 
 __device__ void router_cluster(const Params& p, uint8_t* sm, int cl, int rank) {
   cg::cluster_group cluster = cg::this_cluster();
+  bf16* wr = reinterpret_cast<bf16*>(sm + SmemRT::wr);
   float* xs = reinterpret_cast<float*>(sm + SmemRT::xs);
   float* red = reinterpret_cast<float*>(sm + SmemRT::red);
   float* part = reinterpret_cast<float*>(sm + SmemRT::part);
   float* scores = reinterpret_cast<float*>(sm + SmemRT::scores);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + SmemRT::bar);
   int* flag = reinterpret_cast<int*>(sm + SmemRT::flag);
   const int t0 = cl * RT_TOK;
   const int nt = min(RT_TOK, p.T - t0);
   const int k0 = rank * RT_KR;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
-  // stage the token rows of this K slice
-  stage_rows<RT_KR>(xs, nt, RT_TOK, k0, [&](int t) { return p.xin + (size_t)(t0 + t) * H; });
+  // the router rows [k0, k0 + 256) are one contiguous 128 KB range: two bulk copies
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(bar, RT_KR * E * 2);
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(p.w_router + (size_t)k0 * E);
+    bulk_g2s(wr, src, RT_KR * E, bar);
+    bulk_g2s(reinterpret_cast<uint8_t*>(wr) + RT_KR * E, src + RT_KR * E, RT_KR * E, bar);
+  }
+  pdl_wait();
+  // stage the token rows of this K slice (fp32)
+  for (int c = threadIdx.x; c < RT_TOK * (RT_KR / 8); c += NTHREADS) {
+    const int t = c / (RT_KR / 8), q = c % (RT_KR / 8);
+    float f[8];
+    if (t < nt) {
+      const uint4 v = *reinterpret_cast<const uint4*>(p.xin + (size_t)(t0 + t) * H + k0 + q * 8);
+      bf16x8_to_f32(v, f);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] = 0.f;
+    }
+    float4* d = reinterpret_cast<float4*>(xs + t * RT_KR + q * 8);
+    d[0] = make_float4(f[0], f[1], f[2], f[3]);
+    d[1] = make_float4(f[4], f[5], f[6], f[7]);
+  }
+  if (threadIdx.x == 0) flag[0] = mbar_wait_bounded(bar, 0, p.status) ? 1 : 0;
   __syncthreads();
-
+  const bool have_w = flag[0] != 0;
+  if (have_w)
+    while (!mbar_try_wait(bar, 0)) {
+    }
   // partial logits: lane owns experts 8*lane..8*lane+7, warp owns rows warp, warp+8, ...
   float acc[RT_TOK][8];
 #pragma unroll
   for (int t = 0; t < RT_TOK; ++t)
 #pragma unroll
     for (int q = 0; q < 8; ++q) acc[t][q] = 0.f;
-  const bf16* wr = p.w_router + (size_t)k0 * E + lane * 8;
+  if (have_w) {
 #pragma unroll 8
-  for (int i = 0; i < RT_KR / NWARPS; ++i) {
-    const int r = warp + i * NWARPS;
-    const uint4 w = __ldg(reinterpret_cast<const uint4*>(wr + (size_t)r * E));
-    float wf[8];
-    bf16x8_to_f32(w, wf);
+    for (int i = 0; i < RT_KR / NWARPS; ++i) {
+      const int r = warp + i * NWARPS;
+      const uint4 w = *reinterpret_cast<const uint4*>(wr + r * E + lane * 8);
+      float wf[8];
+      bf16x8_to_f32(w, wf);
 #pragma unroll
-    for (int t = 0; t < RT_TOK; ++t) {
-      const float xv = xs[t * RT_KR + r];
+      for (int t = 0; t < RT_TOK; ++t) {
+        const float xv = xs[t * RT_KR + r];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[t][q] = fmaf(xv, wf[q], acc[t][q]);
+        for (int q = 0; q < 8; ++q) acc[t][q] = fmaf(xv, wf[q], acc[t][q]);
+      }
     }
   }
 #pragma unroll
@@ -385,7 +673,9 @@ __device__ void router_cluster(const Params& p, uint8_t* sm, int cl, int rank) {
       const int e = E - 1 - int(best & 0xFFFFFFFFu);
       sel_e[j] = e;
       sel_s[j] = __uint_as_float(uint32_t(best >> 32));
-      if ((e & 31) == lane) key[e >> 5] = 0;  // scores are >= 0, so 0 never wins again
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (lane + 32 * q == e) key[q] = 0;  // scores are >= 0: an emptied slot never wins
     }
     if (lane == 0) {
       float sum = 0.f;
@@ -403,14 +693,14 @@ __device__ void router_cluster(const Params& p, uint8_t* sm, int cl, int rank) {
     }
   }
   const int n_clusters = (p.T + RT_TOK - 1) / RT_TOK;
-  if (!ticket_arrive(p.tickets + TicketLayout::router, n_clusters, flag)) return;
+  if (!ticket_last(p.tk_router, n_clusters, flag + 1)) return;
   permute_small(p, sm);
 }
 
-// Stable counting sort of the T*K (token, slot) pairs by expert, in one CTA.
+// Stable counting sort of the T*K (token, slot) pairs by expert, in one CTA; also the list
+// of touched experts and the prefix of their token groups.
 __device__ void permute_small(const Params& p, uint8_t* sm) {
   int* s_cnt = reinterpret_cast<int*>(sm + SmemRT::s_cnt);
-  int* s_off = reinterpret_cast<int*>(sm + SmemRT::s_off);
   int* s_fill = reinterpret_cast<int*>(sm + SmemRT::s_fill);
   int* s_wcnt = reinterpret_cast<int*>(sm + SmemRT::s_wcnt);
   int* s_wsum = reinterpret_cast<int*>(sm + SmemRT::s_wsum);
@@ -427,41 +717,50 @@ __device__ void permute_small(const Params& p, uint8_t* sm) {
     atomicAdd(&s_cnt[e], 1);
   }
   __syncthreads();
-  // exclusive scans over experts (tid == expert) of the counts and of "touched" flags
+  // exclusive scans over experts (tid == expert): counts, touched flags, token groups
   const int c = s_cnt[tid];
   const int f = c > 0 ? 1 : 0;
-  int ic = c, jf = f;
+  const int ng = (c + NT_MAX - 1) / NT_MAX;
+  int ic = c, jf = f, kg = ng;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const int a = __shfl_up_sync(0xffffffffu, ic, off);
     const int b = __shfl_up_sync(0xffffffffu, jf, off);
+    const int d = __shfl_up_sync(0xffffffffu, kg, off);
     if (lane >= off) {
       ic += a;
       jf += b;
+      kg += d;
     }
   }
   if (lane == 31) {
     s_wsum[warp] = ic;
     s_wsum[NWARPS + warp] = jf;
+    s_wsum[2 * NWARPS + warp] = kg;
   }
   __syncthreads();
-  int bc = 0, bf = 0;
+  int bc = 0, bf = 0, bg = 0;
   for (int w = 0; w < warp; ++w) {
     bc += s_wsum[w];
     bf += s_wsum[NWARPS + w];
+    bg += s_wsum[2 * NWARPS + w];
   }
   const int off_e = bc + ic - c;
   const int pos = bf + jf - f;
-  s_off[tid] = off_e;
+  const int gpre = bg + kg - ng;
   s_fill[tid] = off_e;
   p.counts[tid] = c;
   p.offsets[tid] = off_e;
   if (p.out_counts) p.out_counts[tid] = c;
-  if (f) p.touched[pos] = tid;
+  if (f) {
+    p.touched[pos] = tid;
+    p.tgp[pos] = gpre;
+  }
   if (tid == NTHREADS - 1) {
     p.offsets[E] = off_e + c;
     *p.n_touched = pos + f;
-    s_wsum[2 * NWARPS] = pos + f;
+    *p.n_groups = gpre + ng;
+    p.tgp[pos + f] = gpre + ng;
   }
   __syncthreads();
   // stable scatter, 256 pairs at a time in (t, j) order
@@ -490,174 +789,58 @@ __device__ void permute_small(const Params& p, uint8_t* sm) {
     }
     __syncthreads();
   }
-  // L2 prefetch of the touched experts' weights when they fit the budget
-  const int nt_exp = s_wsum[2 * NWARPS];
-  const unsigned long long per_expert = 3ull * H * I * 2;
-  if ((unsigned long long)nt_exp * per_expert <= p.prefetch_bytes_max) {
-    constexpr uint32_t CH = 64 * 1024;
-    constexpr int CHUNKS = (H * I * 2) / CH;  // 32 chunks of each 2 MB matrix
-    for (int q = tid; q < nt_exp * 3 * CHUNKS; q += NTHREADS) {
-      const int u = q / (3 * CHUNKS), m = (q / CHUNKS) % 3, cc = q % CHUNKS;
-      const int e = p.touched[u];
-      const bf16* base = m == 0 ? p.w_gate : m == 1 ? p.w_up : p.w_down;
-      prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(base + (size_t)e * H * I) + (size_t)cc * CH, CH);
-    }
-  }
 }
 
 // ================================================================ K2: routed gate/up + shared down
-__device__ void routed_gate_up_tile(const Params& p, const StreamMaps& maps, uint8_t* sm, int unit) {
-  const int u = unit / GU_UPE;
-  const int c = unit % GU_NCH, s = (unit / GU_NCH) % GU_KS;
-  bf16* tiles = reinterpret_cast<bf16*>(sm + SmemGU::tiles);
-  float* xs = reinterpret_cast<float*>(sm + SmemGU::xs);
-  float* red = reinterpret_cast<float*>(sm + SmemGU::red);
-  float* out = reinterpret_cast<float*>(sm + SmemGU::out);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + SmemGU::bar);
-  int* flag = reinterpret_cast<int*>(sm + SmemGU::flag);
-  pdl_wait();
-  if (u >= __ldcg(p.n_touched)) return;
-  const int e = __ldcg(p.touched + u);
-  const int off = __ldcg(p.offsets + e), n = __ldcg(p.counts + e);
-  const int col0 = c * 64, k0 = s * GU_KR;
-  if (threadIdx.x == 0) {
-    mbar_init(bar, 1);
-    fence_mbar_init();
-    mbar_arrive_expect_tx(bar, 2 * TILE_BYTES);
-    tma_load_2d(tiles, &maps.wg, col0, e * H + k0, bar);
-    tma_load_2d(tiles + BOX_ROWS * 64, &maps.wu, col0, e * H + k0, bar);
-  }
-  __syncthreads();
-  if (!mbar_wait_bounded(bar, 0, p.status)) return;
-  const int rows_cap = p.T * K;
-  mac_tokens<2, GU_KR>(
-      tiles, xs, red, out, n,
-      [&](float* xsb, int t0, int nt, int ntb) {
-        stage_rows<GU_KR>(xsb, nt, ntb, k0, [&](int t) {
-          const int tok = __ldcg(p.perm + off + t0 + t) / K;
-          return p.xin + (size_t)tok * H;
-        });
-      },
-      [&](const float* o, int t0, int nt) {
-        for (int q = threadIdx.x; q < nt * 128; q += NTHREADS) {
-          const int t = q / 128, j = q % 128;
-          p.P_gu[((size_t)s * rows_cap + off + t0 + t) * (2 * I) + c * 128 + j] = o[q];
-        }
-      });
-  if (!ticket_arrive(p.tickets + TicketLayout::gu + e * GU_NCH + c, GU_KS, flag)) return;
-  for (int q = threadIdx.x; q < n * 64; q += NTHREADS) {
-    const int t = q / 64, j = q % 64;
-    float g = 0.f, uu = 0.f;
-    for (int ss = 0; ss < GU_KS; ++ss) {
-      const float* P = p.P_gu + ((size_t)ss * rows_cap + off + t) * (2 * I) + c * 128;
-      g += __ldcg(P + j);
-      uu += __ldcg(P + 64 + j);
-    }
-    p.h[(size_t)(off + t) * I + col0 + j] = __float2bfloat16_rn(silu_f32(g) * uu);
-  }
-}
-
-__device__ void shared_down_tile(const Params& p, const StreamMaps& maps, uint8_t* sm, int unit) {
-  const int c = unit % SD_NCH, s = unit / SD_NCH;
-  const int col0 = c * 64, k0 = s * SD_KR;
-  bf16* tiles = reinterpret_cast<bf16*>(sm + SmemSD::tiles);
-  float* xs = reinterpret_cast<float*>(sm + SmemSD::xs);
-  float* red = reinterpret_cast<float*>(sm + SmemSD::red);
-  float* out = reinterpret_cast<float*>(sm + SmemSD::out);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + SmemSD::bar);
-  int* flag = reinterpret_cast<int*>(sm + SmemSD::flag);
-  if (threadIdx.x == 0) {
-    mbar_init(bar, 1);
-    fence_mbar_init();
-    mbar_arrive_expect_tx(bar, TILE_BYTES);
-    tma_load_2d(tiles, &maps.wsd, col0, k0, bar);
-  }
-  pdl_wait();
-  __syncthreads();
-  if (!mbar_wait_bounded(bar, 0, p.status)) return;
-  const int T = p.T;
-  mac_tokens<1, SD_KR>(
-      tiles, xs, red, out, T,
-      [&](float* xsb, int t0, int nt, int ntb) {
-        stage_rows<SD_KR>(xsb, nt, ntb, k0, [&](int t) { return p.hs + (size_t)(t0 + t) * IS; });
-      },
-      [&](const float* o, int t0, int nt) {
-        for (int q = threadIdx.x; q < nt * 64; q += NTHREADS) {
-          const int t = q / 64, j = q % 64;
-          p.P_sd[((size_t)s * STREAM_MAX_T + t0 + t) * H + col0 + j] = o[q];
-        }
-      });
-  if (!ticket_arrive(p.tickets + TicketLayout::sd + c, SD_KS, flag)) return;
-  for (int q = threadIdx.x; q < T * 64; q += NTHREADS) {
-    const int t = q / 64, j = q % 64;
-    float v = 0.f;
-    for (int ss = 0; ss < SD_KS; ++ss) v += __ldcg(p.P_sd + ((size_t)ss * STREAM_MAX_T + t) * H + col0 + j);
-    p.S[(size_t)t * H + col0 + j] = v;
-  }
-}
-
 __global__ void __launch_bounds__(NTHREADS)
-    stream_k2(const __grid_constant__ Params p, const __grid_constant__ StreamMaps maps, int n_routed_ctas) {
+    stream_k2(const __grid_constant__ Params p, const __grid_constant__ StreamMaps maps) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = aligned_smem(smem_raw);
   pdl_launch_dependents();
-  if ((int)blockIdx.x < n_routed_ctas)
-    routed_gate_up_tile(p, maps, sm, blockIdx.x);
-  else
-    shared_down_tile(p, maps, sm, blockIdx.x - n_routed_ctas);
+  pdl_wait();
+  const int groups = __ldcg(p.n_groups);
+  const int U = __ldcg(p.n_touched);
+  // the next kernel reads the touched experts' down matrices: prefetch them when they fit
+  if ((unsigned long long)U * I * H * 2 <= p.prefetch_bytes_max && threadIdx.x == 0) {
+    const size_t per_e = (size_t)I * H * 2;
+    const size_t total = per_e * U;
+    const size_t share = ((total / gridDim.x) + 15) & ~size_t(15);
+    size_t a = share * blockIdx.x, b = a + share < total ? a + share : total;
+    while (a < b) {
+      const int u = int(a / per_e);
+      const size_t in_e = a % per_e;
+      size_t n = per_e - in_e;
+      if (n > b - a) n = b - a;
+      if (n > 65536) n = 65536;
+      const int e = __ldcg(p.touched + u);
+      prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(p.w_down + (size_t)e * I * H) + in_e, uint32_t(n));
+      a += n;
+    }
+  }
+  const int ntg = (p.T + NT_MAX - 1) / NT_MAX;
+  BlockList L;
+  L.k_first = KIND_GU;
+  L.kb_first = GU_KB;
+  L.n_first = groups * GU_NCH * GU_KB;
+  L.k_second = KIND_SD;
+  L.kb_second = SD_KB;
+  L.n_total = L.n_first + ntg * OUT_NCH * SD_KB;
+  stream_blocks(p, maps, L, blockIdx.x, gridDim.x, sm);
 }
 
 // ================================================================ K3: routed down + combine
-__global__ void __launch_bounds__(NTHREADS) stream_k3(const __grid_constant__ Params p, const __grid_constant__ StreamMaps maps) {
+__global__ void __launch_bounds__(NTHREADS)
+    stream_k3(const __grid_constant__ Params p, const __grid_constant__ StreamMaps maps) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = aligned_smem(smem_raw);
   pdl_launch_dependents();
-  const int u = blockIdx.x / DN_NCH, c = blockIdx.x % DN_NCH;
-  bf16* tiles = reinterpret_cast<bf16*>(sm + SmemDN::tiles);
-  float* xs = reinterpret_cast<float*>(sm + SmemDN::xs);
-  float* red = reinterpret_cast<float*>(sm + SmemDN::red);
-  float* out = reinterpret_cast<float*>(sm + SmemDN::out);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + SmemDN::bar);
-  int* flag = reinterpret_cast<int*>(sm + SmemDN::flag);
   pdl_wait();
-  const int n_touched = __ldcg(p.n_touched);
-  if (u >= n_touched) return;
-  const int e = __ldcg(p.touched + u);
-  const int off = __ldcg(p.offsets + e), n = __ldcg(p.counts + e);
-  const int col0 = c * 64;
-  if (threadIdx.x == 0) {
-    mbar_init(bar, 1);
-    fence_mbar_init();
-    mbar_arrive_expect_tx(bar, 2 * TILE_BYTES);
-    tma_load_2d(tiles, &maps.wd, col0, e * I, bar);
-    tma_load_2d(tiles + BOX_ROWS * 64, &maps.wd, col0, e * I + BOX_ROWS, bar);
-  }
-  __syncthreads();
-  if (!mbar_wait_bounded(bar, 0, p.status)) return;
-  mac_tokens<1, I>(
-      tiles, xs, red, out, n,
-      [&](float* xsb, int t0, int nt, int ntb) {
-        stage_rows<I>(xsb, nt, ntb, 0, [&](int t) { return p.h + (size_t)(off + t0 + t) * I; });
-      },
-      [&](const float* o, int t0, int nt) {
-        for (int q = threadIdx.x; q < nt * 64; q += NTHREADS) {
-          const int t = q / 64, j = q % 64;
-          const int row = off + t0 + t;
-          const float g = __ldcg(p.topk_w + __ldcg(p.perm + row));
-          p.Y[(size_t)row * H + col0 + j] = g * o[q];
-        }
-      });
-  if (!ticket_arrive(p.tickets + TicketLayout::dn + c, (uint32_t)n_touched, flag)) return;
-  // combine of column chunk c: y = S + sum_j Y[inv(t, j)] (slot order) [+ x]
-  const bool residual = (p.flags & 2u) != 0;
-  for (int q = threadIdx.x; q < p.T * 64; q += NTHREADS) {
-    const int t = q / 64, j = q % 64;
-    float v = __ldcg(p.S + (size_t)t * H + col0 + j);
-#pragma unroll
-    for (int k = 0; k < K; ++k) v += __ldcg(p.Y + (size_t)__ldcg(p.inv + t * K + k) * H + col0 + j);
-    if (residual) v += __bfloat162float(p.x[(size_t)t * H + col0 + j]);
-    p.y[(size_t)t * H + col0 + j] = __float2bfloat16_rn(v);
-  }
+  const int groups = __ldcg(p.n_groups);
+  BlockList L;
+  L.k_first = L.k_second = KIND_DN;
+  L.kb_first = L.kb_second = DN_KB;
+  L.n_first = L.n_total = groups * OUT_NCH * DN_KB;
+  stream_blocks(p, maps, L, blockIdx.x, gridDim.x, sm);
 }
 
 // ================================================================ K0: RMSNorm (pre-norm layers)
@@ -688,7 +871,8 @@ __global__ void __launch_bounds__(NTHREADS) rmsnorm_kernel(const __grid_constant
     const __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * q] / d, f[2 * q + 1] / d);
     packed[q] = *reinterpret_cast<const uint32_t*>(&b);
   }
-  *reinterpret_cast<uint4*>(p.xn + (size_t)t * H + threadIdx.x * 8) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  *reinterpret_cast<uint4*>(p.xn + (size_t)t * H + threadIdx.x * 8) =
+      make_uint4(packed[0], packed[1], packed[2], packed[3]);
 }
 
 }  // namespace flint
