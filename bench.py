@@ -180,9 +180,13 @@ def run_ours(args, rank, world, local):
 
     times = {T: [] for T in SWEEP}
     clocks = ClockSampler(local)
+    clocks.start()
+    # keep the GPU busy (untimed) long enough for the clock sampler to see it under load
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < 1.5:
+        step({T: [] for T in SWEEP})
     barrier(world)
     torch.cuda.synchronize()
-    clocks.start()
     t_wall = time.perf_counter()
     for _ in range(args.steps):
         step(times)

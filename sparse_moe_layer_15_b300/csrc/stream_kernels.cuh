@@ -73,7 +73,8 @@ struct SmemST {  // persistent streaming CTA
   static constexpr int out = red + NWARPS * NT_MAX * 128 * 4;       // [NT_MAX][128] f32
   static constexpr int bars = out + NT_MAX * 128 * 4;               // NSTAGE mbarriers
   static constexpr int misc = bars + 8 * NSTAGE;                    // item broadcast, flags
-  static constexpr int bytes = misc + 128;
+  static constexpr int meta = misc + 128;                           // [4][E+1] int routing copy
+  static constexpr int bytes = meta + 4 * (E + 1) * 4;
 };
 struct SmemRT {  // router CTA + the permutation
   static constexpr int wr = 0;                                      // [256][256] bf16
@@ -147,12 +148,50 @@ struct Item {
   int KB;    // blocks per item
 };
 
+// Shared-memory copy of the routing metadata, per touched expert u: expert id, first sorted
+// row, row count and first token group (tgp has U+1 entries).
+struct Meta {
+  const int* e;
+  const int* off;
+  const int* cnt;
+  const int* tgp;
+  int U;       // touched experts
+  int groups;  // token groups over all touched experts
+};
+
+// Copy the routing metadata written by the router kernel into shared memory (all threads).
+__device__ Meta load_meta(const Params& p, uint8_t* sm) {
+  int* base = reinterpret_cast<int*>(sm + SmemST::meta);
+  Meta m;
+  m.U = __ldcg(p.n_touched);
+  m.groups = __ldcg(p.n_groups);
+  int* e = base;
+  int* off = base + (E + 1);
+  int* cnt = base + 2 * (E + 1);
+  int* tgp = base + 3 * (E + 1);
+  for (int u = threadIdx.x; u <= m.U; u += NTHREADS) {
+    tgp[u] = __ldcg(p.tgp + u);
+    if (u < m.U) {
+      const int ex = __ldcg(p.touched + u);
+      e[u] = ex;
+      off[u] = __ldcg(p.offsets + ex);
+      cnt[u] = __ldcg(p.counts + ex);
+    }
+  }
+  __syncthreads();
+  m.e = e;
+  m.off = off;
+  m.cnt = cnt;
+  m.tgp = tgp;
+  return m;
+}
+
 // largest u in [0, n) with tgp[u] <= gi
-__device__ __forceinline__ int find_group_owner(const int32_t* tgp, int n, int gi) {
+__device__ __forceinline__ int find_group_owner(const int* tgp, int n, int gi) {
   int lo = 0, hi = n - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (__ldcg(tgp + mid) <= gi)
+    if (tgp[mid] <= gi)
       lo = mid;
     else
       hi = mid - 1;
@@ -160,21 +199,27 @@ __device__ __forceinline__ int find_group_owner(const int32_t* tgp, int n, int g
   return lo;
 }
 
-__device__ Item decode_item(const Params& p, int kind, int idx) {
+// Item numbering: routed gate/up items are token-group major (gi * 8 + c); routed down items
+// are column-chunk major (c * groups + gi), so that each 64-column chunk of the output is a
+// contiguous run of blocks; shared items are token-group major.
+__device__ Item decode_item(const Params& p, const Meta& m, int kind, int idx) {
   Item it;
   it.kind = kind;
   it.idx = idx;
   if (kind == KIND_GU || kind == KIND_DN) {
-    const int nch = kind == KIND_GU ? GU_NCH : OUT_NCH;
-    const int gi = idx / nch;
-    it.c = idx % nch;
-    const int U = __ldcg(p.n_touched);
-    const int u = find_group_owner(p.tgp, U, gi);
-    const int tg = gi - __ldcg(p.tgp + u);
-    it.e = __ldcg(p.touched + u);
-    const int n = __ldcg(p.counts + it.e);
-    it.row0 = __ldcg(p.offsets + it.e) + tg * NT_MAX;
-    it.nt = min(NT_MAX, n - tg * NT_MAX);
+    int gi;
+    if (kind == KIND_GU) {
+      gi = idx / GU_NCH;
+      it.c = idx % GU_NCH;
+    } else {
+      it.c = idx / m.groups;
+      gi = idx % m.groups;
+    }
+    const int u = find_group_owner(m.tgp, m.U, gi);
+    const int tg = gi - m.tgp[u];
+    it.e = m.e[u];
+    it.row0 = m.off[u] + tg * NT_MAX;
+    it.nt = min(NT_MAX, m.cnt[u] - tg * NT_MAX);
     it.KB = kind == KIND_GU ? GU_KB : DN_KB;
   } else {
     const int nch = kind == KIND_SGU ? SGU_NCH : OUT_NCH;
@@ -208,11 +253,11 @@ __device__ __forceinline__ void block_kind(const BlockList& L, int b, int& kind,
   }
 }
 
-__device__ void issue_block(const Params& p, const StreamMaps& maps, const BlockList& L, int b, uint8_t* stage,
-                            uint64_t* bar) {
+__device__ void issue_block(const Params& p, const Meta& m, const StreamMaps& maps, const BlockList& L, int b,
+                            uint8_t* stage, uint64_t* bar) {
   int kind, idx, kb;
   block_kind(L, b, kind, idx, kb);
-  const Item it = decode_item(p, kind, idx);
+  const Item it = decode_item(p, m, kind, idx);
   mbar_arrive_expect_tx(bar, BLK_BYTES);
   const int x = it.c * 64;
   switch (kind) {
@@ -237,11 +282,13 @@ __device__ void issue_block(const Params& p, const StreamMaps& maps, const Block
 struct Stream {
   const Params* p;
   const StreamMaps* maps;
+  Meta meta;
   BlockList L;
-  int b0, nb;  // this CTA's block range
+  int g, nctas;  // this CTA and the grid's streaming CTAs
+  int b0, nb;    // this CTA's block range
   uint8_t* sm;
   uint64_t* bars;
-  int* misc;   // [0..7]: item broadcast; [8]: flags
+  int* misc;  // [0..7]: item broadcast; [8..11]: flags
 };
 
 // Wait for stage `st` of block number j: thread 0 waits (bounded); the others observe the
@@ -330,7 +377,7 @@ __device__ __forceinline__ uint32_t* item_ticket(const Params& p, const Item& it
 }
 
 // Final values of an item (fp32 sums [nt][ncol] in `vals`, row stride ncol) -> outputs.
-__device__ void item_epilogue(const Params& p, const Item& it, const float* vals, int* s_word) {
+__device__ void item_epilogue(const Params& p, const Item& it, const float* vals) {
   const int nt = it.nt, c = it.c;
   if (it.kind == KIND_GU || it.kind == KIND_SGU) {
     bf16* dst = it.kind == KIND_GU ? p.h : p.hs;
@@ -340,24 +387,23 @@ __device__ void item_epilogue(const Params& p, const Item& it, const float* vals
       const float g = vals[t * 128 + j], u = vals[t * 128 + 64 + j];
       dst[(size_t)(it.row0 + t) * ld + c * 64 + j] = __float2bfloat16_rn(silu_f32(g) * u);
     }
-    return;
-  }
-  if (it.kind == KIND_SD) {
+  } else if (it.kind == KIND_SD) {
     for (int q = threadIdx.x; q < nt * 64; q += NTHREADS) {
       const int t = q / 64, j = q % 64;
       p.S[(size_t)(it.row0 + t) * H + c * 64 + j] = vals[t * 64 + j];
     }
-    return;
+  } else {  // routed down: rows scaled by their gate
+    for (int q = threadIdx.x; q < nt * 64; q += NTHREADS) {
+      const int t = q / 64, j = q % 64;
+      const int row = it.row0 + t;
+      const float g = __ldcg(p.topk_w + __ldcg(p.perm + row));
+      p.Y[(size_t)row * H + c * 64 + j] = g * vals[t * 64 + j];
+    }
   }
-  // routed down: gated rows, then the combine of column chunk c once every group is in
-  for (int q = threadIdx.x; q < nt * 64; q += NTHREADS) {
-    const int t = q / 64, j = q % 64;
-    const int row = it.row0 + t;
-    const float g = __ldcg(p.topk_w + __ldcg(p.perm + row));
-    p.Y[(size_t)row * H + c * 64 + j] = g * vals[t * 64 + j];
-  }
-  const int groups = __ldcg(p.n_groups);
-  if (!ticket_last(p.tk_comb + c, uint32_t(groups), s_word)) return;
+}
+
+// The combine of output columns [64c, 64c + 64): y = S + sum_j Y[inv(t, j)] in slot order (+x).
+__device__ void combine_chunk(const Params& p, int c) {
   const bool residual = (p.flags & 2u) != 0;
   for (int q = threadIdx.x; q < p.T * 64; q += NTHREADS) {
     const int t = q / 64, j = q % 64;
@@ -368,6 +414,25 @@ __device__ void item_epilogue(const Params& p, const Item& it, const float* vals
     if (residual) v += __bfloat162float(p.x[(size_t)t * H + col]);
     p.y[(size_t)t * H + col] = __float2bfloat16_rn(v);
   }
+}
+
+// The CTA owning block b when N blocks are split evenly over n CTAs (b0(g) = N*g/n).
+__device__ __forceinline__ int block_owner(long long b, long long N, int n) {
+  return int(((b + 1) * n - 1) / N);
+}
+
+// This CTA has written all its routed-down rows of chunk c: arrive; the last of the CTAs
+// that cover the chunk's blocks runs the combine of the chunk.
+__device__ void arrive_chunk(Stream& S, int c) {
+  const long long N = S.L.n_total;
+  const long long per_chunk = (long long)S.meta.groups * DN_KB;
+  const int g_lo = block_owner(per_chunk * c, N, S.nctas);
+  const int g_hi = block_owner(per_chunk * (c + 1) - 1, N, S.nctas);
+  uint32_t expect = 0;
+  for (int g = g_lo; g <= g_hi; ++g)
+    if (N * (g + 1) / S.nctas > N * g / S.nctas) ++expect;
+  if (ticket_last(S.p->tk_comb + c, expect, S.misc + 11)) combine_chunk(*S.p, c);
+  __syncthreads();
 }
 
 // One segment: blocks [kb_start, kb_start + nblk) of item `it`, consumed as CTA blocks
@@ -415,12 +480,13 @@ __device__ bool run_segment(Stream& S, const Item& it, int kb_start, int nblk, i
                           (kb_start + q) * KR);
     __syncthreads();  // every thread is done with this stage
     if (threadIdx.x == 0 && j + NSTAGE < S.nb)
-      issue_block(p, *S.maps, S.L, S.b0 + j + NSTAGE, S.sm + SmemST::stages + st * BLK_BYTES, S.bars + st);
+      issue_block(p, S.meta, *S.maps, S.L, S.b0 + j + NSTAGE, S.sm + SmemST::stages + st * BLK_BYTES,
+                  S.bars + st);
   }
   reduce_acc<NT, NM>(acc, red, out);
   constexpr int ncol = NM * 64;
   if (kb_start == 0 && nblk == it.KB) {
-    item_epilogue(p, it, out, S.misc + 9);
+    item_epilogue(p, it, out);
     __syncthreads();
     return true;
   }
@@ -438,7 +504,7 @@ __device__ bool run_segment(Stream& S, const Item& it, int kb_start, int nblk, i
       out[q] = s;
     }
     __syncthreads();
-    item_epilogue(p, it, out, S.misc + 9);
+    item_epilogue(p, it, out);
   }
   __syncthreads();
   return true;
@@ -453,13 +519,17 @@ __device__ __forceinline__ bool run_segment_nt(Stream& S, const Item& it, int kb
 }
 
 // Persistent stream over blocks [0, n_total) of L, split evenly over `nctas` CTAs (this is
-// CTA `g`).  All threads of the CTA call it.
-__device__ void stream_blocks(const Params& p, const StreamMaps& maps, const BlockList& L, int g, int nctas,
-                              uint8_t* sm) {
+// CTA `g`).  All threads of the CTA call it.  `meta` is the shared-memory routing copy
+// (unused by shared-expert-only lists).
+__device__ void stream_blocks(const Params& p, const Meta& meta, const StreamMaps& maps, const BlockList& L, int g,
+                              int nctas, uint8_t* sm) {
   Stream S;
   S.p = &p;
   S.maps = &maps;
+  S.meta = meta;
   S.L = L;
+  S.g = g;
+  S.nctas = nctas;
   S.sm = sm;
   S.bars = reinterpret_cast<uint64_t*>(sm + SmemST::bars);
   S.misc = reinterpret_cast<int*>(sm + SmemST::misc);
@@ -472,32 +542,20 @@ __device__ void stream_blocks(const Params& p, const StreamMaps& maps, const Blo
     for (int s = 0; s < NSTAGE; ++s) mbar_init(S.bars + s, 1);
     fence_mbar_init();
     for (int s = 0; s < NSTAGE && s < S.nb; ++s)
-      issue_block(p, maps, L, S.b0 + s, sm + SmemST::stages + s * BLK_BYTES, S.bars + s);
+      issue_block(p, S.meta, maps, L, S.b0 + s, sm + SmemST::stages + s * BLK_BYTES, S.bars + s);
   }
   __syncthreads();
+  const bool combine = L.k_first == KIND_DN;
+  int cur_chunk = -1;
   int j = 0;
   while (j < S.nb) {
     int kind, idx, kb;
     block_kind(L, S.b0 + j, kind, idx, kb);
-    if (threadIdx.x == 0) {
-      const Item it = decode_item(p, kind, idx);
-      int* m = S.misc;
-      m[0] = it.e;
-      m[1] = it.row0;
-      m[2] = it.nt;
-      m[3] = it.c;
-      m[4] = it.KB;
+    const Item it = decode_item(p, S.meta, kind, idx);  // every thread: shared-memory lookups
+    if (combine && it.c != cur_chunk) {
+      if (cur_chunk >= 0) arrive_chunk(S, cur_chunk);
+      cur_chunk = it.c;
     }
-    __syncthreads();
-    Item it;
-    it.kind = kind;
-    it.idx = idx;
-    it.e = S.misc[0];
-    it.row0 = S.misc[1];
-    it.nt = S.misc[2];
-    it.c = S.misc[3];
-    it.KB = S.misc[4];
-    __syncthreads();
     const int nblk = min(it.KB - kb, S.nb - j);
     bool ok;
     if (kind == KIND_GU || kind == KIND_SGU)
@@ -506,6 +564,7 @@ __device__ void stream_blocks(const Params& p, const StreamMaps& maps, const Blo
       ok = run_segment_nt<1, DN_ROWS>(S, it, kb, nblk, j);
     if (!ok) return;
   }
+  if (combine && cur_chunk >= 0) arrive_chunk(S, cur_chunk);
 }
 
 // Spread a bulk L2 prefetch of `bytes` (multiple of 16) at `base` over `nctas` CTAs.
@@ -547,7 +606,8 @@ __global__ void __cluster_dims__(RT_CL, 1, 1) __launch_bounds__(NTHREADS)
   L.k_second = KIND_SGU;
   L.kb_first = L.kb_second = GU_KB;
   L.n_first = L.n_total = ntg * SGU_NCH * GU_KB;
-  stream_blocks(p, maps, L, g, n_stream_ctas, sm);
+  Meta none{};
+  stream_blocks(p, none, maps, L, g, n_stream_ctas, sm);
 }
 
 __device__ void router_cluster(const Params& p, uint8_t* sm, int cl, int rank) {
@@ -798,8 +858,9 @@ __global__ void __launch_bounds__(NTHREADS)
   uint8_t* sm = aligned_smem(smem_raw);
   pdl_launch_dependents();
   pdl_wait();
-  const int groups = __ldcg(p.n_groups);
-  const int U = __ldcg(p.n_touched);
+  const Meta meta = load_meta(p, sm);
+  const int groups = meta.groups;
+  const int U = meta.U;
   // the next kernel reads the touched experts' down matrices: prefetch them when they fit
   if ((unsigned long long)U * I * H * 2 <= p.prefetch_bytes_max && threadIdx.x == 0) {
     const size_t per_e = (size_t)I * H * 2;
@@ -825,7 +886,7 @@ __global__ void __launch_bounds__(NTHREADS)
   L.k_second = KIND_SD;
   L.kb_second = SD_KB;
   L.n_total = L.n_first + ntg * OUT_NCH * SD_KB;
-  stream_blocks(p, maps, L, blockIdx.x, gridDim.x, sm);
+  stream_blocks(p, meta, maps, L, blockIdx.x, gridDim.x, sm);
 }
 
 // ================================================================ K3: routed down + combine
@@ -835,12 +896,12 @@ __global__ void __launch_bounds__(NTHREADS)
   uint8_t* sm = aligned_smem(smem_raw);
   pdl_launch_dependents();
   pdl_wait();
-  const int groups = __ldcg(p.n_groups);
+  const Meta meta = load_meta(p, sm);
   BlockList L;
   L.k_first = L.k_second = KIND_DN;
   L.kb_first = L.kb_second = DN_KB;
-  L.n_first = L.n_total = groups * OUT_NCH * DN_KB;
-  stream_blocks(p, maps, L, blockIdx.x, gridDim.x, sm);
+  L.n_first = L.n_total = meta.groups * OUT_NCH * DN_KB;
+  stream_blocks(p, meta, maps, L, blockIdx.x, gridDim.x, sm);
 }
 
 // ================================================================ K0: RMSNorm (pre-norm layers)
