@@ -337,6 +337,31 @@ def run_reference(args, rank, world, local):
                 e2e=dict(value=round(v, 3), unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
 
 
+def run_profile_case(args):
+    """A small, fixed case for profilers: `steps` forwards at T = --profile tokens, L2
+    flushed before each, nothing else (no soak, no timing passes)."""
+    import torch
+
+    import synth
+    import sparse_moe_layer_15_b300 as fm
+
+    dev = torch.device("cuda", 0)
+    T = args.profile
+    w = synth.flint_weights(seed=0, device=dev)
+    layer = fm.FlintMoE(w, max_tokens=T)
+    x = synth.torch_normal_bf16((T, fm.HIDDEN), 1000 + T, synth.TAG_X, 1.0, device=dev)
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup + args.steps):
+        flush_buf.fill_(1)
+        y = layer.forward(x)
+    torch.cuda.synchronize()
+    rc = layer.poll_device_status()
+    layer.close()
+    print(json.dumps(dict(profile_case=T, steps=args.steps, device_status=rc, y_abs_mean=float(y.float().abs().mean()))))
+    if rc != 0:
+        raise SystemExit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -345,7 +370,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--profile", type=int, default=0, help="profiler case: forwards at this T only")
     args = ap.parse_args()
+    if args.profile:
+        run_profile_case(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     rank, world, local = dist_setup()
