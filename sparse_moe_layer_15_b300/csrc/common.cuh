@@ -64,6 +64,9 @@ struct Params {
   float* P_sgu;
   float* P_sd;
   float* P_dn;
+  float* RP;             // [32][256][E] router partial logits (decode path)
+  uint32_t* bar_count;   // [1] grid-barrier counter (decode path; reset at kernel end)
+  uint32_t* bar_done;    // [1]
   uint32_t* tk_router;   // [1] tickets (zero between kernels: the last arriver resets)
   uint32_t* tk_gu;
   uint32_t* tk_sgu;

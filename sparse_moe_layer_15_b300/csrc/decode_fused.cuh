@@ -1,0 +1,973 @@
+// Decode-size path of the Flint MoE layer (T <= STREAM_MAX_T tokens): ONE persistent
+// cooperative kernel per forward.
+//
+// At these sizes the layer is bound by reading weights once -- 6 MB per touched expert, 12 MB
+// of shared expert, 1 MB of router -- and by latency: a separate kernel per step pays a
+// launch, a ramp-up and a tail each time.  So one CTA per SM runs every step in turn, the
+// steps separated by grid-wide barriers (bounded spins on a global counter; the cooperative
+// launch guarantees that all CTAs are resident):
+//
+//   A  router partial logits (32 KB blocks of W_r rows, all 256 experts) and the shared
+//      expert's gate/up with fused SiLU-mul; the shared down matrix is prefetched into L2;
+//   -- barrier --
+//   B  routing: logits summed over the 32 row blocks in order, + bias, sigmoid, top-6 with
+//      the lower index first on ties, renormalised gates; for T <= 4 every CTA routes every
+//      token itself (no barrier), otherwise each CTA routes its own tokens and a barrier
+//      publishes them; then every CTA builds the expert permutation (stable counting sort)
+//      in its own shared memory and starts streaming step C;
+//   C  routed gate/up (touched experts only) with fused SiLU-mul, and the shared down
+//      projection; the touched experts' down matrices are prefetched into L2 when they fit;
+//   -- barrier --
+//   D  routed down projection scaled by the gates; the last CTA to finish each 64-column
+//      chunk of the output performs the combine y = S + sum_j Y[inv(t, j)] in slot order.
+//
+// Within a step, the weight traffic is a list of equal 32 KB blocks (64 output columns x 128
+// or 256 rows of one or two matrices, or 64 rows of the router); every CTA takes an equal
+// contiguous range and streams it through a 4-stage TMA pipeline into shared memory, where
+// CUDA cores multiply it against the few token rows.  Blocks of the same output columns
+// accumulate in registers; a range boundary inside an item leaves a partial sum that the
+// last CTA to finish the item adds in block order (an integer ticket that records which
+// partial slots exist): deterministic, no floating-point atomics.
+#pragma once
+
+#include "common.cuh"
+
+namespace flint {
+
+constexpr int NTHREADS = 256;
+constexpr int NWARPS = NTHREADS / 32;
+constexpr int STREAM_MAX_T = 256;
+constexpr int NT_MAX = 8;  // token rows per register block (a "token group")
+constexpr int NSTAGE = 4;
+constexpr int BLK_BYTES = 32768;
+constexpr int GU_ROWS = 128;         // gate/up block: 128 rows x 64 columns of gate and of up
+constexpr int DN_ROWS = 256;         // down block: 256 rows x 64 columns
+constexpr int RT_ROWS = 64;          // router block: 64 rows x 256 experts
+constexpr int GU_KB = H / GU_ROWS;   // 16 blocks per gate/up item
+constexpr int SD_KB = IS / DN_ROWS;  // 4 blocks per shared-down item
+constexpr int DN_KB = I / DN_ROWS;   // 2 blocks per routed-down item
+constexpr int RT_NB = H / RT_ROWS;   // 32 router blocks per token group
+constexpr int GU_NCH = I / 64;       // 8 column chunks of a routed expert's gate/up
+constexpr int SGU_NCH = IS / 64;     // 16 column chunks of the shared gate/up
+constexpr int OUT_NCH = H / 64;      // 32 column chunks of a down projection
+constexpr int REDUNDANT_ROUTING_MAX_T = 4;
+constexpr int MAX_PAIRS = STREAM_MAX_T * K;
+
+enum Kind : int { KIND_RT = 0, KIND_GU = 1, KIND_SGU = 2, KIND_SD = 3, KIND_DN = 4 };
+
+struct StreamMaps {
+  CUtensorMap wg;   // w_gate as [E*H][I], box 64 x 128
+  CUtensorMap wu;   // w_up   as [E*H][I], box 64 x 128
+  CUtensorMap wd;   // w_down as [E*I][H], box 64 x 256
+  CUtensorMap wsg;  // [H][IS], box 64 x 128
+  CUtensorMap wsu;  // [H][IS], box 64 x 128
+  CUtensorMap wsd;  // [IS][H], box 64 x 256
+};
+
+// Largest number of token groups (of NT_MAX expert-sorted rows) a call of T tokens can have.
+__host__ __device__ constexpr int max_groups(int T) {
+  const int pairs = T * K;
+  const int u = pairs < E ? pairs : E;
+  const int g = (pairs + NT_MAX - 1) / NT_MAX + u;
+  return g < pairs ? g : pairs;
+}
+
+// ---------------------------------------------------------------- shared memory
+struct Smem {
+  static constexpr int stages = 0;                             // NSTAGE x 32 KB
+  static constexpr int xs = stages + NSTAGE * BLK_BYTES;       // [NT_MAX][<=2048] bf16
+  static constexpr int red = xs + NT_MAX * H * 2;              // [8][NT_MAX][128] f32 (+ reuse)
+  static constexpr int out = red + NWARPS * NT_MAX * 128 * 4;  // [NT_MAX][128] f32
+  static constexpr int bars = out + NT_MAX * 128 * 4;          // NSTAGE mbarriers
+  static constexpr int misc = bars + 8 * NSTAGE;               // flags
+  static constexpr int meta = misc + 128;                      // [4][E+1] int
+  static constexpr int perm = meta + 4 * (E + 1) * 4;          // [MAX_PAIRS] int
+  static constexpr int inv = perm + MAX_PAIRS * 4;             // [MAX_PAIRS] int
+  static constexpr int gw = inv + MAX_PAIRS * 4;               // [MAX_PAIRS] f32
+  static constexpr int bytes = gw + MAX_PAIRS * 4;
+  // reuse of `red` outside the streaming steps
+  static constexpr int scores = red;                  // [4][E] f32 (routing)
+  static constexpr int s_cnt = red;                   // [E] int (permutation)
+  static constexpr int s_fill = s_cnt + E * 4;        // [E] int
+  static constexpr int s_wcnt = s_fill + E * 4;       // [8][E] int
+  static constexpr int s_wsum = s_wcnt + NWARPS * E * 4;   // [3][8] int
+  static constexpr int s_idx = s_wsum + 128;          // [MAX_PAIRS] int
+};
+static_assert(Smem::s_idx + MAX_PAIRS * 4 <= Smem::out, "routing scratch must fit in the reduction buffer");
+constexpr int FUSED_SMEM = Smem::bytes + 1024;
+static_assert(FUSED_SMEM <= 227 * 1024, "shared memory budget");
+
+__device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
+  uint32_t a = smem_u32(raw);
+  uint32_t pad = (1024u - (a & 1023u)) & 1023u;
+  return raw + pad;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// ---------------------------------------------------------------- tickets and barriers
+// Arrive after this CTA's global writes with `add` (nblk in the low 8 bits plus one bit per
+// partial slot); returns in every thread the counter value after the add when this CTA
+// completed the item (low byte == KB), or 0.  The last arriver resets the counter.
+__device__ __forceinline__ uint32_t ticket_add(uint32_t* ticket, uint32_t add, uint32_t KB, int* s_word) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t now = atomicAdd(ticket, add) + add;
+    const bool last = (now & 0xFFu) == KB;
+    if (last) atomicExch(ticket, 0u);
+    *s_word = last ? int(now) : 0;
+  }
+  __syncthreads();
+  const uint32_t v = uint32_t(*s_word);
+  if (v) __threadfence();
+  return v;
+}
+
+__device__ __forceinline__ bool ticket_last(uint32_t* ticket, uint32_t total, int* s_word) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t old = atomicAdd(ticket, 1u);
+    const bool last = (old == total - 1);
+    if (last) atomicExch(ticket, 0u);
+    *s_word = last ? 1 : 0;
+  }
+  __syncthreads();
+  const bool last = *s_word != 0;
+  if (last) __threadfence();
+  return last;
+}
+
+// Grid-wide barrier number `k` (1, 2, ...) of this forward: every CTA adds 1 to a global
+// counter and waits (bounded) until it reaches k * gridDim.x.  Returns false on timeout.
+__device__ bool grid_sync(const Params& p, int k, int* s_flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(p.bar_count, 1u);
+    const uint32_t target = uint32_t(k) * gridDim.x;
+    int ok = 1;
+    if (ld_acquire_u32(p.bar_count) < target) {
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire_u32(p.bar_count) < target) {
+        if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+          record_status(p.status, ST_TIMEOUT);
+          ok = 0;
+          break;
+        }
+      }
+    }
+    __threadfence();
+    *s_flag = ok;
+  }
+  __syncthreads();
+  return *s_flag != 0;
+}
+
+// After the last barrier: the last CTA to get here resets the barrier counter.
+__device__ void grid_done(const Params& p, int* s_flag) {
+  if (ticket_last(p.bar_done, gridDim.x, s_flag) && threadIdx.x == 0) atomicExch(p.bar_count, 0u);
+}
+
+// ---------------------------------------------------------------- work items
+struct Item {
+  int kind;
+  int idx;   // item index within its kind
+  int e;     // routed expert, or -1
+  int row0;  // first row: expert-sorted row (routed), token (shared), token (router)
+  int nt;    // rows in this token group (1..NT_MAX)
+  int c;     // 64-column chunk (router: row block)
+  int KB;    // blocks per item
+};
+
+// Shared-memory routing tables of this CTA, per touched expert u: expert id, first sorted
+// row, row count, first token group (tgp has U+1 entries).
+struct Meta {
+  const int* e;
+  const int* off;
+  const int* cnt;
+  const int* tgp;
+  int U;
+  int groups;
+};
+
+// largest u in [0, n) with tgp[u] <= gi
+__device__ __forceinline__ int find_group_owner(const int* tgp, int n, int gi) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tgp[mid] <= gi)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+// Item numbering: router items (tg * 32 + row block); routed gate/up items token-group major
+// (gi * 8 + c); routed down items column-chunk major (c * groups + gi), so that each 64-column
+// chunk of the output is one contiguous run of blocks; shared items token-group major.
+__device__ __forceinline__ Item decode_item(int T, const Meta& m, int kind, int idx) {
+  Item it;
+  it.kind = kind;
+  it.idx = idx;
+  if (kind == KIND_GU || kind == KIND_DN) {
+    int gi;
+    if (kind == KIND_GU) {
+      gi = idx / GU_NCH;
+      it.c = idx % GU_NCH;
+    } else {
+      it.c = idx / m.groups;
+      gi = idx % m.groups;
+    }
+    const int u = find_group_owner(m.tgp, m.U, gi);
+    const int tg = gi - m.tgp[u];
+    it.e = m.e[u];
+    it.row0 = m.off[u] + tg * NT_MAX;
+    it.nt = min(NT_MAX, m.cnt[u] - tg * NT_MAX);
+    it.KB = kind == KIND_GU ? GU_KB : DN_KB;
+  } else {
+    const int nch = kind == KIND_RT ? RT_NB : kind == KIND_SGU ? SGU_NCH : OUT_NCH;
+    const int tg = idx / nch;
+    it.c = idx % nch;
+    it.e = -1;
+    it.row0 = tg * NT_MAX;
+    it.nt = min(NT_MAX, T - tg * NT_MAX);
+    it.KB = kind == KIND_RT ? 1 : kind == KIND_SGU ? GU_KB : SD_KB;
+  }
+  return it;
+}
+
+// The blocks of one step: [0, n_first) of kind k_first, then [n_first, n_total) of k_second.
+struct BlockList {
+  int k_first, k_second;
+  int n_first, n_total;
+  int kb_first, kb_second;
+};
+
+__device__ __forceinline__ void block_kind(const BlockList& L, int b, int& kind, int& idx, int& kb) {
+  if (b < L.n_first) {
+    kind = L.k_first;
+    idx = b / L.kb_first;
+    kb = b % L.kb_first;
+  } else {
+    kind = L.k_second;
+    const int r = b - L.n_first;
+    idx = r / L.kb_second;
+    kb = r % L.kb_second;
+  }
+}
+
+__device__ void issue_block(const Params& p, const Meta& m, const StreamMaps& maps, const BlockList& L, int b,
+                            uint8_t* stage, uint64_t* bar) {
+  int kind, idx, kb;
+  block_kind(L, b, kind, idx, kb);
+  const Item it = decode_item(p.T, m, kind, idx);
+  mbar_arrive_expect_tx(bar, BLK_BYTES);
+  const int x = it.c * 64;
+  switch (kind) {
+    case KIND_RT:
+      bulk_g2s(stage, p.w_router + (size_t)it.c * RT_ROWS * E, BLK_BYTES, bar);
+      break;
+    case KIND_GU:
+      tma_load_2d(stage, &maps.wg, x, it.e * H + kb * GU_ROWS, bar);
+      tma_load_2d(stage + BLK_BYTES / 2, &maps.wu, x, it.e * H + kb * GU_ROWS, bar);
+      break;
+    case KIND_SGU:
+      tma_load_2d(stage, &maps.wsg, x, kb * GU_ROWS, bar);
+      tma_load_2d(stage + BLK_BYTES / 2, &maps.wsu, x, kb * GU_ROWS, bar);
+      break;
+    case KIND_SD:
+      tma_load_2d(stage, &maps.wsd, x, kb * DN_ROWS, bar);
+      break;
+    default:
+      tma_load_2d(stage, &maps.wd, x, it.e * I + kb * DN_ROWS, bar);
+      break;
+  }
+}
+
+// ---------------------------------------------------------------- the per-CTA stream
+struct Stream {
+  const Params* p;
+  const StreamMaps* maps;
+  Meta meta;
+  BlockList L;
+  int nctas;
+  int b0, nb;  // this CTA's block range
+  int ring;    // blocks consumed by this CTA before this step (stage ring position)
+  uint8_t* sm;
+  uint64_t* bars;
+  int* misc;  // [8..15]: flags
+  const int* perm;
+  const int* inv;
+  const float* gw;
+};
+
+__device__ __forceinline__ uint8_t* stage_ptr(Stream& S, int j) {
+  return S.sm + Smem::stages + ((S.ring + j) % NSTAGE) * BLK_BYTES;
+}
+
+// Wait for CTA-local block j of this step: thread 0 waits (bounded); the others observe the
+// already-completed phase.  Uniform result across the CTA.
+__device__ __forceinline__ bool wait_stage(Stream& S, int j) {
+  const int st = (S.ring + j) % NSTAGE;
+  const uint32_t par = uint32_t((S.ring + j) / NSTAGE) & 1u;
+  int* ok = S.misc + 8;
+  if (threadIdx.x == 0) *ok = mbar_wait_bounded(S.bars + st, par, S.p->status) ? 1 : 0;
+  __syncthreads();
+  if (!*ok) return false;
+  while (!mbar_try_wait(S.bars + st, par)) {
+  }
+  return true;
+}
+
+// Block j has been consumed by every thread: refill its stage with block j + NSTAGE.
+__device__ __forceinline__ void refill(Stream& S, int j) {
+  if (threadIdx.x == 0 && j + NSTAGE < S.nb)
+    issue_block(*S.p, S.meta, *S.maps, S.L, S.b0 + j + NSTAGE, stage_ptr(S, j), S.bars + (S.ring + j) % NSTAGE);
+}
+
+// acc[t][m][q] += sum over rows r of block `stg` of xs[t][k0 + r] * tile_m[r][ch*8 + q].
+// Lane = (row quarter rsub, 16-byte column chunk ch); warps own contiguous row ranges.
+template <int NT, int NM, int KR>
+__device__ __forceinline__ void mac_block(float (&acc)[NT][NM][8], const bf16* __restrict__ stg,
+                                          const bf16* __restrict__ xs, int xlen, int k0) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int rsub = lane >> 3, ch = lane & 7;
+  constexpr int RPW = KR / NWARPS;
+#pragma unroll 4
+  for (int i = 0; i < RPW / 4; ++i) {
+    const int r = warp * RPW + i * 4 + rsub;
+    float xv[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) xv[t] = __bfloat162float(xs[t * xlen + k0 + r]);
+#pragma unroll
+    for (int m = 0; m < NM; ++m) {
+      const uint4 w = *reinterpret_cast<const uint4*>(stg + (size_t)m * KR * 64 + r * 64 + ch * 8);
+      float wf[8];
+      bf16x8_to_f32(w, wf);
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[t][m][q] = fmaf(xv[t], wf[q], acc[t][m][q]);
+    }
+  }
+}
+
+// Sum acc over the row lanes (fixed shuffle tree) and the warps (warp order) into out[t][m*64+c].
+template <int NT, int NM>
+__device__ __forceinline__ void reduce_acc(float (&acc)[NT][NM][8], float* red, float* out) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int rsub = lane >> 3, ch = lane & 7;
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+#pragma unroll
+    for (int m = 0; m < NM; ++m)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float v = acc[t][m][q];
+        v += __shfl_xor_sync(0xffffffffu, v, 8);
+        v += __shfl_xor_sync(0xffffffffu, v, 16);
+        if (rsub == 0) red[((warp * NT + t) * NM + m) * 64 + ch * 8 + q] = v;
+      }
+  __syncthreads();
+  for (int o = threadIdx.x; o < NT * NM * 64; o += NTHREADS) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < NWARPS; ++w) s += red[w * NT * NM * 64 + o];
+    out[o] = s;
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ float* partial_slot(const Params& p, const Item& it, int slot) {
+  switch (it.kind) {
+    case KIND_GU: return p.P_gu + ((size_t)it.idx * GU_KB + slot) * (NT_MAX * 128);
+    case KIND_SGU: return p.P_sgu + ((size_t)it.idx * GU_KB + slot) * (NT_MAX * 128);
+    case KIND_SD: return p.P_sd + ((size_t)it.idx * SD_KB + slot) * (NT_MAX * 64);
+    default: return p.P_dn + ((size_t)it.idx * DN_KB + slot) * (NT_MAX * 64);
+  }
+}
+
+__device__ __forceinline__ uint32_t* item_ticket(const Params& p, const Item& it) {
+  switch (it.kind) {
+    case KIND_GU: return p.tk_gu + it.idx;
+    case KIND_SGU: return p.tk_sgu + it.idx;
+    case KIND_SD: return p.tk_sd + it.idx;
+    default: return p.tk_dn + it.idx;
+  }
+}
+
+// Final values of an item (fp32 sums [nt][ncol] in `vals`) -> outputs.
+__device__ void item_epilogue(Stream& S, const Item& it, const float* vals) {
+  const Params& p = *S.p;
+  const int nt = it.nt, c = it.c;
+  if (it.kind == KIND_GU || it.kind == KIND_SGU) {
+    bf16* dst = it.kind == KIND_GU ? p.h : p.hs;
+    const int ld = it.kind == KIND_GU ? I : IS;
+    for (int q = threadIdx.x; q < nt * 64; q += NTHREADS) {
+      const int t = q / 64, j = q % 64;
+      const float g = vals[t * 128 + j], u = vals[t * 128 + 64 + j];
+      dst[(size_t)(it.row0 + t) * ld + c * 64 + j] = __float2bfloat16_rn(silu_f32(g) * u);
+    }
+  } else if (it.kind == KIND_SD) {
+    for (int q = threadIdx.x; q < nt * 64; q += NTHREADS) {
+      const int t = q / 64, j = q % 64;
+      p.S[(size_t)(it.row0 + t) * H + c * 64 + j] = vals[t * 64 + j];
+    }
+  } else {  // routed down: rows scaled by their gate
+    for (int q = threadIdx.x; q < nt * 64; q += NTHREADS) {
+      const int t = q / 64, j = q % 64;
+      const int row = it.row0 + t;
+      p.Y[(size_t)row * H + c * 64 + j] = S.gw[S.perm[row]] * vals[t * 64 + j];
+    }
+  }
+}
+
+// The combine of output columns [64c, 64c + 64): y = S + sum_j Y[inv(t, j)] in slot order (+x).
+__device__ void combine_chunk(Stream& S, int c) {
+  const Params& p = *S.p;
+  const bool residual = (p.flags & 2u) != 0;
+  for (int q = threadIdx.x; q < p.T * 64; q += NTHREADS) {
+    const int t = q / 64, j = q % 64;
+    const int col = c * 64 + j;
+    float v = __ldcg(p.S + (size_t)t * H + col);
+#pragma unroll
+    for (int k = 0; k < K; ++k) v += __ldcg(p.Y + (size_t)S.inv[t * K + k] * H + col);
+    if (residual) v += __bfloat162float(p.x[(size_t)t * H + col]);
+    p.y[(size_t)t * H + col] = __float2bfloat16_rn(v);
+  }
+}
+
+// The CTA owning block b when N blocks are split evenly over n CTAs (b0(g) = N*g/n).
+__device__ __forceinline__ int block_owner(long long b, long long N, int n) {
+  return int(((b + 1) * n - 1) / N);
+}
+
+// This CTA has written all its routed-down rows of chunk c: arrive; the last of the CTAs
+// that cover the chunk's blocks runs the combine of the chunk.
+__device__ void arrive_chunk(Stream& S, int c) {
+  const long long N = S.L.n_total;
+  const long long per_chunk = (long long)S.meta.groups * DN_KB;
+  const int g_lo = block_owner(per_chunk * c, N, S.nctas);
+  const int g_hi = block_owner(per_chunk * (c + 1) - 1, N, S.nctas);
+  uint32_t expect = 0;
+  for (int g = g_lo; g <= g_hi; ++g)
+    if (N * (g + 1) / S.nctas > N * g / S.nctas) ++expect;
+  if (ticket_last(S.p->tk_comb + c, expect, S.misc + 11)) combine_chunk(S, c);
+  __syncthreads();
+}
+
+// Router block (one item): partial logits of the token group over 64 router rows.
+// Thread e owns expert e: rows ascending, one fma chain per token.
+template <int NT>
+__device__ bool run_router_block(Stream& S, const Item& it, int& j) {
+  const Params& p = *S.p;
+  float* xs = reinterpret_cast<float*>(S.sm + Smem::xs);  // [NT][64] f32
+  const int r0 = it.c * RT_ROWS;
+  for (int q = threadIdx.x; q < NT * RT_ROWS; q += NTHREADS) {
+    const int t = q / RT_ROWS, r = q % RT_ROWS;
+    xs[q] = t < it.nt ? __bfloat162float(p.xin[(size_t)(it.row0 + t) * H + r0 + r]) : 0.f;
+  }
+  __syncthreads();
+  if (!wait_stage(S, j)) return false;
+  const bf16* w = reinterpret_cast<const bf16*>(stage_ptr(S, j));
+  const int e = threadIdx.x;
+  float acc[NT];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+#pragma unroll 8
+  for (int r = 0; r < RT_ROWS; ++r) {
+    const float wv = __bfloat162float(w[r * E + e]);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[t] = fmaf(xs[t * RT_ROWS + r], wv, acc[t]);
+  }
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+    if (t < it.nt) p.RP[((size_t)it.c * STREAM_MAX_T + it.row0 + t) * E + e] = acc[t];
+  __syncthreads();
+  refill(S, j);
+  ++j;
+  return true;
+}
+
+// One segment: blocks [kb_start, kb_start + nblk) of item `it`, consumed as CTA blocks
+// j .. j + nblk - 1.  Returns false on a device timeout.
+template <int NT, int NM, int KR>
+__device__ bool run_segment(Stream& S, const Item& it, int kb_start, int nblk, int& j) {
+  const Params& p = *S.p;
+  bf16* xs = reinterpret_cast<bf16*>(S.sm + Smem::xs);
+  float* red = reinterpret_cast<float*>(S.sm + Smem::red);
+  float* out = reinterpret_cast<float*>(S.sm + Smem::out);
+  // stage the token group's input rows (bf16) for the whole item
+  const int xlen = it.kind == KIND_SD ? IS : it.kind == KIND_DN ? I : H;
+  const int cpr = xlen / 8;
+  for (int q = threadIdx.x; q < NT * cpr; q += NTHREADS) {
+    const int t = q / cpr, k8 = q % cpr;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (t < it.nt) {
+      const bf16* src;
+      if (it.kind == KIND_GU)
+        src = p.xin + (size_t)(S.perm[it.row0 + t] / K) * H;
+      else if (it.kind == KIND_SGU)
+        src = p.xin + (size_t)(it.row0 + t) * H;
+      else if (it.kind == KIND_SD)
+        src = p.hs + (size_t)(it.row0 + t) * IS;
+      else
+        src = p.h + (size_t)(it.row0 + t) * I;
+      v = __ldcg(reinterpret_cast<const uint4*>(src) + k8);
+    }
+    *reinterpret_cast<uint4*>(xs + t * xlen + k8 * 8) = v;
+  }
+  __syncthreads();
+  float acc[NT][NM][8];
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+#pragma unroll
+    for (int m = 0; m < NM; ++m)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[t][m][q] = 0.f;
+  for (int q = 0; q < nblk; ++q, ++j) {
+    if (!wait_stage(S, j)) return false;
+    mac_block<NT, NM, KR>(acc, reinterpret_cast<const bf16*>(stage_ptr(S, j)), xs, xlen, (kb_start + q) * KR);
+    __syncthreads();  // every thread is done with this stage
+    refill(S, j);
+  }
+  reduce_acc<NT, NM>(acc, red, out);
+  constexpr int ncol = NM * 64;
+  if (kb_start == 0 && nblk == it.KB) {
+    item_epilogue(S, it, out);
+    __syncthreads();
+    return true;
+  }
+  float* P = partial_slot(p, it, kb_start);
+  for (int q = threadIdx.x; q < it.nt * ncol; q += NTHREADS) P[q] = out[q];
+  const uint32_t v = ticket_add(item_ticket(p, it), uint32_t(nblk) | (1u << (8 + kb_start)), uint32_t(it.KB),
+                                S.misc + 10);
+  if (v) {
+    // last arriver: add the partial slots in block order
+    const uint32_t mask = v >> 8;
+    for (int q = threadIdx.x; q < it.nt * ncol; q += NTHREADS) {
+      float s = 0.f;
+      for (int sl = 0; sl < it.KB; ++sl)
+        if (mask & (1u << sl)) s += __ldcg(partial_slot(p, it, sl) + q);
+      out[q] = s;
+    }
+    __syncthreads();
+    item_epilogue(S, it, out);
+  }
+  __syncthreads();
+  return true;
+}
+
+template <int NM, int KR>
+__device__ __forceinline__ bool run_segment_nt(Stream& S, const Item& it, int kb, int nblk, int& j) {
+  if (it.nt <= 1) return run_segment<1, NM, KR>(S, it, kb, nblk, j);
+  if (it.nt <= 2) return run_segment<2, NM, KR>(S, it, kb, nblk, j);
+  if (it.nt <= 4) return run_segment<4, NM, KR>(S, it, kb, nblk, j);
+  return run_segment<8, NM, KR>(S, it, kb, nblk, j);
+}
+
+// Issue the first NSTAGE blocks of this CTA's range of step L.
+__device__ void stream_begin(Stream& S, const BlockList& L) {
+  S.L = L;
+  const long long N = L.n_total;
+  const int g = blockIdx.x;
+  S.b0 = int(N * g / S.nctas);
+  S.nb = int(N * (g + 1) / S.nctas) - S.b0;
+  if (threadIdx.x == 0)
+    for (int s = 0; s < NSTAGE && s < S.nb; ++s)
+      issue_block(*S.p, S.meta, *S.maps, L, S.b0 + s, stage_ptr(S, s), S.bars + (S.ring + s) % NSTAGE);
+}
+
+// Consume this CTA's range of the step begun by stream_begin.  Returns false on timeout.
+__device__ bool stream_run(Stream& S) {
+  const bool combine = S.L.k_first == KIND_DN;
+  int cur_chunk = -1;
+  int j = 0;
+  while (j < S.nb) {
+    int kind, idx, kb;
+    block_kind(S.L, S.b0 + j, kind, idx, kb);
+    const Item it = decode_item(S.p->T, S.meta, kind, idx);  // shared-memory lookups only
+    if (combine && it.c != cur_chunk) {
+      if (cur_chunk >= 0) arrive_chunk(S, cur_chunk);
+      cur_chunk = it.c;
+    }
+    bool ok;
+    if (kind == KIND_RT) {
+      ok = it.nt <= 1 ? run_router_block<1>(S, it, j)
+           : it.nt <= 2 ? run_router_block<2>(S, it, j)
+           : it.nt <= 4 ? run_router_block<4>(S, it, j)
+                        : run_router_block<8>(S, it, j);
+    } else {
+      const int nblk = min(it.KB - kb, S.nb - j);
+      if (kind == KIND_GU || kind == KIND_SGU)
+        ok = run_segment_nt<2, GU_ROWS>(S, it, kb, nblk, j);
+      else
+        ok = run_segment_nt<1, DN_ROWS>(S, it, kb, nblk, j);
+    }
+    if (!ok) return false;
+  }
+  if (combine && cur_chunk >= 0) arrive_chunk(S, cur_chunk);
+  S.ring += S.nb;
+  return true;
+}
+
+// Spread a bulk L2 prefetch of `bytes` (multiple of 16) at `base` over the grid.
+__device__ __forceinline__ void prefetch_share(const void* base, size_t bytes) {
+  if (threadIdx.x != 0) return;
+  const size_t per = ((bytes / gridDim.x) + 15) & ~size_t(15);
+  const size_t a = per * blockIdx.x;
+  if (a >= bytes) return;
+  size_t n = per < bytes - a ? per : bytes - a;
+  const uint8_t* src = static_cast<const uint8_t*>(base) + a;
+  while (n) {
+    const uint32_t c = n > 65536 ? 65536u : uint32_t(n);
+    prefetch_l2_bulk(src, c);
+    src += c;
+    n -= c;
+  }
+}
+
+// ---------------------------------------------------------------- routing
+// Scores of up to 4 tokens (list `toks`, count nt) into scores[t][e], then the top-K of each
+// (warp t): key = (score bits, 255 - expert), max = highest score, lowest index on ties.
+__device__ void route_tokens(const Params& p, uint8_t* sm, const int* toks, int nt, int* s_idx, float* s_gw,
+                             bool write_global) {
+  float* scores = reinterpret_cast<float*>(sm + Smem::scores);
+  const int e = threadIdx.x;  // NTHREADS == E
+  for (int t = 0; t < nt; ++t) {
+    const int tok = toks[t];
+    float l = 0.f;
+#pragma unroll 8
+    for (int rb = 0; rb < RT_NB; ++rb) l += __ldcg(p.RP + ((size_t)rb * STREAM_MAX_T + tok) * E + e);
+    if (p.router_bias) l += p.router_bias[e];
+    scores[t * E + e] = 1.0f / (1.0f + expf(-l));
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (warp < nt) {
+    const int tok = toks[warp];
+    uint64_t key[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int ex = lane + 32 * q;
+      key[q] = (uint64_t(__float_as_uint(scores[warp * E + ex])) << 32) | uint32_t(E - 1 - ex);
+    }
+    float sel_s[K];
+    int sel_e[K];
+#pragma unroll
+    for (int jj = 0; jj < K; ++jj) {
+      uint64_t best = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) best = key[q] > best ? key[q] : best;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
+        best = o > best ? o : best;
+      }
+      const int ex = E - 1 - int(best & 0xFFFFFFFFu);
+      sel_e[jj] = ex;
+      sel_s[jj] = __uint_as_float(uint32_t(best >> 32));
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (lane + 32 * q == ex) key[q] = 0;  // scores are >= 0: an emptied slot never wins
+    }
+    if (lane == 0) {
+      float sum = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < K; ++jj) sum += sel_s[jj];
+#pragma unroll
+      for (int jj = 0; jj < K; ++jj) {
+        const float g = sel_s[jj] / sum;
+        if (s_idx) {
+          s_idx[tok * K + jj] = sel_e[jj];
+          s_gw[tok * K + jj] = g;
+        }
+        if (write_global) {
+          p.topk_idx[tok * K + jj] = sel_e[jj];
+          p.topk_w[tok * K + jj] = g;
+          if (p.out_idx) p.out_idx[tok * K + jj] = sel_e[jj];
+          if (p.out_w) p.out_w[tok * K + jj] = g;
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// Stable counting sort of the T*K (token, slot) pairs (expert ids in s_idx) by expert, in
+// this CTA's shared memory: routing tables (Meta), perm (sorted row -> pair), inv.
+// CTA 0 also publishes counts and offsets.
+__device__ Meta build_tables(const Params& p, uint8_t* sm, int* perm, int* inv) {
+  int* s_idx = reinterpret_cast<int*>(sm + Smem::s_idx);
+  int* s_cnt = reinterpret_cast<int*>(sm + Smem::s_cnt);
+  int* s_fill = reinterpret_cast<int*>(sm + Smem::s_fill);
+  int* s_wcnt = reinterpret_cast<int*>(sm + Smem::s_wcnt);
+  int* s_wsum = reinterpret_cast<int*>(sm + Smem::s_wsum);
+  int* mbase = reinterpret_cast<int*>(sm + Smem::meta);
+  int* me = mbase;
+  int* moff = mbase + (E + 1);
+  int* mcnt = mbase + 2 * (E + 1);
+  int* mtgp = mbase + 3 * (E + 1);
+  const int n = p.T * K;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  s_cnt[tid] = 0;
+  __syncthreads();
+  for (int q = tid; q < n; q += NTHREADS) {
+    const int e = s_idx[q];
+    if (e < 0 || e >= E) {
+      record_status(p.status, ST_BOUNDS);
+      continue;
+    }
+    atomicAdd(&s_cnt[e], 1);
+  }
+  __syncthreads();
+  // exclusive scans over experts (tid == expert): counts, touched flags, token groups
+  const int c = s_cnt[tid];
+  const int f = c > 0 ? 1 : 0;
+  const int ng = (c + NT_MAX - 1) / NT_MAX;
+  int ic = c, jf = f, kg = ng;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int a = __shfl_up_sync(0xffffffffu, ic, off);
+    const int b = __shfl_up_sync(0xffffffffu, jf, off);
+    const int d = __shfl_up_sync(0xffffffffu, kg, off);
+    if (lane >= off) {
+      ic += a;
+      jf += b;
+      kg += d;
+    }
+  }
+  if (lane == 31) {
+    s_wsum[warp] = ic;
+    s_wsum[NWARPS + warp] = jf;
+    s_wsum[2 * NWARPS + warp] = kg;
+  }
+  __syncthreads();
+  int bc = 0, bf = 0, bg = 0;
+  for (int w = 0; w < warp; ++w) {
+    bc += s_wsum[w];
+    bf += s_wsum[NWARPS + w];
+    bg += s_wsum[2 * NWARPS + w];
+  }
+  const int off_e = bc + ic - c;
+  const int pos = bf + jf - f;
+  const int gpre = bg + kg - ng;
+  s_fill[tid] = off_e;
+  if (f) {
+    me[pos] = tid;
+    moff[pos] = off_e;
+    mcnt[pos] = c;
+    mtgp[pos] = gpre;
+  }
+  if (tid == NTHREADS - 1) {
+    s_wsum[3 * NWARPS] = pos + f;
+    s_wsum[3 * NWARPS + 1] = gpre + ng;
+    mtgp[pos + f] = gpre + ng;
+  }
+  if (blockIdx.x == 0) {
+    p.counts[tid] = c;
+    p.offsets[tid] = off_e;
+    if (p.out_counts) p.out_counts[tid] = c;
+    if (tid == NTHREADS - 1) p.offsets[E] = off_e + c;
+  }
+  __syncthreads();
+  // stable scatter, 256 pairs at a time in (t, j) order
+  for (int base = 0; base < n; base += NTHREADS) {
+    for (int q = tid; q < NWARPS * E; q += NTHREADS) s_wcnt[q] = 0;
+    __syncthreads();
+    const int pi = base + tid;
+    int e = pi < n ? s_idx[pi] : -1;
+    if (e >= E) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int r = __popc(peers & ((1u << lane) - 1u));
+    if (e >= 0 && r == 0) s_wcnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    if (e >= 0) {
+      int before = 0;
+      for (int w = 0; w < warp; ++w) before += s_wcnt[w * E + e];
+      const int row = s_fill[e] + before + r;
+      perm[row] = pi;
+      inv[pi] = row;
+    }
+    __syncthreads();
+    {
+      int add = 0;
+      for (int w = 0; w < NWARPS; ++w) add += s_wcnt[w * E + tid];
+      s_fill[tid] += add;
+    }
+    __syncthreads();
+  }
+  Meta m;
+  m.e = me;
+  m.off = moff;
+  m.cnt = mcnt;
+  m.tgp = mtgp;
+  m.U = s_wsum[3 * NWARPS];
+  m.groups = s_wsum[3 * NWARPS + 1];
+  __syncthreads();
+  return m;
+}
+
+// ================================================================ the fused decode kernel
+// mode 0: the whole layer; mode 1: routing only (router, top-K, counts).
+__global__ void __launch_bounds__(NTHREADS, 1)
+    decode_fused(const __grid_constant__ Params p, const __grid_constant__ StreamMaps maps, int mode) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = aligned_smem(smem_raw);
+  pdl_launch_dependents();
+  Stream S;
+  S.p = &p;
+  S.maps = &maps;
+  S.meta = Meta{};
+  S.nctas = gridDim.x;
+  S.ring = 0;
+  S.sm = sm;
+  S.bars = reinterpret_cast<uint64_t*>(sm + Smem::bars);
+  S.misc = reinterpret_cast<int*>(sm + Smem::misc);
+  int* perm = reinterpret_cast<int*>(sm + Smem::perm);
+  int* inv = reinterpret_cast<int*>(sm + Smem::inv);
+  float* gw = reinterpret_cast<float*>(sm + Smem::gw);
+  int* s_idx = reinterpret_cast<int*>(sm + Smem::s_idx);
+  S.perm = perm;
+  S.inv = inv;
+  S.gw = gw;
+  const int T = p.T;
+  const int ntg = (T + NT_MAX - 1) / NT_MAX;
+  const bool full = mode == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTAGE; ++s) mbar_init(S.bars + s, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();  // inputs of this forward and the workspace are ready
+
+  // ---- step A: router partial logits and the shared gate/up
+  {
+    BlockList L;
+    L.k_first = KIND_RT;
+    L.kb_first = 1;
+    L.n_first = ntg * RT_NB;
+    L.k_second = KIND_SGU;
+    L.kb_second = GU_KB;
+    L.n_total = L.n_first + (full ? ntg * SGU_NCH * GU_KB : 0);
+    stream_begin(S, L);
+    if (full) prefetch_share(p.ws_down, (size_t)IS * H * 2);
+    if (!stream_run(S)) return;
+  }
+  if (!grid_sync(p, 1, S.misc + 12)) return;
+
+  // ---- step B: routing, then this CTA's permutation tables
+  int nbar = 1;
+  if (T <= REDUNDANT_ROUTING_MAX_T) {
+    int toks[REDUNDANT_ROUTING_MAX_T];
+    for (int t = 0; t < T; ++t) toks[t] = t;
+    route_tokens(p, sm, toks, T, s_idx, gw, blockIdx.x == 0);
+  } else {
+    int toks[4];
+    int nt = 0;
+    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+      toks[nt++] = t;
+      if (nt == 4) {
+        route_tokens(p, sm, toks, nt, nullptr, nullptr, true);
+        nt = 0;
+      }
+    }
+    if (nt) route_tokens(p, sm, toks, nt, nullptr, nullptr, true);
+    if (!grid_sync(p, ++nbar, S.misc + 12)) return;
+    for (int q = threadIdx.x; q < T * K; q += NTHREADS) {
+      s_idx[q] = __ldcg(p.topk_idx + q);
+      gw[q] = __ldcg(p.topk_w + q);
+    }
+    __syncthreads();
+  }
+  S.meta = build_tables(p, sm, perm, inv);
+  if (!full) {
+    grid_done(p, S.misc + 13);
+    return;
+  }
+
+  // ---- step C: routed gate/up and the shared down projection
+  {
+    BlockList L;
+    L.k_first = KIND_GU;
+    L.kb_first = GU_KB;
+    L.n_first = S.meta.groups * GU_NCH * GU_KB;
+    L.k_second = KIND_SD;
+    L.kb_second = SD_KB;
+    L.n_total = L.n_first + ntg * OUT_NCH * SD_KB;
+    stream_begin(S, L);
+    // the touched experts' down matrices are read in step D: prefetch them when they fit
+    if ((unsigned long long)S.meta.U * I * H * 2 <= p.prefetch_bytes_max && threadIdx.x == 0) {
+      const size_t per_e = (size_t)I * H * 2;
+      const size_t total = per_e * S.meta.U;
+      const size_t share = ((total / gridDim.x) + 15) & ~size_t(15);
+      size_t a = share * blockIdx.x;
+      const size_t b = a + share < total ? a + share : total;
+      while (a < b) {
+        const int u = int(a / per_e);
+        const size_t in_e = a % per_e;
+        size_t n = per_e - in_e;
+        if (n > b - a) n = b - a;
+        if (n > 65536) n = 65536;
+        prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(p.w_down + (size_t)S.meta.e[u] * I * H) + in_e,
+                         uint32_t(n));
+        a += n;
+      }
+    }
+    if (!stream_run(S)) return;
+  }
+  if (!grid_sync(p, ++nbar, S.misc + 12)) return;
+
+  // ---- step D: routed down projection and the combine
+  {
+    BlockList L;
+    L.k_first = L.k_second = KIND_DN;
+    L.kb_first = L.kb_second = DN_KB;
+    L.n_first = L.n_total = S.meta.groups * OUT_NCH * DN_KB;
+    stream_begin(S, L);
+    if (!stream_run(S)) return;
+  }
+  grid_done(p, S.misc + 13);
+}
+
+// ================================================================ RMSNorm (pre-norm layers)
+// xn[t] = bf16(x[t] / sqrt(mean(x[t]^2) + eps)), unit weight; one CTA per token.
+__global__ void __launch_bounds__(NTHREADS) rmsnorm_kernel(const __grid_constant__ Params p) {
+  __shared__ float s_w[NWARPS];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int t = blockIdx.x;
+  const bf16* xr = p.x + (size_t)t * H;
+  float f[8];
+  const uint4 v = *reinterpret_cast<const uint4*>(xr + threadIdx.x * 8);
+  bf16x8_to_f32(v, f);
+  float ss = 0.f;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) ss = fmaf(f[q], f[q], ss);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < NWARPS; ++w) tot += s_w[w];
+  const float d = sqrtf(tot / float(H) + p.rms_eps);
+  uint32_t packed[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * q] / d, f[2 * q + 1] / d);
+    packed[q] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  *reinterpret_cast<uint4*>(p.xn + (size_t)t * H + threadIdx.x * 8) =
+      make_uint4(packed[0], packed[1], packed[2], packed[3]);
+}
+
+}  // namespace flint

@@ -9,7 +9,7 @@
 
 #include "../../include/flint_moe.h"
 #include "common.cuh"
-#include "stream_kernels.cuh"
+#include "decode_fused.cuh"
 
 using namespace flint;
 
@@ -20,9 +20,9 @@ constexpr int MAX_EVENTS = 16;
 
 struct Layout {
   // tickets first: [status, tickets) and [tickets, scalars) are cleared together after errors
-  size_t status, tk_router, tk_gu, tk_sgu, tk_sd, tk_dn, tk_comb;
+  size_t status, bar_count, bar_done, tk_router, tk_gu, tk_sgu, tk_sd, tk_dn, tk_comb;
   size_t n_touched, n_groups, touched, tgp, counts, offsets, perm, inv, topk_idx, topk_w;
-  size_t xn, xstage, ystage, h, hs, S, Y, P_gu, P_sgu, P_sd, P_dn;
+  size_t xn, xstage, ystage, h, hs, S, Y, P_gu, P_sgu, P_sd, P_dn, RP;
   size_t total;
 };
 
@@ -41,6 +41,8 @@ Layout make_layout(int max_tokens) {
   const size_t G = (size_t)max_groups(Ts);               // routed token groups
   const size_t Gs = (size_t)(Ts + NT_MAX - 1) / NT_MAX;  // shared token groups
   L.status = take(256);
+  L.bar_count = take(sizeof(uint32_t));
+  L.bar_done = take(sizeof(uint32_t));
   L.tk_router = take(sizeof(uint32_t));
   L.tk_gu = take(sizeof(uint32_t) * G * GU_NCH);
   L.tk_sgu = take(sizeof(uint32_t) * Gs * SGU_NCH);
@@ -68,6 +70,7 @@ Layout make_layout(int max_tokens) {
   L.P_sgu = take(sizeof(float) * Gs * SGU_NCH * GU_KB * NT_MAX * 128);
   L.P_sd = take(sizeof(float) * Gs * OUT_NCH * SD_KB * NT_MAX * 64);
   L.P_dn = take(sizeof(float) * G * OUT_NCH * DN_KB * NT_MAX * 64);
+  L.RP = take(sizeof(float) * RT_NB * STREAM_MAX_T * E);
   L.total = align_up(off, 256);
   return L;
 }
@@ -153,6 +156,8 @@ Params make_params(flint_moe_t h, const void* x, int T, void* y, int32_t* out_id
   p.ws_up = static_cast<const bf16*>(h->w.ws_up);
   p.ws_down = static_cast<const bf16*>(h->w.ws_down);
   p.status = reinterpret_cast<uint32_t*>(ws + L.status);
+  p.bar_count = reinterpret_cast<uint32_t*>(ws + L.bar_count);
+  p.bar_done = reinterpret_cast<uint32_t*>(ws + L.bar_done);
   p.tk_router = reinterpret_cast<uint32_t*>(ws + L.tk_router);
   p.tk_gu = reinterpret_cast<uint32_t*>(ws + L.tk_gu);
   p.tk_sgu = reinterpret_cast<uint32_t*>(ws + L.tk_sgu);
@@ -177,6 +182,7 @@ Params make_params(flint_moe_t h, const void* x, int T, void* y, int32_t* out_id
   p.P_sgu = reinterpret_cast<float*>(ws + L.P_sgu);
   p.P_sd = reinterpret_cast<float*>(ws + L.P_sd);
   p.P_dn = reinterpret_cast<float*>(ws + L.P_dn);
+  p.RP = reinterpret_cast<float*>(ws + L.RP);
   p.out_idx = out_idx;
   p.out_w = out_w;
   p.out_counts = out_counts;
@@ -184,9 +190,11 @@ Params make_params(flint_moe_t h, const void* x, int T, void* y, int32_t* out_id
   return p;
 }
 
+// Launch with programmatic stream serialisation, or as a cooperative grid (all CTAs
+// resident at once, required by kernels with grid-wide barriers).
 template <class... KArgs, class... Args>
 cudaError_t launch(flint_moe_t h, const char* name, void (*kern)(KArgs...), unsigned grid, int smem,
-                   cudaStream_t st, Args&&... args) {
+                   cudaStream_t st, bool cooperative, Args&&... args) {
   if (grid == 0) return cudaSuccess;
   const bool rec = h->timing && h->n_ev < MAX_EVENTS;
   if (rec) {
@@ -199,8 +207,13 @@ cudaError_t launch(flint_moe_t h, const char* name, void (*kern)(KArgs...), unsi
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  if (cooperative) {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
@@ -211,24 +224,15 @@ cudaError_t launch(flint_moe_t h, const char* name, void (*kern)(KArgs...), unsi
   return e;
 }
 
-// The layer on T <= STREAM_MAX_T tokens (streaming path).
-flint_moe_status run_stream(flint_moe_t h, const Params& p, cudaStream_t st, bool full) {
-  const int T = p.T;
+// The layer on T <= STREAM_MAX_T tokens: optional RMSNorm kernel, then the persistent
+// cooperative decode kernel (one CTA per SM).
+flint_moe_status run_decode(flint_moe_t h, const Params& p, cudaStream_t st, bool full) {
   cudaError_t e = cudaSuccess;
-  if (h->cfg.flags & FLINT_MOE_FLAG_PRE_RMSNORM) e = launch(h, "rmsnorm", rmsnorm_kernel, T, 0, st, p);
+  if (h->cfg.flags & FLINT_MOE_FLAG_PRE_RMSNORM) e = launch(h, "rmsnorm", rmsnorm_kernel, p.T, 0, st, false, p);
   if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
-  const int n_router = ((T + RT_TOK - 1) / RT_TOK) * RT_CL;
-  // persistent streaming CTAs of k1: one per SM, rounded up to whole clusters
-  const int n_stream = full ? (h->n_sm + RT_CL - 1) / RT_CL * RT_CL : 0;
-  e = launch(h, "stream_k1_router_sharedgu", stream_k1, n_router + n_stream, K1_SMEM, st, p, h->smaps, n_router,
-             n_stream);
-  if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
-  if (!full) return FLINT_MOE_OK;
-  e = launch(h, "stream_k2_gateup_shareddown", stream_k2, h->n_sm, K23_SMEM, st, p, h->smaps);
-  if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
-  e = launch(h, "stream_k3_down_combine", stream_k3, h->n_sm, K23_SMEM, st, p, h->smaps);
-  if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
-  return FLINT_MOE_OK;
+  e = launch(h, full ? "decode_fused" : "decode_fused_route", decode_fused, h->n_sm, FUSED_SMEM, st, true, p,
+             h->smaps, full ? 0 : 1);
+  return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ERR_CUDA;
 }
 
 flint_moe_status check_call(flint_moe_t h, const void* x, int T) {
@@ -314,9 +318,10 @@ flint_moe_status flint_moe_create(const flint_moe_config* cfg, const flint_moe_w
     delete h;
     return FLINT_MOE_ERR_CUDA;
   }
-  cudaError_t e = cudaFuncSetAttribute(stream_k1, cudaFuncAttributeMaxDynamicSharedMemorySize, K1_SMEM);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(stream_k2, cudaFuncAttributeMaxDynamicSharedMemorySize, K23_SMEM);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(stream_k3, cudaFuncAttributeMaxDynamicSharedMemorySize, K23_SMEM);
+  cudaError_t e = cudaFuncSetAttribute(decode_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, FUSED_SMEM);
+  int per_sm = 0;
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused, NTHREADS, FUSED_SMEM);
+  if (e == cudaSuccess && per_sm < 1) e = cudaErrorCooperativeLaunchTooLarge;
   if (e == cudaSuccess) e = cudaMemset(h->ws, 0, L.xn);  // status, tickets and routing scratch
   for (int i = 0; i < 2 * MAX_EVENTS && e == cudaSuccess; ++i) e = cudaEventCreate(&h->ev[i]);
   if (e != cudaSuccess) {
@@ -334,7 +339,7 @@ flint_moe_status flint_moe_route(flint_moe_t h, const void* x, int T, int32_t* t
   if (!topk_idx || !topk_w) return FLINT_MOE_ERR_INVALID_ARG;
   h->n_ev = 0;
   Params p = make_params(h, x, T, nullptr, topk_idx, topk_w, counts);
-  return run_stream(h, p, reinterpret_cast<cudaStream_t>(stream), false);
+  return run_decode(h, p, reinterpret_cast<cudaStream_t>(stream), false);
 }
 
 flint_moe_status flint_moe_forward(flint_moe_t h, const void* x, int T, void* y, int32_t* topk_idx,
@@ -344,7 +349,7 @@ flint_moe_status flint_moe_forward(flint_moe_t h, const void* x, int T, void* y,
   if (!y || !aligned16(y)) return FLINT_MOE_ERR_INVALID_ARG;
   h->n_ev = 0;
   Params p = make_params(h, x, T, y, topk_idx, topk_w, nullptr);
-  return run_stream(h, p, reinterpret_cast<cudaStream_t>(stream), true);
+  return run_decode(h, p, reinterpret_cast<cudaStream_t>(stream), true);
 }
 
 flint_moe_status flint_moe_forward_host(flint_moe_t h, const void* x_host, int T, void* y_host,
