@@ -356,8 +356,32 @@ def run_profile_case(args):
         y = layer.forward(x)
     torch.cuda.synchronize()
     rc = layer.poll_device_status()
+    trace = None
+    if args.trace:
+        # phase stamps of the decode kernel: per slot, min / median / max over CTAs, in us from
+        # the earliest CTA start; several repetitions, the median of each statistic reported
+        names = {0: "start", 1: "inputs_ready", 11: "A_first_block", 2: "A_done", 3: "barrier1", 4: "routed",
+                 5: "tables", 6: "C_issued", 12: "C_first_block", 7: "C_done", 8: "barrier2", 13: "D_first_block",
+                 9: "D_done", 10: "end"}
+        layer.enable_phase_trace(True)
+        reps = []
+        for _ in range(5):
+            flush_buf.fill_(1)
+            layer.forward(x)
+            rows = layer.read_trace()
+            t0 = min(r[0] for r in rows if r[0])
+            stat = {}
+            for s, nm in names.items():
+                v = sorted((r[s] - t0) / 1e3 for r in rows if r[s])
+                if v:
+                    stat[nm] = (v[0], v[len(v) // 2], v[-1])
+            reps.append(stat)
+        layer.enable_phase_trace(False)
+        trace = {nm: [round(statistics.median(r[nm][i] for r in reps if nm in r), 2) for i in range(3)]
+                 for nm in names.values() if all(nm in r for r in reps)}
     layer.close()
-    print(json.dumps(dict(profile_case=T, steps=args.steps, device_status=rc, y_abs_mean=float(y.float().abs().mean()))))
+    print(json.dumps(dict(profile_case=T, steps=args.steps, device_status=rc, y_abs_mean=float(y.float().abs().mean()),
+                          phase_trace_us_min_med_max=trace)))
     if rc != 0:
         raise SystemExit(1)
 
@@ -371,6 +395,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--profile", type=int, default=0, help="profiler case: forwards at this T only")
+    ap.add_argument("--trace", action="store_true", help="with --profile: print the decode kernel's phase trace")
     args = ap.parse_args()
     if args.profile:
         run_profile_case(args)

@@ -120,13 +120,17 @@ flint_moe_status flint_moe_forward_host(flint_moe_t h, const void* x_host, int T
  * (FLINT_MOE_OK, FLINT_MOE_ERR_DEVICE_TIMEOUT or FLINT_MOE_ERR_DEVICE_BOUNDS). */
 flint_moe_status flint_moe_poll_device_status(flint_moe_t h, flint_stream_t stream);
 
-/* Kernel timing for profiling.  With enable != 0, later forward calls record a CUDA event
- * pair around every kernel they launch (this serialises kernels that would otherwise
- * overlap).  flint_moe_kernel_times synchronises on the last forward's events and writes up
- * to `cap` entries: names[i] (static strings) and ms[i]; *n receives the count. */
+/* Profiling.  enable = 1: later forward calls record a CUDA event pair around every kernel
+ * they launch (this serialises kernels that would otherwise overlap); flint_moe_kernel_times
+ * synchronises on the last call's events and writes up to `cap` entries: names[i] (static
+ * strings) and ms[i]; *n receives the count.  enable = 2: the decode-size kernel stamps the
+ * GPU global timer (ns) at its phase boundaries, 16 slots per CTA, into the workspace;
+ * flint_moe_read_trace synchronises the device and copies up to `cap` stamps (CTA-major) to
+ * host memory `out`.  enable = 0 turns both off. */
 flint_moe_status flint_moe_enable_kernel_timing(flint_moe_t h, int enable);
 flint_moe_status flint_moe_kernel_times(flint_moe_t h, const char** names, float* ms, int cap,
                                         int* n);
+flint_moe_status flint_moe_read_trace(flint_moe_t h, unsigned long long* out, int cap, int* n);
 
 /* Releases the handle's host state.  Does not touch the workspace or the weights. */
 flint_moe_status flint_moe_destroy(flint_moe_t h);

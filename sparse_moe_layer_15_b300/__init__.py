@@ -22,7 +22,8 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "
 # Every entry point declared in include/flint_moe.h.
 EXPORTS = ("flint_moe_status_string", "flint_moe_workspace_bytes", "flint_moe_create", "flint_moe_route",
            "flint_moe_forward", "flint_moe_forward_host", "flint_moe_poll_device_status",
-           "flint_moe_enable_kernel_timing", "flint_moe_kernel_times", "flint_moe_destroy")
+           "flint_moe_enable_kernel_timing", "flint_moe_kernel_times", "flint_moe_read_trace",
+           "flint_moe_destroy")
 
 
 class FlintMoEError(RuntimeError):
@@ -72,6 +73,7 @@ def load_library():
     L.flint_moe_enable_kernel_timing.argtypes = [P, I32]
     L.flint_moe_kernel_times.argtypes = [P, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float), I32,
                                          ctypes.POINTER(I32)]
+    L.flint_moe_read_trace.argtypes = [P, ctypes.POINTER(ctypes.c_ulonglong), I32, ctypes.POINTER(I32)]
     L.flint_moe_destroy.argtypes = [P]
     for name in EXPORTS:
         if name != "flint_moe_status_string":
@@ -173,6 +175,17 @@ class FlintMoE:
 
     def enable_kernel_timing(self, on=True):
         _check(self._L.flint_moe_enable_kernel_timing(self._h, 1 if on else 0), "flint_moe_enable_kernel_timing")
+
+    def enable_phase_trace(self, on=True):
+        _check(self._L.flint_moe_enable_kernel_timing(self._h, 2 if on else 0), "flint_moe_enable_kernel_timing")
+
+    def read_trace(self, slots=16):
+        """Phase stamps (ns) of the last decode-size call: list of per-CTA lists."""
+        cap = 1024 * slots
+        buf = (ctypes.c_ulonglong * cap)()
+        n = ctypes.c_int(0)
+        _check(self._L.flint_moe_read_trace(self._h, buf, cap, ctypes.byref(n)), "flint_moe_read_trace")
+        return [list(buf[i:i + slots]) for i in range(0, n.value, slots)]
 
     def kernel_times(self):
         cap = 16

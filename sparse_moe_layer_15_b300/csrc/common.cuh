@@ -78,7 +78,19 @@ struct Params {
   float* out_w;
   int32_t* out_counts;
   unsigned long long prefetch_bytes_max;  // L2 prefetch budget for the touched down matrices
+  unsigned long long* trace;  // [gridDim.x][TRACE_SLOTS] %globaltimer stamps, or null
 };
+
+constexpr int TRACE_SLOTS = 16;
+
+// Phase trace: thread 0 of each CTA stamps slot `s` with the global timer (ns).
+__device__ __forceinline__ void trace_point(const Params& p, int s) {
+  if (p.trace && threadIdx.x == 0) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    p.trace[blockIdx.x * TRACE_SLOTS + s] = t;
+  }
+}
 
 // ------------------------------------------------------------------ small PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

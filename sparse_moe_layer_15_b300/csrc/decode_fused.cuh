@@ -300,6 +300,7 @@ struct Stream {
   int nctas;
   int b0, nb;  // this CTA's block range
   int ring;    // blocks consumed by this CTA before this step (stage ring position)
+  int first_slot;  // trace slot stamped when the step's first block has arrived
   uint8_t* sm;
   uint64_t* bars;
   int* misc;  // [8..15]: flags
@@ -323,6 +324,7 @@ __device__ __forceinline__ bool wait_stage(Stream& S, int j) {
   if (!*ok) return false;
   while (!mbar_try_wait(S.bars + st, par)) {
   }
+  if (j == 0) trace_point(*S.p, S.first_slot);
   return true;
 }
 
@@ -847,7 +849,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     fence_mbar_init();
   }
   __syncthreads();
+  trace_point(p, 0);
   pdl_wait();  // inputs of this forward and the workspace are ready
+  trace_point(p, 1);
 
   // ---- step A: router partial logits and the shared gate/up
   {
@@ -858,11 +862,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     L.k_second = KIND_SGU;
     L.kb_second = GU_KB;
     L.n_total = L.n_first + (full ? ntg * SGU_NCH * GU_KB : 0);
+    S.first_slot = 11;
     stream_begin(S, L);
     if (full) prefetch_share(p.ws_down, (size_t)IS * H * 2);
     if (!stream_run(S)) return;
   }
+  trace_point(p, 2);
   if (!grid_sync(p, 1, S.misc + 12)) return;
+  trace_point(p, 3);
 
   // ---- step B: routing, then this CTA's permutation tables
   int nbar = 1;
@@ -888,7 +895,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     __syncthreads();
   }
+  trace_point(p, 4);
   S.meta = build_tables(p, sm, perm, inv);
+  trace_point(p, 5);
   if (!full) {
     grid_done(p, S.misc + 13);
     return;
@@ -903,6 +912,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     L.k_second = KIND_SD;
     L.kb_second = SD_KB;
     L.n_total = L.n_first + ntg * OUT_NCH * SD_KB;
+    S.first_slot = 12;
     stream_begin(S, L);
     // the touched experts' down matrices are read in step D: prefetch them when they fit
     if ((unsigned long long)S.meta.U * I * H * 2 <= p.prefetch_bytes_max && threadIdx.x == 0) {
@@ -922,9 +932,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         a += n;
       }
     }
+    trace_point(p, 6);
     if (!stream_run(S)) return;
   }
+  trace_point(p, 7);
   if (!grid_sync(p, ++nbar, S.misc + 12)) return;
+  trace_point(p, 8);
 
   // ---- step D: routed down projection and the combine
   {
@@ -932,10 +945,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     L.k_first = L.k_second = KIND_DN;
     L.kb_first = L.kb_second = DN_KB;
     L.n_first = L.n_total = S.meta.groups * OUT_NCH * DN_KB;
+    S.first_slot = 13;
     stream_begin(S, L);
     if (!stream_run(S)) return;
   }
+  trace_point(p, 9);
   grid_done(p, S.misc + 13);
+  trace_point(p, 10);
 }
 
 // ================================================================ RMSNorm (pre-norm layers)

@@ -17,12 +17,13 @@ namespace {
 
 constexpr int MAX_TOKENS_LIMIT = 65536;
 constexpr int MAX_EVENTS = 16;
+constexpr int MAX_TRACE_CTAS = 1024;
 
 struct Layout {
   // tickets first: [status, tickets) and [tickets, scalars) are cleared together after errors
   size_t status, bar_count, bar_done, tk_router, tk_gu, tk_sgu, tk_sd, tk_dn, tk_comb;
   size_t n_touched, n_groups, touched, tgp, counts, offsets, perm, inv, topk_idx, topk_w;
-  size_t xn, xstage, ystage, h, hs, S, Y, P_gu, P_sgu, P_sd, P_dn, RP;
+  size_t xn, xstage, ystage, h, hs, S, Y, P_gu, P_sgu, P_sd, P_dn, RP, trace;
   size_t total;
 };
 
@@ -71,6 +72,7 @@ Layout make_layout(int max_tokens) {
   L.P_sd = take(sizeof(float) * Gs * OUT_NCH * SD_KB * NT_MAX * 64);
   L.P_dn = take(sizeof(float) * G * OUT_NCH * DN_KB * NT_MAX * 64);
   L.RP = take(sizeof(float) * RT_NB * STREAM_MAX_T * E);
+  L.trace = take(sizeof(unsigned long long) * MAX_TRACE_CTAS * TRACE_SLOTS);
   L.total = align_up(off, 256);
   return L;
 }
@@ -118,6 +120,7 @@ struct flint_moe_s {
   StreamMaps smaps;
   unsigned long long prefetch_max;
   bool timing;
+  bool trace;
   cudaEvent_t ev[2 * MAX_EVENTS];
   const char* ev_name[MAX_EVENTS];
   int n_ev;
@@ -187,6 +190,7 @@ Params make_params(flint_moe_t h, const void* x, int T, void* y, int32_t* out_id
   p.out_w = out_w;
   p.out_counts = out_counts;
   p.prefetch_bytes_max = h->prefetch_max;
+  p.trace = h->trace ? reinterpret_cast<unsigned long long*>(ws + L.trace) : nullptr;
   return p;
 }
 
@@ -302,6 +306,7 @@ flint_moe_status flint_moe_create(const flint_moe_config* cfg, const flint_moe_w
   h->prefetch_max = 40ull << 20;
   if (const char* env = std::getenv("FLINT_MOE_PREFETCH_MB")) h->prefetch_max = std::strtoull(env, nullptr, 10) << 20;
   h->timing = false;
+  h->trace = false;
   h->n_ev = 0;
   if (cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || h->n_sm < 1) {
     delete h;
@@ -382,8 +387,21 @@ flint_moe_status flint_moe_poll_device_status(flint_moe_t h, flint_stream_t stre
 
 flint_moe_status flint_moe_enable_kernel_timing(flint_moe_t h, int enable) {
   if (!h) return FLINT_MOE_ERR_INVALID_ARG;
-  h->timing = enable != 0;
+  h->timing = enable == 1;
+  h->trace = enable == 2;
   h->n_ev = 0;
+  return FLINT_MOE_OK;
+}
+
+flint_moe_status flint_moe_read_trace(flint_moe_t h, unsigned long long* out, int cap, int* n) {
+  if (!h || !n || cap < 0 || (cap > 0 && !out)) return FLINT_MOE_ERR_INVALID_ARG;
+  const int total = (h->n_sm < MAX_TRACE_CTAS ? h->n_sm : MAX_TRACE_CTAS) * TRACE_SLOTS;
+  const int m = total < cap ? total : cap;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  if (m > 0 && cudaMemcpy(out, h->ws + h->L.trace, sizeof(unsigned long long) * m, cudaMemcpyDeviceToHost) !=
+                   cudaSuccess)
+    return FLINT_MOE_ERR_CUDA;
+  *n = m;
   return FLINT_MOE_OK;
 }
 
