@@ -7,56 +7,61 @@
 // steps separated by grid-wide barriers (bounded spins on a global counter; the cooperative
 // launch guarantees that all CTAs are resident):
 //
-//   A  router partial logits (32 KB blocks of W_r rows, all 256 experts) and the shared
+//   A  router partial logits (blocks of 64 W_r rows, all 256 experts) and the shared
 //      expert's gate/up with fused SiLU-mul; the shared down matrix is prefetched into L2;
 //   -- barrier --
 //   B  routing: logits summed over the 32 row blocks in order, + bias, sigmoid, top-6 with
 //      the lower index first on ties, renormalised gates; for T <= 4 every CTA routes every
 //      token itself (no barrier), otherwise each CTA routes its own tokens and a barrier
 //      publishes them; then every CTA builds the expert permutation (stable counting sort)
-//      in its own shared memory and starts streaming step C;
+//      in its own shared memory;
 //   C  routed gate/up (touched experts only) with fused SiLU-mul, and the shared down
 //      projection; the touched experts' down matrices are prefetched into L2 when they fit;
 //   -- barrier --
 //   D  routed down projection scaled by the gates; the last CTA to finish each 64-column
 //      chunk of the output performs the combine y = S + sum_j Y[inv(t, j)] in slot order.
 //
-// Within a step, the weight traffic is a list of equal 32 KB blocks (64 output columns x 128
-// or 256 rows of one or two matrices, or 64 rows of the router); every CTA takes an equal
-// contiguous range and streams it through a 4-stage TMA pipeline into shared memory, where
-// CUDA cores multiply it against the few token rows.  Blocks of the same output columns
-// accumulate in registers; a range boundary inside an item leaves a partial sum that the
-// last CTA to finish the item adds in block order (an integer ticket that records which
-// partial slots exist): deterministic, no floating-point atomics.
+// Within a step the weight traffic is a list of equal 32 KB blocks (64 output columns x 128
+// or 256 rows of one or two matrices, or 64 router rows x 256 experts); every CTA takes an
+// equal contiguous range.  A producer warp streams the range through a 4-stage TMA ring
+// (128-byte swizzled tiles); eight consumer warps multiply each tile against the current
+// token group (up to 8 rows) with warp-level bf16 MMAs (m16n8k16, fp32 accumulate), each warp
+// owning 16 output columns, so a tile needs no cross-warp reduction.  Tiles of the same
+// output columns accumulate in registers; a range boundary inside an item leaves a partial
+// sum that the last CTA to finish the item adds in block order (an integer ticket that
+// records which partial slots exist): deterministic, no floating-point atomics.
 #pragma once
 
 #include "common.cuh"
 
 namespace flint {
 
-constexpr int NTHREADS = 256;
-constexpr int NWARPS = NTHREADS / 32;
+constexpr int NCONS = 256;               // consumer threads (8 warps)
+constexpr int NWARPS = NCONS / 32;
+constexpr int NTHREADS = NCONS + 32;     // + one producer warp
 constexpr int STREAM_MAX_T = 256;
-constexpr int NT_MAX = 8;  // token rows per register block (a "token group")
+constexpr int NT_MAX = 8;                // token rows per group (the MMA's N)
 constexpr int NSTAGE = 4;
 constexpr int BLK_BYTES = 32768;
-constexpr int GU_ROWS = 128;         // gate/up block: 128 rows x 64 columns of gate and of up
-constexpr int DN_ROWS = 256;         // down block: 256 rows x 64 columns
-constexpr int RT_ROWS = 64;          // router block: 64 rows x 256 experts
-constexpr int GU_KB = H / GU_ROWS;   // 16 blocks per gate/up item
-constexpr int SD_KB = IS / DN_ROWS;  // 4 blocks per shared-down item
-constexpr int DN_KB = I / DN_ROWS;   // 2 blocks per routed-down item
-constexpr int RT_NB = H / RT_ROWS;   // 32 router blocks per token group
-constexpr int GU_NCH = I / 64;       // 8 column chunks of a routed expert's gate/up
-constexpr int SGU_NCH = IS / 64;     // 16 column chunks of the shared gate/up
-constexpr int OUT_NCH = H / 64;      // 32 column chunks of a down projection
+constexpr int GU_ROWS = 128;             // gate/up block: 128 rows x 64 columns of gate and of up
+constexpr int DN_ROWS = 256;             // down block: 256 rows x 64 columns
+constexpr int RT_ROWS = 64;              // router block: 64 rows x 256 experts
+constexpr int GU_KB = H / GU_ROWS;       // 16 blocks per gate/up item
+constexpr int SD_KB = IS / DN_ROWS;      // 4 blocks per shared-down item
+constexpr int DN_KB = I / DN_ROWS;       // 2 blocks per routed-down item
+constexpr int RT_NB = H / RT_ROWS;       // 32 router blocks per token group
+constexpr int GU_NCH = I / 64;           // 8 column chunks of a routed expert's gate/up
+constexpr int SGU_NCH = IS / 64;         // 16 column chunks of the shared gate/up
+constexpr int OUT_NCH = H / 64;          // 32 column chunks of a down projection
 constexpr int REDUNDANT_ROUTING_MAX_T = 4;
 constexpr int MAX_PAIRS = STREAM_MAX_T * K;
+constexpr int XPAD = 8;                  // bf16 padding of a staged input row (bank spread)
 
 enum Kind : int { KIND_RT = 0, KIND_GU = 1, KIND_SGU = 2, KIND_SD = 3, KIND_DN = 4 };
 
 struct StreamMaps {
-  CUtensorMap wg;   // w_gate as [E*H][I], box 64 x 128
+  CUtensorMap wr;   // w_router [H][E], box 64 x 64, 128B swizzle
+  CUtensorMap wg;   // w_gate as [E*H][I], box 64 x 128, 128B swizzle
   CUtensorMap wu;   // w_up   as [E*H][I], box 64 x 128
   CUtensorMap wd;   // w_down as [E*I][H], box 64 x 256
   CUtensorMap wsg;  // [H][IS], box 64 x 128
@@ -74,26 +79,27 @@ __host__ __device__ constexpr int max_groups(int T) {
 
 // ---------------------------------------------------------------- shared memory
 struct Smem {
-  static constexpr int stages = 0;                             // NSTAGE x 32 KB
-  static constexpr int xs = stages + NSTAGE * BLK_BYTES;       // [NT_MAX][<=2048] bf16
-  static constexpr int red = xs + NT_MAX * H * 2;              // [8][NT_MAX][128] f32 (+ reuse)
-  static constexpr int out = red + NWARPS * NT_MAX * 128 * 4;  // [NT_MAX][128] f32
-  static constexpr int bars = out + NT_MAX * 128 * 4;          // NSTAGE mbarriers
-  static constexpr int misc = bars + 8 * NSTAGE;               // flags
-  static constexpr int meta = misc + 128;                      // [4][E+1] int
-  static constexpr int perm = meta + 4 * (E + 1) * 4;          // [MAX_PAIRS] int
-  static constexpr int inv = perm + MAX_PAIRS * 4;             // [MAX_PAIRS] int
-  static constexpr int gw = inv + MAX_PAIRS * 4;               // [MAX_PAIRS] f32
+  static constexpr int stages = 0;                                 // NSTAGE x 32 KB
+  static constexpr int xs = stages + NSTAGE * BLK_BYTES;           // [NT_MAX][H + XPAD] bf16
+  static constexpr int xs_bytes = NT_MAX * (H + XPAD) * 2;
+  static constexpr int out = xs + xs_bytes;                        // [2][NT_MAX][128] f32
+  static constexpr int full = out + 2 * NT_MAX * 128 * 4;          // NSTAGE mbarriers
+  static constexpr int empty = full + 8 * NSTAGE;                  // NSTAGE mbarriers
+  static constexpr int misc = empty + 8 * NSTAGE;                  // flags
+  static constexpr int meta = misc + 128;                          // [4][E+1] int
+  static constexpr int perm = meta + 4 * (E + 1) * 4;              // [MAX_PAIRS] int
+  static constexpr int inv = perm + MAX_PAIRS * 4;                 // [MAX_PAIRS] int
+  static constexpr int gw = inv + MAX_PAIRS * 4;                   // [MAX_PAIRS] f32
   static constexpr int bytes = gw + MAX_PAIRS * 4;
-  // reuse of `red` outside the streaming steps
-  static constexpr int scores = red;                  // [4][E] f32 (routing)
-  static constexpr int s_cnt = red;                   // [E] int (permutation)
-  static constexpr int s_fill = s_cnt + E * 4;        // [E] int
-  static constexpr int s_wcnt = s_fill + E * 4;       // [8][E] int
-  static constexpr int s_wsum = s_wcnt + NWARPS * E * 4;   // [3][8] int
-  static constexpr int s_idx = s_wsum + 128;          // [MAX_PAIRS] int
+  // reuse of `xs` during routing (between the streaming steps)
+  static constexpr int scores = xs;                    // [4][E] f32
+  static constexpr int s_cnt = xs + 4 * E * 4;         // [E] int
+  static constexpr int s_fill = s_cnt + E * 4;         // [E] int
+  static constexpr int s_wcnt = s_fill + E * 4;        // [8][E] int
+  static constexpr int s_wsum = s_wcnt + NWARPS * E * 4;  // [4][8] int
+  static constexpr int s_idx = s_wsum + 128;           // [MAX_PAIRS] int
 };
-static_assert(Smem::s_idx + MAX_PAIRS * 4 <= Smem::out, "routing scratch must fit in the reduction buffer");
+static_assert(Smem::s_idx + MAX_PAIRS * 4 <= Smem::xs + Smem::xs_bytes, "routing scratch must fit in xs");
 constexpr int FUSED_SMEM = Smem::bytes + 1024;
 static_assert(FUSED_SMEM <= 227 * 1024, "shared memory budget");
 
@@ -109,35 +115,96 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   return v;
 }
 
+// Barrier among the 256 consumer threads only (the producer warp keeps streaming).
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// ---------------------------------------------------------------- warp MMA helpers
+// Byte offset of (row r, bf16 column m) in a tile of 128-byte rows written by TMA with the
+// 128-byte swizzle (16-byte chunk index XOR row mod 8).
+__device__ __forceinline__ uint32_t swz(int r, int m) {
+  return uint32_t(r * 128 + ((((m >> 3) ^ r) & 7) << 4) + (m & 7) * 2);
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&a)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&b)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// d += A * B over `ksteps` (even) k-steps of 16 rows starting at tile row `r0`, where A = the
+// 16 columns [m0, m0+16) of a swizzled weight tile (rows = k) and B = the staged input rows
+// xs[n][k0 + ...] (8 tokens, row stride xstride bf16).  Two k-steps per B load.
+__device__ __forceinline__ void mma_tile(float (&d)[4], uint32_t tile, int m0, int r0, int ksteps, uint32_t xs,
+                                         int xstride, int k0) {
+  const int lane = threadIdx.x & 31;
+  const int q = lane >> 3, i = lane & 7;
+  // A: matrix q -> (m + 8 * (q & 1), k + 8 * (q >> 1)), lane row i
+  const int am = m0 + ((q & 1) << 3);
+  const int ak = (q >> 1) << 3;
+  // B: matrix q -> k offset 8q, lane row = token i
+  const uint32_t bbase = xs + uint32_t((i * xstride + k0 + q * 8) * 2);
+#pragma unroll 2
+  for (int s = 0; s < ksteps; s += 2) {
+    uint32_t b[4];
+    ldsm_x4(bbase + uint32_t(s * 16 * 2), b);
+    uint32_t a[4];
+    ldsm_x4_trans(tile + swz(r0 + s * 16 + ak + i, am), a);
+    mma_bf16(d, a, b[0], b[1]);
+    ldsm_x4_trans(tile + swz(r0 + (s + 1) * 16 + ak + i, am), a);
+    mma_bf16(d, a, b[2], b[3]);
+  }
+}
+
 // ---------------------------------------------------------------- tickets and barriers
-// Arrive after this CTA's global writes with `add` (nblk in the low 8 bits plus one bit per
-// partial slot); returns in every thread the counter value after the add when this CTA
-// completed the item (low byte == KB), or 0.  The last arriver resets the counter.
+// Arrive (consumers) after this CTA's global writes with `add` (nblk in the low 8 bits plus
+// one bit per partial slot); returns in every consumer thread the counter value after the
+// add when this CTA completed the item (low byte == KB), or 0.  The last arriver resets it.
 __device__ __forceinline__ uint32_t ticket_add(uint32_t* ticket, uint32_t add, uint32_t KB, int* s_word) {
   __threadfence();
-  __syncthreads();
+  csync();
   if (threadIdx.x == 0) {
     const uint32_t now = atomicAdd(ticket, add) + add;
     const bool last = (now & 0xFFu) == KB;
     if (last) atomicExch(ticket, 0u);
     *s_word = last ? int(now) : 0;
   }
-  __syncthreads();
+  csync();
   const uint32_t v = uint32_t(*s_word);
   if (v) __threadfence();
   return v;
 }
 
-__device__ __forceinline__ bool ticket_last(uint32_t* ticket, uint32_t total, int* s_word) {
+// `all_threads`: synchronise the whole CTA (else the consumers only).
+__device__ __forceinline__ bool ticket_last(uint32_t* ticket, uint32_t total, int* s_word, bool all_threads) {
   __threadfence();
-  __syncthreads();
+  if (all_threads)
+    __syncthreads();
+  else
+    csync();
   if (threadIdx.x == 0) {
     const uint32_t old = atomicAdd(ticket, 1u);
     const bool last = (old == total - 1);
     if (last) atomicExch(ticket, 0u);
     *s_word = last ? 1 : 0;
   }
-  __syncthreads();
+  if (all_threads)
+    __syncthreads();
+  else
+    csync();
   const bool last = *s_word != 0;
   if (last) __threadfence();
   return last;
@@ -171,7 +238,20 @@ __device__ bool grid_sync(const Params& p, int k, int* s_flag) {
 
 // After the last barrier: the last CTA to get here resets the barrier counter.
 __device__ void grid_done(const Params& p, int* s_flag) {
-  if (ticket_last(p.bar_done, gridDim.x, s_flag) && threadIdx.x == 0) atomicExch(p.bar_count, 0u);
+  if (ticket_last(p.bar_done, gridDim.x, s_flag, true) && threadIdx.x == 0) atomicExch(p.bar_count, 0u);
+}
+
+// Wait for an mbarrier phase; on running out of time record ST_TIMEOUT and go on (the
+// results are then garbage, flagged by the status word, and nothing hangs).
+__device__ __forceinline__ void mbar_wait_or_flag(uint64_t* bar, uint32_t parity, uint32_t* status) {
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+      record_status(status, ST_TIMEOUT);
+      return;
+    }
+  }
 }
 
 // ---------------------------------------------------------------- work items
@@ -179,7 +259,7 @@ struct Item {
   int kind;
   int idx;   // item index within its kind
   int e;     // routed expert, or -1
-  int row0;  // first row: expert-sorted row (routed), token (shared), token (router)
+  int row0;  // first row: expert-sorted row (routed), token (shared / router)
   int nt;    // rows in this token group (1..NT_MAX)
   int c;     // 64-column chunk (router: row block)
   int KB;    // blocks per item
@@ -272,7 +352,8 @@ __device__ void issue_block(const Params& p, const Meta& m, const StreamMaps& ma
   const int x = it.c * 64;
   switch (kind) {
     case KIND_RT:
-      bulk_g2s(stage, p.w_router + (size_t)it.c * RT_ROWS * E, BLK_BYTES, bar);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tma_load_2d(stage + q * (BLK_BYTES / 4), &maps.wr, q * 64, it.c * RT_ROWS, bar);
       break;
     case KIND_GU:
       tma_load_2d(stage, &maps.wg, x, it.e * H + kb * GU_ROWS, bar);
@@ -298,93 +379,44 @@ struct Stream {
   Meta meta;
   BlockList L;
   int nctas;
-  int b0, nb;  // this CTA's block range
-  int ring;    // blocks consumed by this CTA before this step (stage ring position)
+  int b0, nb;      // this CTA's block range in the current step
+  int ring;        // blocks streamed by this CTA before this step (ring position)
   int first_slot;  // trace slot stamped when the step's first block has arrived
   uint8_t* sm;
-  uint64_t* bars;
+  uint64_t* full;
+  uint64_t* empty;
   int* misc;  // [8..15]: flags
   const int* perm;
   const int* inv;
   const float* gw;
 };
 
-__device__ __forceinline__ uint8_t* stage_ptr(Stream& S, int j) {
+__device__ __forceinline__ uint8_t* stage_ptr(const Stream& S, int j) {
   return S.sm + Smem::stages + ((S.ring + j) % NSTAGE) * BLK_BYTES;
 }
 
-// Wait for CTA-local block j of this step: thread 0 waits (bounded); the others observe the
-// already-completed phase.  Uniform result across the CTA.
-__device__ __forceinline__ bool wait_stage(Stream& S, int j) {
-  const int st = (S.ring + j) % NSTAGE;
-  const uint32_t par = uint32_t((S.ring + j) / NSTAGE) & 1u;
-  int* ok = S.misc + 8;
-  if (threadIdx.x == 0) *ok = mbar_wait_bounded(S.bars + st, par, S.p->status) ? 1 : 0;
-  __syncthreads();
-  if (!*ok) return false;
-  while (!mbar_try_wait(S.bars + st, par)) {
+// Producer (one lane): stream this CTA's range of the step through the stage ring.
+__device__ void produce(Stream& S) {
+  for (int j = 0; j < S.nb; ++j) {
+    const int pos = S.ring + j;
+    const int st = pos % NSTAGE;
+    const int use = pos / NSTAGE;
+    if (use > 0) mbar_wait_or_flag(S.empty + st, uint32_t(use - 1) & 1u, S.p->status);
+    issue_block(*S.p, S.meta, *S.maps, S.L, S.b0 + j, S.sm + Smem::stages + st * BLK_BYTES, S.full + st);
   }
+}
+
+// Consumer side of block j: wait until it has landed.
+__device__ __forceinline__ void wait_full(Stream& S, int j) {
+  const int pos = S.ring + j;
+  mbar_wait_or_flag(S.full + pos % NSTAGE, uint32_t(pos / NSTAGE) & 1u, S.p->status);
   if (j == 0) trace_point(*S.p, S.first_slot);
-  return true;
 }
 
-// Block j has been consumed by every thread: refill its stage with block j + NSTAGE.
-__device__ __forceinline__ void refill(Stream& S, int j) {
-  if (threadIdx.x == 0 && j + NSTAGE < S.nb)
-    issue_block(*S.p, S.meta, *S.maps, S.L, S.b0 + j + NSTAGE, stage_ptr(S, j), S.bars + (S.ring + j) % NSTAGE);
-}
-
-// acc[t][m][q] += sum over rows r of block `stg` of xs[t][k0 + r] * tile_m[r][ch*8 + q].
-// Lane = (row quarter rsub, 16-byte column chunk ch); warps own contiguous row ranges.
-template <int NT, int NM, int KR>
-__device__ __forceinline__ void mac_block(float (&acc)[NT][NM][8], const bf16* __restrict__ stg,
-                                          const bf16* __restrict__ xs, int xlen, int k0) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int rsub = lane >> 3, ch = lane & 7;
-  constexpr int RPW = KR / NWARPS;
-#pragma unroll 4
-  for (int i = 0; i < RPW / 4; ++i) {
-    const int r = warp * RPW + i * 4 + rsub;
-    float xv[NT];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) xv[t] = __bfloat162float(xs[t * xlen + k0 + r]);
-#pragma unroll
-    for (int m = 0; m < NM; ++m) {
-      const uint4 w = *reinterpret_cast<const uint4*>(stg + (size_t)m * KR * 64 + r * 64 + ch * 8);
-      float wf[8];
-      bf16x8_to_f32(w, wf);
-#pragma unroll
-      for (int t = 0; t < NT; ++t)
-#pragma unroll
-        for (int q = 0; q < 8; ++q) acc[t][m][q] = fmaf(xv[t], wf[q], acc[t][m][q]);
-    }
-  }
-}
-
-// Sum acc over the row lanes (fixed shuffle tree) and the warps (warp order) into out[t][m*64+c].
-template <int NT, int NM>
-__device__ __forceinline__ void reduce_acc(float (&acc)[NT][NM][8], float* red, float* out) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int rsub = lane >> 3, ch = lane & 7;
-#pragma unroll
-  for (int t = 0; t < NT; ++t)
-#pragma unroll
-    for (int m = 0; m < NM; ++m)
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        float v = acc[t][m][q];
-        v += __shfl_xor_sync(0xffffffffu, v, 8);
-        v += __shfl_xor_sync(0xffffffffu, v, 16);
-        if (rsub == 0) red[((warp * NT + t) * NM + m) * 64 + ch * 8 + q] = v;
-      }
-  __syncthreads();
-  for (int o = threadIdx.x; o < NT * NM * 64; o += NTHREADS) {
-    float s = 0.f;
-#pragma unroll
-    for (int w = 0; w < NWARPS; ++w) s += red[w * NT * NM * 64 + o];
-    out[o] = s;
-  }
-  __syncthreads();
+// Consumer side of block j: this warp is done reading it.
+__device__ __forceinline__ void release(Stream& S, int j) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(S.empty + (S.ring + j) % NSTAGE);
 }
 
 __device__ __forceinline__ float* partial_slot(const Params& p, const Item& it, int slot) {
@@ -412,18 +444,18 @@ __device__ void item_epilogue(Stream& S, const Item& it, const float* vals) {
   if (it.kind == KIND_GU || it.kind == KIND_SGU) {
     bf16* dst = it.kind == KIND_GU ? p.h : p.hs;
     const int ld = it.kind == KIND_GU ? I : IS;
-    for (int q = threadIdx.x; q < nt * 64; q += NTHREADS) {
+    for (int q = threadIdx.x; q < nt * 64; q += NCONS) {
       const int t = q / 64, j = q % 64;
       const float g = vals[t * 128 + j], u = vals[t * 128 + 64 + j];
       dst[(size_t)(it.row0 + t) * ld + c * 64 + j] = __float2bfloat16_rn(silu_f32(g) * u);
     }
   } else if (it.kind == KIND_SD) {
-    for (int q = threadIdx.x; q < nt * 64; q += NTHREADS) {
+    for (int q = threadIdx.x; q < nt * 64; q += NCONS) {
       const int t = q / 64, j = q % 64;
       p.S[(size_t)(it.row0 + t) * H + c * 64 + j] = vals[t * 64 + j];
     }
   } else {  // routed down: rows scaled by their gate
-    for (int q = threadIdx.x; q < nt * 64; q += NTHREADS) {
+    for (int q = threadIdx.x; q < nt * 64; q += NCONS) {
       const int t = q / 64, j = q % 64;
       const int row = it.row0 + t;
       p.Y[(size_t)row * H + c * 64 + j] = S.gw[S.perm[row]] * vals[t * 64 + j];
@@ -435,7 +467,7 @@ __device__ void item_epilogue(Stream& S, const Item& it, const float* vals) {
 __device__ void combine_chunk(Stream& S, int c) {
   const Params& p = *S.p;
   const bool residual = (p.flags & 2u) != 0;
-  for (int q = threadIdx.x; q < p.T * 64; q += NTHREADS) {
+  for (int q = threadIdx.x; q < p.T * 64; q += NCONS) {
     const int t = q / 64, j = q % 64;
     const int col = c * 64 + j;
     float v = __ldcg(p.S + (size_t)t * H + col);
@@ -452,7 +484,7 @@ __device__ __forceinline__ int block_owner(long long b, long long N, int n) {
 }
 
 // This CTA has written all its routed-down rows of chunk c: arrive; the last of the CTAs
-// that cover the chunk's blocks runs the combine of the chunk.
+// that cover the chunk's blocks runs the combine of the chunk (consumers only).
 __device__ void arrive_chunk(Stream& S, int c) {
   const long long N = S.L.n_total;
   const long long per_chunk = (long long)S.meta.groups * DN_KB;
@@ -461,62 +493,23 @@ __device__ void arrive_chunk(Stream& S, int c) {
   uint32_t expect = 0;
   for (int g = g_lo; g <= g_hi; ++g)
     if (N * (g + 1) / S.nctas > N * g / S.nctas) ++expect;
-  if (ticket_last(S.p->tk_comb + c, expect, S.misc + 11)) combine_chunk(S, c);
-  __syncthreads();
+  if (ticket_last(S.p->tk_comb + c, expect, S.misc + 11, false)) combine_chunk(S, c);
+  csync();
 }
 
-// Router block (one item): partial logits of the token group over 64 router rows.
-// Thread e owns expert e: rows ascending, one fma chain per token.
-template <int NT>
-__device__ bool run_router_block(Stream& S, const Item& it, int& j) {
-  const Params& p = *S.p;
-  float* xs = reinterpret_cast<float*>(S.sm + Smem::xs);  // [NT][64] f32
-  const int r0 = it.c * RT_ROWS;
-  for (int q = threadIdx.x; q < NT * RT_ROWS; q += NTHREADS) {
-    const int t = q / RT_ROWS, r = q % RT_ROWS;
-    xs[q] = t < it.nt ? __bfloat162float(p.xin[(size_t)(it.row0 + t) * H + r0 + r]) : 0.f;
-  }
-  __syncthreads();
-  if (!wait_stage(S, j)) return false;
-  const bf16* w = reinterpret_cast<const bf16*>(stage_ptr(S, j));
-  const int e = threadIdx.x;
-  float acc[NT];
-#pragma unroll
-  for (int t = 0; t < NT; ++t) acc[t] = 0.f;
-#pragma unroll 8
-  for (int r = 0; r < RT_ROWS; ++r) {
-    const float wv = __bfloat162float(w[r * E + e]);
-#pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] = fmaf(xs[t * RT_ROWS + r], wv, acc[t]);
-  }
-#pragma unroll
-  for (int t = 0; t < NT; ++t)
-    if (t < it.nt) p.RP[((size_t)it.c * STREAM_MAX_T + it.row0 + t) * E + e] = acc[t];
-  __syncthreads();
-  refill(S, j);
-  ++j;
-  return true;
-}
-
-// One segment: blocks [kb_start, kb_start + nblk) of item `it`, consumed as CTA blocks
-// j .. j + nblk - 1.  Returns false on a device timeout.
-template <int NT, int NM, int KR>
-__device__ bool run_segment(Stream& S, const Item& it, int kb_start, int nblk, int& j) {
+// Stage the token group's input rows (bf16, row stride xlen + XPAD) for an item (consumers).
+__device__ void stage_inputs(Stream& S, const Item& it, int xlen) {
   const Params& p = *S.p;
   bf16* xs = reinterpret_cast<bf16*>(S.sm + Smem::xs);
-  float* red = reinterpret_cast<float*>(S.sm + Smem::red);
-  float* out = reinterpret_cast<float*>(S.sm + Smem::out);
-  // stage the token group's input rows (bf16) for the whole item
-  const int xlen = it.kind == KIND_SD ? IS : it.kind == KIND_DN ? I : H;
   const int cpr = xlen / 8;
-  for (int q = threadIdx.x; q < NT * cpr; q += NTHREADS) {
+  for (int q = threadIdx.x; q < NT_MAX * cpr; q += NCONS) {
     const int t = q / cpr, k8 = q % cpr;
     uint4 v = make_uint4(0, 0, 0, 0);
     if (t < it.nt) {
       const bf16* src;
       if (it.kind == KIND_GU)
         src = p.xin + (size_t)(S.perm[it.row0 + t] / K) * H;
-      else if (it.kind == KIND_SGU)
+      else if (it.kind == KIND_SGU || it.kind == KIND_RT)
         src = p.xin + (size_t)(it.row0 + t) * H;
       else if (it.kind == KIND_SD)
         src = p.hs + (size_t)(it.row0 + t) * IS;
@@ -524,71 +517,109 @@ __device__ bool run_segment(Stream& S, const Item& it, int kb_start, int nblk, i
         src = p.h + (size_t)(it.row0 + t) * I;
       v = __ldcg(reinterpret_cast<const uint4*>(src) + k8);
     }
-    *reinterpret_cast<uint4*>(xs + t * xlen + k8 * 8) = v;
+    *reinterpret_cast<uint4*>(xs + t * (xlen + XPAD) + k8 * 8) = v;
   }
-  __syncthreads();
-  float acc[NT][NM][8];
+  csync();
+}
+
+// Router block (one item): partial logits of the token group over 64 router rows, written
+// to RP[row block][token][expert].  Warp w owns experts [32w, 32w + 32) (two 16-row tiles).
+__device__ void run_router_block(Stream& S, const Item& it, int& j) {
+  const Params& p = *S.p;
+  stage_inputs(S, it, H);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  wait_full(S, j);
+  const uint32_t tile = smem_u32(stage_ptr(S, j)) + uint32_t((warp >> 1) * (BLK_BYTES / 4));
+  const uint32_t xs = smem_u32(S.sm + Smem::xs);
+  float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+  const int mbase = (warp & 1) * 32;  // column within the 64-expert sub-tile
+  mma_tile(d0, tile, mbase, 0, RT_ROWS / 16, xs, H + XPAD, it.c * RT_ROWS);
+  mma_tile(d1, tile, mbase + 16, 0, RT_ROWS / 16, xs, H + XPAD, it.c * RT_ROWS);
+  release(S, j);
+  // C fragment: (expert m0 + g [+8], token 2*tig [+1])
+  const int g = lane >> 2, tig = lane & 3;
+  const int e0 = warp * 32;
 #pragma unroll
-  for (int t = 0; t < NT; ++t)
+  for (int h = 0; h < 2; ++h) {
+    const float* d = h ? d1 : d0;
 #pragma unroll
-    for (int m = 0; m < NM; ++m)
-#pragma unroll
-      for (int q = 0; q < 8; ++q) acc[t][m][q] = 0.f;
+    for (int r = 0; r < 4; ++r) {
+      const int e = e0 + h * 16 + g + ((r >> 1) << 3);
+      const int t = 2 * tig + (r & 1);
+      if (t < it.nt) p.RP[((size_t)it.c * STREAM_MAX_T + it.row0 + t) * E + e] = d[r];
+    }
+  }
+  csync();  // xs is restaged by the next item
+  ++j;
+}
+
+// One segment: blocks [kb_start, kb_start + nblk) of item `it`, consumed as CTA blocks
+// j .. j + nblk - 1 (consumers).
+__device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, int& j) {
+  const Params& p = *S.p;
+  const bool gu = it.kind == KIND_GU || it.kind == KIND_SGU;
+  const int xlen = it.kind == KIND_SD ? IS : it.kind == KIND_DN ? I : H;
+  stage_inputs(S, it, xlen);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t xs = smem_u32(S.sm + Smem::xs);
+  float d[4] = {0.f, 0.f, 0.f, 0.f};
+  // gate/up: warp w owns columns 16*(w&3) of the gate (w < 4) or up (w >= 4) tile, all 128
+  // rows; down: warp w owns columns 16*(w&3), rows [128*(w>>2), +128) of the 256-row tile.
+  const int m0 = (warp & 3) * 16;
+  const uint32_t sub = gu ? uint32_t((warp >> 2) * (BLK_BYTES / 2)) : 0u;
+  const int r0 = gu ? 0 : (warp >> 2) * 128;
+  const int rows = gu ? GU_ROWS : DN_ROWS;
   for (int q = 0; q < nblk; ++q, ++j) {
-    if (!wait_stage(S, j)) return false;
-    mac_block<NT, NM, KR>(acc, reinterpret_cast<const bf16*>(stage_ptr(S, j)), xs, xlen, (kb_start + q) * KR);
-    __syncthreads();  // every thread is done with this stage
-    refill(S, j);
+    wait_full(S, j);
+    mma_tile(d, smem_u32(stage_ptr(S, j)) + sub, m0, r0, 8, xs, xlen + XPAD, (kb_start + q) * rows + r0);
+    release(S, j);
   }
-  reduce_acc<NT, NM>(acc, red, out);
-  constexpr int ncol = NM * 64;
+  // fragments -> out[half][t][col]: gate/up: col = (w>=4)*64 + 16*(w&3) + m (half 0);
+  // down: col = 16*(w&3) + m, half = w >> 2
+  float* out = reinterpret_cast<float*>(S.sm + Smem::out);
+  const int ncol = gu ? 128 : 64;
+  {
+    const int g = lane >> 2, tig = lane & 3;
+    const int half = gu ? 0 : (warp >> 2);
+    const int cb = gu ? (warp >> 2) * 64 + m0 : m0;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int col = cb + g + ((r >> 1) << 3);
+      const int t = 2 * tig + (r & 1);
+      out[(half * NT_MAX + t) * ncol + col] = d[r];
+    }
+  }
+  csync();
+  if (!gu) {  // down: add the two row halves (fixed order)
+    for (int q = threadIdx.x; q < NT_MAX * 64; q += NCONS) out[q] = out[q] + out[NT_MAX * 64 + q];
+    csync();
+  }
   if (kb_start == 0 && nblk == it.KB) {
     item_epilogue(S, it, out);
-    __syncthreads();
-    return true;
+    csync();
+    return;
   }
   float* P = partial_slot(p, it, kb_start);
-  for (int q = threadIdx.x; q < it.nt * ncol; q += NTHREADS) P[q] = out[q];
+  for (int q = threadIdx.x; q < it.nt * ncol; q += NCONS) P[q] = out[q];
   const uint32_t v = ticket_add(item_ticket(p, it), uint32_t(nblk) | (1u << (8 + kb_start)), uint32_t(it.KB),
                                 S.misc + 10);
   if (v) {
     // last arriver: add the partial slots in block order
     const uint32_t mask = v >> 8;
-    for (int q = threadIdx.x; q < it.nt * ncol; q += NTHREADS) {
+    for (int q = threadIdx.x; q < it.nt * ncol; q += NCONS) {
       float s = 0.f;
       for (int sl = 0; sl < it.KB; ++sl)
         if (mask & (1u << sl)) s += __ldcg(partial_slot(p, it, sl) + q);
       out[q] = s;
     }
-    __syncthreads();
+    csync();
     item_epilogue(S, it, out);
   }
-  __syncthreads();
-  return true;
+  csync();
 }
 
-template <int NM, int KR>
-__device__ __forceinline__ bool run_segment_nt(Stream& S, const Item& it, int kb, int nblk, int& j) {
-  if (it.nt <= 1) return run_segment<1, NM, KR>(S, it, kb, nblk, j);
-  if (it.nt <= 2) return run_segment<2, NM, KR>(S, it, kb, nblk, j);
-  if (it.nt <= 4) return run_segment<4, NM, KR>(S, it, kb, nblk, j);
-  return run_segment<8, NM, KR>(S, it, kb, nblk, j);
-}
-
-// Issue the first NSTAGE blocks of this CTA's range of step L.
-__device__ void stream_begin(Stream& S, const BlockList& L) {
-  S.L = L;
-  const long long N = L.n_total;
-  const int g = blockIdx.x;
-  S.b0 = int(N * g / S.nctas);
-  S.nb = int(N * (g + 1) / S.nctas) - S.b0;
-  if (threadIdx.x == 0)
-    for (int s = 0; s < NSTAGE && s < S.nb; ++s)
-      issue_block(*S.p, S.meta, *S.maps, L, S.b0 + s, stage_ptr(S, s), S.bars + (S.ring + s) % NSTAGE);
-}
-
-// Consume this CTA's range of the step begun by stream_begin.  Returns false on timeout.
-__device__ bool stream_run(Stream& S) {
+// Consumers: work through this CTA's range of the step.
+__device__ void consume(Stream& S) {
   const bool combine = S.L.k_first == KIND_DN;
   int cur_chunk = -1;
   int j = 0;
@@ -600,29 +631,31 @@ __device__ bool stream_run(Stream& S) {
       if (cur_chunk >= 0) arrive_chunk(S, cur_chunk);
       cur_chunk = it.c;
     }
-    bool ok;
-    if (kind == KIND_RT) {
-      ok = it.nt <= 1 ? run_router_block<1>(S, it, j)
-           : it.nt <= 2 ? run_router_block<2>(S, it, j)
-           : it.nt <= 4 ? run_router_block<4>(S, it, j)
-                        : run_router_block<8>(S, it, j);
-    } else {
-      const int nblk = min(it.KB - kb, S.nb - j);
-      if (kind == KIND_GU || kind == KIND_SGU)
-        ok = run_segment_nt<2, GU_ROWS>(S, it, kb, nblk, j);
-      else
-        ok = run_segment_nt<1, DN_ROWS>(S, it, kb, nblk, j);
-    }
-    if (!ok) return false;
+    if (kind == KIND_RT)
+      run_router_block(S, it, j);
+    else
+      run_segment(S, it, kb, min(it.KB - kb, S.nb - j), j);
   }
   if (combine && cur_chunk >= 0) arrive_chunk(S, cur_chunk);
-  S.ring += S.nb;
-  return true;
 }
 
-// Spread a bulk L2 prefetch of `bytes` (multiple of 16) at `base` over the grid.
+// One streaming step for the whole CTA: the producer lane streams, the consumers compute.
+__device__ void run_step(Stream& S, const BlockList& L) {
+  S.L = L;
+  const long long N = L.n_total;
+  S.b0 = int(N * blockIdx.x / S.nctas);
+  S.nb = int(N * (blockIdx.x + 1) / S.nctas) - S.b0;
+  if (threadIdx.x >= NCONS) {
+    if (threadIdx.x == NCONS) produce(S);
+  } else {
+    consume(S);
+  }
+  S.ring += S.nb;
+  __syncthreads();
+}
+
+// Spread a bulk L2 prefetch of `bytes` (multiple of 16) at `base` over the grid (one thread).
 __device__ __forceinline__ void prefetch_share(const void* base, size_t bytes) {
-  if (threadIdx.x != 0) return;
   const size_t per = ((bytes / gridDim.x) + 15) & ~size_t(15);
   const size_t a = per * blockIdx.x;
   if (a >= bytes) return;
@@ -639,17 +672,23 @@ __device__ __forceinline__ void prefetch_share(const void* base, size_t bytes) {
 // ---------------------------------------------------------------- routing
 // Scores of up to 4 tokens (list `toks`, count nt) into scores[t][e], then the top-K of each
 // (warp t): key = (score bits, 255 - expert), max = highest score, lowest index on ties.
+// All threads of the CTA call it.
 __device__ void route_tokens(const Params& p, uint8_t* sm, const int* toks, int nt, int* s_idx, float* s_gw,
                              bool write_global) {
   float* scores = reinterpret_cast<float*>(sm + Smem::scores);
-  const int e = threadIdx.x;  // NTHREADS == E
-  for (int t = 0; t < nt; ++t) {
-    const int tok = toks[t];
-    float l = 0.f;
-#pragma unroll 8
-    for (int rb = 0; rb < RT_NB; ++rb) l += __ldcg(p.RP + ((size_t)rb * STREAM_MAX_T + tok) * E + e);
-    if (p.router_bias) l += p.router_bias[e];
-    scores[t * E + e] = 1.0f / (1.0f + expf(-l));
+  const int e = threadIdx.x;
+  if (e < E) {
+    for (int t = 0; t < nt; ++t) {
+      const int tok = toks[t];
+      float part[RT_NB];
+#pragma unroll
+      for (int rb = 0; rb < RT_NB; ++rb) part[rb] = __ldcg(p.RP + ((size_t)rb * STREAM_MAX_T + tok) * E + e);
+      float l = 0.f;
+#pragma unroll
+      for (int rb = 0; rb < RT_NB; ++rb) l += part[rb];
+      if (p.router_bias) l += p.router_bias[e];
+      scores[t * E + e] = 1.0f / (1.0f + expf(-l));
+    }
   }
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -705,7 +744,7 @@ __device__ void route_tokens(const Params& p, uint8_t* sm, const int* toks, int 
 
 // Stable counting sort of the T*K (token, slot) pairs (expert ids in s_idx) by expert, in
 // this CTA's shared memory: routing tables (Meta), perm (sorted row -> pair), inv.
-// CTA 0 also publishes counts and offsets.
+// CTA 0 also publishes counts and offsets.  All threads of the CTA call it.
 __device__ Meta build_tables(const Params& p, uint8_t* sm, int* perm, int* inv) {
   int* s_idx = reinterpret_cast<int*>(sm + Smem::s_idx);
   int* s_cnt = reinterpret_cast<int*>(sm + Smem::s_cnt);
@@ -719,77 +758,90 @@ __device__ Meta build_tables(const Params& p, uint8_t* sm, int* perm, int* inv) 
   int* mtgp = mbase + 3 * (E + 1);
   const int n = p.T * K;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  s_cnt[tid] = 0;
+  const bool act = tid < E;  // thread == expert; the producer warp only synchronises
+  if (act) s_cnt[tid] = 0;
   __syncthreads();
-  for (int q = tid; q < n; q += NTHREADS) {
-    const int e = s_idx[q];
-    if (e < 0 || e >= E) {
-      record_status(p.status, ST_BOUNDS);
-      continue;
+  if (act)
+    for (int q = tid; q < n; q += E) {
+      const int e = s_idx[q];
+      if (e < 0 || e >= E) {
+        record_status(p.status, ST_BOUNDS);
+        continue;
+      }
+      atomicAdd(&s_cnt[e], 1);
     }
-    atomicAdd(&s_cnt[e], 1);
-  }
   __syncthreads();
-  // exclusive scans over experts (tid == expert): counts, touched flags, token groups
-  const int c = s_cnt[tid];
-  const int f = c > 0 ? 1 : 0;
-  const int ng = (c + NT_MAX - 1) / NT_MAX;
-  int ic = c, jf = f, kg = ng;
+  // exclusive scans over experts: counts, touched flags, token groups
+  int c = 0, f = 0, ng = 0, ic = 0, jf = 0, kg = 0;
+  if (act) {
+    c = s_cnt[tid];
+    f = c > 0 ? 1 : 0;
+    ng = (c + NT_MAX - 1) / NT_MAX;
+    ic = c;
+    jf = f;
+    kg = ng;
 #pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int a = __shfl_up_sync(0xffffffffu, ic, off);
-    const int b = __shfl_up_sync(0xffffffffu, jf, off);
-    const int d = __shfl_up_sync(0xffffffffu, kg, off);
-    if (lane >= off) {
-      ic += a;
-      jf += b;
-      kg += d;
+    for (int off = 1; off < 32; off <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, ic, off);
+      const int b = __shfl_up_sync(0xffffffffu, jf, off);
+      const int d = __shfl_up_sync(0xffffffffu, kg, off);
+      if (lane >= off) {
+        ic += a;
+        jf += b;
+        kg += d;
+      }
+    }
+    if (lane == 31) {
+      s_wsum[warp] = ic;
+      s_wsum[NWARPS + warp] = jf;
+      s_wsum[2 * NWARPS + warp] = kg;
     }
   }
-  if (lane == 31) {
-    s_wsum[warp] = ic;
-    s_wsum[NWARPS + warp] = jf;
-    s_wsum[2 * NWARPS + warp] = kg;
-  }
   __syncthreads();
-  int bc = 0, bf = 0, bg = 0;
-  for (int w = 0; w < warp; ++w) {
-    bc += s_wsum[w];
-    bf += s_wsum[NWARPS + w];
-    bg += s_wsum[2 * NWARPS + w];
-  }
-  const int off_e = bc + ic - c;
-  const int pos = bf + jf - f;
-  const int gpre = bg + kg - ng;
-  s_fill[tid] = off_e;
-  if (f) {
-    me[pos] = tid;
-    moff[pos] = off_e;
-    mcnt[pos] = c;
-    mtgp[pos] = gpre;
-  }
-  if (tid == NTHREADS - 1) {
-    s_wsum[3 * NWARPS] = pos + f;
-    s_wsum[3 * NWARPS + 1] = gpre + ng;
-    mtgp[pos + f] = gpre + ng;
-  }
-  if (blockIdx.x == 0) {
-    p.counts[tid] = c;
-    p.offsets[tid] = off_e;
-    if (p.out_counts) p.out_counts[tid] = c;
-    if (tid == NTHREADS - 1) p.offsets[E] = off_e + c;
+  if (act) {
+    int bc = 0, bf = 0, bg = 0;
+    for (int w = 0; w < warp; ++w) {
+      bc += s_wsum[w];
+      bf += s_wsum[NWARPS + w];
+      bg += s_wsum[2 * NWARPS + w];
+    }
+    const int off_e = bc + ic - c;
+    const int pos = bf + jf - f;
+    const int gpre = bg + kg - ng;
+    s_fill[tid] = off_e;
+    if (f) {
+      me[pos] = tid;
+      moff[pos] = off_e;
+      mcnt[pos] = c;
+      mtgp[pos] = gpre;
+    }
+    if (tid == E - 1) {
+      s_wsum[3 * NWARPS] = pos + f;
+      s_wsum[3 * NWARPS + 1] = gpre + ng;
+      mtgp[pos + f] = gpre + ng;
+    }
+    if (blockIdx.x == 0) {
+      p.counts[tid] = c;
+      p.offsets[tid] = off_e;
+      if (p.out_counts) p.out_counts[tid] = c;
+      if (tid == E - 1) p.offsets[E] = off_e + c;
+    }
   }
   __syncthreads();
   // stable scatter, 256 pairs at a time in (t, j) order
-  for (int base = 0; base < n; base += NTHREADS) {
-    for (int q = tid; q < NWARPS * E; q += NTHREADS) s_wcnt[q] = 0;
+  for (int base = 0; base < n; base += E) {
+    if (act)
+      for (int q = tid; q < NWARPS * E; q += E) s_wcnt[q] = 0;
     __syncthreads();
     const int pi = base + tid;
-    int e = pi < n ? s_idx[pi] : -1;
+    int e = (act && pi < n) ? s_idx[pi] : -1;
     if (e >= E) e = -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const int r = __popc(peers & ((1u << lane) - 1u));
-    if (e >= 0 && r == 0) s_wcnt[warp * E + e] = __popc(peers);
+    int r = 0;
+    if (act) {
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      r = __popc(peers & ((1u << lane) - 1u));
+      if (e >= 0 && r == 0) s_wcnt[warp * E + e] = __popc(peers);
+    }
     __syncthreads();
     if (e >= 0) {
       int before = 0;
@@ -799,7 +851,7 @@ __device__ Meta build_tables(const Params& p, uint8_t* sm, int* perm, int* inv) 
       inv[pi] = row;
     }
     __syncthreads();
-    {
+    if (act) {
       int add = 0;
       for (int w = 0; w < NWARPS; ++w) add += s_wcnt[w * E + tid];
       s_fill[tid] += add;
@@ -823,15 +875,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     decode_fused(const __grid_constant__ Params p, const __grid_constant__ StreamMaps maps, int mode) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = aligned_smem(smem_raw);
-  pdl_launch_dependents();
   Stream S;
   S.p = &p;
   S.maps = &maps;
   S.meta = Meta{};
   S.nctas = gridDim.x;
   S.ring = 0;
+  S.first_slot = 11;
   S.sm = sm;
-  S.bars = reinterpret_cast<uint64_t*>(sm + Smem::bars);
+  S.full = reinterpret_cast<uint64_t*>(sm + Smem::full);
+  S.empty = reinterpret_cast<uint64_t*>(sm + Smem::empty);
   S.misc = reinterpret_cast<int*>(sm + Smem::misc);
   int* perm = reinterpret_cast<int*>(sm + Smem::perm);
   int* inv = reinterpret_cast<int*>(sm + Smem::inv);
@@ -845,7 +898,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const bool full = mode == 0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NSTAGE; ++s) mbar_init(S.bars + s, 1);
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(S.full + s, 1);
+      mbar_init(S.empty + s, NWARPS);
+    }
     fence_mbar_init();
   }
   __syncthreads();
@@ -855,6 +911,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   // ---- step A: router partial logits and the shared gate/up
   {
+    if (full && threadIdx.x == NCONS + 1) prefetch_share(p.ws_down, (size_t)IS * H * 2);
     BlockList L;
     L.k_first = KIND_RT;
     L.kb_first = 1;
@@ -862,10 +919,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     L.k_second = KIND_SGU;
     L.kb_second = GU_KB;
     L.n_total = L.n_first + (full ? ntg * SGU_NCH * GU_KB : 0);
-    S.first_slot = 11;
-    stream_begin(S, L);
-    if (full) prefetch_share(p.ws_down, (size_t)IS * H * 2);
-    if (!stream_run(S)) return;
+    run_step(S, L);
   }
   trace_point(p, 2);
   if (!grid_sync(p, 1, S.misc + 12)) return;
@@ -905,17 +959,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   // ---- step C: routed gate/up and the shared down projection
   {
-    BlockList L;
-    L.k_first = KIND_GU;
-    L.kb_first = GU_KB;
-    L.n_first = S.meta.groups * GU_NCH * GU_KB;
-    L.k_second = KIND_SD;
-    L.kb_second = SD_KB;
-    L.n_total = L.n_first + ntg * OUT_NCH * SD_KB;
-    S.first_slot = 12;
-    stream_begin(S, L);
     // the touched experts' down matrices are read in step D: prefetch them when they fit
-    if ((unsigned long long)S.meta.U * I * H * 2 <= p.prefetch_bytes_max && threadIdx.x == 0) {
+    if (threadIdx.x == NCONS + 1 && (unsigned long long)S.meta.U * I * H * 2 <= p.prefetch_bytes_max) {
       const size_t per_e = (size_t)I * H * 2;
       const size_t total = per_e * S.meta.U;
       const size_t share = ((total / gridDim.x) + 15) & ~size_t(15);
@@ -932,8 +977,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         a += n;
       }
     }
+    BlockList L;
+    L.k_first = KIND_GU;
+    L.kb_first = GU_KB;
+    L.n_first = S.meta.groups * GU_NCH * GU_KB;
+    L.k_second = KIND_SD;
+    L.kb_second = SD_KB;
+    L.n_total = L.n_first + ntg * OUT_NCH * SD_KB;
+    S.first_slot = 12;
     trace_point(p, 6);
-    if (!stream_run(S)) return;
+    run_step(S, L);
   }
   trace_point(p, 7);
   if (!grid_sync(p, ++nbar, S.misc + 12)) return;
@@ -946,8 +999,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     L.kb_first = L.kb_second = DN_KB;
     L.n_first = L.n_total = S.meta.groups * OUT_NCH * DN_KB;
     S.first_slot = 13;
-    stream_begin(S, L);
-    if (!stream_run(S)) return;
+    run_step(S, L);
   }
   trace_point(p, 9);
   grid_done(p, S.misc + 13);
@@ -955,9 +1007,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 // ================================================================ RMSNorm (pre-norm layers)
-// xn[t] = bf16(x[t] / sqrt(mean(x[t]^2) + eps)), unit weight; one CTA per token.
-__global__ void __launch_bounds__(NTHREADS) rmsnorm_kernel(const __grid_constant__ Params p) {
-  __shared__ float s_w[NWARPS];
+// xn[t] = bf16(x[t] / sqrt(mean(x[t]^2) + eps)), unit weight; one CTA of 256 threads per token.
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const __grid_constant__ Params p) {
+  __shared__ float s_w[8];
   pdl_launch_dependents();
   pdl_wait();
   const int t = blockIdx.x;
@@ -974,7 +1026,7 @@ __global__ void __launch_bounds__(NTHREADS) rmsnorm_kernel(const __grid_constant
   __syncthreads();
   float tot = 0.f;
 #pragma unroll
-  for (int w = 0; w < NWARPS; ++w) tot += s_w[w];
+  for (int w = 0; w < 8; ++w) tot += s_w[w];
   const float d = sqrtf(tot / float(H) + p.rms_eps);
   uint32_t packed[4];
 #pragma unroll

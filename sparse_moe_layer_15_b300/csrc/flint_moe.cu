@@ -197,7 +197,7 @@ Params make_params(flint_moe_t h, const void* x, int T, void* y, int32_t* out_id
 // Launch with programmatic stream serialisation, or as a cooperative grid (all CTAs
 // resident at once, required by kernels with grid-wide barriers).
 template <class... KArgs, class... Args>
-cudaError_t launch(flint_moe_t h, const char* name, void (*kern)(KArgs...), unsigned grid, int smem,
+cudaError_t launch(flint_moe_t h, const char* name, void (*kern)(KArgs...), unsigned grid, unsigned block, int smem,
                    cudaStream_t st, bool cooperative, Args&&... args) {
   if (grid == 0) return cudaSuccess;
   const bool rec = h->timing && h->n_ev < MAX_EVENTS;
@@ -207,7 +207,7 @@ cudaError_t launch(flint_moe_t h, const char* name, void (*kern)(KArgs...), unsi
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(NTHREADS);
+  cfg.blockDim = dim3(block);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -232,9 +232,9 @@ cudaError_t launch(flint_moe_t h, const char* name, void (*kern)(KArgs...), unsi
 // cooperative decode kernel (one CTA per SM).
 flint_moe_status run_decode(flint_moe_t h, const Params& p, cudaStream_t st, bool full) {
   cudaError_t e = cudaSuccess;
-  if (h->cfg.flags & FLINT_MOE_FLAG_PRE_RMSNORM) e = launch(h, "rmsnorm", rmsnorm_kernel, p.T, 0, st, false, p);
+  if (h->cfg.flags & FLINT_MOE_FLAG_PRE_RMSNORM) e = launch(h, "rmsnorm", rmsnorm_kernel, p.T, 256, 0, st, false, p);
   if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
-  e = launch(h, full ? "decode_fused" : "decode_fused_route", decode_fused, h->n_sm, FUSED_SMEM, st, true, p,
+  e = launch(h, full ? "decode_fused" : "decode_fused_route", decode_fused, h->n_sm, NTHREADS, FUSED_SMEM, st, true, p,
              h->smaps, full ? 0 : 1);
   return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ERR_CUDA;
 }
@@ -312,13 +312,14 @@ flint_moe_status flint_moe_create(const flint_moe_config* cfg, const flint_moe_w
     delete h;
     return FLINT_MOE_ERR_CUDA;
   }
-  const auto none = CU_TENSOR_MAP_SWIZZLE_NONE;
-  bool ok = make_map(&h->smaps.wg, w->w_gate, (uint64_t)E * H, I, 64, GU_ROWS, none) &&
-            make_map(&h->smaps.wu, w->w_up, (uint64_t)E * H, I, 64, GU_ROWS, none) &&
-            make_map(&h->smaps.wd, w->w_down, (uint64_t)E * I, H, 64, DN_ROWS, none) &&
-            make_map(&h->smaps.wsg, w->ws_gate, H, IS, 64, GU_ROWS, none) &&
-            make_map(&h->smaps.wsu, w->ws_up, H, IS, 64, GU_ROWS, none) &&
-            make_map(&h->smaps.wsd, w->ws_down, IS, H, 64, DN_ROWS, none);
+  const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  bool ok = make_map(&h->smaps.wr, w->w_router, H, E, 64, RT_ROWS, sw) &&
+            make_map(&h->smaps.wg, w->w_gate, (uint64_t)E * H, I, 64, GU_ROWS, sw) &&
+            make_map(&h->smaps.wu, w->w_up, (uint64_t)E * H, I, 64, GU_ROWS, sw) &&
+            make_map(&h->smaps.wd, w->w_down, (uint64_t)E * I, H, 64, DN_ROWS, sw) &&
+            make_map(&h->smaps.wsg, w->ws_gate, H, IS, 64, GU_ROWS, sw) &&
+            make_map(&h->smaps.wsu, w->ws_up, H, IS, 64, GU_ROWS, sw) &&
+            make_map(&h->smaps.wsd, w->ws_down, IS, H, 64, DN_ROWS, sw);
   if (!ok) {
     delete h;
     return FLINT_MOE_ERR_CUDA;
