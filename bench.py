@@ -362,7 +362,7 @@ def run_profile_case(args):
         # the earliest CTA start; several repetitions, the median of each statistic reported
         names = {0: "start", 1: "inputs_ready", 11: "A_first_block", 2: "A_done", 3: "barrier1", 4: "routed",
                  5: "tables", 6: "C_issued", 12: "C_first_block", 7: "C_done", 8: "barrier2", 13: "D_first_block",
-                 9: "D_done", 10: "end"}
+                 9: "D_done", 14: "barrier3", 10: "end"}
         layer.enable_phase_trace(True)
         reps = []
         for _ in range(5):

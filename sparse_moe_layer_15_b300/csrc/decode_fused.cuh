@@ -18,12 +18,13 @@
 //   C  routed gate/up (touched experts only) with fused SiLU-mul, and the shared down
 //      projection; the touched experts' down matrices are prefetched into L2 when they fit;
 //   -- barrier --
-//   D  routed down projection scaled by the gates; the last CTA to finish each 64-column
-//      chunk of the output performs the combine y = S + sum_j Y[inv(t, j)] in slot order.
+//   D  routed down projection scaled by the gates;
+//   -- barrier --
+//   E  the combine y = S + sum_j Y[inv(t, j)] in slot order (+ x), spread over the grid.
 //
 // Within a step the weight traffic is a list of equal 32 KB blocks (64 output columns x 128
 // or 256 rows of one or two matrices, or 64 router rows x 256 experts); every CTA takes an
-// equal contiguous range.  A producer warp streams the range through a 4-stage TMA ring
+// equal contiguous range.  A producer warp streams the range through a 5-stage TMA ring
 // (128-byte swizzled tiles); eight consumer warps multiply each tile against the current
 // token group (up to 8 rows) with warp-level bf16 MMAs (m16n8k16, fp32 accumulate), each warp
 // owning 16 output columns, so a tile needs no cross-warp reduction.  Tiles of the same
@@ -41,7 +42,7 @@ constexpr int NWARPS = NCONS / 32;
 constexpr int NTHREADS = NCONS + 32;     // + one producer warp
 constexpr int STREAM_MAX_T = 256;
 constexpr int NT_MAX = 8;                // token rows per group (the MMA's N)
-constexpr int NSTAGE = 4;
+constexpr int NSTAGE = 5;
 constexpr int BLK_BYTES = 32768;
 constexpr int GU_ROWS = 128;             // gate/up block: 128 rows x 64 columns of gate and of up
 constexpr int DN_ROWS = 256;             // down block: 256 rows x 64 columns
@@ -289,22 +290,17 @@ __device__ __forceinline__ int find_group_owner(const int* tgp, int n, int gi) {
   return lo;
 }
 
-// Item numbering: router items (tg * 32 + row block); routed gate/up items token-group major
-// (gi * 8 + c); routed down items column-chunk major (c * groups + gi), so that each 64-column
-// chunk of the output is one contiguous run of blocks; shared items token-group major.
+// Item numbering is token-group major for every kind (router: tg * 32 + row block; routed:
+// gi * chunks + c; shared: tg * chunks + c), so that consecutive items of a CTA's range
+// usually share their token group and its staged input rows.
 __device__ __forceinline__ Item decode_item(int T, const Meta& m, int kind, int idx) {
   Item it;
   it.kind = kind;
   it.idx = idx;
   if (kind == KIND_GU || kind == KIND_DN) {
-    int gi;
-    if (kind == KIND_GU) {
-      gi = idx / GU_NCH;
-      it.c = idx % GU_NCH;
-    } else {
-      it.c = idx / m.groups;
-      gi = idx % m.groups;
-    }
+    const int nch = kind == KIND_GU ? GU_NCH : OUT_NCH;
+    const int gi = idx / nch;
+    it.c = idx % nch;
     const int u = find_group_owner(m.tgp, m.U, gi);
     const int tg = gi - m.tgp[u];
     it.e = m.e[u];
@@ -382,6 +378,7 @@ struct Stream {
   int b0, nb;      // this CTA's block range in the current step
   int ring;        // blocks streamed by this CTA before this step (ring position)
   int first_slot;  // trace slot stamped when the step's first block has arrived
+  int x_cls, x_row0;  // what the staged input rows hold (-1: nothing valid)
   uint8_t* sm;
   uint64_t* full;
   uint64_t* empty;
@@ -463,42 +460,47 @@ __device__ void item_epilogue(Stream& S, const Item& it, const float* vals) {
   }
 }
 
-// The combine of output columns [64c, 64c + 64): y = S + sum_j Y[inv(t, j)] in slot order (+x).
-__device__ void combine_chunk(Stream& S, int c) {
-  const Params& p = *S.p;
+// The combine, spread over the grid (all threads): y = S + sum_j Y[inv(t, j)] in slot order
+// (+ x), 8 outputs per thread-step (16-byte stores).
+__device__ void combine_share(const Params& p, const int* inv) {
   const bool residual = (p.flags & 2u) != 0;
-  for (int q = threadIdx.x; q < p.T * 64; q += NCONS) {
-    const int t = q / 64, j = q % 64;
-    const int col = c * 64 + j;
-    float v = __ldcg(p.S + (size_t)t * H + col);
+  const int n8 = p.T * (H / 8);
+  for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < n8; q += gridDim.x * blockDim.x) {
+    const int t = q / (H / 8), col = (q % (H / 8)) * 8;
+    float v[8];
+    const float4* s4 = reinterpret_cast<const float4*>(p.S + (size_t)t * H + col);
+    float4 a = __ldcg(s4), b = __ldcg(s4 + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 #pragma unroll
-    for (int k = 0; k < K; ++k) v += __ldcg(p.Y + (size_t)S.inv[t * K + k] * H + col);
-    if (residual) v += __bfloat162float(p.x[(size_t)t * H + col]);
-    p.y[(size_t)t * H + col] = __float2bfloat16_rn(v);
+    for (int k = 0; k < K; ++k) {
+      const float4* y4 = reinterpret_cast<const float4*>(p.Y + (size_t)inv[t * K + k] * H + col);
+      a = __ldcg(y4);
+      b = __ldcg(y4 + 1);
+      v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w; v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
+    }
+    if (residual) {
+      float f[8];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(p.x + (size_t)t * H + col), f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] += f[i];
+    }
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    *reinterpret_cast<uint4*>(p.y + (size_t)t * H + col) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
-// The CTA owning block b when N blocks are split evenly over n CTAs (b0(g) = N*g/n).
-__device__ __forceinline__ int block_owner(long long b, long long N, int n) {
-  return int(((b + 1) * n - 1) / N);
-}
-
-// This CTA has written all its routed-down rows of chunk c: arrive; the last of the CTAs
-// that cover the chunk's blocks runs the combine of the chunk (consumers only).
-__device__ void arrive_chunk(Stream& S, int c) {
-  const long long N = S.L.n_total;
-  const long long per_chunk = (long long)S.meta.groups * DN_KB;
-  const int g_lo = block_owner(per_chunk * c, N, S.nctas);
-  const int g_hi = block_owner(per_chunk * (c + 1) - 1, N, S.nctas);
-  uint32_t expect = 0;
-  for (int g = g_lo; g <= g_hi; ++g)
-    if (N * (g + 1) / S.nctas > N * g / S.nctas) ++expect;
-  if (ticket_last(S.p->tk_comb + c, expect, S.misc + 11, false)) combine_chunk(S, c);
-  csync();
-}
-
-// Stage the token group's input rows (bf16, row stride xlen + XPAD) for an item (consumers).
+// Stage the token group's input rows (bf16, row stride xlen + XPAD) for an item (consumers),
+// unless they are the rows staged last (same source and group).
 __device__ void stage_inputs(Stream& S, const Item& it, int xlen) {
+  const int cls = it.kind == KIND_GU ? 1 : it.kind == KIND_SD ? 2 : it.kind == KIND_DN ? 3 : 0;
+  if (cls == S.x_cls && it.row0 == S.x_row0) return;
+  S.x_cls = cls;
+  S.x_row0 = it.row0;
   const Params& p = *S.p;
   bf16* xs = reinterpret_cast<bf16*>(S.sm + Smem::xs);
   const int cpr = xlen / 8;
@@ -620,28 +622,22 @@ __device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, i
 
 // Consumers: work through this CTA's range of the step.
 __device__ void consume(Stream& S) {
-  const bool combine = S.L.k_first == KIND_DN;
-  int cur_chunk = -1;
   int j = 0;
   while (j < S.nb) {
     int kind, idx, kb;
     block_kind(S.L, S.b0 + j, kind, idx, kb);
     const Item it = decode_item(S.p->T, S.meta, kind, idx);  // shared-memory lookups only
-    if (combine && it.c != cur_chunk) {
-      if (cur_chunk >= 0) arrive_chunk(S, cur_chunk);
-      cur_chunk = it.c;
-    }
     if (kind == KIND_RT)
       run_router_block(S, it, j);
     else
       run_segment(S, it, kb, min(it.KB - kb, S.nb - j), j);
   }
-  if (combine && cur_chunk >= 0) arrive_chunk(S, cur_chunk);
 }
 
 // One streaming step for the whole CTA: the producer lane streams, the consumers compute.
 __device__ void run_step(Stream& S, const BlockList& L) {
   S.L = L;
+  S.x_cls = -1;  // the staging buffer was reused between steps
   const long long N = L.n_total;
   S.b0 = int(N * blockIdx.x / S.nctas);
   S.nb = int(N * (blockIdx.x + 1) / S.nctas) - S.b0;
@@ -1002,6 +998,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     run_step(S, L);
   }
   trace_point(p, 9);
+  if (!grid_sync(p, ++nbar, S.misc + 12)) return;
+  trace_point(p, 14);
+  // ---- the combine, over the whole grid
+  combine_share(p, inv);
   grid_done(p, S.misc + 13);
   trace_point(p, 10);
 }
