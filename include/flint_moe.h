@@ -135,6 +135,23 @@ flint_moe_status flint_moe_read_trace(flint_moe_t h, unsigned long long* out, in
 /* Releases the handle's host state.  Does not touch the workspace or the weights. */
 flint_moe_status flint_moe_destroy(flint_moe_t h);
 
+/* The whole layer for callers that cannot allocate device memory where they run it (a host
+ * program that owns all device memory and gives plugins no allocator, a runtime that plans
+ * its memory at start-up and allows no allocation later, a latency path that cannot take the
+ * implicit synchronisation of cudaMalloc).  The pages have no counterpart of this call: it is
+ * a property of this library, not of the method.
+ *   w, x, y, topk_idx, topk_w, stream: as for flint_moe_create / flint_moe_forward (no flags:
+ *   no pre-norm, no residual); 1 <= T <= 4, a larger T returns FLINT_MOE_ERR_UNSUPPORTED.
+ * Scratch memory comes from one fixed array of 26 MiB that the library declares in device
+ * memory; every GPU that loads the library holds it until the process exits.  The call makes
+ * no allocation.  The first call on a device (with that device current) looks up the array's
+ * device address and sets the kernel's shared-memory limit; make that first call before any
+ * stream capture.  All calls on a device share the array, and it keeps the last call's
+ * contents: the counters that must start at zero are cleared on `stream` at the start of each
+ * call, and calls whose work overlaps on the GPU race on the array. */
+flint_moe_status flint_moe_forward_noalloc(const flint_moe_weights* w, const void* x, int T, void* y,
+                                           int32_t* topk_idx, float* topk_w, flint_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,7 +23,9 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "
 EXPORTS = ("flint_moe_status_string", "flint_moe_workspace_bytes", "flint_moe_create", "flint_moe_route",
            "flint_moe_forward", "flint_moe_forward_host", "flint_moe_poll_device_status",
            "flint_moe_enable_kernel_timing", "flint_moe_kernel_times", "flint_moe_read_trace",
-           "flint_moe_destroy")
+           "flint_moe_destroy", "flint_moe_forward_noalloc")
+
+NOALLOC_MAX_TOKENS = 4
 
 
 class FlintMoEError(RuntimeError):
@@ -75,6 +77,7 @@ def load_library():
                                          ctypes.POINTER(I32)]
     L.flint_moe_read_trace.argtypes = [P, ctypes.POINTER(ctypes.c_ulonglong), I32, ctypes.POINTER(I32)]
     L.flint_moe_destroy.argtypes = [P]
+    L.flint_moe_forward_noalloc.argtypes = [ctypes.POINTER(_Weights), P, I32, P, P, P, P]
     for name in EXPORTS:
         if name != "flint_moe_status_string":
             getattr(L, name).restype = I32
@@ -103,6 +106,22 @@ def workspace_bytes(max_tokens: int, flags: int = 0, rms_eps: float = 1e-6) -> i
     n = ctypes.c_size_t(0)
     _check(L.flint_moe_workspace_bytes(ctypes.byref(cfg), ctypes.byref(n)), "flint_moe_workspace_bytes")
     return n.value
+
+
+def forward_noalloc(weights: dict, x, y=None, topk_idx=None, topk_w=None, stream=None):
+    """The whole layer through flint_moe_forward_noalloc: no workspace, no allocation by the
+    library (for callers that cannot allocate device memory where they run the layer).
+    1 <= T <= NOALLOC_MAX_TOKENS; ``weights`` as for :class:`FlintMoE`.  ``y`` is allocated
+    here by torch when not given, which is the caller's choice, not the library's."""
+    import torch
+    L = load_library()
+    T = x.shape[0]
+    if y is None:
+        y = torch.empty_like(x)
+    w = _Weights(*[(weights[n].data_ptr() if weights.get(n) is not None else None) for n, _ in _Weights._fields_])
+    _check(L.flint_moe_forward_noalloc(ctypes.byref(w), _ptr(x), T, _ptr(y), _ptr(topk_idx), _ptr(topk_w),
+                                       _stream_ptr(stream)), "flint_moe_forward_noalloc")
+    return y
 
 
 class FlintMoE:

@@ -5,6 +5,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "../../include/flint_moe.h"
@@ -429,3 +430,103 @@ flint_moe_status flint_moe_destroy(flint_moe_t h) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------------
+// Allocation-free forward.
+//
+// Some callers cannot allocate device memory at the point where they run the layer: a host
+// application that owns every byte of device memory and hands plugins no allocator, a runtime
+// that plans all of its memory at start-up and forbids allocation afterwards, or a latency
+// path that cannot afford the implicit synchronisation of cudaMalloc.  For them this entry
+// point takes its scratch space from one fixed array in device memory that the library
+// declares itself, so the caller supplies only the weights, the input and the output.
+//
+// The array (26 MiB) holds the workspace of a handle with max_tokens = NOALLOC_MAX_T.
+// Every GPU that loads the library reserves it until the process exits.  All calls on a
+// device share it: calls whose work overlaps on the GPU (on different streams, or from
+// different threads) race on it and must be serialised by the caller.  The counters that must
+// start at zero are cleared on the caller's stream at the start of every call.
+namespace {
+
+constexpr int NOALLOC_MAX_T = 4;
+constexpr size_t NOALLOC_BYTES = size_t(26) << 20;
+constexpr int NOALLOC_MAX_DEVICES = 64;
+
+__device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_BYTES];
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[NOALLOC_MAX_DEVICES];
+int g_noalloc_sms[NOALLOC_MAX_DEVICES];
+
+// First call on a device (with that device current): the device address of the array and the
+// kernel's shared-memory limit.  Later calls reuse them.
+flint_moe_status noalloc_setup(int dev, void** ptr, int* n_sm) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return FLINT_MOE_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+      return FLINT_MOE_ERR_CUDA;
+    if (cudaFuncSetAttribute(decode_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, FUSED_SMEM) !=
+        cudaSuccess)
+      return FLINT_MOE_ERR_CUDA;
+    g_noalloc_sms[dev] = sms;
+    g_noalloc_ptr[dev] = p;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  *n_sm = g_noalloc_sms[dev];
+  return FLINT_MOE_OK;
+}
+
+}  // namespace
+
+extern "C" flint_moe_status flint_moe_forward_noalloc(const flint_moe_weights* w, const void* x, int T, void* y,
+                                                      int32_t* topk_idx, float* topk_w, flint_stream_t stream) {
+  if (!w || !w->w_router || !w->w_gate || !w->w_up || !w->w_down || !w->ws_gate || !w->ws_up || !w->ws_down)
+    return FLINT_MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {w->w_router, w->w_gate, w->w_up, w->w_down, w->ws_gate, w->ws_up, w->ws_down, x, y};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return FLINT_MOE_ERR_INVALID_ARG;
+  if (w->router_bias && (reinterpret_cast<uintptr_t>(w->router_bias) & 3u)) return FLINT_MOE_ERR_INVALID_ARG;
+  if (T < 1) return FLINT_MOE_ERR_INVALID_ARG;
+  if (T > NOALLOC_MAX_T) return FLINT_MOE_ERR_UNSUPPORTED;  // beyond the fixed scratch array
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= NOALLOC_MAX_DEVICES) return FLINT_MOE_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return FLINT_MOE_ERR_CUDA;
+  if (major != 10 || minor != 3) return FLINT_MOE_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  int n_sm = 0;
+  flint_moe_status s = noalloc_setup(dev, &scratch, &n_sm);
+  if (s != FLINT_MOE_OK) return s;
+
+  flint_moe_s h{};  // a handle on the stack: no host or device allocation
+  h.cfg = flint_moe_config{H, E, K, I, IS, NOALLOC_MAX_T, 0u, 1e-6f};
+  h.w = *w;
+  h.device = dev;
+  h.n_sm = n_sm;
+  h.ws = static_cast<uint8_t*>(scratch);
+  h.L = make_layout(NOALLOC_MAX_T);
+  if (h.L.total > NOALLOC_BYTES) return FLINT_MOE_ERR_WORKSPACE;
+  h.ws_bytes = NOALLOC_BYTES;
+  h.prefetch_max = 40ull << 20;
+  h.timing = false;
+  h.trace = false;
+  h.n_ev = 0;
+  const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  const bool ok = make_map(&h.smaps.wr, w->w_router, H, E, 64, RT_ROWS, sw) &&
+                  make_map(&h.smaps.wg, w->w_gate, (uint64_t)E * H, I, 64, GU_ROWS, sw) &&
+                  make_map(&h.smaps.wu, w->w_up, (uint64_t)E * H, I, 64, GU_ROWS, sw) &&
+                  make_map(&h.smaps.wd, w->w_down, (uint64_t)E * I, H, 64, DN_ROWS, sw) &&
+                  make_map(&h.smaps.wsg, w->ws_gate, H, IS, 64, GU_ROWS, sw) &&
+                  make_map(&h.smaps.wsu, w->ws_up, H, IS, 64, GU_ROWS, sw) &&
+                  make_map(&h.smaps.wsd, w->ws_down, IS, H, 64, DN_ROWS, sw);
+  if (!ok) return FLINT_MOE_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // status word, tickets and barrier counters start at zero on every call
+  if (cudaMemsetAsync(h.ws, 0, h.L.n_touched, st) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  Params p = make_params(&h, x, T, y, topk_idx, topk_w, nullptr);
+  return run_decode(&h, p, st, true);
+}
