@@ -35,6 +35,36 @@ SWEEP = (1, 2, 4, 8, 16, 32, 64)
 METRIC = "MoE-layer tokens/s on 1 B300; HBM GB/s (decode) / tensor TFLOPS (prefill) vs peak"
 
 
+KERNEL_SOURCES = ("sparse_moe_layer_15_b300/csrc/decode_fused.cuh", "sparse_moe_layer_15_b300/csrc/common.cuh",
+                  "sparse_moe_layer_15_b300/csrc/flint_moe.cu")
+
+
+def kernel_sources_sha256():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel, sweep):
+    """DRAM bytes per launch of `kernel` averaged over the sweep, from the committed ncu
+    summary profiles/decode_fused_traffic.json, or None when the kernel sources have changed
+    since the counters were taken (or no summary exists)."""
+    path = os.path.join(ROOT, "profiles", "decode_fused_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("kernel") != kernel or rec.get("sources_sha256") != kernel_sources_sha256():
+        return None
+    per = rec["dram_bytes_per_launch"]
+    if not all(str(T) in per for T in sweep):
+        return None
+    return round(sum(per[str(T)] for T in sweep) / len(sweep))
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -226,22 +256,18 @@ def run_ours(args, rank, world, local):
     # dominant kernel: largest summed time over the sweep
     dom = max(kt, key=lambda n: sum(statistics.mean(v) for v in kt[n].values()))
 
-    def kernel_bytes(name, T):
-        u = U[T]
-        if name.startswith("stream_k1"):
-            return 2 * (fm.HIDDEN * fm.N_EXPERTS + 2 * fm.HIDDEN * fm.SHARED_INTER) + 2 * fm.HIDDEN * T
-        if name.startswith("stream_k2"):
-            return 2 * (u * 2 * fm.HIDDEN * fm.EXPERT_INTER + fm.SHARED_INTER * fm.HIDDEN)
-        if name.startswith("stream_k3"):
-            return 2 * (u * fm.EXPERT_INTER * fm.HIDDEN) + 2 * fm.HIDDEN * T
-        return 2 * 2 * fm.HIDDEN * T
-
-    dom_bytes = sum(kernel_bytes(dom, T) for T in SWEEP) / len(SWEEP)
+    # The decode kernel runs the whole layer: its algorithmic bytes per launch are the layer's
+    # (touched experts x 6 MB + shared 12 MB + router 1 MB + bf16 x and y); averaged over the
+    # sweep's launches (one per T).
+    dom_bytes = sum(acc.algorithmic_bytes(U[T], T) for T in SWEEP) / len(SWEEP)
     dom_ms = sum(statistics.mean(kt[dom][T]) for T in SWEEP) / len(SWEEP)
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    traffic = measured_traffic(dom, SWEEP)
     roofline = dict(bound="hbm", kernel=dom, achieved=round(achieved, 1), peak=peaks["hbm_gbs"], unit="GB/s",
-                    frac=round(achieved / peaks["hbm_gbs"], 4), traffic=None,
-                    peak_source=peaks["source"], note="per-launch mean over the sweep's T values")
+                    frac=round(achieved / peaks["hbm_gbs"], 4), traffic=traffic,
+                    alg_bytes_per_launch=round(dom_bytes), peak_source=peaks["source"] + " (hbm_gbs, copy test)",
+                    note="per-launch means over the sweep's 7 launches; traffic: DRAM read+write bytes per "
+                         "launch from the committed ncu summary (null if the kernel sources changed since)")
 
     # end to end through the C ABI with host buffers (H2D of x and D2H of y inside the span)
     xh = {T: xs[T].cpu().pin_memory() for T in SWEEP}
@@ -270,7 +296,7 @@ def run_ours(args, rank, world, local):
                            tokens_per_step=tokens_step, parallelism=f"replicas x{world}",
                            l2="flushed (512 MB write) before every forward"),
                sweep=sweep, kernels_us=kernels, roofline=roofline, e2e=e2e,
-               gpu_launches=args.steps * len(SWEEP) * 3, clocks=clk, wall_s=round(wall, 3))
+               gpu_launches=args.steps * len(SWEEP), clocks=clk, wall_s=round(wall, 3))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, xs, budget_s=args.cpu_budget)
     layer.close()
