@@ -91,7 +91,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// Row-major bf16 matrix [rows][cols] -> 2-D tensor map with a box of box_cols x box_rows.
+// Row-major bf16 matrix [rows][cols] -> 2-D tensor map with a box of box_cols x box_rows.  L2
+// fills are promoted to 128 bytes only: a box row is 128 bytes, and a wider promotion would
+// fetch the neighbouring columns, which are read much later (by then evicted) when the stream
+// is larger than L2.
 bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
               uint32_t box_rows, CUtensorMapSwizzle swz) {
   auto enc = tensor_map_encoder();
@@ -101,7 +104,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
