@@ -1,0 +1,241 @@
+// Tensor-core GEMM engine for sm_103a: tcgen05.mma with accumulators in TMEM, operands staged
+// in shared memory by TMA, one persistent CTA per SM.
+//
+// A tile computes D[128 x 256] += A[128 x K] * B[K x 256] in bf16 with fp32 accumulation:
+//   A: K-major (rows of A are contiguous in K), TMA box 64 (K) x 128 (rows), 128-byte swizzle;
+//   B: N-major (rows of B are contiguous in N, i.e. the weight matrices in y = x W order), four
+//      TMA boxes of 64 (N) x 64 (K rows) per stage, 128-byte swizzle -- each box may come from
+//      its own tensor map and column, so a tile can pair two matrices (gate | up);
+//   D: 256 fp32 TMEM columns; two buffers, so the epilogue of one tile overlaps the main loop
+//      of the next.
+// Warp roles: warp 0 issues TMA (one lane), warp 1 allocates TMEM and issues the MMAs (one
+// lane), warps 2-5 run the epilogue (warp w reads TMEM lanes 32*(w%4) .. +31, one row each).
+// Every wait is bounded (1 s); on expiry the device status word gets ST_TIMEOUT and the
+// kernel runs to its end without hanging; TMEM is always released.
+//
+// A Problem class supplies the tile list and the epilogue:
+//   int num_tiles() const;  int kblocks() const;
+//   void tile(int i, TileInfo& t) const;       // operand coordinates of tile i
+//   void epilogue(const TileInfo& t, uint32_t tmem_row, int row, uint8_t* smem) const;
+//        called by each epilogue thread for its tile row `row` (0..127); tmem_row addresses
+//        column 0 of that row's accumulator (load with tmem_ld32)
+//   uint32_t* status() const;
+#pragma once
+
+#include "common.cuh"
+
+namespace flint {
+namespace tc {
+
+constexpr int TM = 128;
+constexpr int TN = 256;
+constexpr int TK = 64;
+constexpr int KSTEP = 16;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = TM * TK * 2;            // 16 KB
+constexpr int B_CHUNK = TK * 64 * 2;            // 8 KB: 64 K rows x 64 columns
+constexpr int B_BYTES = 4 * B_CHUNK;            // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int EPI_SMEM = 2048;  // per-CTA scratch handed to the epilogue
+
+// kind::f16 instruction descriptor: D fp32, A and B bf16, A K-major, B MN-major, N = 256,
+// M = 128.
+constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
+                           (uint32_t(TN >> 3) << 17) | (uint32_t(TM >> 4) << 24);
+
+struct Smem {
+  static constexpr int stages = 0;
+  static constexpr int full = stages + STAGES * STAGE_BYTES;
+  static constexpr int empty = full + 8 * STAGES;
+  static constexpr int tfull = empty + 8 * STAGES;
+  static constexpr int tempty = tfull + 16;
+  static constexpr int tmem_slot = tempty + 16;
+  static constexpr int epi = tmem_slot + 16;
+  static constexpr int bytes = epi + EPI_SMEM;
+};
+constexpr int SMEM_BYTES = Smem::bytes + 1024;
+
+struct TileInfo {
+  int a_row0;               // first A row (TMA coordinate)
+  int b_row0;               // first B row (K offset of the B matrix in its tensor map)
+  const CUtensorMap* bmap[4];
+  int bcol[4];              // column (N) coordinate of each of the four B boxes
+  int row0;                 // problem-specific: first output row
+  int valid;                // rows of this tile that are real
+  int col0;                 // problem-specific: first output column
+  int aux;                  // problem-specific
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return uint64_t((saddr >> 4) & 0x3FFFu) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
+         (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this thread's TMEM lane (warp-collective).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Bounded mbarrier wait (one thread); records ST_TIMEOUT and returns false on expiry.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, uint32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+      record_status(status, ST_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* raw) {
+  const uint32_t a = smem_u32(raw);
+  return raw + ((1024u - (a & 1023u)) & 1023u);
+}
+
+// ------------------------------------------------------------------ the kernel
+template <class Problem>
+__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_constant__ Problem prob) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + Smem::full);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(sm + Smem::empty);
+  uint64_t* tfull = reinterpret_cast<uint64_t*>(sm + Smem::tfull);
+  uint64_t* tempty = reinterpret_cast<uint64_t*>(sm + Smem::tempty);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Smem::tmem_slot);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t* status = prob.status();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull + b, 1);
+      mbar_init(tempty + b, 4);  // one arrival per epilogue warp
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
+
+  const int ntiles = prob.num_tiles();
+  const int kb_n = prob.kblocks();
+
+  if (warp == 0) {
+    // ---------------- TMA producer
+    if (lane == 0) {
+      int pos = 0;
+      for (int i = blockIdx.x; i < ntiles; i += gridDim.x) {
+        TileInfo t;
+        prob.tile(i, t);
+        for (int kb = 0; kb < kb_n; ++kb, ++pos) {
+          const int st = pos % STAGES, use = pos / STAGES;
+          if (use > 0) wait_bar(empty + st, uint32_t(use - 1) & 1u, status);
+          uint8_t* a = sm + Smem::stages + st * STAGE_BYTES;
+          uint8_t* b = a + A_BYTES;
+          mbar_arrive_expect_tx(full + st, STAGE_BYTES);
+          tma_load_2d(a, prob.amap(), kb * TK, t.a_row0, full + st);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tma_load_2d(b + c * B_CHUNK, t.bmap[c], t.bcol[c], t.b_row0 + kb * TK, full + st);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      int pos = 0, it = 0;
+      for (int i = blockIdx.x; i < ntiles; i += gridDim.x, ++it) {
+        const int buf = it & 1, use = it >> 1;
+        if (use > 0) wait_bar(tempty + buf, uint32_t(use - 1) & 1u, status);
+        tc_fence_after();
+        const uint32_t d = tmem_base + uint32_t(buf * TN);
+        for (int kb = 0; kb < kb_n; ++kb, ++pos) {
+          const int st = pos % STAGES;
+          wait_bar(full + st, uint32_t(pos / STAGES) & 1u, status);
+          tc_fence_after();
+          const uint32_t a = smem_u32(sm + Smem::stages + st * STAGE_BYTES);
+          const uint32_t b = a + A_BYTES;
+#pragma unroll
+          for (int s = 0; s < TK / KSTEP; ++s) {
+            const uint64_t ad = smem_desc(a + s * (KSTEP * 2), 16, 1024);
+            const uint64_t bd = smem_desc(b + s * (KSTEP * 128), B_CHUNK, 1024);
+            mma_bf16(d, ad, bd, (kb | s) != 0 ? 1u : 0u);
+          }
+          mma_commit(empty + st);  // the stage is free once these MMAs have read it
+        }
+        mma_commit(tfull + buf);  // the accumulator is complete
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5)
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    int it = 0;
+    for (int i = blockIdx.x; i < ntiles; i += gridDim.x, ++it) {
+      const int buf = it & 1;
+      if (lane == 0) wait_bar(tfull + buf, uint32_t(it >> 1) & 1u, status);
+      __syncwarp();
+      while (!mbar_try_wait(tfull + buf, uint32_t(it >> 1) & 1u)) {
+        if (*reinterpret_cast<volatile uint32_t*>(status) & ST_TIMEOUT) break;
+      }
+      tc_fence_after();
+      TileInfo t;
+      prob.tile(i, t);
+      const uint32_t trow = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(buf * TN);
+      prob.epilogue(t, trow, row, sm + Smem::epi);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty + buf);
+    }
+  }
+  // wait for the last accumulators to be consumed, then release TMEM
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
+}
+
+}  // namespace tc
+}  // namespace flint
