@@ -65,6 +65,11 @@ struct Params {
   float* P_sd;
   float* P_dn;
   float* RP;             // [32][256][E] router partial logits (decode path)
+  bf16* xs;              // [T*K][H] expert-sorted input rows (prefill path)
+  bf16* Yb;              // [T*K][H] gated routed expert outputs, bf16 (prefill path)
+  int32_t* hist;         // [T/128][E] per-tile expert histogram (prefill path)
+  int32_t* hbase;        // [T/128][E] rows of expert e taken by earlier tiles (prefill path)
+  int32_t* mtp;          // [E+1] 128-row tile prefix over experts (prefill path)
   uint32_t* bar_count;   // [1] grid-barrier counter (decode path; reset at kernel end)
   uint32_t* bar_done;    // [1]
   uint32_t* tk_router;   // [1] tickets (zero between kernels: the last arriver resets)

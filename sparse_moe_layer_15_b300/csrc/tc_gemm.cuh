@@ -14,11 +14,15 @@
 // kernel runs to its end without hanging; TMEM is always released.
 //
 // A Problem class supplies the tile list and the epilogue:
-//   int num_tiles() const;  int kblocks() const;
-//   void tile(int i, TileInfo& t) const;       // operand coordinates of tile i
-//   void epilogue(const TileInfo& t, uint32_t tmem_row, int row, uint8_t* smem) const;
+//   void prologue(uint8_t* tbl) const;          // all threads, once: fill the table region
+//   int num_tiles(const uint8_t* tbl) const;  int kblocks() const;
+//   void tile(int i, TileInfo& t, const uint8_t* tbl) const;  // operand maps and coordinates
+//   void epilogue(const TileInfo& t, uint32_t tmem_row, int row, uint8_t* epi,
+//                 const uint8_t* tbl) const;
 //        called by each epilogue thread for its tile row `row` (0..127); tmem_row addresses
-//        column 0 of that row's accumulator (load with tmem_ld32)
+//        column 0 of that row's accumulator (load with tmem_ld32, warp-collective, so every
+//        lane loads before any lane branches on its row); epi_sync() synchronises the 128
+//        epilogue threads
 //   uint32_t* status() const;
 #pragma once
 
@@ -39,6 +43,7 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int EPI_SMEM = 2048;  // per-CTA scratch handed to the epilogue
+constexpr int TBL_SMEM = 4096;  // per-CTA table filled by the problem's prologue
 
 // kind::f16 instruction descriptor: D fp32, A and B bf16, A K-major, B MN-major, N = 256,
 // M = 128.
@@ -53,11 +58,13 @@ struct Smem {
   static constexpr int tempty = tfull + 16;
   static constexpr int tmem_slot = tempty + 16;
   static constexpr int epi = tmem_slot + 16;
-  static constexpr int bytes = epi + EPI_SMEM;
+  static constexpr int tbl = epi + EPI_SMEM;
+  static constexpr int bytes = tbl + TBL_SMEM;
 };
 constexpr int SMEM_BYTES = Smem::bytes + 1024;
 
 struct TileInfo {
+  const CUtensorMap* amap;  // A operand
   int a_row0;               // first A row (TMA coordinate)
   int b_row0;               // first B row (K offset of the B matrix in its tensor map)
   const CUtensorMap* bmap[4];
@@ -118,6 +125,9 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, uint32_
   return true;
 }
 
+// Barrier among the four epilogue warps (128 threads).
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
 __device__ __forceinline__ uint8_t* align1024(uint8_t* raw) {
   const uint32_t a = smem_u32(raw);
   return raw + ((1024u - (a & 1023u)) & 1023u);
@@ -153,13 +163,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  pdl_launch_dependents();
+  pdl_wait();
+  uint8_t* tbl = sm + Smem::tbl;
+  prob.prologue(tbl);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  pdl_wait();
 
-  const int ntiles = prob.num_tiles();
+  const int ntiles = prob.num_tiles(tbl);
   const int kb_n = prob.kblocks();
 
   if (warp == 0) {
@@ -168,14 +181,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       int pos = 0;
       for (int i = blockIdx.x; i < ntiles; i += gridDim.x) {
         TileInfo t;
-        prob.tile(i, t);
+        prob.tile(i, t, tbl);
         for (int kb = 0; kb < kb_n; ++kb, ++pos) {
           const int st = pos % STAGES, use = pos / STAGES;
           if (use > 0) wait_bar(empty + st, uint32_t(use - 1) & 1u, status);
           uint8_t* a = sm + Smem::stages + st * STAGE_BYTES;
           uint8_t* b = a + A_BYTES;
           mbar_arrive_expect_tx(full + st, STAGE_BYTES);
-          tma_load_2d(a, prob.amap(), kb * TK, t.a_row0, full + st);
+          tma_load_2d(a, t.amap, kb * TK, t.a_row0, full + st);
 #pragma unroll
           for (int c = 0; c < 4; ++c) tma_load_2d(b + c * B_CHUNK, t.bmap[c], t.bcol[c], t.b_row0 + kb * TK, full + st);
         }
@@ -221,9 +234,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       }
       tc_fence_after();
       TileInfo t;
-      prob.tile(i, t);
+      prob.tile(i, t, tbl);
       const uint32_t trow = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(buf * TN);
-      prob.epilogue(t, trow, row, sm + Smem::epi);
+      prob.epilogue(t, trow, row, sm + Smem::epi, tbl);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty + buf);

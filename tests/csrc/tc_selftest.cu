@@ -13,13 +13,14 @@ struct TestGemm {
   float* D;
   int M, N, K;
   uint32_t* st;
-  __device__ int num_tiles() const { return ((M + TM - 1) / TM) * (N / TN); }
+  __device__ void prologue(uint8_t*) const {}
+  __device__ int num_tiles(const uint8_t*) const { return ((M + TM - 1) / TM) * (N / TN); }
   __device__ int kblocks() const { return K / TK; }
-  __device__ const CUtensorMap* amap() const { return &a; }
   __device__ uint32_t* status() const { return st; }
-  __device__ void tile(int i, TileInfo& t) const {
+  __device__ void tile(int i, TileInfo& t, const uint8_t*) const {
     const int nt = N / TN;
     const int mt = i / nt, ntile = i % nt;
+    t.amap = &a;
     t.a_row0 = mt * TM;
     t.b_row0 = 0;
     for (int c = 0; c < 4; ++c) {
@@ -31,7 +32,7 @@ struct TestGemm {
     t.col0 = ntile * TN;
     t.aux = 0;
   }
-  __device__ void epilogue(const TileInfo& t, uint32_t trow, int row, uint8_t*) const {
+  __device__ void epilogue(const TileInfo& t, uint32_t trow, int row, uint8_t*, const uint8_t*) const {
 #pragma unroll 1
     for (int c = 0; c < TN / 32; ++c) {
       float v[32];

@@ -132,6 +132,46 @@ def compare(ref, y, idx, gw, counts=None, full_T=None):
     return rep
 
 
+def check_routing_all(w, x, idx_gpu, gw_gpu, eps=None):
+    """The routing rule on every token (oracle fp64 scores of all tokens; no expert weights
+    needed).  Returns a report with the mismatches, the exempt count and the oracle counts."""
+    x64 = oracle.bf16_to_f64(to_np_bf16(x))
+    xin = x64 if eps is None else oracle.prenorm_input(x64, eps)
+    wr = to_np_bf16(w["w_router"])
+    b = None if w.get("router_bias") is None else w["router_bias"].detach().float().cpu().numpy()
+    _, s = oracle.router(xin, wr, b)
+    idx_r, g_r, gaps = oracle.select(s, 6)
+    idx_g = idx_gpu.detach().cpu().numpy()
+    w_g = gw_gpu.detach().cpu().numpy().astype(np.float64)
+    exempt = gaps[:, 5] <= GAP
+    set_mm, order_err, tie_err = [], [], []
+    gate_err = 0.0
+    for t in range(idx_r.shape[0]):
+        same = set(idx_g[t].tolist()) == set(idx_r[t].tolist())
+        if not same:
+            if not exempt[t]:
+                set_mm.append(t)
+            continue
+        a = 0
+        for j in range(6):
+            if j == 5 or gaps[t, j] > GAP:
+                if set(idx_g[t, a:j + 1].tolist()) != set(idx_r[t, a:j + 1].tolist()):
+                    order_err.append(t)
+                    break
+                a = j + 1
+        for j in range(5):
+            if gaps[t, j] == 0.0 and (idx_g[t, j], idx_g[t, j + 1]) != (idx_r[t, j], idx_r[t, j + 1]):
+                tie_err.append(t)
+        sg = dict(zip(idx_g[t].tolist(), w_g[t].tolist()))
+        for e, g in zip(idx_r[t].tolist(), g_r[t].tolist()):
+            gate_err = max(gate_err, abs(sg[e] - g))
+    rep = dict(n=int(idx_r.shape[0]), n_exempt=int(exempt.sum()), set_mismatch=set_mm[:10], n_set_mismatch=len(set_mm),
+               order_err=order_err[:10], tie_err=tie_err[:10], gate_err=gate_err,
+               oracle_counts=np.bincount(idx_r.reshape(-1), minlength=256), exempt_any=bool(exempt.any()))
+    rep["ok"] = not set_mm and not order_err and not tie_err and gate_err <= GATE_TOL
+    return rep
+
+
 def check_counts(ref_all, idx_gpu, counts_gpu):
     """Counts: exactly the oracle's when no token is exempt; in general exactly the counts
     of the GPU's own choices, which must agree with the oracle's on every non-exempt token
