@@ -49,7 +49,8 @@ def sample(T, n=48):
 
 
 def assert_ok(rep):
-    assert rep["ok"], {k: v for k, v in rep.items() if k not in ("oracle_counts",)}
+    msg = " ".join(f"{k}={v}" for k, v in rep.items() if k not in ("oracle_counts",))
+    assert rep["ok"], msg
 
 
 @pytest.mark.parametrize("T", [257, 300, 1000])
