@@ -106,10 +106,11 @@ def test_adversarial_workload_T16384_ties_and_cold_experts():
     rep = parity.check_routing_all(w, x, idx, gw)
     assert_ok(rep)
     # duplicated hot columns tie exactly: whenever both are chosen the lower index comes first
+    # (an expert whose fp32 score equals theirs may sit between them)
     a, b = sorted((hot[0], hot[1]))
     rows = idx.cpu().numpy()
     both = [(r.tolist().index(a), r.tolist().index(b)) for r in rows if a in r and b in r]
-    assert both and all(ia + 1 == ib for ia, ib in both)
+    assert both and all(ia < ib for ia, ib in both)
     ref = parity.oracle_reference(w, x, sample(16384, 48))
     assert_ok(parity.compare(ref, y, idx, gw))
     layer.close()
