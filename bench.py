@@ -303,7 +303,252 @@ def run_ours(args, rank, world, local):
     return out
 
 
+# ----------------------------------------------------------------------------- other workloads
+
+WORKLOADS = {
+    "single": dict(T=16, seed_x=0, bias=None, bias_seed=None,
+                   desc="single Flint MoE layer, T=16 tokens, seed 0 (x seed 0)"),
+    "prefill": dict(T=8192, seed_x=3, bias="normal", bias_seed=3,
+                    desc="prefill: one Flint MoE layer, T=8192, router bias ~N(0, 0.5) (seed 3), x seed 3"),
+    "adversarial": dict(T=16384, seed_x=5, bias="adversarial", bias_seed=5,
+                        desc="adversarial: one Flint MoE layer, T=16384, router bias +8 on 8 hot / -8 on 200 cold "
+                             "experts, duplicated router columns (exact ties), x seed 5"),
+}
+
+# Algorithmic FLOPs per token of each prefill kernel (2 per multiply-add).
+PF_KERNEL_FLOPS_PER_TOKEN = {
+    "pf_router": 2 * 2048 * 256,
+    "pf_gateup": 6 * 2 * 2 * 2048 * 512 + 2 * 2 * 2048 * 1024,
+    "pf_down": 6 * 2 * 512 * 2048,
+    "pf_shared_down_combine": 2 * 1024 * 2048,
+}
+
+
+def timed_loop(fn, steps, flush, stream, ev):
+    import torch
+    out = []
+    for _ in range(steps):
+        if flush:
+            flush()
+        a, b = ev
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        out.append(a.elapsed_time(b))
+    return out
+
+
+def run_workload(args, rank, world, local):
+    """One workload other than the decode sweep: a step is one forward of T tokens (the
+    47-layer stack: 47 pre-norm residual forwards of T=256 tokens)."""
+    import torch
+
+    import synth
+    import sparse_moe_layer_15_b300 as fm
+    from sparse_moe_layer_15_b300 import accounting as acc
+
+    if args.workload == "stack":
+        return run_stack(args, rank, world, local)
+    cfg = WORKLOADS[args.workload]
+    T = cfg["T"]
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    w = synth.flint_weights(seed=0, device=dev, bias=cfg["bias"], bias_seed=cfg["bias_seed"])
+    layer = fm.FlintMoE(w, max_tokens=T)
+    x = synth.torch_normal_bf16((T, fm.HIDDEN), cfg["seed_x"], synth.TAG_X, 1.0, device=dev)
+    y = torch.empty_like(x)
+    idx = torch.empty((T, fm.TOP_K), dtype=torch.int32, device=dev)
+    gw = torch.empty((T, fm.TOP_K), dtype=torch.float32, device=dev)
+    ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+
+    def fwd():
+        layer.forward(x, y=y, topk_idx=idx, topk_w=gw)
+
+    timed_loop(fwd, args.warmup, flush, stream, ev)
+    _, _, c = layer.route(x)
+    torch.cuda.synchronize()
+    counts = c.cpu().numpy()
+    U = int((counts > 0).sum())
+    clocks = ClockSampler(local)
+    clocks.start()
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < 1.5:
+        timed_loop(fwd, 1, flush, stream, ev)
+    barrier(world)
+    times = timed_loop(fwd, args.steps, flush, stream, ev)
+    clk = clocks.stop()
+    barrier(world)
+    if layer.poll_device_status() != 0:
+        raise RuntimeError("device status error in the timed region")
+    ms = max_over_ranks(statistics.mean(times), world)
+    value = world * T / (ms * 1e-3)
+    flop = acc.flops_per_token() * T
+    alg_bytes = acc.algorithmic_bytes(U, T)
+    # per-kernel times (second pass with kernel events)
+    layer.enable_kernel_timing(True)
+    kt = {}
+    for _ in range(max(3, min(args.steps, 10))):
+        flush()
+        fwd()
+        for name, kms in layer.kernel_times():
+            kt.setdefault(name, []).append(kms)
+    layer.enable_kernel_timing(False)
+    kernels = {k: round(statistics.median(v) * 1e3, 2) for k, v in kt.items()}
+    dom = max(kt, key=lambda n: statistics.mean(kt[n]))
+    dom_ms = statistics.mean(kt[dom])
+    if dom in PF_KERNEL_FLOPS_PER_TOKEN:
+        achieved = PF_KERNEL_FLOPS_PER_TOKEN[dom] * T / (dom_ms * 1e-3) / 1e12
+        roofline = dict(bound="tensor", kernel=dom, achieved=round(achieved, 1), peak=peaks["bf16_tflops"],
+                        unit="TFLOP/s", frac=round(achieved / peaks["bf16_tflops"], 4), traffic=None,
+                        alg_flop_per_launch=PF_KERNEL_FLOPS_PER_TOKEN[dom] * T,
+                        peak_source=peaks["source"] + " (bf16_tflops, burst)",
+                        note="algorithmic FLOPs of the kernel (no tile padding) / its CUDA-event time")
+    else:
+        achieved = alg_bytes / (dom_ms * 1e-3) / 1e9
+        roofline = dict(bound="hbm", kernel=dom, achieved=round(achieved, 1), peak=peaks["hbm_gbs"], unit="GB/s",
+                        frac=round(achieved / peaks["hbm_gbs"], 4), traffic=None, alg_bytes_per_launch=alg_bytes,
+                        peak_source=peaks["source"] + " (hbm_gbs, copy test)")
+    # end to end with host buffers
+    xh = x.cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    e2e_t = timed_loop(lambda: layer.forward_host(xh, yh), args.warmup + args.steps, flush, stream, ev)[args.warmup:]
+    e2e_ms = max_over_ranks(statistics.mean(e2e_t), world)
+    t_roof_ms = max(alg_bytes / (peaks["hbm_gbs"] * 1e9), flop / (peaks["bf16_tflops"] * 1e12)) * 1e3
+    out = dict(metric=METRIC, value=round(value, 1), unit="tokens/s", n_gpus=world, steps=args.steps,
+               warmup=args.warmup, ms_per_step=round(ms, 4), higher_is_better=True, scaling="weak",
+               vs_baseline=None, dtype="bf16", data="synthetic",
+               config=dict(workload=cfg["desc"], tokens_per_step=T, parallelism=f"replicas x{world}",
+                           l2="flushed (512 MB write) before every forward"),
+               layer=dict(touched_experts=U, alg_bytes=alg_bytes, alg_flop=flop,
+                          tflops=round(flop / (ms * 1e-3) / 1e12, 1), gbs=round(alg_bytes / (ms * 1e-3) / 1e9, 1),
+                          roofline_ms=round(t_roof_ms, 4), roofline_frac=round(t_roof_ms / ms, 4),
+                          hot_share=(round(float(np.sort(counts)[::-1][:8].sum() / counts.sum()), 4)
+                                     if args.workload == "adversarial" else None)),
+               kernels_us=kernels, roofline=roofline,
+               e2e=dict(value=round(world * T / (e2e_ms * 1e-3), 1), unit="tokens/s",
+                        h2d_bytes_per_step=2 * fm.HIDDEN * T, d2h_bytes_per_step=2 * fm.HIDDEN * T),
+               gpu_launches=args.steps * len(kernels), clocks=clk)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline_tokens(w, x, n=16, what=args.workload)
+    layer.close()
+    return out
+
+
+def run_stack(args, rank, world, local):
+    """47 Flint MoE layers (weights seed 100+l, about 76 GB), T=256 tokens (x seed 4); each
+    layer x <- x + MoE_l(RMSNorm(x)), eps 1e-6.  One step = the 47 forwards."""
+    import torch
+
+    import synth
+    import sparse_moe_layer_15_b300 as fm
+    from sparse_moe_layer_15_b300 import accounting as acc
+
+    L, T = acc.N_MOE_LAYERS, 256
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+    flags = fm.FLAG_PRE_RMSNORM | fm.FLAG_RESIDUAL
+    ws = torch.empty(fm.workspace_bytes(T, flags, 1e-6), dtype=torch.uint8, device=dev)
+    weights = [synth.flint_weights(seed=100 + l, device=dev) for l in range(L)]
+    layers = [fm.FlintMoE(weights[l], max_tokens=T, flags=flags, rms_eps=1e-6, workspace=ws) for l in range(L)]
+    x0 = synth.torch_normal_bf16((T, fm.HIDDEN), 4, synth.TAG_X, 1.0, device=dev)
+    x = x0.clone()
+    ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+
+    def stack():
+        for lay in layers:
+            lay.forward(x, y=x)
+
+    timed_loop(stack, args.warmup, None, stream, ev)
+    # touched experts per layer on the layer inputs of one pass
+    U = []
+    x.copy_(x0)
+    for lay in layers:
+        _, _, c = lay.route(x)
+        U.append(int((c > 0).sum().item()))
+        lay.forward(x, y=x)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < 1.5:
+        x.copy_(x0)
+        timed_loop(stack, 1, None, stream, ev)
+    barrier(world)
+    times = []
+    for _ in range(args.steps):
+        x.copy_(x0)
+        times += timed_loop(stack, 1, None, stream, ev)
+    clk = clocks.stop()
+    barrier(world)
+    for lay in layers:
+        if lay.poll_device_status() != 0:
+            raise RuntimeError("device status error in the timed region")
+    ms = max_over_ranks(statistics.mean(times), world)
+    alg_bytes = sum(acc.algorithmic_bytes(u, T) for u in U)
+    flop = acc.flops_per_token() * T * L
+    achieved = alg_bytes / (ms * 1e-3) / 1e9
+    roofline = dict(bound="hbm", kernel="decode_fused (x47, + rmsnorm)", achieved=round(achieved, 1),
+                    peak=peaks["hbm_gbs"], unit="GB/s", frac=round(achieved / peaks["hbm_gbs"], 4), traffic=None,
+                    alg_bytes_per_launch=round(alg_bytes / L), peak_source=peaks["source"] + " (hbm_gbs, copy test)",
+                    note="the whole step; the decode kernel is 47 of the 94 launches and nearly all the time")
+    xh = x0.cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+
+    def e2e_step():
+        x.copy_(xh, non_blocking=True)
+        stack()
+        yh.copy_(x, non_blocking=True)
+
+    e2e_t = timed_loop(e2e_step, args.warmup + args.steps, None, stream, ev)[args.warmup:]
+    e2e_ms = max_over_ranks(statistics.mean(e2e_t), world)
+    out = dict(metric=METRIC, value=round(world * T / (ms * 1e-3), 1), unit="tokens/s", n_gpus=world,
+               steps=args.steps, warmup=args.warmup, ms_per_step=round(ms, 4), higher_is_better=True, scaling="weak",
+               vs_baseline=None, dtype="bf16", data="synthetic",
+               config=dict(workload="stack: 47 Flint MoE layers (pre-norm RMSNorm eps 1e-6, residual), T=256, "
+                                    "weights seed 100+l (76 GB resident), x seed 4",
+                           tokens_per_step=T, parallelism=f"replicas x{world}",
+                           l2="inputs larger than L2 (76 GB of weights streamed per step)"),
+               layer=dict(touched_experts_per_layer=U, alg_bytes=alg_bytes, alg_flop=flop,
+                          gbs=round(achieved, 1), roofline_ms=round(alg_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3, 3)),
+               roofline=roofline,
+               e2e=dict(value=round(world * T / (e2e_ms * 1e-3), 1), unit="tokens/s",
+                        h2d_bytes_per_step=2 * fm.HIDDEN * T, d2h_bytes_per_step=2 * fm.HIDDEN * T),
+               gpu_launches=args.steps * 2 * L, clocks=clk)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline_tokens(weights[0], x0, n=8, what="stack layer 0", eps=1e-6)
+    for lay in layers:
+        lay.close()
+    return out
+
+
 # ----------------------------------------------------------------------------- oracle timing
+
+def cpu_baseline_tokens(w, x, n=16, what="", eps=None):
+    """The fp64 oracle (single thread) on the first n tokens of the workload's input."""
+    import oracle
+    from tests import parity
+
+    x64 = oracle.bf16_to_f64(parity.to_np_bf16(x[:n]))
+    if eps is not None:
+        x64 = oracle.prenorm_input(x64, eps)
+    experts = parity.touched_experts(w, x64, list(range(n)))
+    layer = parity.oracle_layer(w, experts=experts)
+    t0 = time.perf_counter()
+    oracle.forward(layer, x64, nthreads=1)
+    dt = time.perf_counter() - t0
+    return dict(value=round(n / dt, 3), unit="tokens/s", cores=1, kind="oracle",
+                sample=f"{what}: the first {n} tokens, fp64, one thread")
+
 
 def cpu_baseline(w, xs, budget_s=20.0, sample=(1, 2, 4, 8)):
     """The fp64 oracle (single thread) on the first tokens of the sweep, until the budget."""
@@ -373,9 +618,11 @@ def run_profile_case(args):
 
     dev = torch.device("cuda", 0)
     T = args.profile
-    w = synth.flint_weights(seed=0, device=dev)
+    cfg = WORKLOADS.get(args.workload)  # router bias and x seed of that workload, at this T
+    w = synth.flint_weights(seed=0, device=dev, bias=cfg["bias"] if cfg else None,
+                            bias_seed=cfg["bias_seed"] if cfg else None)
     layer = fm.FlintMoE(w, max_tokens=T)
-    x = synth.torch_normal_bf16((T, fm.HIDDEN), 1000 + T, synth.TAG_X, 1.0, device=dev)
+    x = synth.torch_normal_bf16((T, fm.HIDDEN), cfg["seed_x"] if cfg else 1000 + T, synth.TAG_X, 1.0, device=dev)
     flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     for _ in range(args.warmup + args.steps):
         flush_buf.fill_(1)
@@ -422,6 +669,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--profile", type=int, default=0, help="profiler case: forwards at this T only")
     ap.add_argument("--trace", action="store_true", help="with --profile: print the decode kernel's phase trace")
+    ap.add_argument("--workload", default="decode", choices=["decode", "single", "prefill", "adversarial", "stack"])
     args = ap.parse_args()
     if args.profile:
         run_profile_case(args)
@@ -433,7 +681,7 @@ def main():
         if rank == 0:
             print(json.dumps(run_reference(args, rank, world, local)), flush=True)
         return
-    out = run_ours(args, rank, world, local)
+    out = run_ours(args, rank, world, local) if args.workload == "decode" else run_workload(args, rank, world, local)
     if rank == 0:
         print(json.dumps(out), flush=True)
 

@@ -24,7 +24,12 @@
  *     are recorded in a status word inside the workspace; they are sticky until read by
  *     flint_moe_poll_device_status.
  *   - A handle may be used from one stream at a time.  Results are bitwise deterministic
- *     for identical inputs (no floating-point atomics).
+ *     for identical inputs (no floating-point atomics).  Several handles (e.g. the layers of
+ *     a stack) may share one workspace when all their calls are ordered on one stream: the
+ *     workspace holds only per-call scratch, and its counters return to zero at the end of
+ *     every call.
+ *   - T <= 256 runs the decode-size path (one persistent cooperative kernel); larger T runs
+ *     the tensor-core path (seven kernels).
  *   - The only supported shape is the Flint layer's (hidden 2048, 256 experts, top-6,
  *     widths 512 / 1024); any other returns FLINT_MOE_ERR_UNSUPPORTED, as does a device
  *     that is not compute capability 10.3 (the serving kit likewise refuses configurations
