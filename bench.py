@@ -320,7 +320,7 @@ PF_KERNEL_FLOPS_PER_TOKEN = {
     "pf_router": 2 * 2048 * 256,
     "pf_gateup": 6 * 2 * 2 * 2048 * 512 + 2 * 2 * 2048 * 1024,
     "pf_down": 6 * 2 * 512 * 2048,
-    "pf_shared_down_combine": 2 * 1024 * 2048,
+    "pf_shared_down": 2 * 1024 * 2048,
 }
 
 
@@ -630,7 +630,28 @@ def run_profile_case(args):
     torch.cuda.synchronize()
     rc = layer.poll_device_status()
     trace = None
-    if args.trace:
+    if args.trace and T > 256:
+        # wait profile of the grouped GEMMs (routed gate/up: slots 0..7, routed down: 8..15):
+        # per CTA, SM kcycles spent waiting, median / max over CTAs, one repetition
+        layer.enable_phase_trace(True)
+        flush_buf.fill_(1)
+        layer.forward(x)
+        rows = layer.read_trace()
+        layer.enable_phase_trace(False)
+        fields = ["producer_wait_free_stage", "mma_wait_loaded_stage", "mma_wait_free_accumulator",
+                  "epilogue_wait_accumulator", "epilogue_busy"]
+        trace = {}
+        for base, kern in ((0, "gateup"), (8, "down")):
+            rr = [r for r in rows if r[base + 7]]
+            d = {}
+            for k, nm in enumerate(fields):
+                v = sorted(r[base + k] / 1e3 for r in rr)
+                d[nm] = [round(v[len(v) // 2], 1), round(v[-1], 1)]
+            span = sorted((r[base + 6] - r[base + 5]) / 1e3 for r in rr)
+            d["cta_span_us"] = [round(span[len(span) // 2], 1), round(span[-1], 1)]
+            d["tiles"] = [int(statistics.median(r[base + 7] for r in rr)), int(max(r[base + 7] for r in rr))]
+            trace[kern] = d
+    elif args.trace:
         # phase stamps of the decode kernel: per slot, min / median / max over CTAs, in us from
         # the earliest CTA start; several repetitions, the median of each statistic reported
         names = {0: "start", 1: "inputs_ready", 11: "A_first_block", 2: "A_done", 3: "barrier1", 4: "routed",
@@ -654,7 +675,7 @@ def run_profile_case(args):
                  for nm in names.values() if all(nm in r for r in reps)}
     layer.close()
     print(json.dumps(dict(profile_case=T, steps=args.steps, device_status=rc, y_abs_mean=float(y.float().abs().mean()),
-                          phase_trace_us_min_med_max=trace)))
+                          trace=trace)))
     if rc != 0:
         raise SystemExit(1)
 
@@ -668,7 +689,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--profile", type=int, default=0, help="profiler case: forwards at this T only")
-    ap.add_argument("--trace", action="store_true", help="with --profile: print the decode kernel's phase trace")
+    ap.add_argument("--trace", action="store_true",
+                    help="with --profile: print the decode kernel's phase trace (T <= 256) or the grouped GEMMs' "
+                         "wait profile (T > 256)")
     ap.add_argument("--workload", default="decode", choices=["decode", "single", "prefill", "adversarial", "stack"])
     args = ap.parse_args()
     if args.profile:

@@ -68,8 +68,7 @@ struct Params {
   bf16* xs;              // [T*K][H] expert-sorted input rows (prefill path)
   bf16* Yb;              // [T*K][H] gated routed expert outputs, bf16 (prefill path)
   int32_t* hist;         // [T/128][E] per-tile expert histogram (prefill path)
-  int32_t* hbase;        // [T/128][E] rows of expert e taken by earlier tiles (prefill path)
-  int32_t* mtp;          // [E+1] 128-row tile prefix over experts (prefill path)
+  int32_t* mtp;          // [E+1] prefix over experts of their 256-row groups (prefill path)
   uint32_t* bar_count;   // [1] grid-barrier counter (decode path; reset at kernel end)
   uint32_t* bar_done;    // [1]
   uint32_t* tk_router;   // [1] tickets (zero between kernels: the last arriver resets)
@@ -206,5 +205,10 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float* f) {
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
 
 __device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
+
+// silu with the hardware exponential and approximate division (a few ulp in fp32, far below
+// the bf16 rounding of the result); for the tensor-core epilogues, whose time per tile is
+// bounded by the MMA time of the next tile.  z < -87 gives -0 / +inf -> 0.
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 }  // namespace flint

@@ -666,8 +666,11 @@ __device__ __forceinline__ void prefetch_share(const void* base, size_t bytes) {
 }
 
 // ---------------------------------------------------------------- routing
-// Scores of up to 4 tokens (list `toks`, count nt) into scores[t][e], then the top-K of each
-// (warp t): key = (score bits, 255 - expert), max = highest score, lowest index on ties.
+// Router logits (+ bias) of up to 4 tokens (list `toks`, count nt) into scores[t][e], then
+// the top-K of each (warp t).  The sigmoid is strictly increasing, so ranking the fp32 logits
+// gives the score order without the fp32 score saturating near 1; only the K chosen logits go
+// through the sigmoid.  key = (order-preserving bits of the logit, 255 - expert): max =
+// highest logit, lowest index on ties (-0 is folded into +0 so that they tie).
 // All threads of the CTA call it.
 __device__ void route_tokens(const Params& p, uint8_t* sm, const int* toks, int nt, int* s_idx, float* s_gw,
                              bool write_global) {
@@ -683,7 +686,8 @@ __device__ void route_tokens(const Params& p, uint8_t* sm, const int* toks, int 
 #pragma unroll
       for (int rb = 0; rb < RT_NB; ++rb) l += part[rb];
       if (p.router_bias) l += p.router_bias[e];
-      scores[t * E + e] = 1.0f / (1.0f + expf(-l));
+      if (l == 0.f) l = 0.f;
+      scores[t * E + e] = l;
     }
   }
   __syncthreads();
@@ -694,7 +698,9 @@ __device__ void route_tokens(const Params& p, uint8_t* sm, const int* toks, int 
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int ex = lane + 32 * q;
-      key[q] = (uint64_t(__float_as_uint(scores[warp * E + ex])) << 32) | uint32_t(E - 1 - ex);
+      const uint32_t u = __float_as_uint(scores[warp * E + ex]);
+      const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+      key[q] = (uint64_t(ord) << 32) | uint32_t(E - 1 - ex);
     }
     float sel_s[K];
     int sel_e[K];
@@ -710,10 +716,10 @@ __device__ void route_tokens(const Params& p, uint8_t* sm, const int* toks, int 
       }
       const int ex = E - 1 - int(best & 0xFFFFFFFFu);
       sel_e[jj] = ex;
-      sel_s[jj] = __uint_as_float(uint32_t(best >> 32));
+      sel_s[jj] = 1.0f / (1.0f + expf(-scores[warp * E + ex]));
 #pragma unroll
       for (int q = 0; q < 8; ++q)
-        if (lane + 32 * q == ex) key[q] = 0;  // scores are >= 0: an emptied slot never wins
+        if (lane + 32 * q == ex) key[q] = 0;  // a non-NaN logit keys above 0: an emptied slot never wins
     }
     if (lane == 0) {
       float sum = 0.f;

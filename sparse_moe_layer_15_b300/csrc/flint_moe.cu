@@ -26,7 +26,7 @@ struct Layout {
   size_t status, bar_count, bar_done, tk_router, tk_gu, tk_sgu, tk_sd, tk_dn, tk_comb;
   size_t n_touched, n_groups, touched, tgp, counts, offsets, perm, inv, topk_idx, topk_w;
   size_t xn, xstage, ystage, h, hs, S, Y, P_gu, P_sgu, P_sd, P_dn, RP, trace;
-  size_t xs, Yb, hist, hbase, mtp;  // prefill path (max_tokens > STREAM_MAX_T), else 0
+  size_t xs, Yb, hist, mtp;  // prefill path (max_tokens > STREAM_MAX_T), else 0
   size_t total;
 };
 
@@ -80,7 +80,6 @@ Layout make_layout(int max_tokens) {
     L.xs = take(sizeof(uint16_t) * T * K * H);
     L.Yb = take(sizeof(uint16_t) * T * K * H);
     L.hist = take(sizeof(int32_t) * ntile * E);
-    L.hbase = take(sizeof(int32_t) * ntile * E);
     L.mtp = take(sizeof(int32_t) * (E + 1));
   }
   L.trace = take(sizeof(unsigned long long) * MAX_TRACE_CTAS * TRACE_SLOTS);
@@ -201,11 +200,10 @@ Params make_params(flint_moe_t h, const void* x, int T, void* y, int32_t* out_id
   p.P_sd = reinterpret_cast<float*>(ws + L.P_sd);
   p.P_dn = reinterpret_cast<float*>(ws + L.P_dn);
   p.RP = reinterpret_cast<float*>(ws + L.RP);
-  if (L.xs) {
+  if (L.Yb) {
     p.xs = reinterpret_cast<bf16*>(ws + L.xs);
     p.Yb = reinterpret_cast<bf16*>(ws + L.Yb);
     p.hist = reinterpret_cast<int32_t*>(ws + L.hist);
-    p.hbase = reinterpret_cast<int32_t*>(ws + L.hbase);
     p.mtp = reinterpret_cast<int32_t*>(ws + L.mtp);
   }
   p.out_idx = out_idx;
@@ -270,29 +268,33 @@ flint_moe_status run_prefill(flint_moe_t h, const Params& p, cudaStream_t st, bo
   if (h->cfg.flags & FLINT_MOE_FLAG_PRE_RMSNORM) e = launch(h, "rmsnorm", rmsnorm_kernel, T, 256, 0, st, false, p);
   if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
   // the A operand of the router and of the shared gate/up: the layer input rows
-  CUtensorMap xin = h->pmaps.xin;
+  CUtensorMap xin = h->pmaps.xin, xin_c = h->pmaps.xin_c;
   if (!(h->cfg.flags & FLINT_MOE_FLAG_PRE_RMSNORM) &&
-      !make_map(&xin, p.x, (uint64_t)T, H, 64, tc::TM, CU_TENSOR_MAP_SWIZZLE_128B))
+      !(make_map(&xin, p.x, (uint64_t)T, H, 64, tc::TM, CU_TENSOR_MAP_SWIZZLE_128B) &&
+        make_map(&xin_c, p.x, (uint64_t)T, H, 64, tc::XC_ROWS, CU_TENSOR_MAP_SWIZZLE_128B)))
     return FLINT_MOE_ERR_CUDA;
   const int n_sm = h->n_sm;
   pf::RouterTC r{p, xin, h->pmaps.wr};
   e = launch(h, "pf_router", tc::gemm_kernel<pf::RouterTC>, ntile < n_sm ? ntile : n_sm, tc::NUM_THREADS,
              tc::SMEM_BYTES, st, false, r);
-  if (e == cudaSuccess) e = launch(h, "pf_scan", pf::scan_kernel, 1, 256, 0, st, false, p);
   if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
-  if (!full) return FLINT_MOE_OK;
-  e = launch(h, "pf_scatter", pf::scatter_kernel, ntile, 256, 0, st, false, p);
-  pf::GateUpTC gu{p, h->pmaps.xs, xin, h->pmaps.wg, h->pmaps.wu, h->pmaps.wsg, h->pmaps.wsu};
+  if (!full) {
+    e = launch(h, "pf_scatter", pf::scatter_kernel, 1, 256, 0, st, false, p, 0);
+    return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ERR_CUDA;
+  }
+  e = launch(h, "pf_scatter", pf::scatter_kernel, ntile * pf::SPLIT, 256, 0, st, false, p, 1);
+  pf::GateUpTC gu{p, h->pmaps.xs, xin_c, h->pmaps.wg, h->pmaps.wu, h->pmaps.wsg, h->pmaps.wsu};
   if (e == cudaSuccess)
     e = launch(h, "pf_gateup", tc::gemm_kernel<pf::GateUpTC>, n_sm, tc::NUM_THREADS, tc::SMEM_BYTES, st, false, gu);
   pf::DownTC dn{p, h->pmaps.h, h->pmaps.wd};
   if (e == cudaSuccess)
     e = launch(h, "pf_down", tc::gemm_kernel<pf::DownTC>, n_sm, tc::NUM_THREADS, tc::SMEM_BYTES, st, false, dn);
   pf::SharedDownTC sd{p, h->pmaps.hs, h->pmaps.wsd};
-  const int sd_tiles = ntile * pf::NCT_OUT;
+  const int sd_tiles = ((T + pf::RG - 1) / pf::RG) * pf::NCT_DN;
   if (e == cudaSuccess)
-    e = launch(h, "pf_shared_down_combine", tc::gemm_kernel<pf::SharedDownTC>, sd_tiles < n_sm ? sd_tiles : n_sm,
+    e = launch(h, "pf_shared_down", tc::gemm_kernel<pf::SharedDownTC>, sd_tiles < n_sm ? sd_tiles : n_sm,
                tc::NUM_THREADS, tc::SMEM_BYTES, st, false, sd);
+  if (e == cudaSuccess) e = launch(h, "pf_combine", pf::combine_kernel, T, 256, 0, st, false, p);
   return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ERR_CUDA;
 }
 
@@ -307,17 +309,19 @@ flint_moe_status check_call(flint_moe_t h, const void* x, int T) {
   return FLINT_MOE_OK;
 }
 
-// Tensor maps of the prefill path (weights: B boxes of 64 x 64; workspace activations: A
-// boxes of 64 x 128).  Needs the workspace carved (h->ws, h->L).
+// Tensor maps of the prefill path (weights: boxes of 64 x 64; activations read by the router's
+// ROWS tiles: boxes of 64 x 128; activations read by COLUMNS tiles: boxes of 64 x 64).  Needs
+// the workspace carved (h->ws, h->L).
 bool make_prefill_maps(flint_moe_t h) {
   const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
   const flint_moe_weights* w = &h->w;
   const uint64_t T = (uint64_t)h->cfg.max_tokens;
   pf::Maps& m = h->pmaps;
   return make_map(&m.xin, h->ws + h->L.xn, T, H, 64, tc::TM, sw) &&
-         make_map(&m.xs, h->ws + h->L.xs, T * K, H, 64, tc::TM, sw) &&
-         make_map(&m.h, h->ws + h->L.h, T * K, I, 64, tc::TM, sw) &&
-         make_map(&m.hs, h->ws + h->L.hs, T, IS, 64, tc::TM, sw) &&
+         make_map(&m.xin_c, h->ws + h->L.xn, T, H, 64, tc::XC_ROWS, sw) &&
+         make_map(&m.xs, h->ws + h->L.xs, T * K, H, 64, tc::XC_ROWS, sw) &&
+         make_map(&m.h, h->ws + h->L.h, T * K, I, 64, tc::XC_ROWS, sw) &&
+         make_map(&m.hs, h->ws + h->L.hs, T, IS, 64, tc::XC_ROWS, sw) &&
          make_map(&m.wr, w->w_router, H, E, 64, tc::TK, sw) &&
          make_map(&m.wg, w->w_gate, (uint64_t)E * H, I, 64, tc::TK, sw) &&
          make_map(&m.wu, w->w_up, (uint64_t)E * H, I, 64, tc::TK, sw) &&
@@ -414,13 +418,13 @@ flint_moe_status flint_moe_create(const flint_moe_config* cfg, const flint_moe_w
             make_map(&h->smaps.wsg, w->ws_gate, H, IS, 64, GU_ROWS, sw) &&
             make_map(&h->smaps.wsu, w->ws_up, H, IS, 64, GU_ROWS, sw) &&
             make_map(&h->smaps.wsd, w->ws_down, IS, H, 64, DN_ROWS, sw);
-  if (ok && L.xs) ok = make_prefill_maps(h);
+  if (ok && L.Yb) ok = make_prefill_maps(h);
   if (!ok) {
     delete h;
     return FLINT_MOE_ERR_CUDA;
   }
   cudaError_t e = cudaFuncSetAttribute(decode_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, FUSED_SMEM);
-  if (e == cudaSuccess && L.xs) e = set_prefill_smem();
+  if (e == cudaSuccess && L.Yb) e = set_prefill_smem();
   int per_sm = 0;
   if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused, NTHREADS, FUSED_SMEM);
   if (e == cudaSuccess && per_sm < 1) e = cudaErrorCooperativeLaunchTooLarge;

@@ -1,18 +1,21 @@
 // Prefill-size path of the Flint MoE layer (T > 256 tokens): the contractions are dense enough
 // for the tensor cores, so every GEMM-shaped step runs on the tcgen05 engine (tc_gemm.cuh):
 //
-//   router    [T x 2048] x W_r [2048 x 256]: epilogue = bias, sigmoid, top-6 with the lower
-//             index first on ties, renormalised gates, and a per-tile histogram of the choices;
-//   scan      one CTA: counts, offsets, per-tile bases of every expert, M-tile prefix;
-//   scatter   one CTA per 128-token tile: stable (t, j)-order placement of the pairs into
-//             expert-sorted rows (perm / inv) and the gathered input rows xs[row] = x[t];
-//   gate/up   grouped over (expert, 128-column pair of gate and up, 128-row tile) plus the shared
-//             expert over (128-column pair, token tile): epilogue h = bf16(silu(g) * u);
-//   down      grouped over (expert, 256 output columns, 128-row tile): epilogue
-//             Y[row] = bf16(gate(row) * acc);
-//   shared down + combine  over (256 output columns, token tile): epilogue
-//             y[t] = bf16(acc + sum_j Y[inv(t, j)] in slot order (+ x[t])).
-// Tiles of one expert's weight column block are numbered consecutively with the row tile
+//   router    [T x 2048] x W_r [2048 x 256] (ROWS): epilogue = bias, top-6 by logit with the
+//             lower index first on ties, sigmoid of the six, renormalised gates, and a
+//             per-tile histogram of the choices;
+//   scatter   SPLIT CTAs per 128-token tile: counts, offsets and the 256-row group prefix of
+//             every expert (each CTA reduces the histograms itself), the stable (t, j)-order
+//             placement of the pairs into expert-sorted rows (perm / inv), and the copied input
+//             rows xs[row] = x[t];
+//   gate/up   grouped over (expert, 64-column pair of gate and up, 256-row group) in COLUMNS
+//             orientation (N = the group's rows rounded up to 16), then the shared expert over
+//             (64-column pair, 256-token group): h = bf16(silu(g) * u);
+//   down      grouped over (expert, 128 output columns, 256-row group), COLUMNS: epilogue
+//             Yb[row] = bf16(gate(row) * acc);
+//   shared down  over (128 output columns, 256-token group), COLUMNS: S[t] = acc (fp32);
+//   combine   y[t] = bf16(S[t] + sum_j Yb[inv(t, j)] in slot order (+ x[t])).
+// Tiles of one expert's weight column block are numbered consecutively with the row group
 // fastest, so concurrent CTAs share each weight tile through L2.
 #pragma once
 
@@ -27,15 +30,17 @@ using tc::TM;
 using tc::tmem_ld32;
 using tc::epi_sync;
 
-constexpr int NCT_GU = I / 128;   // 4 column pairs of a routed expert's gate/up
-constexpr int NCT_SGU = IS / 128; // 8 column pairs of the shared gate/up
-constexpr int NCT_OUT = H / 256;  // 8 output column blocks of a down projection
+constexpr int RG = 2 * TM;        // rows per COLUMNS tile (the MMA's N <= 256)
+constexpr int NCT_GU = I / 64;    // 8 column pairs (64 of gate | 64 of up) of a routed gate/up
+constexpr int NCT_SGU = IS / 64;  // 16 column pairs of the shared gate/up
+constexpr int NCT_DN = H / 128;   // 16 output column blocks of a down projection
 
 struct Maps {
-  CUtensorMap xin;  // [T][H], box 64 x 128 (A operand)
-  CUtensorMap xs;   // [6 max_T][H], box 64 x 128
-  CUtensorMap h;    // [6 max_T][I], box 64 x 128
-  CUtensorMap hs;   // [max_T][IS], box 64 x 128
+  CUtensorMap xin;  // [T][H], box 64 x 128 (router, ROWS tiles)
+  CUtensorMap xin_c;  // [T][H], box 64 x 64 (shared gate/up, COLUMNS tiles)
+  CUtensorMap xs;   // [6 max_T][H], box 64 x 64 (routed gate/up, COLUMNS tiles)
+  CUtensorMap h;    // [6 max_T][I], box 64 x 64 (COLUMNS tiles)
+  CUtensorMap hs;   // [max_T][IS], box 64 x 64 (COLUMNS tiles)
   CUtensorMap wr;   // [H][E], box 64 x 64 (B operand)
   CUtensorMap wg;   // [E H][I], box 64 x 64
   CUtensorMap wu;
@@ -59,12 +64,14 @@ __device__ __forceinline__ void store_bf16x32(bf16* dst, const float* v) {
 
 // ================================================================ router
 struct RouterTC {
+  static constexpr bool kColumns = false;
   Params p;
   CUtensorMap xin, wr;
   __device__ void prologue(uint8_t*) const {}
   __device__ int num_tiles(const uint8_t*) const { return (p.T + TM - 1) / TM; }
   __device__ int kblocks() const { return H / tc::TK; }
   __device__ uint32_t* status() const { return p.status; }
+  __device__ unsigned long long* trace() const { return nullptr; }
   __device__ void tile(int i, TileInfo& t, const uint8_t*) const {
     t.amap = &xin;
     t.a_row0 = i * TM;
@@ -79,18 +86,20 @@ struct RouterTC {
     t.col0 = 0;
     t.aux = i;
   }
-  // Thread `row` owns token row0 + row: its 256 logits stream out of TMEM 32 at a time in
-  // expert order; a running top-6 keeps the higher score, and on equal scores the expert seen
-  // first (the lower index).
+  // Thread `row` owns token row0 + row: its 256 logits (+ bias) stream out of TMEM 32 at a
+  // time in expert order; a running top-6 keeps the higher logit, and on equal logits the
+  // expert seen first (the lower index).  The sigmoid is strictly increasing, so this is the
+  // order of the scores; ranking the fp32 logits also avoids the fp32 score saturating near 1.
+  // Only the six chosen logits go through the sigmoid.
   __device__ void epilogue(const TileInfo& t, uint32_t trow, int row, uint8_t* epi, const uint8_t*) const {
     int* hist = reinterpret_cast<int*>(epi);
     hist[row] = 0;
     hist[row + TM] = 0;
-    float s6[K];
+    float l6[K];
     int e6[K];
 #pragma unroll
     for (int j = 0; j < K; ++j) {
-      s6[j] = -1.f;
+      l6[j] = -INFINITY;
       e6[j] = -1;
     }
 #pragma unroll 1
@@ -102,16 +111,15 @@ struct RouterTC {
         const int e = c * 32 + q;
         float l = v[q];
         if (p.router_bias) l += p.router_bias[e];
-        const float s = 1.0f / (1.0f + expf(-l));
-        if (s > s6[K - 1]) {
-          s6[K - 1] = s;
+        if (l > l6[K - 1]) {
+          l6[K - 1] = l;
           e6[K - 1] = e;
 #pragma unroll
           for (int j = K - 1; j > 0; --j) {
-            if (s6[j] > s6[j - 1]) {
-              const float ts = s6[j];
-              s6[j] = s6[j - 1];
-              s6[j - 1] = ts;
+            if (l6[j] > l6[j - 1]) {
+              const float tl = l6[j];
+              l6[j] = l6[j - 1];
+              l6[j - 1] = tl;
               const int te = e6[j];
               e6[j] = e6[j - 1];
               e6[j - 1] = te;
@@ -120,6 +128,9 @@ struct RouterTC {
         }
       }
     }
+    float s6[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) s6[j] = 1.0f / (1.0f + expf(-l6[j]));
     epi_sync();  // histogram zeroed
     if (row < t.valid) {
       float sum = 0.f;
@@ -143,23 +154,43 @@ struct RouterTC {
   }
 };
 
-// ================================================================ scan (one CTA of 256 threads)
-// counts, offsets (+ user counts), per-tile relative bases hbase[tile][e] = sum of earlier
-// tiles' choices of e, and the M-tile prefix mtp[e] = sum over e' < e of ceil(n_e' / 128).
-__global__ void __launch_bounds__(256) scan_kernel(const __grid_constant__ Params p) {
+// ================================================================ scan + scatter + gather
+// SPLIT CTAs (256 threads) per 128-token tile.  Every CTA first reduces the router's per-tile
+// histograms itself -- thread e sums hist[.][e] over all tiles (count of expert e) and over the
+// tiles before its own (rows of e that earlier tiles take) -- and scans the counts over the
+// experts (offsets, and the RG-row group prefix mtp used by the grouped GEMMs); CTA 0 writes
+// those tables.  Then the tile's 768 (t, j) pairs in order get their expert-sorted rows
+// (stable: token order, then slot order, within an expert), and each CTA copies its share of
+// the input rows, xs[row] = x[t] (TMA then reads them as 64-row boxes; a row gather in the
+// GEMM's producer with cp.async could not keep enough bytes in flight).  `place` = 0 runs the
+// tables only (one CTA: routing alone).
+constexpr int SPLIT = 4;
+
+__global__ void __launch_bounds__(256) scatter_kernel(const __grid_constant__ Params p, int place) {
+  __shared__ int s_fill[E];
+  __shared__ int s_wcnt[8][E];
+  __shared__ int s_rows[TM * K];
   __shared__ int s_w[2][8];
   pdl_launch_dependents();
   pdl_wait();
-  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+  const int tile = blockIdx.x / SPLIT, part = blockIdx.x % SPLIT;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ntiles = (p.T + TM - 1) / TM;
-  int run = 0;
-  for (int tt = 0; tt < ntiles; ++tt) {
-    p.hbase[(size_t)tt * E + e] = run;
-    run += __ldcg(p.hist + (size_t)tt * E + e);
+  // ---- counts and this tile's base rows: independent loads, 16 in flight per thread
+  int tot = 0, pre = 0;
+  for (int t0 = 0; t0 < ntiles; t0 += 16) {
+    int v[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) v[q] = t0 + q < ntiles ? __ldcg(p.hist + (size_t)(t0 + q) * E + tid) : 0;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      tot += v[q];
+      if (t0 + q < tile) pre += v[q];
+    }
   }
-  const int c = run;
-  const int mt = (c + TM - 1) / TM;
-  int ic = c, im = mt;
+  // ---- exclusive scans over the experts of the counts and of their RG-row group counts
+  const int mt = (tot + RG - 1) / RG;
+  int ic = tot, im = mt;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const int a = __shfl_up_sync(0xffffffffu, ic, off);
@@ -179,31 +210,23 @@ __global__ void __launch_bounds__(256) scan_kernel(const __grid_constant__ Param
     bc += s_w[0][w];
     bm += s_w[1][w];
   }
-  const int off_e = bc + ic - c;
-  p.counts[e] = c;
-  p.offsets[e] = off_e;
-  p.mtp[e] = bm + im - mt;
-  if (p.out_counts) p.out_counts[e] = c;
-  if (e == E - 1) {
-    p.offsets[E] = off_e + c;
-    p.mtp[E] = bm + im;
+  const int off_e = bc + ic - tot;
+  if (blockIdx.x == 0) {
+    p.counts[tid] = tot;
+    p.offsets[tid] = off_e;
+    p.mtp[tid] = bm + im - mt;
+    if (p.out_counts) p.out_counts[tid] = tot;
+    if (tid == E - 1) {
+      p.offsets[E] = off_e + tot;
+      p.mtp[E] = bm + im;
+    }
   }
-}
-
-// ================================================================ scatter + gather
-// One CTA (256 threads) per 128-token tile: the tile's 768 (t, j) pairs in order get their
-// expert-sorted rows (stable), and the input row of each pair is copied to xs[row].
-__global__ void __launch_bounds__(256) scatter_kernel(const __grid_constant__ Params p) {
-  __shared__ int s_fill[E];
-  __shared__ int s_wcnt[8][E];
-  __shared__ int s_rows[TM * K];
-  pdl_launch_dependents();
-  pdl_wait();
-  const int tile = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (!place) return;
+  s_fill[tid] = off_e + pre;
+  __syncthreads();
+  // ---- stable placement of the tile's pairs
   const int t0 = tile * TM;
   const int npairs = min(TM, p.T - t0) * K;
-  s_fill[tid] = __ldcg(p.offsets + tid) + __ldcg(p.hbase + (size_t)tile * E + tid);
-  __syncthreads();
   for (int base = 0; base < npairs; base += 256) {
     for (int q = tid; q < 8 * E; q += 256) (&s_wcnt[0][0])[q] = 0;
     __syncthreads();
@@ -221,9 +244,13 @@ __global__ void __launch_bounds__(256) scatter_kernel(const __grid_constant__ Pa
       int before = 0;
       for (int w = 0; w < warp; ++w) before += s_wcnt[w][e];
       const int row = s_fill[e] + before + r;
-      p.perm[row] = t0 * K + pi;
-      p.inv[t0 * K + pi] = row;
+      if (part == 0) {
+        p.perm[row] = t0 * K + pi;
+        p.inv[t0 * K + pi] = row;
+      }
       s_rows[pi] = row;
+    } else if (pi < npairs) {
+      s_rows[pi] = -1;
     }
     __syncthreads();
     int add = 0;
@@ -231,17 +258,40 @@ __global__ void __launch_bounds__(256) scatter_kernel(const __grid_constant__ Pa
     s_fill[tid] += add;
     __syncthreads();
   }
-  // gather: warp w copies pairs w, w+8, ...; 256 x 16 bytes per row, 8 per lane
-  for (int q = warp; q < npairs; q += 8) {
-    const uint4* src = reinterpret_cast<const uint4*>(p.xin + (size_t)(t0 + q / K) * H);
-    uint4* dst = reinterpret_cast<uint4*>(p.xs + (size_t)s_rows[q] * H);
+  // ---- gather: this CTA's contiguous share of the pairs; a warp copies two 4 KB rows at a
+  // time (16 loads of 16 bytes in flight per lane)
+  const int per = (npairs + SPLIT - 1) / SPLIT;
+  const int qb = part * per, qe = min(npairs, qb + per);
+  constexpr int V = H / 8 / 32;  // uint4 per lane per row
+  for (int q = qb + warp; q < qe; q += 16) {
+    const int q2 = q + 8;
+    const bool two = q2 < qe;
+    uint4 a[V], b[V];
+    const uint4* sa = reinterpret_cast<const uint4*>(p.xin + (size_t)(t0 + q / K) * H);
+    const uint4* sb = reinterpret_cast<const uint4*>(p.xin + (size_t)(t0 + (two ? q2 : q) / K) * H);
 #pragma unroll
-    for (int k = 0; k < H / 8 / 32; ++k) dst[lane + 32 * k] = __ldg(src + lane + 32 * k);
+    for (int k = 0; k < V; ++k) a[k] = __ldg(sa + lane + 32 * k);
+#pragma unroll
+    for (int k = 0; k < V; ++k) b[k] = __ldg(sb + lane + 32 * k);
+    const int ra = s_rows[q];
+    if (ra >= 0) {
+      uint4* d = reinterpret_cast<uint4*>(p.xs + (size_t)ra * H);
+#pragma unroll
+      for (int k = 0; k < V; ++k) d[lane + 32 * k] = a[k];
+    }
+    if (two) {
+      const int rb = s_rows[q2];
+      if (rb >= 0) {
+        uint4* d = reinterpret_cast<uint4*>(p.xs + (size_t)rb * H);
+#pragma unroll
+        for (int k = 0; k < V; ++k) d[lane + 32 * k] = b[k];
+      }
+    }
   }
 }
 
-// Routing tables of the grouped GEMMs, copied to shared memory by every CTA: mtp[0..E],
-// offsets[0..E].
+// Routing tables of the grouped GEMMs, copied to shared memory by every CTA: mtp[0..E] (prefix
+// over the experts of their RG-row group counts), offsets[0..E].
 struct GroupTable {
   __device__ static void load(const Params& p, uint8_t* tbl) {
     int* mtp = reinterpret_cast<int*>(tbl);
@@ -266,174 +316,226 @@ struct GroupTable {
 };
 
 // ================================================================ gate/up (routed + shared)
+// COLUMNS tiles: 64 columns of gate (TMEM lanes 0..63) and the same 64 columns of up (lanes
+// 64..127), and up to RG = 256 rows as the MMA's N (rounded up to 16): a routed expert's rows
+// (expert-sorted copies, xs), so a ragged expert costs its own row count instead of whole
+// 128-row tiles; then the shared expert over 256-token groups of the layer input.
 struct GateUpTC {
+  static constexpr bool kColumns = true;
   Params p;
-  CUtensorMap xs, xin, wg, wu, wsg, wsu;
+  CUtensorMap xs, xin_c, wg, wu, wsg, wsu;
   __device__ void prologue(uint8_t* tbl) const { GroupTable::load(p, tbl); }
   __device__ int num_tiles(const uint8_t* tbl) const {
     const int* mtp = reinterpret_cast<const int*>(tbl);
-    return NCT_GU * mtp[E] + NCT_SGU * ((p.T + TM - 1) / TM);
+    return NCT_GU * mtp[E] + NCT_SGU * ((p.T + RG - 1) / RG);
   }
   __device__ int kblocks() const { return H / tc::TK; }
   __device__ uint32_t* status() const { return p.status; }
+  __device__ unsigned long long* trace() const { return p.trace; }  // slots 0..7
   __device__ void tile(int i, TileInfo& t, const uint8_t* tbl) const {
     const int* mtp = reinterpret_cast<const int*>(tbl);
     const int* off = mtp + (E + 1);
     const int routed = NCT_GU * mtp[E];
-    int nt, mt;
     if (i < routed) {
       const int e = GroupTable::find(mtp, NCT_GU, i);
       const int mte = mtp[e + 1] - mtp[e];
       const int local = i - NCT_GU * mtp[e];
-      nt = local / mte;
-      mt = local % mte;
+      const int nt = local / mte, mt = local % mte;
       t.amap = &xs;
-      t.a_row0 = off[e] + mt * TM;
+      t.a_row0 = off[e] + mt * RG;
       t.b_row0 = e * H;
-      t.bmap[0] = t.bmap[1] = &wg;
-      t.bmap[2] = t.bmap[3] = &wu;
-      t.row0 = off[e] + mt * TM;
-      t.valid = min(TM, off[e + 1] - off[e] - mt * TM);
+      t.bmap[0] = &wg;
+      t.bmap[1] = &wu;
+      t.row0 = off[e] + mt * RG;
+      t.valid = min(RG, off[e + 1] - off[e] - mt * RG);
+      t.col0 = nt * 64;
       t.aux = 0;
     } else {
-      const int ntt = (p.T + TM - 1) / TM;
+      const int ng = (p.T + RG - 1) / RG;
       const int j = i - routed;
-      nt = j / ntt;
-      mt = j % ntt;
-      t.amap = &xin;
-      t.a_row0 = mt * TM;
+      const int nt = j / ng, g = j % ng;
+      t.amap = &xin_c;
+      t.a_row0 = g * RG;
       t.b_row0 = 0;
-      t.bmap[0] = t.bmap[1] = &wsg;
-      t.bmap[2] = t.bmap[3] = &wsu;
-      t.row0 = mt * TM;
-      t.valid = min(TM, p.T - mt * TM);
+      t.bmap[0] = &wsg;
+      t.bmap[1] = &wsu;
+      t.row0 = g * RG;
+      t.valid = min(RG, p.T - g * RG);
+      t.col0 = nt * 64;
       t.aux = 1;
     }
-    t.col0 = nt * 128;
-    t.bcol[0] = t.bcol[2] = nt * 128;
-    t.bcol[1] = t.bcol[3] = nt * 128 + 64;
+    t.bcol[0] = t.bcol[1] = t.col0;
+    t.n = (t.valid + 15) & ~15;
   }
-  // accumulator columns 0..127 = gate, 128..255 = up (of output columns col0 .. col0+127)
-  __device__ void epilogue(const TileInfo& t, uint32_t trow, int row, uint8_t*, const uint8_t*) const {
-    bf16* dst = t.aux ? p.hs + (size_t)(t.row0 + row) * IS : p.h + (size_t)(t.row0 + row) * I;
+  // h = bf16(silu(gate) * up) into h (routed) or hs (shared).  Per 32-row chunk the gate lanes
+  // (0..63) and the up lanes (64..127) swap halves through shared memory -- the up lanes receive
+  // the gate of rows 16..31, the gate lanes the up of rows 0..15 -- so all four warps share the
+  // work.
+  __device__ void epilogue(const TileInfo& t, uint32_t trow, int row, uint8_t* epi, const uint8_t*) const {
+    float* xch = reinterpret_cast<float*>(epi);  // [2][16 rows][64 columns] fp32
+    const bool gate_lane = row < 64;
+    const int f = row & 63;
+    const int q0 = gate_lane ? 0 : 16;  // rows of the chunk this lane writes
+    float* give = xch + (gate_lane ? 1024 : 0) + f;
+    const float* take = xch + (gate_lane ? 0 : 1024) + f;
+    const int ld = t.aux ? IS : I;
+    bf16* dst = (t.aux ? p.hs : p.h) + (size_t)t.row0 * ld + t.col0 + f;
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      float g[32], u[32];
-      tmem_ld32(trow + uint32_t(c * 32), g);
-      tmem_ld32(trow + uint32_t(128 + c * 32), u);
+    for (int c = 0; c * 32 < t.valid; ++c) {
+      float v[32];
+      tmem_ld32(trow + uint32_t(c * 32), v);
 #pragma unroll
-      for (int q = 0; q < 32; ++q) g[q] = silu_f32(g[q]) * u[q];
-      if (row < t.valid) store_bf16x32(dst + t.col0 + c * 32, g);
+      for (int q = 0; q < 16; ++q) give[q * 64] = gate_lane ? v[16 + q] : v[q];
+      epi_sync();
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const int r = c * 32 + q0 + q;
+        const float other = take[q * 64];
+        const float g = gate_lane ? v[q] : other;
+        const float u = gate_lane ? other : v[16 + q];
+        if (r < t.valid) dst[(size_t)r * ld] = __float2bfloat16_rn(silu_fast(g) * u);
+      }
+      epi_sync();  // before the next chunk overwrites the exchange buffer
     }
   }
 };
 
 // ================================================================ routed down
+// COLUMNS: 128 output columns on the TMEM lanes, up to RG = 256 of the expert's rows as N.
+// Epilogue: Yb[row][col] = bf16(gate(row) * acc).
 struct DownTC {
+  static constexpr bool kColumns = true;
   Params p;
   CUtensorMap h, wd;
   __device__ void prologue(uint8_t* tbl) const { GroupTable::load(p, tbl); }
-  __device__ int num_tiles(const uint8_t* tbl) const { return NCT_OUT * reinterpret_cast<const int*>(tbl)[E]; }
+  __device__ int num_tiles(const uint8_t* tbl) const { return NCT_DN * reinterpret_cast<const int*>(tbl)[E]; }
   __device__ int kblocks() const { return I / tc::TK; }
   __device__ uint32_t* status() const { return p.status; }
+  __device__ unsigned long long* trace() const { return p.trace ? p.trace + 8 : nullptr; }  // slots 8..15
   __device__ void tile(int i, TileInfo& t, const uint8_t* tbl) const {
     const int* mtp = reinterpret_cast<const int*>(tbl);
     const int* off = mtp + (E + 1);
-    const int e = GroupTable::find(mtp, NCT_OUT, i);
+    const int e = GroupTable::find(mtp, NCT_DN, i);
     const int mte = mtp[e + 1] - mtp[e];
-    const int local = i - NCT_OUT * mtp[e];
+    const int local = i - NCT_DN * mtp[e];
     const int nt = local / mte, mt = local % mte;
     t.amap = &h;
-    t.a_row0 = off[e] + mt * TM;
+    t.a_row0 = off[e] + mt * RG;
     t.b_row0 = e * I;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      t.bmap[c] = &wd;
-      t.bcol[c] = nt * 256 + c * 64;
-    }
-    t.row0 = off[e] + mt * TM;
-    t.valid = min(TM, off[e + 1] - off[e] - mt * TM);
-    t.col0 = nt * 256;
+    t.bmap[0] = t.bmap[1] = &wd;
+    t.bcol[0] = nt * 128;
+    t.bcol[1] = nt * 128 + 64;
+    t.row0 = off[e] + mt * RG;
+    t.valid = min(RG, off[e + 1] - off[e] - mt * RG);
+    t.col0 = nt * 128;
     t.aux = e;
+    t.n = (t.valid + 15) & ~15;
   }
-  __device__ void epilogue(const TileInfo& t, uint32_t trow, int row, uint8_t*, const uint8_t*) const {
-    const bool ok = row < t.valid;
-    const float g = ok ? __ldcg(p.topk_w + __ldcg(p.perm + t.row0 + row)) : 0.f;
-    bf16* dst = p.Yb + (size_t)(t.row0 + row) * H + t.col0;
+  __device__ void epilogue(const TileInfo& t, uint32_t trow, int row, uint8_t* epi, const uint8_t*) const {
+    float* gate = reinterpret_cast<float*>(epi);  // gate of each of the tile's rows
+#pragma unroll
+    for (int k = 0; k < RG / TM; ++k) {
+      const int r = row + k * TM;
+      gate[r] = r < t.valid ? __ldcg(p.topk_w + __ldcg(p.perm + t.row0 + r)) : 0.f;
+    }
+    epi_sync();
+    bf16* dst = p.Yb + (size_t)t.row0 * H + t.col0 + row;
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c * 32 < t.valid; ++c) {
       float v[32];
       tmem_ld32(trow + uint32_t(c * 32), v);
 #pragma unroll
-      for (int q = 0; q < 32; ++q) v[q] *= g;
-      if (ok) store_bf16x32(dst + c * 32, v);
+      for (int q = 0; q < 32; ++q)
+        if (c * 32 + q < t.valid) dst[(size_t)(c * 32 + q) * H] = __float2bfloat16_rn(v[q] * gate[c * 32 + q]);
+    }
+    epi_sync();  // the next tile rewrites the gates
+  }
+};
+
+// ================================================================ shared down
+// COLUMNS over (128 output columns, 256-token group): S[t][col] = acc in fp32.
+struct SharedDownTC {
+  static constexpr bool kColumns = true;
+  Params p;
+  CUtensorMap hs, wsd;
+  __device__ void prologue(uint8_t*) const {}
+  __device__ int num_tiles(const uint8_t*) const { return NCT_DN * ((p.T + RG - 1) / RG); }
+  __device__ int kblocks() const { return IS / tc::TK; }
+  __device__ uint32_t* status() const { return p.status; }
+  __device__ unsigned long long* trace() const { return nullptr; }
+  __device__ void tile(int i, TileInfo& t, const uint8_t*) const {
+    const int ng = (p.T + RG - 1) / RG;
+    const int nt = i / ng, g = i % ng;
+    t.amap = &hs;
+    t.a_row0 = g * RG;
+    t.b_row0 = 0;
+    t.bmap[0] = t.bmap[1] = &wsd;
+    t.bcol[0] = nt * 128;
+    t.bcol[1] = nt * 128 + 64;
+    t.row0 = g * RG;
+    t.valid = min(RG, p.T - g * RG);
+    t.col0 = nt * 128;
+    t.aux = 0;
+    t.n = (t.valid + 15) & ~15;
+  }
+  __device__ void epilogue(const TileInfo& t, uint32_t trow, int row, uint8_t*, const uint8_t*) const {
+    float* dst = p.S + (size_t)t.row0 * H + t.col0 + row;
+#pragma unroll 1
+    for (int c = 0; c * 32 < t.valid; ++c) {
+      float v[32];
+      tmem_ld32(trow + uint32_t(c * 32), v);
+#pragma unroll
+      for (int q = 0; q < 32; ++q)
+        if (c * 32 + q < t.valid) dst[(size_t)(c * 32 + q) * H] = v[q];
     }
   }
 };
 
-// ================================================================ shared down + combine
-struct SharedDownTC {
-  Params p;
-  CUtensorMap hs, wsd;
-  __device__ void prologue(uint8_t*) const {}
-  __device__ int num_tiles(const uint8_t*) const { return NCT_OUT * ((p.T + TM - 1) / TM); }
-  __device__ int kblocks() const { return IS / tc::TK; }
-  __device__ uint32_t* status() const { return p.status; }
-  __device__ void tile(int i, TileInfo& t, const uint8_t*) const {
-    const int ntt = (p.T + TM - 1) / TM;
-    const int nt = i / ntt, mt = i % ntt;
-    t.amap = &hs;
-    t.a_row0 = mt * TM;
-    t.b_row0 = 0;
+// ================================================================ combine
+// y[t] = bf16(S[t] + sum_j Yb[inv(t, j)] in slot order (+ x[t])), fp32; one CTA per token,
+// each thread 8 columns (16-byte loads and stores, coalesced across the CTA).
+__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Params p) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int tok = blockIdx.x;
+  const int col = threadIdx.x * 8;
+  int rows[K];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      t.bmap[c] = &wsd;
-      t.bcol[c] = nt * 256 + c * 64;
+  for (int k = 0; k < K; ++k) rows[k] = __ldcg(p.inv + tok * K + k);
+  float v[8];
+  const float4* s4 = reinterpret_cast<const float4*>(p.S + (size_t)tok * H + col);
+  const float4 s0 = __ldcs(s4), s1 = __ldcs(s4 + 1);
+  v[0] = s0.x, v[1] = s0.y, v[2] = s0.z, v[3] = s0.w, v[4] = s1.x, v[5] = s1.y, v[6] = s1.z, v[7] = s1.w;
+  uint4 yk[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    if ((unsigned)rows[k] >= (unsigned)(p.T * K)) {
+      record_status(p.status, ST_BOUNDS);
+      rows[k] = 0;
     }
-    t.row0 = mt * TM;
-    t.valid = min(TM, p.T - mt * TM);
-    t.col0 = nt * 256;
-    t.aux = 0;
+    yk[k] = __ldcs(reinterpret_cast<const uint4*>(p.Yb + (size_t)rows[k] * H + col));
   }
-  // y[t] = bf16(S + sum_j Y[inv(t, j)] (+ x[t])), fp32, slot order
-  __device__ void epilogue(const TileInfo& t, uint32_t trow, int row, uint8_t*, const uint8_t*) const {
-    const bool ok = row < t.valid;
-    const int tok = t.row0 + row;
-    int rows[K];
 #pragma unroll
-    for (int k = 0; k < K; ++k) rows[k] = ok ? __ldcg(p.inv + tok * K + k) : 0;
-    const bool residual = (p.flags & 2u) != 0;
-#pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
-      float v[32];
-      tmem_ld32(trow + uint32_t(c * 32), v);
-      if (!ok) continue;
-      const int col = t.col0 + c * 32;
+  for (int k = 0; k < K; ++k) {
+    float f[8];
+    bf16x8_to_f32(yk[k], f);
 #pragma unroll
-      for (int k = 0; k < K; ++k) {
-        const uint4* y4 = reinterpret_cast<const uint4*>(p.Yb + (size_t)rows[k] * H + col);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float f[8];
-          bf16x8_to_f32(__ldcg(y4 + q), f);
-#pragma unroll
-          for (int z = 0; z < 8; ++z) v[q * 8 + z] += f[z];
-        }
-      }
-      if (residual) {
-        const uint4* x4 = reinterpret_cast<const uint4*>(p.x + (size_t)tok * H + col);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float f[8];
-          bf16x8_to_f32(__ldg(x4 + q), f);
-#pragma unroll
-          for (int z = 0; z < 8; ++z) v[q * 8 + z] += f[z];
-        }
-      }
-      store_bf16x32(p.y + (size_t)tok * H + col, v);
-    }
+    for (int z = 0; z < 8; ++z) v[z] += f[z];
   }
-};
+  if (p.flags & 2u) {
+    float f[8];
+    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(p.x + (size_t)tok * H + col)), f);
+#pragma unroll
+    for (int z = 0; z < 8; ++z) v[z] += f[z];
+  }
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  *reinterpret_cast<uint4*>(p.y + (size_t)tok * H + col) = make_uint4(w[0], w[1], w[2], w[3]);
+}
 
 }  // namespace pf
 }  // namespace flint

@@ -1,29 +1,46 @@
 // Tensor-core GEMM engine for sm_103a: tcgen05.mma with accumulators in TMEM, operands staged
 // in shared memory by TMA, one persistent CTA per SM.
 //
-// A tile computes D[128 x 256] += A[128 x K] * B[K x 256] in bf16 with fp32 accumulation:
-//   A: K-major (rows of A are contiguous in K), TMA box 64 (K) x 128 (rows), 128-byte swizzle;
-//   B: N-major (rows of B are contiguous in N, i.e. the weight matrices in y = x W order), four
-//      TMA boxes of 64 (N) x 64 (K rows) per stage, 128-byte swizzle -- each box may come from
-//      its own tensor map and column, so a tile can pair two matrices (gate | up);
-//   D: 256 fp32 TMEM columns; two buffers, so the epilogue of one tile overlaps the main loop
-//      of the next.
+// Two operands:
+//   X: activation rows, K-major (rows contiguous in K), TMA boxes of 64 (K) x 128 rows (ROWS)
+//      or 64 (K) x 64 rows (COLUMNS), 128-byte swizzle;
+//   W: weight columns, N-major (rows of W are contiguous in N, i.e. the matrices in y = x W
+//      order), TMA boxes of 64 (N) x 64 (K rows), 128-byte swizzle, 8 KB each -- every box may
+//      come from its own tensor map and column, so a tile can pair two matrices (gate | up).
+// A launch runs all its tiles in one of two orientations (Problem::kColumns):
+//   ROWS:    D[128 rows][256 cols] = X W, one MMA per K step (A = X, M = 128 rows; B = W,
+//            N = 256 columns); TMEM lane = activation row, TMEM column = output column.
+//            Pipeline: 4 stages of 48 KB (1 X box + 4 W boxes) per K block of 64.
+//   COLUMNS: D[128 cols][n rows] = (X W)^T, one MMA per K step (A = W read N-major, M = 128
+//            columns = W boxes 0 and 1; B = X read K-major, N = n rows, a multiple of 16 up to
+//            256); TMEM lane = W column (box 0 on lanes 0..63, box 1 on 64..127), TMEM column =
+//            activation row.  A group of rows costs its own size rounded up to 16 instead of
+//            whole 128-row tiles.  Pipeline: 4 stages of [X: up to 4 boxes of 64 rows, only
+//            ceil(n / 64) loaded, 32 KB | W: 2 boxes, 16 KB] per K block of 64.
+//   Both read 12 KB of shared memory per 128 x 256 x 16 MMA.  Either way a tile owns 256 fp32
+//   TMEM columns; two buffers, so the epilogue of one tile overlaps the main loop of the next.
 // Warp roles: warp 0 issues TMA (one lane), warp 1 allocates TMEM and issues the MMAs (one
 // lane), warps 2-5 run the epilogue (warp w reads TMEM lanes 32*(w%4) .. +31, one row each).
 // Every wait is bounded (1 s); on expiry the device status word gets ST_TIMEOUT and the
 // kernel runs to its end without hanging; TMEM is always released.
 //
 // A Problem class supplies the tile list and the epilogue:
+//   static constexpr bool kColumns;            // orientation of every tile
 //   void prologue(uint8_t* tbl) const;          // all threads, once: fill the table region
 //   int num_tiles(const uint8_t* tbl) const;  int kblocks() const;
 //   void tile(int i, TileInfo& t, const uint8_t* tbl) const;  // operand maps and coordinates
 //   void epilogue(const TileInfo& t, uint32_t tmem_row, int row, uint8_t* epi,
 //                 const uint8_t* tbl) const;
-//        called by each epilogue thread for its tile row `row` (0..127); tmem_row addresses
-//        column 0 of that row's accumulator (load with tmem_ld32, warp-collective, so every
-//        lane loads before any lane branches on its row); epi_sync() synchronises the 128
-//        epilogue threads
+//        called by each epilogue thread for its TMEM lane `row` (0..127: a tile row in ROWS
+//        mode, an output column in COLUMNS mode); tmem_row addresses column 0 of that lane's
+//        accumulator (load with tmem_ld32, warp-collective, so every lane loads before any
+//        lane branches on its row); epi_sync() synchronises the 128 epilogue threads
 //   uint32_t* status() const;
+//   unsigned long long* trace() const;  // null, or 8 slots of a TRACE_SLOTS-wide row per CTA
+//        that receive the CTA's wait profile: SM cycles the producer waited for free slots,
+//        the MMA issuer for loaded slots and for free accumulators, the first epilogue warp
+//        for full accumulators and inside the epilogue; the global timer (ns) at the start and
+//        the end; the tiles processed.
 #pragma once
 
 #include "common.cuh"
@@ -37,42 +54,50 @@ constexpr int TK = 64;
 constexpr int KSTEP = 16;
 constexpr int STAGES = 4;
 constexpr int A_BYTES = TM * TK * 2;            // 16 KB
+constexpr int XC_ROWS = 64;                     // rows of a COLUMNS-mode X box
+constexpr int XC_BYTES = XC_ROWS * TK * 2;      // 8 KB
 constexpr int B_CHUNK = TK * 64 * 2;            // 8 KB: 64 K rows x 64 columns
 constexpr int B_BYTES = 4 * B_CHUNK;            // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int EPI_SMEM = 2048;  // per-CTA scratch handed to the epilogue
+constexpr int EPI_SMEM = 8192;  // per-CTA scratch handed to the epilogue
+constexpr int align_up_c(int v, int a) { return (v + a - 1) / a * a; }
 constexpr int TBL_SMEM = 4096;  // per-CTA table filled by the problem's prologue
 
-// kind::f16 instruction descriptor: D fp32, A and B bf16, A K-major, B MN-major, N = 256,
-// M = 128.
+// kind::f16 instruction descriptors: D fp32 (bits 4-5 = 1), A and B bf16 (bits 7-9 and
+// 10-12 = 1), bit 15 = A MN-major, bit 16 = B MN-major, N >> 3 at bit 17, M >> 4 at bit 24.
+// ROWS: A = X K-major, B = W N-major, N = 256, M = 128.
 constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
                            (uint32_t(TN >> 3) << 17) | (uint32_t(TM >> 4) << 24);
+// COLUMNS: A = W N-major (M = 128 of its columns), B = X K-major (N = n rows, <= 256).
+__host__ __device__ constexpr uint32_t idesc_columns(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (0u << 16) | (uint32_t(n >> 3) << 17) |
+         (uint32_t(TM >> 4) << 24);
+}
 
 struct Smem {
-  static constexpr int stages = 0;
-  static constexpr int full = stages + STAGES * STAGE_BYTES;
-  static constexpr int empty = full + 8 * STAGES;
-  static constexpr int tfull = empty + 8 * STAGES;
-  static constexpr int tempty = tfull + 16;
-  static constexpr int tmem_slot = tempty + 16;
-  static constexpr int epi = tmem_slot + 16;
+  static constexpr int stages = 0;  // STAGES x 48 KB
+  static constexpr int bars = stages + STAGES * STAGE_BYTES;  // 16 mbarriers
+  static constexpr int tmem_slot = bars + 8 * 16;
+  static constexpr int epi = align_up_c(tmem_slot + 16, 128);
   static constexpr int tbl = epi + EPI_SMEM;
   static constexpr int bytes = tbl + TBL_SMEM;
 };
 constexpr int SMEM_BYTES = Smem::bytes + 1024;
+constexpr int BAR_FULL = 0, BAR_EMPTY = 4, BAR_TFULL = 8, BAR_TEMPTY = 10;
 
 struct TileInfo {
-  const CUtensorMap* amap;  // A operand
-  int a_row0;               // first A row (TMA coordinate)
-  int b_row0;               // first B row (K offset of the B matrix in its tensor map)
+  const CUtensorMap* amap;  // X operand (activation rows)
+  int a_row0;               // first X row (TMA coordinate)
+  int b_row0;               // first W row (K offset of the weight matrix in its tensor map)
   const CUtensorMap* bmap[4];
-  int bcol[4];              // column (N) coordinate of each of the four B boxes
+  int bcol[4];              // column (N) coordinate of each of the four W boxes
   int row0;                 // problem-specific: first output row
   int valid;                // rows of this tile that are real
   int col0;                 // problem-specific: first output column
   int aux;                  // problem-specific
+  int n = 0;                // COLUMNS: rows fed to the MMA (valid rounded up to 16, <= 256)
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -81,11 +106,12 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
          (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate));
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -136,20 +162,23 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* raw) {
 // ------------------------------------------------------------------ the kernel
 template <class Problem>
 __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_constant__ Problem prob) {
+  constexpr bool cols = Problem::kColumns;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + Smem::full);
-  uint64_t* empty = reinterpret_cast<uint64_t*>(sm + Smem::empty);
-  uint64_t* tfull = reinterpret_cast<uint64_t*>(sm + Smem::tfull);
-  uint64_t* tempty = reinterpret_cast<uint64_t*>(sm + Smem::tempty);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Smem::bars);
+  uint64_t* tfull = bars + BAR_TFULL;
+  uint64_t* tempty = bars + BAR_TEMPTY;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Smem::tmem_slot);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint32_t* status = prob.status();
+  unsigned long long* trace = prob.trace();
+  if (trace) trace += (size_t)blockIdx.x * TRACE_SLOTS;
+  if (trace && threadIdx.x == 0) trace[5] = globaltimer_ns();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full + s, 1);
-      mbar_init(empty + s, 1);
+      mbar_init(bars + BAR_FULL + s, 1);
+      mbar_init(bars + BAR_EMPTY + s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull + b, 1);
@@ -176,48 +205,95 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
   const int kb_n = prob.kblocks();
 
   if (warp == 0) {
-    // ---------------- TMA producer
-    if (lane == 0) {
+    // ---------------- producer
+    long long w_wait = 0;
+    if constexpr (cols) {
+      if (lane == 0) {
+        int pos = 0;
+        for (int i = blockIdx.x; i < ntiles; i += gridDim.x) {
+          TileInfo t;
+          prob.tile(i, t, tbl);
+          const int nxb = (t.n + XC_ROWS - 1) / XC_ROWS;  // 1..4 X boxes of 64 rows
+          for (int kb = 0; kb < kb_n; ++kb, ++pos) {
+            const int st = pos % STAGES, use = pos / STAGES;
+            const long long c0 = clock64();
+            if (use > 0) wait_bar(bars + BAR_EMPTY + st, uint32_t(use - 1) & 1u, status);
+            w_wait += clock64() - c0;
+            uint8_t* x = sm + Smem::stages + st * STAGE_BYTES;
+            uint8_t* w = x + 2 * A_BYTES;
+            uint64_t* full = bars + BAR_FULL + st;
+            mbar_arrive_expect_tx(full, uint32_t(nxb * XC_BYTES + 2 * B_CHUNK));
+            for (int c = 0; c < nxb; ++c) tma_load_2d(x + c * XC_BYTES, t.amap, kb * TK, t.a_row0 + c * XC_ROWS, full);
+            tma_load_2d(w, t.bmap[0], t.bcol[0], t.b_row0 + kb * TK, full);
+            tma_load_2d(w + B_CHUNK, t.bmap[1], t.bcol[1], t.b_row0 + kb * TK, full);
+          }
+        }
+      }
+    } else if (lane == 0) {
       int pos = 0;
       for (int i = blockIdx.x; i < ntiles; i += gridDim.x) {
         TileInfo t;
         prob.tile(i, t, tbl);
         for (int kb = 0; kb < kb_n; ++kb, ++pos) {
           const int st = pos % STAGES, use = pos / STAGES;
-          if (use > 0) wait_bar(empty + st, uint32_t(use - 1) & 1u, status);
+          const long long c0 = clock64();
+          if (use > 0) wait_bar(bars + BAR_EMPTY + st, uint32_t(use - 1) & 1u, status);
+          w_wait += clock64() - c0;
           uint8_t* a = sm + Smem::stages + st * STAGE_BYTES;
           uint8_t* b = a + A_BYTES;
-          mbar_arrive_expect_tx(full + st, STAGE_BYTES);
-          tma_load_2d(a, t.amap, kb * TK, t.a_row0, full + st);
+          mbar_arrive_expect_tx(bars + BAR_FULL + st, STAGE_BYTES);
+          tma_load_2d(a, t.amap, kb * TK, t.a_row0, bars + BAR_FULL + st);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tma_load_2d(b + c * B_CHUNK, t.bmap[c], t.bcol[c], t.b_row0 + kb * TK, full + st);
+          for (int c = 0; c < 4; ++c)
+            tma_load_2d(b + c * B_CHUNK, t.bmap[c], t.bcol[c], t.b_row0 + kb * TK, bars + BAR_FULL + st);
         }
       }
     }
+    if (trace && lane == 0) trace[0] = (unsigned long long)w_wait;
   } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0) {
       int pos = 0, it = 0;
+      long long w_full = 0, w_tempty = 0;
       for (int i = blockIdx.x; i < ntiles; i += gridDim.x, ++it) {
+        TileInfo t;
+        prob.tile(i, t, tbl);
+        const uint32_t idesc = cols ? idesc_columns(t.n) : IDESC;
         const int buf = it & 1, use = it >> 1;
+        long long c0 = clock64();
         if (use > 0) wait_bar(tempty + buf, uint32_t(use - 1) & 1u, status);
+        w_tempty += clock64() - c0;
         tc_fence_after();
         const uint32_t d = tmem_base + uint32_t(buf * TN);
         for (int kb = 0; kb < kb_n; ++kb, ++pos) {
+          uint32_t x, w;
+          c0 = clock64();
           const int st = pos % STAGES;
-          wait_bar(full + st, uint32_t(pos / STAGES) & 1u, status);
+          wait_bar(bars + BAR_FULL + st, uint32_t(pos / STAGES) & 1u, status);
+          x = smem_u32(sm + Smem::stages + st * STAGE_BYTES);
+          w = x + (cols ? 2 : 1) * A_BYTES;
+          w_full += clock64() - c0;
           tc_fence_after();
-          const uint32_t a = smem_u32(sm + Smem::stages + st * STAGE_BYTES);
-          const uint32_t b = a + A_BYTES;
 #pragma unroll
           for (int s = 0; s < TK / KSTEP; ++s) {
-            const uint64_t ad = smem_desc(a + s * (KSTEP * 2), 16, 1024);
-            const uint64_t bd = smem_desc(b + s * (KSTEP * 128), B_CHUNK, 1024);
-            mma_bf16(d, ad, bd, (kb | s) != 0 ? 1u : 0u);
+            // X K-major: a K step is 32 bytes along the swizzled row (8-row groups 1 KB apart);
+            // W N-major: a K step is 16 rows of 128 bytes, 64-column boxes 8 KB apart
+            const uint64_t xd = smem_desc(x + s * (KSTEP * 2), 16, 1024);
+            const uint64_t wd = smem_desc(w + s * (KSTEP * 128), B_CHUNK, 1024);
+            const uint32_t acc = (kb | s) != 0 ? 1u : 0u;
+            if constexpr (cols)
+              mma_bf16(d, wd, xd, idesc, acc);
+            else
+              mma_bf16(d, xd, wd, idesc, acc);
           }
-          mma_commit(empty + st);  // the stage is free once these MMAs have read it
+          // the slots are free once these MMAs have read them
+          mma_commit(bars + BAR_EMPTY + st);
         }
         mma_commit(tfull + buf);  // the accumulator is complete
+      }
+      if (trace) {
+        trace[1] = (unsigned long long)w_full;
+        trace[2] = (unsigned long long)w_tempty;
       }
     }
   } else {
@@ -225,14 +301,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     int it = 0;
+    long long w_tfull = 0, busy = 0;
     for (int i = blockIdx.x; i < ntiles; i += gridDim.x, ++it) {
       const int buf = it & 1;
+      const long long c0 = clock64();
       if (lane == 0) wait_bar(tfull + buf, uint32_t(it >> 1) & 1u, status);
       __syncwarp();
       while (!mbar_try_wait(tfull + buf, uint32_t(it >> 1) & 1u)) {
         if (*reinterpret_cast<volatile uint32_t*>(status) & ST_TIMEOUT) break;
       }
       tc_fence_after();
+      const long long c1 = clock64();
       TileInfo t;
       prob.tile(i, t, tbl);
       const uint32_t trow = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(buf * TN);
@@ -240,12 +319,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty + buf);
+      w_tfull += c1 - c0;
+      busy += clock64() - c1;
+    }
+    if (trace && warp == 2 && lane == 0) {
+      trace[3] = (unsigned long long)w_tfull;
+      trace[4] = (unsigned long long)busy;
+      trace[7] = (unsigned long long)it;
     }
   }
   // wait for the last accumulators to be consumed, then release TMEM
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (trace && threadIdx.x == 0) trace[6] = globaltimer_ns();
   if (warp == 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
 }
