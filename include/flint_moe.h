@@ -62,6 +62,12 @@ typedef enum {
 /* config.flags */
 #define FLINT_MOE_FLAG_PRE_RMSNORM 0x1u /* route and run the experts on r = x / rms(x)     */
 #define FLINT_MOE_FLAG_RESIDUAL 0x2u    /* y = x + MoE(...) (y may alias x)                 */
+/* For tests of the device-timeout path only: every route / forward call makes one bounded device
+ * wait on a workspace word that nothing writes.  The wait gives up after 0.25 s (a quarter of
+ * the 1 s limit of every other device wait, so the call's results are unaffected) and records
+ * the timeout: flint_moe_poll_device_status then returns FLINT_MOE_ERR_DEVICE_TIMEOUT, and the
+ * context stays usable.  It is not part of the method. */
+#define FLINT_MOE_FLAG_TEST_WAIT_TIMEOUT 0x80000000u
 
 typedef struct {
   int hidden;       /* must be 2048 */

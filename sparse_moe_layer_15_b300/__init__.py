@@ -15,6 +15,7 @@ LIB_NAME = "libflint_moe.so"
 HIDDEN, N_EXPERTS, TOP_K, EXPERT_INTER, SHARED_INTER = 2048, 256, 6, 512, 1024
 FLAG_PRE_RMSNORM = 0x1
 FLAG_RESIDUAL = 0x2
+FLAG_TEST_WAIT_TIMEOUT = 0x80000000  # tests of the device-timeout path only
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "cuda error",
           5: "device timeout", 6: "device bounds"}

@@ -158,6 +158,22 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return true;
 }
 
+// FLINT_MOE_FLAG_TEST_WAIT_TIMEOUT (tests of the device-timeout path only): one thread waits
+// for a workspace word that nothing ever writes (status[1]), gives up after a quarter of the
+// wait limit -- shorter than every other bounded wait, so the rest of the call proceeds
+// normally -- and records ST_TIMEOUT.
+constexpr unsigned FLAG_TEST_WAIT_TIMEOUT = 0x80000000u;
+__device__ __forceinline__ void test_wait_timeout(uint32_t* status) {
+  const volatile uint32_t* never = status + 1;
+  const uint64_t t0 = globaltimer_ns();
+  while (*never == 0u) {
+    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS / 4) {
+      record_status(status, ST_TIMEOUT);
+      return;
+    }
+  }
+}
+
 // 1-D bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16), completing
 // `bytes` transaction bytes on `bar`.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

@@ -910,6 +910,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   trace_point(p, 0);
   pdl_wait();  // inputs of this forward and the workspace are ready
   trace_point(p, 1);
+  if ((p.flags & FLAG_TEST_WAIT_TIMEOUT) && blockIdx.x == 0 && threadIdx.x == 0) test_wait_timeout(p.status);
 
   // ---- step A: router partial logits and the shared gate/up
   {

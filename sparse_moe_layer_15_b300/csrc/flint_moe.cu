@@ -15,6 +15,8 @@
 
 using namespace flint;
 
+static_assert(FLINT_MOE_FLAG_TEST_WAIT_TIMEOUT == flint::FLAG_TEST_WAIT_TIMEOUT, "flag value");
+
 namespace {
 
 constexpr int MAX_TOKENS_LIMIT = 65536;
@@ -147,7 +149,8 @@ flint_moe_status check_config(const flint_moe_config* c) {
   if (c->hidden != H || c->n_experts != E || c->top_k != K || c->expert_inter != I || c->shared_inter != IS)
     return FLINT_MOE_ERR_UNSUPPORTED;
   if (c->max_tokens < 1 || c->max_tokens > MAX_TOKENS_LIMIT) return FLINT_MOE_ERR_INVALID_ARG;
-  if (c->flags & ~(FLINT_MOE_FLAG_PRE_RMSNORM | FLINT_MOE_FLAG_RESIDUAL)) return FLINT_MOE_ERR_UNSUPPORTED;
+  if (c->flags & ~(FLINT_MOE_FLAG_PRE_RMSNORM | FLINT_MOE_FLAG_RESIDUAL | FLINT_MOE_FLAG_TEST_WAIT_TIMEOUT))
+    return FLINT_MOE_ERR_UNSUPPORTED;
   if ((c->flags & FLINT_MOE_FLAG_PRE_RMSNORM) && !(c->rms_eps > 0.f)) return FLINT_MOE_ERR_INVALID_ARG;
   return FLINT_MOE_OK;
 }

@@ -67,7 +67,9 @@ struct RouterTC {
   static constexpr bool kColumns = false;
   Params p;
   CUtensorMap xin, wr;
-  __device__ void prologue(uint8_t*) const {}
+  __device__ void prologue(uint8_t*) const {
+    if ((p.flags & FLAG_TEST_WAIT_TIMEOUT) && blockIdx.x == 0 && threadIdx.x == 0) test_wait_timeout(p.status);
+  }
   __device__ int num_tiles(const uint8_t*) const { return (p.T + TM - 1) / TM; }
   __device__ int kblocks() const { return H / tc::TK; }
   __device__ uint32_t* status() const { return p.status; }
