@@ -319,8 +319,7 @@ WORKLOADS = {
 PF_KERNEL_FLOPS_PER_TOKEN = {
     "pf_router": 2 * 2048 * 256,
     "pf_gateup": 6 * 2 * 2 * 2048 * 512 + 2 * 2 * 2048 * 1024,
-    "pf_down": 6 * 2 * 512 * 2048,
-    "pf_shared_down": 2 * 1024 * 2048,
+    "pf_down": 6 * 2 * 512 * 2048 + 2 * 1024 * 2048,  # routed and shared down projections
 }
 
 

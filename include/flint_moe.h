@@ -29,7 +29,7 @@
  *     workspace holds only per-call scratch, and its counters return to zero at the end of
  *     every call.
  *   - T <= 256 runs the decode-size path (one persistent cooperative kernel); larger T runs
- *     the tensor-core path (seven kernels).
+ *     the tensor-core path (five kernels).  Pre-norm adds one RMSNorm kernel to either.
  *   - The only supported shape is the Flint layer's (hidden 2048, 256 experts, top-6,
  *     widths 512 / 1024); any other returns FLINT_MOE_ERR_UNSUPPORTED, as does a device
  *     that is not compute capability 10.3 (the serving kit likewise refuses configurations

@@ -262,8 +262,8 @@ flint_moe_status run_decode(flint_moe_t h, const Params& p, cudaStream_t st, boo
   return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ERR_CUDA;
 }
 
-// The layer on T > STREAM_MAX_T tokens: the tensor-core path (prefill_kernels.cuh), seven
-// stream-ordered kernels with programmatic dependent launch.
+// The layer on T > STREAM_MAX_T tokens: the tensor-core path (prefill_kernels.cuh), five (six
+// with pre-norm) stream-ordered kernels with programmatic dependent launch.
 flint_moe_status run_prefill(flint_moe_t h, const Params& p, cudaStream_t st, bool full) {
   const int T = p.T;
   const int ntile = (T + tc::TM - 1) / tc::TM;
@@ -289,14 +289,9 @@ flint_moe_status run_prefill(flint_moe_t h, const Params& p, cudaStream_t st, bo
   pf::GateUpTC gu{p, h->pmaps.xs, xin_c, h->pmaps.wg, h->pmaps.wu, h->pmaps.wsg, h->pmaps.wsu};
   if (e == cudaSuccess)
     e = launch(h, "pf_gateup", tc::gemm_kernel<pf::GateUpTC>, n_sm, tc::NUM_THREADS, tc::SMEM_BYTES, st, false, gu);
-  pf::DownTC dn{p, h->pmaps.h, h->pmaps.wd};
+  pf::DownTC dn{p, h->pmaps.h, h->pmaps.wd, h->pmaps.hs, h->pmaps.wsd};
   if (e == cudaSuccess)
     e = launch(h, "pf_down", tc::gemm_kernel<pf::DownTC>, n_sm, tc::NUM_THREADS, tc::SMEM_BYTES, st, false, dn);
-  pf::SharedDownTC sd{p, h->pmaps.hs, h->pmaps.wsd};
-  const int sd_tiles = ((T + pf::RG - 1) / pf::RG) * pf::NCT_DN;
-  if (e == cudaSuccess)
-    e = launch(h, "pf_shared_down", tc::gemm_kernel<pf::SharedDownTC>, sd_tiles < n_sm ? sd_tiles : n_sm,
-               tc::NUM_THREADS, tc::SMEM_BYTES, st, false, sd);
   if (e == cudaSuccess) e = launch(h, "pf_combine", pf::combine_kernel, T, 256, 0, st, false, p);
   return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ERR_CUDA;
 }
@@ -342,9 +337,6 @@ cudaError_t set_prefill_smem() {
                              tc::SMEM_BYTES);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(tc::gemm_kernel<pf::DownTC>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(tc::gemm_kernel<pf::SharedDownTC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             tc::SMEM_BYTES);
   return e;
 }
 

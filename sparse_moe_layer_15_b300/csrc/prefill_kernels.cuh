@@ -12,8 +12,8 @@
 //             orientation (N = the group's rows rounded up to 16), then the shared expert over
 //             (64-column pair, 256-token group): h = bf16(silu(g) * u);
 //   down      grouped over (expert, 128 output columns, 256-row group), COLUMNS: epilogue
-//             Yb[row] = bf16(gate(row) * acc);
-//   shared down  over (128 output columns, 256-token group), COLUMNS: S[t] = acc (fp32);
+//             Yb[row] = bf16(gate(row) * acc); then the shared expert's down projection over
+//             (128 output columns, 256-token group): S[t] = acc (fp32);
 //   combine   y[t] = bf16(S[t] + sum_j Yb[inv(t, j)] in slot order (+ x[t])).
 // Tiles of one expert's weight column block are numbered consecutively with the row group
 // fastest, so concurrent CTAs share each weight tile through L2.
@@ -317,6 +317,18 @@ struct GroupTable {
   }
 };
 
+// Position p of a list of R routed tiles followed by S shared-expert tiles: returns true and
+// the shared tile's index, or false and the routed tile's index.  (Spreading the shared tiles
+// evenly through the routed ones was measured slower: 0.746 vs 0.684 ms per layer at T = 8192.)
+__device__ __forceinline__ bool shared_tile(int p, int R, int& idx) {
+  if (p >= R) {
+    idx = p - R;
+    return true;
+  }
+  idx = p;
+  return false;
+}
+
 // ================================================================ gate/up (routed + shared)
 // COLUMNS tiles: 64 columns of gate (TMEM lanes 0..63) and the same 64 columns of up (lanes
 // 64..127), and up to RG = 256 rows as the MMA's N (rounded up to 16): a routed expert's rows
@@ -338,10 +350,11 @@ struct GateUpTC {
     const int* mtp = reinterpret_cast<const int*>(tbl);
     const int* off = mtp + (E + 1);
     const int routed = NCT_GU * mtp[E];
-    if (i < routed) {
-      const int e = GroupTable::find(mtp, NCT_GU, i);
+    int j;
+    if (!shared_tile(i, routed, j)) {
+      const int e = GroupTable::find(mtp, NCT_GU, j);
       const int mte = mtp[e + 1] - mtp[e];
-      const int local = i - NCT_GU * mtp[e];
+      const int local = j - NCT_GU * mtp[e];
       const int nt = local / mte, mt = local % mte;
       t.amap = &xs;
       t.a_row0 = off[e] + mt * RG;
@@ -354,7 +367,6 @@ struct GateUpTC {
       t.aux = 0;
     } else {
       const int ng = (p.T + RG - 1) / RG;
-      const int j = i - routed;
       const int nt = j / ng, g = j % ng;
       t.amap = &xin_c;
       t.a_row0 = g * RG;
@@ -402,38 +414,69 @@ struct GateUpTC {
   }
 };
 
-// ================================================================ routed down
-// COLUMNS: 128 output columns on the TMEM lanes, up to RG = 256 of the expert's rows as N.
-// Epilogue: Yb[row][col] = bf16(gate(row) * acc).
+// ================================================================ down (routed + shared)
+// COLUMNS: 128 output columns on the TMEM lanes and up to RG = 256 rows as N -- a routed
+// expert's rows (h, K = 512; epilogue Yb[row][col] = bf16(gate(row) * acc)) or a 256-token
+// group of the shared expert (hs, K = 1024; epilogue S[t][col] = acc in fp32) after the routed
+// tiles.
 struct DownTC {
   static constexpr bool kColumns = true;
   Params p;
-  CUtensorMap h, wd;
+  CUtensorMap h, wd, hs, wsd;
   __device__ void prologue(uint8_t* tbl) const { GroupTable::load(p, tbl); }
-  __device__ int num_tiles(const uint8_t* tbl) const { return NCT_DN * reinterpret_cast<const int*>(tbl)[E]; }
+  __device__ int num_tiles(const uint8_t* tbl) const {
+    return NCT_DN * (reinterpret_cast<const int*>(tbl)[E] + (p.T + RG - 1) / RG);
+  }
   __device__ int kblocks() const { return I / tc::TK; }
   __device__ uint32_t* status() const { return p.status; }
   __device__ unsigned long long* trace() const { return p.trace ? p.trace + 8 : nullptr; }  // slots 8..15
   __device__ void tile(int i, TileInfo& t, const uint8_t* tbl) const {
     const int* mtp = reinterpret_cast<const int*>(tbl);
     const int* off = mtp + (E + 1);
-    const int e = GroupTable::find(mtp, NCT_DN, i);
-    const int mte = mtp[e + 1] - mtp[e];
-    const int local = i - NCT_DN * mtp[e];
-    const int nt = local / mte, mt = local % mte;
-    t.amap = &h;
-    t.a_row0 = off[e] + mt * RG;
-    t.b_row0 = e * I;
-    t.bmap[0] = t.bmap[1] = &wd;
-    t.bcol[0] = nt * 128;
-    t.bcol[1] = nt * 128 + 64;
-    t.row0 = off[e] + mt * RG;
-    t.valid = min(RG, off[e + 1] - off[e] - mt * RG);
-    t.col0 = nt * 128;
-    t.aux = e;
+    const int ng = (p.T + RG - 1) / RG;
+    int j;
+    if (!shared_tile(i, NCT_DN * mtp[E], j)) {
+      const int e = GroupTable::find(mtp, NCT_DN, j);
+      const int mte = mtp[e + 1] - mtp[e];
+      const int local = j - NCT_DN * mtp[e];
+      const int nt = local / mte, mt = local % mte;
+      t.amap = &h;
+      t.a_row0 = off[e] + mt * RG;
+      t.b_row0 = e * I;
+      t.bmap[0] = t.bmap[1] = &wd;
+      t.row0 = off[e] + mt * RG;
+      t.valid = min(RG, off[e + 1] - off[e] - mt * RG);
+      t.col0 = nt * 128;
+      t.aux = e;
+    } else {
+      const int nt = j / ng, g = j % ng;
+      t.amap = &hs;
+      t.a_row0 = g * RG;
+      t.b_row0 = 0;
+      t.bmap[0] = t.bmap[1] = &wsd;
+      t.row0 = g * RG;
+      t.valid = min(RG, p.T - g * RG);
+      t.col0 = nt * 128;
+      t.aux = -1;
+      t.nkb = IS / tc::TK;
+    }
+    t.bcol[0] = t.col0;
+    t.bcol[1] = t.col0 + 64;
     t.n = (t.valid + 15) & ~15;
   }
   __device__ void epilogue(const TileInfo& t, uint32_t trow, int row, uint8_t* epi, const uint8_t*) const {
+    if (t.aux < 0) {
+      float* dst = p.S + (size_t)t.row0 * H + t.col0 + row;
+#pragma unroll 1
+      for (int c = 0; c * 32 < t.valid; ++c) {
+        float v[32];
+        tmem_ld32(trow + uint32_t(c * 32), v);
+#pragma unroll
+        for (int q = 0; q < 32; ++q)
+          if (c * 32 + q < t.valid) dst[(size_t)(c * 32 + q) * H] = v[q];
+      }
+      return;
+    }
     float* gate = reinterpret_cast<float*>(epi);  // gate of each of the tile's rows
 #pragma unroll
     for (int k = 0; k < RG / TM; ++k) {
@@ -451,45 +494,6 @@ struct DownTC {
         if (c * 32 + q < t.valid) dst[(size_t)(c * 32 + q) * H] = __float2bfloat16_rn(v[q] * gate[c * 32 + q]);
     }
     epi_sync();  // the next tile rewrites the gates
-  }
-};
-
-// ================================================================ shared down
-// COLUMNS over (128 output columns, 256-token group): S[t][col] = acc in fp32.
-struct SharedDownTC {
-  static constexpr bool kColumns = true;
-  Params p;
-  CUtensorMap hs, wsd;
-  __device__ void prologue(uint8_t*) const {}
-  __device__ int num_tiles(const uint8_t*) const { return NCT_DN * ((p.T + RG - 1) / RG); }
-  __device__ int kblocks() const { return IS / tc::TK; }
-  __device__ uint32_t* status() const { return p.status; }
-  __device__ unsigned long long* trace() const { return nullptr; }
-  __device__ void tile(int i, TileInfo& t, const uint8_t*) const {
-    const int ng = (p.T + RG - 1) / RG;
-    const int nt = i / ng, g = i % ng;
-    t.amap = &hs;
-    t.a_row0 = g * RG;
-    t.b_row0 = 0;
-    t.bmap[0] = t.bmap[1] = &wsd;
-    t.bcol[0] = nt * 128;
-    t.bcol[1] = nt * 128 + 64;
-    t.row0 = g * RG;
-    t.valid = min(RG, p.T - g * RG);
-    t.col0 = nt * 128;
-    t.aux = 0;
-    t.n = (t.valid + 15) & ~15;
-  }
-  __device__ void epilogue(const TileInfo& t, uint32_t trow, int row, uint8_t*, const uint8_t*) const {
-    float* dst = p.S + (size_t)t.row0 * H + t.col0 + row;
-#pragma unroll 1
-    for (int c = 0; c * 32 < t.valid; ++c) {
-      float v[32];
-      tmem_ld32(trow + uint32_t(c * 32), v);
-#pragma unroll
-      for (int q = 0; q < 32; ++q)
-        if (c * 32 + q < t.valid) dst[(size_t)(c * 32 + q) * H] = v[q];
-    }
   }
 };
 

@@ -27,7 +27,8 @@
 // A Problem class supplies the tile list and the epilogue:
 //   static constexpr bool kColumns;            // orientation of every tile
 //   void prologue(uint8_t* tbl) const;          // all threads, once: fill the table region
-//   int num_tiles(const uint8_t* tbl) const;  int kblocks() const;
+//   int num_tiles(const uint8_t* tbl) const;
+//   int kblocks() const;                        // K blocks of 64 per tile, unless TileInfo::nkb says otherwise
 //   void tile(int i, TileInfo& t, const uint8_t* tbl) const;  // operand maps and coordinates
 //   void epilogue(const TileInfo& t, uint32_t tmem_row, int row, uint8_t* epi,
 //                 const uint8_t* tbl) const;
@@ -98,6 +99,7 @@ struct TileInfo {
   int col0;                 // problem-specific: first output column
   int aux;                  // problem-specific
   int n = 0;                // COLUMNS: rows fed to the MMA (valid rounded up to 16, <= 256)
+  int nkb = 0;              // K blocks of this tile (0: Problem::kblocks())
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -214,7 +216,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           TileInfo t;
           prob.tile(i, t, tbl);
           const int nxb = (t.n + XC_ROWS - 1) / XC_ROWS;  // 1..4 X boxes of 64 rows
-          for (int kb = 0; kb < kb_n; ++kb, ++pos) {
+          const int nkb = t.nkb ? t.nkb : kb_n;
+          for (int kb = 0; kb < nkb; ++kb, ++pos) {
             const int st = pos % STAGES, use = pos / STAGES;
             const long long c0 = clock64();
             if (use > 0) wait_bar(bars + BAR_EMPTY + st, uint32_t(use - 1) & 1u, status);
@@ -234,7 +237,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       for (int i = blockIdx.x; i < ntiles; i += gridDim.x) {
         TileInfo t;
         prob.tile(i, t, tbl);
-        for (int kb = 0; kb < kb_n; ++kb, ++pos) {
+        const int nkb = t.nkb ? t.nkb : kb_n;
+        for (int kb = 0; kb < nkb; ++kb, ++pos) {
           const int st = pos % STAGES, use = pos / STAGES;
           const long long c0 = clock64();
           if (use > 0) wait_bar(bars + BAR_EMPTY + st, uint32_t(use - 1) & 1u, status);
@@ -265,7 +269,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         w_tempty += clock64() - c0;
         tc_fence_after();
         const uint32_t d = tmem_base + uint32_t(buf * TN);
-        for (int kb = 0; kb < kb_n; ++kb, ++pos) {
+        const int nkb = t.nkb ? t.nkb : kb_n;
+        for (int kb = 0; kb < nkb; ++kb, ++pos) {
           uint32_t x, w;
           c0 = clock64();
           const int st = pos % STAGES;
