@@ -65,6 +65,12 @@ def measured_traffic(kernel, sweep):
     return round(sum(per[str(T)] for T in sweep) / len(sweep))
 
 
+# The B300's nominal HBM3e bandwidth and dense bf16 rate, for the "spec" fractions next to the
+# measured ones.
+SPEC_HBM_GBS = 8000.0
+SPEC_BF16_TFLOPS = 2250.0
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -235,10 +241,13 @@ def run_ours(args, rank, world, local):
     sweep = {}
     for T in SWEEP:
         med = statistics.median(times[T])
+        q = sorted(times[T])
         b = acc.algorithmic_bytes(U[T], T)
-        sweep[str(T)] = dict(us=round(med * 1e3, 2), tokens_per_s=round(T / (med * 1e-3), 1), touched_experts=U[T],
-                             alg_bytes=b, gbs=round(b / (med * 1e-3) / 1e9, 1),
-                             hbm_frac=round(b / (med * 1e-3) / 1e9 / peaks["hbm_gbs"], 4))
+        sweep[str(T)] = dict(us=round(med * 1e3, 2), us_p10=round(q[len(q) // 10] * 1e3, 2),
+                             us_p90=round(q[(9 * len(q)) // 10] * 1e3, 2), tokens_per_s=round(T / (med * 1e-3), 1),
+                             touched_experts=U[T], alg_bytes=b, gbs=round(b / (med * 1e-3) / 1e9, 1),
+                             hbm_frac=round(b / (med * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                             hbm_frac_spec=round(b / (med * 1e-3) / 1e9 / SPEC_HBM_GBS, 4))
 
     # per-kernel times (second pass with kernel events; same workload, same flushes)
     layer.enable_kernel_timing(True)
@@ -265,6 +274,7 @@ def run_ours(args, rank, world, local):
     traffic = measured_traffic(dom, SWEEP)
     roofline = dict(bound="hbm", kernel=dom, achieved=round(achieved, 1), peak=peaks["hbm_gbs"], unit="GB/s",
                     frac=round(achieved / peaks["hbm_gbs"], 4), traffic=traffic,
+                    frac_vs_spec=round(achieved / SPEC_HBM_GBS, 4),
                     alg_bytes_per_launch=round(dom_bytes), peak_source=peaks["source"] + " (hbm_gbs, copy test)",
                     note="per-launch means over the sweep's 7 launches; traffic: DRAM read+write bytes per "
                          "launch from the committed ncu summary (null if the kernel sources changed since)")
@@ -407,6 +417,7 @@ def run_workload(args, rank, world, local):
         achieved = PF_KERNEL_FLOPS_PER_TOKEN[dom] * T / (dom_ms * 1e-3) / 1e12
         roofline = dict(bound="tensor", kernel=dom, achieved=round(achieved, 1), peak=peaks["bf16_tflops"],
                         unit="TFLOP/s", frac=round(achieved / peaks["bf16_tflops"], 4), traffic=None,
+                        frac_vs_spec=round(achieved / SPEC_BF16_TFLOPS, 4),
                         alg_flop_per_launch=PF_KERNEL_FLOPS_PER_TOKEN[dom] * T,
                         peak_source=peaks["source"] + " (bf16_tflops, burst)",
                         note="algorithmic FLOPs of the kernel (no tile padding) / its CUDA-event time")

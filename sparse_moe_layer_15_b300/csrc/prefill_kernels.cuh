@@ -15,8 +15,9 @@
 //             Yb[row] = bf16(gate(row) * acc); then the shared expert's down projection over
 //             (128 output columns, 256-token group): S[t] = acc (fp32);
 //   combine   y[t] = bf16(S[t] + sum_j Yb[inv(t, j)] in slot order (+ x[t])).
-// Tiles of one expert's weight column block are numbered consecutively with the row group
-// fastest, so concurrent CTAs share each weight tile through L2.
+// An expert's tiles are numbered with the column block fastest: the CTAs working at the same time
+// read whole weight rows (all column blocks of one row group) and the next row group of the
+// expert finds its weights in L2.
 #pragma once
 
 #include "common.cuh"
@@ -353,9 +354,8 @@ struct GateUpTC {
     int j;
     if (!shared_tile(i, routed, j)) {
       const int e = GroupTable::find(mtp, NCT_GU, j);
-      const int mte = mtp[e + 1] - mtp[e];
       const int local = j - NCT_GU * mtp[e];
-      const int nt = local / mte, mt = local % mte;
+      const int mt = local / NCT_GU, nt = local % NCT_GU;  // column blocks of a row group together
       t.amap = &xs;
       t.a_row0 = off[e] + mt * RG;
       t.b_row0 = e * H;
@@ -437,9 +437,8 @@ struct DownTC {
     int j;
     if (!shared_tile(i, NCT_DN * mtp[E], j)) {
       const int e = GroupTable::find(mtp, NCT_DN, j);
-      const int mte = mtp[e + 1] - mtp[e];
       const int local = j - NCT_DN * mtp[e];
-      const int nt = local / mte, mt = local % mte;
+      const int mt = local / NCT_DN, nt = local % NCT_DN;  // column blocks of a row group together
       t.amap = &h;
       t.a_row0 = off[e] + mt * RG;
       t.b_row0 = e * I;
