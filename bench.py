@@ -641,7 +641,7 @@ def run_profile_case(args):
     rc = layer.poll_device_status()
     trace = None
     if args.trace and T > 256:
-        # wait profile of the grouped GEMMs (routed gate/up: slots 0..7, routed down: 8..15):
+        # wait profile of the GEMMs (gate/up: slots 0..7, down: 8..15, router: 16..23):
         # per CTA, SM kcycles spent waiting, median / max over CTAs, one repetition
         layer.enable_phase_trace(True)
         flush_buf.fill_(1)
@@ -651,7 +651,7 @@ def run_profile_case(args):
         fields = ["producer_wait_free_stage", "mma_wait_loaded_stage", "mma_wait_free_accumulator",
                   "epilogue_wait_accumulator", "epilogue_busy"]
         trace = {}
-        for base, kern in ((0, "gateup"), (8, "down")):
+        for base, kern in ((16, "router"), (0, "gateup"), (8, "down")):
             rr = [r for r in rows if r[base + 7]]
             d = {}
             for k, nm in enumerate(fields):
@@ -660,7 +660,13 @@ def run_profile_case(args):
             span = sorted((r[base + 6] - r[base + 5]) / 1e3 for r in rr)
             d["cta_span_us"] = [round(span[len(span) // 2], 1), round(span[-1], 1)]
             d["tiles"] = [int(statistics.median(r[base + 7] for r in rr)), int(max(r[base + 7] for r in rr))]
+            d["first_start_last_end_ns"] = [min(r[base + 5] for r in rr), max(r[base + 6] for r in rr)]
             trace[kern] = d
+        # timeline (us from the router's first CTA start): each GEMM's first CTA start and last CTA end
+        t0 = trace["router"]["first_start_last_end_ns"][0]
+        for d in trace.values():
+            a, b = d.pop("first_start_last_end_ns")
+            d["span_from_router_start_us"] = [round((a - t0) / 1e3, 1), round((b - t0) / 1e3, 1)]
     elif args.trace:
         # phase stamps of the decode kernel: per slot, min / median / max over CTAs, in us from
         # the earliest CTA start; several repetitions, the median of each statistic reported

@@ -134,10 +134,12 @@ flint_moe_status flint_moe_poll_device_status(flint_moe_t h, flint_stream_t stre
 /* Profiling.  enable = 1: later forward calls record a CUDA event pair around every kernel
  * they launch (this serialises kernels that would otherwise overlap); flint_moe_kernel_times
  * synchronises on the last call's events and writes up to `cap` entries: names[i] (static
- * strings) and ms[i]; *n receives the count.  enable = 2: the decode-size kernel stamps the
- * GPU global timer (ns) at its phase boundaries, 16 slots per CTA, into the workspace;
- * flint_moe_read_trace synchronises the device and copies up to `cap` stamps (CTA-major) to
- * host memory `out`.  enable = 0 turns both off. */
+ * strings) and ms[i]; *n receives the count.  enable = 2: 24 slots per CTA in the workspace
+ * record a trace -- at T <= 256 the decode-size kernel's GPU global timer stamps (ns) at its
+ * phase boundaries; at T > 256 the wait profiles of the routed gate/up (slots 0-7), down (8-15)
+ * and router (16-23) GEMMs: SM cycles the producer, the MMA issuer and the epilogue waited, the
+ * global timer at start and end, tiles processed.  flint_moe_read_trace synchronises the device
+ * and copies up to `cap` values (CTA-major) to host memory `out`.  enable = 0 turns both off. */
 flint_moe_status flint_moe_enable_kernel_timing(flint_moe_t h, int enable);
 flint_moe_status flint_moe_kernel_times(flint_moe_t h, const char** names, float* ms, int cap,
                                         int* n);

@@ -16,6 +16,7 @@ HIDDEN, N_EXPERTS, TOP_K, EXPERT_INTER, SHARED_INTER = 2048, 256, 6, 512, 1024
 FLAG_PRE_RMSNORM = 0x1
 FLAG_RESIDUAL = 0x2
 FLAG_TEST_WAIT_TIMEOUT = 0x80000000  # tests of the device-timeout path only
+TRACE_SLOTS = 24  # trace values per CTA (flint_moe_read_trace)
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "cuda error",
           5: "device timeout", 6: "device bounds"}
@@ -199,8 +200,8 @@ class FlintMoE:
     def enable_phase_trace(self, on=True):
         _check(self._L.flint_moe_enable_kernel_timing(self._h, 2 if on else 0), "flint_moe_enable_kernel_timing")
 
-    def read_trace(self, slots=16):
-        """Phase stamps (ns) of the last decode-size call: list of per-CTA lists."""
+    def read_trace(self, slots=TRACE_SLOTS):
+        """The last call's trace (see flint_moe_enable_kernel_timing): list of per-CTA lists."""
         cap = 1024 * slots
         buf = (ctypes.c_ulonglong * cap)()
         n = ctypes.c_int(0)

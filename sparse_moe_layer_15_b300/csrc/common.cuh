@@ -85,7 +85,7 @@ struct Params {
   unsigned long long* trace;  // [gridDim.x][TRACE_SLOTS] %globaltimer stamps, or null
 };
 
-constexpr int TRACE_SLOTS = 16;
+constexpr int TRACE_SLOTS = 24;
 
 // Phase trace: thread 0 of each CTA stamps slot `s` with the global timer (ns).
 __device__ __forceinline__ void trace_point(const Params& p, int s) {

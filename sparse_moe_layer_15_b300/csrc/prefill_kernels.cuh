@@ -74,7 +74,7 @@ struct RouterTC {
   __device__ int num_tiles(const uint8_t*) const { return (p.T + TM - 1) / TM; }
   __device__ int kblocks() const { return H / tc::TK; }
   __device__ uint32_t* status() const { return p.status; }
-  __device__ unsigned long long* trace() const { return nullptr; }
+  __device__ unsigned long long* trace() const { return p.trace ? p.trace + 16 : nullptr; }  // slots 16..23
   __device__ void tile(int i, TileInfo& t, const uint8_t*) const {
     t.amap = &xin;
     t.a_row0 = i * TM;
