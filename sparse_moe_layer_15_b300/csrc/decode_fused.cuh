@@ -41,7 +41,7 @@ constexpr int NCONS = 256;               // consumer threads (8 warps)
 constexpr int NWARPS = NCONS / 32;
 constexpr int NTHREADS = NCONS + 32;     // + one producer warp
 constexpr int STREAM_MAX_T = 256;
-constexpr int NT_MAX = 8;                // token rows per group (the MMA's N)
+constexpr int NT_MAX = 16;               // most token rows per group (two 8-token MMA N tiles)
 constexpr int NSTAGE = 4;                // measured: 4 stages beat 5 (and 3) over the decode sweep
 constexpr int BLK_BYTES = 32768;
 constexpr int GU_ROWS = 128;             // gate/up block: 128 rows x 64 columns of gate and of up
@@ -70,28 +70,47 @@ struct StreamMaps {
   CUtensorMap wsd;  // [IS][H], box 64 x 256
 };
 
-// Largest number of token groups (of NT_MAX expert-sorted rows) a call of T tokens can have.
+// Token rows per group for a call of T tokens: 16 when T > 64 (the weights of the shared
+// expert, the router and any expert with more than 8 rows are then streamed once per 16 rows
+// instead of 8), else 8 (measured faster for the small calls: fewer zero rows staged and
+// computed).
+__host__ __device__ constexpr int group_rows(int T) { return T > 64 ? NT_MAX : NT_MAX / 2; }
+
+// Largest number of token groups (of group_rows(T) expert-sorted rows) a call of T tokens can have.
 __host__ __device__ constexpr int max_groups(int T) {
   const int pairs = T * K;
   const int u = pairs < E ? pairs : E;
-  const int g = (pairs + NT_MAX - 1) / NT_MAX + u;
+  const int G = group_rows(T);
+  const int g = (pairs + G - 1) / G + u;
   return g < pairs ? g : pairs;
 }
 
+// Largest numbers of routed and of shared token groups over the calls of 1..Ts tokens (the group
+// width changes at 64 tokens, so the largest call is not always the one with the most groups).
+__host__ __device__ constexpr int max_groups_upto(int Ts) {
+  const int a = max_groups(Ts < 64 ? Ts : 64), b = max_groups(Ts);
+  return a > b ? a : b;
+}
+__host__ __device__ constexpr int max_shared_groups_upto(int Ts) {
+  const int s = Ts < 64 ? Ts : 64;
+  const int a = (s + group_rows(s) - 1) / group_rows(s), b = (Ts + group_rows(Ts) - 1) / group_rows(Ts);
+  return a > b ? a : b;
+}
+
 // ---------------------------------------------------------------- shared memory
+// The staged input rows come last, so that a call launches with only the rows its group width
+// needs (fused_smem_bytes): a smaller footprint leaves more of the SM's memory to L1.
 struct Smem {
   static constexpr int stages = 0;                                 // NSTAGE x 32 KB
-  static constexpr int xs = stages + NSTAGE * BLK_BYTES;           // [NT_MAX][H + XPAD] bf16
-  static constexpr int xs_bytes = NT_MAX * (H + XPAD) * 2;
-  static constexpr int out = xs + xs_bytes;                        // [2][NT_MAX][128] f32
-  static constexpr int full = out + 2 * NT_MAX * 128 * 4;          // NSTAGE mbarriers
+  static constexpr int out = stages + NSTAGE * BLK_BYTES;  // f32: [NT_MAX][128] (gate/up) or [2][NT_MAX][64] (down)
+  static constexpr int full = out + NT_MAX * 128 * 4;              // NSTAGE mbarriers
   static constexpr int empty = full + 8 * NSTAGE;                  // NSTAGE mbarriers
   static constexpr int misc = empty + 8 * NSTAGE;                  // flags
   static constexpr int meta = misc + 128;                          // [4][E+1] int
   static constexpr int perm = meta + 4 * (E + 1) * 4;              // [MAX_PAIRS] int
   static constexpr int inv = perm + MAX_PAIRS * 4;                 // [MAX_PAIRS] int
   static constexpr int gw = inv + MAX_PAIRS * 4;                   // [MAX_PAIRS] f32
-  static constexpr int bytes = gw + MAX_PAIRS * 4;
+  static constexpr int xs = gw + MAX_PAIRS * 4;                    // [G][H + XPAD] bf16, G <= NT_MAX
   // reuse of `xs` during routing (between the streaming steps)
   static constexpr int scores = xs;                    // [4][E] f32
   static constexpr int s_cnt = xs + 4 * E * 4;         // [E] int
@@ -100,8 +119,11 @@ struct Smem {
   static constexpr int s_wsum = s_wcnt + NWARPS * E * 4;  // [4][8] int
   static constexpr int s_idx = s_wsum + 128;           // [MAX_PAIRS] int
 };
-static_assert(Smem::s_idx + MAX_PAIRS * 4 <= Smem::xs + Smem::xs_bytes, "routing scratch must fit in xs");
-constexpr int FUSED_SMEM = Smem::bytes + 1024;
+__host__ __device__ constexpr int xs_bytes(int G) { return G * (H + XPAD) * 2; }
+// Dynamic shared memory of a launch whose token groups have G rows (+ 1 KB for alignment).
+__host__ __device__ constexpr int fused_smem_bytes(int G) { return Smem::xs + xs_bytes(G) + 1024; }
+static_assert(Smem::s_idx + MAX_PAIRS * 4 <= Smem::xs + xs_bytes(NT_MAX / 2), "routing scratch must fit in xs");
+constexpr int FUSED_SMEM = fused_smem_bytes(NT_MAX);  // the largest launch
 static_assert(FUSED_SMEM <= 227 * 1024, "shared memory budget");
 
 __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
@@ -146,28 +168,43 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// d += A * B over `ksteps` (even) k-steps of 16 rows starting at tile row `r0`, where A = the
-// 16 columns [m0, m0+16) of a swizzled weight tile (rows = k) and B = the staged input rows
-// xs[n][k0 + ...] (8 tokens, row stride xstride bf16).  Two k-steps per B load.
-__device__ __forceinline__ void mma_tile(float (&d)[4], uint32_t tile, int m0, int r0, int ksteps, uint32_t xs,
-                                         int xstride, int k0) {
+// d[h] += A * B_h over `ksteps` (even) k-steps of 16 rows starting at tile row `r0`, where A =
+// the 16 columns [m0, m0+16) of a swizzled weight tile (rows = k) and B_h = the staged input
+// rows xs[8h + n][k0 + ...] (8 tokens each, row stride xstride bf16); B_1 (tokens 8..15) only
+// when TWO.  Two k-steps per B load.
+template <bool TWO>
+__device__ __forceinline__ void mma_tile_t(float (&d)[2][4], uint32_t tile, int m0, int r0, int ksteps, uint32_t xs,
+                                           int xstride, int k0) {
   const int lane = threadIdx.x & 31;
   const int q = lane >> 3, i = lane & 7;
   // A: matrix q -> (m + 8 * (q & 1), k + 8 * (q >> 1)), lane row i
   const int am = m0 + ((q & 1) << 3);
   const int ak = (q >> 1) << 3;
-  // B: matrix q -> k offset 8q, lane row = token i
+  // B: matrix q -> k offset 8q, lane row = token i (+ 8 for B_1)
   const uint32_t bbase = xs + uint32_t((i * xstride + k0 + q * 8) * 2);
+  const uint32_t bhi = uint32_t(8 * xstride * 2);
 #pragma unroll 2
   for (int s = 0; s < ksteps; s += 2) {
-    uint32_t b[4];
+    uint32_t b[4], b2[4];
     ldsm_x4(bbase + uint32_t(s * 16 * 2), b);
+    if constexpr (TWO) ldsm_x4(bbase + bhi + uint32_t(s * 16 * 2), b2);
     uint32_t a[4];
     ldsm_x4_trans(tile + swz(r0 + s * 16 + ak + i, am), a);
-    mma_bf16(d, a, b[0], b[1]);
+    mma_bf16(d[0], a, b[0], b[1]);
+    if constexpr (TWO) mma_bf16(d[1], a, b2[0], b2[1]);
     ldsm_x4_trans(tile + swz(r0 + (s + 1) * 16 + ak + i, am), a);
-    mma_bf16(d, a, b[2], b[3]);
+    mma_bf16(d[0], a, b[2], b[3]);
+    if constexpr (TWO) mma_bf16(d[1], a, b2[2], b2[3]);
   }
+}
+
+// `two` is warp-uniform: a group of at most 8 rows runs the one-tile loop.
+__device__ __forceinline__ void mma_tile(float (&d)[2][4], uint32_t tile, int m0, int r0, int ksteps, uint32_t xs,
+                                         int xstride, int k0, bool two) {
+  if (two)
+    mma_tile_t<true>(d, tile, m0, r0, ksteps, xs, xstride, k0);
+  else
+    mma_tile_t<false>(d, tile, m0, r0, ksteps, xs, xstride, k0);
 }
 
 // ---------------------------------------------------------------- tickets and barriers
@@ -303,17 +340,19 @@ __device__ __forceinline__ Item decode_item(int T, const Meta& m, int kind, int 
     it.c = idx % nch;
     const int u = find_group_owner(m.tgp, m.U, gi);
     const int tg = gi - m.tgp[u];
+    const int G = group_rows(T);
     it.e = m.e[u];
-    it.row0 = m.off[u] + tg * NT_MAX;
-    it.nt = min(NT_MAX, m.cnt[u] - tg * NT_MAX);
+    it.row0 = m.off[u] + tg * G;
+    it.nt = min(G, m.cnt[u] - tg * G);
     it.KB = kind == KIND_GU ? GU_KB : DN_KB;
   } else {
     const int nch = kind == KIND_RT ? RT_NB : kind == KIND_SGU ? SGU_NCH : OUT_NCH;
     const int tg = idx / nch;
     it.c = idx % nch;
+    const int G = group_rows(T);
     it.e = -1;
-    it.row0 = tg * NT_MAX;
-    it.nt = min(NT_MAX, T - tg * NT_MAX);
+    it.row0 = tg * G;
+    it.nt = min(G, T - tg * G);
     it.KB = kind == KIND_RT ? 1 : kind == KIND_SGU ? GU_KB : SD_KB;
   }
   return it;
@@ -494,8 +533,8 @@ __device__ void combine_share(const Params& p, const int* inv) {
   }
 }
 
-// Stage the token group's input rows (bf16, row stride xlen + XPAD) for an item (consumers),
-// unless they are the rows staged last (same source and group).
+// Stage the token group's input rows (bf16, row stride xlen + XPAD; rows nt .. G-1 zero) for an
+// item (consumers), unless they are the rows staged last (same source and group).
 __device__ void stage_inputs(Stream& S, const Item& it, int xlen) {
   const int cls = it.kind == KIND_GU ? 1 : it.kind == KIND_SD ? 2 : it.kind == KIND_DN ? 3 : 0;
   if (cls == S.x_cls && it.row0 == S.x_row0) return;
@@ -504,7 +543,8 @@ __device__ void stage_inputs(Stream& S, const Item& it, int xlen) {
   const Params& p = *S.p;
   bf16* xs = reinterpret_cast<bf16*>(S.sm + Smem::xs);
   const int cpr = xlen / 8;
-  for (int q = threadIdx.x; q < NT_MAX * cpr; q += NCONS) {
+  const int G = group_rows(p.T);
+  for (int q = threadIdx.x; q < G * cpr; q += NCONS) {
     const int t = q / cpr, k8 = q % cpr;
     uint4 v = make_uint4(0, 0, 0, 0);
     if (t < it.nt) {
@@ -533,22 +573,26 @@ __device__ void run_router_block(Stream& S, const Item& it, int& j) {
   wait_full(S, j);
   const uint32_t tile = smem_u32(stage_ptr(S, j)) + uint32_t((warp >> 1) * (BLK_BYTES / 4));
   const uint32_t xs = smem_u32(S.sm + Smem::xs);
-  float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+  float d0[2][4] = {}, d1[2][4] = {};
   const int mbase = (warp & 1) * 32;  // column within the 64-expert sub-tile
-  mma_tile(d0, tile, mbase, 0, RT_ROWS / 16, xs, H + XPAD, it.c * RT_ROWS);
-  mma_tile(d1, tile, mbase + 16, 0, RT_ROWS / 16, xs, H + XPAD, it.c * RT_ROWS);
+  const bool two = it.nt > 8;
+  mma_tile(d0, tile, mbase, 0, RT_ROWS / 16, xs, H + XPAD, it.c * RT_ROWS, two);
+  mma_tile(d1, tile, mbase + 16, 0, RT_ROWS / 16, xs, H + XPAD, it.c * RT_ROWS, two);
   release(S, j);
-  // C fragment: (expert m0 + g [+8], token 2*tig [+1])
+  // C fragment: (expert m0 + g [+8], token 8 * half + 2*tig [+1])
   const int g = lane >> 2, tig = lane & 3;
   const int e0 = warp * 32;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const float* d = h ? d1 : d0;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int e = e0 + h * 16 + g + ((r >> 1) << 3);
-      const int t = 2 * tig + (r & 1);
-      if (t < it.nt) p.RP[((size_t)it.c * STREAM_MAX_T + it.row0 + t) * E + e] = d[r];
+    for (int h2 = 0; h2 < 2; ++h2) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int e = e0 + h * 16 + g + ((r >> 1) << 3);
+        const int t = 8 * h2 + 2 * tig + (r & 1);
+        const float v = h ? d1[h2][r] : d0[h2][r];
+        if (t < it.nt) p.RP[((size_t)it.c * STREAM_MAX_T + it.row0 + t) * E + e] = v;
+      }
     }
   }
   csync();  // xs is restaged by the next item
@@ -564,7 +608,8 @@ __device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, i
   stage_inputs(S, it, xlen);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t xs = smem_u32(S.sm + Smem::xs);
-  float d[4] = {0.f, 0.f, 0.f, 0.f};
+  float d[2][4] = {};
+  const bool two = it.nt > 8;
   // gate/up: warp w owns columns 16*(w&3) of the gate (w < 4) or up (w >= 4) tile, all 128
   // rows; down: warp w owns columns 16*(w&3), rows [128*(w>>2), +128) of the 256-row tile.
   const int m0 = (warp & 3) * 16;
@@ -573,7 +618,7 @@ __device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, i
   const int rows = gu ? GU_ROWS : DN_ROWS;
   for (int q = 0; q < nblk; ++q, ++j) {
     wait_full(S, j);
-    mma_tile(d, smem_u32(stage_ptr(S, j)) + sub, m0, r0, 8, xs, xlen + XPAD, (kb_start + q) * rows + r0);
+    mma_tile(d, smem_u32(stage_ptr(S, j)) + sub, m0, r0, 8, xs, xlen + XPAD, (kb_start + q) * rows + r0, two);
     release(S, j);
   }
   // fragments -> out[half][t][col]: gate/up: col = (w>=4)*64 + 16*(w&3) + m (half 0);
@@ -585,15 +630,19 @@ __device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, i
     const int half = gu ? 0 : (warp >> 2);
     const int cb = gu ? (warp >> 2) * 64 + m0 : m0;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int col = cb + g + ((r >> 1) << 3);
-      const int t = 2 * tig + (r & 1);
-      out[(half * NT_MAX + t) * ncol + col] = d[r];
+    for (int h2 = 0; h2 < 2; ++h2) {
+      if (h2 == 1 && !two) break;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int col = cb + g + ((r >> 1) << 3);
+        const int t = 8 * h2 + 2 * tig + (r & 1);
+        out[(half * NT_MAX + t) * ncol + col] = d[h2][r];
+      }
     }
   }
   csync();
   if (!gu) {  // down: add the two row halves (fixed order)
-    for (int q = threadIdx.x; q < NT_MAX * 64; q += NCONS) out[q] = out[q] + out[NT_MAX * 64 + q];
+    for (int q = threadIdx.x; q < it.nt * 64; q += NCONS) out[q] = out[q] + out[NT_MAX * 64 + q];
     csync();
   }
   if (kb_start == 0 && nblk == it.KB) {
@@ -778,7 +827,7 @@ __device__ Meta build_tables(const Params& p, uint8_t* sm, int* perm, int* inv) 
   if (act) {
     c = s_cnt[tid];
     f = c > 0 ? 1 : 0;
-    ng = (c + NT_MAX - 1) / NT_MAX;
+    ng = (c + group_rows(p.T) - 1) / group_rows(p.T);
     ic = c;
     jf = f;
     kg = ng;
@@ -896,7 +945,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   S.inv = inv;
   S.gw = gw;
   const int T = p.T;
-  const int ntg = (T + NT_MAX - 1) / NT_MAX;
+  const int ntg = (T + group_rows(T) - 1) / group_rows(T);
   const bool full = mode == 0;
 
   if (threadIdx.x == 0) {

@@ -44,8 +44,8 @@ Layout make_layout(int max_tokens) {
   };
   const size_t T = (size_t)max_tokens;
   const int Ts = max_tokens < STREAM_MAX_T ? max_tokens : STREAM_MAX_T;
-  const size_t G = (size_t)max_groups(Ts);               // routed token groups
-  const size_t Gs = (size_t)(Ts + NT_MAX - 1) / NT_MAX;  // shared token groups
+  const size_t G = (size_t)max_groups_upto(Ts);          // routed token groups
+  const size_t Gs = (size_t)max_shared_groups_upto(Ts);  // shared token groups
   L.status = take(256);
   L.bar_count = take(sizeof(uint32_t));
   L.bar_done = take(sizeof(uint32_t));
@@ -257,7 +257,8 @@ flint_moe_status run_decode(flint_moe_t h, const Params& p, cudaStream_t st, boo
   cudaError_t e = cudaSuccess;
   if (h->cfg.flags & FLINT_MOE_FLAG_PRE_RMSNORM) e = launch(h, "rmsnorm", rmsnorm_kernel, p.T, 256, 0, st, false, p);
   if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
-  e = launch(h, full ? "decode_fused" : "decode_fused_route", decode_fused, h->n_sm, NTHREADS, FUSED_SMEM, st, true, p,
+  e = launch(h, full ? "decode_fused" : "decode_fused_route", decode_fused, h->n_sm, NTHREADS,
+             fused_smem_bytes(group_rows(p.T)), st, true, p,
              h->smaps, full ? 0 : 1);
   return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ERR_CUDA;
 }
@@ -535,7 +536,7 @@ flint_moe_status flint_moe_destroy(flint_moe_t h) {
 // point takes its scratch space from one fixed array in device memory that the library
 // declares itself, so the caller supplies only the weights, the input and the output.
 //
-// The array (26 MiB) holds the workspace of a handle with max_tokens = NOALLOC_MAX_T.
+// The array (42 MiB) holds the workspace of a handle with max_tokens = NOALLOC_MAX_T.
 // Every GPU that loads the library reserves it until the process exits.  All calls on a
 // device share it: calls whose work overlaps on the GPU (on different streams, or from
 // different threads) race on it and must be serialised by the caller.  The counters that must
@@ -543,7 +544,7 @@ flint_moe_status flint_moe_destroy(flint_moe_t h) {
 namespace {
 
 constexpr int NOALLOC_MAX_T = 4;
-constexpr size_t NOALLOC_BYTES = size_t(26) << 20;
+constexpr size_t NOALLOC_BYTES = size_t(42) << 20;
 constexpr int NOALLOC_MAX_DEVICES = 64;
 
 __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_BYTES];
