@@ -26,8 +26,8 @@
 // or 256 rows of one or two matrices, or 64 router rows x 256 experts); every CTA takes an
 // equal contiguous range.  A producer warp streams the range through a 4-stage TMA ring
 // (128-byte swizzled tiles); eight consumer warps multiply each tile against the current
-// token group (up to 8 rows) with warp-level bf16 MMAs (m16n8k16, fp32 accumulate), each warp
-// owning 16 output columns, so a tile needs no cross-warp reduction.  Tiles of the same
+// token group (8 rows, or 16 above 64 tokens) with warp-level bf16 MMAs (m16n8k16, fp32
+// accumulate), each warp owning 16 output columns, so a tile needs no cross-warp reduction.  Tiles of the same
 // output columns accumulate in registers; a range boundary inside an item leaves a partial
 // sum that the last CTA to finish the item adds in block order (an integer ticket that
 // records which partial slots exist): deterministic, no floating-point atomics.
