@@ -39,13 +39,31 @@ KERNEL_SOURCES = ("sparse_moe_layer_15_b300/csrc/decode_fused.cuh", "sparse_moe_
                   "sparse_moe_layer_15_b300/csrc/flint_moe.cu")
 
 
-def kernel_sources_sha256():
+# The sources the prefill path's tensor-core kernels are built from.
+PREFILL_SOURCES = ("sparse_moe_layer_15_b300/csrc/prefill_kernels.cuh", "sparse_moe_layer_15_b300/csrc/tc_gemm.cuh",
+                   "sparse_moe_layer_15_b300/csrc/common.cuh", "sparse_moe_layer_15_b300/csrc/flint_moe.cu")
+
+
+def kernel_sources_sha256(sources=KERNEL_SOURCES):
     import hashlib
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
+
+
+def measured_prefill_traffic(kernel, workload):
+    """DRAM bytes per launch of the prefill kernel `kernel` on `workload`, from the committed ncu
+    summary profiles/<kernel>_traffic.json, or None when the prefill sources have changed since."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("sources_sha256") != kernel_sources_sha256(PREFILL_SOURCES):
+        return None
+    return rec.get("dram_bytes_per_launch", {}).get(workload)
 
 
 def measured_traffic(kernel, sweep):
@@ -416,7 +434,8 @@ def run_workload(args, rank, world, local):
     if dom in PF_KERNEL_FLOPS_PER_TOKEN:
         achieved = PF_KERNEL_FLOPS_PER_TOKEN[dom] * T / (dom_ms * 1e-3) / 1e12
         roofline = dict(bound="tensor", kernel=dom, achieved=round(achieved, 1), peak=peaks["bf16_tflops"],
-                        unit="TFLOP/s", frac=round(achieved / peaks["bf16_tflops"], 4), traffic=None,
+                        unit="TFLOP/s", frac=round(achieved / peaks["bf16_tflops"], 4),
+                        traffic=measured_prefill_traffic(dom, args.workload),
                         frac_vs_spec=round(achieved / SPEC_BF16_TFLOPS, 4),
                         alg_flop_per_launch=PF_KERNEL_FLOPS_PER_TOKEN[dom] * T,
                         peak_source=peaks["source"] + " (bf16_tflops, burst)",
