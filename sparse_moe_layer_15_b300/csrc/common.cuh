@@ -45,10 +45,6 @@ struct Params {
   const bf16* ws_down;   // [IS][H]
   // workspace
   uint32_t* status;      // [1] device status word (ST_* bits)
-  int32_t* n_touched;    // [1] experts with at least one token
-  int32_t* n_groups;     // [1] token groups (of up to 8 expert-sorted rows) over all experts
-  int32_t* touched;      // [E] touched experts, ascending
-  int32_t* tgp;          // [E+1] token-group prefix over the touched experts
   int32_t* counts;       // [E]
   int32_t* offsets;      // [E+1]
   int32_t* perm;         // [T*K] sorted row -> pair (t*K + j)
@@ -71,12 +67,10 @@ struct Params {
   int32_t* mtp;          // [E+1] prefix over experts of their 256-row groups (prefill path)
   uint32_t* bar_count;   // [1] grid-barrier counter (decode path; reset at kernel end)
   uint32_t* bar_done;    // [1]
-  uint32_t* tk_router;   // [1] tickets (zero between kernels: the last arriver resets)
-  uint32_t* tk_gu;
+  uint32_t* tk_gu;       // item tickets (zero between kernels: the last arriver resets)
   uint32_t* tk_sgu;
   uint32_t* tk_sd;
   uint32_t* tk_dn;
-  uint32_t* tk_comb;     // [H/64]
   // user-visible copies (may be null)
   int32_t* out_idx;
   float* out_w;

@@ -25,8 +25,9 @@ constexpr int MAX_TRACE_CTAS = 1024;
 
 struct Layout {
   // tickets first: [status, tickets) and [tickets, scalars) are cleared together after errors
-  size_t status, bar_count, bar_done, tk_router, tk_gu, tk_sgu, tk_sd, tk_dn, tk_comb;
-  size_t n_touched, n_groups, touched, tgp, counts, offsets, perm, inv, topk_idx, topk_w;
+  size_t status, bar_count, bar_done, tk_gu, tk_sgu, tk_sd, tk_dn;
+  size_t zero_end;  // [0, zero_end): status word, barrier counters and tickets (cleared between uses)
+  size_t counts, offsets, perm, inv, topk_idx, topk_w;
   size_t xn, xstage, ystage, h, hs, S, Y, P_gu, P_sgu, P_sd, P_dn, RP, trace;
   size_t xs, Yb, hist, mtp;  // prefill path (max_tokens > STREAM_MAX_T), else 0
   size_t total;
@@ -49,16 +50,11 @@ Layout make_layout(int max_tokens) {
   L.status = take(256);
   L.bar_count = take(sizeof(uint32_t));
   L.bar_done = take(sizeof(uint32_t));
-  L.tk_router = take(sizeof(uint32_t));
   L.tk_gu = take(sizeof(uint32_t) * G * GU_NCH);
   L.tk_sgu = take(sizeof(uint32_t) * Gs * SGU_NCH);
   L.tk_sd = take(sizeof(uint32_t) * Gs * OUT_NCH);
   L.tk_dn = take(sizeof(uint32_t) * G * OUT_NCH);
-  L.tk_comb = take(sizeof(uint32_t) * OUT_NCH);
-  L.n_touched = take(sizeof(int32_t));
-  L.n_groups = take(sizeof(int32_t));
-  L.touched = take(sizeof(int32_t) * E);
-  L.tgp = take(sizeof(int32_t) * (E + 1));
+  L.zero_end = align_up(off, 256);
   L.counts = take(sizeof(int32_t) * E);
   L.offsets = take(sizeof(int32_t) * (E + 1));
   L.perm = take(sizeof(int32_t) * T * K);
@@ -178,16 +174,10 @@ Params make_params(flint_moe_t h, const void* x, int T, void* y, int32_t* out_id
   p.status = reinterpret_cast<uint32_t*>(ws + L.status);
   p.bar_count = reinterpret_cast<uint32_t*>(ws + L.bar_count);
   p.bar_done = reinterpret_cast<uint32_t*>(ws + L.bar_done);
-  p.tk_router = reinterpret_cast<uint32_t*>(ws + L.tk_router);
   p.tk_gu = reinterpret_cast<uint32_t*>(ws + L.tk_gu);
   p.tk_sgu = reinterpret_cast<uint32_t*>(ws + L.tk_sgu);
   p.tk_sd = reinterpret_cast<uint32_t*>(ws + L.tk_sd);
   p.tk_dn = reinterpret_cast<uint32_t*>(ws + L.tk_dn);
-  p.tk_comb = reinterpret_cast<uint32_t*>(ws + L.tk_comb);
-  p.n_touched = reinterpret_cast<int32_t*>(ws + L.n_touched);
-  p.n_groups = reinterpret_cast<int32_t*>(ws + L.n_groups);
-  p.tgp = reinterpret_cast<int32_t*>(ws + L.tgp);
-  p.touched = reinterpret_cast<int32_t*>(ws + L.touched);
   p.counts = reinterpret_cast<int32_t*>(ws + L.counts);
   p.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
   p.perm = reinterpret_cast<int32_t*>(ws + L.perm);
@@ -478,7 +468,7 @@ flint_moe_status flint_moe_poll_device_status(flint_moe_t h, flint_stream_t stre
     return FLINT_MOE_ERR_CUDA;
   if (word == 0) return FLINT_MOE_OK;
   // A device error may leave tickets mid-count: clear them with the status word.
-  if (cudaMemset(h->ws + h->L.status, 0, h->L.n_touched - h->L.status) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  if (cudaMemset(h->ws + h->L.status, 0, h->L.zero_end - h->L.status) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
   return (word & ST_TIMEOUT) ? FLINT_MOE_ERR_DEVICE_TIMEOUT : FLINT_MOE_ERR_DEVICE_BOUNDS;
 }
 
@@ -621,7 +611,7 @@ extern "C" flint_moe_status flint_moe_forward_noalloc(const flint_moe_weights* w
   if (!ok) return FLINT_MOE_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // status word, tickets and barrier counters start at zero on every call
-  if (cudaMemsetAsync(h.ws, 0, h.L.n_touched, st) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  if (cudaMemsetAsync(h.ws, 0, h.L.zero_end, st) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
   Params p = make_params(&h, x, T, y, topk_idx, topk_w, nullptr);
   return run_decode(&h, p, st, true);
 }
