@@ -56,10 +56,7 @@ struct Params {
   bf16* hs;              // [T][IS] shared SwiGLU activations
   float* Y;              // [T*K][H] gated routed expert outputs
   float* S;              // [T][H] shared expert output
-  float* P_gu;           // split-item partial sums of the streaming path, per kind
-  float* P_sgu;
-  float* P_sd;
-  float* P_dn;
+  float* P;              // [MAX_STREAM_CTAS][2][PSLOT] split-item partial sums (decode path)
   float* RP;             // [32][256][E] router partial logits (decode path)
   bf16* xs;              // [T*K][H] expert-sorted input rows (prefill path)
   bf16* Yb;              // [T*K][H] gated routed expert outputs, bf16 (prefill path)

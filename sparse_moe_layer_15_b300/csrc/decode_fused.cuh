@@ -22,15 +22,20 @@
 //   -- barrier --
 //   E  the combine y = S + sum_j Y[inv(t, j)] in slot order (+ x), spread over the grid.
 //
-// Within a step the weight traffic is a list of equal 32 KB blocks (64 output columns x 128
-// or 256 rows of one or two matrices, or 64 router rows x 256 experts); every CTA takes an
-// equal contiguous range.  A producer warp streams the range through a 4-stage TMA ring
-// (128-byte swizzled tiles); eight consumer warps multiply each tile against the current
-// token group (8 rows, or 16 above 64 tokens) with warp-level bf16 MMAs (m16n8k16, fp32
-// accumulate), each warp owning 16 output columns, so a tile needs no cross-warp reduction.  Tiles of the same
-// output columns accumulate in registers; a range boundary inside an item leaves a partial
-// sum that the last CTA to finish the item adds in block order (an integer ticket that
-// records which partial slots exist): deterministic, no floating-point atomics.
+// Within a step the weight traffic is a list of equal 32 KB blocks -- 64 rows x 128 output
+// columns of gate and of up, 128 rows x 128 output columns of a down matrix, or 64 router
+// rows x 256 experts -- and every CTA takes an equal contiguous range.  A producer warp
+// streams the range through a 4-stage TMA ring of 128-byte swizzled boxes; a block is read as
+// 8 or 16 KB boxes, two adjacent 64-column chunks of the same rows side by side (measured:
+// 5.3 TB/s against 4.8-4.9 for one 64-column chunk of twice the rows).  Eight consumer warps
+// multiply each block against the current token group (8 rows, or 16 above 64 tokens) with
+// warp-level bf16 MMAs (m16n8k16, fp32 accumulate), each warp owning its own output columns
+// over all rows of the block, so a block needs no cross-warp reduction.  Blocks of the same
+// output columns (one item) accumulate in registers.  A CTA's range splits at most two items,
+// one where it starts and one where it ends: each split piece goes to one of the CTA's two
+// partial slots, and the last CTA to finish the item (an integer ticket counting its blocks)
+// adds the pieces in block order, finding them from the range arithmetic alone:
+// deterministic, no floating-point atomics.
 #pragma once
 
 #include "common.cuh"
@@ -44,16 +49,18 @@ constexpr int STREAM_MAX_T = 256;
 constexpr int NT_MAX = 16;               // most token rows per group (two 8-token MMA N tiles)
 constexpr int NSTAGE = 4;                // measured: 4 stages beat 5 (and 3) over the decode sweep
 constexpr int BLK_BYTES = 32768;
-constexpr int GU_ROWS = 128;             // gate/up block: 128 rows x 64 columns of gate and of up
-constexpr int DN_ROWS = 256;             // down block: 256 rows x 64 columns
+constexpr int GU_ROWS = 64;              // gate/up block: 64 rows x 128 columns of gate and of up
+constexpr int DN_ROWS = 128;             // down block: 128 rows x 128 columns
 constexpr int RT_ROWS = 64;              // router block: 64 rows x 256 experts
-constexpr int GU_KB = H / GU_ROWS;       // 16 blocks per gate/up item
-constexpr int SD_KB = IS / DN_ROWS;      // 4 blocks per shared-down item
-constexpr int DN_KB = I / DN_ROWS;       // 2 blocks per routed-down item
+constexpr int GU_KB = H / GU_ROWS;       // 32 blocks per gate/up item
+constexpr int SD_KB = IS / DN_ROWS;      // 8 blocks per shared-down item
+constexpr int DN_KB = I / DN_ROWS;       // 4 blocks per routed-down item
 constexpr int RT_NB = H / RT_ROWS;       // 32 router blocks per token group
-constexpr int GU_NCH = I / 64;           // 8 column chunks of a routed expert's gate/up
-constexpr int SGU_NCH = IS / 64;         // 16 column chunks of the shared gate/up
-constexpr int OUT_NCH = H / 64;          // 32 column chunks of a down projection
+constexpr int GU_NCB = I / 128;          // 4 column blocks (128 wide) of a routed expert's gate/up
+constexpr int SGU_NCB = IS / 128;        // 8 column blocks of the shared gate/up
+constexpr int OUT_NCB = H / 128;         // 16 column blocks of a down projection
+constexpr int MAX_STREAM_CTAS = 256;     // largest grid of the decode kernel (the workspace holds its partial slots)
+constexpr int PSLOT = NT_MAX * 256;      // floats of one partial slot: [rows][256] gate|up, or [rows][128] down
 constexpr int REDUNDANT_ROUTING_MAX_T = 4;
 constexpr int MAX_PAIRS = STREAM_MAX_T * K;
 constexpr int XPAD = 8;                  // bf16 padding of a staged input row (bank spread)
@@ -62,12 +69,12 @@ enum Kind : int { KIND_RT = 0, KIND_GU = 1, KIND_SGU = 2, KIND_SD = 3, KIND_DN =
 
 struct StreamMaps {
   CUtensorMap wr;   // w_router [H][E], box 64 x 64, 128B swizzle
-  CUtensorMap wg;   // w_gate as [E*H][I], box 64 x 128, 128B swizzle
-  CUtensorMap wu;   // w_up   as [E*H][I], box 64 x 128
-  CUtensorMap wd;   // w_down as [E*I][H], box 64 x 256
-  CUtensorMap wsg;  // [H][IS], box 64 x 128
-  CUtensorMap wsu;  // [H][IS], box 64 x 128
-  CUtensorMap wsd;  // [IS][H], box 64 x 256
+  CUtensorMap wg;   // w_gate as [E*H][I], box 64 x 64 (columns x rows), 128B swizzle
+  CUtensorMap wu;   // w_up   as [E*H][I], box 64 x 64
+  CUtensorMap wd;   // w_down as [E*I][H], box 64 x 128
+  CUtensorMap wsg;  // [H][IS], box 64 x 64
+  CUtensorMap wsu;  // [H][IS], box 64 x 64
+  CUtensorMap wsd;  // [IS][H], box 64 x 128
 };
 
 // Token rows per group for a call of T tokens: 16 when T > 64 (the weights of the shared
@@ -98,19 +105,21 @@ __host__ __device__ constexpr int max_shared_groups_upto(int Ts) {
 }
 
 // ---------------------------------------------------------------- shared memory
-// The staged input rows come last, so that a call launches with only the rows its group width
-// needs (fused_smem_bytes): a smaller footprint leaves more of the SM's memory to L1.
+// The staged input rows and the output tile come last, so that a call launches with only the
+// rows its group width needs (fused_smem_bytes): a smaller footprint leaves more of the SM's
+// memory to L1.
 struct Smem {
   static constexpr int stages = 0;                                 // NSTAGE x 32 KB
-  static constexpr int out = stages + NSTAGE * BLK_BYTES;  // f32: [NT_MAX][128] (gate/up) or [2][NT_MAX][64] (down)
-  static constexpr int full = out + NT_MAX * 128 * 4;              // NSTAGE mbarriers
+  static constexpr int full = stages + NSTAGE * BLK_BYTES;         // NSTAGE mbarriers
   static constexpr int empty = full + 8 * NSTAGE;                  // NSTAGE mbarriers
   static constexpr int misc = empty + 8 * NSTAGE;                  // flags
-  static constexpr int meta = misc + 128;                          // [4][E+1] int
-  static constexpr int perm = meta + 4 * (E + 1) * 4;              // [MAX_PAIRS] int
-  static constexpr int inv = perm + MAX_PAIRS * 4;                 // [MAX_PAIRS] int
-  static constexpr int gw = inv + MAX_PAIRS * 4;                   // [MAX_PAIRS] f32
+  static constexpr int plist = misc + 128;                         // [64] int: partial slots of an item
+  static constexpr int meta = plist + 256;                         // [4][E+1] int
+  static constexpr int perm = meta + 4 * (E + 1) * 4;              // [MAX_PAIRS] uint16
+  static constexpr int inv = perm + MAX_PAIRS * 2;                 // [MAX_PAIRS] uint16
+  static constexpr int gw = inv + MAX_PAIRS * 2;                   // [MAX_PAIRS] f32
   static constexpr int xs = gw + MAX_PAIRS * 4;                    // [G][H + XPAD] bf16, G <= NT_MAX
+  // then the output tile at out_offset(G), f32: [G][256] (gate/up) or [G][128] (down)
   // reuse of `xs` during routing (between the streaming steps)
   static constexpr int scores = xs;                    // [4][E] f32
   static constexpr int s_cnt = xs + 4 * E * 4;         // [E] int
@@ -120,11 +129,18 @@ struct Smem {
   static constexpr int s_idx = s_wsum + 128;           // [MAX_PAIRS] int
 };
 __host__ __device__ constexpr int xs_bytes(int G) { return G * (H + XPAD) * 2; }
+__host__ __device__ constexpr int out_offset(int G) { return Smem::xs + xs_bytes(G); }
 // Dynamic shared memory of a launch whose token groups have G rows (+ 1 KB for alignment).
-__host__ __device__ constexpr int fused_smem_bytes(int G) { return Smem::xs + xs_bytes(G) + 1024; }
+__host__ __device__ constexpr int fused_smem_bytes(int G) { return out_offset(G) + G * 256 * 4 + 1024; }
 static_assert(Smem::s_idx + MAX_PAIRS * 4 <= Smem::xs + xs_bytes(NT_MAX / 2), "routing scratch must fit in xs");
+static_assert(Smem::perm % 16 == 0 && Smem::gw % 16 == 0 && Smem::xs % 16 == 0, "16-byte aligned tables");
 constexpr int FUSED_SMEM = fused_smem_bytes(NT_MAX);  // the largest launch
 static_assert(FUSED_SMEM <= 227 * 1024, "shared memory budget");
+static_assert(GU_KB <= 64 && SD_KB <= 64 && DN_KB <= 64, "an item's pieces fit the slot list");
+// Most blocks of one step (step C: routed and shared gate/up; step D has half as many per group).
+constexpr long long MAX_STEP_BLOCKS = (long long)max_groups_upto(STREAM_MAX_T) * GU_NCB * GU_KB +
+                                      (long long)max_shared_groups_upto(STREAM_MAX_T) * SGU_NCB * GU_KB;
+static_assert(MAX_STEP_BLOCKS * (MAX_STREAM_CTAS + 1) < (1ll << 32), "32-bit range arithmetic");
 
 __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
   uint32_t a = smem_u32(raw);
@@ -207,23 +223,61 @@ __device__ __forceinline__ void mma_tile(float (&d)[2][4], uint32_t tile, int m0
     mma_tile_t<false>(d, tile, m0, r0, ksteps, xs, xstride, k0);
 }
 
+// d[m][h] += A_m * B_h for the two 16-column tiles A_0 = columns [m0, m0+16) and A_1 =
+// [m0+16, m0+32) of a swizzled weight tile (rows 0 .. 16*ksteps-1 = k), B_h as in mma_tile_t;
+// one B load feeds both tiles.
+template <bool TWO>
+__device__ __forceinline__ void mma_pair_t(float (&d)[2][2][4], uint32_t tile, int m0, int ksteps, uint32_t xs,
+                                           int xstride, int k0) {
+  const int lane = threadIdx.x & 31;
+  const int q = lane >> 3, i = lane & 7;
+  const int am = m0 + ((q & 1) << 3);
+  const int ak = (q >> 1) << 3;
+  const uint32_t bbase = xs + uint32_t((i * xstride + k0 + q * 8) * 2);
+  const uint32_t bhi = uint32_t(8 * xstride * 2);
+#pragma unroll
+  for (int s = 0; s < ksteps; s += 2) {
+    uint32_t b[4], b2[4];
+    ldsm_x4(bbase + uint32_t(s * 16 * 2), b);
+    if constexpr (TWO) ldsm_x4(bbase + bhi + uint32_t(s * 16 * 2), b2);
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      uint32_t a[4];
+      ldsm_x4_trans(tile + swz(s * 16 + ak + i, am + 16 * m), a);
+      mma_bf16(d[m][0], a, b[0], b[1]);
+      if constexpr (TWO) mma_bf16(d[m][1], a, b2[0], b2[1]);
+      ldsm_x4_trans(tile + swz((s + 1) * 16 + ak + i, am + 16 * m), a);
+      mma_bf16(d[m][0], a, b[2], b[3]);
+      if constexpr (TWO) mma_bf16(d[m][1], a, b2[2], b2[3]);
+    }
+  }
+}
+
+__device__ __forceinline__ void mma_pair(float (&d)[2][2][4], uint32_t tile, int m0, int ksteps, uint32_t xs,
+                                         int xstride, int k0, bool two) {
+  if (two)
+    mma_pair_t<true>(d, tile, m0, ksteps, xs, xstride, k0);
+  else
+    mma_pair_t<false>(d, tile, m0, ksteps, xs, xstride, k0);
+}
+
 // ---------------------------------------------------------------- tickets and barriers
-// Arrive (consumers) after this CTA's global writes with `add` (nblk in the low 8 bits plus
-// one bit per partial slot); returns in every consumer thread the counter value after the
-// add when this CTA completed the item (low byte == KB), or 0.  The last arriver resets it.
-__device__ __forceinline__ uint32_t ticket_add(uint32_t* ticket, uint32_t add, uint32_t KB, int* s_word) {
+// Arrive (consumers) after this CTA's global writes, adding the `nblk` blocks of the item that
+// this CTA computed; true in every consumer thread when this CTA completed the item (the count
+// reached KB).  The last arriver resets the counter.
+__device__ __forceinline__ bool ticket_add(uint32_t* ticket, uint32_t nblk, uint32_t KB, int* s_word) {
   __threadfence();
   csync();
   if (threadIdx.x == 0) {
-    const uint32_t now = atomicAdd(ticket, add) + add;
-    const bool last = (now & 0xFFu) == KB;
+    const uint32_t now = atomicAdd(ticket, nblk) + nblk;
+    const bool last = now == KB;
     if (last) atomicExch(ticket, 0u);
-    *s_word = last ? int(now) : 0;
+    *s_word = last ? 1 : 0;
   }
   csync();
-  const uint32_t v = uint32_t(*s_word);
-  if (v) __threadfence();
-  return v;
+  const bool last = *s_word != 0;
+  if (last) __threadfence();
+  return last;
 }
 
 // `all_threads`: synchronise the whole CTA (else the consumers only).
@@ -299,7 +353,7 @@ struct Item {
   int e;     // routed expert, or -1
   int row0;  // first row: expert-sorted row (routed), token (shared / router)
   int nt;    // rows in this token group (1..NT_MAX)
-  int c;     // 64-column chunk (router: row block)
+  int c;     // 128-column block (router: row block)
   int KB;    // blocks per item
 };
 
@@ -335,7 +389,7 @@ __device__ __forceinline__ Item decode_item(int T, const Meta& m, int kind, int 
   it.kind = kind;
   it.idx = idx;
   if (kind == KIND_GU || kind == KIND_DN) {
-    const int nch = kind == KIND_GU ? GU_NCH : OUT_NCH;
+    const int nch = kind == KIND_GU ? GU_NCB : OUT_NCB;
     const int gi = idx / nch;
     it.c = idx % nch;
     const int u = find_group_owner(m.tgp, m.U, gi);
@@ -346,7 +400,7 @@ __device__ __forceinline__ Item decode_item(int T, const Meta& m, int kind, int 
     it.nt = min(G, m.cnt[u] - tg * G);
     it.KB = kind == KIND_GU ? GU_KB : DN_KB;
   } else {
-    const int nch = kind == KIND_RT ? RT_NB : kind == KIND_SGU ? SGU_NCH : OUT_NCH;
+    const int nch = kind == KIND_RT ? RT_NB : kind == KIND_SGU ? SGU_NCB : OUT_NCB;
     const int tg = idx / nch;
     it.c = idx % nch;
     const int G = group_rows(T);
@@ -384,25 +438,38 @@ __device__ void issue_block(const Params& p, const Meta& m, const StreamMaps& ma
   block_kind(L, b, kind, idx, kb);
   const Item it = decode_item(p.T, m, kind, idx);
   mbar_arrive_expect_tx(bar, BLK_BYTES);
-  const int x = it.c * 64;
+  // gate/up: boxes [gate chunk 2c | gate 2c+1 | up 2c | up 2c+1] of 8 KB; down: [chunk 2c | 2c+1]
+  // of 16 KB (64 columns each: the 128-byte swizzle span)
+  const int x = it.c * 128;
+  constexpr int Q = BLK_BYTES / 4, Hb = BLK_BYTES / 2;
   switch (kind) {
     case KIND_RT:
 #pragma unroll
-      for (int q = 0; q < 4; ++q) tma_load_2d(stage + q * (BLK_BYTES / 4), &maps.wr, q * 64, it.c * RT_ROWS, bar);
+      for (int q = 0; q < 4; ++q) tma_load_2d(stage + q * Q, &maps.wr, q * 64, it.c * RT_ROWS, bar);
       break;
-    case KIND_GU:
-      tma_load_2d(stage, &maps.wg, x, it.e * H + kb * GU_ROWS, bar);
-      tma_load_2d(stage + BLK_BYTES / 2, &maps.wu, x, it.e * H + kb * GU_ROWS, bar);
+    case KIND_GU: {
+      const int y = it.e * H + kb * GU_ROWS;
+      tma_load_2d(stage, &maps.wg, x, y, bar);
+      tma_load_2d(stage + Q, &maps.wg, x + 64, y, bar);
+      tma_load_2d(stage + 2 * Q, &maps.wu, x, y, bar);
+      tma_load_2d(stage + 3 * Q, &maps.wu, x + 64, y, bar);
       break;
-    case KIND_SGU:
-      tma_load_2d(stage, &maps.wsg, x, kb * GU_ROWS, bar);
-      tma_load_2d(stage + BLK_BYTES / 2, &maps.wsu, x, kb * GU_ROWS, bar);
+    }
+    case KIND_SGU: {
+      const int y = kb * GU_ROWS;
+      tma_load_2d(stage, &maps.wsg, x, y, bar);
+      tma_load_2d(stage + Q, &maps.wsg, x + 64, y, bar);
+      tma_load_2d(stage + 2 * Q, &maps.wsu, x, y, bar);
+      tma_load_2d(stage + 3 * Q, &maps.wsu, x + 64, y, bar);
       break;
+    }
     case KIND_SD:
       tma_load_2d(stage, &maps.wsd, x, kb * DN_ROWS, bar);
+      tma_load_2d(stage + Hb, &maps.wsd, x + 64, kb * DN_ROWS, bar);
       break;
     default:
       tma_load_2d(stage, &maps.wd, x, it.e * I + kb * DN_ROWS, bar);
+      tma_load_2d(stage + Hb, &maps.wd, x + 64, it.e * I + kb * DN_ROWS, bar);
       break;
   }
 }
@@ -422,8 +489,10 @@ struct Stream {
   uint64_t* full;
   uint64_t* empty;
   int* misc;  // [8..15]: flags
-  const int* perm;
-  const int* inv;
+  int* plist;  // partial slots of the item being finished
+  float* out;  // output tile of the current segment
+  const uint16_t* perm;
+  const uint16_t* inv;
   const float* gw;
 };
 
@@ -455,13 +524,36 @@ __device__ __forceinline__ void release(Stream& S, int j) {
   if ((threadIdx.x & 31) == 0) mbar_arrive(S.empty + (S.ring + j) % NSTAGE);
 }
 
-__device__ __forceinline__ float* partial_slot(const Params& p, const Item& it, int slot) {
-  switch (it.kind) {
-    case KIND_GU: return p.P_gu + ((size_t)it.idx * GU_KB + slot) * (NT_MAX * 128);
-    case KIND_SGU: return p.P_sgu + ((size_t)it.idx * GU_KB + slot) * (NT_MAX * 128);
-    case KIND_SD: return p.P_sd + ((size_t)it.idx * SD_KB + slot) * (NT_MAX * 64);
-    default: return p.P_dn + ((size_t)it.idx * DN_KB + slot) * (NT_MAX * 64);
+// Partial slot `slot` (0: the piece that opens CTA `cta`'s range, 1: the piece that closes it).
+__device__ __forceinline__ float* partial_slot(const Params& p, int cta, int slot) {
+  return p.P + ((size_t)cta * 2 + slot) * PSLOT;
+}
+
+// First block of CTA c's range when n_total blocks are split over nctas CTAs (32-bit: the
+// product stays below 2^32, see MAX_STEP_BLOCKS).
+__device__ __forceinline__ int range_begin(int n_total, int nctas, int c) {
+  return int(unsigned(n_total) * unsigned(c) / unsigned(nctas));
+}
+
+// The partial slots holding the pieces of an item split over several CTAs' ranges: blocks
+// [s, s + KB) of the step's list.  Written to `list` in block order (thread 0); returns the count.
+__device__ int item_slots(int n_total, int nctas, int s, int KB, int* list) {
+  const int e = s + KB;
+  int c = int(unsigned(s) * unsigned(nctas) / unsigned(n_total));  // range_begin(c) <= s
+  int b1 = range_begin(n_total, nctas, c + 1);
+  while (c + 1 < nctas && b1 <= s) {
+    ++c;
+    b1 = range_begin(n_total, nctas, c + 1);
   }
+  int n = 0;
+  int b0 = range_begin(n_total, nctas, c);
+  while (c < nctas && b0 < e) {
+    if (b1 > b0 && b1 > s) list[n++] = c * 2 + (b0 >= s ? 0 : 1);  // (an empty range holds no piece)
+    ++c;
+    b0 = b1;
+    b1 = range_begin(n_total, nctas, c + 1);
+  }
+  return n;
 }
 
 __device__ __forceinline__ uint32_t* item_ticket(const Params& p, const Item& it) {
@@ -476,32 +568,32 @@ __device__ __forceinline__ uint32_t* item_ticket(const Params& p, const Item& it
 // Final values of an item (fp32 sums [nt][ncol] in `vals`) -> outputs.
 __device__ void item_epilogue(Stream& S, const Item& it, const float* vals) {
   const Params& p = *S.p;
-  const int nt = it.nt, c = it.c;
-  if (it.kind == KIND_GU || it.kind == KIND_SGU) {
+  const int nt = it.nt, c0 = it.c * 128;
+  if (it.kind == KIND_GU || it.kind == KIND_SGU) {  // vals[t][256]: gate columns, then up columns
     bf16* dst = it.kind == KIND_GU ? p.h : p.hs;
     const int ld = it.kind == KIND_GU ? I : IS;
-    for (int q = threadIdx.x; q < nt * 64; q += NCONS) {
-      const int t = q / 64, j = q % 64;
-      const float g = vals[t * 128 + j], u = vals[t * 128 + 64 + j];
-      dst[(size_t)(it.row0 + t) * ld + c * 64 + j] = __float2bfloat16_rn(silu_f32(g) * u);
+    for (int q = threadIdx.x; q < nt * 128; q += NCONS) {
+      const int t = q >> 7, j = q & 127;
+      const float g = vals[t * 256 + j], u = vals[t * 256 + 128 + j];
+      dst[(size_t)(it.row0 + t) * ld + c0 + j] = __float2bfloat16_rn(silu_f32(g) * u);
     }
-  } else if (it.kind == KIND_SD) {
-    for (int q = threadIdx.x; q < nt * 64; q += NCONS) {
-      const int t = q / 64, j = q % 64;
-      p.S[(size_t)(it.row0 + t) * H + c * 64 + j] = vals[t * 64 + j];
+  } else if (it.kind == KIND_SD) {  // vals[t][128]
+    for (int q = threadIdx.x; q < nt * 128; q += NCONS) {
+      const int t = q >> 7, j = q & 127;
+      p.S[(size_t)(it.row0 + t) * H + c0 + j] = vals[q];
     }
   } else {  // routed down: rows scaled by their gate
-    for (int q = threadIdx.x; q < nt * 64; q += NCONS) {
-      const int t = q / 64, j = q % 64;
+    for (int q = threadIdx.x; q < nt * 128; q += NCONS) {
+      const int t = q >> 7, j = q & 127;
       const int row = it.row0 + t;
-      p.Y[(size_t)row * H + c * 64 + j] = S.gw[S.perm[row]] * vals[t * 64 + j];
+      p.Y[(size_t)row * H + c0 + j] = S.gw[S.perm[row]] * vals[q];
     }
   }
 }
 
 // The combine, spread over the grid (all threads): y = S + sum_j Y[inv(t, j)] in slot order
 // (+ x), 8 outputs per thread-step (16-byte stores).
-__device__ void combine_share(const Params& p, const int* inv) {
+__device__ void combine_share(const Params& p, const uint16_t* inv) {
   const bool residual = (p.flags & 2u) != 0;
   const int n8 = p.T * (H / 8);
   for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < n8; q += gridDim.x * blockDim.x) {
@@ -607,60 +699,77 @@ __device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, i
   const int xlen = it.kind == KIND_SD ? IS : it.kind == KIND_DN ? I : H;
   stage_inputs(S, it, xlen);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j0 = j;
   const uint32_t xs = smem_u32(S.sm + Smem::xs);
-  float d[2][4] = {};
   const bool two = it.nt > 8;
-  // gate/up: warp w owns columns 16*(w&3) of the gate (w < 4) or up (w >= 4) tile, all 128
-  // rows; down: warp w owns columns 16*(w&3), rows [128*(w>>2), +128) of the 256-row tile.
-  const int m0 = (warp & 3) * 16;
-  const uint32_t sub = gu ? uint32_t((warp >> 2) * (BLK_BYTES / 2)) : 0u;
-  const int r0 = gu ? 0 : (warp >> 2) * 128;
-  const int rows = gu ? GU_ROWS : DN_ROWS;
-  for (int q = 0; q < nblk; ++q, ++j) {
-    wait_full(S, j);
-    mma_tile(d, smem_u32(stage_ptr(S, j)) + sub, m0, r0, 8, xs, xlen + XPAD, (kb_start + q) * rows + r0, two);
-    release(S, j);
-  }
-  // fragments -> out[half][t][col]: gate/up: col = (w>=4)*64 + 16*(w&3) + m (half 0);
-  // down: col = 16*(w&3) + m, half = w >> 2
-  float* out = reinterpret_cast<float*>(S.sm + Smem::out);
-  const int ncol = gu ? 128 : 64;
-  {
-    const int g = lane >> 2, tig = lane & 3;
-    const int half = gu ? 0 : (warp >> 2);
-    const int cb = gu ? (warp >> 2) * 64 + m0 : m0;
+  float* out = S.out;
+  const int ncol = gu ? 256 : 128;
+  const int g = lane >> 2, tig = lane & 3;
+  // C fragment (m16n8): column (weight) m0 + g (+8 for r >= 2), token 8*h2 + 2*tig (+1 for odd r)
+  if (gu) {
+    // warp w: box w >> 1 (gate 2c, gate 2c+1, up 2c, up 2c+1), columns [32*(w&1), +32) as two
+    // 16-column tiles, all 64 rows; out columns: 64 * box + column
+    float d[2][2][4] = {};
+    const uint32_t sub = uint32_t((warp >> 1) * (BLK_BYTES / 4));
+    const int m0 = (warp & 1) * 32;
+    for (int q = 0; q < nblk; ++q, ++j) {
+      wait_full(S, j);
+      mma_pair(d, smem_u32(stage_ptr(S, j)) + sub, m0, GU_ROWS / 16, xs, xlen + XPAD, (kb_start + q) * GU_ROWS, two);
+      release(S, j);
+    }
+    const int cb = (warp >> 1) * 64 + m0;
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        if (h2 == 1 && !two) break;
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+          out[(8 * h2 + 2 * tig + (r & 1)) * 256 + cb + 16 * m + g + ((r >> 1) << 3)] = d[m][h2][r];
+      }
+  } else {
+    // warp w: box w >> 2 (chunk 2c or 2c+1), columns [16*(w&3), +16), all 128 rows
+    float d[2][4] = {};
+    const uint32_t sub = uint32_t((warp >> 2) * (BLK_BYTES / 2));
+    const int m0 = (warp & 3) * 16;
+    for (int q = 0; q < nblk; ++q, ++j) {
+      wait_full(S, j);
+      mma_tile(d, smem_u32(stage_ptr(S, j)) + sub, m0, 0, DN_ROWS / 16, xs, xlen + XPAD, (kb_start + q) * DN_ROWS,
+               two);
+      release(S, j);
+    }
+    const int cb = (warp >> 2) * 64 + m0;
 #pragma unroll
     for (int h2 = 0; h2 < 2; ++h2) {
       if (h2 == 1 && !two) break;
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int col = cb + g + ((r >> 1) << 3);
-        const int t = 8 * h2 + 2 * tig + (r & 1);
-        out[(half * NT_MAX + t) * ncol + col] = d[h2][r];
-      }
+      for (int r = 0; r < 4; ++r) out[(8 * h2 + 2 * tig + (r & 1)) * 128 + cb + g + ((r >> 1) << 3)] = d[h2][r];
     }
   }
   csync();
-  if (!gu) {  // down: add the two row halves (fixed order)
-    for (int q = threadIdx.x; q < it.nt * 64; q += NCONS) out[q] = out[q] + out[NT_MAX * 64 + q];
-    csync();
-  }
   if (kb_start == 0 && nblk == it.KB) {
     item_epilogue(S, it, out);
     csync();
     return;
   }
-  float* P = partial_slot(p, it, kb_start);
+  // a piece of a split item: it opens this CTA's range (slot 0) or closes it (slot 1)
+  float* P = partial_slot(p, blockIdx.x, j0 == 0 ? 0 : 1);
   for (int q = threadIdx.x; q < it.nt * ncol; q += NCONS) P[q] = out[q];
-  const uint32_t v = ticket_add(item_ticket(p, it), uint32_t(nblk) | (1u << (8 + kb_start)), uint32_t(it.KB),
-                                S.misc + 10);
-  if (v) {
-    // last arriver: add the partial slots in block order
-    const uint32_t mask = v >> 8;
+  if (ticket_add(item_ticket(p, it), uint32_t(nblk), uint32_t(it.KB), S.misc + 10)) {
+    // last arriver: add the item's pieces in block order
+    if (threadIdx.x == 0) S.misc[11] = item_slots(S.L.n_total, S.nctas, S.b0 + j0 - kb_start, it.KB, S.plist);
+    csync();
+    const int npc = S.misc[11];
     for (int q = threadIdx.x; q < it.nt * ncol; q += NCONS) {
       float s = 0.f;
-      for (int sl = 0; sl < it.KB; ++sl)
-        if (mask & (1u << sl)) s += __ldcg(partial_slot(p, it, sl) + q);
+      for (int k0 = 0; k0 < npc; k0 += 8) {  // eight loads in flight, added in slot order
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = k0 + u < npc ? __ldcg(p.P + (size_t)S.plist[k0 + u] * PSLOT + q) : 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (k0 + u < npc) s += v[u];
+      }
       out[q] = s;
     }
     csync();
@@ -687,9 +796,8 @@ __device__ void consume(Stream& S) {
 __device__ void run_step(Stream& S, const BlockList& L) {
   S.L = L;
   S.x_cls = -1;  // the staging buffer was reused between steps
-  const long long N = L.n_total;
-  S.b0 = int(N * blockIdx.x / S.nctas);
-  S.nb = int(N * (blockIdx.x + 1) / S.nctas) - S.b0;
+  S.b0 = range_begin(L.n_total, S.nctas, blockIdx.x);
+  S.nb = range_begin(L.n_total, S.nctas, blockIdx.x + 1) - S.b0;
   if (threadIdx.x >= NCONS) {
     if (threadIdx.x == NCONS) produce(S);
   } else {
@@ -796,7 +904,7 @@ __device__ void route_tokens(const Params& p, uint8_t* sm, const int* toks, int 
 // Stable counting sort of the T*K (token, slot) pairs (expert ids in s_idx) by expert, in
 // this CTA's shared memory: routing tables (Meta), perm (sorted row -> pair), inv.
 // CTA 0 also publishes counts and offsets.  All threads of the CTA call it.
-__device__ Meta build_tables(const Params& p, uint8_t* sm, int* perm, int* inv) {
+__device__ Meta build_tables(const Params& p, uint8_t* sm, uint16_t* perm, uint16_t* inv) {
   int* s_idx = reinterpret_cast<int*>(sm + Smem::s_idx);
   int* s_cnt = reinterpret_cast<int*>(sm + Smem::s_cnt);
   int* s_fill = reinterpret_cast<int*>(sm + Smem::s_fill);
@@ -898,8 +1006,8 @@ __device__ Meta build_tables(const Params& p, uint8_t* sm, int* perm, int* inv) 
       int before = 0;
       for (int w = 0; w < warp; ++w) before += s_wcnt[w * E + e];
       const int row = s_fill[e] + before + r;
-      perm[row] = pi;
-      inv[pi] = row;
+      perm[row] = uint16_t(pi);
+      inv[pi] = uint16_t(row);
     }
     __syncthreads();
     if (act) {
@@ -937,8 +1045,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   S.full = reinterpret_cast<uint64_t*>(sm + Smem::full);
   S.empty = reinterpret_cast<uint64_t*>(sm + Smem::empty);
   S.misc = reinterpret_cast<int*>(sm + Smem::misc);
-  int* perm = reinterpret_cast<int*>(sm + Smem::perm);
-  int* inv = reinterpret_cast<int*>(sm + Smem::inv);
+  S.plist = reinterpret_cast<int*>(sm + Smem::plist);
+  S.out = reinterpret_cast<float*>(sm + out_offset(group_rows(p.T)));
+  uint16_t* perm = reinterpret_cast<uint16_t*>(sm + Smem::perm);
+  uint16_t* inv = reinterpret_cast<uint16_t*>(sm + Smem::inv);
   float* gw = reinterpret_cast<float*>(sm + Smem::gw);
   int* s_idx = reinterpret_cast<int*>(sm + Smem::s_idx);
   S.perm = perm;
@@ -1031,10 +1141,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     BlockList L;
     L.k_first = KIND_GU;
     L.kb_first = GU_KB;
-    L.n_first = S.meta.groups * GU_NCH * GU_KB;
+    L.n_first = S.meta.groups * GU_NCB * GU_KB;
     L.k_second = KIND_SGU;
     L.kb_second = GU_KB;
-    L.n_total = L.n_first + ntg * SGU_NCH * GU_KB;
+    L.n_total = L.n_first + ntg * SGU_NCB * GU_KB;
     S.first_slot = 12;
     trace_point(p, 6);
     run_step(S, L);
@@ -1048,10 +1158,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     BlockList L;
     L.k_first = KIND_DN;
     L.kb_first = DN_KB;
-    L.n_first = S.meta.groups * OUT_NCH * DN_KB;
+    L.n_first = S.meta.groups * OUT_NCB * DN_KB;
     L.k_second = KIND_SD;
     L.kb_second = SD_KB;
-    L.n_total = L.n_first + ntg * OUT_NCH * SD_KB;
+    L.n_total = L.n_first + ntg * OUT_NCB * SD_KB;
     S.first_slot = 13;
     run_step(S, L);
   }

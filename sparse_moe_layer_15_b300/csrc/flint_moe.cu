@@ -28,7 +28,7 @@ struct Layout {
   size_t status, bar_count, bar_done, tk_gu, tk_sgu, tk_sd, tk_dn;
   size_t zero_end;  // [0, zero_end): status word, barrier counters and tickets (cleared between uses)
   size_t counts, offsets, perm, inv, topk_idx, topk_w;
-  size_t xn, xstage, ystage, h, hs, S, Y, P_gu, P_sgu, P_sd, P_dn, RP, trace;
+  size_t xn, xstage, ystage, h, hs, S, Y, P, RP, trace;
   size_t xs, Yb, hist, mtp;  // prefill path (max_tokens > STREAM_MAX_T), else 0
   size_t total;
 };
@@ -50,10 +50,10 @@ Layout make_layout(int max_tokens) {
   L.status = take(256);
   L.bar_count = take(sizeof(uint32_t));
   L.bar_done = take(sizeof(uint32_t));
-  L.tk_gu = take(sizeof(uint32_t) * G * GU_NCH);
-  L.tk_sgu = take(sizeof(uint32_t) * Gs * SGU_NCH);
-  L.tk_sd = take(sizeof(uint32_t) * Gs * OUT_NCH);
-  L.tk_dn = take(sizeof(uint32_t) * G * OUT_NCH);
+  L.tk_gu = take(sizeof(uint32_t) * G * GU_NCB);
+  L.tk_sgu = take(sizeof(uint32_t) * Gs * SGU_NCB);
+  L.tk_sd = take(sizeof(uint32_t) * Gs * OUT_NCB);
+  L.tk_dn = take(sizeof(uint32_t) * G * OUT_NCB);
   L.zero_end = align_up(off, 256);
   L.counts = take(sizeof(int32_t) * E);
   L.offsets = take(sizeof(int32_t) * (E + 1));
@@ -68,10 +68,7 @@ Layout make_layout(int max_tokens) {
   L.hs = take(sizeof(uint16_t) * T * IS);
   L.S = take(sizeof(float) * T * H);
   L.Y = take(sizeof(float) * (size_t)Ts * K * H);
-  L.P_gu = take(sizeof(float) * G * GU_NCH * GU_KB * NT_MAX * 128);
-  L.P_sgu = take(sizeof(float) * Gs * SGU_NCH * GU_KB * NT_MAX * 128);
-  L.P_sd = take(sizeof(float) * Gs * OUT_NCH * SD_KB * NT_MAX * 64);
-  L.P_dn = take(sizeof(float) * G * OUT_NCH * DN_KB * NT_MAX * 64);
+  L.P = take(sizeof(float) * MAX_STREAM_CTAS * 2 * PSLOT);
   L.RP = take(sizeof(float) * RT_NB * STREAM_MAX_T * E);
   if (max_tokens > STREAM_MAX_T) {
     const size_t ntile = (T + tc::TM - 1) / tc::TM;
@@ -188,10 +185,7 @@ Params make_params(flint_moe_t h, const void* x, int T, void* y, int32_t* out_id
   p.hs = reinterpret_cast<bf16*>(ws + L.hs);
   p.S = reinterpret_cast<float*>(ws + L.S);
   p.Y = reinterpret_cast<float*>(ws + L.Y);
-  p.P_gu = reinterpret_cast<float*>(ws + L.P_gu);
-  p.P_sgu = reinterpret_cast<float*>(ws + L.P_sgu);
-  p.P_sd = reinterpret_cast<float*>(ws + L.P_sd);
-  p.P_dn = reinterpret_cast<float*>(ws + L.P_dn);
+  p.P = reinterpret_cast<float*>(ws + L.P);
   p.RP = reinterpret_cast<float*>(ws + L.RP);
   if (L.Yb) {
     p.xs = reinterpret_cast<bf16*>(ws + L.xs);
@@ -247,7 +241,8 @@ flint_moe_status run_decode(flint_moe_t h, const Params& p, cudaStream_t st, boo
   cudaError_t e = cudaSuccess;
   if (h->cfg.flags & FLINT_MOE_FLAG_PRE_RMSNORM) e = launch(h, "rmsnorm", rmsnorm_kernel, p.T, 256, 0, st, false, p);
   if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
-  e = launch(h, full ? "decode_fused" : "decode_fused_route", decode_fused, h->n_sm, NTHREADS,
+  const int grid = h->n_sm < MAX_STREAM_CTAS ? h->n_sm : MAX_STREAM_CTAS;
+  e = launch(h, full ? "decode_fused" : "decode_fused_route", decode_fused, grid, NTHREADS,
              fused_smem_bytes(group_rows(p.T)), st, true, p,
              h->smaps, full ? 0 : 1);
   return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ERR_CUDA;
@@ -526,7 +521,7 @@ flint_moe_status flint_moe_destroy(flint_moe_t h) {
 // point takes its scratch space from one fixed array in device memory that the library
 // declares itself, so the caller supplies only the weights, the input and the output.
 //
-// The array (42 MiB) holds the workspace of a handle with max_tokens = NOALLOC_MAX_T.
+// The array (17 MiB) holds the workspace of a handle with max_tokens = NOALLOC_MAX_T.
 // Every GPU that loads the library reserves it until the process exits.  All calls on a
 // device share it: calls whose work overlaps on the GPU (on different streams, or from
 // different threads) race on it and must be serialised by the caller.  The counters that must
@@ -534,7 +529,7 @@ flint_moe_status flint_moe_destroy(flint_moe_t h) {
 namespace {
 
 constexpr int NOALLOC_MAX_T = 4;
-constexpr size_t NOALLOC_BYTES = size_t(42) << 20;
+constexpr size_t NOALLOC_BYTES = size_t(17) << 20;
 constexpr int NOALLOC_MAX_DEVICES = 64;
 
 __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_BYTES];
