@@ -807,15 +807,16 @@ __device__ void run_step(Stream& S, const BlockList& L) {
   __syncthreads();
 }
 
-// Spread a bulk L2 prefetch of `bytes` (multiple of 16) at `base` over the grid (one thread).
-__device__ __forceinline__ void prefetch_share(const void* base, size_t bytes) {
-  const size_t per = ((bytes / gridDim.x) + 15) & ~size_t(15);
-  const size_t a = per * blockIdx.x;
+// Spread a bulk L2 prefetch of `bytes` (multiple of 16, below 2^32) at `base` over the grid
+// (one thread; 32-bit arithmetic: a 64-bit division costs the producer warp microseconds).
+__device__ __forceinline__ void prefetch_share(const void* base, uint32_t bytes) {
+  const uint32_t per = ((bytes / gridDim.x) + 15u) & ~15u;
+  const uint32_t a = per * blockIdx.x;
   if (a >= bytes) return;
-  size_t n = per < bytes - a ? per : bytes - a;
+  uint32_t n = per < bytes - a ? per : bytes - a;
   const uint8_t* src = static_cast<const uint8_t*>(base) + a;
   while (n) {
-    const uint32_t c = n > 65536 ? 65536u : uint32_t(n);
+    const uint32_t c = n > 65536u ? 65536u : n;
     prefetch_l2_bulk(src, c);
     src += c;
     n -= c;
@@ -1075,7 +1076,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // routed experts: its blocks stream from L2 while the routed ones stream from HBM, and a
   // short step A starts the routing sooner; measured 908 vs 944 us over the decode sweep.)
   {
-    if (full && threadIdx.x == NCONS + 1) prefetch_share(p.ws_down, (size_t)IS * H * 2);
+    if (full && threadIdx.x == NCONS + 1) prefetch_share(p.ws_down, uint32_t(IS) * H * 2);
     BlockList L;
     L.k_first = L.k_second = KIND_RT;
     L.kb_first = L.kb_second = 1;
@@ -1122,17 +1123,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   {
     // the touched experts' down matrices are read in step D: prefetch them when they fit
     if (threadIdx.x == NCONS + 1 && (unsigned long long)S.meta.U * I * H * 2 <= p.prefetch_bytes_max) {
-      const size_t per_e = (size_t)I * H * 2;
-      const size_t total = per_e * S.meta.U;
-      const size_t share = ((total / gridDim.x) + 15) & ~size_t(15);
-      size_t a = share * blockIdx.x;
-      const size_t b = a + share < total ? a + share : total;
+      // 32-bit offsets: U * I * H * 2 <= 512 MB
+      constexpr uint32_t per_e = uint32_t(I) * H * 2;
+      const uint32_t total = per_e * uint32_t(S.meta.U);
+      const uint32_t share = ((total / gridDim.x) + 15u) & ~15u;
+      uint32_t a = share * blockIdx.x;
+      const uint32_t b = a < total ? (total - a > share ? a + share : total) : a;
       while (a < b) {
         const int u = int(a / per_e);
-        const size_t in_e = a % per_e;
-        size_t n = per_e - in_e;
+        const uint32_t in_e = a % per_e;
+        uint32_t n = per_e - in_e;
         if (n > b - a) n = b - a;
-        if (n > 65536) n = 65536;
+        if (n > 65536u) n = 65536u;
         prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(p.w_down + (size_t)S.meta.e[u] * I * H) + in_e,
                          uint32_t(n));
         a += n;
