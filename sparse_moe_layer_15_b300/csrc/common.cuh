@@ -68,6 +68,7 @@ struct Params {
   uint32_t* tk_sgu;
   uint32_t* tk_sd;
   uint32_t* tk_dn;
+  uint32_t* tk_comb;     // [H/128] down items finished per 128-column block (decode path)
   // user-visible copies (may be null)
   int32_t* out_idx;
   float* out_w;

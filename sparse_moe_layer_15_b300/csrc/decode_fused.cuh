@@ -62,6 +62,7 @@ constexpr int OUT_NCB = H / 128;         // 16 column blocks of a down projectio
 constexpr int MAX_STREAM_CTAS = 256;     // largest grid of the decode kernel (the workspace holds its partial slots)
 constexpr int PSLOT = NT_MAX * 256;      // floats of one partial slot: [rows][256] gate|up, or [rows][128] down
 constexpr int REDUNDANT_ROUTING_MAX_T = 4;
+constexpr int PREISSUE_MAX_T = 4;  // step D's first block is issued before its barrier up to this many tokens
 constexpr int MAX_PAIRS = STREAM_MAX_T * K;
 constexpr int XPAD = 8;                  // bf16 padding of a staged input row (bank spread)
 
@@ -491,6 +492,7 @@ struct Stream {
   int* misc;  // [8..15]: flags
   int* plist;  // partial slots of the item being finished
   float* out;  // output tile of the current segment
+  int comb_items;  // > 0: combine each 128-column block when its comb_items down items are done
   const uint16_t* perm;
   const uint16_t* inv;
   const float* gw;
@@ -500,9 +502,9 @@ __device__ __forceinline__ uint8_t* stage_ptr(const Stream& S, int j) {
   return S.sm + Smem::stages + ((S.ring + j) % NSTAGE) * BLK_BYTES;
 }
 
-// Producer (one lane): stream this CTA's range of the step through the stage ring.
-__device__ void produce(Stream& S) {
-  for (int j = 0; j < S.nb; ++j) {
+// Producer (one lane): issue blocks [from, to) of this CTA's range of the step into the stage ring.
+__device__ void produce(Stream& S, int from, int to) {
+  for (int j = from; j < to; ++j) {
     const int pos = S.ring + j;
     const int st = pos % NSTAGE;
     const int use = pos / NSTAGE;
@@ -591,38 +593,45 @@ __device__ void item_epilogue(Stream& S, const Item& it, const float* vals) {
   }
 }
 
-// The combine, spread over the grid (all threads): y = S + sum_j Y[inv(t, j)] in slot order
-// (+ x), 8 outputs per thread-step (16-byte stores).
-__device__ void combine_share(const Params& p, const uint16_t* inv) {
-  const bool residual = (p.flags & 2u) != 0;
-  const int n8 = p.T * (H / 8);
-  for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < n8; q += gridDim.x * blockDim.x) {
-    const int t = q / (H / 8), col = (q % (H / 8)) * 8;
-    float v[8];
-    const float4* s4 = reinterpret_cast<const float4*>(p.S + (size_t)t * H + col);
-    float4 a = __ldcg(s4), b = __ldcg(s4 + 1);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+// y[t][col .. col+8) = S + sum_j Y[inv(t, j)] in slot order (+ x), one 16-byte store.
+__device__ __forceinline__ void combine8(const Params& p, const uint16_t* inv, int t, int col) {
+  float v[8];
+  const float4* s4 = reinterpret_cast<const float4*>(p.S + (size_t)t * H + col);
+  float4 a = __ldcg(s4), b = __ldcg(s4 + 1);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 #pragma unroll
-    for (int k = 0; k < K; ++k) {
-      const float4* y4 = reinterpret_cast<const float4*>(p.Y + (size_t)inv[t * K + k] * H + col);
-      a = __ldcg(y4);
-      b = __ldcg(y4 + 1);
-      v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w; v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
-    }
-    if (residual) {
-      float f[8];
-      bf16x8_to_f32(*reinterpret_cast<const uint4*>(p.x + (size_t)t * H + col), f);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] += f[i];
-    }
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-      w[i] = *reinterpret_cast<const uint32_t*>(&h2);
-    }
-    *reinterpret_cast<uint4*>(p.y + (size_t)t * H + col) = make_uint4(w[0], w[1], w[2], w[3]);
+  for (int k = 0; k < K; ++k) {
+    const float4* y4 = reinterpret_cast<const float4*>(p.Y + (size_t)inv[t * K + k] * H + col);
+    a = __ldcg(y4);
+    b = __ldcg(y4 + 1);
+    v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w; v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
   }
+  if (p.flags & 2u) {  // residual
+    float f[8];
+    bf16x8_to_f32(*reinterpret_cast<const uint4*>(p.x + (size_t)t * H + col), f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] += f[i];
+  }
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<const uint32_t*>(&h2);
+  }
+  *reinterpret_cast<uint4*>(p.y + (size_t)t * H + col) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// The combine, spread over the grid (all threads), after the last grid barrier.
+__device__ void combine_share(const Params& p, const uint16_t* inv) {
+  const int n8 = p.T * (H / 8);
+  for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < n8; q += gridDim.x * blockDim.x)
+    combine8(p, inv, q / (H / 8), (q % (H / 8)) * 8);
+}
+
+// The combine of 128-column block cb for all tokens (consumers), by the CTA that finished the
+// block's last down item.
+__device__ void combine_block(const Params& p, const uint16_t* inv, int cb) {
+  for (int q = threadIdx.x; q < p.T * 16; q += NCONS) combine8(p, inv, q >> 4, cb * 128 + (q & 15) * 8);
 }
 
 // Stage the token group's input rows (bf16, row stride xlen + XPAD; rows nt .. G-1 zero) for an
@@ -747,35 +756,39 @@ __device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, i
     }
   }
   csync();
-  if (kb_start == 0 && nblk == it.KB) {
-    item_epilogue(S, it, out);
-    csync();
-    return;
-  }
-  // a piece of a split item: it opens this CTA's range (slot 0) or closes it (slot 1)
-  float* P = partial_slot(p, blockIdx.x, j0 == 0 ? 0 : 1);
-  for (int q = threadIdx.x; q < it.nt * ncol; q += NCONS) P[q] = out[q];
-  if (ticket_add(item_ticket(p, it), uint32_t(nblk), uint32_t(it.KB), S.misc + 10)) {
-    // last arriver: add the item's pieces in block order
-    if (threadIdx.x == 0) S.misc[11] = item_slots(S.L.n_total, S.nctas, S.b0 + j0 - kb_start, it.KB, S.plist);
-    csync();
-    const int npc = S.misc[11];
-    for (int q = threadIdx.x; q < it.nt * ncol; q += NCONS) {
-      float s = 0.f;
-      for (int k0 = 0; k0 < npc; k0 += 8) {  // eight loads in flight, added in slot order
-        float v[8];
+  bool done = true;  // this CTA writes the item's outputs
+  if (kb_start != 0 || nblk != it.KB) {
+    // a piece of a split item: it opens this CTA's range (slot 0) or closes it (slot 1)
+    float* P = partial_slot(p, blockIdx.x, j0 == 0 ? 0 : 1);
+    for (int q = threadIdx.x; q < it.nt * ncol; q += NCONS) P[q] = out[q];
+    done = ticket_add(item_ticket(p, it), uint32_t(nblk), uint32_t(it.KB), S.misc + 10);
+    if (done) {
+      // last arriver: add the item's pieces in block order
+      if (threadIdx.x == 0) S.misc[11] = item_slots(S.L.n_total, S.nctas, S.b0 + j0 - kb_start, it.KB, S.plist);
+      csync();
+      const int npc = S.misc[11];
+      for (int q = threadIdx.x; q < it.nt * ncol; q += NCONS) {
+        float s = 0.f;
+        for (int k0 = 0; k0 < npc; k0 += 8) {  // eight loads in flight, added in slot order
+          float v[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = k0 + u < npc ? __ldcg(p.P + (size_t)S.plist[k0 + u] * PSLOT + q) : 0.f;
+          for (int u = 0; u < 8; ++u) v[u] = k0 + u < npc ? __ldcg(p.P + (size_t)S.plist[k0 + u] * PSLOT + q) : 0.f;
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (k0 + u < npc) s += v[u];
+          for (int u = 0; u < 8; ++u)
+            if (k0 + u < npc) s += v[u];
+        }
+        out[q] = s;
       }
-      out[q] = s;
+      csync();
     }
-    csync();
-    item_epilogue(S, it, out);
   }
+  if (done) item_epilogue(S, it, out);
   csync();
+  // down outputs: the last item of a 128-column block combines that block for every token
+  if (done && S.comb_items && !gu && ticket_last(p.tk_comb + it.c, uint32_t(S.comb_items), S.misc + 14, false)) {
+    combine_block(p, S.inv, it.c);
+    csync();
+  }
 }
 
 // Consumers: work through this CTA's range of the step.
@@ -792,19 +805,34 @@ __device__ void consume(Stream& S) {
   }
 }
 
-// One streaming step for the whole CTA: the producer lane streams, the consumers compute.
-__device__ void run_step(Stream& S, const BlockList& L) {
+// Make L the current step: this CTA's range of its blocks.
+__device__ __forceinline__ void set_step(Stream& S, const BlockList& L) {
   S.L = L;
   S.x_cls = -1;  // the staging buffer was reused between steps
   S.b0 = range_begin(L.n_total, S.nctas, blockIdx.x);
   S.nb = range_begin(L.n_total, S.nctas, blockIdx.x + 1) - S.b0;
+}
+
+// Run the current step for the whole CTA: the producer lane streams (its first `pre` blocks
+// were issued already), the consumers compute.
+__device__ void run_step(Stream& S, int pre = 0) {
   if (threadIdx.x >= NCONS) {
-    if (threadIdx.x == NCONS) produce(S);
+    if (threadIdx.x == NCONS) produce(S, pre, S.nb);
   } else {
     consume(S);
   }
   S.ring += S.nb;
   __syncthreads();
+}
+
+// Bounded wait (one thread) for blocks [0, n) of the current step to land: a CTA that leaves
+// early must not exit with copies into its shared memory in flight.
+__device__ void drain_issued(Stream& S, int n) {
+  if (threadIdx.x == NCONS)
+    for (int j = 0; j < n; ++j) {
+      const int pos = S.ring + j;
+      mbar_wait_or_flag(S.full + pos % NSTAGE, uint32_t(pos / NSTAGE) & 1u, S.p->status);
+    }
 }
 
 // Spread a bulk L2 prefetch of `bytes` (multiple of 16, below 2^32) at `base` over the grid
@@ -1048,6 +1076,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   S.misc = reinterpret_cast<int*>(sm + Smem::misc);
   S.plist = reinterpret_cast<int*>(sm + Smem::plist);
   S.out = reinterpret_cast<float*>(sm + out_offset(group_rows(p.T)));
+  S.comb_items = 0;
   uint16_t* perm = reinterpret_cast<uint16_t*>(sm + Smem::perm);
   uint16_t* inv = reinterpret_cast<uint16_t*>(sm + Smem::inv);
   float* gw = reinterpret_cast<float*>(sm + Smem::gw);
@@ -1081,7 +1110,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     L.k_first = L.k_second = KIND_RT;
     L.kb_first = L.kb_second = 1;
     L.n_first = L.n_total = ntg * RT_NB;
-    run_step(S, L);
+    set_step(S, L);
+    run_step(S);
   }
   trace_point(p, 2);
   if (!grid_sync(p, 1, S.misc + 12)) return;
@@ -1149,13 +1179,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     L.n_total = L.n_first + ntg * SGU_NCB * GU_KB;
     S.first_slot = 12;
     trace_point(p, 6);
-    run_step(S, L);
+    set_step(S, L);
+    run_step(S);
   }
   trace_point(p, 7);
-  if (!grid_sync(p, ++nbar, S.misc + 12)) return;
-  trace_point(p, 8);
 
-  // ---- step D: routed down projection and the shared down projection
+  // ---- step D: routed down projection and the shared down projection.  Its blocks are weights
+  // only: for small calls (latency-bound) the producer issues the first one before the barrier
+  // that publishes step C's outputs.  (Measured: more early blocks, or early blocks for larger
+  // calls, slow the CTAs still streaming step C, which set the barrier's time.)
   {
     BlockList L;
     L.k_first = KIND_DN;
@@ -1164,14 +1196,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     L.k_second = KIND_SD;
     L.kb_second = SD_KB;
     L.n_total = L.n_first + ntg * OUT_NCB * SD_KB;
-    S.first_slot = 13;
-    run_step(S, L);
+    set_step(S, L);
   }
+  const int pre = T <= PREISSUE_MAX_T ? min(1, S.nb) : 0;
+  if (threadIdx.x == NCONS) produce(S, 0, pre);
+  if (!grid_sync(p, ++nbar, S.misc + 12)) {
+    drain_issued(S, pre);
+    return;
+  }
+  trace_point(p, 8);
+  // When the grid has a CTA for every down item, the combine of each 128-column block follows
+  // its last down item (no further barrier); otherwise the whole grid combines after a barrier
+  // (a ticket per item then costs each CTA a fence and an atomic per item: slower).
+  S.comb_items = (S.meta.groups + ntg) * OUT_NCB <= S.nctas ? S.meta.groups + ntg : 0;
+  S.first_slot = 13;
+  run_step(S, pre);
   trace_point(p, 9);
-  if (!grid_sync(p, ++nbar, S.misc + 12)) return;
-  trace_point(p, 14);
-  // ---- the combine, over the whole grid
-  combine_share(p, inv);
+  if (!S.comb_items) {
+    if (!grid_sync(p, ++nbar, S.misc + 12)) return;
+    trace_point(p, 14);
+    combine_share(p, inv);
+  }
   grid_done(p, S.misc + 13);
   trace_point(p, 10);
 }

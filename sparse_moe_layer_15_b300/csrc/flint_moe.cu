@@ -25,7 +25,7 @@ constexpr int MAX_TRACE_CTAS = 1024;
 
 struct Layout {
   // tickets first: [status, tickets) and [tickets, scalars) are cleared together after errors
-  size_t status, bar_count, bar_done, tk_gu, tk_sgu, tk_sd, tk_dn;
+  size_t status, bar_count, bar_done, tk_gu, tk_sgu, tk_sd, tk_dn, tk_comb;
   size_t zero_end;  // [0, zero_end): status word, barrier counters and tickets (cleared between uses)
   size_t counts, offsets, perm, inv, topk_idx, topk_w;
   size_t xn, xstage, ystage, h, hs, S, Y, P, RP, trace;
@@ -54,6 +54,7 @@ Layout make_layout(int max_tokens) {
   L.tk_sgu = take(sizeof(uint32_t) * Gs * SGU_NCB);
   L.tk_sd = take(sizeof(uint32_t) * Gs * OUT_NCB);
   L.tk_dn = take(sizeof(uint32_t) * G * OUT_NCB);
+  L.tk_comb = take(sizeof(uint32_t) * OUT_NCB);
   L.zero_end = align_up(off, 256);
   L.counts = take(sizeof(int32_t) * E);
   L.offsets = take(sizeof(int32_t) * (E + 1));
@@ -175,6 +176,7 @@ Params make_params(flint_moe_t h, const void* x, int T, void* y, int32_t* out_id
   p.tk_sgu = reinterpret_cast<uint32_t*>(ws + L.tk_sgu);
   p.tk_sd = reinterpret_cast<uint32_t*>(ws + L.tk_sd);
   p.tk_dn = reinterpret_cast<uint32_t*>(ws + L.tk_dn);
+  p.tk_comb = reinterpret_cast<uint32_t*>(ws + L.tk_comb);
   p.counts = reinterpret_cast<int32_t*>(ws + L.counts);
   p.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
   p.perm = reinterpret_cast<int32_t*>(ws + L.perm);
@@ -283,6 +285,10 @@ flint_moe_status run_prefill(flint_moe_t h, const Params& p, cudaStream_t st, bo
 }
 
 flint_moe_status run_layer(flint_moe_t h, const Params& p, cudaStream_t st, bool full) {
+  // a traced call starts from a cleared trace: slots that its kernels do not stamp read 0
+  if (p.trace && cudaMemsetAsync(p.trace, 0, sizeof(unsigned long long) * MAX_TRACE_CTAS * TRACE_SLOTS, st) !=
+                     cudaSuccess)
+    return FLINT_MOE_ERR_CUDA;
   return p.T <= STREAM_MAX_T ? run_decode(h, p, st, full) : run_prefill(h, p, st, full);
 }
 
