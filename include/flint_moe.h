@@ -165,6 +165,49 @@ flint_moe_status flint_moe_destroy(flint_moe_t h);
 flint_moe_status flint_moe_forward_noalloc(const flint_moe_weights* w, const void* x, int T, void* y,
                                            int32_t* topk_idx, float* topk_w, flint_stream_t stream);
 
+/* ---------------------------------------------------------------- the layer stack
+ * The model runs its MoE layers back to back: two dense layers, then 47 MoE layers (Recursive
+ * Flint serving-kit post, section "The architecture, from the config"); the pages' own engine
+ * fuses the decode forward pass into one kernel (news article "Recursive opens Flint, a 40B
+ * coding model with 2.5B active", section "Built with the Eureka Machine").  A stack handle applies
+ * n_layers MoE layers, each with its own weights, in place,
+ *     x <- [x +] MoE_l([RMSNorm](x)),  l = 0 .. n_layers-1  (the config's flags, for every layer),
+ * For T <= 16 in ONE persistent cooperative kernel launch: each layer's steps as in
+ * flint_moe_forward, a grid-wide barrier between layers instead of a kernel boundary, and the
+ * next layer's pre-norm done by the CTAs that combine each token row; for larger T (where that
+ * kernel measured slower) as the single-layer launches, layer by layer, on `stream`.  Either way
+ * the results are bitwise those of n_layers successive flint_moe_forward calls (x in, y = x) with
+ * the same config on the layers' weights.  Decode sizes only: cfg->max_tokens <= 256, else
+ * FLINT_MOE_ERR_UNSUPPORTED. */
+typedef struct flint_moe_stack_s* flint_moe_stack_t;
+
+/* Workspace bytes for a stack of n_layers (>= 1) layers: one layer's scratch plus a device
+ * table of the layers' tensor maps (about 1 KB per layer). */
+flint_moe_status flint_moe_stack_workspace_bytes(const flint_moe_config* cfg, int n_layers, size_t* bytes);
+
+/* layers: host array of n_layers weight sets (each as for flint_moe_create; borrowed, they must
+ * stay valid).  workspace: caller-owned device memory, 256-byte aligned, at least
+ * flint_moe_stack_workspace_bytes; the call writes the layer table into it (synchronously). */
+flint_moe_status flint_moe_stack_create(const flint_moe_config* cfg, const flint_moe_weights* layers, int n_layers,
+                                        void* workspace, size_t workspace_bytes, flint_moe_stack_t* out);
+
+/* x: device bf16 [T][2048], 16-byte aligned, read and overwritten with the stack's output;
+ * 1 <= T <= max_tokens.  topk_idx / topk_w: optional device [n_layers][T][6] copies of every
+ * layer's routing (null to skip).  Asynchronous on `stream`; no allocation. */
+flint_moe_status flint_moe_stack_forward(flint_moe_stack_t s, void* x, int T, int32_t* topk_idx, float* topk_w,
+                                         flint_stream_t stream);
+
+/* As flint_moe_poll_device_status, for the stack's workspace. */
+flint_moe_status flint_moe_stack_poll_device_status(flint_moe_stack_t s, flint_stream_t stream);
+
+/* As flint_moe_enable_kernel_timing / flint_moe_read_trace, for the stack's launches (the phase
+ * trace holds the last layer's stamps). */
+flint_moe_status flint_moe_stack_enable_kernel_timing(flint_moe_stack_t s, int enable);
+flint_moe_status flint_moe_stack_read_trace(flint_moe_stack_t s, unsigned long long* out, int cap, int* n);
+
+/* Releases the stack's host state (not the workspace or the weights). */
+flint_moe_status flint_moe_stack_destroy(flint_moe_stack_t s);
+
 #ifdef __cplusplus
 }
 #endif

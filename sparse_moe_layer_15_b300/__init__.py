@@ -25,7 +25,9 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "
 EXPORTS = ("flint_moe_status_string", "flint_moe_workspace_bytes", "flint_moe_create", "flint_moe_route",
            "flint_moe_forward", "flint_moe_forward_host", "flint_moe_poll_device_status",
            "flint_moe_enable_kernel_timing", "flint_moe_kernel_times", "flint_moe_read_trace",
-           "flint_moe_destroy", "flint_moe_forward_noalloc")
+           "flint_moe_destroy", "flint_moe_forward_noalloc", "flint_moe_stack_workspace_bytes",
+           "flint_moe_stack_create", "flint_moe_stack_forward", "flint_moe_stack_poll_device_status",
+           "flint_moe_stack_enable_kernel_timing", "flint_moe_stack_read_trace", "flint_moe_stack_destroy")
 
 NOALLOC_MAX_TOKENS = 4
 
@@ -80,6 +82,14 @@ def load_library():
     L.flint_moe_read_trace.argtypes = [P, ctypes.POINTER(ctypes.c_ulonglong), I32, ctypes.POINTER(I32)]
     L.flint_moe_destroy.argtypes = [P]
     L.flint_moe_forward_noalloc.argtypes = [ctypes.POINTER(_Weights), P, I32, P, P, P, P]
+    L.flint_moe_stack_workspace_bytes.argtypes = [ctypes.POINTER(_Config), I32, ctypes.POINTER(ctypes.c_size_t)]
+    L.flint_moe_stack_create.argtypes = [ctypes.POINTER(_Config), ctypes.POINTER(_Weights), I32, P, ctypes.c_size_t,
+                                         ctypes.POINTER(P)]
+    L.flint_moe_stack_forward.argtypes = [P, P, I32, P, P, P]
+    L.flint_moe_stack_poll_device_status.argtypes = [P, P]
+    L.flint_moe_stack_enable_kernel_timing.argtypes = [P, I32]
+    L.flint_moe_stack_read_trace.argtypes = [P, ctypes.POINTER(ctypes.c_ulonglong), I32, ctypes.POINTER(I32)]
+    L.flint_moe_stack_destroy.argtypes = [P]
     for name in EXPORTS:
         if name != "flint_moe_status_string":
             getattr(L, name).restype = I32
@@ -219,6 +229,79 @@ class FlintMoE:
     def close(self):
         if getattr(self, "_h", None):
             self._L.flint_moe_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def stack_workspace_bytes(n_layers: int, max_tokens: int, flags: int = 0, rms_eps: float = 1e-6) -> int:
+    L = load_library()
+    cfg = _Config(HIDDEN, N_EXPERTS, TOP_K, EXPERT_INTER, SHARED_INTER, max_tokens, flags, rms_eps)
+    n = ctypes.c_size_t(0)
+    _check(L.flint_moe_stack_workspace_bytes(ctypes.byref(cfg), int(n_layers), ctypes.byref(n)),
+           "flint_moe_stack_workspace_bytes")
+    return n.value
+
+
+class FlintMoEStack:
+    """n MoE layers applied in place in one kernel launch (flint_moe_stack_*): x <- [x +]
+    MoE_l([RMSNorm](x)) for l = 0..n-1 with the config's flags.  ``weights_list``: one dict per
+    layer as for :class:`FlintMoE` (borrowed; keep them alive).  Decode sizes: max_tokens <= 256."""
+
+    def __init__(self, weights_list, max_tokens: int, flags: int = 0, rms_eps: float = 1e-6, workspace=None):
+        import torch
+        self._L = load_library()
+        self.n_layers = len(weights_list)
+        self.max_tokens = int(max_tokens)
+        self._weights = weights_list
+        for w in weights_list:
+            for k, v in w.items():
+                if v is not None and not v.is_contiguous():
+                    raise ValueError(f"{k} must be contiguous")
+        self._cfg = _Config(HIDDEN, N_EXPERTS, TOP_K, EXPERT_INTER, SHARED_INTER, self.max_tokens, int(flags),
+                            float(rms_eps))
+        arr = (_Weights * self.n_layers)(*[
+            _Weights(*[(w[n].data_ptr() if w.get(n) is not None else None) for n, _ in _Weights._fields_])
+            for w in weights_list])
+        nbytes = stack_workspace_bytes(self.n_layers, self.max_tokens, flags, rms_eps)
+        if workspace is None:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=weights_list[0]["w_router"].device)
+        self.workspace = workspace
+        h = ctypes.c_void_p()
+        _check(self._L.flint_moe_stack_create(ctypes.byref(self._cfg), arr, self.n_layers,
+                                              ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                                              ctypes.byref(h)), "flint_moe_stack_create")
+        self._h = h
+
+    def forward(self, x, topk_idx=None, topk_w=None, stream=None):
+        """In place on x (bf16 [T, 2048] on the GPU); returns x.  topk_idx / topk_w: optional
+        [n_layers, T, 6] int32 / float32 device tensors receiving every layer's routing."""
+        _check(self._L.flint_moe_stack_forward(self._h, _ptr(x), x.shape[0], _ptr(topk_idx), _ptr(topk_w),
+                                               _stream_ptr(stream)), "flint_moe_stack_forward")
+        return x
+
+    def poll_device_status(self, stream=None):
+        return self._L.flint_moe_stack_poll_device_status(self._h, _stream_ptr(stream))
+
+    def enable_phase_trace(self, on=True):
+        _check(self._L.flint_moe_stack_enable_kernel_timing(self._h, 2 if on else 0),
+               "flint_moe_stack_enable_kernel_timing")
+
+    def read_trace(self, slots=TRACE_SLOTS):
+        """The last call's phase trace (the last layer's stamps): list of per-CTA lists."""
+        cap = 1024 * slots
+        buf = (ctypes.c_ulonglong * cap)()
+        n = ctypes.c_int(0)
+        _check(self._L.flint_moe_stack_read_trace(self._h, buf, cap, ctypes.byref(n)), "flint_moe_stack_read_trace")
+        return [list(buf[i:i + slots]) for i in range(0, n.value, slots)]
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._L.flint_moe_stack_destroy(self._h)
             self._h = None
 
     def __del__(self):

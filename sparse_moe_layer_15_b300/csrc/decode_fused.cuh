@@ -593,8 +593,8 @@ __device__ void item_epilogue(Stream& S, const Item& it, const float* vals) {
   }
 }
 
-// y[t][col .. col+8) = S + sum_j Y[inv(t, j)] in slot order (+ x), one 16-byte store.
-__device__ __forceinline__ void combine8(const Params& p, const uint16_t* inv, int t, int col) {
+// y[t][col .. col+8) = S + sum_j Y[inv(t, j)] in slot order (+ x), one 16-byte store (returned).
+__device__ __forceinline__ uint4 combine8(const Params& p, const uint16_t* inv, int t, int col) {
   float v[8];
   const float4* s4 = reinterpret_cast<const float4*>(p.S + (size_t)t * H + col);
   float4 a = __ldcg(s4), b = __ldcg(s4 + 1);
@@ -618,7 +618,9 @@ __device__ __forceinline__ void combine8(const Params& p, const uint16_t* inv, i
     const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
     w[i] = *reinterpret_cast<const uint32_t*>(&h2);
   }
-  *reinterpret_cast<uint4*>(p.y + (size_t)t * H + col) = make_uint4(w[0], w[1], w[2], w[3]);
+  const uint4 out = make_uint4(w[0], w[1], w[2], w[3]);
+  *reinterpret_cast<uint4*>(p.y + (size_t)t * H + col) = out;
+  return out;
 }
 
 // The combine, spread over the grid (all threads), after the last grid barrier.
@@ -858,8 +860,10 @@ __device__ __forceinline__ void prefetch_share(const void* base, uint32_t bytes)
 // through the sigmoid.  key = (order-preserving bits of the logit, 255 - expert): max =
 // highest logit, lowest index on ties (-0 is folded into +0 so that they tie).
 // All threads of the CTA call it.
-__device__ void route_tokens(const Params& p, uint8_t* sm, const int* toks, int nt, int* s_idx, float* s_gw,
-                             bool write_global) {
+// bias: the layer's router bias (or null); out_idx / out_w: the caller's copies of the routing
+// (or null).
+__device__ void route_tokens(const Params& p, const float* bias, int32_t* out_idx, float* out_w, uint8_t* sm,
+                             const int* toks, int nt, int* s_idx, float* s_gw, bool write_global) {
   float* scores = reinterpret_cast<float*>(sm + Smem::scores);
   const int e = threadIdx.x;
   if (e < E) {
@@ -871,7 +875,7 @@ __device__ void route_tokens(const Params& p, uint8_t* sm, const int* toks, int 
       float l = 0.f;
 #pragma unroll
       for (int rb = 0; rb < RT_NB; ++rb) l += part[rb];
-      if (p.router_bias) l += p.router_bias[e];
+      if (bias) l += bias[e];
       if (l == 0.f) l = 0.f;
       scores[t * E + e] = l;
     }
@@ -921,8 +925,8 @@ __device__ void route_tokens(const Params& p, uint8_t* sm, const int* toks, int 
         if (write_global) {
           p.topk_idx[tok * K + jj] = sel_e[jj];
           p.topk_w[tok * K + jj] = g;
-          if (p.out_idx) p.out_idx[tok * K + jj] = sel_e[jj];
-          if (p.out_w) p.out_w[tok * K + jj] = g;
+          if (out_idx) out_idx[tok * K + jj] = sel_e[jj];
+          if (out_w) out_w[tok * K + jj] = g;
         }
       }
     }
@@ -1122,18 +1126,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (T <= REDUNDANT_ROUTING_MAX_T) {
     int toks[REDUNDANT_ROUTING_MAX_T];
     for (int t = 0; t < T; ++t) toks[t] = t;
-    route_tokens(p, sm, toks, T, s_idx, gw, blockIdx.x == 0);
+    route_tokens(p, p.router_bias, p.out_idx, p.out_w, sm, toks, T, s_idx, gw, blockIdx.x == 0);
   } else {
     int toks[4];
     int nt = 0;
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
       toks[nt++] = t;
       if (nt == 4) {
-        route_tokens(p, sm, toks, nt, nullptr, nullptr, true);
+        route_tokens(p, p.router_bias, p.out_idx, p.out_w, sm, toks, nt, nullptr, nullptr, true);
         nt = 0;
       }
     }
-    if (nt) route_tokens(p, sm, toks, nt, nullptr, nullptr, true);
+    if (nt) route_tokens(p, p.router_bias, p.out_idx, p.out_w, sm, toks, nt, nullptr, nullptr, true);
     if (!grid_sync(p, ++nbar, S.misc + 12)) return;
     for (int q = threadIdx.x; q < T * K; q += NTHREADS) {
       s_idx[q] = __ldcg(p.topk_idx + q);
@@ -1216,6 +1220,233 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (!grid_sync(p, ++nbar, S.misc + 12)) return;
     trace_point(p, 14);
     combine_share(p, inv);
+  }
+  grid_done(p, S.misc + 13);
+  trace_point(p, 10);
+}
+
+// ================================================================ the layer stack in one launch
+// n_layers layers applied in place, x <- [x +] MoE_l([RMSNorm](x)), by one persistent cooperative
+// kernel: each layer runs steps A-D as decode_fused does, and a grid barrier replaces the kernel
+// boundary.  The combine gives each CTA whole token rows, so the same CTA normalises those rows
+// for the next layer right away (no separate pre-norm pass).  Layer l's tensor maps, router bias
+// and prefetch pointers come from a table in device memory; everything else is the launch's
+// parameters (read from the constant bank: a shared-memory copy of them measured 3-4 % slower).
+
+// Up to this many tokens the stack runs in one launch of decode_stack; above, as one launch of
+// decode_fused per layer.  Measured on B300 (12 layers, pre-norm + residual, us per layer): T = 1
+// 34.8 vs 38.5, T = 4 56.0 vs 60.3, T = 16 118.4 vs 119.4, T = 64 259.4 vs 249.8, T = 256 367.8
+// vs 357.0.  The phase trace puts the larger calls' difference in the streaming steps C and D,
+// whose code the two kernels share (the gate/up step streams about 6 % slower inside the layer
+// loop).
+constexpr int STACK_ONE_LAUNCH_MAX_T = 16;
+
+// Per-layer entry of the stack's device table (aligned as its tensor maps; the table starts on a
+// 256-byte boundary).
+struct LayerTab {
+  StreamMaps maps;
+  const float* router_bias;
+  const bf16* w_down;
+  const bf16* ws_down;
+};
+static_assert(alignof(LayerTab) >= 64 && alignof(LayerTab) <= 256, "tensor maps stay aligned in the table");
+
+
+// r = bf16(v / sqrt(mean(v^2) + eps)) of one token row whose eight values v (bf16, packed)
+// column chunk threadIdx.x holds, written to xn: the reduction of rmsnorm_kernel (thread i sums
+// its chunk in order, a butterfly over the warp, the eight warp sums in order).  Consumers only;
+// `red` is [NWARPS] floats of shared scratch.
+__device__ __forceinline__ void norm_row(const Params& p, int t, uint4 v, float* red) {
+  float f[8];
+  bf16x8_to_f32(v, f);
+  float ss = 0.f;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) ss = fmaf(f[q], f[q], ss);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  csync();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < NWARPS; ++w) tot += red[w];
+  const float d = sqrtf(tot / float(H) + p.rms_eps);
+  uint32_t packed[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * q] / d, f[2 * q + 1] / d);
+    packed[q] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  *(reinterpret_cast<uint4*>(p.xn + (size_t)t * H) + threadIdx.x) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  csync();  // red is reused by the next row
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    decode_stack(const __grid_constant__ Params base, const LayerTab* __restrict__ tab, int n_layers) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = aligned_smem(smem_raw);
+  const int T = base.T;
+  const int G = group_rows(T);
+  const int ntg = (T + G - 1) / G;
+  const bool prenorm = (base.flags & 1u) != 0;  // FLINT_MOE_FLAG_PRE_RMSNORM
+  const Params& p = base;
+  Stream S;
+  S.p = &base;
+  S.meta = Meta{};
+  S.nctas = gridDim.x;
+  S.ring = 0;
+  S.first_slot = 11;
+  S.sm = sm;
+  S.full = reinterpret_cast<uint64_t*>(sm + Smem::full);
+  S.empty = reinterpret_cast<uint64_t*>(sm + Smem::empty);
+  S.misc = reinterpret_cast<int*>(sm + Smem::misc);
+  S.plist = reinterpret_cast<int*>(sm + Smem::plist);
+  S.out = reinterpret_cast<float*>(sm + out_offset(G));
+  S.comb_items = 0;  // the combine always follows a barrier here: it also normalises
+  uint16_t* perm = reinterpret_cast<uint16_t*>(sm + Smem::perm);
+  uint16_t* inv = reinterpret_cast<uint16_t*>(sm + Smem::inv);
+  float* gw = reinterpret_cast<float*>(sm + Smem::gw);
+  int* s_idx = reinterpret_cast<int*>(sm + Smem::s_idx);
+  S.perm = perm;
+  S.inv = inv;
+  S.gw = gw;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(S.full + s, 1);
+      mbar_init(S.empty + s, NWARPS);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  trace_point(p, 0);
+  pdl_wait();
+  trace_point(p, 1);
+  if ((base.flags & FLAG_TEST_WAIT_TIMEOUT) && blockIdx.x == 0 && threadIdx.x == 0) test_wait_timeout(base.status);
+  int nbar = 0;
+  // the first layer's pre-norm: whole rows per CTA
+  if (prenorm) {
+    if (threadIdx.x < NCONS)
+      for (int t = blockIdx.x; t < T; t += gridDim.x)
+        norm_row(p, t, __ldcg(reinterpret_cast<const uint4*>(p.x + (size_t)t * H) + threadIdx.x), S.out);
+    if (!grid_sync(p, ++nbar, S.misc + 12)) return;
+  }
+  for (int l = 0; l < n_layers; ++l) {
+    const float* bias = tab[l].router_bias;
+    int32_t* out_idx = base.out_idx ? base.out_idx + (size_t)l * T * K : nullptr;
+    float* out_w = base.out_w ? base.out_w + (size_t)l * T * K : nullptr;
+    S.maps = &tab[l].maps;
+    if (threadIdx.x == NCONS) {  // the layer's descriptors are read from device memory by every TMA issue
+      prefetch_tensormap(&S.maps->wr);
+      prefetch_tensormap(&S.maps->wg);
+      prefetch_tensormap(&S.maps->wu);
+      prefetch_tensormap(&S.maps->wd);
+      prefetch_tensormap(&S.maps->wsg);
+      prefetch_tensormap(&S.maps->wsu);
+      prefetch_tensormap(&S.maps->wsd);
+    }
+    // ---- step A: router partial logits
+    {
+      if (threadIdx.x == NCONS + 1) prefetch_share(tab[l].ws_down, uint32_t(IS) * H * 2);
+      BlockList L;
+      L.k_first = L.k_second = KIND_RT;
+      L.kb_first = L.kb_second = 1;
+      L.n_first = L.n_total = ntg * RT_NB;
+      S.first_slot = 11;
+      set_step(S, L);
+      run_step(S);
+    }
+    trace_point(p, 2);
+    if (!grid_sync(p, ++nbar, S.misc + 12)) return;
+    trace_point(p, 3);
+    // ---- step B: routing, then this CTA's permutation tables
+    if (T <= REDUNDANT_ROUTING_MAX_T) {
+      int toks[REDUNDANT_ROUTING_MAX_T];
+      for (int t = 0; t < T; ++t) toks[t] = t;
+      route_tokens(p, bias, out_idx, out_w, sm, toks, T, s_idx, gw, blockIdx.x == 0);
+    } else {
+      int toks[4];
+      int nt = 0;
+      for (int t = blockIdx.x; t < T; t += gridDim.x) {
+        toks[nt++] = t;
+        if (nt == 4) {
+          route_tokens(p, bias, out_idx, out_w, sm, toks, nt, nullptr, nullptr, true);
+          nt = 0;
+        }
+      }
+      if (nt) route_tokens(p, bias, out_idx, out_w, sm, toks, nt, nullptr, nullptr, true);
+      if (!grid_sync(p, ++nbar, S.misc + 12)) return;
+      for (int q = threadIdx.x; q < T * K; q += NTHREADS) {
+        s_idx[q] = __ldcg(p.topk_idx + q);
+        gw[q] = __ldcg(p.topk_w + q);
+      }
+      __syncthreads();
+    }
+    trace_point(p, 4);
+    S.meta = build_tables(p, sm, perm, inv);
+    trace_point(p, 5);
+    // ---- step C: routed gate/up and the shared gate/up
+    {
+      const bf16* w_down = tab[l].w_down;
+      if (threadIdx.x == NCONS + 1 && (unsigned long long)S.meta.U * I * H * 2 <= p.prefetch_bytes_max) {
+        constexpr uint32_t per_e = uint32_t(I) * H * 2;
+        const uint32_t total = per_e * uint32_t(S.meta.U);
+        const uint32_t share = ((total / gridDim.x) + 15u) & ~15u;
+        uint32_t a = share * blockIdx.x;
+        const uint32_t b = a < total ? (total - a > share ? a + share : total) : a;
+        while (a < b) {
+          const int u = int(a / per_e);
+          const uint32_t in_e = a % per_e;
+          uint32_t n = per_e - in_e;
+          if (n > b - a) n = b - a;
+          if (n > 65536u) n = 65536u;
+          prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(w_down + (size_t)S.meta.e[u] * I * H) + in_e,
+                           uint32_t(n));
+          a += n;
+        }
+      }
+      BlockList L;
+      L.k_first = KIND_GU;
+      L.kb_first = GU_KB;
+      L.n_first = S.meta.groups * GU_NCB * GU_KB;
+      L.k_second = KIND_SGU;
+      L.kb_second = GU_KB;
+      L.n_total = L.n_first + ntg * SGU_NCB * GU_KB;
+      S.first_slot = 12;
+      trace_point(p, 6);
+      set_step(S, L);
+      run_step(S);
+    }
+    trace_point(p, 7);
+    // ---- step D (first block issued before the barrier for small calls, as in decode_fused)
+    {
+      BlockList L;
+      L.k_first = KIND_DN;
+      L.kb_first = DN_KB;
+      L.n_first = S.meta.groups * OUT_NCB * DN_KB;
+      L.k_second = KIND_SD;
+      L.kb_second = SD_KB;
+      L.n_total = L.n_first + ntg * OUT_NCB * SD_KB;
+      set_step(S, L);
+    }
+    const int pre = T <= PREISSUE_MAX_T ? min(1, S.nb) : 0;
+    if (threadIdx.x == NCONS) produce(S, 0, pre);
+    if (!grid_sync(p, ++nbar, S.misc + 12)) {
+      drain_issued(S, pre);
+      return;
+    }
+    trace_point(p, 8);
+    S.first_slot = 13;
+    run_step(S, pre);
+    trace_point(p, 9);
+    if (!grid_sync(p, ++nbar, S.misc + 12)) return;
+    trace_point(p, 14);
+    // ---- the combine by whole rows, and the next layer's pre-norm of the same rows
+    const bool norm_next = prenorm && l + 1 < n_layers;
+    if (threadIdx.x < NCONS)
+      for (int t = blockIdx.x; t < T; t += gridDim.x) {
+        const uint4 v = combine8(p, inv, t, threadIdx.x * 8);
+        if (norm_next) norm_row(p, t, v, S.out);
+      }
+    if (l + 1 < n_layers && !grid_sync(p, ++nbar, S.misc + 12)) return;
   }
   grid_done(p, S.misc + 13);
   trace_point(p, 10);

@@ -7,6 +7,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <vector>
 
 #include "../../include/flint_moe.h"
 #include "common.cuh"
@@ -117,6 +118,14 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+struct flint_moe_stack_s {
+  flint_moe_t h;    // handle on layer 0's weights and the shared scratch
+  int n_layers;
+  void* tab;        // device table of LayerTab entries (in the workspace)
+  std::vector<flint_moe_weights> w;  // the layers' weights (per-layer launches)
+  std::vector<StreamMaps> maps;      // host copies of the layers' tensor maps
+};
 
 struct flint_moe_s {
   flint_moe_config cfg;
@@ -237,17 +246,21 @@ cudaError_t launch(flint_moe_t h, const char* name, void (*kern)(KArgs...), unsi
   return e;
 }
 
-// The layer on T <= STREAM_MAX_T tokens: optional RMSNorm kernel, then the persistent
-// cooperative decode kernel (one CTA per SM).
-flint_moe_status run_decode(flint_moe_t h, const Params& p, cudaStream_t st, bool full) {
+// The layer on T <= STREAM_MAX_T tokens (weights described by `maps` and p): optional RMSNorm
+// kernel, then the persistent cooperative decode kernel (one CTA per SM).
+flint_moe_status run_decode_maps(flint_moe_t h, const Params& p, const StreamMaps& maps, cudaStream_t st,
+                                 bool full) {
   cudaError_t e = cudaSuccess;
   if (h->cfg.flags & FLINT_MOE_FLAG_PRE_RMSNORM) e = launch(h, "rmsnorm", rmsnorm_kernel, p.T, 256, 0, st, false, p);
   if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
   const int grid = h->n_sm < MAX_STREAM_CTAS ? h->n_sm : MAX_STREAM_CTAS;
   e = launch(h, full ? "decode_fused" : "decode_fused_route", decode_fused, grid, NTHREADS,
-             fused_smem_bytes(group_rows(p.T)), st, true, p,
-             h->smaps, full ? 0 : 1);
+             fused_smem_bytes(group_rows(p.T)), st, true, p, maps, full ? 0 : 1);
   return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ERR_CUDA;
+}
+
+flint_moe_status run_decode(flint_moe_t h, const Params& p, cudaStream_t st, bool full) {
+  return run_decode_maps(h, p, h->smaps, st, full);
 }
 
 // The layer on T > STREAM_MAX_T tokens: the tensor-core path (prefill_kernels.cuh), five (six
@@ -512,6 +525,145 @@ flint_moe_status flint_moe_destroy(flint_moe_t h) {
   for (int i = 0; i < 2 * MAX_EVENTS; ++i)
     if (h->ev[i]) cudaEventDestroy(h->ev[i]);
   delete h;
+  return FLINT_MOE_OK;
+}
+
+// ---------------------------------------------------------------- the layer stack
+// The stack's workspace: the scratch of one layer with max_tokens tokens (its counters,
+// tables and intermediates serve every layer in turn), then the device table of per-layer
+// tensor maps and weight pointers.
+flint_moe_status flint_moe_stack_workspace_bytes(const flint_moe_config* cfg, int n_layers, size_t* bytes) {
+  flint_moe_status s = check_config(cfg);
+  if (s != FLINT_MOE_OK) return s;
+  if (!bytes || n_layers < 1) return FLINT_MOE_ERR_INVALID_ARG;
+  if (cfg->max_tokens > STREAM_MAX_T) return FLINT_MOE_ERR_UNSUPPORTED;
+  *bytes = align_up(make_layout(cfg->max_tokens).total, 256) + align_up(sizeof(LayerTab) * n_layers, 256);
+  return FLINT_MOE_OK;
+}
+
+flint_moe_status flint_moe_stack_create(const flint_moe_config* cfg, const flint_moe_weights* layers, int n_layers,
+                                        void* workspace, size_t workspace_bytes, flint_moe_stack_t* out) {
+  if (!out) return FLINT_MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  size_t need = 0;
+  flint_moe_status s = flint_moe_stack_workspace_bytes(cfg, n_layers, &need);
+  if (s != FLINT_MOE_OK) return s;
+  if (!layers) return FLINT_MOE_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return FLINT_MOE_ERR_WORKSPACE;
+  for (int l = 0; l < n_layers; ++l) {
+    const flint_moe_weights* w = &layers[l];
+    if (!w->w_router || !w->w_gate || !w->w_up || !w->w_down || !w->ws_gate || !w->ws_up || !w->ws_down)
+      return FLINT_MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {w->w_router, w->w_gate, w->w_up, w->w_down, w->ws_gate, w->ws_up, w->ws_down};
+    for (const void* q : ptrs)
+      if (!aligned16(q)) return FLINT_MOE_ERR_INVALID_ARG;
+    if (w->router_bias && (reinterpret_cast<uintptr_t>(w->router_bias) & 3u)) return FLINT_MOE_ERR_INVALID_ARG;
+  }
+  const size_t scratch = align_up(make_layout(cfg->max_tokens).total, 256);
+  flint_moe_t h = nullptr;
+  s = flint_moe_create(cfg, &layers[0], workspace, scratch, &h);
+  if (s != FLINT_MOE_OK) return s;
+  std::vector<LayerTab> tab(n_layers);
+  const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  bool ok = true;
+  for (int l = 0; l < n_layers && ok; ++l) {
+    const flint_moe_weights* w = &layers[l];
+    LayerTab& t = tab[l];
+    std::memset(&t, 0, sizeof t);
+    ok = make_map(&t.maps.wr, w->w_router, H, E, 64, RT_ROWS, sw) &&
+         make_map(&t.maps.wg, w->w_gate, (uint64_t)E * H, I, 64, GU_ROWS, sw) &&
+         make_map(&t.maps.wu, w->w_up, (uint64_t)E * H, I, 64, GU_ROWS, sw) &&
+         make_map(&t.maps.wd, w->w_down, (uint64_t)E * I, H, 64, DN_ROWS, sw) &&
+         make_map(&t.maps.wsg, w->ws_gate, H, IS, 64, GU_ROWS, sw) &&
+         make_map(&t.maps.wsu, w->ws_up, H, IS, 64, GU_ROWS, sw) &&
+         make_map(&t.maps.wsd, w->ws_down, IS, H, 64, DN_ROWS, sw);
+    t.router_bias = w->router_bias;
+    t.w_down = static_cast<const bf16*>(w->w_down);
+    t.ws_down = static_cast<const bf16*>(w->ws_down);
+  }
+  LayerTab* dtab = reinterpret_cast<LayerTab*>(static_cast<uint8_t*>(workspace) + scratch);
+  cudaError_t e = ok ? cudaSuccess : cudaErrorInvalidValue;
+  if (e == cudaSuccess) e = cudaMemcpy(dtab, tab.data(), sizeof(LayerTab) * n_layers, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_stack, cudaFuncAttributeMaxDynamicSharedMemorySize, FUSED_SMEM);
+  int per_sm = 0;
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stack, NTHREADS, FUSED_SMEM);
+  if (e == cudaSuccess && per_sm < 1) e = cudaErrorCooperativeLaunchTooLarge;
+  flint_moe_stack_s* st = e == cudaSuccess ? new (std::nothrow) flint_moe_stack_s() : nullptr;
+  if (!st) {
+    flint_moe_destroy(h);
+    return FLINT_MOE_ERR_CUDA;
+  }
+  st->h = h;
+  st->n_layers = n_layers;
+  st->tab = dtab;
+  st->w.assign(layers, layers + n_layers);
+  st->maps.resize(n_layers);
+  for (int l = 0; l < n_layers; ++l) st->maps[l] = tab[l].maps;
+  *out = st;
+  return FLINT_MOE_OK;
+}
+
+flint_moe_status flint_moe_stack_forward(flint_moe_stack_t st, void* x, int T, int32_t* topk_idx, float* topk_w,
+                                         flint_stream_t stream) {
+  if (!st) return FLINT_MOE_ERR_INVALID_ARG;
+  flint_moe_t h = st->h;
+  flint_moe_status s = check_call(h, x, T);
+  if (s != FLINT_MOE_OK) return s;
+  h->n_ev = 0;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (T > STACK_ONE_LAUNCH_MAX_T) {
+    // per-layer launches of the single-layer path (measured faster at these sizes)
+    for (int l = 0; l < st->n_layers; ++l) {
+      const flint_moe_weights& w = st->w[l];
+      Params p = make_params(h, x, T, x, topk_idx ? topk_idx + (size_t)l * T * K : nullptr,
+                             topk_w ? topk_w + (size_t)l * T * K : nullptr, nullptr);
+      p.w_router = static_cast<const bf16*>(w.w_router);
+      p.router_bias = w.router_bias;
+      p.w_gate = static_cast<const bf16*>(w.w_gate);
+      p.w_up = static_cast<const bf16*>(w.w_up);
+      p.w_down = static_cast<const bf16*>(w.w_down);
+      p.ws_gate = static_cast<const bf16*>(w.ws_gate);
+      p.ws_up = static_cast<const bf16*>(w.ws_up);
+      p.ws_down = static_cast<const bf16*>(w.ws_down);
+      if (p.trace && cudaMemsetAsync(p.trace, 0, sizeof(unsigned long long) * MAX_TRACE_CTAS * TRACE_SLOTS, cs) !=
+                         cudaSuccess)
+        return FLINT_MOE_ERR_CUDA;
+      const flint_moe_status r = run_decode_maps(h, p, st->maps[l], cs, true);
+      if (r != FLINT_MOE_OK) return r;
+    }
+    return FLINT_MOE_OK;
+  }
+  Params p = make_params(h, x, T, x, topk_idx, topk_w, nullptr);
+  if (p.trace && cudaMemsetAsync(p.trace, 0, sizeof(unsigned long long) * MAX_TRACE_CTAS * TRACE_SLOTS, cs) !=
+                     cudaSuccess)
+    return FLINT_MOE_ERR_CUDA;
+  const int grid = h->n_sm < MAX_STREAM_CTAS ? h->n_sm : MAX_STREAM_CTAS;
+  const cudaError_t e = launch(h, "decode_stack", decode_stack, grid, NTHREADS, fused_smem_bytes(group_rows(T)),
+                               reinterpret_cast<cudaStream_t>(stream), true, p,
+                               static_cast<const LayerTab*>(st->tab), st->n_layers);
+  return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ERR_CUDA;
+}
+
+flint_moe_status flint_moe_stack_poll_device_status(flint_moe_stack_t st, flint_stream_t stream) {
+  if (!st) return FLINT_MOE_ERR_INVALID_ARG;
+  return flint_moe_poll_device_status(st->h, stream);
+}
+
+flint_moe_status flint_moe_stack_enable_kernel_timing(flint_moe_stack_t st, int enable) {
+  if (!st) return FLINT_MOE_ERR_INVALID_ARG;
+  return flint_moe_enable_kernel_timing(st->h, enable);
+}
+
+flint_moe_status flint_moe_stack_read_trace(flint_moe_stack_t st, unsigned long long* out, int cap, int* n) {
+  if (!st) return FLINT_MOE_ERR_INVALID_ARG;
+  return flint_moe_read_trace(st->h, out, cap, n);
+}
+
+flint_moe_status flint_moe_stack_destroy(flint_moe_stack_t st) {
+  if (!st) return FLINT_MOE_ERR_INVALID_ARG;
+  flint_moe_destroy(st->h);
+  delete st;
   return FLINT_MOE_OK;
 }
 

@@ -74,3 +74,25 @@ def test_create_rejects_missing_workspace_before_touching_a_device():
     assert lib.flint_moe_create(ctypes.byref(cfg), ctypes.byref(w), None, 0, ctypes.byref(h)) == 3
     w_bad = fm._Weights(*([258] * 8))  # misaligned
     assert lib.flint_moe_create(ctypes.byref(cfg), ctypes.byref(w_bad), None, 0, ctypes.byref(h)) == 1
+
+
+def test_stack_workspace_and_argument_checks():
+    lib = fm.load_library()
+    flags = fm.FLAG_PRE_RMSNORM | fm.FLAG_RESIDUAL
+    one = fm.stack_workspace_bytes(1, 256, flags)
+    many = fm.stack_workspace_bytes(47, 256, flags)
+    assert one % 256 == 0 and many > one and many - one < 47 * 2048  # a table entry per layer
+    cfg = fm._Config(2048, 256, 6, 512, 1024, 256, flags, 1e-6)
+    out = ctypes.c_size_t(0)
+    assert lib.flint_moe_stack_workspace_bytes(ctypes.byref(cfg), 0, ctypes.byref(out)) == 1  # no layers
+    big = fm._Config(2048, 256, 6, 512, 1024, 512, flags, 1e-6)
+    assert lib.flint_moe_stack_workspace_bytes(ctypes.byref(big), 4, ctypes.byref(out)) == 2  # decode sizes only
+    arr = (fm._Weights * 2)(fm._Weights(*([256] * 8)), fm._Weights(*([256] * 8)))
+    h = ctypes.c_void_p()
+    assert lib.flint_moe_stack_create(ctypes.byref(cfg), arr, 2, None, 0, ctypes.byref(h)) == 3
+    arr[1] = fm._Weights(*([258] * 8))  # misaligned second layer
+    assert lib.flint_moe_stack_create(ctypes.byref(cfg), arr, 2, ctypes.c_void_p(256), 1 << 40,
+                                      ctypes.byref(h)) == 1
+    assert lib.flint_moe_stack_forward(None, None, 1, None, None, None) == 1
+    assert lib.flint_moe_stack_poll_device_status(None, None) == 1
+    assert lib.flint_moe_stack_destroy(None) == 1

@@ -3,7 +3,8 @@ seed 100 + l, about 76 GB resident), checked layer by layer with teacher forcing
 layer l takes the GPU's bf16 input to layer l, on sampled layers 0, 23 and 46 -- all 256 tokens
 for routing, a spread sample of tokens for outputs.  A routing flip in an early layer would make
 an end-to-end comparison meaningless, so the end-to-end output is only checked to be finite and
-bitwise deterministic."""
+bitwise deterministic, and the stack handle (one launch at 16 tokens) must reproduce the per-layer
+results bitwise."""
 import numpy as np
 import pytest
 import torch
@@ -59,3 +60,23 @@ def test_stack_47_layers_teacher_forced_parity():
         assert rep["ok"], (l, rep)
     for lay in layers:
         lay.close()
+    # the stack handle: bitwise the per-layer result, at T = 256 (per-layer launches) and, through
+    # all 47 layers in one launch, at 16 tokens
+    stack = fm.FlintMoEStack(weights, max_tokens=T, flags=flags, rms_eps=EPS)
+    x = x0.clone()
+    stack.forward(x)
+    torch.cuda.synchronize()
+    assert stack.poll_device_status() == 0
+    assert torch.equal(x.view(torch.int16), y2.view(torch.int16))
+    xs = x0[:16].clone()
+    stack.forward(xs)
+    small = [fm.FlintMoE(weights[l], max_tokens=16, flags=flags, rms_eps=EPS) for l in range(L)]
+    xr = x0[:16].clone()
+    for lay in small:
+        lay.forward(xr, y=xr)
+    torch.cuda.synchronize()
+    assert stack.poll_device_status() == 0
+    assert torch.equal(xs.view(torch.int16), xr.view(torch.int16))
+    for lay in small:
+        lay.close()
+    stack.close()
