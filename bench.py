@@ -83,6 +83,27 @@ def measured_traffic(kernel, sweep):
     return round(sum(per[str(T)] for T in sweep) / len(sweep))
 
 
+# The stack call runs every layer in one launch up to this many tokens (decode_fused.cuh,
+# STACK_ONE_LAUNCH_MAX_T).
+STACK_ONE_LAUNCH_MAX_T = 16
+
+
+def measured_stack_traffic(T, n_layers):
+    """DRAM bytes of one launch of decode_stack over n_layers at T tokens: the committed ncu
+    summary profiles/decode_stack_traffic.json holds a small stack's bytes per layer (the
+    weights of each layer are streamed once, so the bytes scale with the layers); None when the
+    sources changed since or the summary has no entry for T."""
+    path = os.path.join(ROOT, "profiles", "decode_stack_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("sources_sha256") != kernel_sources_sha256():
+        return None
+    per = rec.get("dram_bytes_per_layer", {}).get(str(T))
+    return None if per is None else round(per * n_layers)
+
+
 # The B300's nominal HBM3e bandwidth and dense bf16 rate, for the "spec" fractions next to the
 # measured ones.
 SPEC_HBM_GBS = 8000.0
@@ -473,14 +494,17 @@ def run_workload(args, rank, world, local):
 
 def run_stack(args, rank, world, local):
     """47 Flint MoE layers (weights seed 100+l, about 76 GB), T=256 tokens (x seed 4); each
-    layer x <- x + MoE_l(RMSNorm(x)), eps 1e-6.  One step = the 47 forwards."""
+    layer x <- x + MoE_l(RMSNorm(x)), eps 1e-6.  One step = the 47 forwards, through the stack
+    call.  --stack-tokens T measures the same stack at T tokens (up to 16: one launch for all
+    layers); --stack-layers N < 47 is a small case for the profiler, not the configuration."""
     import torch
 
     import synth
     import sparse_moe_layer_15_b300 as fm
     from sparse_moe_layer_15_b300 import accounting as acc
 
-    L, T = acc.N_MOE_LAYERS, 256
+    L, T = args.stack_layers, args.stack_tokens
+    one_launch = T <= STACK_ONE_LAUNCH_MAX_T
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     peaks = load_peaks()
@@ -489,8 +513,8 @@ def run_stack(args, rank, world, local):
     ws = torch.empty(fm.workspace_bytes(T, flags, 1e-6), dtype=torch.uint8, device=dev)
     weights = [synth.flint_weights(seed=100 + l, device=dev) for l in range(L)]
     layers = [fm.FlintMoE(weights[l], max_tokens=T, flags=flags, rms_eps=1e-6, workspace=ws) for l in range(L)]
-    # the public stack call (at T = 256 it launches the pre-norm and decode kernels layer by layer:
-    # measured faster than its one-launch kernel at this size)
+    # the public stack call (up to 16 tokens one launch of decode_stack for all layers; above, the
+    # pre-norm and decode kernels layer by layer: measured faster than the one-launch kernel there)
     stack_handle = fm.FlintMoEStack(weights, max_tokens=T, flags=flags, rms_eps=1e-6)
     x0 = synth.torch_normal_bf16((T, fm.HIDDEN), 4, synth.TAG_X, 1.0, device=dev)
     x = x0.clone()
@@ -530,10 +554,20 @@ def run_stack(args, rank, world, local):
     alg_bytes = sum(acc.algorithmic_bytes(u, T) for u in U)
     flop = acc.flops_per_token() * T * L
     achieved = alg_bytes / (ms * 1e-3) / 1e9
-    roofline = dict(bound="hbm", kernel="decode_fused (x47, + rmsnorm)", achieved=round(achieved, 1),
-                    peak=peaks["hbm_gbs"], unit="GB/s", frac=round(achieved / peaks["hbm_gbs"], 4), traffic=None,
-                    alg_bytes_per_launch=round(alg_bytes / L), peak_source=peaks["source"] + " (hbm_gbs, copy test)",
-                    note="the whole step; the decode kernel is 47 of the 94 launches and nearly all the time")
+    if one_launch:
+        roofline = dict(bound="hbm", kernel=f"decode_stack (one launch, {L} layers)", achieved=round(achieved, 1),
+                        peak=peaks["hbm_gbs"], unit="GB/s", frac=round(achieved / peaks["hbm_gbs"], 4),
+                        traffic=measured_stack_traffic(T, L), alg_bytes_per_launch=round(alg_bytes),
+                        peak_source=peaks["source"] + " (hbm_gbs, copy test)",
+                        note="the step is one launch; traffic: DRAM bytes per layer from the committed ncu "
+                             "summary of a small stack, times the layers (null if the sources changed)")
+    else:
+        roofline = dict(bound="hbm", kernel=f"decode_fused (x{L}, + rmsnorm)", achieved=round(achieved, 1),
+                        peak=peaks["hbm_gbs"], unit="GB/s", frac=round(achieved / peaks["hbm_gbs"], 4), traffic=None,
+                        alg_bytes_per_launch=round(alg_bytes / L),
+                        peak_source=peaks["source"] + " (hbm_gbs, copy test)",
+                        note=f"the whole step; the decode kernel is {L} of the {2 * L} launches and nearly all the "
+                             "time")
     xh = x0.cpu().pin_memory()
     yh = torch.empty_like(xh).pin_memory()
 
@@ -547,18 +581,19 @@ def run_stack(args, rank, world, local):
     out = dict(metric=METRIC, value=round(world * T / (ms * 1e-3), 1), unit="tokens/s", n_gpus=world,
                steps=args.steps, warmup=args.warmup, ms_per_step=round(ms, 4), higher_is_better=True, scaling="weak",
                vs_baseline=None, dtype="bf16", data="synthetic",
-               config=dict(workload="stack: 47 Flint MoE layers (pre-norm RMSNorm eps 1e-6, residual), T=256, "
-                                    "weights seed 100+l (76 GB resident), x seed 4",
+               config=dict(workload=f"stack: {L} Flint MoE layers (pre-norm RMSNorm eps 1e-6, residual), T={T}, "
+                                    f"weights seed 100+l ({L * 1.62:.0f} GB resident), x seed 4"
+                                    + ("" if L == acc.N_MOE_LAYERS else " (a small profiling case)"),
                            tokens_per_step=T, parallelism=f"replicas x{world}",
-                           l2="inputs larger than L2 (76 GB of weights streamed per step)"),
+                           l2=f"inputs larger than L2 ({alg_bytes / 1e9:.1f} GB of touched weights streamed per step)"),
                layer=dict(touched_experts_per_layer=U, alg_bytes=alg_bytes, alg_flop=flop,
                           gbs=round(achieved, 1), roofline_ms=round(alg_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3, 3)),
                roofline=roofline,
                e2e=dict(value=round(world * T / (e2e_ms * 1e-3), 1), unit="tokens/s",
                         h2d_bytes_per_step=2 * fm.HIDDEN * T, d2h_bytes_per_step=2 * fm.HIDDEN * T),
-               gpu_launches=args.steps * 2 * L, clocks=clk)
+               gpu_launches=args.steps * (1 if one_launch else 2 * L), clocks=clk)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline_tokens(weights[0], x0, n=8, what="stack layer 0", eps=1e-6)
+        out["cpu_baseline"] = cpu_baseline_tokens(weights[0], x0, n=min(8, T), what="stack layer 0", eps=1e-6)
     for lay in layers:
         lay.close()
     stack_handle.close()
@@ -733,6 +768,9 @@ def main():
                     help="with --profile: print the decode kernel's phase trace (T <= 256) or the grouped GEMMs' "
                          "wait profile (T > 256)")
     ap.add_argument("--workload", default="decode", choices=["decode", "single", "prefill", "adversarial", "stack"])
+    ap.add_argument("--stack-tokens", type=int, default=256, help="stack workload: tokens per step (1..256)")
+    ap.add_argument("--stack-layers", type=int, default=47,
+                    help="stack workload: layers (fewer than 47 only as a small profiling case)")
     args = ap.parse_args()
     if args.profile:
         run_profile_case(args)
