@@ -74,6 +74,22 @@ def test_ragged_and_max_stream_sizes(w0, layer0, T):
     assert_parity(parity.compare(ref, y, idx, gw))
 
 
+@pytest.mark.parametrize("T", [2, 4, 16])
+def test_identical_tokens_share_experts(w0, layer0, T):
+    """One input row repeated T times: every token picks the same six experts.  At T = 2 and 4
+    that leaves fewer down items than CTAs, so each 128-column block is combined by the CTA that
+    finishes its last down item (the path T = 1 takes otherwise); at T = 16 the experts hold two
+    8-row groups each.  Up to 8 tokens all rows sit in one group and go through the same
+    arithmetic, so the output rows are bitwise equal."""
+    x = x_rows(1, 4242).repeat(T, 1).contiguous()
+    y, idx, gw = run_forward(layer0, x)
+    assert (idx == idx[0]).all() and (gw == gw[0]).all()
+    ref = parity.oracle_reference(w0, x, range(T))
+    assert_parity(parity.compare(ref, y, idx, gw))
+    if T <= 8:
+        assert (y.view(torch.int16) == y[0].view(torch.int16)).all()
+
+
 def test_route_matches_forward_routing_and_counts(w0, layer0):
     x = x_rows(64, 5)
     y, idx, gw = run_forward(layer0, x)
