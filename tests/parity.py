@@ -4,14 +4,19 @@ Routing: on every token whose oracle gap between the 6th and 7th score exceeds 1
 must choose the same expert set; inside the chosen list, the GPU order must equal the oracle
 order across every adjacent pair whose oracle gap exceeds 1e-4, and every exactly tied pair
 (equal fp64 scores) must keep its relative order, lower index first.  Tokens at or below the gap are exempt:
-their fp32 scores may legitimately pick the other near-tied expert; the oracle then
-re-evaluates them with the GPU's choice (gates = its fp64 scores renormalised).
+their fp32 scores may legitimately pick the other near-tied expert, but only a near-tied one:
+the GPU's list must hold 6 distinct experts, every chosen expert must score within the gap of
+every expert left out (min over the chosen >= max over the rest - 1e-4, oracle fp64 scores),
+and the list must descend in score up to the gap.  The oracle then re-evaluates such a token
+with the GPU's choice (gates = its fp64 scores renormalised).
 
 Outputs (bf16): max |y_gpu - y_ref| <= 2e-2 * max |y_ref| and
 sum |y_gpu - y_ref| / sum |y_ref| <= 5e-3 (relative L1).
 Gates: |g_gpu - g_ref| <= 2e-5 per chosen expert, and the GPU's gates sum to 1 within 1e-5.
 """
 from __future__ import annotations
+
+import os
 
 import numpy as np
 
@@ -22,6 +27,8 @@ GAP = 1e-4
 MAX_ABS_REL = 2e-2
 REL_L1 = 5e-3
 GATE_TOL = 2e-5
+# threads for full-batch oracle references (each token is the same single-threaded computation)
+ORACLE_THREADS = max(1, min(os.cpu_count() or 8, 64))
 
 
 def tie_broken_wrong(idx_g, idx_r, gaps):
@@ -35,6 +42,46 @@ def tie_broken_wrong(idx_g, idx_r, gaps):
             if a in pos and b in pos and pos[a] > pos[b]:
                 return True
     return False
+
+
+def near_tie_choice_valid(idx_g, s):
+    """The GPU's expert list ``idx_g`` for one exempt token is a top-k of the oracle's fp64
+    scores ``s`` [E] perturbed by less than the gap: distinct experts in range, every chosen
+    expert scoring no less than every expert left out minus GAP (so an expert the GPU took in
+    is near the oracle's k-th score, and an oracle expert it dropped is near the (k+1)-th),
+    and the list descending in score up to GAP."""
+    E = s.shape[0]
+    g = [int(e) for e in idx_g]
+    if len(set(g)) != len(g) or any(e < 0 or e >= E for e in g):
+        return False
+    chosen = np.zeros(E, bool)
+    chosen[g] = True
+    if chosen.all():
+        return True
+    if s[chosen].min() < s[~chosen].max() - GAP:
+        return False
+    return all(s[g[j]] >= s[g[j + 1]] - GAP for j in range(len(g) - 1))
+
+
+def routing_verdict(idx_g, idx_r, gaps, s):
+    """The routing rule on one token: "ok", "set" (a non-exempt token chose another set),
+    "near_tie" (an exempt token's other choice is not a near-tied one), "order" (a segment
+    of the ranking between gaps > GAP holds other experts) or "tie" (an exact tie in the
+    wrong order).  ``s``: the oracle's fp64 scores of the token (all experts)."""
+    same = set(int(e) for e in idx_g) == set(int(e) for e in idx_r)
+    if not same:
+        if gaps[5] > GAP:
+            return "set"
+        return "ok" if near_tie_choice_valid(idx_g, s) else "near_tie"
+    a = 0
+    for j in range(6):
+        if j == 5 or gaps[j] > GAP:
+            if set(int(e) for e in idx_g[a:j + 1]) != set(int(e) for e in idx_r[a:j + 1]):
+                return "order"
+            a = j + 1
+    if tie_broken_wrong(idx_g, idx_r, gaps):
+        return "tie"
+    return "ok"
 
 
 def to_np_bf16(t):
@@ -63,7 +110,7 @@ def touched_experts(w, xin64, tokens):
     return sorted(need)
 
 
-def oracle_reference(w, x, tokens, xin64=None, nthreads=8, residual=False, eps=None):
+def oracle_reference(w, x, tokens, xin64=None, nthreads=ORACLE_THREADS, residual=False, eps=None):
     """Oracle outputs for the token rows ``tokens`` of x (bf16 torch tensor).  With ``eps``
     the layer is pre-normed (x' = rms(x)) and, with ``residual``, y = x + MoE(x')."""
     x64 = oracle.bf16_to_f64(to_np_bf16(x))
@@ -92,24 +139,17 @@ def compare(ref, y, idx, gw, counts=None, full_T=None):
     exempt = gaps[:, 5] <= GAP
     set_mismatch, order_err, tie_err = [], [], []
     for i in range(n):
-        same_set = set(idx_g[i].tolist()) == set(idx_r[i].tolist())
-        if not same_set:
-            if not exempt[i]:
-                set_mismatch.append(int(tokens[i]))
-            continue
-        # segments of the ranked list separated by gaps > GAP must hold the same experts
-        a = 0
-        for j in range(6):
-            if j == 5 or gaps[i, j] > GAP:
-                if set(idx_g[i, a:j + 1].tolist()) != set(idx_r[i, a:j + 1].tolist()):
-                    order_err.append(int(tokens[i]))
-                    break
-                a = j + 1
-        if tie_broken_wrong(idx_g[i], idx_r[i], gaps[i]):
+        v = routing_verdict(idx_g[i], idx_r[i], gaps[i], s_r[i])
+        if v in ("set", "near_tie"):
+            set_mismatch.append(int(tokens[i]))
+        elif v == "order":
+            order_err.append(int(tokens[i]))
+        elif v == "tie":
             tie_err.append(int(tokens[i]))
     # re-evaluate exempt tokens whose set differs, with the GPU's choice
     y_ref = ref["y"].copy()
-    reeval = [i for i in range(n) if set(idx_g[i].tolist()) != set(idx_r[i].tolist()) and exempt[i]]
+    reeval = [i for i in range(n) if set(idx_g[i].tolist()) != set(idx_r[i].tolist()) and exempt[i]
+              and int(tokens[i]) not in set_mismatch]
     missing = []
     if reeval:
         try:
@@ -159,23 +199,18 @@ def check_routing_all(w, x, idx_gpu, gw_gpu, eps=None):
     set_mm, order_err, tie_err = [], [], []
     gate_err = 0.0
     for t in range(idx_r.shape[0]):
-        same = set(idx_g[t].tolist()) == set(idx_r[t].tolist())
-        if not same:
-            if not exempt[t]:
-                set_mm.append(t)
+        v = routing_verdict(idx_g[t], idx_r[t], gaps[t], s[t])
+        if v in ("set", "near_tie"):
+            set_mm.append(t)
             continue
-        a = 0
-        for j in range(6):
-            if j == 5 or gaps[t, j] > GAP:
-                if set(idx_g[t, a:j + 1].tolist()) != set(idx_r[t, a:j + 1].tolist()):
-                    order_err.append(t)
-                    break
-                a = j + 1
-        if tie_broken_wrong(idx_g[t], idx_r[t], gaps[t]):
+        if v == "order":
+            order_err.append(t)
+        elif v == "tie":
             tie_err.append(t)
-        sg = dict(zip(idx_g[t].tolist(), w_g[t].tolist()))
-        for e, g in zip(idx_r[t].tolist(), g_r[t].tolist()):
-            gate_err = max(gate_err, abs(sg[e] - g))
+        # gates against the oracle's fp64 scores of the experts the GPU chose
+        sc = s[t, idx_g[t]]
+        for g, ref in zip(w_g[t].tolist(), (sc / sc.sum()).tolist()):
+            gate_err = max(gate_err, abs(g - ref))
     rep = dict(n=int(idx_r.shape[0]), n_exempt=int(exempt.sum()), set_mismatch=set_mm[:10], n_set_mismatch=len(set_mm),
                order_err=order_err[:10], tie_err=tie_err[:10], gate_err=gate_err,
                oracle_counts=np.bincount(idx_r.reshape(-1), minlength=256), exempt_any=bool(exempt.any()))

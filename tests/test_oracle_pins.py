@@ -282,6 +282,84 @@ def test_forward_given_equals_forward_on_its_own_choice():
     np.testing.assert_array_equal(out["y"], y2)
 
 
+def brute_force_given(p, x, chosen):
+    """Dense evaluation of every expert masked by a GIVEN expert set per row (``chosen``
+    [T, k]), the gates being the fp64 sigmoid scores of that set normalised over it.  numpy
+    only; shares no code with the C oracle."""
+    Wr, Wg, Wu, Wd = f64(p["Wr"]), f64(p["Wg"]), f64(p["Wu"]), f64(p["Wd"])
+    Wsg, Wsu, Wsd = f64(p["Wsg"]), f64(p["Wsu"]), f64(p["Wsd"])
+    E = Wr.shape[1]
+    b = np.zeros(E) if p["b"] is None else p["b"].astype(np.float64)
+    s = expit(x @ Wr + b)
+    mask = np.zeros_like(s)
+    np.put_along_axis(mask, np.asarray(chosen, dtype=np.int64), 1.0, axis=1)
+    w = mask * s
+    w = w / w.sum(axis=1, keepdims=True)
+
+    def mlp(a, g, u, d):
+        zg = a @ g
+        return (zg * expit(zg) * (a @ u)) @ d
+
+    y = mlp(x, Wsg, Wsu, Wsd)
+    for e in range(E):
+        y = y + w[:, e : e + 1] * mlp(x, Wg[e], Wu[e], Wd[e])
+    return y
+
+
+def non_top_sets(s, k, rng):
+    """Per row, two sets that are NOT the top-k: ranks 2..k+1 of the (score desc, index asc)
+    order (the best expert dropped, the (k+1)-th taken in), and a random k-subset, each listed
+    in a scrambled order (the result must not depend on the listing order)."""
+    E = s.shape[1]
+    order = np.lexsort((np.broadcast_to(np.arange(E), s.shape), -s), axis=1)
+    shifted = order[:, 1 : k + 1].copy()
+    rand = np.stack([rng.choice(E, size=k, replace=False) for _ in range(s.shape[0])])
+    for row in shifted:
+        rng.shuffle(row)
+    return shifted.astype(np.int32), rand.astype(np.int32), order[:, :k]
+
+
+def test_forward_given_matches_bruteforce_on_sets_that_are_not_the_top_k():
+    # A re-evaluation that ignored the given set (re-selecting the top-k), or normalised the
+    # gates over the wrong experts (all, or the true top-k), fails here: the given sets are
+    # never the top-k.
+    rng = np.random.default_rng(21)
+    p = tiny_layer(seed=13, E=16, k=4, bias=True)
+    x = x_rows(12, 64, seed=14)
+    _, s = oracle.router(x, p["Wr"], p["b"])
+    shifted, rand, top = non_top_sets(s, 4, rng)
+    L = to_layer(p)
+    for given in (shifted, rand):
+        assert all(set(g.tolist()) != set(t.tolist()) for g, t in zip(given, top))
+        y = oracle.forward_given(L, x, given)
+        np.testing.assert_allclose(y, brute_force_given(p, x, given), rtol=1e-11, atol=1e-12)
+        assert np.max(np.abs(y - oracle.forward(L, x)["y"])) > 1e-3
+
+
+def test_forward_given_matches_bruteforce_real_widths():
+    # Real hidden / expert / shared widths and k = 6, 16 experts, a given set of ranks 2..7.
+    rng = np.random.default_rng(22)
+    p = tiny_layer(seed=14, H=2048, E=16, k=6, I=512, Is=1024, bias=True)
+    p["Wg"] = bf16((16, 2048, 512), 14, synth.TAG_GATE, 0.02)
+    p["Wu"] = bf16((16, 2048, 512), 14, synth.TAG_UP, 0.02)
+    p["Wd"] = bf16((16, 512, 2048), 14, synth.TAG_DOWN, 0.02)
+    p["Wsg"] = bf16((2048, 1024), 14, synth.TAG_SGATE, 0.02)
+    p["Wsu"] = bf16((2048, 1024), 14, synth.TAG_SUP, 0.02)
+    p["Wsd"] = bf16((1024, 2048), 14, synth.TAG_SDOWN, 0.02)
+    x = x_rows(3, 2048, seed=15)
+    _, s = oracle.router(x, p["Wr"], p["b"])
+    shifted, _, _ = non_top_sets(s, 6, rng)
+    y = oracle.forward_given(to_layer(p), x, shifted)
+    np.testing.assert_allclose(y, brute_force_given(p, x, shifted), rtol=1e-10, atol=1e-12)
+
+
+def test_forward_given_rejects_out_of_range_experts():
+    p = tiny_layer(seed=15)
+    x = x_rows(1, 64)
+    with pytest.raises(RuntimeError):
+        oracle.forward_given(to_layer(p), x, np.array([[0, 1, 2, 16]], np.int32))
+
+
 def test_missing_expert_is_reported():
     p = tiny_layer(seed=10)
     L = oracle.Layer(p["Wr"], {0: p["Wg"][0]}, {0: p["Wu"][0]}, {0: p["Wd"][0]}, p["Wsg"], p["Wsu"], p["Wsd"], k=4)
