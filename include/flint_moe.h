@@ -105,7 +105,10 @@ flint_moe_status flint_moe_workspace_bytes(const flint_moe_config* cfg, size_t* 
 flint_moe_status flint_moe_create(const flint_moe_config* cfg, const flint_moe_weights* w,
                                   void* workspace, size_t workspace_bytes, flint_moe_t* out);
 
-/* Router scoring, normalised top-k and the expert permutation only.
+/* Router scoring, normalised top-k and the expert permutation only (serving-kit post, section
+ * "The architecture, from the config": sigmoid router scoring with normalised top-k, 6 of 256
+ * routed experts per token; the per-expert counts and the expert-sorted order are this
+ * library's layout of the routed work).
  *   x        bf16 [T][hidden] (the layer input; with PRE_RMSNORM the routing uses rms(x))
  *   topk_idx int32 [T][top_k]: chosen experts, score descending, lower index first on ties
  *   topk_w   fp32 [T][top_k]: their normalised gates
@@ -114,7 +117,10 @@ flint_moe_status flint_moe_create(const flint_moe_config* cfg, const flint_moe_w
 flint_moe_status flint_moe_route(flint_moe_t h, const void* x, int T, int32_t* topk_idx,
                                  float* topk_w, int32_t* counts, flint_stream_t stream);
 
-/* The whole layer: y bf16 [T][hidden] = shared(x') + sum_j g_j E_{e_j}(x') with x' = x, or
+/* The whole layer (serving-kit post, section "The architecture, from the config"; news article
+ * "Recursive opens Flint, a 40B coding model with 2.5B active", section "What runs on each
+ * token": the six chosen experts of width 512 plus one always-on shared expert of width 1024):
+ * y bf16 [T][hidden] = shared(x') + sum_j g_j E_{e_j}(x') with x' = x, or
  * rms(x) under PRE_RMSNORM; plus x under RESIDUAL (then y may alias x).  topk_idx / topk_w
  * (same layout as flint_moe_route) receive the routing when not NULL.  1 <= T <= max_tokens. */
 flint_moe_status flint_moe_forward(flint_moe_t h, const void* x, int T, void* y,
@@ -158,12 +164,24 @@ flint_moe_status flint_moe_destroy(flint_moe_t h);
  * Scratch memory comes from one fixed array of 17 MiB that the library declares in device
  * memory; every GPU that loads the library holds it until the process exits.  The call makes
  * no allocation.  The first call on a device (with that device current) looks up the array's
- * device address and sets the kernel's shared-memory limit; make that first call before any
- * stream capture.  All calls on a device share the array, and it keeps the last call's
- * contents: the counters that must start at zero are cleared on `stream` at the start of each
- * call, and calls whose work overlaps on the GPU race on the array. */
+ * device address, sets the kernel's shared-memory limit, checks that one CTA fits on every SM
+ * and clears the array's status word (synchronously); make that first call before any stream
+ * capture.  The address is kept for the life of the process: after cudaDeviceReset (or any
+ * other destruction of the device's primary context) do not call these entry points on that
+ * device again.  All calls on a device share the array, and it keeps the last call's contents:
+ * the barrier counters and tickets, which must start at zero, are cleared on `stream` at the
+ * start of each call, and calls whose work overlaps on the GPU race on the array.  Device
+ * errors (a bounded wait that ran out, an index out of range) are recorded in the array's
+ * status word and stay there until flint_moe_noalloc_poll_device_status reads them. */
 flint_moe_status flint_moe_forward_noalloc(const flint_moe_weights* w, const void* x, int T, void* y,
                                            int32_t* topk_idx, float* topk_w, flint_stream_t stream);
+
+/* Synchronises `stream`, then returns and clears the status word of the current device's
+ * fixed scratch array (FLINT_MOE_OK, FLINT_MOE_ERR_DEVICE_TIMEOUT or FLINT_MOE_ERR_DEVICE_BOUNDS):
+ * the device errors of every flint_moe_forward_noalloc call on this device since the last poll
+ * (the array is shared by all of them).  Allocates nothing; like flint_moe_forward_noalloc, a
+ * first call on a device does that device's one-time set-up. */
+flint_moe_status flint_moe_noalloc_poll_device_status(flint_stream_t stream);
 
 /* ---------------------------------------------------------------- the layer stack
  * The model runs its MoE layers back to back: two dense layers, then 47 MoE layers (Recursive

@@ -25,7 +25,8 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "
 EXPORTS = ("flint_moe_status_string", "flint_moe_workspace_bytes", "flint_moe_create", "flint_moe_route",
            "flint_moe_forward", "flint_moe_forward_host", "flint_moe_poll_device_status",
            "flint_moe_enable_kernel_timing", "flint_moe_kernel_times", "flint_moe_read_trace",
-           "flint_moe_destroy", "flint_moe_forward_noalloc", "flint_moe_stack_workspace_bytes",
+           "flint_moe_destroy", "flint_moe_forward_noalloc", "flint_moe_noalloc_poll_device_status",
+           "flint_moe_stack_workspace_bytes",
            "flint_moe_stack_create", "flint_moe_stack_forward", "flint_moe_stack_poll_device_status",
            "flint_moe_stack_enable_kernel_timing", "flint_moe_stack_read_trace", "flint_moe_stack_destroy")
 
@@ -82,6 +83,7 @@ def load_library():
     L.flint_moe_read_trace.argtypes = [P, ctypes.POINTER(ctypes.c_ulonglong), I32, ctypes.POINTER(I32)]
     L.flint_moe_destroy.argtypes = [P]
     L.flint_moe_forward_noalloc.argtypes = [ctypes.POINTER(_Weights), P, I32, P, P, P, P]
+    L.flint_moe_noalloc_poll_device_status.argtypes = [P]
     L.flint_moe_stack_workspace_bytes.argtypes = [ctypes.POINTER(_Config), I32, ctypes.POINTER(ctypes.c_size_t)]
     L.flint_moe_stack_create.argtypes = [ctypes.POINTER(_Config), ctypes.POINTER(_Weights), I32, P, ctypes.c_size_t,
                                          ctypes.POINTER(P)]
@@ -134,6 +136,12 @@ def forward_noalloc(weights: dict, x, y=None, topk_idx=None, topk_w=None, stream
     _check(L.flint_moe_forward_noalloc(ctypes.byref(w), _ptr(x), T, _ptr(y), _ptr(topk_idx), _ptr(topk_w),
                                        _stream_ptr(stream)), "flint_moe_forward_noalloc")
     return y
+
+
+def noalloc_poll_device_status(stream=None) -> int:
+    """Status code of the allocation-free entry point's device errors on the current device
+    since the last poll (0 = ok, 5 = device timeout, 6 = device bounds); clears it."""
+    return load_library().flint_moe_noalloc_poll_device_status(_stream_ptr(stream))
 
 
 class FlintMoE:

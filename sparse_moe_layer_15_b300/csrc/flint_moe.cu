@@ -682,8 +682,15 @@ flint_moe_status flint_moe_stack_destroy(flint_moe_stack_t st) {
 // The array (17 MiB) holds the workspace of a handle with max_tokens = NOALLOC_MAX_T.
 // Every GPU that loads the library reserves it until the process exits.  All calls on a
 // device share it: calls whose work overlaps on the GPU (on different streams, or from
-// different threads) race on it and must be serialised by the caller.  The counters that must
-// start at zero are cleared on the caller's stream at the start of every call.
+// different threads) race on it and must be serialised by the caller.  The barrier counters
+// and tickets, which must start at zero, are cleared on the caller's stream at the start of
+// every call; the status word is not: a device error (a bounded wait that ran out, an index
+// out of range) stays recorded until flint_moe_noalloc_poll_device_status reads and clears it.
+//
+// The array's device address is looked up once per device and kept for the life of the
+// process.  It belongs to the device's primary context: after cudaDeviceReset (or anything
+// else that destroys and recreates that context) the kept address is stale, so these entry
+// points must not be used on that device again in the same process.
 namespace {
 
 constexpr int NOALLOC_MAX_T = 4;
@@ -696,8 +703,9 @@ std::mutex g_noalloc_mutex;
 void* g_noalloc_ptr[NOALLOC_MAX_DEVICES];
 int g_noalloc_sms[NOALLOC_MAX_DEVICES];
 
-// First call on a device (with that device current): the device address of the array and the
-// kernel's shared-memory limit.  Later calls reuse them.
+// First call on a device (with that device current): the device address of the array, the
+// kernel's shared-memory limit and occupancy, and a synchronous clear of the array's status
+// word and counters.  Later calls reuse the address.
 flint_moe_status noalloc_setup(int dev, void** ptr, int* n_sm) {
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
   if (!g_noalloc_ptr[dev]) {
@@ -709,6 +717,13 @@ flint_moe_status noalloc_setup(int dev, void** ptr, int* n_sm) {
     if (cudaFuncSetAttribute(decode_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, FUSED_SMEM) !=
         cudaSuccess)
       return FLINT_MOE_ERR_CUDA;
+    // the cooperative launch needs one CTA resident on every SM (as flint_moe_create checks)
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused, NTHREADS, FUSED_SMEM) != cudaSuccess)
+      return FLINT_MOE_ERR_CUDA;
+    if (per_sm < 1) return FLINT_MOE_ERR_UNSUPPORTED;
+    // the status word starts clear (later calls clear only the counters and tickets)
+    if (cudaMemset(p, 0, make_layout(NOALLOC_MAX_T).zero_end) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
     g_noalloc_sms[dev] = sms;
     g_noalloc_ptr[dev] = p;
   }
@@ -763,8 +778,28 @@ extern "C" flint_moe_status flint_moe_forward_noalloc(const flint_moe_weights* w
                   make_map(&h.smaps.wsd, w->ws_down, IS, H, 64, DN_ROWS, sw);
   if (!ok) return FLINT_MOE_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // status word, tickets and barrier counters start at zero on every call
-  if (cudaMemsetAsync(h.ws, 0, h.L.zero_end, st) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  // barrier counters and tickets start at zero on every call; the status word (and the word
+  // after it, which the timeout test waits on) is left for flint_moe_noalloc_poll_device_status
+  if (cudaMemsetAsync(h.ws + h.L.bar_count, 0, h.L.zero_end - h.L.bar_count, st) != cudaSuccess)
+    return FLINT_MOE_ERR_CUDA;
   Params p = make_params(&h, x, T, y, topk_idx, topk_w, nullptr);
   return run_decode(&h, p, st, true);
+}
+
+extern "C" flint_moe_status flint_moe_noalloc_poll_device_status(flint_stream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= NOALLOC_MAX_DEVICES) return FLINT_MOE_ERR_CUDA;
+  void* scratch = nullptr;
+  int n_sm = 0;
+  flint_moe_status s = noalloc_setup(dev, &scratch, &n_sm);
+  if (s != FLINT_MOE_OK) return s;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  const Layout L = make_layout(NOALLOC_MAX_T);
+  uint8_t* ws = static_cast<uint8_t*>(scratch);
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, ws + L.status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  if (word == 0) return FLINT_MOE_OK;
+  // a device error may leave tickets mid-count: clear them with the status word
+  if (cudaMemset(ws + L.status, 0, L.zero_end - L.status) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  return (word & ST_TIMEOUT) ? FLINT_MOE_ERR_DEVICE_TIMEOUT : FLINT_MOE_ERR_DEVICE_BOUNDS;
 }

@@ -21,8 +21,11 @@
 //   TMEM columns; two buffers, so the epilogue of one tile overlaps the main loop of the next.
 // Warp roles: warp 0 issues TMA (one lane), warp 1 allocates TMEM and issues the MMAs (one
 // lane), warps 2-5 run the epilogue (warp w reads TMEM lanes 32*(w%4) .. +31, one row each).
-// Every wait is bounded (1 s); on expiry the device status word gets ST_TIMEOUT and the
-// kernel runs to its end without hanging; TMEM is always released.
+// Every wait is bounded (1 s); on expiry the device status word gets ST_TIMEOUT and the CTA
+// aborts: a shared abort flag stops every role from issuing more work, the producer waits
+// (bounded) for the TMA loads it has issued to land, the MMA issuer commits and waits
+// (bounded) for the MMAs it has issued, and only then is TMEM released and the CTA ends, so
+// no asynchronous copy or MMA is left in flight on freed shared memory or TMEM.
 //
 // A Problem class supplies the tile list and the epilogue:
 //   static constexpr bool kColumns;            // orientation of every tile
@@ -86,7 +89,8 @@ struct Smem {
   static constexpr int bytes = tbl + TBL_SMEM;
 };
 constexpr int SMEM_BYTES = Smem::bytes + 1024;
-constexpr int BAR_FULL = 0, BAR_EMPTY = 4, BAR_TFULL = 8, BAR_TEMPTY = 10;
+constexpr int BAR_FULL = 0, BAR_EMPTY = 4, BAR_TFULL = 8, BAR_TEMPTY = 10, BAR_DRAIN = 12;
+// tmem_slot[0]: the TMEM base address written by tcgen05.alloc; tmem_slot[1]: the abort flag.
 
 struct TileInfo {
   const CUtensorMap* amap;  // X operand (activation rows)
@@ -140,21 +144,51 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Bounded mbarrier wait (one thread); records ST_TIMEOUT and returns false on expiry.
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, uint32_t* status) {
+// Bounded mbarrier wait that also gives up as soon as another role of the CTA has aborted
+// (*abort != 0).  On expiry it records ST_TIMEOUT and raises the abort flag.  Returns false
+// when the phase did not complete.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                         volatile uint32_t* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
     if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
       record_status(status, ST_TIMEOUT);
+      *abort = 1u;
       return false;
     }
   }
   return true;
 }
 
+// Drain wait after an abort: bounded by the wait limit only (the abort flag is already up).
+__device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, uint32_t* status) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+      record_status(status, ST_TIMEOUT);
+      return;
+    }
+  }
+}
+
 // Barrier among the four epilogue warps (128 threads).
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
+// Barrier among the four epilogue warps that also returns true in every one of them when `fail`
+// is true in any: they skip a tile (and end) together, never some of them entering the
+// epilogue's own barriers without the others.
+__device__ __forceinline__ bool epi_any(bool fail) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 2, 128, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(fail ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* raw) {
   const uint32_t a = smem_u32(raw);
@@ -171,6 +205,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
   uint64_t* tfull = bars + BAR_TFULL;
   uint64_t* tempty = bars + BAR_TEMPTY;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Smem::tmem_slot);
+  volatile uint32_t* abort = tmem_slot + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint32_t* status = prob.status();
   unsigned long long* trace = prob.trace();
@@ -186,6 +221,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       mbar_init(tfull + b, 1);
       mbar_init(tempty + b, 4);  // one arrival per epilogue warp
     }
+    mbar_init(bars + BAR_DRAIN, 1);
+    *abort = 0u;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -209,10 +246,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
   if (warp == 0) {
     // ---------------- producer
     long long w_wait = 0;
+    int pos = 0;  // stages issued
     if constexpr (cols) {
       if (lane == 0) {
-        int pos = 0;
-        for (int i = blockIdx.x; i < ntiles; i += gridDim.x) {
+        for (int i = blockIdx.x; i < ntiles && !*abort; i += gridDim.x) {
           TileInfo t;
           prob.tile(i, t, tbl);
           const int nxb = (t.n + XC_ROWS - 1) / XC_ROWS;  // 1..4 X boxes of 64 rows
@@ -220,7 +257,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           for (int kb = 0; kb < nkb; ++kb, ++pos) {
             const int st = pos % STAGES, use = pos / STAGES;
             const long long c0 = clock64();
-            if (use > 0) wait_bar(bars + BAR_EMPTY + st, uint32_t(use - 1) & 1u, status);
+            if (use > 0 && !wait_bar(bars + BAR_EMPTY + st, uint32_t(use - 1) & 1u, status, abort)) break;
+            if (*abort) break;
             w_wait += clock64() - c0;
             uint8_t* x = sm + Smem::stages + st * STAGE_BYTES;
             uint8_t* w = x + 2 * A_BYTES;
@@ -233,15 +271,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         }
       }
     } else if (lane == 0) {
-      int pos = 0;
-      for (int i = blockIdx.x; i < ntiles; i += gridDim.x) {
+      for (int i = blockIdx.x; i < ntiles && !*abort; i += gridDim.x) {
         TileInfo t;
         prob.tile(i, t, tbl);
         const int nkb = t.nkb ? t.nkb : kb_n;
         for (int kb = 0; kb < nkb; ++kb, ++pos) {
           const int st = pos % STAGES, use = pos / STAGES;
           const long long c0 = clock64();
-          if (use > 0) wait_bar(bars + BAR_EMPTY + st, uint32_t(use - 1) & 1u, status);
+          if (use > 0 && !wait_bar(bars + BAR_EMPTY + st, uint32_t(use - 1) & 1u, status, abort)) break;
+          if (*abort) break;
           w_wait += clock64() - c0;
           uint8_t* a = sm + Smem::stages + st * STAGE_BYTES;
           uint8_t* b = a + A_BYTES;
@@ -253,28 +291,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         }
       }
     }
+    // the loads already issued must land before the CTA may end, also after an abort (the last
+    // use of each slot is the only phase of its full barrier that can still be pending; without
+    // an abort the MMA issuer has waited for them all, and these waits return at once)
+    if (lane == 0)
+      for (int st = 0; st < STAGES && st < pos; ++st)
+        drain_bar(bars + BAR_FULL + st, uint32_t((pos - 1 - st) / STAGES) & 1u, status);
     if (trace && lane == 0) trace[0] = (unsigned long long)w_wait;
   } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0) {
       int pos = 0, it = 0;
+      bool issued = false;
       long long w_full = 0, w_tempty = 0;
-      for (int i = blockIdx.x; i < ntiles; i += gridDim.x, ++it) {
+      for (int i = blockIdx.x; i < ntiles && !*abort; i += gridDim.x, ++it) {
         TileInfo t;
         prob.tile(i, t, tbl);
         const uint32_t idesc = cols ? idesc_columns(t.n) : IDESC;
         const int buf = it & 1, use = it >> 1;
         long long c0 = clock64();
-        if (use > 0) wait_bar(tempty + buf, uint32_t(use - 1) & 1u, status);
+        if (use > 0 && !wait_bar(tempty + buf, uint32_t(use - 1) & 1u, status, abort)) break;
         w_tempty += clock64() - c0;
         tc_fence_after();
         const uint32_t d = tmem_base + uint32_t(buf * TN);
         const int nkb = t.nkb ? t.nkb : kb_n;
+        bool done = true;
         for (int kb = 0; kb < nkb; ++kb, ++pos) {
           uint32_t x, w;
           c0 = clock64();
           const int st = pos % STAGES;
-          wait_bar(bars + BAR_FULL + st, uint32_t(pos / STAGES) & 1u, status);
+          if (!wait_bar(bars + BAR_FULL + st, uint32_t(pos / STAGES) & 1u, status, abort)) {
+            done = false;
+            break;
+          }
+          issued = true;
           x = smem_u32(sm + Smem::stages + st * STAGE_BYTES);
           w = x + (cols ? 2 : 1) * A_BYTES;
           w_full += clock64() - c0;
@@ -294,7 +344,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           // the slots are free once these MMAs have read them
           mma_commit(bars + BAR_EMPTY + st);
         }
+        if (!done) break;
         mma_commit(tfull + buf);  // the accumulator is complete
+      }
+      // every MMA issued completes before TMEM is released, also after an abort (without one,
+      // the epilogue has waited for the last accumulator already)
+      if (issued) {
+        mma_commit(bars + BAR_DRAIN);
+        drain_bar(bars + BAR_DRAIN, 0u, status);
       }
       if (trace) {
         trace[1] = (unsigned long long)w_full;
@@ -310,11 +367,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     for (int i = blockIdx.x; i < ntiles; i += gridDim.x, ++it) {
       const int buf = it & 1;
       const long long c0 = clock64();
-      if (lane == 0) wait_bar(tfull + buf, uint32_t(it >> 1) & 1u, status);
-      __syncwarp();
-      while (!mbar_try_wait(tfull + buf, uint32_t(it >> 1) & 1u)) {
-        if (*reinterpret_cast<volatile uint32_t*>(status) & ST_TIMEOUT) break;
-      }
+      // every thread waits itself; the four warps skip the tile (and end) together on an abort
+      const bool ok = wait_bar(tfull + buf, uint32_t(it >> 1) & 1u, status, abort);
+      if (epi_any(!ok)) break;
       tc_fence_after();
       const long long c1 = clock64();
       TileInfo t;

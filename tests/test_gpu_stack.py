@@ -1,11 +1,10 @@
 """The 47-layer stack workload (T = 256 tokens, x <- x + MoE_l(RMSNorm(x)), eps 1e-6, weights
 seed 100 + l, about 76 GB resident), checked layer by layer with teacher forcing: the oracle's
-layer l takes the GPU's bf16 input to layer l, on sampled layers 0, 23 and 46 -- all 256 tokens
-for routing, a spread sample of tokens for outputs.  A routing flip in an early layer would make
+layer l takes the GPU's bf16 input to layer l, on sampled layers 0, 23 and 46 -- routing and
+outputs on all 256 tokens.  A routing flip in an early layer would make
 an end-to-end comparison meaningless, so the end-to-end output is only checked to be finite and
 bitwise deterministic, and the stack handle (one launch at 16 tokens) must reproduce the per-layer
 results bitwise."""
-import numpy as np
 import pytest
 import torch
 
@@ -50,12 +49,11 @@ def test_stack_47_layers_teacher_forced_parity():
     y2, _ = run(())
     assert torch.isfinite(y1.float()).all()
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
-    sample = sorted(set(np.linspace(0, T - 1, 16).astype(int).tolist()))
     for l in CHECKED:
         xin, yout, idx, gw = seen[l]
         rep = parity.check_routing_all(weights[l], xin, idx, gw, eps=EPS)
         assert rep["ok"], (l, {k: v for k, v in rep.items() if k != "oracle_counts"})
-        ref = parity.oracle_reference(weights[l], xin, sample, eps=EPS, residual=True)
+        ref = parity.oracle_reference(weights[l], xin, range(T), eps=EPS, residual=True)
         rep = parity.compare(ref, yout, idx, gw)
         assert rep["ok"], (l, rep)
     for lay in layers:

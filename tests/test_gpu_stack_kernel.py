@@ -59,8 +59,10 @@ def test_stack_equals_layer_calls_prenorm_residual(layer_weights, T):
     stack.close()
 
 
-def test_stack_equals_layer_calls_without_norm_or_residual(layer_weights):
-    T = 16
+@pytest.mark.parametrize("T", [16, 64, 256])
+def test_stack_equals_layer_calls_without_norm_or_residual(layer_weights, T):
+    # T = 16: one launch; T > 16: per-layer launches with y == x and the router and gate/up
+    # reading x directly (no pre-norm copy), i.e. the layer reads and overwrites one buffer
     x0 = synth.torch_normal_bf16((T, fm.HIDDEN), 4100, synth.TAG_X, 1.0, device=DEV)
     ref, _, _ = per_layer(layer_weights[:2], x0, 0, T)
     stack = fm.FlintMoEStack(layer_weights[:2], max_tokens=T, flags=0)
