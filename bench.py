@@ -35,6 +35,28 @@ SWEEP = (1, 2, 4, 8, 16, 32, 64)
 METRIC = "MoE-layer tokens/s on 1 B300; HBM GB/s (decode) / tensor TFLOPS (prefill) vs peak"
 
 
+def sweep_config(world):
+    """The decode-sweep workload's config object (identical on both arms)."""
+    return dict(workload="decode sweep: one Flint MoE layer (H2048 E256 top6 I512 shared1024), "
+                         "T=1,2,4,8,16,32,64 per step",
+                tokens_per_step=sum(SWEEP), parallelism=f"replicas x{world}",
+                l2="flushed (512 MB write) before every forward")
+
+
+def host_cpu():
+    """The host's logical core count and CPU model (for the oracle's baseline lines)."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.startswith("model name"):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return dict(nproc=os.cpu_count(), cpu_model=model)
+
+
 KERNEL_SOURCES = ("sparse_moe_layer_15_b300/csrc/decode_fused.cuh", "sparse_moe_layer_15_b300/csrc/common.cuh",
                   "sparse_moe_layer_15_b300/csrc/flint_moe.cu")
 
@@ -339,16 +361,24 @@ def run_ours(args, rank, world, local):
 
     out = dict(metric=METRIC, value=round(value, 1), unit="tokens/s", n_gpus=world, steps=args.steps,
                warmup=args.warmup, ms_per_step=round(ms_step, 4), higher_is_better=True, scaling="weak",
-               vs_baseline=None, dtype="bf16", data="synthetic",
-               config=dict(workload="decode sweep: one Flint MoE layer (H2048 E256 top6 I512 shared1024), "
-                                    "T=1,2,4,8,16,32,64 per step",
-                           tokens_per_step=tokens_step, parallelism=f"replicas x{world}",
-                           l2="flushed (512 MB write) before every forward"),
+               vs_baseline=None, dtype="bf16", data="synthetic", config=sweep_config(world),
                sweep=sweep, kernels_us=kernels, roofline=roofline, e2e=e2e,
                gpu_launches=args.steps * len(SWEEP), clocks=clk, wall_s=round(wall, 3))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, xs, budget_s=args.cpu_budget)
     layer.close()
+    del layer, w
+    torch.cuda.empty_cache()
+    if not args.no_configs:
+        # the other configurations, each measured on its own (own clocks, own roofline, own e2e)
+        out["configs"] = {}
+        for name in ("single", "prefill", "adversarial", "stack"):
+            sub_args = argparse.Namespace(**vars(args))
+            sub_args.workload = name
+            sub_args.steps = min(args.steps, 20)
+            r = run_workload(sub_args, rank, world, local, summary=True)
+            out["configs"][name] = r
+            torch.cuda.empty_cache()
     return out
 
 
@@ -387,9 +417,20 @@ def timed_loop(fn, steps, flush, stream, ev):
     return out
 
 
-def run_workload(args, rank, world, local):
+def summarize(out):
+    """The per-configuration entry of the default line: the workload's own line without the
+    keys that belong to the whole run."""
+    drop = ("metric", "unit", "n_gpus", "steps", "warmup", "higher_is_better", "scaling", "vs_baseline", "dtype",
+            "data")
+    r = {k: v for k, v in out.items() if k not in drop}
+    r["tokens_per_s"] = r.pop("value")
+    return r
+
+
+def run_workload(args, rank, world, local, summary=False):
     """One workload other than the decode sweep: a step is one forward of T tokens (the
-    47-layer stack: 47 pre-norm residual forwards of T=256 tokens)."""
+    47-layer stack: 47 pre-norm residual forwards of T=256 tokens).  summary=True: the entry of
+    the default line's `configs` object (no CPU baseline)."""
     import torch
 
     import synth
@@ -397,7 +438,7 @@ def run_workload(args, rank, world, local):
     from sparse_moe_layer_15_b300 import accounting as acc
 
     if args.workload == "stack":
-        return run_stack(args, rank, world, local)
+        return run_stack(args, rank, world, local, summary=summary)
     cfg = WORKLOADS[args.workload]
     T = cfg["T"]
     torch.cuda.set_device(local)
@@ -433,6 +474,7 @@ def run_workload(args, rank, world, local):
     barrier(world)
     times = timed_loop(fwd, args.steps, flush, stream, ev)
     clk = clocks.stop()
+    q = sorted(times)
     barrier(world)
     if layer.poll_device_status() != 0:
         raise RuntimeError("device status error in the timed region")
@@ -480,19 +522,23 @@ def run_workload(args, rank, world, local):
                layer=dict(touched_experts=U, alg_bytes=alg_bytes, alg_flop=flop,
                           tflops=round(flop / (ms * 1e-3) / 1e12, 1), gbs=round(alg_bytes / (ms * 1e-3) / 1e9, 1),
                           roofline_ms=round(t_roof_ms, 4), roofline_frac=round(t_roof_ms / ms, 4),
+                          us_median=round(statistics.median(times) * 1e3, 2), us_p10=round(q[len(q) // 10] * 1e3, 2),
+                          us_p90=round(q[(9 * len(q)) // 10] * 1e3, 2),
                           hot_share=(round(float(np.sort(counts)[::-1][:8].sum() / counts.sum()), 4)
                                      if args.workload == "adversarial" else None)),
                kernels_us=kernels, roofline=roofline,
                e2e=dict(value=round(world * T / (e2e_ms * 1e-3), 1), unit="tokens/s",
                         h2d_bytes_per_step=2 * fm.HIDDEN * T, d2h_bytes_per_step=2 * fm.HIDDEN * T),
                gpu_launches=args.steps * len(kernels), clocks=clk)
+    layer.close()
+    if summary:
+        return summarize(out)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline_tokens(w, x, n=16, what=args.workload)
-    layer.close()
     return out
 
 
-def run_stack(args, rank, world, local):
+def run_stack(args, rank, world, local, summary=False):
     """47 Flint MoE layers (weights seed 100+l, about 76 GB), T=256 tokens (x seed 4); each
     layer x <- x + MoE_l(RMSNorm(x)), eps 1e-6.  One step = the 47 forwards, through the stack
     call.  --stack-tokens T measures the same stack at T tokens (up to 16: one launch for all
@@ -592,11 +638,13 @@ def run_stack(args, rank, world, local):
                e2e=dict(value=round(world * T / (e2e_ms * 1e-3), 1), unit="tokens/s",
                         h2d_bytes_per_step=2 * fm.HIDDEN * T, d2h_bytes_per_step=2 * fm.HIDDEN * T),
                gpu_launches=args.steps * (1 if one_launch else 2 * L), clocks=clk)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline_tokens(weights[0], x0, n=min(8, T), what="stack layer 0", eps=1e-6)
     for lay in layers:
         lay.close()
     stack_handle.close()
+    if summary:
+        return summarize(out)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline_tokens(weights[0], x0, n=min(8, T), what="stack layer 0", eps=1e-6)
     return out
 
 
@@ -616,7 +664,7 @@ def cpu_baseline_tokens(w, x, n=16, what="", eps=None):
     oracle.forward(layer, x64, nthreads=1)
     dt = time.perf_counter() - t0
     return dict(value=round(n / dt, 3), unit="tokens/s", cores=1, kind="oracle",
-                sample=f"{what}: the first {n} tokens, fp64, one thread")
+                sample=f"{what}: the first {n} tokens, fp64, one thread", **host_cpu())
 
 
 def cpu_baseline(w, xs, budget_s=20.0, sample=(1, 2, 4, 8)):
@@ -637,18 +685,20 @@ def cpu_baseline(w, xs, budget_s=20.0, sample=(1, 2, 4, 8)):
             break
     dt = time.perf_counter() - t0
     return dict(value=round(n_tok / dt, 3), unit="tokens/s", cores=1, kind="oracle",
-                sample=f"decode-sweep forwards at T={done} ({n_tok} tokens), fp64, one thread")
+                sample=f"decode-sweep forwards at T={done} ({n_tok} tokens), fp64, one thread", **host_cpu())
 
 
 def run_reference(args, rank, world, local):
-    """--impl reference: the fp64 CPU oracle as the reference arm (rank 0 only)."""
+    """--impl reference: the fp64 CPU oracle as the reference arm (rank 0 only), one thread, on
+    the same decode sweep as our arm (one step = the forwards at T = 1, 2, 4, 8, 16, 32, 64, 127
+    tokens, x seed 1000+T)."""
     import torch
 
     import synth
     import oracle
     from tests import parity
 
-    sample = (1, 2, 4, 8)
+    sample = SWEEP
     w = synth.flint_weights(seed=0, device="cuda" if torch.cuda.is_available() else "cpu")
     layer = parity.oracle_layer(w)
     xin = {T: oracle.bf16_to_f64(parity.to_np_bf16(synth.torch_normal_bf16((T, 2048), 1000 + T, synth.TAG_X, 1.0,
@@ -669,11 +719,10 @@ def run_reference(args, rank, world, local):
     return dict(metric=METRIC, value=round(v, 3), unit="tokens/s", n_gpus=world, steps=args.steps,
                 warmup=args.warmup, ms_per_step=round(dt / args.steps * 1e3, 3), higher_is_better=True,
                 scaling="weak", vs_baseline=None, dtype="f64", data="synthetic", impl="reference",
-                config=dict(workload="decode sweep: one Flint MoE layer (H2048 E256 top6 I512 shared1024); "
-                                     "reference step = the T=1,2,4,8 forwards (15 tokens)",
-                            tokens_per_step=sum(sample), parallelism="rank 0 only"),
+                config=sweep_config(world),
                 cpu_baseline=dict(value=round(v, 3), unit="tokens/s", cores=1, kind="oracle",
-                                  sample="decode-sweep forwards at T=1,2,4,8 per step, fp64, one thread"),
+                                  sample="the whole decode sweep per step (T=1..64, 127 tokens), fp64, one thread",
+                                  **host_cpu()),
                 e2e=dict(value=round(v, 3), unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
 
 
@@ -762,6 +811,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="default workload only: skip the other four configurations")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--profile", type=int, default=0, help="profiler case: forwards at this T only")
     ap.add_argument("--trace", action="store_true",

@@ -226,6 +226,55 @@ flint_moe_status flint_moe_stack_read_trace(flint_moe_stack_t s, unsigned long l
 /* Releases the stack's host state (not the workspace or the weights). */
 flint_moe_status flint_moe_stack_destroy(flint_moe_stack_t s);
 
+/* ---------------------------------------------------------------- the dense MLP layers
+ * The model's first two layers are dense SwiGLU MLP layers instead of MoE layers (serving-kit
+ * post, section "The architecture, from the config": "2 dense MLP layers (mlp_only_layers: [0,
+ * 1]), then 47 MoE layers"; the two "add about 75M" parameters).  The pages give no width; the
+ * one their parameter count fixes is 6144 (2 x 3 x 2048 x 6144 = 75.5M), and the layer is read
+ * as the same SwiGLU MLP as an expert: y = (silu(x' Wg) * (x' Wu)) Wd [+ x], x' = x or rms(x).
+ * The conventions of the MoE calls above hold (caller-owned device memory, asynchronous on
+ * `stream`, no allocation in forward, sticky device status, bitwise deterministic).  T <= 256
+ * runs the decode-size kernel (the MoE kernel's shared-expert steps at this width), larger T
+ * the tensor-core GEMMs. */
+typedef struct flint_dense_s* flint_dense_t;
+
+typedef struct {
+  int hidden;       /* must be 2048 */
+  int inter;        /* must be 6144 */
+  int max_tokens;   /* largest T any call on this handle will pass; 1..65536 */
+  unsigned flags;   /* FLINT_MOE_FLAG_PRE_RMSNORM, FLINT_MOE_FLAG_RESIDUAL (y may alias x),
+                       FLINT_MOE_FLAG_TEST_WAIT_TIMEOUT */
+  float rms_eps;    /* RMSNorm epsilon (with FLINT_MOE_FLAG_PRE_RMSNORM), > 0 */
+} flint_dense_config;
+
+typedef struct {
+  const void* w_gate; /* bf16 [hidden][inter], 16-byte aligned */
+  const void* w_up;   /* bf16 [hidden][inter] */
+  const void* w_down; /* bf16 [inter][hidden] */
+} flint_dense_weights;
+
+/* Bytes of device workspace a dense layer with `cfg` needs (the caller allocates it, 256-byte
+ * aligned, and keeps it alive until flint_dense_destroy). */
+flint_moe_status flint_dense_workspace_bytes(const flint_dense_config* cfg, size_t* bytes);
+
+/* As flint_moe_create: validates, builds the TMA descriptors, zeroes the workspace's counters
+ * and status word (synchronously).  The weights are borrowed. */
+flint_moe_status flint_dense_create(const flint_dense_config* cfg, const flint_dense_weights* w, void* workspace,
+                                    size_t workspace_bytes, flint_dense_t* out);
+
+/* y bf16 [T][hidden] = (silu(x' Wg) * (x' Wu)) Wd [+ x]; 1 <= T <= max_tokens; x, y device,
+ * 16-byte aligned. */
+flint_moe_status flint_dense_forward(flint_dense_t d, const void* x, int T, void* y, flint_stream_t stream);
+
+/* As flint_moe_poll_device_status / flint_moe_enable_kernel_timing / flint_moe_kernel_times,
+ * for a dense layer. */
+flint_moe_status flint_dense_poll_device_status(flint_dense_t d, flint_stream_t stream);
+flint_moe_status flint_dense_enable_kernel_timing(flint_dense_t d, int enable);
+flint_moe_status flint_dense_kernel_times(flint_dense_t d, const char** names, float* ms, int cap, int* n);
+
+/* Releases the handle's host state (not the workspace or the weights). */
+flint_moe_status flint_dense_destroy(flint_dense_t d);
+
 #ifdef __cplusplus
 }
 #endif

@@ -166,6 +166,29 @@ def swiglu(x, wg, wu, wd):
     return out
 
 
+def dense(x, wg, wu, wd, nthreads: int = 1):
+    """A dense SwiGLU MLP layer on rows x ([T,H] float64): the same per-row computation as
+    :func:`swiglu` (oracle_swiglu), with disjoint row ranges evaluated concurrently."""
+    x = _f64(np.atleast_2d(x))
+    wg, wu, wd = _u16(wg), _u16(wu), _u16(wd)
+    H, I = wg.shape
+    out = np.empty((x.shape[0], H))
+    L = _lib()
+
+    def run(a, b):
+        hbuf = np.empty(I)
+        for t in range(a, b):
+            L.oracle_swiglu(_ptr(x[t]), H, I, _ptr(wg), _ptr(wu), _ptr(wd), _ptr(out[t]), _ptr(hbuf))
+
+    parts = _split(x.shape[0], nthreads)
+    if len(parts) <= 1:
+        run(0, x.shape[0])
+    else:
+        with ThreadPoolExecutor(len(parts)) as ex:
+            list(ex.map(lambda ab: run(*ab), parts))
+    return out
+
+
 def _split(T, nthreads):
     n = max(1, min(nthreads, T))
     b = np.linspace(0, T, n + 1).astype(int)

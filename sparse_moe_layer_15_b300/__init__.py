@@ -28,9 +28,13 @@ EXPORTS = ("flint_moe_status_string", "flint_moe_workspace_bytes", "flint_moe_cr
            "flint_moe_destroy", "flint_moe_forward_noalloc", "flint_moe_noalloc_poll_device_status",
            "flint_moe_stack_workspace_bytes",
            "flint_moe_stack_create", "flint_moe_stack_forward", "flint_moe_stack_poll_device_status",
-           "flint_moe_stack_enable_kernel_timing", "flint_moe_stack_read_trace", "flint_moe_stack_destroy")
+           "flint_moe_stack_enable_kernel_timing", "flint_moe_stack_read_trace", "flint_moe_stack_destroy",
+           "flint_dense_workspace_bytes", "flint_dense_create", "flint_dense_forward",
+           "flint_dense_poll_device_status", "flint_dense_enable_kernel_timing", "flint_dense_kernel_times",
+           "flint_dense_destroy")
 
 NOALLOC_MAX_TOKENS = 4
+DENSE_INTER = 6144  # width of the dense MLP layers
 
 
 class FlintMoEError(RuntimeError):
@@ -43,6 +47,15 @@ class _Config(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int), ("n_experts", ctypes.c_int), ("top_k", ctypes.c_int),
                 ("expert_inter", ctypes.c_int), ("shared_inter", ctypes.c_int), ("max_tokens", ctypes.c_int),
                 ("flags", ctypes.c_uint), ("rms_eps", ctypes.c_float)]
+
+
+class _DenseConfig(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int), ("inter", ctypes.c_int), ("max_tokens", ctypes.c_int),
+                ("flags", ctypes.c_uint), ("rms_eps", ctypes.c_float)]
+
+
+class _DenseWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("w_gate", "w_up", "w_down")]
 
 
 class _Weights(ctypes.Structure):
@@ -92,6 +105,15 @@ def load_library():
     L.flint_moe_stack_enable_kernel_timing.argtypes = [P, I32]
     L.flint_moe_stack_read_trace.argtypes = [P, ctypes.POINTER(ctypes.c_ulonglong), I32, ctypes.POINTER(I32)]
     L.flint_moe_stack_destroy.argtypes = [P]
+    L.flint_dense_workspace_bytes.argtypes = [ctypes.POINTER(_DenseConfig), ctypes.POINTER(ctypes.c_size_t)]
+    L.flint_dense_create.argtypes = [ctypes.POINTER(_DenseConfig), ctypes.POINTER(_DenseWeights), P,
+                                     ctypes.c_size_t, ctypes.POINTER(P)]
+    L.flint_dense_forward.argtypes = [P, P, I32, P, P]
+    L.flint_dense_poll_device_status.argtypes = [P, P]
+    L.flint_dense_enable_kernel_timing.argtypes = [P, I32]
+    L.flint_dense_kernel_times.argtypes = [P, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float), I32,
+                                           ctypes.POINTER(I32)]
+    L.flint_dense_destroy.argtypes = [P]
     for name in EXPORTS:
         if name != "flint_moe_status_string":
             getattr(L, name).restype = I32
@@ -310,6 +332,67 @@ class FlintMoEStack:
     def close(self):
         if getattr(self, "_h", None):
             self._L.flint_moe_stack_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class FlintDense:
+    """One dense SwiGLU MLP layer (width 6144) bound to borrowed bf16 device weights:
+    ``w_gate``/``w_up`` [2048, 6144], ``w_down`` [6144, 2048] (contiguous).
+    y = (silu(x' Wg) * (x' Wu)) Wd [+ x] with x' = x or rms(x) (flags as for FlintMoE)."""
+
+    def __init__(self, weights: dict, max_tokens: int, flags: int = 0, rms_eps: float = 1e-6, workspace=None):
+        import torch
+        self._L = load_library()
+        self.max_tokens = int(max_tokens)
+        self._weights = weights
+        for k, v in weights.items():
+            if not v.is_contiguous():
+                raise ValueError(f"{k} must be contiguous")
+        self._cfg = _DenseConfig(HIDDEN, DENSE_INTER, self.max_tokens, int(flags), float(rms_eps))
+        self._w = _DenseWeights(*[weights[n].data_ptr() for n, _ in _DenseWeights._fields_])
+        nbytes = ctypes.c_size_t(0)
+        _check(self._L.flint_dense_workspace_bytes(ctypes.byref(self._cfg), ctypes.byref(nbytes)),
+               "flint_dense_workspace_bytes")
+        if workspace is None:
+            workspace = torch.empty(nbytes.value, dtype=torch.uint8, device=weights["w_gate"].device)
+        self.workspace = workspace
+        h = ctypes.c_void_p()
+        _check(self._L.flint_dense_create(ctypes.byref(self._cfg), ctypes.byref(self._w),
+                                          ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                                          ctypes.byref(h)), "flint_dense_create")
+        self._h = h
+
+    def forward(self, x, y=None, stream=None):
+        import torch
+        if y is None:
+            y = torch.empty_like(x)
+        _check(self._L.flint_dense_forward(self._h, _ptr(x), x.shape[0], _ptr(y), _stream_ptr(stream)),
+               "flint_dense_forward")
+        return y
+
+    def poll_device_status(self, stream=None):
+        return self._L.flint_dense_poll_device_status(self._h, _stream_ptr(stream))
+
+    def enable_kernel_timing(self, on=True):
+        _check(self._L.flint_dense_enable_kernel_timing(self._h, 1 if on else 0), "flint_dense_enable_kernel_timing")
+
+    def kernel_times(self):
+        cap = 16
+        names = (ctypes.c_char_p * cap)()
+        ms = (ctypes.c_float * cap)()
+        n = ctypes.c_int(0)
+        _check(self._L.flint_dense_kernel_times(self._h, names, ms, cap, ctypes.byref(n)), "flint_dense_kernel_times")
+        return [(names[i].decode(), float(ms[i])) for i in range(n.value)]
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._L.flint_dense_destroy(self._h)
             self._h = None
 
     def __del__(self):

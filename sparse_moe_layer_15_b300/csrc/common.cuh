@@ -17,6 +17,10 @@ constexpr int E = 256;
 constexpr int K = 6;
 constexpr int I = 512;
 constexpr int IS = 1024;
+// The dense SwiGLU MLP layers before the MoE layers (serving-kit post, "The architecture, from
+// the config": mlp_only_layers [0, 1], about 75M parameters for the two) have this width:
+// 2 layers x 3 x 2048 x 6144 = 75.5M.  A dense layer runs as the shared-expert path alone.
+constexpr int ID = 6144;
 
 using bf16 = __nv_bfloat16;
 
@@ -32,6 +36,8 @@ struct Params {
   int T;                 // tokens in this call
   unsigned flags;        // FLINT_MOE_FLAG_*
   float rms_eps;
+  int sw;                // width of the shared expert: IS, or ID for a dense MLP layer
+  int dense;             // 1: a dense SwiGLU MLP layer (the shared-expert path alone; y = MLP(x') [+ x])
   const bf16* x;         // layer input [T][H]
   const bf16* xin;       // expert / router input: x, or rms(x) in xn
   bf16* y;               // output [T][H]
@@ -40,9 +46,9 @@ struct Params {
   const bf16* w_gate;    // [E][H][I]
   const bf16* w_up;      // [E][H][I]
   const bf16* w_down;    // [E][I][H]
-  const bf16* ws_gate;   // [H][IS]
-  const bf16* ws_up;     // [H][IS]
-  const bf16* ws_down;   // [IS][H]
+  const bf16* ws_gate;   // [H][sw]
+  const bf16* ws_up;     // [H][sw]
+  const bf16* ws_down;   // [sw][H]
   // workspace
   uint32_t* status;      // [1] device status word (ST_* bits)
   int32_t* counts;       // [E]
@@ -53,7 +59,7 @@ struct Params {
   float* topk_w;         // [T*K]
   bf16* xn;              // [T][H] rms-normalised input
   bf16* h;               // [T*K][I] routed SwiGLU activations, expert-sorted rows
-  bf16* hs;              // [T][IS] shared SwiGLU activations
+  bf16* hs;              // [T][sw] shared SwiGLU activations
   float* Y;              // [T*K][H] gated routed expert outputs
   float* S;              // [T][H] shared expert output
   float* P;              // [MAX_STREAM_CTAS][2][PSLOT] split-item partial sums (decode path)

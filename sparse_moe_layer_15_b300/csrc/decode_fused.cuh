@@ -142,6 +142,10 @@ static_assert(GU_KB <= 64 && SD_KB <= 64 && DN_KB <= 64, "an item's pieces fit t
 constexpr long long MAX_STEP_BLOCKS = (long long)max_groups_upto(STREAM_MAX_T) * GU_NCB * GU_KB +
                                       (long long)max_shared_groups_upto(STREAM_MAX_T) * SGU_NCB * GU_KB;
 static_assert(MAX_STEP_BLOCKS * (MAX_STREAM_CTAS + 1) < (1ll << 32), "32-bit range arithmetic");
+// a dense layer's step C (the largest of its two steps) stays below the MoE's
+static_assert((long long)max_shared_groups_upto(STREAM_MAX_T) * (ID / 128) * GU_KB <= MAX_STEP_BLOCKS,
+              "32-bit range arithmetic, dense layer");
+static_assert(ID / DN_ROWS <= 64, "a dense down item's pieces fit the slot list");
 
 __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
   uint32_t a = smem_u32(raw);
@@ -385,7 +389,9 @@ __device__ __forceinline__ int find_group_owner(const int* tgp, int n, int gi) {
 // Item numbering is token-group major for every kind (router: tg * 32 + row block; routed:
 // gi * chunks + c; shared: tg * chunks + c), so that consecutive items of a CTA's range
 // usually share their token group and its staged input rows.
-__device__ __forceinline__ Item decode_item(int T, const Meta& m, int kind, int idx) {
+// sncb: 128-column blocks of the shared expert's width (its gate/up items per token group, and
+// the K blocks of its down items).
+__device__ __forceinline__ Item decode_item(int T, int sncb, const Meta& m, int kind, int idx) {
   Item it;
   it.kind = kind;
   it.idx = idx;
@@ -401,14 +407,14 @@ __device__ __forceinline__ Item decode_item(int T, const Meta& m, int kind, int 
     it.nt = min(G, m.cnt[u] - tg * G);
     it.KB = kind == KIND_GU ? GU_KB : DN_KB;
   } else {
-    const int nch = kind == KIND_RT ? RT_NB : kind == KIND_SGU ? SGU_NCB : OUT_NCB;
+    const int nch = kind == KIND_RT ? RT_NB : kind == KIND_SGU ? sncb : OUT_NCB;
     const int tg = idx / nch;
     it.c = idx % nch;
     const int G = group_rows(T);
     it.e = -1;
     it.row0 = tg * G;
     it.nt = min(G, T - tg * G);
-    it.KB = kind == KIND_RT ? 1 : kind == KIND_SGU ? GU_KB : SD_KB;
+    it.KB = kind == KIND_RT ? 1 : kind == KIND_SGU ? GU_KB : sncb;
   }
   return it;
 }
@@ -437,7 +443,7 @@ __device__ void issue_block(const Params& p, const Meta& m, const StreamMaps& ma
                             uint8_t* stage, uint64_t* bar) {
   int kind, idx, kb;
   block_kind(L, b, kind, idx, kb);
-  const Item it = decode_item(p.T, m, kind, idx);
+  const Item it = decode_item(p.T, p.sw / 128, m, kind, idx);
   mbar_arrive_expect_tx(bar, BLK_BYTES);
   // gate/up: boxes [gate chunk 2c | gate 2c+1 | up 2c | up 2c+1] of 8 KB; down: [chunk 2c | 2c+1]
   // of 16 KB (64 columns each: the 128-byte swizzle span)
@@ -485,7 +491,7 @@ struct Stream {
   int b0, nb;      // this CTA's block range in the current step
   int ring;        // blocks streamed by this CTA before this step (ring position)
   int first_slot;  // trace slot stamped when the step's first block has arrived
-  int x_cls, x_row0;  // what the staged input rows hold (-1: nothing valid)
+  int x_cls, x_row0, x_k0;  // what the staged input rows hold (-1: nothing valid), from column x_k0
   uint8_t* sm;
   uint64_t* full;
   uint64_t* empty;
@@ -573,11 +579,19 @@ __device__ void item_epilogue(Stream& S, const Item& it, const float* vals) {
   const int nt = it.nt, c0 = it.c * 128;
   if (it.kind == KIND_GU || it.kind == KIND_SGU) {  // vals[t][256]: gate columns, then up columns
     bf16* dst = it.kind == KIND_GU ? p.h : p.hs;
-    const int ld = it.kind == KIND_GU ? I : IS;
+    const int ld = it.kind == KIND_GU ? I : p.sw;
     for (int q = threadIdx.x; q < nt * 128; q += NCONS) {
       const int t = q >> 7, j = q & 127;
       const float g = vals[t * 256 + j], u = vals[t * 256 + 128 + j];
       dst[(size_t)(it.row0 + t) * ld + c0 + j] = __float2bfloat16_rn(silu_f32(g) * u);
+    }
+  } else if (it.kind == KIND_SD && p.dense) {  // a dense layer's output: y = bf16(vals [+ x])
+    for (int q = threadIdx.x; q < nt * 128; q += NCONS) {
+      const int t = q >> 7, j = q & 127;
+      const size_t o = (size_t)(it.row0 + t) * H + c0 + j;
+      float v = vals[q];
+      if (p.flags & 2u) v += __bfloat162float(p.x[o]);  // residual
+      p.y[o] = __float2bfloat16_rn(v);
     }
   } else if (it.kind == KIND_SD) {  // vals[t][128]
     for (int q = threadIdx.x; q < nt * 128; q += NCONS) {
@@ -636,13 +650,16 @@ __device__ void combine_block(const Params& p, const uint16_t* inv, int cb) {
   for (int q = threadIdx.x; q < p.T * 16; q += NCONS) combine8(p, inv, q >> 4, cb * 128 + (q & 15) * 8);
 }
 
-// Stage the token group's input rows (bf16, row stride xlen + XPAD; rows nt .. G-1 zero) for an
-// item (consumers), unless they are the rows staged last (same source and group).
-__device__ void stage_inputs(Stream& S, const Item& it, int xlen) {
+// Stage the token group's input rows (bf16, columns [k0, k0 + xlen), row stride xlen + XPAD; rows
+// nt .. G-1 zero) for an item (consumers), unless they are the rows staged last (same source,
+// group and columns).  xlen <= H: a longer row (a dense layer's down input, 6144 wide) is staged
+// in windows.
+__device__ void stage_inputs(Stream& S, const Item& it, int xlen, int k0 = 0) {
   const int cls = it.kind == KIND_GU ? 1 : it.kind == KIND_SD ? 2 : it.kind == KIND_DN ? 3 : 0;
-  if (cls == S.x_cls && it.row0 == S.x_row0) return;
+  if (cls == S.x_cls && it.row0 == S.x_row0 && k0 == S.x_k0) return;
   S.x_cls = cls;
   S.x_row0 = it.row0;
+  S.x_k0 = k0;
   const Params& p = *S.p;
   bf16* xs = reinterpret_cast<bf16*>(S.sm + Smem::xs);
   const int cpr = xlen / 8;
@@ -657,7 +674,7 @@ __device__ void stage_inputs(Stream& S, const Item& it, int xlen) {
       else if (it.kind == KIND_SGU || it.kind == KIND_RT)
         src = p.xin + (size_t)(it.row0 + t) * H;
       else if (it.kind == KIND_SD)
-        src = p.hs + (size_t)(it.row0 + t) * IS;
+        src = p.hs + (size_t)(it.row0 + t) * p.sw + k0;
       else
         src = p.h + (size_t)(it.row0 + t) * I;
       v = __ldcg(reinterpret_cast<const uint4*>(src) + k8);
@@ -707,8 +724,11 @@ __device__ void run_router_block(Stream& S, const Item& it, int& j) {
 __device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, int& j) {
   const Params& p = *S.p;
   const bool gu = it.kind == KIND_GU || it.kind == KIND_SGU;
-  const int xlen = it.kind == KIND_SD ? IS : it.kind == KIND_DN ? I : H;
-  stage_inputs(S, it, xlen);
+  // a shared down input longer than a staged row (a dense layer) is staged from the segment's
+  // first K row, and restaged when the segment runs past the window
+  int k0 = (it.kind == KIND_SD && p.sw > H) ? kb_start * DN_ROWS : 0;
+  int xlen = it.kind == KIND_SD ? min(p.sw - k0, H) : it.kind == KIND_DN ? I : H;
+  stage_inputs(S, it, xlen, k0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j0 = j;
   const uint32_t xs = smem_u32(S.sm + Smem::xs);
@@ -744,9 +764,15 @@ __device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, i
     const uint32_t sub = uint32_t((warp >> 2) * (BLK_BYTES / 2));
     const int m0 = (warp & 3) * 16;
     for (int q = 0; q < nblk; ++q, ++j) {
+      const int kr = (kb_start + q) * DN_ROWS;  // first K row of this block
+      if (kr - k0 >= xlen) {  // past the staged window (dense layers only; warp-uniform, all warps)
+        csync();  // every warp is done with the window
+        k0 = kr;
+        xlen = min(p.sw - k0, H);
+        stage_inputs(S, it, xlen, k0);
+      }
       wait_full(S, j);
-      mma_tile(d, smem_u32(stage_ptr(S, j)) + sub, m0, 0, DN_ROWS / 16, xs, xlen + XPAD, (kb_start + q) * DN_ROWS,
-               two);
+      mma_tile(d, smem_u32(stage_ptr(S, j)) + sub, m0, 0, DN_ROWS / 16, xs, xlen + XPAD, kr - k0, two);
       release(S, j);
     }
     const int cb = (warp >> 2) * 64 + m0;
@@ -799,7 +825,7 @@ __device__ void consume(Stream& S) {
   while (j < S.nb) {
     int kind, idx, kb;
     block_kind(S.L, S.b0 + j, kind, idx, kb);
-    const Item it = decode_item(S.p->T, S.meta, kind, idx);  // shared-memory lookups only
+    const Item it = decode_item(S.p->T, S.p->sw / 128, S.meta, kind, idx);  // shared-memory lookups only
     if (kind == KIND_RT)
       run_router_block(S, it, j);
     else
@@ -811,6 +837,7 @@ __device__ void consume(Stream& S) {
 __device__ __forceinline__ void set_step(Stream& S, const BlockList& L) {
   S.L = L;
   S.x_cls = -1;  // the staging buffer was reused between steps
+  S.x_k0 = 0;
   S.b0 = range_begin(L.n_total, S.nctas, blockIdx.x);
   S.nb = range_begin(L.n_total, S.nctas, blockIdx.x + 1) - S.b0;
 }
@@ -1061,8 +1088,48 @@ __device__ Meta build_tables(const Params& p, uint8_t* sm, uint16_t* perm, uint1
   return m;
 }
 
+// A dense SwiGLU MLP layer (p.dense, width p.sw = ID): the shared-expert steps alone -- step C
+// the gate/up of the whole width, a barrier, step D the down projection, whose items write
+// y = bf16(MLP(x') [+ x]) directly (no router, no routing, no combine).
+__device__ void dense_layer(Stream& S, const Params& p, int ntg) {
+  const int sncb = p.sw / 128;
+  {
+    BlockList L;
+    L.k_first = L.k_second = KIND_SGU;
+    L.kb_first = L.kb_second = GU_KB;
+    L.n_first = 0;
+    L.n_total = ntg * sncb * GU_KB;
+    S.first_slot = 12;
+    trace_point(p, 6);
+    set_step(S, L);
+    run_step(S);
+  }
+  trace_point(p, 7);
+  {
+    BlockList L;
+    L.k_first = L.k_second = KIND_SD;
+    L.kb_first = L.kb_second = sncb;
+    L.n_first = 0;
+    L.n_total = ntg * OUT_NCB * sncb;
+    set_step(S, L);
+  }
+  const int pre = p.T <= PREISSUE_MAX_T ? min(1, S.nb) : 0;
+  if (threadIdx.x == NCONS) produce(S, 0, pre);
+  if (!grid_sync(p, 1, S.misc + 12)) {
+    drain_issued(S, pre);
+    return;
+  }
+  trace_point(p, 8);
+  S.first_slot = 13;
+  run_step(S, pre);
+  trace_point(p, 9);
+  grid_done(p, S.misc + 13);
+  trace_point(p, 10);
+}
+
 // ================================================================ the fused decode kernel
-// mode 0: the whole layer; mode 1: routing only (router, top-K, counts).
+// mode 0: the whole layer; mode 1: routing only (router, top-K, counts); a dense layer
+// (p.dense) runs dense_layer instead.
 __global__ void __launch_bounds__(NTHREADS, 1)
     decode_fused(const __grid_constant__ Params p, const __grid_constant__ StreamMaps maps, int mode) {
   extern __shared__ uint8_t smem_raw[];
@@ -1104,6 +1171,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   pdl_wait();  // inputs of this forward and the workspace are ready
   trace_point(p, 1);
   if ((p.flags & FLAG_TEST_WAIT_TIMEOUT) && blockIdx.x == 0 && threadIdx.x == 0) test_wait_timeout(p.status);
+  if (p.dense) {
+    dense_layer(S, p, ntg);
+    return;
+  }
 
   // ---- step A: router partial logits.  (The shared expert runs in steps C and D, beside the
   // routed experts: its blocks stream from L2 while the routed ones stream from HBM, and a

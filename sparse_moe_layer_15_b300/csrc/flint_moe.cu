@@ -36,7 +36,9 @@ struct Layout {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-Layout make_layout(int max_tokens) {
+// sw: the shared expert's width (IS), or a dense layer's (ID, with dense = true: no routed
+// scratch).
+Layout make_layout(int max_tokens, int sw = IS, bool dense = false) {
   Layout L{};
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -52,7 +54,7 @@ Layout make_layout(int max_tokens) {
   L.bar_count = take(sizeof(uint32_t));
   L.bar_done = take(sizeof(uint32_t));
   L.tk_gu = take(sizeof(uint32_t) * G * GU_NCB);
-  L.tk_sgu = take(sizeof(uint32_t) * Gs * SGU_NCB);
+  L.tk_sgu = take(sizeof(uint32_t) * Gs * (sw / 128));
   L.tk_sd = take(sizeof(uint32_t) * Gs * OUT_NCB);
   L.tk_dn = take(sizeof(uint32_t) * G * OUT_NCB);
   L.tk_comb = take(sizeof(uint32_t) * OUT_NCB);
@@ -67,12 +69,12 @@ Layout make_layout(int max_tokens) {
   L.xstage = take(sizeof(uint16_t) * T * H);
   L.ystage = take(sizeof(uint16_t) * T * H);
   L.h = take(sizeof(uint16_t) * T * K * I);
-  L.hs = take(sizeof(uint16_t) * T * IS);
+  L.hs = take(sizeof(uint16_t) * T * sw);
   L.S = take(sizeof(float) * T * H);
   L.Y = take(sizeof(float) * (size_t)Ts * K * H);
   L.P = take(sizeof(float) * MAX_STREAM_CTAS * 2 * PSLOT);
   L.RP = take(sizeof(float) * RT_NB * STREAM_MAX_T * E);
-  if (max_tokens > STREAM_MAX_T) {
+  if (max_tokens > STREAM_MAX_T && !dense) {
     const size_t ntile = (T + tc::TM - 1) / tc::TM;
     L.xs = take(sizeof(uint16_t) * T * K * H);
     L.Yb = take(sizeof(uint16_t) * T * K * H);
@@ -130,6 +132,8 @@ struct flint_moe_stack_s {
 struct flint_moe_s {
   flint_moe_config cfg;
   flint_moe_weights w;
+  int sw;      // the shared expert's width (IS), or the dense layer's (ID)
+  int dense;   // 1: a dense SwiGLU MLP layer (flint_dense_*): the shared-expert path alone
   int device;
   int n_sm;
   uint8_t* ws;
@@ -166,6 +170,8 @@ Params make_params(flint_moe_t h, const void* x, int T, void* y, int32_t* out_id
   p.T = T;
   p.flags = h->cfg.flags;
   p.rms_eps = h->cfg.rms_eps;
+  p.sw = h->sw;
+  p.dense = h->dense;
   p.x = static_cast<const bf16*>(x);
   p.xn = reinterpret_cast<bf16*>(ws + L.xn);
   p.xin = (h->cfg.flags & FLINT_MOE_FLAG_PRE_RMSNORM) ? p.xn : p.x;
@@ -278,6 +284,14 @@ flint_moe_status run_prefill(flint_moe_t h, const Params& p, cudaStream_t st, bo
         make_map(&xin_c, p.x, (uint64_t)T, H, 64, tc::XC_ROWS, CU_TENSOR_MAP_SWIZZLE_128B)))
     return FLINT_MOE_ERR_CUDA;
   const int n_sm = h->n_sm;
+  if (h->dense) {  // the shared-expert GEMMs alone; the down epilogue writes y
+    pf::GateUpTC gu{p, h->pmaps.xs, xin_c, h->pmaps.wg, h->pmaps.wu, h->pmaps.wsg, h->pmaps.wsu};
+    e = launch(h, "pf_gateup", tc::gemm_kernel<pf::GateUpTC>, n_sm, tc::NUM_THREADS, tc::SMEM_BYTES, st, false, gu);
+    pf::DownTC dn{p, h->pmaps.h, h->pmaps.wd, h->pmaps.hs, h->pmaps.wsd};
+    if (e == cudaSuccess)
+      e = launch(h, "pf_down", tc::gemm_kernel<pf::DownTC>, n_sm, tc::NUM_THREADS, tc::SMEM_BYTES, st, false, dn);
+    return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ERR_CUDA;
+  }
   pf::RouterTC r{p, xin, h->pmaps.wr};
   e = launch(h, "pf_router", tc::gemm_kernel<pf::RouterTC>, ntile < n_sm ? ntile : n_sm, tc::NUM_THREADS,
              tc::SMEM_BYTES, st, false, r);
@@ -320,6 +334,13 @@ bool make_prefill_maps(flint_moe_t h) {
   const flint_moe_weights* w = &h->w;
   const uint64_t T = (uint64_t)h->cfg.max_tokens;
   pf::Maps& m = h->pmaps;
+  const uint64_t S = (uint64_t)h->sw;
+  if (h->dense)
+    return make_map(&m.xin, h->ws + h->L.xn, T, H, 64, tc::TM, sw) &&
+           make_map(&m.xin_c, h->ws + h->L.xn, T, H, 64, tc::XC_ROWS, sw) &&
+           make_map(&m.hs, h->ws + h->L.hs, T, S, 64, tc::XC_ROWS, sw) &&
+           make_map(&m.wsg, w->ws_gate, H, S, 64, tc::TK, sw) && make_map(&m.wsu, w->ws_up, H, S, 64, tc::TK, sw) &&
+           make_map(&m.wsd, w->ws_down, S, H, 64, tc::TK, sw);
   return make_map(&m.xin, h->ws + h->L.xn, T, H, 64, tc::TM, sw) &&
          make_map(&m.xin_c, h->ws + h->L.xn, T, H, 64, tc::XC_ROWS, sw) &&
          make_map(&m.xs, h->ws + h->L.xs, T * K, H, 64, tc::XC_ROWS, sw) &&
@@ -370,19 +391,15 @@ flint_moe_status flint_moe_workspace_bytes(const flint_moe_config* cfg, size_t* 
   return FLINT_MOE_OK;
 }
 
-flint_moe_status flint_moe_create(const flint_moe_config* cfg, const flint_moe_weights* w, void* workspace,
-                                  size_t workspace_bytes, flint_moe_t* out) {
-  if (!out) return FLINT_MOE_ERR_INVALID_ARG;
-  *out = nullptr;
-  flint_moe_status s = check_config(cfg);
-  if (s != FLINT_MOE_OK) return s;
-  if (!w || !w->w_router || !w->w_gate || !w->w_up || !w->w_down || !w->ws_gate || !w->ws_up || !w->ws_down)
-    return FLINT_MOE_ERR_INVALID_ARG;
-  const void* ptrs[] = {w->w_router, w->w_gate, w->w_up, w->w_down, w->ws_gate, w->ws_up, w->ws_down};
-  for (const void* q : ptrs)
-    if (!aligned16(q)) return FLINT_MOE_ERR_INVALID_ARG;
-  if (w->router_bias && (reinterpret_cast<uintptr_t>(w->router_bias) & 3u)) return FLINT_MOE_ERR_INVALID_ARG;
-  Layout L = make_layout(cfg->max_tokens);
+}  // extern "C"
+
+namespace {
+
+// A handle on validated arguments: the MoE layer (sw = IS, dense = false; every weight pointer
+// set) or a dense layer (sw = ID, dense = true; only the shared-expert pointers of `w` are used).
+flint_moe_status create_handle(const flint_moe_config* cfg, const flint_moe_weights* w, void* workspace,
+                               size_t workspace_bytes, int swidth, bool dense, flint_moe_t* out) {
+  Layout L = make_layout(cfg->max_tokens, swidth, dense);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < L.total)
     return FLINT_MOE_ERR_WORKSPACE;
   int dev = 0;
@@ -397,6 +414,8 @@ flint_moe_status flint_moe_create(const flint_moe_config* cfg, const flint_moe_w
   if (!h) return FLINT_MOE_ERR_CUDA;
   h->cfg = *cfg;
   h->w = *w;
+  h->sw = swidth;
+  h->dense = dense ? 1 : 0;
   h->device = dev;
   h->ws = static_cast<uint8_t*>(workspace);
   h->ws_bytes = workspace_bytes;
@@ -411,20 +430,23 @@ flint_moe_status flint_moe_create(const flint_moe_config* cfg, const flint_moe_w
     return FLINT_MOE_ERR_CUDA;
   }
   const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
-  bool ok = make_map(&h->smaps.wr, w->w_router, H, E, 64, RT_ROWS, sw) &&
-            make_map(&h->smaps.wg, w->w_gate, (uint64_t)E * H, I, 64, GU_ROWS, sw) &&
-            make_map(&h->smaps.wu, w->w_up, (uint64_t)E * H, I, 64, GU_ROWS, sw) &&
-            make_map(&h->smaps.wd, w->w_down, (uint64_t)E * I, H, 64, DN_ROWS, sw) &&
-            make_map(&h->smaps.wsg, w->ws_gate, H, IS, 64, GU_ROWS, sw) &&
-            make_map(&h->smaps.wsu, w->ws_up, H, IS, 64, GU_ROWS, sw) &&
-            make_map(&h->smaps.wsd, w->ws_down, IS, H, 64, DN_ROWS, sw);
-  if (ok && L.Yb) ok = make_prefill_maps(h);
+  const uint64_t S = (uint64_t)swidth;
+  bool ok = make_map(&h->smaps.wsg, w->ws_gate, H, S, 64, GU_ROWS, sw) &&
+            make_map(&h->smaps.wsu, w->ws_up, H, S, 64, GU_ROWS, sw) &&
+            make_map(&h->smaps.wsd, w->ws_down, S, H, 64, DN_ROWS, sw);
+  if (ok && !dense)
+    ok = make_map(&h->smaps.wr, w->w_router, H, E, 64, RT_ROWS, sw) &&
+         make_map(&h->smaps.wg, w->w_gate, (uint64_t)E * H, I, 64, GU_ROWS, sw) &&
+         make_map(&h->smaps.wu, w->w_up, (uint64_t)E * H, I, 64, GU_ROWS, sw) &&
+         make_map(&h->smaps.wd, w->w_down, (uint64_t)E * I, H, 64, DN_ROWS, sw);
+  const bool prefill = cfg->max_tokens > STREAM_MAX_T;
+  if (ok && prefill) ok = make_prefill_maps(h);
   if (!ok) {
     delete h;
     return FLINT_MOE_ERR_CUDA;
   }
   cudaError_t e = cudaFuncSetAttribute(decode_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, FUSED_SMEM);
-  if (e == cudaSuccess && L.Yb) e = set_prefill_smem();
+  if (e == cudaSuccess && prefill) e = set_prefill_smem();
   int per_sm = 0;
   if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused, NTHREADS, FUSED_SMEM);
   if (e == cudaSuccess && per_sm < 1) e = cudaErrorCooperativeLaunchTooLarge;
@@ -436,6 +458,25 @@ flint_moe_status flint_moe_create(const flint_moe_config* cfg, const flint_moe_w
   }
   *out = h;
   return FLINT_MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+flint_moe_status flint_moe_create(const flint_moe_config* cfg, const flint_moe_weights* w, void* workspace,
+                                  size_t workspace_bytes, flint_moe_t* out) {
+  if (!out) return FLINT_MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  flint_moe_status s = check_config(cfg);
+  if (s != FLINT_MOE_OK) return s;
+  if (!w || !w->w_router || !w->w_gate || !w->w_up || !w->w_down || !w->ws_gate || !w->ws_up || !w->ws_down)
+    return FLINT_MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {w->w_router, w->w_gate, w->w_up, w->w_down, w->ws_gate, w->ws_up, w->ws_down};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return FLINT_MOE_ERR_INVALID_ARG;
+  if (w->router_bias && (reinterpret_cast<uintptr_t>(w->router_bias) & 3u)) return FLINT_MOE_ERR_INVALID_ARG;
+  return create_handle(cfg, w, workspace, workspace_bytes, IS, false, out);
 }
 
 flint_moe_status flint_moe_route(flint_moe_t h, const void* x, int T, int32_t* topk_idx, float* topk_w,
@@ -758,6 +799,8 @@ extern "C" flint_moe_status flint_moe_forward_noalloc(const flint_moe_weights* w
   flint_moe_s h{};  // a handle on the stack: no host or device allocation
   h.cfg = flint_moe_config{H, E, K, I, IS, NOALLOC_MAX_T, 0u, 1e-6f};
   h.w = *w;
+  h.sw = IS;
+  h.dense = 0;
   h.device = dev;
   h.n_sm = n_sm;
   h.ws = static_cast<uint8_t*>(scratch);
@@ -803,3 +846,94 @@ extern "C" flint_moe_status flint_moe_noalloc_poll_device_status(flint_stream_t 
   if (cudaMemset(ws + L.status, 0, L.zero_end - L.status) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
   return (word & ST_TIMEOUT) ? FLINT_MOE_ERR_DEVICE_TIMEOUT : FLINT_MOE_ERR_DEVICE_BOUNDS;
 }
+
+// ------------------------------------------------------------------------------------------
+// The dense SwiGLU MLP layers (serving-kit post, "The architecture, from the config": the
+// model's first two layers are dense MLP layers, mlp_only_layers [0, 1], about 75M parameters
+// for the two, i.e. width 6144).  A dense layer is run as the MoE layer's shared-expert path
+// alone, at width ID: the decode-size kernel's shared gate/up and down steps up to 256 tokens,
+// the tensor-core path's shared gate/up and down tiles above.
+struct flint_dense_s {
+  flint_moe_t h;
+};
+
+namespace {
+
+flint_moe_status check_dense_config(const flint_dense_config* c) {
+  if (!c) return FLINT_MOE_ERR_INVALID_ARG;
+  if (c->hidden != H || c->inter != ID) return FLINT_MOE_ERR_UNSUPPORTED;
+  if (c->max_tokens < 1 || c->max_tokens > MAX_TOKENS_LIMIT) return FLINT_MOE_ERR_INVALID_ARG;
+  if (c->flags & ~(FLINT_MOE_FLAG_PRE_RMSNORM | FLINT_MOE_FLAG_RESIDUAL | FLINT_MOE_FLAG_TEST_WAIT_TIMEOUT))
+    return FLINT_MOE_ERR_UNSUPPORTED;
+  if ((c->flags & FLINT_MOE_FLAG_PRE_RMSNORM) && !(c->rms_eps > 0.f)) return FLINT_MOE_ERR_INVALID_ARG;
+  return FLINT_MOE_OK;
+}
+
+flint_moe_config moe_config_of(const flint_dense_config* c) {
+  return flint_moe_config{H, E, K, I, IS, c->max_tokens, c->flags, c->rms_eps};
+}
+
+}  // namespace
+
+extern "C" {
+
+flint_moe_status flint_dense_workspace_bytes(const flint_dense_config* cfg, size_t* bytes) {
+  const flint_moe_status s = check_dense_config(cfg);
+  if (s != FLINT_MOE_OK) return s;
+  if (!bytes) return FLINT_MOE_ERR_INVALID_ARG;
+  *bytes = make_layout(cfg->max_tokens, ID, true).total;
+  return FLINT_MOE_OK;
+}
+
+flint_moe_status flint_dense_create(const flint_dense_config* cfg, const flint_dense_weights* w, void* workspace,
+                                    size_t workspace_bytes, flint_dense_t* out) {
+  if (!out) return FLINT_MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  flint_moe_status s = check_dense_config(cfg);
+  if (s != FLINT_MOE_OK) return s;
+  if (!w || !w->w_gate || !w->w_up || !w->w_down) return FLINT_MOE_ERR_INVALID_ARG;
+  if (!aligned16(w->w_gate) || !aligned16(w->w_up) || !aligned16(w->w_down)) return FLINT_MOE_ERR_INVALID_ARG;
+  flint_moe_weights mw{};
+  mw.ws_gate = w->w_gate;
+  mw.ws_up = w->w_up;
+  mw.ws_down = w->w_down;
+  const flint_moe_config mc = moe_config_of(cfg);
+  flint_dense_s* d = new (std::nothrow) flint_dense_s();
+  if (!d) return FLINT_MOE_ERR_CUDA;
+  s = create_handle(&mc, &mw, workspace, workspace_bytes, ID, true, &d->h);
+  if (s != FLINT_MOE_OK) {
+    delete d;
+    return s;
+  }
+  *out = d;
+  return FLINT_MOE_OK;
+}
+
+flint_moe_status flint_dense_forward(flint_dense_t d, const void* x, int T, void* y, flint_stream_t stream) {
+  if (!d) return FLINT_MOE_ERR_INVALID_ARG;
+  return flint_moe_forward(d->h, x, T, y, nullptr, nullptr, stream);
+}
+
+flint_moe_status flint_dense_poll_device_status(flint_dense_t d, flint_stream_t stream) {
+  if (!d) return FLINT_MOE_ERR_INVALID_ARG;
+  return flint_moe_poll_device_status(d->h, stream);
+}
+
+flint_moe_status flint_dense_enable_kernel_timing(flint_dense_t d, int enable) {
+  if (!d) return FLINT_MOE_ERR_INVALID_ARG;
+  return flint_moe_enable_kernel_timing(d->h, enable);
+}
+
+flint_moe_status flint_dense_kernel_times(flint_dense_t d, const char** names, float* ms, int cap, int* n) {
+  if (!d) return FLINT_MOE_ERR_INVALID_ARG;
+  return flint_moe_kernel_times(d->h, names, ms, cap, n);
+}
+
+flint_moe_status flint_dense_destroy(flint_dense_t d) {
+  if (!d) return FLINT_MOE_ERR_INVALID_ARG;
+  flint_moe_destroy(d->h);
+  delete d;
+  return FLINT_MOE_OK;
+}
+
+}  // extern "C"

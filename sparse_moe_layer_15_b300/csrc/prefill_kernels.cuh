@@ -33,7 +33,7 @@ using tc::epi_sync;
 
 constexpr int RG = 2 * TM;        // rows per COLUMNS tile (the MMA's N <= 256)
 constexpr int NCT_GU = I / 64;    // 8 column pairs (64 of gate | 64 of up) of a routed gate/up
-constexpr int NCT_SGU = IS / 64;  // 16 column pairs of the shared gate/up
+// (the shared gate/up has p.sw / 64 column pairs: 16 for the MoE's shared expert, 96 for a dense layer)
 constexpr int NCT_DN = H / 128;   // 16 output column blocks of a down projection
 
 struct Maps {
@@ -41,14 +41,14 @@ struct Maps {
   CUtensorMap xin_c;  // [T][H], box 64 x 64 (shared gate/up, COLUMNS tiles)
   CUtensorMap xs;   // [6 max_T][H], box 64 x 64 (routed gate/up, COLUMNS tiles)
   CUtensorMap h;    // [6 max_T][I], box 64 x 64 (COLUMNS tiles)
-  CUtensorMap hs;   // [max_T][IS], box 64 x 64 (COLUMNS tiles)
+  CUtensorMap hs;   // [max_T][sw], box 64 x 64 (COLUMNS tiles)
   CUtensorMap wr;   // [H][E], box 64 x 64 (B operand)
   CUtensorMap wg;   // [E H][I], box 64 x 64
   CUtensorMap wu;
   CUtensorMap wd;   // [E I][H], box 64 x 64
-  CUtensorMap wsg;  // [H][IS], box 64 x 64
+  CUtensorMap wsg;  // [H][sw], box 64 x 64
   CUtensorMap wsu;
-  CUtensorMap wsd;  // [IS][H], box 64 x 64
+  CUtensorMap wsd;  // [sw][H], box 64 x 64
 };
 
 __device__ __forceinline__ void store_bf16x32(bf16* dst, const float* v) {
@@ -294,14 +294,15 @@ __global__ void __launch_bounds__(256) scatter_kernel(const __grid_constant__ Pa
 }
 
 // Routing tables of the grouped GEMMs, copied to shared memory by every CTA: mtp[0..E] (prefix
-// over the experts of their RG-row group counts), offsets[0..E].
+// over the experts of their RG-row group counts), offsets[0..E].  A dense layer has no routed
+// rows: all zero.
 struct GroupTable {
   __device__ static void load(const Params& p, uint8_t* tbl) {
     int* mtp = reinterpret_cast<int*>(tbl);
     int* off = mtp + (E + 1);
     for (int i = threadIdx.x; i <= E; i += blockDim.x) {
-      mtp[i] = __ldcg(p.mtp + i);
-      off[i] = __ldcg(p.offsets + i);
+      mtp[i] = p.dense ? 0 : __ldcg(p.mtp + i);
+      off[i] = p.dense ? 0 : __ldcg(p.offsets + i);
     }
   }
   // expert whose tile range [per * mtp[e], per * mtp[e+1]) holds tile i
@@ -342,7 +343,7 @@ struct GateUpTC {
   __device__ void prologue(uint8_t* tbl) const { GroupTable::load(p, tbl); }
   __device__ int num_tiles(const uint8_t* tbl) const {
     const int* mtp = reinterpret_cast<const int*>(tbl);
-    return NCT_GU * mtp[E] + NCT_SGU * ((p.T + RG - 1) / RG);
+    return NCT_GU * mtp[E] + (p.sw / 64) * ((p.T + RG - 1) / RG);
   }
   __device__ int kblocks() const { return H / tc::TK; }
   __device__ uint32_t* status() const { return p.status; }
@@ -392,7 +393,7 @@ struct GateUpTC {
     const int q0 = gate_lane ? 0 : 16;  // rows of the chunk this lane writes
     float* give = xch + (gate_lane ? 1024 : 0) + f;
     const float* take = xch + (gate_lane ? 0 : 1024) + f;
-    const int ld = t.aux ? IS : I;
+    const int ld = t.aux ? p.sw : I;
     bf16* dst = (t.aux ? p.hs : p.h) + (size_t)t.row0 * ld + t.col0 + f;
 #pragma unroll 1
     for (int c = 0; c * 32 < t.valid; ++c) {
@@ -457,13 +458,29 @@ struct DownTC {
       t.valid = min(RG, p.T - g * RG);
       t.col0 = nt * 128;
       t.aux = -1;
-      t.nkb = IS / tc::TK;
+      t.nkb = p.sw / tc::TK;
     }
     t.bcol[0] = t.col0;
     t.bcol[1] = t.col0 + 64;
     t.n = (t.valid + 15) & ~15;
   }
   __device__ void epilogue(const TileInfo& t, uint32_t trow, int row, uint8_t* epi, const uint8_t*) const {
+    if (t.aux < 0 && p.dense) {  // a dense layer's output: y = bf16(acc [+ x])
+      const size_t o = (size_t)t.row0 * H + t.col0 + row;
+#pragma unroll 1
+      for (int c = 0; c * 32 < t.valid; ++c) {
+        float v[32];
+        tmem_ld32(trow + uint32_t(c * 32), v);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          if (c * 32 + q >= t.valid) continue;
+          const size_t oq = o + (size_t)(c * 32 + q) * H;
+          const float r = (p.flags & 2u) ? __bfloat162float(p.x[oq]) : 0.f;  // residual
+          p.y[oq] = __float2bfloat16_rn(v[q] + r);
+        }
+      }
+      return;
+    }
     if (t.aux < 0) {
       float* dst = p.S + (size_t)t.row0 * H + t.col0 + row;
 #pragma unroll 1

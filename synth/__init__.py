@@ -48,6 +48,9 @@ TAG_SGATE = 7
 TAG_SUP = 8
 TAG_SDOWN = 9
 TAG_PERM = 10
+TAG_DGATE = 11  # dense MLP layers
+TAG_DUP = 12
+TAG_DDOWN = 13
 
 _MASK = (1 << 64) - 1
 
@@ -226,6 +229,16 @@ def flint_weights(seed: int, device="cuda", bias: str | None = None, bias_seed: 
     elif bias is not None:
         raise ValueError(bias)
     return w
+
+
+DENSE_SHAPES = {"w_gate": (2048, 6144), "w_up": (2048, 6144), "w_down": (6144, 2048)}
+_DENSE_TAGS = {"w_gate": TAG_DGATE, "w_up": TAG_DUP, "w_down": TAG_DDOWN}
+
+
+def dense_weights(seed: int, device="cuda"):
+    """A dense SwiGLU MLP layer's weights (width 6144), bf16 ~N(0, 0.02^2) like the experts'."""
+    return {name: torch_normal_bf16(shape, seed, _DENSE_TAGS[name], SIGMA_EXPERT, device=device)
+            for name, shape in DENSE_SHAPES.items()}
 
 
 def adversarial_sets(seed: int = 5):

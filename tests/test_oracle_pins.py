@@ -449,3 +449,25 @@ def test_flop_and_byte_formulas():
     assert acc.touched_weight_bytes(6) == 6 * 6_291_456 + 12_582_912 + 1_048_576
     assert acc.layer_weight_bytes() == 1_624_244_224
     assert abs(acc.expected_touched_experts(16) - 80.8) < 0.05
+
+
+# ---------------------------------------------------------------- dense MLP layers
+
+def test_dense_layer_real_width_matches_textbook_swiglu_torch():
+    # The dense layers' width 6144 (2 x 3 x 2048 x 6144 = 75.5M parameters, the pages' "about
+    # 75M" for the two), against torch's silu on the same bf16 weights, and not the swapped
+    # gate/up.
+    H, Id = 2048, 6144
+    wg = bf16((H, Id), 3, synth.TAG_DGATE, 0.02)
+    wu = bf16((H, Id), 3, synth.TAG_DUP, 0.02)
+    wd = bf16((Id, H), 3, synth.TAG_DDOWN, 0.02)
+    x = x_rows(3, H, seed=17)
+    y = oracle.dense(x, wg, wu, wd, nthreads=2)
+    X = torch.from_numpy(x)
+    F = torch.nn.functional
+    G, U, D = (torch.from_numpy(f64(a)) for a in (wg, wu, wd))
+    ref = (F.silu(X @ G) * (X @ U)) @ D
+    np.testing.assert_allclose(y, ref.numpy(), rtol=1e-11, atol=1e-13)
+    swapped = (F.silu(X @ U) * (X @ G)) @ D
+    assert np.max(np.abs(y - swapped.numpy())) > 1e-3
+    assert 2 * (3 * H * Id) == 75_497_472
