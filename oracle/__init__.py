@@ -59,6 +59,8 @@ def _lib():
         L.oracle_rmsnorm.restype = None
         L.oracle_round_bf16.argtypes = [ctypes.c_double]
         L.oracle_round_bf16.restype = ctypes.c_double
+        L.oracle_swa_decode.argtypes = [_P, _P, _P, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, _P]
         L.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
         L.oracle_bf16_to_f64.restype = ctypes.c_double
         _LIB = L
@@ -280,4 +282,33 @@ def prenorm_residual(layer: Layer, x, eps, nthreads: int = 1):
     out = forward(layer, r, nthreads=nthreads)
     out["y"] = x + out["y"]
     out["r"] = r
+    return out
+
+
+def swa_decode(q, k, v, sinks, pos, nthreads: int = 1):
+    """Sliding-window decode attention with per-head sinks (oracle_swa_decode): q [B,nh,d],
+    k, v [B,W,nkv,d] (bf16 bits, uint16), sinks [nh] fp32, pos [B] int32 -> out [B,nh,d]
+    float64.  ``nthreads`` > 1 evaluates disjoint batch ranges concurrently."""
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    sinks = np.ascontiguousarray(sinks, dtype=np.float32)
+    pos = np.ascontiguousarray(pos, dtype=np.int32)
+    B, nh, d = q.shape
+    W, nkv = k.shape[1], k.shape[2]
+    out = np.empty((B, nh, d))
+    L = _lib()
+
+    def run(a, b):
+        if b <= a:
+            return 0
+        return L.oracle_swa_decode(_ptr(q[a:b]), _ptr(k[a:b]), _ptr(v[a:b]), _ptr(sinks), _ptr(pos[a:b]), b - a, nh,
+                                   nkv, d, W, _ptr(out[a:b]))
+
+    parts = _split(B, nthreads)
+    if len(parts) <= 1:
+        rcs = [run(0, B)]
+    else:
+        with ThreadPoolExecutor(len(parts)) as ex:
+            rcs = list(ex.map(lambda ab: run(*ab), parts))
+    for rc in rcs:
+        _check(rc, "swa_decode")
     return out

@@ -262,3 +262,44 @@ void oracle_rmsnorm(const double* x, int T, int H, double eps, double* r) {
     for (int h = 0; h < H; ++h) r[(size_t)t * H + h] = xt[h] / d;
   }
 }
+
+/* Decode attention with a learned sink per head, over each sequence's ring of W cached tokens. */
+int oracle_swa_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* sinks,
+                      const int32_t* pos, int B, int nh, int nkv, int d, int W, double* out) {
+  if (!q || !k || !v || !sinks || !pos || !out || B < 0 || nh <= 0 || nkv <= 0 || nh % nkv || d <= 0 || W <= 0)
+    return ORACLE_EINVAL;
+  const int group = nh / nkv;
+  const double scale = 1.0 / sqrt((double)d);
+  double* s = (double*)malloc(sizeof(double) * (size_t)W);
+  if (!s) return ORACLE_EINVAL;
+  for (int b = 0; b < B; ++b) {
+    if (pos[b] < 0) {
+      free(s);
+      return ORACLE_EINVAL;
+    }
+    const int n = pos[b] + 1 < W ? pos[b] + 1 : W;
+    for (int h = 0; h < nh; ++h) {
+      const int g = h / group;
+      const uint16_t* qh = q + ((size_t)b * nh + h) * d;
+      double m = (double)sinks[h];
+      for (int j = 0; j < n; ++j) {
+        const uint16_t* kj = k + (((size_t)b * W + j) * nkv + g) * d;
+        double dot = 0.0;
+        for (int i = 0; i < d; ++i) dot += oracle_bf16_to_f64(qh[i]) * oracle_bf16_to_f64(kj[i]);
+        s[j] = dot * scale;
+        if (s[j] > m) m = s[j];
+      }
+      double den = exp((double)sinks[h] - m);
+      for (int j = 0; j < n; ++j) den += exp(s[j] - m);
+      double* o = out + ((size_t)b * nh + h) * d;
+      for (int i = 0; i < d; ++i) o[i] = 0.0;
+      for (int j = 0; j < n; ++j) {
+        const double p = exp(s[j] - m) / den;
+        const uint16_t* vj = v + (((size_t)b * W + j) * nkv + g) * d;
+        for (int i = 0; i < d; ++i) o[i] += p * oracle_bf16_to_f64(vj[i]);
+      }
+    }
+  }
+  free(s);
+  return ORACLE_OK;
+}

@@ -92,6 +92,22 @@ double oracle_round_bf16(double v);
 /* r[t] = x[t] / sqrt(mean_h x[t][h]^2 + eps)  (unit weight). */
 void oracle_rmsnorm(const double* x, int T, int H, double eps, double* r);
 
+/* Decode attention of one sliding-window layer (serving-kit post, "The architecture, from the
+ * config": 32 query heads, 4 KV heads, head dimension 128; sliding-window layers attend to a
+ * 513-token window, the current token plus 512 back; learned per-head attention sinks; news
+ * article "Recursive opens Flint, a 40B coding model with 2.5B active", section "What runs on
+ * each token": a sink is a slot that can take attention no real token needs).  Readings: the
+ * sink of head h is a logit that joins the softmax denominator and carries no value; scores
+ * are q.k / sqrt(head_dim); query head h reads KV head h / (n_heads / n_kv); q and k arrive
+ * normalised and rotated (the per-head QK RMSNorm and RoPE belong to the projections).
+ * The cache of each sequence is a ring of W slots holding its last W tokens (position p in
+ * slot p mod W); with pos[b] the position of the sequence's current token (its K and V
+ * already stored), the valid slots are 0 .. min(pos[b] + 1, W) - 1.
+ *   q [B][nh][d], k, v [B][W][nkv][d] (bf16 bits), sinks [nh], pos [B]; out [B][nh][d]:
+ *   out[b][h] = sum_j e^(s_j - m) v_j / (e^(sink_h - m) + sum_j e^(s_j - m)), m = max(sink_h, s_j). */
+int oracle_swa_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* sinks,
+                      const int32_t* pos, int B, int nh, int nkv, int d, int W, double* out);
+
 #ifdef __cplusplus
 }
 #endif

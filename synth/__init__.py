@@ -51,6 +51,10 @@ TAG_PERM = 10
 TAG_DGATE = 11  # dense MLP layers
 TAG_DUP = 12
 TAG_DDOWN = 13
+TAG_Q = 14  # sliding-window decode attention
+TAG_K = 15
+TAG_V = 16
+TAG_SINK = 17
 
 _MASK = (1 << 64) - 1
 
@@ -263,3 +267,24 @@ def weights_to_host(w, experts=None):
     b = w.get("router_bias")
     out["router_bias"] = None if b is None else b.detach().float().cpu().numpy()
     return out
+
+
+# --------------------------------------------------------------------------------------
+# Sliding-window decode attention inputs: 32 query heads, 4 KV heads, head dimension 128, a ring
+# of 513 cached tokens per sequence.  q and k rows ~N(0, 1) (what a per-head RMSNorm leaves),
+# v ~N(0, 1), one sink logit per head ~N(0, 1) (bf16-valued fp32), and a length mix: the current
+# token's position cycles through SWA_POSITIONS, so some sequences are shorter than the window
+# (0, 17, 511 tokens back) and the rest fill it.
+SWA_HEADS, SWA_KV_HEADS, SWA_HEAD_DIM, SWA_WINDOW = 32, 4, 128, 513
+SWA_POSITIONS = (4095, 511, 0, 512, 131071, 17, 513, 1023)
+
+
+def swa_inputs(B: int, seed: int, device="cuda"):
+    """dict(q [B,32,128], k, v [B,513,4,128] bf16, sinks [32] fp32, pos [B] int32)."""
+    import torch
+    q = torch_normal_bf16((B, SWA_HEADS, SWA_HEAD_DIM), seed, TAG_Q, 1.0, device=device)
+    k = torch_normal_bf16((B, SWA_WINDOW, SWA_KV_HEADS, SWA_HEAD_DIM), seed, TAG_K, 1.0, device=device)
+    v = torch_normal_bf16((B, SWA_WINDOW, SWA_KV_HEADS, SWA_HEAD_DIM), seed, TAG_V, 1.0, device=device)
+    sinks = torch_normal_bf16((SWA_HEADS,), seed, TAG_SINK, 1.0, device=device).float().contiguous()
+    pos = torch.tensor([SWA_POSITIONS[b % len(SWA_POSITIONS)] for b in range(B)], dtype=torch.int32, device=device)
+    return dict(q=q, k=k, v=v, sinks=sinks, pos=pos)
