@@ -61,6 +61,11 @@ def _lib():
         L.oracle_round_bf16.restype = ctypes.c_double
         L.oracle_swa_decode.argtypes = [_P, _P, _P, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_int, _P]
+        L.oracle_e2m1_to_f64.argtypes = [ctypes.c_uint]
+        L.oracle_e2m1_to_f64.restype = ctypes.c_double
+        L.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint]
+        L.oracle_e4m3_to_f64.restype = ctypes.c_double
+        L.oracle_nvfp4_dequant.argtypes = [_P, _P, ctypes.c_float, ctypes.c_int, ctypes.c_int, _P]
         L.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
         L.oracle_bf16_to_f64.restype = ctypes.c_double
         _LIB = L
@@ -312,3 +317,37 @@ def swa_decode(q, k, v, sinks, pos, nthreads: int = 1):
     for rc in rcs:
         _check(rc, "swa_decode")
     return out
+
+
+def e2m1_to_f64(code: int) -> float:
+    return _lib().oracle_e2m1_to_f64(int(code))
+
+
+def e4m3_to_f64(byte: int) -> float:
+    return _lib().oracle_e4m3_to_f64(int(byte))
+
+
+def nvfp4_dequant(codes, scales, tensor_scale) -> np.ndarray:
+    """W [K, N] float64 from NVFP4 codes [K, N/2] (uint8, two per byte, low nibble first), E4M3
+    block scales [K/16, N] (uint8) and the fp32 tensor scale."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    K, N = codes.shape[0], codes.shape[1] * 2
+    out = np.empty((K, N))
+    _check(_lib().oracle_nvfp4_dequant(_ptr(codes), _ptr(scales), float(tensor_scale), K, N, _ptr(out)),
+           "nvfp4_dequant")
+    return out
+
+
+def f64_to_bf16_exact(w) -> np.ndarray:
+    """bf16 bit patterns of float64 values that bf16 holds exactly (raises otherwise): NVFP4
+    weights with a power-of-two tensor scale are such values (a 2-bit by 4-bit significand
+    product), so the bf16 layer above computes the dequantised layer exactly."""
+    w = np.asarray(w, dtype=np.float64)
+    f = w.astype(np.float32)
+    if not np.array_equal(f.astype(np.float64), w):
+        raise ValueError("not representable in float32")
+    bits = f.view(np.uint32)
+    if np.any(bits & np.uint32(0xFFFF)):
+        raise ValueError("not representable in bf16")
+    return (bits >> np.uint32(16)).astype(np.uint16)

@@ -303,3 +303,32 @@ int oracle_swa_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, c
   free(s);
   return ORACLE_OK;
 }
+
+/* FP4 E2M1: bit 3 sign, bits 2..1 exponent (bias 1), bit 0 mantissa; exponent 0 is subnormal. */
+double oracle_e2m1_to_f64(unsigned code) {
+  const unsigned sign = (code >> 3) & 1u, e = (code >> 1) & 3u, m = code & 1u;
+  const double mag = e == 0 ? 0.5 * (double)m : ldexp(1.0 + 0.5 * (double)m, (int)e - 1);
+  return sign ? -mag : mag;
+}
+
+/* FP8 E4M3 (the variant without infinities): bit 7 sign, bits 6..3 exponent (bias 7), bits 2..0
+ * mantissa; exponent 0 is subnormal; exponent 15 with mantissa 7 is NaN. */
+double oracle_e4m3_to_f64(unsigned byte) {
+  const unsigned sign = (byte >> 7) & 1u, e = (byte >> 3) & 15u, m = byte & 7u;
+  if (e == 15u && m == 7u) return NAN;
+  const double mag = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, (int)e - 7);
+  return sign ? -mag : mag;
+}
+
+int oracle_nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, float tensor_scale, int K, int N,
+                         double* out) {
+  if (!codes || !scales || !out || K <= 0 || N <= 0 || K % 16 || N % 2) return ORACLE_EINVAL;
+  for (int k = 0; k < K; ++k)
+    for (int n = 0; n < N; ++n) {
+      const uint8_t byte = codes[(size_t)k * (N / 2) + n / 2];
+      const unsigned code = (n % 2) ? (byte >> 4) : (byte & 15u);
+      const double s = oracle_e4m3_to_f64(scales[(size_t)(k / 16) * N + n]);
+      out[(size_t)k * N + n] = oracle_e2m1_to_f64(code) * s * (double)tensor_scale;
+    }
+  return ORACLE_OK;
+}

@@ -92,6 +92,20 @@ double oracle_round_bf16(double v);
 /* r[t] = x[t] / sqrt(mean_h x[t][h]^2 + eps)  (unit weight). */
 void oracle_rmsnorm(const double* x, int T, int H, double eps, double* r);
 
+/* NVFP4 weights (the pages' four-bit builds: news article "Recursive opens Flint, a 40B coding
+ * model with 2.5B active", section "Built with the Eureka Machine"; the format's published
+ * definition): every element is an FP4 E2M1 code (sign, 2 exponent bits with bias 1, 1 mantissa
+ * bit: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), every 16 consecutive elements along the
+ * contraction dimension share one FP8 E4M3 scale (sign, 4 exponent bits with bias 7, 3 mantissa
+ * bits; no infinities, 0x7F / 0xFF are NaN; largest 448), and the tensor has one fp32 scale:
+ * value = e2m1 * e4m3 * tensor_scale. */
+double oracle_e2m1_to_f64(unsigned code);  /* low 4 bits */
+double oracle_e4m3_to_f64(unsigned byte);
+/* W [K][N] from codes [K][N/2] (byte (k, j): column 2j in the low nibble, 2j+1 in the high),
+ * scales [K/16][N] (E4M3 bytes) and the tensor scale; out [K][N].  K % 16 == 0, N even. */
+int oracle_nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, float tensor_scale, int K, int N,
+                         double* out);
+
 /* Decode attention of one sliding-window layer (serving-kit post, "The architecture, from the
  * config": 32 query heads, 4 KV heads, head dimension 128; sliding-window layers attend to a
  * 513-token window, the current token plus 512 back; learned per-head attention sinks; news

@@ -288,3 +288,67 @@ def swa_inputs(B: int, seed: int, device="cuda"):
     sinks = torch_normal_bf16((SWA_HEADS,), seed, TAG_SINK, 1.0, device=device).float().contiguous()
     pos = torch.tensor([SWA_POSITIONS[b % len(SWA_POSITIONS)] for b in range(B)], dtype=torch.int32, device=device)
     return dict(q=q, k=k, v=v, sinks=sinks, pos=pos)
+
+
+# --------------------------------------------------------------------------------------
+# NVFP4 expert weights.  The layer consumes NVFP4 weights as given; this module prepares seeded
+# synthetic ones by quantising the seeded bf16 weights above (input preparation, done once):
+#   tensor scale  t = 2^ceil(log2(amax / (6 * 448)))  (a power of two, one per matrix)
+#   block scale   s = the smallest E4M3 value >= amax(block of 16 along K) / 6 / t
+#   code          e2m1 = round(w / (s t)) to the nearest of 0, .5, 1, 1.5, 2, 3, 4, 6, ties to the
+#                 even code, sign kept
+# Layouts: codes [.., K, N/2] uint8 (column 2j in the low nibble of byte j), scales [.., K/16, N]
+# uint8 (E4M3 bits), tensor scales [..] fp32.
+
+_E2M1_MID = (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0)  # midpoints between the magnitudes
+
+
+def _e2m1_round_code(a):
+    """Magnitude code 0..7 of |v| (torch float32 tensor a >= 0), nearest with ties to even."""
+    import torch
+    mids = torch.tensor(_E2M1_MID, dtype=torch.float32, device=a.device)
+    idx = torch.bucketize(a, mids, right=False)  # a <= mids[i] -> i (a tie goes to the lower code)
+    # a tie at mids[i] goes to the even code of the pair (i, i + 1)
+    tie = torch.zeros_like(a, dtype=torch.bool)
+    for i, m in enumerate(_E2M1_MID):
+        tie |= (a == m) & torch.tensor(i % 2 == 1, device=a.device)
+    return torch.where(tie, idx + 1, idx).clamp(max=7)
+
+
+def nvfp4_quantize(w):
+    """(codes, scales, tensor_scale) of bf16 matrices w [..., K, N] (torch; any device)."""
+    import torch
+    lead = w.shape[:-2]
+    K, N = w.shape[-2], w.shape[-1]
+    w32 = w.float().reshape(-1, K, N)
+    M = w32.shape[0]
+    amax = w32.abs().amax(dim=(1, 2))
+    ts = torch.where(amax > 0, torch.exp2(torch.ceil(torch.log2(amax / (6.0 * 448.0)))), torch.ones_like(amax))
+    blk = w32.view(M, K // 16, 16, N)
+    need = blk.abs().amax(dim=2) / 6.0 / ts.view(M, 1, 1)  # the block scale must reach this
+    sb = need.to(torch.float8_e4m3fn)
+    bits = sb.view(torch.uint8)
+    low = sb.float() < need
+    bits = torch.where(low, bits + 1, bits)  # round up to the next E4M3 value
+    sbf = bits.view(torch.float8_e4m3fn).float()
+    denom = (sbf * ts.view(M, 1, 1)).unsqueeze(2)  # [M, K/16, 1, N]
+    v = torch.where(denom > 0, blk / torch.where(denom > 0, denom, torch.ones_like(denom)), torch.zeros_like(blk))
+    mag = _e2m1_round_code(v.abs())
+    code = (mag | torch.where(v < 0, 8, 0)).to(torch.uint8).view(M, K, N)
+    code = torch.where(mag.view(M, K, N) == 0, torch.zeros_like(code), code)  # no negative zero
+    packed = (code[..., 0::2] | (code[..., 1::2] << 4)).contiguous()
+    return (packed.view(*lead, K, N // 2), bits.contiguous().view(*lead, K // 16, N),
+            ts.view(*lead) if lead else ts.view(()))
+
+
+def nvfp4_weights(w):
+    """NVFP4 copies of a layer's expert matrices (routed and shared; the router stays bf16):
+    dict name -> (codes, scales, tensor_scale), quantised in chunks of experts on w's device."""
+    import torch
+    out = {}
+    for name in ("w_gate", "w_up", "w_down"):
+        parts = [nvfp4_quantize(w[name][e0:e0 + 32]) for e0 in range(0, w[name].shape[0], 32)]
+        out[name] = tuple(torch.cat([p[i] for p in parts]) for i in range(3))
+    for name in ("ws_gate", "ws_up", "ws_down"):
+        out[name] = nvfp4_quantize(w[name])
+    return out
