@@ -379,6 +379,14 @@ def run_ours(args, rank, world, local):
             r = run_workload(sub_args, rank, world, local, summary=True)
             out["configs"][name] = r
             torch.cuda.empty_cache()
+        # the rows beyond the MoE layer: the dense MLP layers and sliding-window decode attention
+        out["extra"] = {}
+        for T in (1, 64, 8192):
+            out["extra"][f"dense_T{T}"] = run_dense(args, local, T)
+        for B in (64, 256):
+            out["extra"][f"swa_B{B}"] = run_swa(args, local, B)
+        out["extra"]["nvfp4_decode_sweep"] = run_nvfp4_sweep(args, local)
+        torch.cuda.empty_cache()
     return out
 
 
@@ -648,6 +656,153 @@ def run_stack(args, rank, world, local, summary=False):
     return out
 
 
+def run_dense(args, local, T):
+    """One dense SwiGLU MLP layer (width 6144, weights seed 7, x seed 600+T): tokens/s, and the
+    roofline of the layer -- weight bytes (75.5 MB) at the copy bandwidth, or its FLOPs
+    (75.5 MFLOP per token) at the bf16 peak, whichever is slower."""
+    import torch
+
+    import synth
+    import sparse_moe_layer_15_b300 as fm
+
+    dev = torch.device("cuda", local)
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    w = synth.dense_weights(seed=7, device=dev)
+    layer = fm.FlintDense(w, max_tokens=T)
+    x = synth.torch_normal_bf16((T, fm.HIDDEN), 600 + T, synth.TAG_X, 1.0, device=dev)
+    y = torch.empty_like(x)
+    ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    steps = min(args.steps, 20)
+    timed_loop(lambda: layer.forward(x, y=y), args.warmup, lambda: flush_buf.fill_(1), stream, ev)
+    times = timed_loop(lambda: layer.forward(x, y=y), steps, lambda: flush_buf.fill_(1), stream, ev)
+    if layer.poll_device_status() != 0:
+        raise RuntimeError("device status error (dense layer)")
+    layer.enable_kernel_timing(True)
+    kt = {}
+    for _ in range(3):
+        flush_buf.fill_(1)
+        layer.forward(x, y=y)
+        for name, kms in layer.kernel_times():
+            kt.setdefault(name, []).append(kms)
+    layer.enable_kernel_timing(False)
+    layer.close()
+    ms = statistics.mean(times)
+    wbytes = 3 * fm.HIDDEN * fm.DENSE_INTER * 2
+    alg_bytes = wbytes + 2 * 2 * fm.HIDDEN * T
+    flop = 2 * 3 * fm.HIDDEN * fm.DENSE_INTER * T
+    t_mem, t_flop = alg_bytes / (peaks["hbm_gbs"] * 1e9), flop / (peaks["bf16_tflops"] * 1e12)
+    if t_mem >= t_flop:
+        roof = dict(bound="hbm", achieved=round(alg_bytes / (ms * 1e-3) / 1e9, 1), peak=peaks["hbm_gbs"], unit="GB/s",
+                    frac=round(alg_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4), alg_bytes=alg_bytes)
+    else:
+        roof = dict(bound="tensor", achieved=round(flop / (ms * 1e-3) / 1e12, 1), peak=peaks["bf16_tflops"],
+                    unit="TFLOP/s", frac=round(flop / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4), alg_flop=flop)
+    roof.update(kernel="+".join(sorted(kt)), traffic=None, note="the whole layer call / its CUDA-event time")
+    return dict(workload=f"dense SwiGLU MLP layer (2048 -> 6144 -> 2048), T={T}, L2 flushed before every call",
+                tokens_per_s=round(T / (ms * 1e-3), 1), us_median=round(statistics.median(times) * 1e3, 2),
+                kernels_us={k: round(statistics.median(v) * 1e3, 2) for k, v in kt.items()}, roofline=roof,
+                gpu_launches=steps * len(kt))
+
+
+# NVFP4 bytes: E2M1 codes (4 bits) + one E4M3 scale per 16 weights = 4.5 bits per weight.
+NVFP4_EXPERT_BYTES = 3 * 2048 * 512 // 2 + 3 * 2048 * 512 // 16      # 1,769,472 per routed expert
+NVFP4_SHARED_BYTES = 3 * 2048 * 1024 // 2 + 3 * 2048 * 1024 // 16    # 3,538,944
+
+
+def nvfp4_alg_bytes(U, T):
+    """Touched bytes of one layer call on NVFP4 expert weights: U experts' codes and scales, the
+    shared expert's, the bf16 router (1 MB) and the bf16 input and output rows."""
+    return U * NVFP4_EXPERT_BYTES + NVFP4_SHARED_BYTES + 2048 * 256 * 2 + 2 * 2 * 2048 * T
+
+
+def run_nvfp4_sweep(args, local):
+    """The decode sweep (T = 1..64, x seed 1000+T, L2 flushed before every forward) on NVFP4
+    expert weights quantised from the seed-0 layer: tokens/s and the HBM roofline of the 4.5-bit
+    weight stream."""
+    import torch
+
+    import synth
+    import sparse_moe_layer_15_b300 as fm
+
+    dev = torch.device("cuda", local)
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    w = synth.flint_weights(seed=0, device=dev)
+    q = synth.nvfp4_weights(w)
+    wr = w["w_router"]
+    del w
+    layer = fm.FlintMoE.nvfp4(wr, q, max_tokens=max(SWEEP))
+    ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    steps = min(args.steps, 20)
+    per_t, tot_ms, tot_bytes = {}, 0.0, 0
+    for T in SWEEP:
+        x = synth.torch_normal_bf16((T, fm.HIDDEN), 1000 + T, synth.TAG_X, 1.0, device=dev)
+        y = torch.empty_like(x)
+        timed_loop(lambda: layer.forward(x, y=y), args.warmup, lambda: flush_buf.fill_(1), stream, ev)
+        times = timed_loop(lambda: layer.forward(x, y=y), steps, lambda: flush_buf.fill_(1), stream, ev)
+        _, _, c = layer.route(x)
+        torch.cuda.synchronize()
+        U = int((c > 0).sum().item())
+        ms = statistics.mean(times)
+        b = nvfp4_alg_bytes(U, T)
+        tot_ms += ms
+        tot_bytes += b
+        per_t[str(T)] = dict(us=round(statistics.median(times) * 1e3, 2), touched_experts=U, alg_bytes=b,
+                             hbm_frac=round(b / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4))
+    if layer.poll_device_status() != 0:
+        raise RuntimeError("device status error (nvfp4)")
+    layer.close()
+    gbs = tot_bytes / (tot_ms * 1e-3) / 1e9
+    return dict(workload="decode sweep T=1..64 on NVFP4 expert weights (E2M1 + E4M3 per 16 + fp32 per matrix; "
+                         "router bf16), L2 flushed before every forward",
+                tokens_per_s=round(sum(SWEEP) / (tot_ms * 1e-3), 1), ms_per_step=round(tot_ms, 4), sweep=per_t,
+                roofline=dict(bound="hbm", kernel="decode_fused (NVFP4 stream)", achieved=round(gbs, 1),
+                              peak=peaks["hbm_gbs"], unit="GB/s", frac=round(gbs / peaks["hbm_gbs"], 4),
+                              traffic=None, note="4.5-bit weights: U x 1,769,472 + 3,538,944 + 1 MB router + x, y"),
+                gpu_launches=steps * len(SWEEP))
+
+
+def run_swa(args, local, B):
+    """Sliding-window decode attention with sinks over B sequences (the input recipe's length
+    mix, seed 900+B): sequences/s, and HBM bytes (the valid K/V cache slots + q + out) at the
+    copy bandwidth."""
+    import torch
+
+    import synth
+    import sparse_moe_layer_15_b300 as fm
+
+    dev = torch.device("cuda", local)
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    attn = fm.SwaAttention(max_batch=B, device=dev)
+    inp = synth.swa_inputs(B, seed=900 + B, device=dev)
+    out = torch.empty_like(inp["q"])
+    ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    steps = min(args.steps, 20)
+
+    def step():
+        attn.decode(inp["q"], inp["k"], inp["v"], inp["sinks"], inp["pos"], out=out)
+
+    timed_loop(step, args.warmup, lambda: flush_buf.fill_(1), stream, ev)
+    times = timed_loop(step, steps, lambda: flush_buf.fill_(1), stream, ev)
+    if attn.poll_device_status() != 0:
+        raise RuntimeError("device status error (swa)")
+    ms = statistics.mean(times)
+    n_valid = np.minimum(inp["pos"].cpu().numpy().astype(np.int64) + 1, fm.SWA_WINDOW)
+    alg_bytes = int(n_valid.sum()) * fm.SWA_KV_HEADS * fm.SWA_HEAD_DIM * 2 * 2 + 2 * B * 32 * 128 * 2 + 32 * 4
+    gbs = alg_bytes / (ms * 1e-3) / 1e9
+    return dict(workload=f"sliding-window decode attention, 32/4 heads x 128, window 513, sinks, B={B} "
+                         "(length mix of the input recipe), L2 flushed before every call",
+                sequences_per_s=round(B / (ms * 1e-3), 1), us_median=round(statistics.median(times) * 1e3, 2),
+                roofline=dict(bound="hbm", kernel="swa::decode_kernel", achieved=round(gbs, 1), peak=peaks["hbm_gbs"],
+                              unit="GB/s", frac=round(gbs / peaks["hbm_gbs"], 4), alg_bytes=alg_bytes, traffic=None),
+                gpu_launches=steps)
+
+
 # ----------------------------------------------------------------------------- oracle timing
 
 def cpu_baseline_tokens(w, x, n=16, what="", eps=None):
@@ -736,12 +891,38 @@ def run_profile_case(args):
 
     dev = torch.device("cuda", 0)
     T = args.profile
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    if args.workload in ("dense", "swa", "nvfp4"):
+        # the dense MLP layer at T tokens, or SWA decode attention over B = T sequences
+        if args.workload == "nvfp4":
+            w0 = synth.flint_weights(seed=0, device=dev)
+            q = synth.nvfp4_weights(w0)
+            lay = fm.FlintMoE.nvfp4(w0["w_router"], q, max_tokens=T)
+            x = synth.torch_normal_bf16((T, fm.HIDDEN), 1000 + T, synth.TAG_X, 1.0, device=dev)
+            fn, poll = (lambda: lay.forward(x)), lay.poll_device_status
+        elif args.workload == "dense":
+            lay = fm.FlintDense(synth.dense_weights(seed=7, device=dev), max_tokens=T)
+            x = synth.torch_normal_bf16((T, fm.HIDDEN), 600 + T, synth.TAG_X, 1.0, device=dev)
+            fn, poll = (lambda: lay.forward(x)), lay.poll_device_status
+        else:
+            attn = fm.SwaAttention(max_batch=T, device=dev)
+            inp = synth.swa_inputs(T, seed=900 + T, device=dev)
+            fn = lambda: attn.decode(inp["q"], inp["k"], inp["v"], inp["sinks"], inp["pos"])  # noqa: E731
+            poll = attn.poll_device_status
+        for _ in range(args.warmup + args.steps):
+            flush_buf.fill_(1)
+            fn()
+        torch.cuda.synchronize()
+        rc = poll()
+        print(json.dumps(dict(profile_case=T, workload=args.workload, steps=args.steps, device_status=rc)))
+        if rc != 0:
+            raise SystemExit(1)
+        return
     cfg = WORKLOADS.get(args.workload)  # router bias and x seed of that workload, at this T
     w = synth.flint_weights(seed=0, device=dev, bias=cfg["bias"] if cfg else None,
                             bias_seed=cfg["bias_seed"] if cfg else None)
     layer = fm.FlintMoE(w, max_tokens=T)
     x = synth.torch_normal_bf16((T, fm.HIDDEN), cfg["seed_x"] if cfg else 1000 + T, synth.TAG_X, 1.0, device=dev)
-    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     for _ in range(args.warmup + args.steps):
         flush_buf.fill_(1)
         y = layer.forward(x)
@@ -818,7 +999,9 @@ def main():
     ap.add_argument("--trace", action="store_true",
                     help="with --profile: print the decode kernel's phase trace (T <= 256) or the grouped GEMMs' "
                          "wait profile (T > 256)")
-    ap.add_argument("--workload", default="decode", choices=["decode", "single", "prefill", "adversarial", "stack"])
+    ap.add_argument("--workload", default="decode",
+                    choices=["decode", "single", "prefill", "adversarial", "stack", "dense", "swa", "nvfp4"],
+                    help="dense / swa / nvfp4: only with --profile (the default line measures them under 'extra')")
     ap.add_argument("--stack-tokens", type=int, default=256, help="stack workload: tokens per step (1..256)")
     ap.add_argument("--stack-layers", type=int, default=47,
                     help="stack workload: layers (fewer than 47 only as a small profiling case)")

@@ -154,6 +154,47 @@ flint_moe_status flint_moe_read_trace(flint_moe_t h, unsigned long long* out, in
 /* Releases the handle's host state.  Does not touch the workspace or the weights. */
 flint_moe_status flint_moe_destroy(flint_moe_t h);
 
+/* ---------------------------------------------------------------- NVFP4 expert weights
+ * The pages' four-bit builds (news article "Recursive opens Flint, a 40B coding model with 2.5B
+ * active", section "Built with the Eureka Machine": the NVFP4 model; serving-kit post, section
+ * "What isn't validated, and what the kit refuses to do": the quantized builds run on other
+ * engines).  NVFP4, by the format's published definition: each weight is an FP4 E2M1 code, every
+ * 16 consecutive weights along the contraction dimension share one FP8 E4M3 scale, and each
+ * matrix has one fp32 tensor scale: w = e2m1 * e4m3 * tensor_scale.  Layouts (device memory,
+ * 16-byte aligned), for a matrix W [K][N] of the math orientation y = x W:
+ *   codes  uint8 [K][N/2]: byte (k, j) holds W[k][2j] in its low nibble, W[k][2j+1] in its high;
+ *   scales uint8 [K/16][N]: E4M3 bits of the scale of W[16g .. 16g+15][n].
+ * The routed experts' matrices are stacked as in flint_moe_weights, with one tensor scale per
+ * expert and matrix (device fp32 arrays); the router stays bf16.  A handle made by
+ * flint_moe_create_nvfp4 is used with flint_moe_route / flint_moe_forward / flint_moe_destroy
+ * and the other per-handle calls; it runs the decode-size kernel, streaming the codes and scales
+ * (4.5 bits per weight) and dequantising in shared memory (e2m1 * e4m3 is exact in bf16), with
+ * the tensor scale applied to each finished output in fp32.  Decode sizes only: max_tokens <= 64,
+ * else FLINT_MOE_ERR_UNSUPPORTED. */
+typedef struct {
+  const void* w_router;         /* bf16 [hidden][n_experts] */
+  const float* router_bias;     /* fp32 [n_experts] or NULL */
+  const uint8_t* gate_codes;    /* [n_experts][hidden][expert_inter / 2] */
+  const uint8_t* up_codes;      /* [n_experts][hidden][expert_inter / 2] */
+  const uint8_t* down_codes;    /* [n_experts][expert_inter][hidden / 2] */
+  const uint8_t* gate_scales;   /* [n_experts][hidden / 16][expert_inter] */
+  const uint8_t* up_scales;     /* [n_experts][hidden / 16][expert_inter] */
+  const uint8_t* down_scales;   /* [n_experts][expert_inter / 16][hidden] */
+  const float* gate_tscale;     /* device fp32 [n_experts] */
+  const float* up_tscale;       /* device fp32 [n_experts] */
+  const float* down_tscale;     /* device fp32 [n_experts] */
+  const uint8_t* sgate_codes;   /* [hidden][shared_inter / 2] */
+  const uint8_t* sup_codes;     /* [hidden][shared_inter / 2] */
+  const uint8_t* sdown_codes;   /* [shared_inter][hidden / 2] */
+  const uint8_t* sgate_scales;  /* [hidden / 16][shared_inter] */
+  const uint8_t* sup_scales;    /* [hidden / 16][shared_inter] */
+  const uint8_t* sdown_scales;  /* [shared_inter / 16][hidden] */
+  float sgate_tscale, sup_tscale, sdown_tscale;
+} flint_moe_nvfp4_weights;
+
+flint_moe_status flint_moe_create_nvfp4(const flint_moe_config* cfg, const flint_moe_nvfp4_weights* w,
+                                        void* workspace, size_t workspace_bytes, flint_moe_t* out);
+
 /* The whole layer for callers that cannot allocate device memory where they run it (a host
  * program that owns all device memory and gives plugins no allocator, a runtime that plans
  * its memory at start-up and allows no allocation later, a latency path that cannot take the
@@ -274,6 +315,37 @@ flint_moe_status flint_dense_kernel_times(flint_dense_t d, const char** names, f
 
 /* Releases the handle's host state (not the workspace or the weights). */
 flint_moe_status flint_dense_destroy(flint_dense_t d);
+
+/* ---------------------------------------------------------------- sliding-window decode attention
+ * One decode step of a sliding-window attention layer (serving-kit post, section "The
+ * architecture, from the config": 35 layers attend to a 513-token window, the current token plus
+ * 512 back; 32 query heads, 4 KV heads, head dimension 128; learned per-head attention sinks.
+ * News article "Recursive opens Flint, a 40B coding model with 2.5B active", section "What runs
+ * on each token": a sink is a slot that can take attention no real token needs).  For every
+ * sequence b and query head h (KV head h / 8):
+ *   out[b][h] = sum_j e^(s_j - m) v_j / (e^(sinks[h] - m) + sum_j e^(s_j - m)),
+ *   s_j = q[b][h] . k_j / sqrt(128), m = max(sinks[h], s_j),
+ * over the sequence's valid cache slots.  Readings taken: the sink is a logit of the softmax
+ * denominator that carries no value; q and k are passed already normalised and rotated (the
+ * per-head QK RMSNorm and RoPE belong to the projections).
+ * Layouts (device memory, caller-owned, 16-byte aligned; bf16 row-major):
+ *   q       [B][32][128]
+ *   k_cache [B][513][4][128], v_cache the same: each sequence's ring of its last 513 tokens,
+ *           position p in slot p mod 513, the current token's K and V already stored;
+ *   sinks   fp32 [32];  pos int32 [B]: position of each sequence's current token (>= 0; the
+ *           slots 0 .. min(pos + 1, 513) - 1 are valid; a negative pos is a device bounds error);
+ *   out     [B][32][128] bf16.
+ * One kernel launch, asynchronous on `stream`, no allocation, bitwise deterministic.  The
+ * workspace (caller-owned, 256-byte aligned, flint_swa_workspace_bytes) holds chunk partials
+ * and tickets; initialise it once with flint_swa_workspace_init; its tickets return to zero at
+ * the end of every call.  Calls sharing one workspace must be ordered on one stream. */
+flint_moe_status flint_swa_workspace_bytes(int max_batch, size_t* bytes);
+flint_moe_status flint_swa_workspace_init(void* workspace, size_t workspace_bytes, flint_stream_t stream);
+flint_moe_status flint_swa_decode(void* workspace, size_t workspace_bytes, const void* q, const void* k_cache,
+                                  const void* v_cache, const float* sinks, const int32_t* pos, int B, void* out,
+                                  flint_stream_t stream);
+/* Synchronises `stream`, then returns and clears the workspace's device status word. */
+flint_moe_status flint_swa_poll_device_status(void* workspace, flint_stream_t stream);
 
 #ifdef __cplusplus
 }

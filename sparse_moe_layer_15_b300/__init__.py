@@ -31,7 +31,8 @@ EXPORTS = ("flint_moe_status_string", "flint_moe_workspace_bytes", "flint_moe_cr
            "flint_moe_stack_enable_kernel_timing", "flint_moe_stack_read_trace", "flint_moe_stack_destroy",
            "flint_dense_workspace_bytes", "flint_dense_create", "flint_dense_forward",
            "flint_dense_poll_device_status", "flint_dense_enable_kernel_timing", "flint_dense_kernel_times",
-           "flint_dense_destroy")
+           "flint_dense_destroy", "flint_swa_workspace_bytes", "flint_swa_workspace_init", "flint_swa_decode",
+           "flint_swa_poll_device_status", "flint_moe_create_nvfp4")
 
 NOALLOC_MAX_TOKENS = 4
 DENSE_INTER = 6144  # width of the dense MLP layers
@@ -56,6 +57,14 @@ class _DenseConfig(ctypes.Structure):
 
 class _DenseWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("w_gate", "w_up", "w_down")]
+
+
+class _Nvfp4Weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("w_router", "router_bias", "gate_codes", "up_codes", "down_codes", "gate_scales", "up_scales",
+                 "down_scales", "gate_tscale", "up_tscale", "down_tscale", "sgate_codes", "sup_codes",
+                 "sdown_codes", "sgate_scales", "sup_scales", "sdown_scales")] + \
+               [("sgate_tscale", ctypes.c_float), ("sup_tscale", ctypes.c_float), ("sdown_tscale", ctypes.c_float)]
 
 
 class _Weights(ctypes.Structure):
@@ -114,6 +123,12 @@ def load_library():
     L.flint_dense_kernel_times.argtypes = [P, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float), I32,
                                            ctypes.POINTER(I32)]
     L.flint_dense_destroy.argtypes = [P]
+    L.flint_moe_create_nvfp4.argtypes = [ctypes.POINTER(_Config), ctypes.POINTER(_Nvfp4Weights), P, ctypes.c_size_t,
+                                         ctypes.POINTER(P)]
+    L.flint_swa_workspace_bytes.argtypes = [I32, ctypes.POINTER(ctypes.c_size_t)]
+    L.flint_swa_workspace_init.argtypes = [P, ctypes.c_size_t, P]
+    L.flint_swa_decode.argtypes = [P, ctypes.c_size_t, P, P, P, P, P, I32, P, P]
+    L.flint_swa_poll_device_status.argtypes = [P, P]
     for name in EXPORTS:
         if name != "flint_moe_status_string":
             getattr(L, name).restype = I32
@@ -200,6 +215,48 @@ class FlintMoE:
                                         ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
                                         ctypes.byref(h)), "flint_moe_create")
         self._h = h
+
+    @classmethod
+    def nvfp4(cls, w_router, q, max_tokens: int, router_bias=None, flags: int = 0, rms_eps: float = 1e-6,
+              workspace=None):
+        """A layer on NVFP4 expert weights (flint_moe_create_nvfp4; decode sizes, max_tokens <= 64).
+        ``q``: name -> (codes, scales, tensor_scale) for w_gate, w_up, w_down (routed: tensor scales
+        [256] fp32 on the device) and ws_gate, ws_up, ws_down (shared: scalar tensor scales), in the
+        layouts of include/flint_moe.h; ``w_router`` bf16 [2048, 256].  Borrowed: keep them alive."""
+        import torch
+        self = cls.__new__(cls)
+        self._L = load_library()
+        self.max_tokens = int(max_tokens)
+        self.flags = int(flags)
+        self._weights = (w_router, router_bias, q)
+        self._cfg = _Config(HIDDEN, N_EXPERTS, TOP_K, EXPERT_INTER, SHARED_INTER, self.max_tokens, self.flags,
+                            float(rms_eps))
+
+        def ptr(t):
+            if not t.is_contiguous():
+                raise ValueError("NVFP4 tensors must be contiguous")
+            return t.data_ptr()
+
+        self._w = _Nvfp4Weights(
+            ptr(w_router), None if router_bias is None else ptr(router_bias),
+            ptr(q["w_gate"][0]), ptr(q["w_up"][0]), ptr(q["w_down"][0]),
+            ptr(q["w_gate"][1]), ptr(q["w_up"][1]), ptr(q["w_down"][1]),
+            ptr(q["w_gate"][2]), ptr(q["w_up"][2]), ptr(q["w_down"][2]),
+            ptr(q["ws_gate"][0]), ptr(q["ws_up"][0]), ptr(q["ws_down"][0]),
+            ptr(q["ws_gate"][1]), ptr(q["ws_up"][1]), ptr(q["ws_down"][1]),
+            float(q["ws_gate"][2]), float(q["ws_up"][2]), float(q["ws_down"][2]))
+        nbytes = ctypes.c_size_t(0)
+        _check(self._L.flint_moe_workspace_bytes(ctypes.byref(self._cfg), ctypes.byref(nbytes)),
+               "flint_moe_workspace_bytes")
+        if workspace is None:
+            workspace = torch.empty(nbytes.value, dtype=torch.uint8, device=w_router.device)
+        self.workspace = workspace
+        h = ctypes.c_void_p()
+        _check(self._L.flint_moe_create_nvfp4(ctypes.byref(self._cfg), ctypes.byref(self._w),
+                                              ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                                              ctypes.byref(h)), "flint_moe_create_nvfp4")
+        self._h = h
+        return self
 
     def route(self, x, topk_idx=None, topk_w=None, counts=None, stream=None):
         import torch
@@ -400,3 +457,39 @@ class FlintDense:
             self.close()
         except Exception:
             pass
+
+
+SWA_HEADS, SWA_KV_HEADS, SWA_HEAD_DIM, SWA_WINDOW = 32, 4, 128, 513
+
+
+class SwaAttention:
+    """Decode attention of the sliding-window layers (flint_swa_*): 32 query heads, 4 KV heads,
+    head dimension 128, a ring of 513 cached tokens per sequence, one learned sink per head.
+    The workspace is allocated here by torch (for up to ``max_batch`` sequences) and
+    initialised once."""
+
+    def __init__(self, max_batch: int, device="cuda", stream=None):
+        import torch
+        self._L = load_library()
+        n = ctypes.c_size_t(0)
+        _check(self._L.flint_swa_workspace_bytes(int(max_batch), ctypes.byref(n)), "flint_swa_workspace_bytes")
+        self.workspace = torch.empty(n.value, dtype=torch.uint8, device=device)
+        _check(self._L.flint_swa_workspace_init(_ptr(self.workspace), n.value, _stream_ptr(stream)),
+               "flint_swa_workspace_init")
+
+    def decode(self, q, k_cache, v_cache, sinks, pos, out=None, stream=None):
+        """q [B,32,128] bf16, k_cache / v_cache [B,513,4,128] bf16, sinks [32] fp32, pos [B] int32
+        (device tensors) -> out [B,32,128] bf16."""
+        import torch
+        if out is None:
+            out = torch.empty_like(q)
+        for t in (q, k_cache, v_cache, sinks, pos, out):
+            if not t.is_contiguous():
+                raise ValueError("flint_swa_decode takes contiguous tensors")
+        _check(self._L.flint_swa_decode(_ptr(self.workspace), self.workspace.numel(), _ptr(q), _ptr(k_cache),
+                                        _ptr(v_cache), _ptr(sinks), _ptr(pos), q.shape[0], _ptr(out),
+                                        _stream_ptr(stream)), "flint_swa_decode")
+        return out
+
+    def poll_device_status(self, stream=None):
+        return self._L.flint_swa_poll_device_status(_ptr(self.workspace), _stream_ptr(stream))

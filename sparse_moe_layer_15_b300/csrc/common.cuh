@@ -38,6 +38,14 @@ struct Params {
   float rms_eps;
   int sw;                // width of the shared expert: IS, or ID for a dense MLP layer
   int dense;             // 1: a dense SwiGLU MLP layer (the shared-expert path alone; y = MLP(x') [+ x])
+  int fp4;               // 1: NVFP4 expert weights (decode sizes, T <= FP4_MAX_T)
+  const float* ts_gate;  // [E] fp32 tensor scales of the routed NVFP4 matrices (fp4)
+  const float* ts_up;
+  const float* ts_down;
+  float ts_sgate, ts_sup, ts_sdown;  // the shared expert's (fp4)
+  const uint8_t* q_down;   // [E][I][H/2] routed down codes (fp4; L2 prefetch of the touched experts)
+  const uint8_t* q_sdown;  // [IS][H/2] shared down codes (fp4; L2 prefetch)
+  const void* fp4_maps;    // the NVFP4 tensor maps (an Fp4Maps in the workspace; fp4)
   const bf16* x;         // layer input [T][H]
   const bf16* xin;       // expert / router input: x, or rms(x) in xn
   bf16* y;               // output [T][H]

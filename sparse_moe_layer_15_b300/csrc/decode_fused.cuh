@@ -78,6 +78,31 @@ struct StreamMaps {
   CUtensorMap wsd;  // [IS][H], box 64 x 128
 };
 
+// NVFP4 expert weights (Params::fp4), kept in the workspace (Params::fp4_maps): E2M1 codes two per
+// byte, [rows][cols / 2] uint8, boxes of 64 bytes (128 columns) x 256 rows; E4M3 scales [rows /
+// 16][cols] uint8, boxes of 128 bytes x 16 (gate / up) or 32 (down) scale rows.  No swizzle.
+struct Fp4Maps {
+  CUtensorMap qg, qu, qd, qsg, qsu, qsd;  // codes: [E*H][I/2], [E*H][I/2], [E*I][H/2], [H][IS/2], ., [IS][H/2]
+  CUtensorMap sg, su, sd, ssg, ssu, ssd;  // scales: [E*H/16][I], ., [E*I/16][H], [H/16][IS], ., [IS/16][H]
+};
+
+// ---- NVFP4 streaming (decode sizes): a block is 256 rows x 128 columns of gate and of up (32 KB of
+// codes + 4 KB of scales), or 512 rows x 128 columns of a down matrix (the same sizes); the codes
+// land in the stage ring, the scales in a ring of 4 KB slots beside it.  Each warp dequantises
+// (e2m1 * e4m3, exact in bf16) the part of a block it multiplies into a 16 KB bf16 tile -- 32 rows
+// of gate/up or 64 rows of down at a time -- and runs the bf16 warp MMAs on it; the tensor scale
+// multiplies the finished item in fp32.  Token groups of 8 rows only (T <= FP4_MAX_T).
+constexpr int FP4_MAX_T = 64;
+constexpr int FP4_GU_ROWS = 256;
+constexpr int FP4_DN_ROWS = 512;
+constexpr int FP4_GU_KB = H / FP4_GU_ROWS;    // 8 blocks per gate/up item
+constexpr int FP4_DN_KB = I / FP4_DN_ROWS;    // 1 block per routed down item
+constexpr int FP4_SD_KB = IS / FP4_DN_ROWS;   // 2 blocks per shared down item
+constexpr int FP4_CODE_BYTES = 32768;
+constexpr int FP4_SCALE_BYTES = 4096;
+constexpr int FP4_DQ_BYTES = 16384;
+static_assert(FP4_CODE_BYTES <= BLK_BYTES, "the codes fit a stage");
+
 // Token rows per group for a call of T tokens: 16 when T > 64 (the weights of the shared
 // expert, the router and any expert with more than 8 rows are then streamed once per 16 rows
 // instead of 8), else 8 (measured faster for the small calls: fewer zero rows staged and
@@ -136,6 +161,11 @@ __host__ __device__ constexpr int fused_smem_bytes(int G) { return out_offset(G)
 static_assert(Smem::s_idx + MAX_PAIRS * 4 <= Smem::xs + xs_bytes(NT_MAX / 2), "routing scratch must fit in xs");
 static_assert(Smem::perm % 16 == 0 && Smem::gw % 16 == 0 && Smem::xs % 16 == 0, "16-byte aligned tables");
 constexpr int FUSED_SMEM = fused_smem_bytes(NT_MAX);  // the largest launch
+// NVFP4 launches (8-row groups): the scale slots and the dequantised tile after the output tile.
+__host__ __device__ constexpr int fp4_scl_offset() { return (out_offset(NT_MAX / 2) + NT_MAX / 2 * 256 * 4 + 1023) / 1024 * 1024; }
+__host__ __device__ constexpr int fp4_dq_offset() { return fp4_scl_offset() + NSTAGE * FP4_SCALE_BYTES; }
+__host__ __device__ constexpr int fp4_smem_bytes() { return fp4_dq_offset() + FP4_DQ_BYTES + 1024; }
+static_assert(fp4_smem_bytes() <= FUSED_SMEM, "an NVFP4 launch fits the kernel's shared-memory limit");
 static_assert(FUSED_SMEM <= 227 * 1024, "shared memory budget");
 static_assert(GU_KB <= 64 && SD_KB <= 64 && DN_KB <= 64, "an item's pieces fit the slot list");
 // Most blocks of one step (step C: routed and shared gate/up; step D has half as many per group).
@@ -389,9 +419,21 @@ __device__ __forceinline__ int find_group_owner(const int* tgp, int n, int gi) {
 // Item numbering is token-group major for every kind (router: tg * 32 + row block; routed:
 // gi * chunks + c; shared: tg * chunks + c), so that consecutive items of a CTA's range
 // usually share their token group and its staged input rows.
-// sncb: 128-column blocks of the shared expert's width (its gate/up items per token group, and
-// the K blocks of its down items).
-__device__ __forceinline__ Item decode_item(int T, int sncb, const Meta& m, int kind, int idx) {
+// K blocks per item of a kind: 64-row (gate/up) or 128-row (down) bf16 blocks, or the NVFP4
+// blocks of 256 / 512 rows.
+__device__ __forceinline__ int kblocks_of(const Params& p, int kind) {
+  switch (kind) {
+    case KIND_RT: return 1;
+    case KIND_GU:
+    case KIND_SGU: return p.fp4 ? FP4_GU_KB : GU_KB;
+    case KIND_DN: return p.fp4 ? FP4_DN_KB : DN_KB;
+    default: return p.fp4 ? FP4_SD_KB : p.dense ? ID / DN_ROWS : SD_KB;
+  }
+}
+
+__device__ __forceinline__ Item decode_item(const Params& p, const Meta& m, int kind, int idx) {
+  const int T = p.T;
+  const int sncb = p.dense ? ID / 128 : SGU_NCB;  // 128-column blocks of the shared gate/up
   Item it;
   it.kind = kind;
   it.idx = idx;
@@ -405,16 +447,17 @@ __device__ __forceinline__ Item decode_item(int T, int sncb, const Meta& m, int 
     it.e = m.e[u];
     it.row0 = m.off[u] + tg * G;
     it.nt = min(G, m.cnt[u] - tg * G);
-    it.KB = kind == KIND_GU ? GU_KB : DN_KB;
+    it.KB = kblocks_of(p, kind);
   } else {
-    const int nch = kind == KIND_RT ? RT_NB : kind == KIND_SGU ? sncb : OUT_NCB;
-    const int tg = idx / nch;
-    it.c = idx % nch;
+    // (the MoE's column-block counts are powers of two: shifts; a dense layer's 48 divides)
+    const int nch = kind == KIND_RT ? RT_NB : kind == KIND_SGU ? (p.dense ? sncb : SGU_NCB) : OUT_NCB;
+    const int tg = p.dense ? idx / nch : idx / (kind == KIND_RT ? RT_NB : kind == KIND_SGU ? SGU_NCB : OUT_NCB);
+    it.c = idx - tg * nch;
     const int G = group_rows(T);
     it.e = -1;
     it.row0 = tg * G;
     it.nt = min(G, T - tg * G);
-    it.KB = kind == KIND_RT ? 1 : kind == KIND_SGU ? GU_KB : sncb;
+    it.KB = kblocks_of(p, kind);
   }
   return it;
 }
@@ -439,11 +482,56 @@ __device__ __forceinline__ void block_kind(const BlockList& L, int b, int& kind,
   }
 }
 
+// NVFP4 block (codes into `stage`, scales into `scl`): gate/up 256 rows of gate and of up; down
+// 512 rows, as two 256-row code boxes.
+__device__ void issue_block_fp4(const Item& it, const Fp4Maps& maps, int kb, uint8_t* stage, uint8_t* scl,
+                                uint64_t* bar) {
+  mbar_arrive_expect_tx(bar, FP4_CODE_BYTES + FP4_SCALE_BYTES);
+  const int xc = it.c * 64, xs = it.c * 128;  // code bytes, scale bytes (= columns)
+  constexpr int HALF = FP4_CODE_BYTES / 2, SH = FP4_SCALE_BYTES / 2;
+  switch (it.kind) {
+    case KIND_GU: {
+      const int y = it.e * H + kb * FP4_GU_ROWS, ys = y / 16;
+      tma_load_2d(stage, &maps.qg, xc, y, bar);
+      tma_load_2d(stage + HALF, &maps.qu, xc, y, bar);
+      tma_load_2d(scl, &maps.sg, xs, ys, bar);
+      tma_load_2d(scl + SH, &maps.su, xs, ys, bar);
+      break;
+    }
+    case KIND_SGU: {
+      const int y = kb * FP4_GU_ROWS, ys = y / 16;
+      tma_load_2d(stage, &maps.qsg, xc, y, bar);
+      tma_load_2d(stage + HALF, &maps.qsu, xc, y, bar);
+      tma_load_2d(scl, &maps.ssg, xs, ys, bar);
+      tma_load_2d(scl + SH, &maps.ssu, xs, ys, bar);
+      break;
+    }
+    case KIND_SD: {
+      const int y = kb * FP4_DN_ROWS;
+      tma_load_2d(stage, &maps.qsd, xc, y, bar);
+      tma_load_2d(stage + HALF, &maps.qsd, xc, y + FP4_DN_ROWS / 2, bar);
+      tma_load_2d(scl, &maps.ssd, xs, y / 16, bar);
+      break;
+    }
+    default: {
+      const int y = it.e * I + kb * FP4_DN_ROWS;
+      tma_load_2d(stage, &maps.qd, xc, y, bar);
+      tma_load_2d(stage + HALF, &maps.qd, xc, y + FP4_DN_ROWS / 2, bar);
+      tma_load_2d(scl, &maps.sd, xs, y / 16, bar);
+      break;
+    }
+  }
+}
+
 __device__ void issue_block(const Params& p, const Meta& m, const StreamMaps& maps, const BlockList& L, int b,
-                            uint8_t* stage, uint64_t* bar) {
+                            uint8_t* stage, uint64_t* bar, uint8_t* scl) {
   int kind, idx, kb;
   block_kind(L, b, kind, idx, kb);
-  const Item it = decode_item(p.T, p.sw / 128, m, kind, idx);
+  const Item it = decode_item(p, m, kind, idx);
+  if (p.fp4 && kind != KIND_RT) {
+    issue_block_fp4(it, *static_cast<const Fp4Maps*>(p.fp4_maps), kb, stage, scl, bar);
+    return;
+  }
   mbar_arrive_expect_tx(bar, BLK_BYTES);
   // gate/up: boxes [gate chunk 2c | gate 2c+1 | up 2c | up 2c+1] of 8 KB; down: [chunk 2c | 2c+1]
   // of 16 KB (64 columns each: the 128-byte swizzle span)
@@ -515,7 +603,8 @@ __device__ void produce(Stream& S, int from, int to) {
     const int st = pos % NSTAGE;
     const int use = pos / NSTAGE;
     if (use > 0) mbar_wait_or_flag(S.empty + st, uint32_t(use - 1) & 1u, S.p->status);
-    issue_block(*S.p, S.meta, *S.maps, S.L, S.b0 + j, S.sm + Smem::stages + st * BLK_BYTES, S.full + st);
+    issue_block(*S.p, S.meta, *S.maps, S.L, S.b0 + j, S.sm + Smem::stages + st * BLK_BYTES, S.full + st,
+                S.sm + fp4_scl_offset() + st * FP4_SCALE_BYTES);
   }
 }
 
@@ -524,6 +613,84 @@ __device__ __forceinline__ void wait_full(Stream& S, int j) {
   const int pos = S.ring + j;
   mbar_wait_or_flag(S.full + pos % NSTAGE, uint32_t(pos / NSTAGE) & 1u, S.p->status);
   if (j == 0) trace_point(*S.p, S.first_slot);
+}
+
+// ---- NVFP4 dequantisation (warp-local: each warp writes exactly the part of the bf16 tile that
+// its own MMAs read, so only __syncwarp orders the two)
+// Two E2M1 codes (one byte, the first in the low nibble) -> f16x2 (the first in the low half).
+__device__ __forceinline__ uint32_t e2m1x2_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(r) : "r"(byte));
+  return r;
+}
+// Two E4M3 values (the first in the low byte) -> f16x2.
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t half) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(r) : "r"(half));
+  return r;
+}
+// 8 consecutive columns: codes (4 bytes) times their 8 scales (4 f16x2) -> 8 bf16.  Every product
+// e2m1 * e4m3 has at most 5 significant bits and lies in [2^-10, 2688]: exact in f16 and in bf16.
+__device__ __forceinline__ uint4 dq8(uint32_t codes, const uint32_t (&s2)[4]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t h = e2m1x2_f16x2((codes >> (8 * q)) & 0xFFu);
+    const __half2 prod = __hmul2(*reinterpret_cast<const __half2*>(&h), *reinterpret_cast<const __half2*>(&s2[q]));
+    const float2 f = __half22float2(prod);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+    w[q] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+__device__ __forceinline__ void scales8(const uint8_t* p, uint32_t (&s2)[4]) {
+  const uint2 v = *reinterpret_cast<const uint2*>(p);
+  s2[0] = e4m3x2_f16x2(v.x & 0xFFFFu);
+  s2[1] = e4m3x2_f16x2(v.x >> 16);
+  s2[2] = e4m3x2_f16x2(v.y & 0xFFFFu);
+  s2[3] = e4m3x2_f16x2(v.y >> 16);
+}
+
+// Gate/up: rows [32 sub, +32) of the block (codes [gate | up][256 rows][64 B], scales [gate |
+// up][16][128 B]) -> the warp's 32 columns of its box (boxes [gate 2c | gate 2c+1 | up 2c | up
+// 2c+1], 32 rows x 64 columns, 128-byte swizzled rows) of the 16 KB tile.
+__device__ __forceinline__ void dequant_gu(const uint8_t* codes, const uint8_t* scl, uint8_t* dq, int sub) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int box = warp >> 1, mat = box >> 1;
+  const int m = (warp & 1) * 32 + 8 * (lane & 3);  // first of the lane's 8 columns, in the box
+  const int col = (box & 1) * 64 + m;              // ... in the 128-column block
+  const uint8_t* cb = codes + mat * (FP4_CODE_BYTES / 2) + col / 2;
+  const uint8_t* sb = scl + mat * (FP4_SCALE_BYTES / 2) + col;
+  uint8_t* tile = dq + box * (32 * 128);
+#pragma unroll
+  for (int gi = 0; gi < 2; ++gi) {  // the two 16-row scale groups of the 32 rows
+    uint32_t s2[4];
+    scales8(sb + (sub * 2 + gi) * 128, s2);
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const int r = (lane >> 2) + 8 * (2 * gi + rr);  // row in the sub-tile
+      const uint32_t c4 = *reinterpret_cast<const uint32_t*>(cb + (sub * 32 + r) * 64);
+      *reinterpret_cast<uint4*>(tile + swz(r, m)) = dq8(c4, s2);
+    }
+  }
+}
+
+// Down: rows [64 sub, +64) of the block (codes [512 rows][64 B], scales [32][128 B]) -> the warp's
+// 16 columns of its box (boxes [chunk 2c | 2c+1], 64 rows x 64 columns) of the tile.
+__device__ __forceinline__ void dequant_dn(const uint8_t* codes, const uint8_t* scl, uint8_t* dq, int sub) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int box = warp >> 2;
+  const int m = (warp & 3) * 16 + 8 * (lane & 1);
+  const int col = box * 64 + m;
+  uint8_t* tile = dq + box * (64 * 128);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {  // rows in four 16-row scale groups
+    const int r = (lane >> 1) + 16 * i;
+    uint32_t s2[4];
+    scales8(scl + (sub * 4 + i) * 128 + col, s2);
+    const uint32_t c4 = *reinterpret_cast<const uint32_t*>(codes + (sub * 64 + r) * 64 + col / 2);
+    *reinterpret_cast<uint4*>(tile + swz(r, m)) = dq8(c4, s2);
+  }
 }
 
 // Consumer side of block j: this warp is done reading it.
@@ -579,7 +746,17 @@ __device__ void item_epilogue(Stream& S, const Item& it, const float* vals) {
   const int nt = it.nt, c0 = it.c * 128;
   if (it.kind == KIND_GU || it.kind == KIND_SGU) {  // vals[t][256]: gate columns, then up columns
     bf16* dst = it.kind == KIND_GU ? p.h : p.hs;
-    const int ld = it.kind == KIND_GU ? I : p.sw;
+    const int ld = it.kind == KIND_GU ? I : p.dense ? ID : IS;
+    if (p.fp4) {  // NVFP4: the matrices' tensor scales
+      const float tg = it.kind == KIND_GU ? __ldg(p.ts_gate + it.e) : p.ts_sgate;
+      const float tu = it.kind == KIND_GU ? __ldg(p.ts_up + it.e) : p.ts_sup;
+      for (int q = threadIdx.x; q < nt * 128; q += NCONS) {
+        const int t = q >> 7, j = q & 127;
+        const float g = vals[t * 256 + j] * tg, u = vals[t * 256 + 128 + j] * tu;
+        dst[(size_t)(it.row0 + t) * ld + c0 + j] = __float2bfloat16_rn(silu_f32(g) * u);
+      }
+      return;
+    }
     for (int q = threadIdx.x; q < nt * 128; q += NCONS) {
       const int t = q >> 7, j = q & 127;
       const float g = vals[t * 256 + j], u = vals[t * 256 + 128 + j];
@@ -594,15 +771,17 @@ __device__ void item_epilogue(Stream& S, const Item& it, const float* vals) {
       p.y[o] = __float2bfloat16_rn(v);
     }
   } else if (it.kind == KIND_SD) {  // vals[t][128]
+    const float ts = p.fp4 ? p.ts_sdown : 1.0f;
     for (int q = threadIdx.x; q < nt * 128; q += NCONS) {
       const int t = q >> 7, j = q & 127;
-      p.S[(size_t)(it.row0 + t) * H + c0 + j] = vals[q];
+      p.S[(size_t)(it.row0 + t) * H + c0 + j] = p.fp4 ? vals[q] * ts : vals[q];
     }
-  } else {  // routed down: rows scaled by their gate
+  } else {  // routed down: rows scaled by their gate (and, NVFP4, the matrix's tensor scale)
+    const float ts = p.fp4 ? __ldg(p.ts_down + it.e) : 1.0f;
     for (int q = threadIdx.x; q < nt * 128; q += NCONS) {
       const int t = q >> 7, j = q & 127;
       const int row = it.row0 + t;
-      p.Y[(size_t)row * H + c0 + j] = S.gw[S.perm[row]] * vals[q];
+      p.Y[(size_t)row * H + c0 + j] = p.fp4 ? S.gw[S.perm[row]] * (vals[q] * ts) : S.gw[S.perm[row]] * vals[q];
     }
   }
 }
@@ -674,7 +853,7 @@ __device__ void stage_inputs(Stream& S, const Item& it, int xlen, int k0 = 0) {
       else if (it.kind == KIND_SGU || it.kind == KIND_RT)
         src = p.xin + (size_t)(it.row0 + t) * H;
       else if (it.kind == KIND_SD)
-        src = p.hs + (size_t)(it.row0 + t) * p.sw + k0;
+        src = p.dense ? p.hs + (size_t)(it.row0 + t) * ID + k0 : p.hs + (size_t)(it.row0 + t) * IS;
       else
         src = p.h + (size_t)(it.row0 + t) * I;
       v = __ldcg(reinterpret_cast<const uint4*>(src) + k8);
@@ -726,8 +905,8 @@ __device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, i
   const bool gu = it.kind == KIND_GU || it.kind == KIND_SGU;
   // a shared down input longer than a staged row (a dense layer) is staged from the segment's
   // first K row, and restaged when the segment runs past the window
-  int k0 = (it.kind == KIND_SD && p.sw > H) ? kb_start * DN_ROWS : 0;
-  int xlen = it.kind == KIND_SD ? min(p.sw - k0, H) : it.kind == KIND_DN ? I : H;
+  int k0 = (p.dense && it.kind == KIND_SD) ? kb_start * DN_ROWS : 0;
+  int xlen = it.kind == KIND_SD ? (p.dense ? min(ID - k0, H) : IS) : it.kind == KIND_DN ? I : H;
   stage_inputs(S, it, xlen, k0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j0 = j;
@@ -743,10 +922,31 @@ __device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, i
     float d[2][2][4] = {};
     const uint32_t sub = uint32_t((warp >> 1) * (BLK_BYTES / 4));
     const int m0 = (warp & 1) * 32;
-    for (int q = 0; q < nblk; ++q, ++j) {
-      wait_full(S, j);
-      mma_pair(d, smem_u32(stage_ptr(S, j)) + sub, m0, GU_ROWS / 16, xs, xlen + XPAD, (kb_start + q) * GU_ROWS, two);
-      release(S, j);
+    if (p.fp4) {
+      // NVFP4 block of 256 rows: eight 32-row sub-tiles dequantised into the warp's part of the tile
+      uint8_t* dq = S.sm + fp4_dq_offset();
+      const uint32_t tile = smem_u32(dq) + uint32_t((warp >> 1) * (32 * 128));
+      for (int q = 0; q < nblk; ++q, ++j) {
+        wait_full(S, j);
+        const uint8_t* codes = stage_ptr(S, j);
+        const uint8_t* scl = S.sm + fp4_scl_offset() + ((S.ring + j) % NSTAGE) * FP4_SCALE_BYTES;
+        for (int s = 0; s < FP4_GU_ROWS / 32; ++s) {
+          dequant_gu(codes, scl, dq, s);
+          if (s == FP4_GU_ROWS / 32 - 1)
+            release(S, j);  // the codes and scales are read (release synchronises the warp first)
+          else
+            __syncwarp();
+          mma_pair(d, tile, m0, 2, xs, xlen + XPAD, (kb_start + q) * FP4_GU_ROWS + s * 32, two);
+          __syncwarp();  // before the next sub-tile overwrites the warp's part
+        }
+      }
+    } else {
+      for (int q = 0; q < nblk; ++q, ++j) {
+        wait_full(S, j);
+        mma_pair(d, smem_u32(stage_ptr(S, j)) + sub, m0, GU_ROWS / 16, xs, xlen + XPAD, (kb_start + q) * GU_ROWS,
+                 two);
+        release(S, j);
+      }
     }
     const int cb = (warp >> 1) * 64 + m0;
 #pragma unroll
@@ -763,17 +963,37 @@ __device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, i
     float d[2][4] = {};
     const uint32_t sub = uint32_t((warp >> 2) * (BLK_BYTES / 2));
     const int m0 = (warp & 3) * 16;
-    for (int q = 0; q < nblk; ++q, ++j) {
-      const int kr = (kb_start + q) * DN_ROWS;  // first K row of this block
-      if (kr - k0 >= xlen) {  // past the staged window (dense layers only; warp-uniform, all warps)
-        csync();  // every warp is done with the window
-        k0 = kr;
-        xlen = min(p.sw - k0, H);
-        stage_inputs(S, it, xlen, k0);
+    if (p.fp4) {
+      // NVFP4 block of 512 rows: eight 64-row sub-tiles
+      uint8_t* dq = S.sm + fp4_dq_offset();
+      const uint32_t tile = smem_u32(dq) + uint32_t((warp >> 2) * (64 * 128));
+      for (int q = 0; q < nblk; ++q, ++j) {
+        wait_full(S, j);
+        const uint8_t* codes = stage_ptr(S, j);
+        const uint8_t* scl = S.sm + fp4_scl_offset() + ((S.ring + j) % NSTAGE) * FP4_SCALE_BYTES;
+        for (int s = 0; s < FP4_DN_ROWS / 64; ++s) {
+          dequant_dn(codes, scl, dq, s);
+          if (s == FP4_DN_ROWS / 64 - 1)
+            release(S, j);
+          else
+            __syncwarp();
+          mma_tile(d, tile, m0, 0, 4, xs, xlen + XPAD, (kb_start + q) * FP4_DN_ROWS + s * 64 - k0, two);
+          __syncwarp();
+        }
       }
-      wait_full(S, j);
-      mma_tile(d, smem_u32(stage_ptr(S, j)) + sub, m0, 0, DN_ROWS / 16, xs, xlen + XPAD, kr - k0, two);
-      release(S, j);
+    } else {
+      for (int q = 0; q < nblk; ++q, ++j) {
+        const int kr = (kb_start + q) * DN_ROWS;  // first K row of this block
+        if (p.dense && kr - k0 >= xlen) {  // past the staged window (dense layers only; all warps)
+          csync();  // every warp is done with the window
+          k0 = kr;
+          xlen = min(ID - k0, H);
+          stage_inputs(S, it, xlen, k0);
+        }
+        wait_full(S, j);
+        mma_tile(d, smem_u32(stage_ptr(S, j)) + sub, m0, 0, DN_ROWS / 16, xs, xlen + XPAD, kr - k0, two);
+        release(S, j);
+      }
     }
     const int cb = (warp >> 2) * 64 + m0;
 #pragma unroll
@@ -825,7 +1045,7 @@ __device__ void consume(Stream& S) {
   while (j < S.nb) {
     int kind, idx, kb;
     block_kind(S.L, S.b0 + j, kind, idx, kb);
-    const Item it = decode_item(S.p->T, S.p->sw / 128, S.meta, kind, idx);  // shared-memory lookups only
+    const Item it = decode_item(*S.p, S.meta, kind, idx);  // shared-memory lookups only
     if (kind == KIND_RT)
       run_router_block(S, it, j);
     else
@@ -1092,7 +1312,7 @@ __device__ Meta build_tables(const Params& p, uint8_t* sm, uint16_t* perm, uint1
 // the gate/up of the whole width, a barrier, step D the down projection, whose items write
 // y = bf16(MLP(x') [+ x]) directly (no router, no routing, no combine).
 __device__ void dense_layer(Stream& S, const Params& p, int ntg) {
-  const int sncb = p.sw / 128;
+  constexpr int sncb = ID / 128;
   {
     BlockList L;
     L.k_first = L.k_second = KIND_SGU;
@@ -1108,9 +1328,9 @@ __device__ void dense_layer(Stream& S, const Params& p, int ntg) {
   {
     BlockList L;
     L.k_first = L.k_second = KIND_SD;
-    L.kb_first = L.kb_second = sncb;
+    L.kb_first = L.kb_second = ID / DN_ROWS;
     L.n_first = 0;
-    L.n_total = ntg * OUT_NCB * sncb;
+    L.n_total = ntg * OUT_NCB * (ID / DN_ROWS);
     set_step(S, L);
   }
   const int pre = p.T <= PREISSUE_MAX_T ? min(1, S.nb) : 0;
@@ -1180,7 +1400,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // routed experts: its blocks stream from L2 while the routed ones stream from HBM, and a
   // short step A starts the routing sooner; measured 908 vs 944 us over the decode sweep.)
   {
-    if (full && threadIdx.x == NCONS + 1) prefetch_share(p.ws_down, uint32_t(IS) * H * 2);
+    if (full && threadIdx.x == NCONS + 1) {
+      if (p.fp4)
+        prefetch_share(p.q_sdown, uint32_t(IS) * H / 2);
+      else
+        prefetch_share(p.ws_down, uint32_t(IS) * H * 2);
+    }
     BlockList L;
     L.k_first = L.k_second = KIND_RT;
     L.kb_first = L.kb_second = 1;
@@ -1227,9 +1452,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // ---- step C: routed gate/up and the shared gate/up
   {
     // the touched experts' down matrices are read in step D: prefetch them when they fit
-    if (threadIdx.x == NCONS + 1 && (unsigned long long)S.meta.U * I * H * 2 <= p.prefetch_bytes_max) {
+    const uint32_t per_e = p.fp4 ? uint32_t(I) * H / 2 : uint32_t(I) * H * 2;  // codes / bf16 bytes
+    const uint8_t* dbase = p.fp4 ? p.q_down : reinterpret_cast<const uint8_t*>(p.w_down);
+    if (threadIdx.x == NCONS + 1 && (unsigned long long)S.meta.U * per_e <= p.prefetch_bytes_max) {
       // 32-bit offsets: U * I * H * 2 <= 512 MB
-      constexpr uint32_t per_e = uint32_t(I) * H * 2;
       const uint32_t total = per_e * uint32_t(S.meta.U);
       const uint32_t share = ((total / gridDim.x) + 15u) & ~15u;
       uint32_t a = share * blockIdx.x;
@@ -1240,18 +1466,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         uint32_t n = per_e - in_e;
         if (n > b - a) n = b - a;
         if (n > 65536u) n = 65536u;
-        prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(p.w_down + (size_t)S.meta.e[u] * I * H) + in_e,
-                         uint32_t(n));
+        prefetch_l2_bulk(dbase + (size_t)S.meta.e[u] * per_e + in_e, uint32_t(n));
         a += n;
       }
     }
     BlockList L;
+    const int kgu = kblocks_of(p, KIND_GU);
     L.k_first = KIND_GU;
-    L.kb_first = GU_KB;
-    L.n_first = S.meta.groups * GU_NCB * GU_KB;
+    L.kb_first = kgu;
+    L.n_first = S.meta.groups * GU_NCB * kgu;
     L.k_second = KIND_SGU;
-    L.kb_second = GU_KB;
-    L.n_total = L.n_first + ntg * SGU_NCB * GU_KB;
+    L.kb_second = kgu;
+    L.n_total = L.n_first + ntg * SGU_NCB * kgu;
     S.first_slot = 12;
     trace_point(p, 6);
     set_step(S, L);
@@ -1265,12 +1491,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // calls, slow the CTAs still streaming step C, which set the barrier's time.)
   {
     BlockList L;
+    const int kdn = kblocks_of(p, KIND_DN), ksd = kblocks_of(p, KIND_SD);
     L.k_first = KIND_DN;
-    L.kb_first = DN_KB;
-    L.n_first = S.meta.groups * OUT_NCB * DN_KB;
+    L.kb_first = kdn;
+    L.n_first = S.meta.groups * OUT_NCB * kdn;
     L.k_second = KIND_SD;
-    L.kb_second = SD_KB;
-    L.n_total = L.n_first + ntg * OUT_NCB * SD_KB;
+    L.kb_second = ksd;
+    L.n_total = L.n_first + ntg * OUT_NCB * ksd;
     set_step(S, L);
   }
   const int pre = T <= PREISSUE_MAX_T ? min(1, S.nb) : 0;

@@ -13,6 +13,7 @@
 #include "common.cuh"
 #include "decode_fused.cuh"
 #include "prefill_kernels.cuh"
+#include "swa_attention.cuh"
 
 using namespace flint;
 
@@ -31,6 +32,7 @@ struct Layout {
   size_t counts, offsets, perm, inv, topk_idx, topk_w;
   size_t xn, xstage, ystage, h, hs, S, Y, P, RP, trace;
   size_t xs, Yb, hist, mtp;  // prefill path (max_tokens > STREAM_MAX_T), else 0
+  size_t fp4maps;            // the NVFP4 tensor maps of a handle on NVFP4 weights
   size_t total;
 };
 
@@ -82,6 +84,7 @@ Layout make_layout(int max_tokens, int sw = IS, bool dense = false) {
     L.mtp = take(sizeof(int32_t) * (E + 1));
   }
   L.trace = take(sizeof(unsigned long long) * MAX_TRACE_CTAS * TRACE_SLOTS);
+  L.fp4maps = take(sizeof(Fp4Maps));
   L.total = align_up(off, 256);
   return L;
 }
@@ -119,6 +122,22 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Row-major uint8 matrix [rows][cols] (NVFP4 codes or scales) -> 2-D tensor map, box of box_cols
+// bytes x box_rows, no swizzle.
+bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                 uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 struct flint_moe_stack_s {
@@ -134,6 +153,8 @@ struct flint_moe_s {
   flint_moe_weights w;
   int sw;      // the shared expert's width (IS), or the dense layer's (ID)
   int dense;   // 1: a dense SwiGLU MLP layer (flint_dense_*): the shared-expert path alone
+  int fp4;     // 1: NVFP4 expert weights (flint_moe_create_nvfp4)
+  flint_moe_nvfp4_weights q;  // the NVFP4 weights (fp4)
   int device;
   int n_sm;
   uint8_t* ws;
@@ -172,6 +193,18 @@ Params make_params(flint_moe_t h, const void* x, int T, void* y, int32_t* out_id
   p.rms_eps = h->cfg.rms_eps;
   p.sw = h->sw;
   p.dense = h->dense;
+  p.fp4 = h->fp4;
+  if (h->fp4) {
+    p.ts_gate = h->q.gate_tscale;
+    p.ts_up = h->q.up_tscale;
+    p.ts_down = h->q.down_tscale;
+    p.ts_sgate = h->q.sgate_tscale;
+    p.ts_sup = h->q.sup_tscale;
+    p.ts_sdown = h->q.sdown_tscale;
+    p.q_down = h->q.down_codes;
+    p.q_sdown = h->q.sdown_codes;
+    p.fp4_maps = ws + L.fp4maps;
+  }
   p.x = static_cast<const bf16*>(x);
   p.xn = reinterpret_cast<bf16*>(ws + L.xn);
   p.xin = (h->cfg.flags & FLINT_MOE_FLAG_PRE_RMSNORM) ? p.xn : p.x;
@@ -261,7 +294,7 @@ flint_moe_status run_decode_maps(flint_moe_t h, const Params& p, const StreamMap
   if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
   const int grid = h->n_sm < MAX_STREAM_CTAS ? h->n_sm : MAX_STREAM_CTAS;
   e = launch(h, full ? "decode_fused" : "decode_fused_route", decode_fused, grid, NTHREADS,
-             fused_smem_bytes(group_rows(p.T)), st, true, p, maps, full ? 0 : 1);
+             h->fp4 ? fp4_smem_bytes() : fused_smem_bytes(group_rows(p.T)), st, true, p, maps, full ? 0 : 1);
   return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ERR_CUDA;
 }
 
@@ -396,9 +429,11 @@ flint_moe_status flint_moe_workspace_bytes(const flint_moe_config* cfg, size_t* 
 namespace {
 
 // A handle on validated arguments: the MoE layer (sw = IS, dense = false; every weight pointer
-// set) or a dense layer (sw = ID, dense = true; only the shared-expert pointers of `w` are used).
+// set), a dense layer (sw = ID, dense = true; only the shared-expert pointers of `w` are used) or
+// an NVFP4 MoE layer (router_only: only the router's maps here; the caller adds the NVFP4 ones).
 flint_moe_status create_handle(const flint_moe_config* cfg, const flint_moe_weights* w, void* workspace,
-                               size_t workspace_bytes, int swidth, bool dense, flint_moe_t* out) {
+                               size_t workspace_bytes, int swidth, bool dense, flint_moe_t* out,
+                               bool router_only = false) {
   Layout L = make_layout(cfg->max_tokens, swidth, dense);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < L.total)
     return FLINT_MOE_ERR_WORKSPACE;
@@ -431,10 +466,11 @@ flint_moe_status create_handle(const flint_moe_config* cfg, const flint_moe_weig
   }
   const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
   const uint64_t S = (uint64_t)swidth;
-  bool ok = make_map(&h->smaps.wsg, w->ws_gate, H, S, 64, GU_ROWS, sw) &&
-            make_map(&h->smaps.wsu, w->ws_up, H, S, 64, GU_ROWS, sw) &&
-            make_map(&h->smaps.wsd, w->ws_down, S, H, 64, DN_ROWS, sw);
-  if (ok && !dense)
+  bool ok = router_only ? make_map(&h->smaps.wr, w->w_router, H, E, 64, RT_ROWS, sw)
+                        : make_map(&h->smaps.wsg, w->ws_gate, H, S, 64, GU_ROWS, sw) &&
+                              make_map(&h->smaps.wsu, w->ws_up, H, S, 64, GU_ROWS, sw) &&
+                              make_map(&h->smaps.wsd, w->ws_down, S, H, 64, DN_ROWS, sw);
+  if (ok && !dense && !router_only)
     ok = make_map(&h->smaps.wr, w->w_router, H, E, 64, RT_ROWS, sw) &&
          make_map(&h->smaps.wg, w->w_gate, (uint64_t)E * H, I, 64, GU_ROWS, sw) &&
          make_map(&h->smaps.wu, w->w_up, (uint64_t)E * H, I, 64, GU_ROWS, sw) &&
@@ -937,3 +973,156 @@ flint_moe_status flint_dense_destroy(flint_dense_t d) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------------
+// Decode attention of the sliding-window layers (swa_attention.cuh).  The workspace: the status
+// word, one ticket per (sequence, KV head), the chunk partials.
+namespace {
+
+constexpr int SWA_MAX_BATCH = 65535;  // the grid's z extent
+
+struct SwaLayout {
+  size_t status, ticket, zero_end, part, total;
+};
+
+SwaLayout swa_layout(int max_batch) {
+  SwaLayout L{};
+  L.status = 0;
+  L.ticket = 256;
+  L.zero_end = align_up(L.ticket + sizeof(uint32_t) * (size_t)max_batch * swa::NKV, 256);
+  L.part = L.zero_end;
+  L.total = align_up(L.part + sizeof(float) * (size_t)max_batch * swa::NH * swa::NSPLIT * swa::PSTRIDE, 256);
+  return L;
+}
+
+// The largest batch a workspace of `bytes` holds (0 if none).
+int swa_capacity(size_t bytes) {
+  int lo = 0, hi = SWA_MAX_BATCH;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) / 2;
+    if (swa_layout(mid).total <= bytes)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+}  // namespace
+
+extern "C" {
+
+flint_moe_status flint_swa_workspace_bytes(int max_batch, size_t* bytes) {
+  if (!bytes || max_batch < 1 || max_batch > SWA_MAX_BATCH) return FLINT_MOE_ERR_INVALID_ARG;
+  *bytes = swa_layout(max_batch).total;
+  return FLINT_MOE_OK;
+}
+
+flint_moe_status flint_swa_workspace_init(void* workspace, size_t workspace_bytes, flint_stream_t stream) {
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FLINT_MOE_ERR_WORKSPACE;
+  const int cap = swa_capacity(workspace_bytes);
+  if (cap < 1) return FLINT_MOE_ERR_WORKSPACE;
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return FLINT_MOE_ERR_CUDA;
+  if (major != 10 || minor != 3) return FLINT_MOE_ERR_UNSUPPORTED;
+  const SwaLayout L = swa_layout(cap);
+  return cudaMemsetAsync(workspace, 0, L.zero_end, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FLINT_MOE_OK
+             : FLINT_MOE_ERR_CUDA;
+}
+
+flint_moe_status flint_swa_decode(void* workspace, size_t workspace_bytes, const void* q, const void* k_cache,
+                                  const void* v_cache, const float* sinks, const int32_t* pos, int B, void* out,
+                                  flint_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !sinks || !pos || !out) return FLINT_MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k_cache, v_cache, out};
+  for (const void* x : ptrs)
+    if (!aligned16(x)) return FLINT_MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(sinks) & 3u) || (reinterpret_cast<uintptr_t>(pos) & 3u))
+    return FLINT_MOE_ERR_INVALID_ARG;
+  if (B < 1 || B > SWA_MAX_BATCH) return FLINT_MOE_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FLINT_MOE_ERR_WORKSPACE;
+  const int cap = swa_capacity(workspace_bytes);
+  if (B > cap) return FLINT_MOE_ERR_WORKSPACE;
+  const SwaLayout L = swa_layout(cap);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  swa::Params p{};
+  p.q = static_cast<const bf16*>(q);
+  p.k = static_cast<const bf16*>(k_cache);
+  p.v = static_cast<const bf16*>(v_cache);
+  p.sinks = sinks;
+  p.pos = pos;
+  p.out = static_cast<bf16*>(out);
+  p.B = B;
+  p.part = reinterpret_cast<float*>(ws + L.part);
+  p.ticket = reinterpret_cast<uint32_t*>(ws + L.ticket);
+  p.status = reinterpret_cast<uint32_t*>(ws + L.status);
+  swa::decode_kernel<<<dim3(swa::NSPLIT, swa::NKV, B), swa::NT, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  return cudaGetLastError() == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ERR_CUDA;
+}
+
+flint_moe_status flint_swa_poll_device_status(void* workspace, flint_stream_t stream) {
+  if (!workspace) return FLINT_MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  if (word == 0) return FLINT_MOE_OK;
+  if (cudaMemset(workspace, 0, sizeof word) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  return (word & ST_TIMEOUT) ? FLINT_MOE_ERR_DEVICE_TIMEOUT : FLINT_MOE_ERR_DEVICE_BOUNDS;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------------------------------
+// NVFP4 expert weights (decode sizes): the handle carries the codes, scales and tensor scales of
+// the routed and shared experts; the router stays bf16.  Every call runs the decode-size kernel
+// with its NVFP4 stream (decode_fused.cuh).
+extern "C" flint_moe_status flint_moe_create_nvfp4(const flint_moe_config* cfg, const flint_moe_nvfp4_weights* w,
+                                                   void* workspace, size_t workspace_bytes, flint_moe_t* out) {
+  if (!out) return FLINT_MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  flint_moe_status s = check_config(cfg);
+  if (s != FLINT_MOE_OK) return s;
+  if (cfg->max_tokens > FP4_MAX_T) return FLINT_MOE_ERR_UNSUPPORTED;
+  if (!w || !w->w_router || !aligned16(w->w_router)) return FLINT_MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {w->gate_codes, w->up_codes, w->down_codes, w->gate_scales, w->up_scales, w->down_scales,
+                        w->sgate_codes, w->sup_codes, w->sdown_codes, w->sgate_scales, w->sup_scales, w->sdown_scales};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return FLINT_MOE_ERR_INVALID_ARG;
+  if (!w->gate_tscale || !w->up_tscale || !w->down_tscale) return FLINT_MOE_ERR_INVALID_ARG;
+  if (w->router_bias && (reinterpret_cast<uintptr_t>(w->router_bias) & 3u)) return FLINT_MOE_ERR_INVALID_ARG;
+  // the handle's bf16 maps cover the router only; the expert maps are the NVFP4 ones
+  flint_moe_weights bw{};
+  bw.w_router = w->w_router;
+  bw.router_bias = w->router_bias;
+  s = create_handle(cfg, &bw, workspace, workspace_bytes, IS, false, out, true);
+  if (s != FLINT_MOE_OK) return s;
+  flint_moe_t h = *out;
+  h->fp4 = 1;
+  h->q = *w;
+  Fp4Maps m;
+  const uint64_t EH = (uint64_t)E * H, EI = (uint64_t)E * I;
+  const bool ok =
+      make_map_u8(&m.qg, w->gate_codes, EH, I / 2, 64, FP4_GU_ROWS) &&
+      make_map_u8(&m.qu, w->up_codes, EH, I / 2, 64, FP4_GU_ROWS) &&
+      make_map_u8(&m.qd, w->down_codes, EI, H / 2, 64, FP4_DN_ROWS / 2) &&
+      make_map_u8(&m.qsg, w->sgate_codes, H, IS / 2, 64, FP4_GU_ROWS) &&
+      make_map_u8(&m.qsu, w->sup_codes, H, IS / 2, 64, FP4_GU_ROWS) &&
+      make_map_u8(&m.qsd, w->sdown_codes, IS, H / 2, 64, FP4_DN_ROWS / 2) &&
+      make_map_u8(&m.sg, w->gate_scales, EH / 16, I, 128, FP4_GU_ROWS / 16) &&
+      make_map_u8(&m.su, w->up_scales, EH / 16, I, 128, FP4_GU_ROWS / 16) &&
+      make_map_u8(&m.sd, w->down_scales, EI / 16, H, 128, FP4_DN_ROWS / 16) &&
+      make_map_u8(&m.ssg, w->sgate_scales, H / 16, IS, 128, FP4_GU_ROWS / 16) &&
+      make_map_u8(&m.ssu, w->sup_scales, H / 16, IS, 128, FP4_GU_ROWS / 16) &&
+      make_map_u8(&m.ssd, w->sdown_scales, IS / 16, H, 128, FP4_DN_ROWS / 16) &&
+      cudaMemcpy(h->ws + h->L.fp4maps, &m, sizeof m, cudaMemcpyHostToDevice) == cudaSuccess;
+  if (!ok) {
+    flint_moe_destroy(h);
+    *out = nullptr;
+    return FLINT_MOE_ERR_CUDA;
+  }
+  return FLINT_MOE_OK;
+}

@@ -229,3 +229,38 @@ def check_counts(ref_all, idx_gpu, counts_gpu):
     if ref_all is not None and not (ref_all["gaps"][:, 5] <= GAP).any():
         ok = ok and np.array_equal(c_g, np.bincount(ref_all["idx"].reshape(-1), minlength=256))
     return ok
+
+
+def nvfp4_host_layer(w, q, experts):
+    """The oracle's layer for NVFP4 expert weights: the router and bias of ``w`` (bf16 weights
+    dict) and, for the given routed experts and the shared expert, the dequantised NVFP4 values
+    (oracle.nvfp4_dequant; bf16-exact with the generator's power-of-two tensor scales)."""
+    def dq(codes, scales, ts):
+        return oracle.f64_to_bf16_exact(oracle.nvfp4_dequant(codes.cpu().numpy(), scales.cpu().numpy(), float(ts)))
+
+    wr = to_np_bf16(w["w_router"])
+    b = None if w.get("router_bias") is None else w["router_bias"].detach().float().cpu().numpy()
+    routed = {}
+    for name in ("w_gate", "w_up", "w_down"):
+        c, s, t = q[name]
+        routed[name] = {int(e): dq(c[int(e)], s[int(e)], t[int(e)].item()) for e in experts}
+    shared = {name: dq(*q[name]) for name in ("ws_gate", "ws_up", "ws_down")}
+    return oracle.Layer(wr, routed["w_gate"], routed["w_up"], routed["w_down"], shared["ws_gate"], shared["ws_up"],
+                        shared["ws_down"], router_bias=b, k=6)
+
+
+def oracle_reference_nvfp4(w, q, x, tokens, nthreads=ORACLE_THREADS, residual=False, eps=None):
+    """oracle_reference for a layer on NVFP4 expert weights ``q`` (router from ``w``)."""
+    x64 = oracle.bf16_to_f64(to_np_bf16(x))
+    tokens = np.asarray(tokens, dtype=np.int64)
+    xin = x64 if eps is None else oracle.prenorm_input(x64, eps)
+    experts = touched_experts(w, xin, tokens)
+    layer = nvfp4_host_layer(w, q, experts)
+    out = oracle.forward(layer, xin[tokens], nthreads=nthreads, want_scores=True)
+    if residual:
+        out["y"] = x64[tokens] + out["y"]
+    out["tokens"] = tokens
+    out["layer"] = layer
+    out["xin"] = xin[tokens]
+    out["xres"] = x64[tokens] if residual else None
+    return out

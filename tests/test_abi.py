@@ -18,7 +18,7 @@ def declared_functions():
         if fn.endswith(".h"):
             src = open(os.path.join(inc, fn)).read()
             src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-            names += re.findall(r"\b(flint_(?:moe|dense)_\w+)\s*\(", src)
+            names += re.findall(r"\b(flint_(?:moe|dense|swa)_\w+)\s*\(", src)
     return sorted(set(names))
 
 
