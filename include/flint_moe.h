@@ -202,7 +202,7 @@ flint_moe_status flint_moe_create_nvfp4(const flint_moe_config* cfg, const flint
  * a property of this library, not of the method.
  *   w, x, y, topk_idx, topk_w, stream: as for flint_moe_create / flint_moe_forward (no flags:
  *   no pre-norm, no residual); 1 <= T <= 4, a larger T returns FLINT_MOE_ERR_UNSUPPORTED.
- * Scratch memory comes from one fixed array of 17 MiB that the library declares in device
+ * Scratch memory comes from one fixed array of 25 MiB that the library declares in device
  * memory; every GPU that loads the library holds it until the process exits.  The call makes
  * no allocation.  The first call on a device (with that device current) looks up the array's
  * device address, sets the kernel's shared-memory limit, checks that one CTA fits on every SM

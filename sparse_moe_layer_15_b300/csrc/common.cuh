@@ -70,7 +70,7 @@ struct Params {
   bf16* hs;              // [T][sw] shared SwiGLU activations
   float* Y;              // [T*K][H] gated routed expert outputs
   float* S;              // [T][H] shared expert output
-  float* P;              // [MAX_STREAM_CTAS][2][PSLOT] split-item partial sums (decode path)
+  float* P;              // [2 steps][MAX_STREAM_CTAS][2][PSLOT] split-item partial sums (decode path)
   float* RP;             // [32][256][E] router partial logits (decode path)
   bf16* xs;              // [T*K][H] expert-sorted input rows (prefill path)
   bf16* Yb;              // [T*K][H] gated routed expert outputs, bf16 (prefill path)
@@ -83,6 +83,8 @@ struct Params {
   uint32_t* tk_sd;
   uint32_t* tk_dn;
   uint32_t* tk_comb;     // [H/128] down items finished per 128-column block (decode path)
+  uint32_t* hdone;       // [routed groups] gate/up items finished per routed token group (decode path)
+  uint32_t* hsdone;      // [shared groups] shared gate/up items finished per token group (decode path)
   // user-visible copies (may be null)
   int32_t* out_idx;
   float* out_w;

@@ -86,6 +86,12 @@ struct Fp4Maps {
   CUtensorMap sg, su, sd, ssg, ssu, ssd;  // scales: [E*H/16][I], ., [E*I/16][H], [H/16][IS], ., [IS/16][H]
 };
 
+// Kernel modes, each its own instantiation (the bf16 MoE kernel carries no code of the others:
+// its latency-bound phases run cold instruction fetches once per call).
+constexpr int MODE_MOE = 0;    // the MoE layer, bf16 weights
+constexpr int MODE_FP4 = 1;    // the MoE layer, NVFP4 expert weights
+constexpr int MODE_DENSE = 2;  // a dense SwiGLU MLP layer (the shared-expert steps at width ID)
+
 // ---- NVFP4 streaming (decode sizes): a block is 256 rows x 128 columns of gate and of up (32 KB of
 // codes + 4 KB of scales), or 512 rows x 128 columns of a down matrix (the same sizes); the codes
 // land in the stage ring, the scales in a ring of 4 KB slots beside it.  Each warp dequantises
@@ -363,9 +369,13 @@ __device__ bool grid_sync(const Params& p, int k, int* s_flag) {
   return *s_flag != 0;
 }
 
-// After the last barrier: the last CTA to get here resets the barrier counter.
-__device__ void grid_done(const Params& p, int* s_flag) {
-  if (ticket_last(p.bar_done, gridDim.x, s_flag, true) && threadIdx.x == 0) atomicExch(p.bar_count, 0u);
+// After the last barrier: the last CTA to get here resets the barrier counter and the first
+// `ng` routed and `ns` shared token-group counters of the dataflow (every CTA is done with them).
+__device__ void grid_done(const Params& p, int* s_flag, int ng = 0, int ns = 0) {
+  if (!ticket_last(p.bar_done, gridDim.x, s_flag, true)) return;
+  if (threadIdx.x == 0) atomicExch(p.bar_count, 0u);
+  for (int i = threadIdx.x; i < ng; i += blockDim.x) p.hdone[i] = 0u;
+  for (int i = threadIdx.x; i < ns; i += blockDim.x) p.hsdone[i] = 0u;
 }
 
 // Wait for an mbarrier phase; on running out of time record ST_TIMEOUT and go on (the
@@ -421,19 +431,21 @@ __device__ __forceinline__ int find_group_owner(const int* tgp, int n, int gi) {
 // usually share their token group and its staged input rows.
 // K blocks per item of a kind: 64-row (gate/up) or 128-row (down) bf16 blocks, or the NVFP4
 // blocks of 256 / 512 rows.
+template <int MODE>
 __device__ __forceinline__ int kblocks_of(const Params& p, int kind) {
   switch (kind) {
     case KIND_RT: return 1;
     case KIND_GU:
-    case KIND_SGU: return p.fp4 ? FP4_GU_KB : GU_KB;
-    case KIND_DN: return p.fp4 ? FP4_DN_KB : DN_KB;
-    default: return p.fp4 ? FP4_SD_KB : p.dense ? ID / DN_ROWS : SD_KB;
+    case KIND_SGU: return MODE == MODE_FP4 ? FP4_GU_KB : GU_KB;
+    case KIND_DN: return MODE == MODE_FP4 ? FP4_DN_KB : DN_KB;
+    default: return MODE == MODE_FP4 ? FP4_SD_KB : MODE == MODE_DENSE ? ID / DN_ROWS : SD_KB;
   }
 }
 
+template <int MODE>
 __device__ __forceinline__ Item decode_item(const Params& p, const Meta& m, int kind, int idx) {
   const int T = p.T;
-  const int sncb = p.dense ? ID / 128 : SGU_NCB;  // 128-column blocks of the shared gate/up
+  const int sncb = MODE == MODE_DENSE ? ID / 128 : SGU_NCB;  // 128-column blocks of the shared gate/up
   Item it;
   it.kind = kind;
   it.idx = idx;
@@ -447,17 +459,16 @@ __device__ __forceinline__ Item decode_item(const Params& p, const Meta& m, int 
     it.e = m.e[u];
     it.row0 = m.off[u] + tg * G;
     it.nt = min(G, m.cnt[u] - tg * G);
-    it.KB = kblocks_of(p, kind);
+    it.KB = kblocks_of<MODE>(p, kind);
   } else {
-    // (the MoE's column-block counts are powers of two: shifts; a dense layer's 48 divides)
-    const int nch = kind == KIND_RT ? RT_NB : kind == KIND_SGU ? (p.dense ? sncb : SGU_NCB) : OUT_NCB;
-    const int tg = p.dense ? idx / nch : idx / (kind == KIND_RT ? RT_NB : kind == KIND_SGU ? SGU_NCB : OUT_NCB);
-    it.c = idx - tg * nch;
+    const int nch = kind == KIND_RT ? RT_NB : kind == KIND_SGU ? sncb : OUT_NCB;
+    const int tg = idx / nch;
+    it.c = idx % nch;
     const int G = group_rows(T);
     it.e = -1;
     it.row0 = tg * G;
     it.nt = min(G, T - tg * G);
-    it.KB = kblocks_of(p, kind);
+    it.KB = kblocks_of<MODE>(p, kind);
   }
   return it;
 }
@@ -523,12 +534,13 @@ __device__ void issue_block_fp4(const Item& it, const Fp4Maps& maps, int kb, uin
   }
 }
 
+template <int MODE>
 __device__ void issue_block(const Params& p, const Meta& m, const StreamMaps& maps, const BlockList& L, int b,
                             uint8_t* stage, uint64_t* bar, uint8_t* scl) {
   int kind, idx, kb;
   block_kind(L, b, kind, idx, kb);
-  const Item it = decode_item(p, m, kind, idx);
-  if (p.fp4 && kind != KIND_RT) {
+  const Item it = decode_item<MODE>(p, m, kind, idx);
+  if (MODE == MODE_FP4 && kind != KIND_RT) {
     issue_block_fp4(it, *static_cast<const Fp4Maps*>(p.fp4_maps), kb, stage, scl, bar);
     return;
   }
@@ -587,6 +599,8 @@ struct Stream {
   int* plist;  // partial slots of the item being finished
   float* out;  // output tile of the current segment
   int comb_items;  // > 0: combine each 128-column block when its comb_items down items are done
+  bool dataflow;   // gate/up items signal their token group; down items wait for theirs (no C-D barrier)
+  float* pbank;    // the current step's partial slots (steps C and D use separate banks)
   const uint16_t* perm;
   const uint16_t* inv;
   const float* gw;
@@ -597,13 +611,14 @@ __device__ __forceinline__ uint8_t* stage_ptr(const Stream& S, int j) {
 }
 
 // Producer (one lane): issue blocks [from, to) of this CTA's range of the step into the stage ring.
+template <int MODE>
 __device__ void produce(Stream& S, int from, int to) {
   for (int j = from; j < to; ++j) {
     const int pos = S.ring + j;
     const int st = pos % NSTAGE;
     const int use = pos / NSTAGE;
     if (use > 0) mbar_wait_or_flag(S.empty + st, uint32_t(use - 1) & 1u, S.p->status);
-    issue_block(*S.p, S.meta, *S.maps, S.L, S.b0 + j, S.sm + Smem::stages + st * BLK_BYTES, S.full + st,
+    issue_block<MODE>(*S.p, S.meta, *S.maps, S.L, S.b0 + j, S.sm + Smem::stages + st * BLK_BYTES, S.full + st,
                 S.sm + fp4_scl_offset() + st * FP4_SCALE_BYTES);
   }
 }
@@ -699,9 +714,38 @@ __device__ __forceinline__ void release(Stream& S, int j) {
   if ((threadIdx.x & 31) == 0) mbar_arrive(S.empty + (S.ring + j) % NSTAGE);
 }
 
-// Partial slot `slot` (0: the piece that opens CTA `cta`'s range, 1: the piece that closes it).
-__device__ __forceinline__ float* partial_slot(const Params& p, int cta, int slot) {
-  return p.P + ((size_t)cta * 2 + slot) * PSLOT;
+// Partial slot `slot` (0: the piece that opens CTA `cta`'s range, 1: the piece that closes it) of
+// the current step's bank.
+__device__ __forceinline__ float* partial_slot(const Stream& S, int cta, int slot) {
+  return S.pbank + ((size_t)cta * 2 + slot) * PSLOT;
+}
+
+// Partial-slot bank of step C (0) or D (1): without a grid barrier between the two steps a CTA
+// may start writing its step-D pieces while another CTA still adds up its step-C ones.
+__device__ __forceinline__ float* partial_bank(const Params& p, int bank) {
+  return p.P + (size_t)bank * MAX_STREAM_CTAS * 2 * PSLOT;
+}
+
+// ---- dataflow between the gate/up and down steps
+// The CTA that finishes a gate/up item (its outputs written by all consumers) adds 1 to the
+// counter of the item's token group (consumers).
+__device__ __forceinline__ void signal_done(uint32_t* ctr) {
+  __threadfence();
+  csync();
+  if (threadIdx.x == 0) atomicAdd(ctr, 1u);
+}
+// Wait (thread 0, bounded; then the consumers) until a token group's counter reaches `need`.
+__device__ __forceinline__ void wait_done(const Params& p, const uint32_t* ctr, uint32_t need) {
+  if (threadIdx.x == 0 && ld_acquire_u32(ctr) < need) {
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_acquire_u32(ctr) < need) {
+      if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+        record_status(p.status, ST_TIMEOUT);
+        break;
+      }
+    }
+  }
+  csync();
 }
 
 // First block of CTA c's range when n_total blocks are split over nctas CTAs (32-bit: the
@@ -741,13 +785,14 @@ __device__ __forceinline__ uint32_t* item_ticket(const Params& p, const Item& it
 }
 
 // Final values of an item (fp32 sums [nt][ncol] in `vals`) -> outputs.
+template <int MODE>
 __device__ void item_epilogue(Stream& S, const Item& it, const float* vals) {
   const Params& p = *S.p;
   const int nt = it.nt, c0 = it.c * 128;
   if (it.kind == KIND_GU || it.kind == KIND_SGU) {  // vals[t][256]: gate columns, then up columns
     bf16* dst = it.kind == KIND_GU ? p.h : p.hs;
-    const int ld = it.kind == KIND_GU ? I : p.dense ? ID : IS;
-    if (p.fp4) {  // NVFP4: the matrices' tensor scales
+    const int ld = it.kind == KIND_GU ? I : MODE == MODE_DENSE ? ID : IS;
+    if constexpr (MODE == MODE_FP4) {  // NVFP4: the matrices' tensor scales
       const float tg = it.kind == KIND_GU ? __ldg(p.ts_gate + it.e) : p.ts_sgate;
       const float tu = it.kind == KIND_GU ? __ldg(p.ts_up + it.e) : p.ts_sup;
       for (int q = threadIdx.x; q < nt * 128; q += NCONS) {
@@ -755,14 +800,14 @@ __device__ void item_epilogue(Stream& S, const Item& it, const float* vals) {
         const float g = vals[t * 256 + j] * tg, u = vals[t * 256 + 128 + j] * tu;
         dst[(size_t)(it.row0 + t) * ld + c0 + j] = __float2bfloat16_rn(silu_f32(g) * u);
       }
-      return;
+    } else {
+      for (int q = threadIdx.x; q < nt * 128; q += NCONS) {
+        const int t = q >> 7, j = q & 127;
+        const float g = vals[t * 256 + j], u = vals[t * 256 + 128 + j];
+        dst[(size_t)(it.row0 + t) * ld + c0 + j] = __float2bfloat16_rn(silu_f32(g) * u);
+      }
     }
-    for (int q = threadIdx.x; q < nt * 128; q += NCONS) {
-      const int t = q >> 7, j = q & 127;
-      const float g = vals[t * 256 + j], u = vals[t * 256 + 128 + j];
-      dst[(size_t)(it.row0 + t) * ld + c0 + j] = __float2bfloat16_rn(silu_f32(g) * u);
-    }
-  } else if (it.kind == KIND_SD && p.dense) {  // a dense layer's output: y = bf16(vals [+ x])
+  } else if (it.kind == KIND_SD && MODE == MODE_DENSE) {  // a dense layer's output: y = bf16(vals [+ x])
     for (int q = threadIdx.x; q < nt * 128; q += NCONS) {
       const int t = q >> 7, j = q & 127;
       const size_t o = (size_t)(it.row0 + t) * H + c0 + j;
@@ -771,17 +816,17 @@ __device__ void item_epilogue(Stream& S, const Item& it, const float* vals) {
       p.y[o] = __float2bfloat16_rn(v);
     }
   } else if (it.kind == KIND_SD) {  // vals[t][128]
-    const float ts = p.fp4 ? p.ts_sdown : 1.0f;
+    const float ts = MODE == MODE_FP4 ? p.ts_sdown : 1.0f;
     for (int q = threadIdx.x; q < nt * 128; q += NCONS) {
       const int t = q >> 7, j = q & 127;
-      p.S[(size_t)(it.row0 + t) * H + c0 + j] = p.fp4 ? vals[q] * ts : vals[q];
+      p.S[(size_t)(it.row0 + t) * H + c0 + j] = MODE == MODE_FP4 ? vals[q] * ts : vals[q];
     }
   } else {  // routed down: rows scaled by their gate (and, NVFP4, the matrix's tensor scale)
-    const float ts = p.fp4 ? __ldg(p.ts_down + it.e) : 1.0f;
+    const float ts = MODE == MODE_FP4 ? __ldg(p.ts_down + it.e) : 1.0f;
     for (int q = threadIdx.x; q < nt * 128; q += NCONS) {
       const int t = q >> 7, j = q & 127;
       const int row = it.row0 + t;
-      p.Y[(size_t)row * H + c0 + j] = p.fp4 ? S.gw[S.perm[row]] * (vals[q] * ts) : S.gw[S.perm[row]] * vals[q];
+      p.Y[(size_t)row * H + c0 + j] = MODE == MODE_FP4 ? S.gw[S.perm[row]] * (vals[q] * ts) : S.gw[S.perm[row]] * vals[q];
     }
   }
 }
@@ -833,6 +878,7 @@ __device__ void combine_block(const Params& p, const uint16_t* inv, int cb) {
 // nt .. G-1 zero) for an item (consumers), unless they are the rows staged last (same source,
 // group and columns).  xlen <= H: a longer row (a dense layer's down input, 6144 wide) is staged
 // in windows.
+template <int MODE>
 __device__ void stage_inputs(Stream& S, const Item& it, int xlen, int k0 = 0) {
   const int cls = it.kind == KIND_GU ? 1 : it.kind == KIND_SD ? 2 : it.kind == KIND_DN ? 3 : 0;
   if (cls == S.x_cls && it.row0 == S.x_row0 && k0 == S.x_k0) return;
@@ -840,6 +886,8 @@ __device__ void stage_inputs(Stream& S, const Item& it, int xlen, int k0 = 0) {
   S.x_row0 = it.row0;
   S.x_k0 = k0;
   const Params& p = *S.p;
+  if (S.dataflow && it.kind == KIND_DN) wait_done(p, p.hdone + it.idx / OUT_NCB, GU_NCB);
+  if (S.dataflow && it.kind == KIND_SD) wait_done(p, p.hsdone + it.idx / OUT_NCB, MODE == MODE_DENSE ? ID / 128 : SGU_NCB);
   bf16* xs = reinterpret_cast<bf16*>(S.sm + Smem::xs);
   const int cpr = xlen / 8;
   const int G = group_rows(p.T);
@@ -853,7 +901,7 @@ __device__ void stage_inputs(Stream& S, const Item& it, int xlen, int k0 = 0) {
       else if (it.kind == KIND_SGU || it.kind == KIND_RT)
         src = p.xin + (size_t)(it.row0 + t) * H;
       else if (it.kind == KIND_SD)
-        src = p.dense ? p.hs + (size_t)(it.row0 + t) * ID + k0 : p.hs + (size_t)(it.row0 + t) * IS;
+        src = MODE == MODE_DENSE ? p.hs + (size_t)(it.row0 + t) * ID + k0 : p.hs + (size_t)(it.row0 + t) * IS;
       else
         src = p.h + (size_t)(it.row0 + t) * I;
       v = __ldcg(reinterpret_cast<const uint4*>(src) + k8);
@@ -865,9 +913,10 @@ __device__ void stage_inputs(Stream& S, const Item& it, int xlen, int k0 = 0) {
 
 // Router block (one item): partial logits of the token group over 64 router rows, written
 // to RP[row block][token][expert].  Warp w owns experts [32w, 32w + 32) (two 16-row tiles).
+template <int MODE>
 __device__ void run_router_block(Stream& S, const Item& it, int& j) {
   const Params& p = *S.p;
-  stage_inputs(S, it, H);
+  stage_inputs<MODE>(S, it, H);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   wait_full(S, j);
   const uint32_t tile = smem_u32(stage_ptr(S, j)) + uint32_t((warp >> 1) * (BLK_BYTES / 4));
@@ -900,14 +949,15 @@ __device__ void run_router_block(Stream& S, const Item& it, int& j) {
 
 // One segment: blocks [kb_start, kb_start + nblk) of item `it`, consumed as CTA blocks
 // j .. j + nblk - 1 (consumers).
+template <int MODE>
 __device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, int& j) {
   const Params& p = *S.p;
   const bool gu = it.kind == KIND_GU || it.kind == KIND_SGU;
   // a shared down input longer than a staged row (a dense layer) is staged from the segment's
   // first K row, and restaged when the segment runs past the window
-  int k0 = (p.dense && it.kind == KIND_SD) ? kb_start * DN_ROWS : 0;
-  int xlen = it.kind == KIND_SD ? (p.dense ? min(ID - k0, H) : IS) : it.kind == KIND_DN ? I : H;
-  stage_inputs(S, it, xlen, k0);
+  int kw = (MODE == MODE_DENSE && it.kind == KIND_SD) ? kb_start * DN_ROWS : 0;  // first staged K column
+  int xlen = it.kind == KIND_SD ? (MODE == MODE_DENSE ? min(ID - kw, H) : IS) : it.kind == KIND_DN ? I : H;
+  stage_inputs<MODE>(S, it, xlen, kw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j0 = j;
   const uint32_t xs = smem_u32(S.sm + Smem::xs);
@@ -922,7 +972,7 @@ __device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, i
     float d[2][2][4] = {};
     const uint32_t sub = uint32_t((warp >> 1) * (BLK_BYTES / 4));
     const int m0 = (warp & 1) * 32;
-    if (p.fp4) {
+    if constexpr (MODE == MODE_FP4) {
       // NVFP4 block of 256 rows: eight 32-row sub-tiles dequantised into the warp's part of the tile
       uint8_t* dq = S.sm + fp4_dq_offset();
       const uint32_t tile = smem_u32(dq) + uint32_t((warp >> 1) * (32 * 128));
@@ -963,7 +1013,7 @@ __device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, i
     float d[2][4] = {};
     const uint32_t sub = uint32_t((warp >> 2) * (BLK_BYTES / 2));
     const int m0 = (warp & 3) * 16;
-    if (p.fp4) {
+    if constexpr (MODE == MODE_FP4) {
       // NVFP4 block of 512 rows: eight 64-row sub-tiles
       uint8_t* dq = S.sm + fp4_dq_offset();
       const uint32_t tile = smem_u32(dq) + uint32_t((warp >> 2) * (64 * 128));
@@ -977,21 +1027,21 @@ __device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, i
             release(S, j);
           else
             __syncwarp();
-          mma_tile(d, tile, m0, 0, 4, xs, xlen + XPAD, (kb_start + q) * FP4_DN_ROWS + s * 64 - k0, two);
+          mma_tile(d, tile, m0, 0, 4, xs, xlen + XPAD, (kb_start + q) * FP4_DN_ROWS + s * 64 - kw, two);
           __syncwarp();
         }
       }
     } else {
       for (int q = 0; q < nblk; ++q, ++j) {
         const int kr = (kb_start + q) * DN_ROWS;  // first K row of this block
-        if (p.dense && kr - k0 >= xlen) {  // past the staged window (dense layers only; all warps)
+        if (MODE == MODE_DENSE && kr - kw >= xlen) {  // past the staged window (dense layers only; all warps)
           csync();  // every warp is done with the window
-          k0 = kr;
-          xlen = min(ID - k0, H);
-          stage_inputs(S, it, xlen, k0);
+          kw = kr;
+          xlen = min(ID - kw, H);
+          stage_inputs<MODE>(S, it, xlen, kw);
         }
         wait_full(S, j);
-        mma_tile(d, smem_u32(stage_ptr(S, j)) + sub, m0, 0, DN_ROWS / 16, xs, xlen + XPAD, kr - k0, two);
+        mma_tile(d, smem_u32(stage_ptr(S, j)) + sub, m0, 0, DN_ROWS / 16, xs, xlen + XPAD, kr - kw, two);
         release(S, j);
       }
     }
@@ -1007,7 +1057,7 @@ __device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, i
   bool done = true;  // this CTA writes the item's outputs
   if (kb_start != 0 || nblk != it.KB) {
     // a piece of a split item: it opens this CTA's range (slot 0) or closes it (slot 1)
-    float* P = partial_slot(p, blockIdx.x, j0 == 0 ? 0 : 1);
+    float* P = partial_slot(S, blockIdx.x, j0 == 0 ? 0 : 1);
     for (int q = threadIdx.x; q < it.nt * ncol; q += NCONS) P[q] = out[q];
     done = ticket_add(item_ticket(p, it), uint32_t(nblk), uint32_t(it.KB), S.misc + 10);
     if (done) {
@@ -1020,7 +1070,7 @@ __device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, i
         for (int k0 = 0; k0 < npc; k0 += 8) {  // eight loads in flight, added in slot order
           float v[8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) v[u] = k0 + u < npc ? __ldcg(p.P + (size_t)S.plist[k0 + u] * PSLOT + q) : 0.f;
+          for (int u = 0; u < 8; ++u) v[u] = k0 + u < npc ? __ldcg(S.pbank + (size_t)S.plist[k0 + u] * PSLOT + q) : 0.f;
 #pragma unroll
           for (int u = 0; u < 8; ++u)
             if (k0 + u < npc) s += v[u];
@@ -1030,8 +1080,13 @@ __device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, i
       csync();
     }
   }
-  if (done) item_epilogue(S, it, out);
+  if (done) item_epilogue<MODE>(S, it, out);
   csync();
+  // gate/up outputs of a token group complete: its down items may stage them
+  if (done && gu && S.dataflow) {
+    const int sncb = MODE == MODE_DENSE ? ID / 128 : SGU_NCB;
+    signal_done(it.kind == KIND_GU ? p.hdone + it.idx / GU_NCB : p.hsdone + it.idx / sncb);
+  }
   // down outputs: the last item of a 128-column block combines that block for every token
   if (done && S.comb_items && !gu && ticket_last(p.tk_comb + it.c, uint32_t(S.comb_items), S.misc + 14, false)) {
     combine_block(p, S.inv, it.c);
@@ -1040,16 +1095,17 @@ __device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, i
 }
 
 // Consumers: work through this CTA's range of the step.
+template <int MODE>
 __device__ void consume(Stream& S) {
   int j = 0;
   while (j < S.nb) {
     int kind, idx, kb;
     block_kind(S.L, S.b0 + j, kind, idx, kb);
-    const Item it = decode_item(*S.p, S.meta, kind, idx);  // shared-memory lookups only
+    const Item it = decode_item<MODE>(*S.p, S.meta, kind, idx);  // shared-memory lookups only
     if (kind == KIND_RT)
-      run_router_block(S, it, j);
+      run_router_block<MODE>(S, it, j);
     else
-      run_segment(S, it, kb, min(it.KB - kb, S.nb - j), j);
+      run_segment<MODE>(S, it, kb, min(it.KB - kb, S.nb - j), j);
   }
 }
 
@@ -1064,11 +1120,12 @@ __device__ __forceinline__ void set_step(Stream& S, const BlockList& L) {
 
 // Run the current step for the whole CTA: the producer lane streams (its first `pre` blocks
 // were issued already), the consumers compute.
+template <int MODE>
 __device__ void run_step(Stream& S, int pre = 0) {
   if (threadIdx.x >= NCONS) {
-    if (threadIdx.x == NCONS) produce(S, pre, S.nb);
+    if (threadIdx.x == NCONS) produce<MODE>(S, pre, S.nb);
   } else {
-    consume(S);
+    consume<MODE>(S);
   }
   S.ring += S.nb;
   __syncthreads();
@@ -1308,11 +1365,14 @@ __device__ Meta build_tables(const Params& p, uint8_t* sm, uint16_t* perm, uint1
   return m;
 }
 
-// A dense SwiGLU MLP layer (p.dense, width p.sw = ID): the shared-expert steps alone -- step C
+// A dense SwiGLU MLP layer (MODE_DENSE, width ID): the shared-expert steps alone -- step C
 // the gate/up of the whole width, a barrier, step D the down projection, whose items write
 // y = bf16(MLP(x') [+ x]) directly (no router, no routing, no combine).
+template <int MODE>
 __device__ void dense_layer(Stream& S, const Params& p, int ntg) {
   constexpr int sncb = ID / 128;
+  S.dataflow = true;  // the down items wait for their token group's gate/up outputs: no barrier
+  S.pbank = partial_bank(p, 0);
   {
     BlockList L;
     L.k_first = L.k_second = KIND_SGU;
@@ -1322,7 +1382,7 @@ __device__ void dense_layer(Stream& S, const Params& p, int ntg) {
     S.first_slot = 12;
     trace_point(p, 6);
     set_step(S, L);
-    run_step(S);
+    run_step<MODE>(S);
   }
   trace_point(p, 7);
   {
@@ -1333,23 +1393,19 @@ __device__ void dense_layer(Stream& S, const Params& p, int ntg) {
     L.n_total = ntg * OUT_NCB * (ID / DN_ROWS);
     set_step(S, L);
   }
-  const int pre = p.T <= PREISSUE_MAX_T ? min(1, S.nb) : 0;
-  if (threadIdx.x == NCONS) produce(S, 0, pre);
-  if (!grid_sync(p, 1, S.misc + 12)) {
-    drain_issued(S, pre);
-    return;
-  }
+  S.pbank = partial_bank(p, 1);
   trace_point(p, 8);
   S.first_slot = 13;
-  run_step(S, pre);
+  run_step<MODE>(S);
   trace_point(p, 9);
-  grid_done(p, S.misc + 13);
+  grid_done(p, S.misc + 13, 0, ntg);
   trace_point(p, 10);
 }
 
 // ================================================================ the fused decode kernel
 // mode 0: the whole layer; mode 1: routing only (router, top-K, counts); a dense layer
-// (p.dense) runs dense_layer instead.
+// (MODE_DENSE) runs dense_layer instead.
+template <int MODE>
 __global__ void __launch_bounds__(NTHREADS, 1)
     decode_fused(const __grid_constant__ Params p, const __grid_constant__ StreamMaps maps, int mode) {
   extern __shared__ uint8_t smem_raw[];
@@ -1368,6 +1424,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   S.plist = reinterpret_cast<int*>(sm + Smem::plist);
   S.out = reinterpret_cast<float*>(sm + out_offset(group_rows(p.T)));
   S.comb_items = 0;
+  S.dataflow = false;
+  S.pbank = partial_bank(p, 0);
   uint16_t* perm = reinterpret_cast<uint16_t*>(sm + Smem::perm);
   uint16_t* inv = reinterpret_cast<uint16_t*>(sm + Smem::inv);
   float* gw = reinterpret_cast<float*>(sm + Smem::gw);
@@ -1391,8 +1449,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   pdl_wait();  // inputs of this forward and the workspace are ready
   trace_point(p, 1);
   if ((p.flags & FLAG_TEST_WAIT_TIMEOUT) && blockIdx.x == 0 && threadIdx.x == 0) test_wait_timeout(p.status);
-  if (p.dense) {
-    dense_layer(S, p, ntg);
+  if constexpr (MODE == MODE_DENSE) {
+    dense_layer<MODE>(S, p, ntg);
     return;
   }
 
@@ -1401,7 +1459,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // short step A starts the routing sooner; measured 908 vs 944 us over the decode sweep.)
   {
     if (full && threadIdx.x == NCONS + 1) {
-      if (p.fp4)
+      if (MODE == MODE_FP4)
         prefetch_share(p.q_sdown, uint32_t(IS) * H / 2);
       else
         prefetch_share(p.ws_down, uint32_t(IS) * H * 2);
@@ -1411,7 +1469,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     L.kb_first = L.kb_second = 1;
     L.n_first = L.n_total = ntg * RT_NB;
     set_step(S, L);
-    run_step(S);
+    run_step<MODE>(S);
   }
   trace_point(p, 2);
   if (!grid_sync(p, 1, S.misc + 12)) return;
@@ -1452,8 +1510,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // ---- step C: routed gate/up and the shared gate/up
   {
     // the touched experts' down matrices are read in step D: prefetch them when they fit
-    const uint32_t per_e = p.fp4 ? uint32_t(I) * H / 2 : uint32_t(I) * H * 2;  // codes / bf16 bytes
-    const uint8_t* dbase = p.fp4 ? p.q_down : reinterpret_cast<const uint8_t*>(p.w_down);
+    const uint32_t per_e = MODE == MODE_FP4 ? uint32_t(I) * H / 2 : uint32_t(I) * H * 2;  // codes / bf16 bytes
+    const uint8_t* dbase = MODE == MODE_FP4 ? p.q_down : reinterpret_cast<const uint8_t*>(p.w_down);
     if (threadIdx.x == NCONS + 1 && (unsigned long long)S.meta.U * per_e <= p.prefetch_bytes_max) {
       // 32-bit offsets: U * I * H * 2 <= 512 MB
       const uint32_t total = per_e * uint32_t(S.meta.U);
@@ -1471,7 +1529,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
     BlockList L;
-    const int kgu = kblocks_of(p, KIND_GU);
+    const int kgu = kblocks_of<MODE>(p, KIND_GU);
     L.k_first = KIND_GU;
     L.kb_first = kgu;
     L.n_first = S.meta.groups * GU_NCB * kgu;
@@ -1479,19 +1537,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     L.kb_second = kgu;
     L.n_total = L.n_first + ntg * SGU_NCB * kgu;
     S.first_slot = 12;
+    S.dataflow = true;  // gate/up items signal their token group; step D waits per group
     trace_point(p, 6);
     set_step(S, L);
-    run_step(S);
+    run_step<MODE>(S);
   }
   trace_point(p, 7);
 
-  // ---- step D: routed down projection and the shared down projection.  Its blocks are weights
-  // only: for small calls (latency-bound) the producer issues the first one before the barrier
-  // that publishes step C's outputs.  (Measured: more early blocks, or early blocks for larger
-  // calls, slow the CTAs still streaming step C, which set the barrier's time.)
+  // ---- step D: routed down projection and the shared down projection, with no grid barrier
+  // after step C: a CTA streams its down blocks (weights only) as soon as its step-C range is
+  // done, and each down item waits only for the gate/up outputs of its own token group.  The
+  // partial sums of split items use a second bank, since step-C pieces may still be being added.
   {
     BlockList L;
-    const int kdn = kblocks_of(p, KIND_DN), ksd = kblocks_of(p, KIND_SD);
+    const int kdn = kblocks_of<MODE>(p, KIND_DN), ksd = kblocks_of<MODE>(p, KIND_SD);
     L.k_first = KIND_DN;
     L.kb_first = kdn;
     L.n_first = S.meta.groups * OUT_NCB * kdn;
@@ -1500,26 +1559,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     L.n_total = L.n_first + ntg * OUT_NCB * ksd;
     set_step(S, L);
   }
-  const int pre = T <= PREISSUE_MAX_T ? min(1, S.nb) : 0;
-  if (threadIdx.x == NCONS) produce(S, 0, pre);
-  if (!grid_sync(p, ++nbar, S.misc + 12)) {
-    drain_issued(S, pre);
-    return;
-  }
+  S.pbank = partial_bank(p, 1);
   trace_point(p, 8);
   // When the grid has a CTA for every down item, the combine of each 128-column block follows
   // its last down item (no further barrier); otherwise the whole grid combines after a barrier
   // (a ticket per item then costs each CTA a fence and an atomic per item: slower).
   S.comb_items = (S.meta.groups + ntg) * OUT_NCB <= S.nctas ? S.meta.groups + ntg : 0;
   S.first_slot = 13;
-  run_step(S, pre);
+  run_step<MODE>(S);
   trace_point(p, 9);
   if (!S.comb_items) {
     if (!grid_sync(p, ++nbar, S.misc + 12)) return;
     trace_point(p, 14);
     combine_share(p, inv);
   }
-  grid_done(p, S.misc + 13);
+  grid_done(p, S.misc + 13, S.meta.groups, ntg);
   trace_point(p, 10);
 }
 
@@ -1599,6 +1653,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   S.misc = reinterpret_cast<int*>(sm + Smem::misc);
   S.plist = reinterpret_cast<int*>(sm + Smem::plist);
   S.out = reinterpret_cast<float*>(sm + out_offset(G));
+  S.dataflow = false;  // the layers keep their grid barriers
+  S.pbank = partial_bank(base, 0);
   S.comb_items = 0;  // the combine always follows a barrier here: it also normalises
   uint16_t* perm = reinterpret_cast<uint16_t*>(sm + Smem::perm);
   uint16_t* inv = reinterpret_cast<uint16_t*>(sm + Smem::inv);
@@ -1650,7 +1706,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       L.n_first = L.n_total = ntg * RT_NB;
       S.first_slot = 11;
       set_step(S, L);
-      run_step(S);
+      run_step<MODE_MOE>(S);
     }
     trace_point(p, 2);
     if (!grid_sync(p, ++nbar, S.misc + 12)) return;
@@ -1711,7 +1767,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       S.first_slot = 12;
       trace_point(p, 6);
       set_step(S, L);
-      run_step(S);
+      run_step<MODE_MOE>(S);
     }
     trace_point(p, 7);
     // ---- step D (first block issued before the barrier for small calls, as in decode_fused)
@@ -1726,14 +1782,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       set_step(S, L);
     }
     const int pre = T <= PREISSUE_MAX_T ? min(1, S.nb) : 0;
-    if (threadIdx.x == NCONS) produce(S, 0, pre);
+    if (threadIdx.x == NCONS) produce<MODE_MOE>(S, 0, pre);
     if (!grid_sync(p, ++nbar, S.misc + 12)) {
       drain_issued(S, pre);
       return;
     }
     trace_point(p, 8);
     S.first_slot = 13;
-    run_step(S, pre);
+    run_step<MODE_MOE>(S, pre);
     trace_point(p, 9);
     if (!grid_sync(p, ++nbar, S.misc + 12)) return;
     trace_point(p, 14);

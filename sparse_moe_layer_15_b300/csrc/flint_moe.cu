@@ -27,7 +27,7 @@ constexpr int MAX_TRACE_CTAS = 1024;
 
 struct Layout {
   // tickets first: [status, tickets) and [tickets, scalars) are cleared together after errors
-  size_t status, bar_count, bar_done, tk_gu, tk_sgu, tk_sd, tk_dn, tk_comb;
+  size_t status, bar_count, bar_done, tk_gu, tk_sgu, tk_sd, tk_dn, tk_comb, hdone, hsdone;
   size_t zero_end;  // [0, zero_end): status word, barrier counters and tickets (cleared between uses)
   size_t counts, offsets, perm, inv, topk_idx, topk_w;
   size_t xn, xstage, ystage, h, hs, S, Y, P, RP, trace;
@@ -60,6 +60,8 @@ Layout make_layout(int max_tokens, int sw = IS, bool dense = false) {
   L.tk_sd = take(sizeof(uint32_t) * Gs * OUT_NCB);
   L.tk_dn = take(sizeof(uint32_t) * G * OUT_NCB);
   L.tk_comb = take(sizeof(uint32_t) * OUT_NCB);
+  L.hdone = take(sizeof(uint32_t) * G);
+  L.hsdone = take(sizeof(uint32_t) * Gs);
   L.zero_end = align_up(off, 256);
   L.counts = take(sizeof(int32_t) * E);
   L.offsets = take(sizeof(int32_t) * (E + 1));
@@ -74,7 +76,7 @@ Layout make_layout(int max_tokens, int sw = IS, bool dense = false) {
   L.hs = take(sizeof(uint16_t) * T * sw);
   L.S = take(sizeof(float) * T * H);
   L.Y = take(sizeof(float) * (size_t)Ts * K * H);
-  L.P = take(sizeof(float) * MAX_STREAM_CTAS * 2 * PSLOT);
+  L.P = take(sizeof(float) * 2 * MAX_STREAM_CTAS * 2 * PSLOT);  // two banks: steps C and D
   L.RP = take(sizeof(float) * RT_NB * STREAM_MAX_T * E);
   if (max_tokens > STREAM_MAX_T && !dense) {
     const size_t ntile = (T + tc::TM - 1) / tc::TM;
@@ -225,6 +227,8 @@ Params make_params(flint_moe_t h, const void* x, int T, void* y, int32_t* out_id
   p.tk_sd = reinterpret_cast<uint32_t*>(ws + L.tk_sd);
   p.tk_dn = reinterpret_cast<uint32_t*>(ws + L.tk_dn);
   p.tk_comb = reinterpret_cast<uint32_t*>(ws + L.tk_comb);
+  p.hdone = reinterpret_cast<uint32_t*>(ws + L.hdone);
+  p.hsdone = reinterpret_cast<uint32_t*>(ws + L.hsdone);
   p.counts = reinterpret_cast<int32_t*>(ws + L.counts);
   p.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
   p.perm = reinterpret_cast<int32_t*>(ws + L.perm);
@@ -293,7 +297,8 @@ flint_moe_status run_decode_maps(flint_moe_t h, const Params& p, const StreamMap
   if (h->cfg.flags & FLINT_MOE_FLAG_PRE_RMSNORM) e = launch(h, "rmsnorm", rmsnorm_kernel, p.T, 256, 0, st, false, p);
   if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
   const int grid = h->n_sm < MAX_STREAM_CTAS ? h->n_sm : MAX_STREAM_CTAS;
-  e = launch(h, full ? "decode_fused" : "decode_fused_route", decode_fused, grid, NTHREADS,
+  auto kern = h->fp4 ? decode_fused<MODE_FP4> : h->dense ? decode_fused<MODE_DENSE> : decode_fused<MODE_MOE>;
+  e = launch(h, full ? "decode_fused" : "decode_fused_route", kern, grid, NTHREADS,
              h->fp4 ? fp4_smem_bytes() : fused_smem_bytes(group_rows(p.T)), st, true, p, maps, full ? 0 : 1);
   return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ERR_CUDA;
 }
@@ -481,11 +486,15 @@ flint_moe_status create_handle(const flint_moe_config* cfg, const flint_moe_weig
     delete h;
     return FLINT_MOE_ERR_CUDA;
   }
-  cudaError_t e = cudaFuncSetAttribute(decode_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, FUSED_SMEM);
+  // every mode's instantiation (a handle made here may be turned into an NVFP4 one by the caller)
+  cudaError_t e = cudaSuccess;
+  for (auto kern : {decode_fused<MODE_MOE>, decode_fused<MODE_FP4>, decode_fused<MODE_DENSE>}) {
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FUSED_SMEM);
+    int per_sm = 0;
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NTHREADS, FUSED_SMEM);
+    if (e == cudaSuccess && per_sm < 1) e = cudaErrorCooperativeLaunchTooLarge;
+  }
   if (e == cudaSuccess && prefill) e = set_prefill_smem();
-  int per_sm = 0;
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused, NTHREADS, FUSED_SMEM);
-  if (e == cudaSuccess && per_sm < 1) e = cudaErrorCooperativeLaunchTooLarge;
   if (e == cudaSuccess) e = cudaMemset(h->ws, 0, L.xn);  // status, tickets and routing scratch
   for (int i = 0; i < 2 * MAX_EVENTS && e == cudaSuccess; ++i) e = cudaEventCreate(&h->ev[i]);
   if (e != cudaSuccess) {
@@ -756,7 +765,7 @@ flint_moe_status flint_moe_stack_destroy(flint_moe_stack_t st) {
 // point takes its scratch space from one fixed array in device memory that the library
 // declares itself, so the caller supplies only the weights, the input and the output.
 //
-// The array (17 MiB) holds the workspace of a handle with max_tokens = NOALLOC_MAX_T.
+// The array (25 MiB) holds the workspace of a handle with max_tokens = NOALLOC_MAX_T.
 // Every GPU that loads the library reserves it until the process exits.  All calls on a
 // device share it: calls whose work overlaps on the GPU (on different streams, or from
 // different threads) race on it and must be serialised by the caller.  The barrier counters
@@ -771,7 +780,7 @@ flint_moe_status flint_moe_stack_destroy(flint_moe_stack_t st) {
 namespace {
 
 constexpr int NOALLOC_MAX_T = 4;
-constexpr size_t NOALLOC_BYTES = size_t(17) << 20;
+constexpr size_t NOALLOC_BYTES = size_t(25) << 20;
 constexpr int NOALLOC_MAX_DEVICES = 64;
 
 __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_BYTES];
@@ -791,12 +800,13 @@ flint_moe_status noalloc_setup(int dev, void** ptr, int* n_sm) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
       return FLINT_MOE_ERR_CUDA;
-    if (cudaFuncSetAttribute(decode_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, FUSED_SMEM) !=
+    if (cudaFuncSetAttribute(decode_fused<MODE_MOE>, cudaFuncAttributeMaxDynamicSharedMemorySize, FUSED_SMEM) !=
         cudaSuccess)
       return FLINT_MOE_ERR_CUDA;
     // the cooperative launch needs one CTA resident on every SM (as flint_moe_create checks)
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused, NTHREADS, FUSED_SMEM) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused<MODE_MOE>, NTHREADS, FUSED_SMEM) !=
+        cudaSuccess)
       return FLINT_MOE_ERR_CUDA;
     if (per_sm < 1) return FLINT_MOE_ERR_UNSUPPORTED;
     // the status word starts clear (later calls clear only the counters and tickets)
