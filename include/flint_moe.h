@@ -337,7 +337,8 @@ flint_moe_status flint_dense_destroy(flint_dense_t d);
  *   out     [B][32][128] bf16.
  * One kernel launch, asynchronous on `stream`, no allocation, bitwise deterministic.  The
  * workspace (caller-owned, 256-byte aligned, flint_swa_workspace_bytes) holds chunk partials
- * and tickets; initialise it once with flint_swa_workspace_init; its tickets return to zero at
+ * and tickets; initialise it once with flint_swa_workspace_init (on each device that will run
+ * decode calls: it also sets the kernel's shared-memory limit); its tickets return to zero at
  * the end of every call.  Calls sharing one workspace must be ordered on one stream. */
 flint_moe_status flint_swa_workspace_bytes(int max_batch, size_t* bytes);
 flint_moe_status flint_swa_workspace_init(void* workspace, size_t workspace_bytes, flint_stream_t stream);

@@ -125,9 +125,9 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Row-major uint8 matrix [rows][cols] (NVFP4 codes or scales) -> 2-D tensor map, box of box_cols
-// bytes x box_rows, no swizzle.
+// bytes x box_rows (codes: 64-byte rows with the 64-byte swizzle; scales: no swizzle).
 bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
-                 uint32_t box_rows) {
+                 uint32_t box_rows, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -135,7 +135,7 @@ bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -1039,6 +1039,9 @@ flint_moe_status flint_swa_workspace_init(void* workspace, size_t workspace_byte
     return FLINT_MOE_ERR_CUDA;
   if (major != 10 || minor != 3) return FLINT_MOE_ERR_UNSUPPORTED;
   const SwaLayout L = swa_layout(cap);
+  if (cudaFuncSetAttribute(swa::decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, swa::SMEM_BYTES) !=
+      cudaSuccess)
+    return FLINT_MOE_ERR_CUDA;
   return cudaMemsetAsync(workspace, 0, L.zero_end, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? FLINT_MOE_OK
              : FLINT_MOE_ERR_CUDA;
@@ -1070,7 +1073,15 @@ flint_moe_status flint_swa_decode(void* workspace, size_t workspace_bytes, const
   p.part = reinterpret_cast<float*>(ws + L.part);
   p.ticket = reinterpret_cast<uint32_t*>(ws + L.ticket);
   p.status = reinterpret_cast<uint32_t*>(ws + L.status);
-  swa::decode_kernel<<<dim3(swa::NSPLIT, swa::NKV, B), swa::NT, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  // one CTA per (sequence, KV head) walking the 9 chunks once the batch has a pair per SM; below,
+  // each pair split over 9 CTAs of one chunk (merged by the last of them)
+  int dev = 0, n_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess)
+    return FLINT_MOE_ERR_CUDA;
+  const int nsplit = B * swa::NKV >= n_sm ? 1 : swa::NSPLIT;
+  swa::decode_kernel<<<dim3(nsplit, swa::NKV, B), swa::NT, swa::SMEM_BYTES, reinterpret_cast<cudaStream_t>(stream)>>>(
+      p);
   return cudaGetLastError() == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ERR_CUDA;
 }
 
@@ -1116,12 +1127,12 @@ extern "C" flint_moe_status flint_moe_create_nvfp4(const flint_moe_config* cfg, 
   Fp4Maps m;
   const uint64_t EH = (uint64_t)E * H, EI = (uint64_t)E * I;
   const bool ok =
-      make_map_u8(&m.qg, w->gate_codes, EH, I / 2, 64, FP4_GU_ROWS) &&
-      make_map_u8(&m.qu, w->up_codes, EH, I / 2, 64, FP4_GU_ROWS) &&
-      make_map_u8(&m.qd, w->down_codes, EI, H / 2, 64, FP4_DN_ROWS / 2) &&
-      make_map_u8(&m.qsg, w->sgate_codes, H, IS / 2, 64, FP4_GU_ROWS) &&
-      make_map_u8(&m.qsu, w->sup_codes, H, IS / 2, 64, FP4_GU_ROWS) &&
-      make_map_u8(&m.qsd, w->sdown_codes, IS, H / 2, 64, FP4_DN_ROWS / 2) &&
+      make_map_u8(&m.qg, w->gate_codes, EH, I / 2, 64, FP4_GU_ROWS, CU_TENSOR_MAP_SWIZZLE_64B) &&
+      make_map_u8(&m.qu, w->up_codes, EH, I / 2, 64, FP4_GU_ROWS, CU_TENSOR_MAP_SWIZZLE_64B) &&
+      make_map_u8(&m.qd, w->down_codes, EI, H / 2, 64, FP4_DN_ROWS / 2, CU_TENSOR_MAP_SWIZZLE_64B) &&
+      make_map_u8(&m.qsg, w->sgate_codes, H, IS / 2, 64, FP4_GU_ROWS, CU_TENSOR_MAP_SWIZZLE_64B) &&
+      make_map_u8(&m.qsu, w->sup_codes, H, IS / 2, 64, FP4_GU_ROWS, CU_TENSOR_MAP_SWIZZLE_64B) &&
+      make_map_u8(&m.qsd, w->sdown_codes, IS, H / 2, 64, FP4_DN_ROWS / 2, CU_TENSOR_MAP_SWIZZLE_64B) &&
       make_map_u8(&m.sg, w->gate_scales, EH / 16, I, 128, FP4_GU_ROWS / 16) &&
       make_map_u8(&m.su, w->up_scales, EH / 16, I, 128, FP4_GU_ROWS / 16) &&
       make_map_u8(&m.sd, w->down_scales, EI / 16, H, 128, FP4_DN_ROWS / 16) &&

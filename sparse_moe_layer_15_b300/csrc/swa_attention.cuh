@@ -13,16 +13,16 @@
 // the projections).
 //
 // The step reads 513 x 4 x 128 x 2 x 2 = 525 KB of cache per full sequence and does about 8
-// MFLOP: HBM-bound.  Work split: one CTA per (57-slot chunk, KV head, sequence) -- 9 chunks
-// cover the 513 slots exactly -- so a batch of B sequences launches 36 B CTAs of 29 KB of
-// loads each, several resident per SM.  A CTA stages its chunk's K and V rows (256 bytes each,
-// 16-byte loads, rows padded to spread shared-memory banks) and the group's 8 query rows, then
-// runs both contractions as bf16 warp MMAs (m16n8k16, fp32 accumulate) with the 8 heads as the
-// rows of a 16-row tile: S = Q K^T split over the warps by slots, the chunk's softmax statistics
-// reduced across the warps in fp32, the probabilities rounded to bf16, O = P V split over the
-// warps by output dimensions.  The chunk's unnormalised output, max and sum go to the workspace; an
-// integer ticket per (sequence, KV head) elects the last of the 9 CTAs, which merges the chunks
-// in chunk order together with the sink: deterministic, no floating-point atomics.
+// MFLOP: HBM-bound.  The window is cut into 9 chunks of 57 slots.  A CTA takes one (sequence, KV
+// head) and walks its chunks with a running softmax, loading chunk c + 1 (cp.async, 16 bytes per
+// thread, rows padded to spread shared-memory banks) while chunk c is computed; both
+// contractions are bf16 warp MMAs (m16n8k16, fp32 accumulate) with the 8 heads of the group as the
+// rows of a 16-row tile: S = Q K^T split over the warps by slots, the chunk's row max reduced
+// across the warps, P rounded to bf16, O = P V split over the warps by output dimensions.  When a
+// batch has fewer (sequence, KV head) pairs than SMs, each pair is split over 9 CTAs of one chunk
+// each: a CTA writes its unnormalised output, max and sum to the workspace, and an integer
+// ticket per (sequence, KV head) elects the last of them, which merges the chunks in chunk order
+// together with the sink.  Deterministic either way, no floating-point atomics.
 #pragma once
 
 #include "common.cuh"
@@ -60,6 +60,7 @@ constexpr float SCALE = 0.08838834764831845f;
 constexpr int KP = 64;       // slots of a chunk padded to the MMA tiles (slots >= 57 are zero)
 constexpr int RS = HD + 8;   // bf16 row stride of the staged K, V and query rows (272 bytes: banks spread)
 constexpr int PS = KP + 8;   // bf16 row stride of the probabilities
+static_assert((2 * KP * (HD / 8)) % NT == 0, "a chunk's copies are whole rounds of the CTA");
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -84,18 +85,41 @@ __device__ __forceinline__ void frag_a(uint32_t base, int rs, int k0, uint32_t (
   ldsm_x4(base + uint32_t((((q & 1) * 8 + (lane & 7)) * rs + k0 + (q >> 1) * 8) * 2), a);
 }
 
-// The chunk's attention with the group's 8 query heads as the rows of 16-row MMA tiles (rows 8..15
-// zero): S = Q K^T over 128 dimensions (warp w: slots [8w, 8w + 8)), the chunk's softmax across
-// the warps (fp32), P rounded to bf16, O = P V over the 64 padded slots (warp w: dimensions
-// [16w, 16w + 16)).
+// cp.async of 16 bytes global -> shared, zero-filled when !valid (src_size 0).
+__device__ __forceinline__ void cp16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Shared memory (dynamic): two chunk buffers of K and V rows, the query rows, the probabilities.
+struct Smem {
+  static constexpr int kv = 0;                              // [2 buffers][K | V][KP][RS] bf16
+  static constexpr int qs = kv + 2 * 2 * KP * RS * 2;      // [16][RS] bf16
+  static constexpr int ps = qs + 16 * RS * 2;              // [16][PS] bf16
+  static constexpr int red = ps + 16 * PS * 2;             // [2][GQ][8] f32
+  static constexpr int bytes = red + 2 * GQ * 8 * 4 + 16;
+};
+constexpr int SMEM_BYTES = Smem::bytes;
+
+// One CTA per (split, KV head, sequence) walks chunks [split * cpc, +cpc) of the 9 (cpc = 9 /
+// splits): chunk c + 1 is loaded (cp.async, slots beyond the valid ones zero-filled) while chunk
+// c is computed.  Per chunk, with the group's 8 query heads as the rows of 16-row MMA tiles (rows
+// 8..15 zero): S = Q K^T (warp w: slots [8w, 8w + 8)), the chunk's row max across the warps, the
+// running softmax (max m, sum l, output O rescaled by e^(m_old - m_new)), P rounded to bf16, O +=
+// P V (warp w: dimensions [16w, 16w + 16)).  One split: the CTA writes the output with the sink;
+// several: its (O, m, l) go to the workspace and the last CTA of (b, g) merges them.
 __global__ void __launch_bounds__(NT) decode_kernel(const __grid_constant__ Params p) {
-  __shared__ __align__(16) bf16 ks[KP * RS];
-  __shared__ __align__(16) bf16 vs[KP * RS];
-  __shared__ __align__(16) bf16 qs[16 * RS];
-  __shared__ __align__(16) bf16 ps[16 * PS];
-  __shared__ float red_m[GQ][8], red_l[GQ][8];
+  extern __shared__ __align__(16) uint8_t smem[];
+  bf16* kvb = reinterpret_cast<bf16*>(smem + Smem::kv);
+  bf16* qs = reinterpret_cast<bf16*>(smem + Smem::qs);
+  bf16* ps = reinterpret_cast<bf16*>(smem + Smem::ps);
+  float* red = reinterpret_cast<float*>(smem + Smem::red);  // [0]: row maxima, [1]: row sums
   __shared__ int s_last;
-  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int nsplit = gridDim.x, split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int cpc = NSPLIT / nsplit;  // chunks per CTA
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int pb = __ldg(p.pos + b);
   if (pb < 0) {
@@ -103,121 +127,150 @@ __global__ void __launch_bounds__(NT) decode_kernel(const __grid_constant__ Para
     pb = 0;
   }
   const int n = pb + 1 < W ? pb + 1 : W;
-  const int j0 = split * CH;
-  const int nk = n - j0 < 0 ? 0 : (n - j0 < CH ? n - j0 : CH);  // valid slots of this chunk
-
-  // ---- stage K and V rows (zero beyond the valid slots), the group's 8 query rows (+ 8 zero rows),
-  // and zero probability rows 8..15
   constexpr int RV = HD / 8;  // 16-byte pieces per row
-  {
-    const uint4* kg = reinterpret_cast<const uint4*>(p.k + ((size_t)b * W + j0) * NKV * HD + (size_t)g * HD);
-    const uint4* vg = reinterpret_cast<const uint4*>(p.v + ((size_t)b * W + j0) * NKV * HD + (size_t)g * HD);
-    constexpr int PER = (2 * KP * RV + NT - 1) / NT;  // 8
-    uint4 buf[PER];
+
+  // chunk c -> buffer c & 1 (K rows, then V rows; slots beyond the valid ones zero-filled)
+  auto load_chunk = [&](int c) {
+    const int j0 = c * CH;
+    const int nk = n - j0 < 0 ? 0 : (n - j0 < CH ? n - j0 : CH);
+    const bf16* kg = p.k + ((size_t)b * W + j0) * NKV * HD + (size_t)g * HD;
+    const bf16* vg = p.v + ((size_t)b * W + j0) * NKV * HD + (size_t)g * HD;
+    bf16* dst = kvb + (c & 1) * 2 * KP * RS;
 #pragma unroll
-    for (int u = 0; u < PER; ++u) {  // all loads in flight before the stores
+    for (int u = 0; u < 2 * KP * RV / NT; ++u) {
       const int i = tid + u * NT;
-      const int r = i / RV, c = i % RV;
+      const int r = i / RV, cc = i % RV;
       const int j = r < KP ? r : r - KP;
-      buf[u] = make_uint4(0, 0, 0, 0);
-      if (j < nk) buf[u] = __ldcs((r < KP ? kg : vg) + (size_t)j * NKV * RV + c);
+      const bool ok = j < nk;
+      const bf16* src = (r < KP ? kg : vg) + (size_t)(ok ? j : 0) * NKV * HD + cc * 8;
+      cp16(dst + r * RS + cc * 8, src, ok);
     }
-#pragma unroll
-    for (int u = 0; u < PER; ++u) {
-      const int i = tid + u * NT;
-      const int r = i / RV, c = i % RV;
-      const int j = r < KP ? r : r - KP;
-      *reinterpret_cast<uint4*>((r < KP ? ks : vs) + j * RS + c * 8) = buf[u];
-    }
+    cp_commit();
+  };
+
+  const int c0 = split * cpc;
+  load_chunk(c0);
+  {  // the group's 8 query rows (+ 8 zero rows) and zero probability rows 8..15
     const uint4 zero = make_uint4(0, 0, 0, 0);
-    {
-      const int r = tid / RV, c = tid % RV;  // 256 threads: 16 rows x 16 pieces
-      *reinterpret_cast<uint4*>(qs + r * RS + c * 8) =
-          r < GQ ? __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t)b * NH + (size_t)g * GQ + r) * HD) + c) : zero;
-    }
+    const int r = tid / RV, cc = tid % RV;  // 256 threads: 16 rows x 16 pieces
+    *reinterpret_cast<uint4*>(qs + r * RS + cc * 8) =
+        r < GQ ? __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t)b * NH + (size_t)g * GQ + r) * HD) + cc) : zero;
     if (tid < 8 * (KP / 8)) *reinterpret_cast<uint4*>(ps + (8 + tid / (KP / 8)) * PS + (tid % (KP / 8)) * 8) = zero;
   }
-  __syncthreads();
 
-  // ---- S = Q K^T: warp w, slots [8w, 8w + 8)
   const int row = lane >> 2;          // query head within the group (C-fragment rows 0..7)
   const int cq = 2 * (lane & 3);      // C-fragment column pair
-  float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-  {
-    const uint32_t qb = smem_u32(qs), kb = smem_u32(ks);
-    const int q = lane >> 3;
-#pragma unroll
-    for (int k0 = 0; k0 < HD; k0 += 32) {
-      uint32_t a0[4], a1[4], bb[4];
-      frag_a(qb, RS, k0, a0);
-      frag_a(qb, RS, k0 + 16, a1);
-      ldsm_x4(kb + uint32_t(((warp * 8 + (lane & 7)) * RS + k0 + q * 8) * 2), bb);
-      mma16816(sacc, a0, bb[0], bb[1]);
-      mma16816(sacc, a1, bb[2], bb[3]);
-    }
-  }
-  const int jA = warp * 8 + cq;
-  const float s0 = jA < nk ? sacc[0] * SCALE : -INFINITY;
-  const float s1 = jA + 1 < nk ? sacc[1] * SCALE : -INFINITY;
-  float mw = fmaxf(s0, s1);
-  mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 1));
-  mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 2));
-  if ((lane & 3) == 0) red_m[warp][row] = mw;
-  __syncthreads();
-  float m = red_m[0][row];
-#pragma unroll
-  for (int w = 1; w < GQ; ++w) m = fmaxf(m, red_m[w][row]);
-  // m = -inf only when the chunk has no valid slot: every probability is 0 then
-  const float p0 = jA < nk ? expf(s0 - m) : 0.f;
-  const float p1 = jA + 1 < nk ? expf(s1 - m) : 0.f;
-  float lw = p0 + p1;
-  lw += __shfl_xor_sync(0xffffffffu, lw, 1);
-  lw += __shfl_xor_sync(0xffffffffu, lw, 2);
-  if ((lane & 3) == 0) red_l[warp][row] = lw;
-  *reinterpret_cast<__nv_bfloat162*>(ps + row * PS + jA) = __floats2bfloat162_rn(p0, p1);
-  __syncthreads();
-
-  // ---- O = P V: warp w, dimensions [16w, 16w + 16) (two 8-column tiles)
+  const int q8 = lane >> 3;
+  float m_run = -INFINITY, l_run = 0.f;
   float o[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  {
-    const uint32_t pb0 = smem_u32(ps), vb = smem_u32(vs);
-    const int q = lane >> 3;
+  for (int c = c0; c < c0 + cpc; ++c) {
+    if (c + 1 < c0 + cpc) {
+      load_chunk(c + 1);
+      cp_wait<1>();  // chunk c has landed (this thread's copies)
+    } else {
+      cp_wait<0>();
+    }
+    __syncthreads();  // every thread's copies of chunk c (and, first time, the query rows)
+    const int j0 = c * CH;
+    const int nk = n - j0 < 0 ? 0 : (n - j0 < CH ? n - j0 : CH);
+    const bf16* kb_ = kvb + (c & 1) * 2 * KP * RS;
+    const bf16* vb_ = kb_ + KP * RS;
+    // ---- S = Q K^T: warp w, slots [8w, 8w + 8)
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+      const uint32_t qb = smem_u32(qs), kb = smem_u32(kb_);
 #pragma unroll
-    for (int k0 = 0; k0 < KP; k0 += 32) {
-      uint32_t a0[4], a1[4];
-      frag_a(pb0, PS, k0, a0);
-      frag_a(pb0, PS, k0 + 16, a1);
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        uint32_t bb[4];
-        ldsm_x4_t(vb + uint32_t(((k0 + q * 8 + (lane & 7)) * RS + warp * 16 + t * 8) * 2), bb);
-        mma16816(o[t], a0, bb[0], bb[1]);
-        mma16816(o[t], a1, bb[2], bb[3]);
+      for (int k0 = 0; k0 < HD; k0 += 32) {
+        uint32_t a0[4], a1[4], bb[4];
+        frag_a(qb, RS, k0, a0);
+        frag_a(qb, RS, k0 + 16, a1);
+        ldsm_x4(kb + uint32_t(((warp * 8 + (lane & 7)) * RS + k0 + q8 * 8) * 2), bb);
+        mma16816(sacc, a0, bb[0], bb[1]);
+        mma16816(sacc, a1, bb[2], bb[3]);
       }
     }
+    const int jA = warp * 8 + cq;
+    const float s0 = jA < nk ? sacc[0] * SCALE : -INFINITY;
+    const float s1 = jA + 1 < nk ? sacc[1] * SCALE : -INFINITY;
+    float mw = fmaxf(s0, s1);
+    mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 1));
+    mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 2));
+    if ((lane & 3) == 0) red[warp * 8 + row] = mw;
+    __syncthreads();
+    float mc = red[row];
+#pragma unroll
+    for (int w = 1; w < GQ; ++w) mc = fmaxf(mc, red[w * 8 + row]);
+    const float m_new = fmaxf(m_run, mc);
+    // a chunk without valid slots leaves everything as it is (m_new may still be -inf)
+    const float alpha = m_new == -INFINITY ? 1.f : expf(m_run - m_new);
+    const float p0 = jA < nk ? expf(s0 - m_new) : 0.f;
+    const float p1 = jA + 1 < nk ? expf(s1 - m_new) : 0.f;
+    float lw = p0 + p1;
+    lw += __shfl_xor_sync(0xffffffffu, lw, 1);
+    lw += __shfl_xor_sync(0xffffffffu, lw, 2);
+    if ((lane & 3) == 0) red[GQ * 8 + warp * 8 + row] = lw;
+    *reinterpret_cast<__nv_bfloat162*>(ps + row * PS + jA) = __floats2bfloat162_rn(p0, p1);
+    __syncthreads();
+    float lc = 0.f;
+#pragma unroll
+    for (int w = 0; w < GQ; ++w) lc += red[GQ * 8 + w * 8 + row];
+    l_run = l_run * alpha + lc;
+    m_run = m_new;
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) o[t][r] *= alpha;  // rows 8..15 (r >= 2) are zero anyway
+    // ---- O += P V: warp w, dimensions [16w, 16w + 16)
+    {
+      const uint32_t pb0 = smem_u32(ps), vb = smem_u32(vb_);
+#pragma unroll
+      for (int k0 = 0; k0 < KP; k0 += 32) {
+        uint32_t a0[4], a1[4];
+        frag_a(pb0, PS, k0, a0);
+        frag_a(pb0, PS, k0 + 16, a1);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          uint32_t bb[4];
+          ldsm_x4_t(vb + uint32_t(((k0 + q8 * 8 + (lane & 7)) * RS + warp * 16 + t * 8) * 2), bb);
+          mma16816(o[t], a0, bb[0], bb[1]);
+          mma16816(o[t], a1, bb[2], bb[3]);
+        }
+      }
+    }
+    __syncthreads();  // P, the reductions and this chunk's buffer are free for the next chunk
   }
-  // chunk partials: o (unnormalised, fp32), m, l per query head
+
   const int h = g * GQ + row;
+  if (nsplit == 1) {  // the whole window: the output with the sink
+    const float sink = __ldg(p.sinks + h);
+    const float M = fmaxf(m_run, sink);
+    const float a = m_run == -INFINITY ? 0.f : expf(m_run - M);
+    const float inv = 1.0f / (l_run * a + expf(sink - M));
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+      *reinterpret_cast<__nv_bfloat162*>(p.out + ((size_t)b * NH + h) * HD + warp * 16 + t * 8 + cq) =
+          __floats2bfloat162_rn(o[t][0] * a * inv, o[t][1] * a * inv);
+    return;
+  }
+
+  // ---- several splits: the split's partials (o unnormalised, fp32; m; l) per query head
   float* pp = p.part + (((size_t)b * NH + h) * NSPLIT + split) * PSTRIDE;
 #pragma unroll
   for (int t = 0; t < 2; ++t)
     *reinterpret_cast<float2*>(pp + warp * 16 + t * 8 + cq) = make_float2(o[t][0], o[t][1]);
   if (warp == 0 && (lane & 3) == 0) {
-    float l = red_l[0][row];
-#pragma unroll
-    for (int w = 1; w < GQ; ++w) l += red_l[w][row];
-    pp[HD] = m;  // -inf for a chunk without valid slots (then l = 0 and o = 0)
-    pp[HD + 1] = l;
+    pp[HD] = m_run;  // -inf for a split without valid slots (then l = 0 and o = 0)
+    pp[HD + 1] = l_run;
   }
 
-  // ---- the last of the NSPLIT CTAs of (b, g) merges the chunks with the sink (warp w: head 8g + w,
-  // lane: dimensions 4 lane .. 4 lane + 3), in chunk order
+  // the last of the splits of (b, g) merges them with the sink (warp w: head 8g + w, lane:
+  // dimensions 4 lane .. 4 lane + 3), in split order
   __threadfence();
   __syncthreads();
   if (tid == 0) {
     uint32_t* tk = p.ticket + (size_t)b * NKV + g;
     const uint32_t prev = atomicAdd(tk, 1u);
-    s_last = prev == NSPLIT - 1;
+    s_last = prev == uint32_t(nsplit - 1);
     if (s_last) *tk = 0u;  // every CTA of (b, g) has arrived: ready for the next call
   }
   __syncthreads();
@@ -229,13 +282,14 @@ __global__ void __launch_bounds__(NT) decode_kernel(const __grid_constant__ Para
   float ms[NSPLIT], M = sink;
 #pragma unroll
   for (int c = 0; c < NSPLIT; ++c) {
-    ms[c] = __ldcg(ph + c * PSTRIDE + HD);
+    ms[c] = c < nsplit ? __ldcg(ph + c * PSTRIDE + HD) : -INFINITY;
     M = fmaxf(M, ms[c]);
   }
   float L = expf(sink - M);
   float O[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int c = 0; c < NSPLIT; ++c) {
+    if (c >= nsplit) break;
     const float wgt = ms[c] == -INFINITY ? 0.f : expf(ms[c] - M);
     const float4 oc = __ldcg(reinterpret_cast<const float4*>(ph + c * PSTRIDE + 4 * lane));
     L = fmaf(wgt, __ldcg(ph + c * PSTRIDE + HD + 1), L);
