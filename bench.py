@@ -881,6 +881,30 @@ def run_reference(args, rank, world, local):
                 e2e=dict(value=round(v, 3), unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
 
 
+def decode_phase_trace(layer, fn, flush_buf):
+    """Phase stamps of the decode kernel: per slot, min / median / max over CTAs, in us from the
+    earliest CTA start; five repetitions, the median of each statistic reported."""
+    names = {0: "start", 1: "inputs_ready", 11: "A_first_block", 2: "A_done", 3: "barrier1", 4: "routed",
+             5: "tables", 6: "C_issued", 12: "C_first_block", 7: "C_done", 8: "D_start", 13: "D_first_block",
+             9: "D_done", 14: "barrier3", 10: "end"}
+    layer.enable_phase_trace(True)
+    reps = []
+    for _ in range(5):
+        flush_buf.fill_(1)
+        fn()
+        rows = layer.read_trace()
+        t0 = min(r[0] for r in rows if r[0])
+        stat = {}
+        for s, nm in names.items():
+            v = sorted((r[s] - t0) / 1e3 for r in rows if r[s])
+            if v:
+                stat[nm] = (v[0], v[len(v) // 2], v[-1])
+        reps.append(stat)
+    layer.enable_phase_trace(False)
+    return {nm: [round(statistics.median(r[nm][i] for r in reps if nm in r), 2) for i in range(3)]
+            for nm in names.values() if all(nm in r for r in reps)}
+
+
 def run_profile_case(args):
     """A small, fixed case for profilers: `steps` forwards at T = --profile tokens, L2
     flushed before each, nothing else (no soak, no timing passes)."""
@@ -914,7 +938,11 @@ def run_profile_case(args):
             fn()
         torch.cuda.synchronize()
         rc = poll()
-        print(json.dumps(dict(profile_case=T, workload=args.workload, steps=args.steps, device_status=rc)))
+        trace = None
+        if args.trace and args.workload == "nvfp4":
+            trace = decode_phase_trace(lay, fn, flush_buf)
+        print(json.dumps(dict(profile_case=T, workload=args.workload, steps=args.steps, device_status=rc,
+                              trace=trace)))
         if rc != 0:
             raise SystemExit(1)
         return
@@ -957,27 +985,7 @@ def run_profile_case(args):
             a, b = d.pop("first_start_last_end_ns")
             d["span_from_router_start_us"] = [round((a - t0) / 1e3, 1), round((b - t0) / 1e3, 1)]
     elif args.trace:
-        # phase stamps of the decode kernel: per slot, min / median / max over CTAs, in us from
-        # the earliest CTA start; several repetitions, the median of each statistic reported
-        names = {0: "start", 1: "inputs_ready", 11: "A_first_block", 2: "A_done", 3: "barrier1", 4: "routed",
-                 5: "tables", 6: "C_issued", 12: "C_first_block", 7: "C_done", 8: "barrier2", 13: "D_first_block",
-                 9: "D_done", 14: "barrier3", 10: "end"}
-        layer.enable_phase_trace(True)
-        reps = []
-        for _ in range(5):
-            flush_buf.fill_(1)
-            layer.forward(x)
-            rows = layer.read_trace()
-            t0 = min(r[0] for r in rows if r[0])
-            stat = {}
-            for s, nm in names.items():
-                v = sorted((r[s] - t0) / 1e3 for r in rows if r[s])
-                if v:
-                    stat[nm] = (v[0], v[len(v) // 2], v[-1])
-            reps.append(stat)
-        layer.enable_phase_trace(False)
-        trace = {nm: [round(statistics.median(r[nm][i] for r in reps if nm in r), 2) for i in range(3)]
-                 for nm in names.values() if all(nm in r for r in reps)}
+        trace = decode_phase_trace(layer, lambda: layer.forward(x), flush_buf)
     layer.close()
     print(json.dumps(dict(profile_case=T, steps=args.steps, device_status=rc, y_abs_mean=float(y.float().abs().mean()),
                           trace=trace)))

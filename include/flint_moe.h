@@ -161,34 +161,36 @@ flint_moe_status flint_moe_destroy(flint_moe_t h);
  * engines).  NVFP4, by the format's published definition: each weight is an FP4 E2M1 code, every
  * 16 consecutive weights along the contraction dimension share one FP8 E4M3 scale, and each
  * matrix has one fp32 tensor scale: w = e2m1 * e4m3 * tensor_scale.  Layouts (device memory,
- * 16-byte aligned), for a matrix W [K][N] of the math orientation y = x W:
- *   codes  uint8 [K][N/2]: byte (k, j) holds W[k][2j] in its low nibble, W[k][2j+1] in its high;
- *   scales uint8 [K/16][N]: E4M3 bits of the scale of W[16g .. 16g+15][n].
+ * 16-byte aligned), K-major, for a matrix W [K][N] of the math orientation y = x W (K the
+ * contraction dimension):
+ *   codes  uint8 [N][K/2]: byte (n, j) holds W[2j][n] in its low nibble, W[2j+1][n] in its high;
+ *   scales uint8 [N][K/16]: E4M3 bits of the scale of W[16g .. 16g+15][n].
  * The routed experts' matrices are stacked as in flint_moe_weights, with one tensor scale per
  * expert and matrix (device fp32 arrays); the router stays bf16.  A handle made by
  * flint_moe_create_nvfp4 is used with flint_moe_route / flint_moe_forward / flint_moe_destroy
  * and the other per-handle calls; it runs the decode-size kernel, streaming the codes and scales
- * (4.5 bits per weight) and dequantising in shared memory (e2m1 * e4m3 is exact in bf16), with
- * the tensor scale applied to each finished output in fp32.  Decode sizes only: max_tokens <= 64,
- * else FLINT_MOE_ERR_UNSUPPORTED. */
+ * (4.5 bits per weight) and multiplying them in f16 (e2m1 * e4m3 is exact in f16; the layer input
+ * and the SwiGLU activations are rounded to f16 for these products, so inputs must stay within
+ * f16's range, |x| < 65504), with the tensor scale applied to each finished output in fp32.
+ * Decode sizes only: max_tokens <= 64, else FLINT_MOE_ERR_UNSUPPORTED. */
 typedef struct {
   const void* w_router;         /* bf16 [hidden][n_experts] */
   const float* router_bias;     /* fp32 [n_experts] or NULL */
-  const uint8_t* gate_codes;    /* [n_experts][hidden][expert_inter / 2] */
-  const uint8_t* up_codes;      /* [n_experts][hidden][expert_inter / 2] */
-  const uint8_t* down_codes;    /* [n_experts][expert_inter][hidden / 2] */
-  const uint8_t* gate_scales;   /* [n_experts][hidden / 16][expert_inter] */
-  const uint8_t* up_scales;     /* [n_experts][hidden / 16][expert_inter] */
-  const uint8_t* down_scales;   /* [n_experts][expert_inter / 16][hidden] */
+  const uint8_t* gate_codes;    /* [n_experts][expert_inter][hidden / 2] */
+  const uint8_t* up_codes;      /* [n_experts][expert_inter][hidden / 2] */
+  const uint8_t* down_codes;    /* [n_experts][hidden][expert_inter / 2] */
+  const uint8_t* gate_scales;   /* [n_experts][expert_inter][hidden / 16] */
+  const uint8_t* up_scales;     /* [n_experts][expert_inter][hidden / 16] */
+  const uint8_t* down_scales;   /* [n_experts][hidden][expert_inter / 16] */
   const float* gate_tscale;     /* device fp32 [n_experts] */
   const float* up_tscale;       /* device fp32 [n_experts] */
   const float* down_tscale;     /* device fp32 [n_experts] */
-  const uint8_t* sgate_codes;   /* [hidden][shared_inter / 2] */
-  const uint8_t* sup_codes;     /* [hidden][shared_inter / 2] */
-  const uint8_t* sdown_codes;   /* [shared_inter][hidden / 2] */
-  const uint8_t* sgate_scales;  /* [hidden / 16][shared_inter] */
-  const uint8_t* sup_scales;    /* [hidden / 16][shared_inter] */
-  const uint8_t* sdown_scales;  /* [shared_inter / 16][hidden] */
+  const uint8_t* sgate_codes;   /* [shared_inter][hidden / 2] */
+  const uint8_t* sup_codes;     /* [shared_inter][hidden / 2] */
+  const uint8_t* sdown_codes;   /* [hidden][shared_inter / 2] */
+  const uint8_t* sgate_scales;  /* [shared_inter][hidden / 16] */
+  const uint8_t* sup_scales;    /* [shared_inter][hidden / 16] */
+  const uint8_t* sdown_scales;  /* [hidden][shared_inter / 16] */
   float sgate_tscale, sup_tscale, sdown_tscale;
 } flint_moe_nvfp4_weights;
 

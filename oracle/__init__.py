@@ -328,11 +328,12 @@ def e4m3_to_f64(byte: int) -> float:
 
 
 def nvfp4_dequant(codes, scales, tensor_scale) -> np.ndarray:
-    """W [K, N] float64 from NVFP4 codes [K, N/2] (uint8, two per byte, low nibble first), E4M3
-    block scales [K/16, N] (uint8) and the fp32 tensor scale."""
+    """W [K, N] float64 from the K-major NVFP4 encoding: codes [N, K/2] (uint8, two consecutive k
+    per byte, the lower k in the low nibble), E4M3 block scales [N, K/16] (uint8) and the fp32
+    tensor scale."""
     codes = np.ascontiguousarray(codes, dtype=np.uint8)
     scales = np.ascontiguousarray(scales, dtype=np.uint8)
-    K, N = codes.shape[0], codes.shape[1] * 2
+    N, K = codes.shape[0], codes.shape[1] * 2
     out = np.empty((K, N))
     _check(_lib().oracle_nvfp4_dequant(_ptr(codes), _ptr(scales), float(tensor_scale), K, N, _ptr(out)),
            "nvfp4_dequant")

@@ -322,12 +322,12 @@ double oracle_e4m3_to_f64(unsigned byte) {
 
 int oracle_nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, float tensor_scale, int K, int N,
                          double* out) {
-  if (!codes || !scales || !out || K <= 0 || N <= 0 || K % 16 || N % 2) return ORACLE_EINVAL;
+  if (!codes || !scales || !out || K <= 0 || N <= 0 || K % 16) return ORACLE_EINVAL;
   for (int k = 0; k < K; ++k)
     for (int n = 0; n < N; ++n) {
-      const uint8_t byte = codes[(size_t)k * (N / 2) + n / 2];
-      const unsigned code = (n % 2) ? (byte >> 4) : (byte & 15u);
-      const double s = oracle_e4m3_to_f64(scales[(size_t)(k / 16) * N + n]);
+      const uint8_t byte = codes[(size_t)n * (K / 2) + k / 2];
+      const unsigned code = (k % 2) ? (byte >> 4) : (byte & 15u);
+      const double s = oracle_e4m3_to_f64(scales[(size_t)n * (K / 16) + k / 16]);
       out[(size_t)k * N + n] = oracle_e2m1_to_f64(code) * s * (double)tensor_scale;
     }
   return ORACLE_OK;

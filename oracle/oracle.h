@@ -101,8 +101,9 @@ void oracle_rmsnorm(const double* x, int T, int H, double eps, double* r);
  * value = e2m1 * e4m3 * tensor_scale. */
 double oracle_e2m1_to_f64(unsigned code);  /* low 4 bits */
 double oracle_e4m3_to_f64(unsigned byte);
-/* W [K][N] from codes [K][N/2] (byte (k, j): column 2j in the low nibble, 2j+1 in the high),
- * scales [K/16][N] (E4M3 bytes) and the tensor scale; out [K][N].  K % 16 == 0, N even. */
+/* W [K][N] (the math orientation y = x W) from the K-major encoding: codes [N][K/2] (byte
+ * (n, j): W[2j][n] in the low nibble, W[2j+1][n] in the high), scales [N][K/16] (E4M3 bytes; the
+ * scale of W[16g .. 16g+15][n]) and the tensor scale; out [K][N].  K % 16 == 0. */
 int oracle_nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, float tensor_scale, int K, int N,
                          double* out);
 

@@ -78,12 +78,16 @@ struct StreamMaps {
   CUtensorMap wsd;  // [IS][H], box 64 x 128
 };
 
-// NVFP4 expert weights (Params::fp4), kept in the workspace (Params::fp4_maps): E2M1 codes two per
-// byte, [rows][cols / 2] uint8, boxes of 64 bytes (128 columns) x 256 rows; E4M3 scales [rows /
-// 16][cols] uint8, boxes of 128 bytes x 16 (gate / up) or 32 (down) scale rows.  No swizzle.
+// NVFP4 expert weights (Params::fp4), kept in the workspace (Params::fp4_maps), K-major: for a
+// matrix W [K][N] of y = x W, E2M1 codes [N][K/2] uint8 (two consecutive k per byte) and E4M3
+// scales [N][K/16] uint8.  Gate/up codes: 3-D maps (128 bytes of a row, rows, the row's eight
+// 128-byte pieces), boxes of 128 x 16 rows x 8 with the 128-byte swizzle (shared-memory line = piece
+// x 16 + row, so the rows of an MMA fragment fall on distinct banks); their scales: boxes of 128
+// bytes x 16 rows.  Down codes: boxes of 128 bytes x 128 rows (128-byte swizzle); their scales: the
+// block's 4 KB as 32 rows of 128 bytes.
 struct Fp4Maps {
-  CUtensorMap qg, qu, qd, qsg, qsu, qsd;  // codes: [E*H][I/2], [E*H][I/2], [E*I][H/2], [H][IS/2], ., [IS][H/2]
-  CUtensorMap sg, su, sd, ssg, ssu, ssd;  // scales: [E*H/16][I], ., [E*I/16][H], [H/16][IS], ., [IS/16][H]
+  CUtensorMap qg, qu, qd, qsg, qsu, qsd;  // codes: [E*I][H/2], ., [E*H][I/2], [IS][H/2], ., [H][IS/2]
+  CUtensorMap sg, su, sd, ssg, ssu, ssd;  // scales: [E*I][H/16], ., [E*H][I/16], [IS][H/16], ., [H][IS/16]
 };
 
 // Kernel modes, each its own instantiation (the bf16 MoE kernel carries no code of the others:
@@ -92,21 +96,23 @@ constexpr int MODE_MOE = 0;    // the MoE layer, bf16 weights
 constexpr int MODE_FP4 = 1;    // the MoE layer, NVFP4 expert weights
 constexpr int MODE_DENSE = 2;  // a dense SwiGLU MLP layer (the shared-expert steps at width ID)
 
-// ---- NVFP4 streaming (decode sizes): a block is 256 rows x 128 columns of gate and of up (32 KB of
-// codes + 4 KB of scales), or 512 rows x 128 columns of a down matrix (the same sizes); the codes
-// land in the stage ring, the scales in a ring of 4 KB slots beside it.  Each warp dequantises
-// (e2m1 * e4m3, exact in bf16) the part of a block it multiplies into a 16 KB bf16 tile -- 32 rows
-// of gate/up or 64 rows of down at a time -- and runs the bf16 warp MMAs on it; the tensor scale
-// multiplies the finished item in fp32.  Token groups of 8 rows only (T <= FP4_MAX_T).
+// ---- NVFP4 streaming (decode sizes): a gate/up block is 16 columns x all 2048 k of gate and of up
+// (each matrix's 16 K-major rows are one contiguous 16 KB of codes and 2 KB of scales: one copy
+// each; the eight warps split K and add their partial sums in shared memory, so an item is one
+// block), a down block 128 columns x 512 k (32 KB of codes in two boxes, 4 KB of scales); the
+// codes land in the stage ring, the scales in a ring of 4 KB slots beside it.  Each lane builds
+// the MMA A fragments of its rows straight from the codes in registers (e2m1 -> f16 by the
+// hardware conversion, times the block's e4m3 scale: exact in f16) and the warp runs f16 MMAs
+// against the token rows staged in f16; the tensor scale multiplies the finished item in fp32.
+// Token groups of 8 rows only (T <= FP4_MAX_T).
 constexpr int FP4_MAX_T = 64;
-constexpr int FP4_GU_ROWS = 256;
+constexpr int FP4_GU_COLS = 16;               // columns of gate and of up per gate/up block (all K)
 constexpr int FP4_DN_ROWS = 512;
-constexpr int FP4_GU_KB = H / FP4_GU_ROWS;    // 8 blocks per gate/up item
+constexpr int FP4_GU_KB = 1;                  // one block per gate/up item
 constexpr int FP4_DN_KB = I / FP4_DN_ROWS;    // 1 block per routed down item
 constexpr int FP4_SD_KB = IS / FP4_DN_ROWS;   // 2 blocks per shared down item
 constexpr int FP4_CODE_BYTES = 32768;
 constexpr int FP4_SCALE_BYTES = 4096;
-constexpr int FP4_DQ_BYTES = 16384;
 static_assert(FP4_CODE_BYTES <= BLK_BYTES, "the codes fit a stage");
 
 // Token rows per group for a call of T tokens: 16 when T > 64 (the weights of the shared
@@ -167,10 +173,11 @@ __host__ __device__ constexpr int fused_smem_bytes(int G) { return out_offset(G)
 static_assert(Smem::s_idx + MAX_PAIRS * 4 <= Smem::xs + xs_bytes(NT_MAX / 2), "routing scratch must fit in xs");
 static_assert(Smem::perm % 16 == 0 && Smem::gw % 16 == 0 && Smem::xs % 16 == 0, "16-byte aligned tables");
 constexpr int FUSED_SMEM = fused_smem_bytes(NT_MAX);  // the largest launch
-// NVFP4 launches (8-row groups): the scale slots and the dequantised tile after the output tile.
+// NVFP4 launches (8-row groups): the scale slots after the output tile.
 __host__ __device__ constexpr int fp4_scl_offset() { return (out_offset(NT_MAX / 2) + NT_MAX / 2 * 256 * 4 + 1023) / 1024 * 1024; }
-__host__ __device__ constexpr int fp4_dq_offset() { return fp4_scl_offset() + NSTAGE * FP4_SCALE_BYTES; }
-__host__ __device__ constexpr int fp4_smem_bytes() { return fp4_dq_offset() + FP4_DQ_BYTES + 1024; }
+__host__ __device__ constexpr int fp4_red_offset() { return fp4_scl_offset() + NSTAGE * FP4_SCALE_BYTES; }
+// (+ the warps' partial sums of a gate/up block: 8 x 256 floats)
+__host__ __device__ constexpr int fp4_smem_bytes() { return fp4_red_offset() + NWARPS * 256 * 4 + 1024; }
 static_assert(fp4_smem_bytes() <= FUSED_SMEM, "an NVFP4 launch fits the kernel's shared-memory limit");
 static_assert(FUSED_SMEM <= 227 * 1024, "shared memory budget");
 static_assert(GU_KB <= 64 && SD_KB <= 64 && DN_KB <= 64, "an item's pieces fit the slot list");
@@ -224,12 +231,27 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// The same with f16 operands (the NVFP4 mode: its dequantised weights are exact f16 values).
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+template <bool F16>
+__device__ __forceinline__ void mma_op(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (F16)
+    mma_f16(d, a, b0, b1);
+  else
+    mma_bf16(d, a, b0, b1);
+}
 
 // d[h] += A * B_h over `ksteps` (even) k-steps of 16 rows starting at tile row `r0`, where A =
 // the 16 columns [m0, m0+16) of a swizzled weight tile (rows = k) and B_h = the staged input
 // rows xs[8h + n][k0 + ...] (8 tokens each, row stride xstride bf16); B_1 (tokens 8..15) only
 // when TWO.  Two k-steps per B load.
-template <bool TWO>
+template <bool TWO, bool F16 = false>
 __device__ __forceinline__ void mma_tile_t(float (&d)[2][4], uint32_t tile, int m0, int r0, int ksteps, uint32_t xs,
                                            int xstride, int k0) {
   const int lane = threadIdx.x & 31;
@@ -247,27 +269,28 @@ __device__ __forceinline__ void mma_tile_t(float (&d)[2][4], uint32_t tile, int 
     if constexpr (TWO) ldsm_x4(bbase + bhi + uint32_t(s * 16 * 2), b2);
     uint32_t a[4];
     ldsm_x4_trans(tile + swz(r0 + s * 16 + ak + i, am), a);
-    mma_bf16(d[0], a, b[0], b[1]);
-    if constexpr (TWO) mma_bf16(d[1], a, b2[0], b2[1]);
+    mma_op<F16>(d[0], a, b[0], b[1]);
+    if constexpr (TWO) mma_op<F16>(d[1], a, b2[0], b2[1]);
     ldsm_x4_trans(tile + swz(r0 + (s + 1) * 16 + ak + i, am), a);
-    mma_bf16(d[0], a, b[2], b[3]);
-    if constexpr (TWO) mma_bf16(d[1], a, b2[2], b2[3]);
+    mma_op<F16>(d[0], a, b[2], b[3]);
+    if constexpr (TWO) mma_op<F16>(d[1], a, b2[2], b2[3]);
   }
 }
 
 // `two` is warp-uniform: a group of at most 8 rows runs the one-tile loop.
+template <bool F16 = false>
 __device__ __forceinline__ void mma_tile(float (&d)[2][4], uint32_t tile, int m0, int r0, int ksteps, uint32_t xs,
                                          int xstride, int k0, bool two) {
   if (two)
-    mma_tile_t<true>(d, tile, m0, r0, ksteps, xs, xstride, k0);
+    mma_tile_t<true, F16>(d, tile, m0, r0, ksteps, xs, xstride, k0);
   else
-    mma_tile_t<false>(d, tile, m0, r0, ksteps, xs, xstride, k0);
+    mma_tile_t<false, F16>(d, tile, m0, r0, ksteps, xs, xstride, k0);
 }
 
 // d[m][h] += A_m * B_h for the two 16-column tiles A_0 = columns [m0, m0+16) and A_1 =
 // [m0+16, m0+32) of a swizzled weight tile (rows 0 .. 16*ksteps-1 = k), B_h as in mma_tile_t;
 // one B load feeds both tiles.
-template <bool TWO>
+template <bool TWO, bool F16 = false>
 __device__ __forceinline__ void mma_pair_t(float (&d)[2][2][4], uint32_t tile, int m0, int ksteps, uint32_t xs,
                                            int xstride, int k0) {
   const int lane = threadIdx.x & 31;
@@ -285,21 +308,22 @@ __device__ __forceinline__ void mma_pair_t(float (&d)[2][2][4], uint32_t tile, i
     for (int m = 0; m < 2; ++m) {
       uint32_t a[4];
       ldsm_x4_trans(tile + swz(s * 16 + ak + i, am + 16 * m), a);
-      mma_bf16(d[m][0], a, b[0], b[1]);
-      if constexpr (TWO) mma_bf16(d[m][1], a, b2[0], b2[1]);
+      mma_op<F16>(d[m][0], a, b[0], b[1]);
+      if constexpr (TWO) mma_op<F16>(d[m][1], a, b2[0], b2[1]);
       ldsm_x4_trans(tile + swz((s + 1) * 16 + ak + i, am + 16 * m), a);
-      mma_bf16(d[m][0], a, b[2], b[3]);
-      if constexpr (TWO) mma_bf16(d[m][1], a, b2[2], b2[3]);
+      mma_op<F16>(d[m][0], a, b[2], b[3]);
+      if constexpr (TWO) mma_op<F16>(d[m][1], a, b2[2], b2[3]);
     }
   }
 }
 
+template <bool F16 = false>
 __device__ __forceinline__ void mma_pair(float (&d)[2][2][4], uint32_t tile, int m0, int ksteps, uint32_t xs,
                                          int xstride, int k0, bool two) {
   if (two)
-    mma_pair_t<true>(d, tile, m0, ksteps, xs, xstride, k0);
+    mma_pair_t<true, F16>(d, tile, m0, ksteps, xs, xstride, k0);
   else
-    mma_pair_t<false>(d, tile, m0, ksteps, xs, xstride, k0);
+    mma_pair_t<false, F16>(d, tile, m0, ksteps, xs, xstride, k0);
 }
 
 // ---------------------------------------------------------------- tickets and barriers
@@ -431,6 +455,14 @@ __device__ __forceinline__ int find_group_owner(const int* tgp, int n, int gi) {
 // usually share their token group and its staged input rows.
 // K blocks per item of a kind: 64-row (gate/up) or 128-row (down) bf16 blocks, or the NVFP4
 // blocks of 256 / 512 rows.
+// Column blocks of a routed and of the shared expert's gate/up, per token group.
+template <int MODE>
+__host__ __device__ constexpr int gu_ncb() { return MODE == MODE_FP4 ? I / FP4_GU_COLS : GU_NCB; }
+template <int MODE>
+__host__ __device__ constexpr int sgu_ncb() {
+  return MODE == MODE_FP4 ? IS / FP4_GU_COLS : MODE == MODE_DENSE ? ID / 128 : SGU_NCB;
+}
+
 template <int MODE>
 __device__ __forceinline__ int kblocks_of(const Params& p, int kind) {
   switch (kind) {
@@ -445,12 +477,12 @@ __device__ __forceinline__ int kblocks_of(const Params& p, int kind) {
 template <int MODE>
 __device__ __forceinline__ Item decode_item(const Params& p, const Meta& m, int kind, int idx) {
   const int T = p.T;
-  const int sncb = MODE == MODE_DENSE ? ID / 128 : SGU_NCB;  // 128-column blocks of the shared gate/up
+  const int sncb = sgu_ncb<MODE>();  // column blocks of the shared gate/up
   Item it;
   it.kind = kind;
   it.idx = idx;
   if (kind == KIND_GU || kind == KIND_DN) {
-    const int nch = kind == KIND_GU ? GU_NCB : OUT_NCB;
+    const int nch = kind == KIND_GU ? gu_ncb<MODE>() : OUT_NCB;
     const int gi = idx / nch;
     it.c = idx % nch;
     const int u = find_group_owner(m.tgp, m.U, gi);
@@ -493,42 +525,42 @@ __device__ __forceinline__ void block_kind(const BlockList& L, int b, int& kind,
   }
 }
 
-// NVFP4 block (codes into `stage`, scales into `scl`): gate/up 256 rows of gate and of up; down
-// 512 rows, as two 256-row code boxes.
+// NVFP4 block (codes into `stage`, scales into `scl`), K-major: gate/up 16 columns x all 2048 k of
+// gate and of up (a 16 KB code box and a 2 KB scale box each); down 128 columns x 512 k (two 16 KB
+// code boxes of 256 k, one 4 KB scale box).
 __device__ void issue_block_fp4(const Item& it, const Fp4Maps& maps, int kb, uint8_t* stage, uint8_t* scl,
                                 uint64_t* bar) {
   mbar_arrive_expect_tx(bar, FP4_CODE_BYTES + FP4_SCALE_BYTES);
-  const int xc = it.c * 64, xs = it.c * 128;  // code bytes, scale bytes (= columns)
   constexpr int HALF = FP4_CODE_BYTES / 2, SH = FP4_SCALE_BYTES / 2;
   switch (it.kind) {
     case KIND_GU: {
-      const int y = it.e * H + kb * FP4_GU_ROWS, ys = y / 16;
-      tma_load_2d(stage, &maps.qg, xc, y, bar);
-      tma_load_2d(stage + HALF, &maps.qu, xc, y, bar);
-      tma_load_2d(scl, &maps.sg, xs, ys, bar);
-      tma_load_2d(scl + SH, &maps.su, xs, ys, bar);
+      const int y = it.e * I + it.c * FP4_GU_COLS;
+      tma_load_3d(stage, &maps.qg, 0, y, 0, bar);
+      tma_load_3d(stage + HALF, &maps.qu, 0, y, 0, bar);
+      tma_load_2d(scl, &maps.sg, 0, y, bar);
+      tma_load_2d(scl + SH, &maps.su, 0, y, bar);
       break;
     }
     case KIND_SGU: {
-      const int y = kb * FP4_GU_ROWS, ys = y / 16;
-      tma_load_2d(stage, &maps.qsg, xc, y, bar);
-      tma_load_2d(stage + HALF, &maps.qsu, xc, y, bar);
-      tma_load_2d(scl, &maps.ssg, xs, ys, bar);
-      tma_load_2d(scl + SH, &maps.ssu, xs, ys, bar);
+      const int y = it.c * FP4_GU_COLS;
+      tma_load_3d(stage, &maps.qsg, 0, y, 0, bar);
+      tma_load_3d(stage + HALF, &maps.qsu, 0, y, 0, bar);
+      tma_load_2d(scl, &maps.ssg, 0, y, bar);
+      tma_load_2d(scl + SH, &maps.ssu, 0, y, bar);
       break;
     }
     case KIND_SD: {
-      const int y = kb * FP4_DN_ROWS;
-      tma_load_2d(stage, &maps.qsd, xc, y, bar);
-      tma_load_2d(stage + HALF, &maps.qsd, xc, y + FP4_DN_ROWS / 2, bar);
-      tma_load_2d(scl, &maps.ssd, xs, y / 16, bar);
+      const int y = it.c * 128, x = kb * FP4_DN_ROWS / 2;
+      tma_load_2d(stage, &maps.qsd, x, y, bar);
+      tma_load_2d(stage + HALF, &maps.qsd, x + 128, y, bar);
+      tma_load_2d(scl, &maps.ssd, kb * FP4_DN_ROWS / 16, y, bar);
       break;
     }
     default: {
-      const int y = it.e * I + kb * FP4_DN_ROWS;
-      tma_load_2d(stage, &maps.qd, xc, y, bar);
-      tma_load_2d(stage + HALF, &maps.qd, xc, y + FP4_DN_ROWS / 2, bar);
-      tma_load_2d(scl, &maps.sd, xs, y / 16, bar);
+      const int y = it.e * H + it.c * 128;
+      tma_load_2d(stage, &maps.qd, 0, y, bar);
+      tma_load_2d(stage + HALF, &maps.qd, 128, y, bar);
+      tma_load_2d(scl, &maps.sd, 0, y / 4, bar);  // the block's 128 rows x 32 bytes as 32 x 128
       break;
     }
   }
@@ -600,6 +632,8 @@ struct Stream {
   float* out;  // output tile of the current segment
   int comb_items;  // > 0: combine each 128-column block when its comb_items down items are done
   bool dataflow;   // gate/up items signal their token group; down items wait for theirs (no C-D barrier)
+  uint32_t* sig_ctr;  // the token-group counter with finished items not yet signalled (dataflow)
+  uint32_t sig_n;     // how many
   float* pbank;    // the current step's partial slots (steps C and D use separate banks)
   const uint16_t* perm;
   const uint16_t* inv;
@@ -644,67 +678,97 @@ __device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t half) {
   asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(r) : "r"(half));
   return r;
 }
-// 8 consecutive columns: codes (4 bytes) times their 8 scales (4 f16x2) -> 8 bf16.  Every product
-// e2m1 * e4m3 has at most 5 significant bits and lies in [2^-10, 2688]: exact in f16 and in bf16.
-__device__ __forceinline__ uint4 dq8(uint32_t codes, const uint32_t (&s2)[4]) {
-  uint32_t w[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint32_t h = e2m1x2_f16x2((codes >> (8 * q)) & 0xFFu);
-    const __half2 prod = __hmul2(*reinterpret_cast<const __half2*>(&h), *reinterpret_cast<const __half2*>(&s2[q]));
-    const float2 f = __half22float2(prod);
-    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
-    w[q] = *reinterpret_cast<const uint32_t*>(&b);
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
+// The e4m3 scale bytes k, k + 1 (k even) of 16 bytes (a uint4) as f16x2 (k in the low half).
+__device__ __forceinline__ uint32_t scale_pair(const uint4& s, int k) {
+  const uint32_t w = k < 4 ? s.x : k < 8 ? s.y : k < 12 ? s.z : s.w;
+  return e4m3x2_f16x2((w >> (8 * (k & 3))) & 0xFFFFu);
 }
-__device__ __forceinline__ void scales8(const uint8_t* p, uint32_t (&s2)[4]) {
-  const uint2 v = *reinterpret_cast<const uint2*>(p);
-  s2[0] = e4m3x2_f16x2(v.x & 0xFFFFu);
-  s2[1] = e4m3x2_f16x2(v.x >> 16);
-  s2[2] = e4m3x2_f16x2(v.y & 0xFFFFu);
-  s2[3] = e4m3x2_f16x2(v.y >> 16);
+// f16x2 of the low (lo = true) or high half of v in both halves.
+__device__ __forceinline__ uint32_t bcast_half(uint32_t v, bool lo) { return __byte_perm(v, 0u, lo ? 0x1010 : 0x3232); }
+
+// Two k-steps (ks, ks + 1) of one 16-row MMA tile of a K-major NVFP4 code tile: `c0` and `c1` are the
+// 16 code bytes of rows g and g + 8 for the two k-steps (bytes 0-7: k-step ks, 8-15: ks + 1; in a
+// k-step, byte j holds k = 2j, 2j + 1), `sg`, `sg8` the rows' two scales as f16x2.  Lane (g, t)
+// takes bytes t and t + 4 of each k-step (the m16n8k16 A layout: k = 2t, 2t + 1 and 2t + 8, 2t + 9),
+// converts them to f16 pairs, multiplies by the scale (exact) and runs the MMA against b.
+__device__ __forceinline__ void fp4_mma2(float (&d)[4], const uint4& c0, const uint4& c1, uint32_t sg, uint32_t sg8,
+                                         int sh, const uint32_t (&b)[4]) {
+#pragma unroll
+  for (int kk = 0; kk < 2; ++kk) {
+    const uint32_t w[4] = {kk ? c0.z : c0.x, kk ? c1.z : c1.x, kk ? c0.w : c0.y, kk ? c1.w : c1.y};
+    const uint32_t s0 = bcast_half(sg, kk == 0), s8 = bcast_half(sg8, kk == 0);
+    uint32_t a[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t h = e2m1x2_f16x2((w[q] >> sh) & 0xFFu);
+      const uint32_t sc = (q & 1) ? s8 : s0;
+      const __half2 prod = __hmul2(*reinterpret_cast<const __half2*>(&h), *reinterpret_cast<const __half2*>(&sc));
+      a[q] = *reinterpret_cast<const uint32_t*>(&prod);
+    }
+    mma_f16(d, a, b[2 * kk], b[2 * kk + 1]);
+  }
 }
 
-// Gate/up: rows [32 sub, +32) of the block (codes [gate | up][256 rows][64 B], scales [gate |
-// up][16][128 B]) -> the warp's 32 columns of its box (boxes [gate 2c | gate 2c+1 | up 2c | up
-// 2c+1], 32 rows x 64 columns, 128-byte swizzled rows) of the 16 KB tile.
-__device__ __forceinline__ void dequant_gu(const uint8_t* codes, const uint8_t* scl, uint8_t* dq, int sub) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int box = warp >> 1, mat = box >> 1;
-  const int m = (warp & 1) * 32 + 8 * (lane & 3);  // first of the lane's 8 columns, in the box
-  const int col = (box & 1) * 64 + m;              // ... in the 128-column block
-  const uint8_t* cb = codes + mat * (FP4_CODE_BYTES / 2) + col / 2;
-  const uint8_t* sb = scl + mat * (FP4_SCALE_BYTES / 2) + col;
-  uint8_t* tile = dq + box * (32 * 128);
+// B fragments (m16n8k16) of two k-steps from the staged token rows (f16), as in mma_tile_t.
+__device__ __forceinline__ void frag_b2(uint32_t xs, int xstride, int k0, uint32_t (&b)[4]) {
+  const int lane = threadIdx.x & 31;
+  ldsm_x4(xs + uint32_t(((lane & 7) * xstride + k0 + (lane >> 3) * 8) * 2), b);
+}
+
+// Gate/up block (NVFP4): warp w takes the block's k in [256 w, +256) (code piece w) for its 16
+// gate and 16 up columns; d[0] = gate, d[1] = up (partial sums over the warp's k).  Codes in
+// shared memory: [piece 8][row 16][128 bytes] per matrix (128-byte swizzled lines: both rows of
+// a lane, g and g + 8, have the swizzle key g); scales [row 16][128 bytes].
+__device__ __forceinline__ void fp4_gateup_block(float (&d)[2][4], const uint8_t* codes, const uint8_t* scl,
+                                                 uint32_t xs, int xstride) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, sh = 8 * (lane & 3);
+  const uint8_t* row = codes + (warp * FP4_GU_COLS + g) * 128;  // gate, row g of piece `warp`
+  uint4 sr[2][2];  // the lane's scale bytes of the warp's k: matrices x rows g, g + 8
 #pragma unroll
-  for (int gi = 0; gi < 2; ++gi) {  // the two 16-row scale groups of the 32 rows
-    uint32_t s2[4];
-    scales8(sb + (sub * 2 + gi) * 128, s2);
+  for (int m = 0; m < 2; ++m) {
+    const uint8_t* sm = scl + m * (FP4_SCALE_BYTES / 2) + 16 * warp;
+    sr[m][0] = *reinterpret_cast<const uint4*>(sm + g * 128);
+    sr[m][1] = *reinterpret_cast<const uint4*>(sm + (g + 8) * 128);
+  }
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      const int r = (lane >> 2) + 8 * (2 * gi + rr);  // row in the sub-tile
-      const uint32_t c4 = *reinterpret_cast<const uint32_t*>(cb + (sub * 32 + r) * 64);
-      *reinterpret_cast<uint4*>(tile + swz(r, m)) = dq8(c4, s2);
+  for (int ks = 0; ks < 16; ks += 2) {  // a 16-byte chunk of each row: k-steps ks, ks + 1
+    uint32_t b[4];
+    frag_b2(xs, xstride, 256 * warp + ks * 16, b);
+    const int off = ((ks >> 1) ^ g) << 4;  // the swizzled chunk (key g: lines g and g + 8)
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      const uint8_t* rm = row + m * (FP4_CODE_BYTES / 2);
+      const uint4 c0 = *reinterpret_cast<const uint4*>(rm + off);
+      const uint4 c1 = *reinterpret_cast<const uint4*>(rm + 8 * 128 + off);
+      fp4_mma2(d[m], c0, c1, scale_pair(sr[m][0], ks), scale_pair(sr[m][1], ks), sh, b);
     }
   }
 }
 
-// Down: rows [64 sub, +64) of the block (codes [512 rows][64 B], scales [32][128 B]) -> the warp's
-// 16 columns of its box (boxes [chunk 2c | 2c+1], 64 rows x 64 columns) of the tile.
-__device__ __forceinline__ void dequant_dn(const uint8_t* codes, const uint8_t* scl, uint8_t* dq, int sub) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int box = warp >> 2;
-  const int m = (warp & 3) * 16 + 8 * (lane & 1);
-  const int col = box * 64 + m;
-  uint8_t* tile = dq + box * (64 * 128);
+// Down block (NVFP4): warp w takes columns [16 w, +16) over the block's 512 k (two code boxes of
+// [128 rows][128 bytes], 128-byte swizzled: rows 16w + g and 16w + g + 8 have the swizzle key g).
+__device__ __forceinline__ void fp4_down_block(float (&d)[2][4], const uint8_t* codes, const uint8_t* scl,
+                                               uint32_t xs, int xstride, int k0) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, sh = 8 * (lane & 3);
+  const int r0 = 16 * warp;
+  uint4 sr[2][2];  // the lane's scale rows (32 bytes each): rows g, g + 8 x k halves
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {  // rows in four 16-row scale groups
-    const int r = (lane >> 1) + 16 * i;
-    uint32_t s2[4];
-    scales8(scl + (sub * 4 + i) * 128 + col, s2);
-    const uint32_t c4 = *reinterpret_cast<const uint32_t*>(codes + (sub * 64 + r) * 64 + col / 2);
-    *reinterpret_cast<uint4*>(tile + swz(r, m)) = dq8(c4, s2);
+  for (int h = 0; h < 2; ++h) {
+    sr[0][h] = *reinterpret_cast<const uint4*>(scl + (r0 + g) * 32 + 16 * h);
+    sr[1][h] = *reinterpret_cast<const uint4*>(scl + (r0 + g + 8) * 32 + 16 * h);
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {  // code box h: k [256 h, +256)
+    const uint8_t* row = codes + h * (FP4_CODE_BYTES / 2) + (r0 + g) * 128;
+#pragma unroll
+    for (int ks = 0; ks < 16; ks += 2) {
+      uint32_t b[4];
+      frag_b2(xs, xstride, k0 + h * 256 + ks * 16, b);
+      const int off = ((ks >> 1) ^ g) << 4;
+      const uint4 c0 = *reinterpret_cast<const uint4*>(row + off);
+      const uint4 c1 = *reinterpret_cast<const uint4*>(row + 8 * 128 + off);
+      fp4_mma2(d[0], c0, c1, scale_pair(sr[0][h], ks), scale_pair(sr[1][h], ks), sh, b);
+    }
   }
 }
 
@@ -734,6 +798,24 @@ __device__ __forceinline__ void signal_done(uint32_t* ctr) {
   csync();
   if (threadIdx.x == 0) atomicAdd(ctr, 1u);
 }
+// A CTA's finished gate/up items are counted per token group and signalled once per run of
+// consecutive items of the group (its items of a group are consecutive in its range), which
+// saves a fence and an atomic per item: flush_done signals the pending run, when the CTA starts an
+// item of another group or ends the step; pend_done adds one finished item of counter `ctr`.
+__device__ __forceinline__ void flush_done(Stream& S) {
+  if (S.sig_ctr && S.sig_n) {
+    __threadfence();
+    csync();
+    if (threadIdx.x == 0) atomicAdd(S.sig_ctr, S.sig_n);
+  }
+  S.sig_ctr = nullptr;
+  S.sig_n = 0;
+}
+__device__ __forceinline__ void pend_done(Stream& S, uint32_t* ctr) {
+  S.sig_ctr = ctr;
+  ++S.sig_n;
+}
+
 // Wait (thread 0, bounded; then the consumers) until a token group's counter reaches `need`.
 __device__ __forceinline__ void wait_done(const Params& p, const uint32_t* ctr, uint32_t need) {
   if (threadIdx.x == 0 && ld_acquire_u32(ctr) < need) {
@@ -792,13 +874,15 @@ __device__ void item_epilogue(Stream& S, const Item& it, const float* vals) {
   if (it.kind == KIND_GU || it.kind == KIND_SGU) {  // vals[t][256]: gate columns, then up columns
     bf16* dst = it.kind == KIND_GU ? p.h : p.hs;
     const int ld = it.kind == KIND_GU ? I : MODE == MODE_DENSE ? ID : IS;
-    if constexpr (MODE == MODE_FP4) {  // NVFP4: the matrices' tensor scales
+    if constexpr (MODE == MODE_FP4) {  // NVFP4: the matrices' tensor scales; h kept in f16
       const float tg = it.kind == KIND_GU ? __ldg(p.ts_gate + it.e) : p.ts_sgate;
       const float tu = it.kind == KIND_GU ? __ldg(p.ts_up + it.e) : p.ts_sup;
-      for (int q = threadIdx.x; q < nt * 128; q += NCONS) {
-        const int t = q >> 7, j = q & 127;
-        const float g = vals[t * 256 + j] * tg, u = vals[t * 256 + 128 + j] * tu;
-        dst[(size_t)(it.row0 + t) * ld + c0 + j] = __float2bfloat16_rn(silu_f32(g) * u);
+      __half* dh = reinterpret_cast<__half*>(dst);
+      const int cf = it.c * FP4_GU_COLS;  // vals [t][32]: 16 gate columns, then 16 up columns
+      for (int q = threadIdx.x; q < nt * FP4_GU_COLS; q += NCONS) {
+        const int t = q / FP4_GU_COLS, j = q % FP4_GU_COLS;
+        const float g = vals[t * 32 + j] * tg, u = vals[t * 32 + FP4_GU_COLS + j] * tu;
+        dh[(size_t)(it.row0 + t) * ld + cf + j] = __float2half_rn(silu_f32(g) * u);
       }
     } else {
       for (int q = threadIdx.x; q < nt * 128; q += NCONS) {
@@ -880,14 +964,18 @@ __device__ void combine_block(const Params& p, const uint16_t* inv, int cb) {
 // in windows.
 template <int MODE>
 __device__ void stage_inputs(Stream& S, const Item& it, int xlen, int k0 = 0) {
-  const int cls = it.kind == KIND_GU ? 1 : it.kind == KIND_SD ? 2 : it.kind == KIND_DN ? 3 : 0;
+  // NVFP4: the gate/up inputs are staged as f16 (the router's stay bf16), so the shared gate/up
+  // rows are a class of their own
+  constexpr bool F16X = MODE == MODE_FP4;
+  const int cls = it.kind == KIND_GU ? 1 : it.kind == KIND_SD ? 2 : it.kind == KIND_DN ? 3
+                  : (F16X && it.kind == KIND_SGU) ? 4 : 0;
   if (cls == S.x_cls && it.row0 == S.x_row0 && k0 == S.x_k0) return;
   S.x_cls = cls;
   S.x_row0 = it.row0;
   S.x_k0 = k0;
   const Params& p = *S.p;
-  if (S.dataflow && it.kind == KIND_DN) wait_done(p, p.hdone + it.idx / OUT_NCB, GU_NCB);
-  if (S.dataflow && it.kind == KIND_SD) wait_done(p, p.hsdone + it.idx / OUT_NCB, MODE == MODE_DENSE ? ID / 128 : SGU_NCB);
+  if (S.dataflow && it.kind == KIND_DN) wait_done(p, p.hdone + it.idx / OUT_NCB, gu_ncb<MODE>());
+  if (S.dataflow && it.kind == KIND_SD) wait_done(p, p.hsdone + it.idx / OUT_NCB, sgu_ncb<MODE>());
   bf16* xs = reinterpret_cast<bf16*>(S.sm + Smem::xs);
   const int cpr = xlen / 8;
   const int G = group_rows(p.T);
@@ -905,6 +993,17 @@ __device__ void stage_inputs(Stream& S, const Item& it, int xlen, int k0 = 0) {
       else
         src = p.h + (size_t)(it.row0 + t) * I;
       v = __ldcg(reinterpret_cast<const uint4*>(src) + k8);
+      if (F16X && (it.kind == KIND_GU || it.kind == KIND_SGU)) {  // bf16 -> f16 (inputs |x| < 65504)
+        float f[8];
+        bf16x8_to_f32(v, f);
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __half2 h2 = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+          w[i] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        v = make_uint4(w[0], w[1], w[2], w[3]);
+      }
     }
     *reinterpret_cast<uint4*>(xs + t * (xlen + XPAD) + k8 * 8) = v;
   }
@@ -953,6 +1052,12 @@ template <int MODE>
 __device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, int& j) {
   const Params& p = *S.p;
   const bool gu = it.kind == KIND_GU || it.kind == KIND_SGU;
+  // the token-group counter of a gate/up item; a pending run of another group is signalled now
+  uint32_t* gctr = nullptr;
+  if (gu && S.dataflow) {
+    gctr = it.kind == KIND_GU ? p.hdone + it.idx / gu_ncb<MODE>() : p.hsdone + it.idx / sgu_ncb<MODE>();
+    if (S.sig_ctr != gctr) flush_done(S);
+  }
   // a shared down input longer than a staged row (a dense layer) is staged from the segment's
   // first K row, and restaged when the segment runs past the window
   int kw = (MODE == MODE_DENSE && it.kind == KIND_SD) ? kb_start * DN_ROWS : 0;  // first staged K column
@@ -973,23 +1078,27 @@ __device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, i
     const uint32_t sub = uint32_t((warp >> 1) * (BLK_BYTES / 4));
     const int m0 = (warp & 1) * 32;
     if constexpr (MODE == MODE_FP4) {
-      // NVFP4 block of 256 rows: eight 32-row sub-tiles dequantised into the warp's part of the tile
-      uint8_t* dq = S.sm + fp4_dq_offset();
-      const uint32_t tile = smem_u32(dq) + uint32_t((warp >> 1) * (32 * 128));
+      // NVFP4 block (one per item): each warp's k piece, then the sum over the warps in shared
+      // memory -> out [t][32] (16 gate columns, then 16 up columns)
+      float acc[2][4] = {};
       for (int q = 0; q < nblk; ++q, ++j) {
         wait_full(S, j);
         const uint8_t* codes = stage_ptr(S, j);
         const uint8_t* scl = S.sm + fp4_scl_offset() + ((S.ring + j) % NSTAGE) * FP4_SCALE_BYTES;
-        for (int s = 0; s < FP4_GU_ROWS / 32; ++s) {
-          dequant_gu(codes, scl, dq, s);
-          if (s == FP4_GU_ROWS / 32 - 1)
-            release(S, j);  // the codes and scales are read (release synchronises the warp first)
-          else
-            __syncwarp();
-          mma_pair(d, tile, m0, 2, xs, xlen + XPAD, (kb_start + q) * FP4_GU_ROWS + s * 32, two);
-          __syncwarp();  // before the next sub-tile overwrites the warp's part
-        }
+        fp4_gateup_block(acc, codes, scl, xs, xlen + XPAD);
+        release(S, j);
       }
+      float* red = reinterpret_cast<float*>(S.sm + fp4_red_offset());
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+          red[warp * 256 + (2 * tig + (r & 1)) * 32 + 16 * m + g + ((r >> 1) << 3)] = acc[m][r];
+      csync();
+      float sum = 0.f;
+#pragma unroll
+      for (int w = 0; w < NWARPS; ++w) sum += red[w * 256 + threadIdx.x];
+      out[threadIdx.x] = sum;
     } else {
       for (int q = 0; q < nblk; ++q, ++j) {
         wait_full(S, j);
@@ -998,38 +1107,31 @@ __device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, i
         release(S, j);
       }
     }
-    const int cb = (warp >> 1) * 64 + m0;
+    if constexpr (MODE != MODE_FP4) {
+      const int cb = (warp >> 1) * 64 + m0;
 #pragma unroll
-    for (int m = 0; m < 2; ++m)
+      for (int m = 0; m < 2; ++m)
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        if (h2 == 1 && !two) break;
+        for (int h2 = 0; h2 < 2; ++h2) {
+          if (h2 == 1 && !two) break;
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
-          out[(8 * h2 + 2 * tig + (r & 1)) * 256 + cb + 16 * m + g + ((r >> 1) << 3)] = d[m][h2][r];
-      }
+          for (int r = 0; r < 4; ++r)
+            out[(8 * h2 + 2 * tig + (r & 1)) * 256 + cb + 16 * m + g + ((r >> 1) << 3)] = d[m][h2][r];
+        }
+    }
   } else {
     // warp w: box w >> 2 (chunk 2c or 2c+1), columns [16*(w&3), +16), all 128 rows
     float d[2][4] = {};
     const uint32_t sub = uint32_t((warp >> 2) * (BLK_BYTES / 2));
     const int m0 = (warp & 3) * 16;
     if constexpr (MODE == MODE_FP4) {
-      // NVFP4 block of 512 rows: eight 64-row sub-tiles
-      uint8_t* dq = S.sm + fp4_dq_offset();
-      const uint32_t tile = smem_u32(dq) + uint32_t((warp >> 2) * (64 * 128));
+      // NVFP4 block: 512 k of the warp's 16 down columns, A fragments from the codes
       for (int q = 0; q < nblk; ++q, ++j) {
         wait_full(S, j);
         const uint8_t* codes = stage_ptr(S, j);
         const uint8_t* scl = S.sm + fp4_scl_offset() + ((S.ring + j) % NSTAGE) * FP4_SCALE_BYTES;
-        for (int s = 0; s < FP4_DN_ROWS / 64; ++s) {
-          dequant_dn(codes, scl, dq, s);
-          if (s == FP4_DN_ROWS / 64 - 1)
-            release(S, j);
-          else
-            __syncwarp();
-          mma_tile(d, tile, m0, 0, 4, xs, xlen + XPAD, (kb_start + q) * FP4_DN_ROWS + s * 64 - kw, two);
-          __syncwarp();
-        }
+        fp4_down_block(d, codes, scl, xs, xlen + XPAD, (kb_start + q) * FP4_DN_ROWS - kw);
+        release(S, j);
       }
     } else {
       for (int q = 0; q < nblk; ++q, ++j) {
@@ -1082,11 +1184,8 @@ __device__ void run_segment(Stream& S, const Item& it, int kb_start, int nblk, i
   }
   if (done) item_epilogue<MODE>(S, it, out);
   csync();
-  // gate/up outputs of a token group complete: its down items may stage them
-  if (done && gu && S.dataflow) {
-    const int sncb = MODE == MODE_DENSE ? ID / 128 : SGU_NCB;
-    signal_done(it.kind == KIND_GU ? p.hdone + it.idx / GU_NCB : p.hsdone + it.idx / sncb);
-  }
+  // gate/up outputs of a token group complete: its down items may stage them (signalled per run)
+  if (done && gu && S.dataflow) pend_done(S, gctr);
   // down outputs: the last item of a 128-column block combines that block for every token
   if (done && S.comb_items && !gu && ticket_last(p.tk_comb + it.c, uint32_t(S.comb_items), S.misc + 14, false)) {
     combine_block(p, S.inv, it.c);
@@ -1107,6 +1206,7 @@ __device__ void consume(Stream& S) {
     else
       run_segment<MODE>(S, it, kb, min(it.KB - kb, S.nb - j), j);
   }
+  if (S.dataflow) flush_done(S);  // the step's last run of gate/up items
 }
 
 // Make L the current step: this CTA's range of its blocks.
@@ -1425,6 +1525,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   S.out = reinterpret_cast<float*>(sm + out_offset(group_rows(p.T)));
   S.comb_items = 0;
   S.dataflow = false;
+  S.sig_ctr = nullptr;
+  S.sig_n = 0;
   S.pbank = partial_bank(p, 0);
   uint16_t* perm = reinterpret_cast<uint16_t*>(sm + Smem::perm);
   uint16_t* inv = reinterpret_cast<uint16_t*>(sm + Smem::inv);
@@ -1532,10 +1634,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int kgu = kblocks_of<MODE>(p, KIND_GU);
     L.k_first = KIND_GU;
     L.kb_first = kgu;
-    L.n_first = S.meta.groups * GU_NCB * kgu;
+    L.n_first = S.meta.groups * gu_ncb<MODE>() * kgu;
     L.k_second = KIND_SGU;
     L.kb_second = kgu;
-    L.n_total = L.n_first + ntg * SGU_NCB * kgu;
+    L.n_total = L.n_first + ntg * sgu_ncb<MODE>() * kgu;
     S.first_slot = 12;
     S.dataflow = true;  // gate/up items signal their token group; step D waits per group
     trace_point(p, 6);
@@ -1654,6 +1756,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   S.plist = reinterpret_cast<int*>(sm + Smem::plist);
   S.out = reinterpret_cast<float*>(sm + out_offset(G));
   S.dataflow = false;  // the layers keep their grid barriers
+  S.sig_ctr = nullptr;
+  S.sig_n = 0;
   S.pbank = partial_bank(base, 0);
   S.comb_items = 0;  // the combine always follows a barrier here: it also normalises
   uint16_t* perm = reinterpret_cast<uint16_t*>(sm + Smem::perm);

@@ -124,8 +124,24 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// K-major NVFP4 gate/up codes [rows][1024 bytes] as a 3-D tensor (128 bytes of a row, rows, the row's
+// eight 128-byte pieces): a box of 128 x 16 rows x 8 pieces is 16 whole rows (16 KB, contiguous in
+// memory), laid out in shared memory as [piece][row][128 bytes] with the 128-byte swizzle.
+bool make_map_fp4_rows(CUtensorMap* m, const void* base, uint64_t rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {128, rows, 8};
+  cuuint64_t strides[2] = {1024, 128};
+  cuuint32_t box[3] = {128, 16, 8};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Row-major uint8 matrix [rows][cols] (NVFP4 codes or scales) -> 2-D tensor map, box of box_cols
-// bytes x box_rows (codes: 64-byte rows with the 64-byte swizzle; scales: no swizzle).
+// bytes x box_rows (codes: 128-byte rows with the 128-byte swizzle; scales: no swizzle).
 bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
                  uint32_t box_rows, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
   auto enc = tensor_map_encoder();
@@ -1127,18 +1143,16 @@ extern "C" flint_moe_status flint_moe_create_nvfp4(const flint_moe_config* cfg, 
   Fp4Maps m;
   const uint64_t EH = (uint64_t)E * H, EI = (uint64_t)E * I;
   const bool ok =
-      make_map_u8(&m.qg, w->gate_codes, EH, I / 2, 64, FP4_GU_ROWS, CU_TENSOR_MAP_SWIZZLE_64B) &&
-      make_map_u8(&m.qu, w->up_codes, EH, I / 2, 64, FP4_GU_ROWS, CU_TENSOR_MAP_SWIZZLE_64B) &&
-      make_map_u8(&m.qd, w->down_codes, EI, H / 2, 64, FP4_DN_ROWS / 2, CU_TENSOR_MAP_SWIZZLE_64B) &&
-      make_map_u8(&m.qsg, w->sgate_codes, H, IS / 2, 64, FP4_GU_ROWS, CU_TENSOR_MAP_SWIZZLE_64B) &&
-      make_map_u8(&m.qsu, w->sup_codes, H, IS / 2, 64, FP4_GU_ROWS, CU_TENSOR_MAP_SWIZZLE_64B) &&
-      make_map_u8(&m.qsd, w->sdown_codes, IS, H / 2, 64, FP4_DN_ROWS / 2, CU_TENSOR_MAP_SWIZZLE_64B) &&
-      make_map_u8(&m.sg, w->gate_scales, EH / 16, I, 128, FP4_GU_ROWS / 16) &&
-      make_map_u8(&m.su, w->up_scales, EH / 16, I, 128, FP4_GU_ROWS / 16) &&
-      make_map_u8(&m.sd, w->down_scales, EI / 16, H, 128, FP4_DN_ROWS / 16) &&
-      make_map_u8(&m.ssg, w->sgate_scales, H / 16, IS, 128, FP4_GU_ROWS / 16) &&
-      make_map_u8(&m.ssu, w->sup_scales, H / 16, IS, 128, FP4_GU_ROWS / 16) &&
-      make_map_u8(&m.ssd, w->sdown_scales, IS / 16, H, 128, FP4_DN_ROWS / 16) &&
+      make_map_fp4_rows(&m.qg, w->gate_codes, EI) && make_map_fp4_rows(&m.qu, w->up_codes, EI) &&
+      make_map_fp4_rows(&m.qsg, w->sgate_codes, IS) && make_map_fp4_rows(&m.qsu, w->sup_codes, IS) &&
+      make_map_u8(&m.qd, w->down_codes, EH, I / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+      make_map_u8(&m.qsd, w->sdown_codes, H, IS / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+      make_map_u8(&m.sg, w->gate_scales, EI, H / 16, 128, FP4_GU_COLS) &&
+      make_map_u8(&m.su, w->up_scales, EI, H / 16, 128, FP4_GU_COLS) &&
+      make_map_u8(&m.ssg, w->sgate_scales, IS, H / 16, 128, FP4_GU_COLS) &&
+      make_map_u8(&m.ssu, w->sup_scales, IS, H / 16, 128, FP4_GU_COLS) &&
+      make_map_u8(&m.sd, w->down_scales, EH / 4, 128, 128, 32) &&  // [E*H][32 B] viewed as [E*H/4][128 B]
+      make_map_u8(&m.ssd, w->sdown_scales, H, IS / 16, FP4_DN_ROWS / 16, 128) &&
       cudaMemcpy(h->ws + h->L.fp4maps, &m, sizeof m, cudaMemcpyHostToDevice) == cudaSuccess;
   if (!ok) {
     flint_moe_destroy(h);

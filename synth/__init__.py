@@ -297,8 +297,9 @@ def swa_inputs(B: int, seed: int, device="cuda"):
 #   block scale   s = the smallest E4M3 value >= amax(block of 16 along K) / 6 / t
 #   code          e2m1 = round(w / (s t)) to the nearest of 0, .5, 1, 1.5, 2, 3, 4, 6, ties to the
 #                 even code, sign kept
-# Layouts: codes [.., K, N/2] uint8 (column 2j in the low nibble of byte j), scales [.., K/16, N]
-# uint8 (E4M3 bits), tensor scales [..] fp32.
+# Layouts (K-major, for W [K][N] of y = x W): codes [.., N, K/2] uint8 (W[2j][n] in the low
+# nibble of byte (n, j), W[2j+1][n] in the high), scales [.., N, K/16] uint8 (E4M3 bits), tensor
+# scales [..] fp32.
 
 _E2M1_MID = (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0)  # midpoints between the magnitudes
 
@@ -336,8 +337,9 @@ def nvfp4_quantize(w):
     mag = _e2m1_round_code(v.abs())
     code = (mag | torch.where(v < 0, 8, 0)).to(torch.uint8).view(M, K, N)
     code = torch.where(mag.view(M, K, N) == 0, torch.zeros_like(code), code)  # no negative zero
+    code = code.transpose(1, 2)  # [M, N, K]: K-major
     packed = (code[..., 0::2] | (code[..., 1::2] << 4)).contiguous()
-    return (packed.view(*lead, K, N // 2), bits.contiguous().view(*lead, K // 16, N),
+    return (packed.view(*lead, N, K // 2), bits.transpose(1, 2).contiguous().view(*lead, N, K // 16),
             ts.view(*lead) if lead else ts.view(()))
 
 

@@ -37,19 +37,22 @@ def test_e4m3_by_hand_and_every_byte_against_torch():
 
 
 def test_dequant_of_a_hand_built_block():
-    # K = 32 rows (two scale groups), N = 4 columns
-    codes = np.zeros((32, 2), np.uint8)
-    codes[0, 0] = 0x7 | (0xB << 4)   # row 0: col 0 = +6, col 1 = -1.5
-    codes[17, 1] = 0x2 | (0x9 << 4)  # row 17: col 2 = +1, col 3 = -0.5
-    scales = np.zeros((2, 4), np.uint8)
-    scales[0] = [0x38, 0x40, 0x38, 0x38]   # group 0: 1, 2, 1, 1
-    scales[1] = [0x38, 0x38, 0x3C, 0x01]   # group 1: 1, 1, 1.5, 2^-9
+    # K = 32 (two scale groups), N = 4 columns; K-major: codes [N][K/2], scales [N][K/16]
+    codes = np.zeros((4, 16), np.uint8)
+    codes[0, 0] = 0x7 | (0xB << 4)   # column 0: k = 0 -> +6, k = 1 -> -1.5
+    codes[2, 8] = 0x2 | (0x9 << 4)   # column 2: k = 16 -> +1, k = 17 -> -0.5
+    codes[3, 0] = 0x5                # column 3: k = 0 -> +3
+    scales = np.zeros((4, 2), np.uint8)
+    scales[0] = [0x38, 0x40]   # column 0: group 0 -> 1, group 1 -> 2
+    scales[2] = [0x38, 0x3C]   # column 2: 1, 1.5
+    scales[3] = [0x01, 0x38]   # column 3: 2^-9, 1
     w = oracle.nvfp4_dequant(codes, scales, 0.25)
     want = np.zeros((32, 4))
     want[0, 0] = 6 * 1 * 0.25
-    want[0, 1] = -1.5 * 2 * 0.25
-    want[17, 2] = 1 * 1.5 * 0.25
-    want[17, 3] = -0.5 * 2.0 ** -9 * 0.25
+    want[1, 0] = -1.5 * 1 * 0.25
+    want[16, 2] = 1 * 1.5 * 0.25
+    want[17, 2] = -0.5 * 1.5 * 0.25
+    want[0, 3] = 3 * 2.0 ** -9 * 0.25
     assert np.array_equal(w, want)
 
 
@@ -74,7 +77,9 @@ def numpy_quantize(w):
                 dist = [abs(a - m) for m in E2M1]
                 best = min(range(8), key=lambda i: (dist[i], i % 2))  # nearest, ties to the even code
                 codes[16 * g + r, n] = (best | (8 if v < 0 and best else 0))
-    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8), scales, ts
+    # K-major encoding: codes [N][K/2] (the lower k in the low nibble), scales [N][K/16]
+    ct = codes.T
+    return (ct[:, 0::2] | (ct[:, 1::2] << 4)).astype(np.uint8), np.ascontiguousarray(scales.T), ts
 
 
 def test_round_trip_through_a_numpy_quantiser_and_the_generator_agrees():
@@ -84,7 +89,7 @@ def test_round_trip_through_a_numpy_quantiser_and_the_generator_agrees():
     codes, scales, ts = numpy_quantize(w64)
     dq = oracle.nvfp4_dequant(codes, scales, ts)
     # error bound: half the widest E2M1 step (4 -> 6) times the block's scale
-    s = np.repeat(np.array([[oracle.e4m3_to_f64(b) for b in row] for row in scales]), 16, axis=0) * ts
+    s = np.repeat(np.array([[oracle.e4m3_to_f64(b) for b in row] for row in scales.T]), 16, axis=0) * ts
     assert np.all(np.abs(dq - w64) <= 1.0 * s + 1e-30)
     assert np.max(np.abs(dq - w64)) > 0
     # the block scale is rounded up: no element needed clamping at 6
@@ -97,5 +102,5 @@ def test_round_trip_through_a_numpy_quantiser_and_the_generator_agrees():
 
 
 def test_dequant_rejects_bad_shapes():
-    with pytest.raises(RuntimeError):
-        oracle.nvfp4_dequant(np.zeros((8, 2), np.uint8), np.zeros((1, 4), np.uint8), 1.0)
+    with pytest.raises(RuntimeError):  # K = 4 is not a multiple of the 16-weight scale block
+        oracle.nvfp4_dequant(np.zeros((8, 2), np.uint8), np.zeros((8, 1), np.uint8), 1.0)
