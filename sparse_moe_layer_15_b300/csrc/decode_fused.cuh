@@ -62,7 +62,6 @@ constexpr int OUT_NCB = H / 128;         // 16 column blocks of a down projectio
 constexpr int MAX_STREAM_CTAS = 256;     // largest grid of the decode kernel (the workspace holds its partial slots)
 constexpr int PSLOT = NT_MAX * 256;      // floats of one partial slot: [rows][256] gate|up, or [rows][128] down
 constexpr int REDUNDANT_ROUTING_MAX_T = 4;
-constexpr int PREISSUE_MAX_T = 4;  // step D's first block is issued before its barrier up to this many tokens
 constexpr int MAX_PAIRS = STREAM_MAX_T * K;
 constexpr int XPAD = 8;                  // bf16 padding of a staged input row (bank spread)
 
@@ -1221,24 +1220,14 @@ __device__ __forceinline__ void set_step(Stream& S, const BlockList& L) {
 // Run the current step for the whole CTA: the producer lane streams (its first `pre` blocks
 // were issued already), the consumers compute.
 template <int MODE>
-__device__ void run_step(Stream& S, int pre = 0) {
+__device__ void run_step(Stream& S) {
   if (threadIdx.x >= NCONS) {
-    if (threadIdx.x == NCONS) produce<MODE>(S, pre, S.nb);
+    if (threadIdx.x == NCONS) produce<MODE>(S, 0, S.nb);
   } else {
     consume<MODE>(S);
   }
   S.ring += S.nb;
   __syncthreads();
-}
-
-// Bounded wait (one thread) for blocks [0, n) of the current step to land: a CTA that leaves
-// early must not exit with copies into its shared memory in flight.
-__device__ void drain_issued(Stream& S, int n) {
-  if (threadIdx.x == NCONS)
-    for (int j = 0; j < n; ++j) {
-      const int pos = S.ring + j;
-      mbar_wait_or_flag(S.full + pos % NSTAGE, uint32_t(pos / NSTAGE) & 1u, S.p->status);
-    }
 }
 
 // Spread a bulk L2 prefetch of `bytes` (multiple of 16, below 2^32) at `base` over the grid
@@ -1688,11 +1677,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // parameters (read from the constant bank: a shared-memory copy of them measured 3-4 % slower).
 
 // Up to this many tokens the stack runs in one launch of decode_stack; above, as one launch of
-// decode_fused per layer.  Measured on B300 (12 layers, pre-norm + residual, us per layer): T = 1
-// 34.8 vs 38.5, T = 4 56.0 vs 60.3, T = 16 118.4 vs 119.4, T = 64 259.4 vs 249.8, T = 256 367.8
-// vs 357.0.  The phase trace puts the larger calls' difference in the streaming steps C and D,
-// whose code the two kernels share (the gate/up step streams about 6 % slower inside the layer
-// loop).
+// decode_fused per layer.  Measured on B300 (12 layers, pre-norm + residual, us per layer): one
+// launch against per-layer calls, T = 1 34.8 vs 38.5, T = 4 56.0 vs 60.3, T = 16 118.4 vs 119.4,
+// T = 64 255.2 vs 244.0, T = 256 370.4 vs 355.4 (the last two with the C-D dataflow and the next
+// layer's L2 prefetch below, which took the one-launch T = 1, 4, 16 to 32.8, 50.7, 115.5).  The
+// larger calls lose in the streaming steps, whose code the two kernels share; tensor maps passed
+// as kernel parameters instead of the device table measured the same (one layer, T = 256: 378.9
+// vs 378.9 us).
 constexpr int STACK_ONE_LAUNCH_MAX_T = 16;
 
 // Per-layer entry of the stack's device table (aligned as its tensor maps; the table starts on a
@@ -1700,7 +1691,10 @@ constexpr int STACK_ONE_LAUNCH_MAX_T = 16;
 struct LayerTab {
   StreamMaps maps;
   const float* router_bias;
+  const bf16* w_router;
   const bf16* w_down;
+  const bf16* ws_gate;
+  const bf16* ws_up;
   const bf16* ws_down;
 };
 static_assert(alignof(LayerTab) >= 64 && alignof(LayerTab) <= 256, "tensor maps stay aligned in the table");
@@ -1755,7 +1749,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   S.misc = reinterpret_cast<int*>(sm + Smem::misc);
   S.plist = reinterpret_cast<int*>(sm + Smem::plist);
   S.out = reinterpret_cast<float*>(sm + out_offset(G));
-  S.dataflow = false;  // the layers keep their grid barriers
+  S.dataflow = false;
   S.sig_ctr = nullptr;
   S.sig_n = 0;
   S.pbank = partial_bank(base, 0);
@@ -1803,7 +1797,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     // ---- step A: router partial logits
     {
-      if (threadIdx.x == NCONS + 1) prefetch_share(tab[l].ws_down, uint32_t(IS) * H * 2);
+      if (l == 0 && threadIdx.x == NCONS + 1) prefetch_share(tab[l].ws_down, uint32_t(IS) * H * 2);
       BlockList L;
       L.k_first = L.k_second = KIND_RT;
       L.kb_first = L.kb_second = 1;
@@ -1869,12 +1863,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       L.kb_second = GU_KB;
       L.n_total = L.n_first + ntg * SGU_NCB * GU_KB;
       S.first_slot = 12;
+      S.pbank = partial_bank(base, 0);
+      S.dataflow = true;  // gate/up items signal their token group; step D waits per group
       trace_point(p, 6);
       set_step(S, L);
       run_step<MODE_MOE>(S);
     }
     trace_point(p, 7);
-    // ---- step D (first block issued before the barrier for small calls, as in decode_fused)
+    // ---- step D, with no grid barrier after step C (the dataflow of decode_fused)
     {
       BlockList L;
       L.k_first = KIND_DN;
@@ -1885,18 +1881,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       L.n_total = L.n_first + ntg * OUT_NCB * SD_KB;
       set_step(S, L);
     }
-    const int pre = T <= PREISSUE_MAX_T ? min(1, S.nb) : 0;
-    if (threadIdx.x == NCONS) produce<MODE_MOE>(S, 0, pre);
-    if (!grid_sync(p, ++nbar, S.misc + 12)) {
-      drain_issued(S, pre);
-      return;
-    }
+    S.pbank = partial_bank(base, 1);
     trace_point(p, 8);
     S.first_slot = 13;
-    run_step<MODE_MOE>(S, pre);
+    run_step<MODE_MOE>(S);
+    S.dataflow = false;
     trace_point(p, 9);
+    // The next layer's router and shared-expert weights (13 MB) do not depend on this layer's
+    // results: a CTA that has finished its step-D range asks L2 for its share of them, while HBM
+    // serves the other CTAs' last down blocks, so that the next layer's router step and shared
+    // blocks read from L2.
+    if (l + 1 < n_layers && threadIdx.x == NCONS + 1) {
+      const LayerTab& nx = tab[l + 1];
+      prefetch_share(nx.w_router, uint32_t(H) * E * 2);
+      prefetch_share(nx.ws_gate, uint32_t(H) * IS * 2);
+      prefetch_share(nx.ws_up, uint32_t(H) * IS * 2);
+      prefetch_share(nx.ws_down, uint32_t(IS) * H * 2);
+    }
     if (!grid_sync(p, ++nbar, S.misc + 12)) return;
     trace_point(p, 14);
+    // every step-D wait of this layer is over: clear the token-group counters for the next layer
+    // (the barrier at the end of the combine orders these stores before its first signal)
+    for (int i = blockIdx.x * NTHREADS + threadIdx.x; i < S.meta.groups; i += gridDim.x * NTHREADS) p.hdone[i] = 0u;
+    for (int i = blockIdx.x * NTHREADS + threadIdx.x; i < ntg; i += gridDim.x * NTHREADS) p.hsdone[i] = 0u;
     // ---- the combine by whole rows, and the next layer's pre-norm of the same rows
     const bool norm_next = prenorm && l + 1 < n_layers;
     if (threadIdx.x < NCONS)

@@ -681,7 +681,10 @@ flint_moe_status flint_moe_stack_create(const flint_moe_config* cfg, const flint
          make_map(&t.maps.wsu, w->ws_up, H, IS, 64, GU_ROWS, sw) &&
          make_map(&t.maps.wsd, w->ws_down, IS, H, 64, DN_ROWS, sw);
     t.router_bias = w->router_bias;
+    t.w_router = static_cast<const bf16*>(w->w_router);
     t.w_down = static_cast<const bf16*>(w->w_down);
+    t.ws_gate = static_cast<const bf16*>(w->ws_gate);
+    t.ws_up = static_cast<const bf16*>(w->ws_up);
     t.ws_down = static_cast<const bf16*>(w->ws_down);
   }
   LayerTab* dtab = reinterpret_cast<LayerTab*>(static_cast<uint8_t*>(workspace) + scratch);
