@@ -975,14 +975,15 @@ __device__ void stage_inputs(Stream& S, const Item& it, int xlen, int k0 = 0) {
   const Params& p = *S.p;
   if (S.dataflow && it.kind == KIND_DN) wait_done(p, p.hdone + it.idx / OUT_NCB, gu_ncb<MODE>());
   if (S.dataflow && it.kind == KIND_SD) wait_done(p, p.hsdone + it.idx / OUT_NCB, sgu_ncb<MODE>());
+  // every copy of the group is in flight at once (cp.async, L2 only): one round trip, where a
+  // load-then-store loop would pay one per iteration while the weight stream waits
   bf16* xs = reinterpret_cast<bf16*>(S.sm + Smem::xs);
   const int cpr = xlen / 8;
   const int G = group_rows(p.T);
   for (int q = threadIdx.x; q < G * cpr; q += NCONS) {
     const int t = q / cpr, k8 = q % cpr;
-    uint4 v = make_uint4(0, 0, 0, 0);
+    const bf16* src = p.xin;  // rows nt .. G-1: zero-filled (the address is not read)
     if (t < it.nt) {
-      const bf16* src;
       if (it.kind == KIND_GU)
         src = p.xin + (size_t)(S.perm[it.row0 + t] / K) * H;
       else if (it.kind == KIND_SGU || it.kind == KIND_RT)
@@ -991,20 +992,25 @@ __device__ void stage_inputs(Stream& S, const Item& it, int xlen, int k0 = 0) {
         src = MODE == MODE_DENSE ? p.hs + (size_t)(it.row0 + t) * ID + k0 : p.hs + (size_t)(it.row0 + t) * IS;
       else
         src = p.h + (size_t)(it.row0 + t) * I;
-      v = __ldcg(reinterpret_cast<const uint4*>(src) + k8);
-      if (F16X && (it.kind == KIND_GU || it.kind == KIND_SGU)) {  // bf16 -> f16 (inputs |x| < 65504)
-        float f[8];
-        bf16x8_to_f32(v, f);
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const __half2 h2 = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
-          w[i] = *reinterpret_cast<const uint32_t*>(&h2);
-        }
-        v = make_uint4(w[0], w[1], w[2], w[3]);
-      }
     }
-    *reinterpret_cast<uint4*>(xs + t * (xlen + XPAD) + k8 * 8) = v;
+    cp16(xs + t * (xlen + XPAD) + k8 * 8, src + k8 * 8, t < it.nt);
+  }
+  cp_commit();
+  cp_wait<0>();
+  if (F16X && (it.kind == KIND_GU || it.kind == KIND_SGU)) {
+    // bf16 -> f16 in place (inputs |x| < 65504); each thread converts the copies it made
+    for (int q = threadIdx.x; q < it.nt * cpr; q += NCONS) {
+      uint4* a = reinterpret_cast<uint4*>(xs + (q / cpr) * (xlen + XPAD) + (q % cpr) * 8);
+      float f[8];
+      bf16x8_to_f32(*a, f);
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half2 h2 = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      *a = make_uint4(w[0], w[1], w[2], w[3]);
+    }
   }
   csync();
 }

@@ -85,15 +85,6 @@ __device__ __forceinline__ void frag_a(uint32_t base, int rs, int k0, uint32_t (
   ldsm_x4(base + uint32_t((((q & 1) * 8 + (lane & 7)) * rs + k0 + (q >> 1) * 8) * 2), a);
 }
 
-// cp.async of 16 bytes global -> shared, zero-filled when !valid (src_size 0).
-__device__ __forceinline__ void cp16(void* dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(valid ? 16 : 0)
-               : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
 // Shared memory (dynamic): two chunk buffers of K and V rows, the query rows, the probabilities.
 struct Smem {
   static constexpr int kv = 0;                              // [2 buffers][K | V][KP][RS] bf16
