@@ -89,7 +89,6 @@ struct Params {
   int32_t* out_idx;
   float* out_w;
   int32_t* out_counts;
-  unsigned long long prefetch_bytes_max;  // L2 prefetch budget for the touched down matrices
   unsigned long long* trace;  // [gridDim.x][TRACE_SLOTS] %globaltimer stamps, or null
 };
 

@@ -1606,25 +1606,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   // ---- step C: routed gate/up and the shared gate/up
   {
-    // the touched experts' down matrices are read in step D: prefetch them when they fit
-    const uint32_t per_e = MODE == MODE_FP4 ? uint32_t(I) * H / 2 : uint32_t(I) * H * 2;  // codes / bf16 bytes
-    const uint8_t* dbase = MODE == MODE_FP4 ? p.q_down : reinterpret_cast<const uint8_t*>(p.w_down);
-    if (threadIdx.x == NCONS + 1 && (unsigned long long)S.meta.U * per_e <= p.prefetch_bytes_max) {
-      // 32-bit offsets: U * I * H * 2 <= 512 MB
-      const uint32_t total = per_e * uint32_t(S.meta.U);
-      const uint32_t share = ((total / gridDim.x) + 15u) & ~15u;
-      uint32_t a = share * blockIdx.x;
-      const uint32_t b = a < total ? (total - a > share ? a + share : total) : a;
-      while (a < b) {
-        const int u = int(a / per_e);
-        const uint32_t in_e = a % per_e;
-        uint32_t n = per_e - in_e;
-        if (n > b - a) n = b - a;
-        if (n > 65536u) n = 65536u;
-        prefetch_l2_bulk(dbase + (size_t)S.meta.e[u] * per_e + in_e, uint32_t(n));
-        a += n;
-      }
-    }
     BlockList L;
     const int kgu = kblocks_of<MODE>(p, KIND_GU);
     L.k_first = KIND_GU;
@@ -1698,7 +1679,6 @@ struct LayerTab {
   StreamMaps maps;
   const float* router_bias;
   const bf16* w_router;
-  const bf16* w_down;
   const bf16* ws_gate;
   const bf16* ws_up;
   const bf16* ws_down;
@@ -1843,24 +1823,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     trace_point(p, 5);
     // ---- step C: routed gate/up and the shared gate/up
     {
-      const bf16* w_down = tab[l].w_down;
-      if (threadIdx.x == NCONS + 1 && (unsigned long long)S.meta.U * I * H * 2 <= p.prefetch_bytes_max) {
-        constexpr uint32_t per_e = uint32_t(I) * H * 2;
-        const uint32_t total = per_e * uint32_t(S.meta.U);
-        const uint32_t share = ((total / gridDim.x) + 15u) & ~15u;
-        uint32_t a = share * blockIdx.x;
-        const uint32_t b = a < total ? (total - a > share ? a + share : total) : a;
-        while (a < b) {
-          const int u = int(a / per_e);
-          const uint32_t in_e = a % per_e;
-          uint32_t n = per_e - in_e;
-          if (n > b - a) n = b - a;
-          if (n > 65536u) n = 65536u;
-          prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(w_down + (size_t)S.meta.e[u] * I * H) + in_e,
-                           uint32_t(n));
-          a += n;
-        }
-      }
       BlockList L;
       L.k_first = KIND_GU;
       L.kb_first = GU_KB;

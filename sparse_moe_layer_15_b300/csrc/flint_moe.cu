@@ -180,7 +180,6 @@ struct flint_moe_s {
   Layout L;
   StreamMaps smaps;
   pf::Maps pmaps;  // prefill path (max_tokens > STREAM_MAX_T); pmaps.xin is on xn
-  unsigned long long prefetch_max;
   bool timing;
   bool trace;
   cudaEvent_t ev[2 * MAX_EVENTS];
@@ -266,7 +265,6 @@ Params make_params(flint_moe_t h, const void* x, int T, void* y, int32_t* out_id
   p.out_idx = out_idx;
   p.out_w = out_w;
   p.out_counts = out_counts;
-  p.prefetch_bytes_max = h->prefetch_max;
   p.trace = h->trace ? reinterpret_cast<unsigned long long*>(ws + L.trace) : nullptr;
   return p;
 }
@@ -476,8 +474,6 @@ flint_moe_status create_handle(const flint_moe_config* cfg, const flint_moe_weig
   h->ws = static_cast<uint8_t*>(workspace);
   h->ws_bytes = workspace_bytes;
   h->L = L;
-  h->prefetch_max = 40ull << 20;
-  if (const char* env = std::getenv("FLINT_MOE_PREFETCH_MB")) h->prefetch_max = std::strtoull(env, nullptr, 10) << 20;
   h->timing = false;
   h->trace = false;
   h->n_ev = 0;
@@ -682,7 +678,6 @@ flint_moe_status flint_moe_stack_create(const flint_moe_config* cfg, const flint
          make_map(&t.maps.wsd, w->ws_down, IS, H, 64, DN_ROWS, sw);
     t.router_bias = w->router_bias;
     t.w_router = static_cast<const bf16*>(w->w_router);
-    t.w_down = static_cast<const bf16*>(w->w_down);
     t.ws_gate = static_cast<const bf16*>(w->ws_gate);
     t.ws_up = static_cast<const bf16*>(w->ws_up);
     t.ws_down = static_cast<const bf16*>(w->ws_down);
@@ -872,7 +867,6 @@ extern "C" flint_moe_status flint_moe_forward_noalloc(const flint_moe_weights* w
   h.L = make_layout(NOALLOC_MAX_T);
   if (h.L.total > NOALLOC_BYTES) return FLINT_MOE_ERR_WORKSPACE;
   h.ws_bytes = NOALLOC_BYTES;
-  h.prefetch_max = 40ull << 20;
   h.timing = false;
   h.trace = false;
   h.n_ev = 0;
