@@ -313,7 +313,7 @@ flint_moe_status run_decode_maps(flint_moe_t h, const Params& p, const StreamMap
   const int grid = h->n_sm < MAX_STREAM_CTAS ? h->n_sm : MAX_STREAM_CTAS;
   auto kern = h->fp4 ? decode_fused<MODE_FP4> : h->dense ? decode_fused<MODE_DENSE> : decode_fused<MODE_MOE>;
   e = launch(h, full ? "decode_fused" : "decode_fused_route", kern, grid, NTHREADS,
-             h->fp4 ? fp4_smem_bytes() : fused_smem_bytes(group_rows(p.T)), st, true, p, maps, full ? 0 : 1);
+             h->fp4 ? fp4_smem_bytes() : fused_smem_bytes(group_rows_mode(p.T, h->dense ? MODE_DENSE : MODE_MOE)), st, true, p, maps, full ? 0 : 1);
   return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ERR_CUDA;
 }
 
