@@ -105,11 +105,6 @@ def measured_traffic(kernel, sweep):
     return round(sum(per[str(T)] for T in sweep) / len(sweep))
 
 
-# The stack call runs every layer in one launch up to this many tokens (decode_fused.cuh,
-# STACK_ONE_LAUNCH_MAX_T).
-STACK_ONE_LAUNCH_MAX_T = 16
-
-
 def measured_stack_traffic(T, n_layers):
     """DRAM bytes of one launch of decode_stack over n_layers at T tokens: the committed ncu
     summary profiles/decode_stack_traffic.json holds a small stack's bytes per layer (the
@@ -549,8 +544,8 @@ def run_workload(args, rank, world, local, summary=False):
 def run_stack(args, rank, world, local, summary=False):
     """47 Flint MoE layers (weights seed 100+l, about 76 GB), T=256 tokens (x seed 4); each
     layer x <- x + MoE_l(RMSNorm(x)), eps 1e-6.  One step = the 47 forwards, through the stack
-    call.  --stack-tokens T measures the same stack at T tokens (up to 16: one launch for all
-    layers); --stack-layers N < 47 is a small case for the profiler, not the configuration."""
+    call (one launch of decode_stack for all layers).  --stack-tokens T measures the same stack at
+    T tokens; --stack-layers N < 47 is a small case for the profiler, not the configuration."""
     import torch
 
     import synth
@@ -558,7 +553,6 @@ def run_stack(args, rank, world, local, summary=False):
     from sparse_moe_layer_15_b300 import accounting as acc
 
     L, T = args.stack_layers, args.stack_tokens
-    one_launch = T <= STACK_ONE_LAUNCH_MAX_T
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     peaks = load_peaks()
@@ -567,8 +561,7 @@ def run_stack(args, rank, world, local, summary=False):
     ws = torch.empty(fm.workspace_bytes(T, flags, 1e-6), dtype=torch.uint8, device=dev)
     weights = [synth.flint_weights(seed=100 + l, device=dev) for l in range(L)]
     layers = [fm.FlintMoE(weights[l], max_tokens=T, flags=flags, rms_eps=1e-6, workspace=ws) for l in range(L)]
-    # the public stack call (up to 16 tokens one launch of decode_stack for all layers; above, the
-    # pre-norm and decode kernels layer by layer: measured faster than the one-launch kernel there)
+    # the public stack call: one launch of decode_stack for all layers
     stack_handle = fm.FlintMoEStack(weights, max_tokens=T, flags=flags, rms_eps=1e-6)
     x0 = synth.torch_normal_bf16((T, fm.HIDDEN), 4, synth.TAG_X, 1.0, device=dev)
     x = x0.clone()
@@ -608,20 +601,12 @@ def run_stack(args, rank, world, local, summary=False):
     alg_bytes = sum(acc.algorithmic_bytes(u, T) for u in U)
     flop = acc.flops_per_token() * T * L
     achieved = alg_bytes / (ms * 1e-3) / 1e9
-    if one_launch:
-        roofline = dict(bound="hbm", kernel=f"decode_stack (one launch, {L} layers)", achieved=round(achieved, 1),
-                        peak=peaks["hbm_gbs"], unit="GB/s", frac=round(achieved / peaks["hbm_gbs"], 4),
-                        traffic=measured_stack_traffic(T, L), alg_bytes_per_launch=round(alg_bytes),
-                        peak_source=peaks["source"] + " (hbm_gbs, copy test)",
-                        note="the step is one launch; traffic: DRAM bytes per layer from the committed ncu "
-                             "summary of a small stack, times the layers (null if the sources changed)")
-    else:
-        roofline = dict(bound="hbm", kernel=f"decode_fused (x{L}, + rmsnorm)", achieved=round(achieved, 1),
-                        peak=peaks["hbm_gbs"], unit="GB/s", frac=round(achieved / peaks["hbm_gbs"], 4), traffic=None,
-                        alg_bytes_per_launch=round(alg_bytes / L),
-                        peak_source=peaks["source"] + " (hbm_gbs, copy test)",
-                        note=f"the whole step; the decode kernel is {L} of the {2 * L} launches and nearly all the "
-                             "time")
+    roofline = dict(bound="hbm", kernel=f"decode_stack (one launch, {L} layers)", achieved=round(achieved, 1),
+                    peak=peaks["hbm_gbs"], unit="GB/s", frac=round(achieved / peaks["hbm_gbs"], 4),
+                    traffic=measured_stack_traffic(T, L), alg_bytes_per_launch=round(alg_bytes),
+                    peak_source=peaks["source"] + " (hbm_gbs, copy test)",
+                    note="the step is one launch; traffic: DRAM bytes per layer from the committed ncu "
+                         "summary of a small stack, times the layers (null if the sources changed)")
     xh = x0.cpu().pin_memory()
     yh = torch.empty_like(xh).pin_memory()
 
@@ -645,7 +630,7 @@ def run_stack(args, rank, world, local, summary=False):
                roofline=roofline,
                e2e=dict(value=round(world * T / (e2e_ms * 1e-3), 1), unit="tokens/s",
                         h2d_bytes_per_step=2 * fm.HIDDEN * T, d2h_bytes_per_step=2 * fm.HIDDEN * T),
-               gpu_launches=args.steps * (1 if one_launch else 2 * L), clocks=clk)
+               gpu_launches=args.steps, clocks=clk)
     for lay in layers:
         lay.close()
     stack_handle.close()

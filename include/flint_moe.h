@@ -233,12 +233,12 @@ flint_moe_status flint_moe_noalloc_poll_device_status(flint_stream_t stream);
  * coding model with 2.5B active", section "Built with the Eureka Machine").  A stack handle applies
  * n_layers MoE layers, each with its own weights, in place,
  *     x <- [x +] MoE_l([RMSNorm](x)),  l = 0 .. n_layers-1  (the config's flags, for every layer),
- * For T <= 16 in ONE persistent cooperative kernel launch: each layer's steps as in
- * flint_moe_forward, a grid-wide barrier between layers instead of a kernel boundary, and the
- * next layer's pre-norm done by the CTAs that combine each token row; for larger T (where that
- * kernel measured slower) as the single-layer launches, layer by layer, on `stream`.  Either way
- * the results are bitwise those of n_layers successive flint_moe_forward calls (x in, y = x) with
- * the same config on the layers' weights.  Decode sizes only: cfg->max_tokens <= 256, else
+ * in ONE persistent cooperative kernel launch: each layer's steps as in flint_moe_forward, a
+ * grid-wide barrier between layers instead of a kernel boundary, the next layer's pre-norm done by
+ * the CTAs that combine each token row, and the next layer's router and shared-expert weights
+ * requested into L2 while this layer's down step finishes.  The results are bitwise those of
+ * n_layers successive flint_moe_forward calls (x in, y = x) with the same config on the layers'
+ * weights.  Decode sizes only: cfg->max_tokens <= 256, else
  * FLINT_MOE_ERR_UNSUPPORTED. */
 typedef struct flint_moe_stack_s* flint_moe_stack_t;
 

@@ -1681,15 +1681,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // and prefetch pointers come from a table in device memory; everything else is the launch's
 // parameters (read from the constant bank: a shared-memory copy of them measured 3-4 % slower).
 
-// Up to this many tokens the stack runs in one launch of decode_stack; above, as one launch of
-// decode_fused per layer.  Measured on B300 (12 layers, pre-norm + residual, us per layer): one
-// launch against per-layer calls, T = 1 34.8 vs 38.5, T = 4 56.0 vs 60.3, T = 16 118.4 vs 119.4,
-// T = 64 255.2 vs 244.0, T = 256 370.4 vs 355.4 (the last two with the C-D dataflow and the next
-// layer's L2 prefetch below, which took the one-launch T = 1, 4, 16 to 32.8, 50.7, 115.5).  The
-// larger calls lose in the streaming steps, whose code the two kernels share; tensor maps passed
-// as kernel parameters instead of the device table measured the same (one layer, T = 256: 378.9
-// vs 378.9 us).
-constexpr int STACK_ONE_LAUNCH_MAX_T = 16;
+// The stack runs in one launch at every decode size.  Measured on B300 (12 layers, pre-norm +
+// residual, us per layer, one launch against per-layer calls of decode_fused): T = 1 32.8 vs
+// 38.5, T = 4 50.7 vs 60.3, T = 32 156.8 vs 160.5, T = 64 220.8 vs 224.8, T = 256 301.7 vs 303.8.
 
 // Per-layer entry of the stack's device table (aligned as its tensor maps; the table starts on a
 // 256-byte boundary).

@@ -162,8 +162,6 @@ struct flint_moe_stack_s {
   flint_moe_t h;    // handle on layer 0's weights and the shared scratch
   int n_layers;
   void* tab;        // device table of LayerTab entries (in the workspace)
-  std::vector<flint_moe_weights> w;  // the layers' weights (per-layer launches)
-  std::vector<StreamMaps> maps;      // host copies of the layers' tensor maps
 };
 
 struct flint_moe_s {
@@ -697,9 +695,6 @@ flint_moe_status flint_moe_stack_create(const flint_moe_config* cfg, const flint
   st->h = h;
   st->n_layers = n_layers;
   st->tab = dtab;
-  st->w.assign(layers, layers + n_layers);
-  st->maps.resize(n_layers);
-  for (int l = 0; l < n_layers; ++l) st->maps[l] = tab[l].maps;
   *out = st;
   return FLINT_MOE_OK;
 }
@@ -712,35 +707,12 @@ flint_moe_status flint_moe_stack_forward(flint_moe_stack_t st, void* x, int T, i
   if (s != FLINT_MOE_OK) return s;
   h->n_ev = 0;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (T > STACK_ONE_LAUNCH_MAX_T) {
-    // per-layer launches of the single-layer path (measured faster at these sizes)
-    for (int l = 0; l < st->n_layers; ++l) {
-      const flint_moe_weights& w = st->w[l];
-      Params p = make_params(h, x, T, x, topk_idx ? topk_idx + (size_t)l * T * K : nullptr,
-                             topk_w ? topk_w + (size_t)l * T * K : nullptr, nullptr);
-      p.w_router = static_cast<const bf16*>(w.w_router);
-      p.router_bias = w.router_bias;
-      p.w_gate = static_cast<const bf16*>(w.w_gate);
-      p.w_up = static_cast<const bf16*>(w.w_up);
-      p.w_down = static_cast<const bf16*>(w.w_down);
-      p.ws_gate = static_cast<const bf16*>(w.ws_gate);
-      p.ws_up = static_cast<const bf16*>(w.ws_up);
-      p.ws_down = static_cast<const bf16*>(w.ws_down);
-      if (p.trace && cudaMemsetAsync(p.trace, 0, sizeof(unsigned long long) * MAX_TRACE_CTAS * TRACE_SLOTS, cs) !=
-                         cudaSuccess)
-        return FLINT_MOE_ERR_CUDA;
-      const flint_moe_status r = run_decode_maps(h, p, st->maps[l], cs, true);
-      if (r != FLINT_MOE_OK) return r;
-    }
-    return FLINT_MOE_OK;
-  }
   Params p = make_params(h, x, T, x, topk_idx, topk_w, nullptr);
   if (p.trace && cudaMemsetAsync(p.trace, 0, sizeof(unsigned long long) * MAX_TRACE_CTAS * TRACE_SLOTS, cs) !=
                      cudaSuccess)
     return FLINT_MOE_ERR_CUDA;
   const int grid = h->n_sm < MAX_STREAM_CTAS ? h->n_sm : MAX_STREAM_CTAS;
-  const cudaError_t e = launch(h, "decode_stack", decode_stack, grid, NTHREADS, fused_smem_bytes(group_rows(T)),
-                               reinterpret_cast<cudaStream_t>(stream), true, p,
+  const cudaError_t e = launch(h, "decode_stack", decode_stack, grid, NTHREADS, fused_smem_bytes(group_rows(T)), cs, true, p,
                                static_cast<const LayerTab*>(st->tab), st->n_layers);
   return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ERR_CUDA;
 }

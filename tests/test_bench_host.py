@@ -64,10 +64,3 @@ def test_two_gloo_ranks_barrier_max_and_rank0_output():
     assert out1 == ""
 
 
-def test_stack_one_launch_threshold_matches_the_library():
-    import re
-    sys.path.insert(0, ROOT)
-    import bench
-    src = open(os.path.join(ROOT, "sparse_moe_layer_15_b300", "csrc", "decode_fused.cuh")).read()
-    m = re.search(r"constexpr int STACK_ONE_LAUNCH_MAX_T = (\d+);", src)
-    assert m and int(m.group(1)) == bench.STACK_ONE_LAUNCH_MAX_T

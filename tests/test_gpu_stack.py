@@ -3,7 +3,7 @@ seed 100 + l, about 76 GB resident), checked layer by layer with teacher forcing
 layer l takes the GPU's bf16 input to layer l, on sampled layers 0, 23 and 46 -- routing and
 outputs on all 256 tokens.  A routing flip in an early layer would make
 an end-to-end comparison meaningless, so the end-to-end output is only checked to be finite and
-bitwise deterministic, and the stack handle (one launch at 16 tokens) must reproduce the per-layer
+bitwise deterministic, and the stack handle (one launch for the 47 layers) must reproduce the per-layer
 results bitwise."""
 import pytest
 import torch
@@ -58,8 +58,8 @@ def test_stack_47_layers_teacher_forced_parity():
         assert rep["ok"], (l, rep)
     for lay in layers:
         lay.close()
-    # the stack handle: bitwise the per-layer result, at T = 256 (per-layer launches) and, through
-    # all 47 layers in one launch, at 16 tokens
+    # the stack handle (all 47 layers in one launch): bitwise the per-layer result, at T = 256 and
+    # at 16 tokens
     stack = fm.FlintMoEStack(weights, max_tokens=T, flags=flags, rms_eps=EPS)
     x = x0.clone()
     stack.forward(x)

@@ -1,5 +1,5 @@
-"""The layer stack (flint_moe_stack_*: one launch of decode_stack up to 16 tokens, per-layer
-launches above) against successive single-layer calls on the same weights: the results, and
+"""The layer stack (flint_moe_stack_*: one launch of decode_stack for all layers) against
+successive single-layer calls on the same weights: the results, and
 every layer's routing, must be bitwise equal (the stack kernel runs each layer's steps with the
 same arithmetic; the single-layer path is itself checked against the oracle in
 test_gpu_parity.py and test_gpu_stack.py)."""
@@ -61,8 +61,7 @@ def test_stack_equals_layer_calls_prenorm_residual(layer_weights, T):
 
 @pytest.mark.parametrize("T", [16, 64, 256])
 def test_stack_equals_layer_calls_without_norm_or_residual(layer_weights, T):
-    # T = 16: one launch; T > 16: per-layer launches with y == x and the router and gate/up
-    # reading x directly (no pre-norm copy), i.e. the layer reads and overwrites one buffer
+    # no pre-norm copy: the router and gate/up read x directly, and the combine overwrites it
     x0 = synth.torch_normal_bf16((T, fm.HIDDEN), 4100, synth.TAG_X, 1.0, device=DEV)
     ref, _, _ = per_layer(layer_weights[:2], x0, 0, T)
     stack = fm.FlintMoEStack(layer_weights[:2], max_tokens=T, flags=0)
