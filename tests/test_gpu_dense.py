@@ -57,6 +57,20 @@ def test_dense_layer_all_tokens(wd, host_w, T):
     layer.close()
 
 
+def test_dense_layer_full_prefill_size_sampled(wd, host_w):
+    # the bench's dense workload at T = 8192 (weights seed 7, x seed 600 + T as there): every 16th
+    # token, which samples every 256-row group of the GEMM tiles
+    T = 8192
+    layer = fm.FlintDense(wd, max_tokens=T)
+    x = synth.torch_normal_bf16((T, fm.HIDDEN), 600 + T, synth.TAG_X, 1.0, device=DEV)
+    y = layer.forward(x)
+    torch.cuda.synchronize()
+    assert layer.poll_device_status() == 0
+    rows = torch.arange(0, T, 16, device=DEV)
+    check(y[rows], reference(host_w, x[rows]))
+    layer.close()
+
+
 @pytest.mark.parametrize("T", [4, 512])
 def test_dense_layer_prenorm_residual_in_place(wd, host_w, T):
     flags = fm.FLAG_PRE_RMSNORM | fm.FLAG_RESIDUAL
