@@ -1301,32 +1301,37 @@ __device__ void route_tokens(const Params& p, const float* bias, int32_t* out_id
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (warp < nt) {
     const int tok = toks[warp];
-    uint64_t key[8];
+    // lane holds experts lane + 32 q; key = the logit's bits in an order-preserving unsigned form
+    // (a non-NaN logit keys above 0, so 0 marks a taken expert).  Each round: the warp's largest
+    // key (redux max over the lanes' own maxima), then the lowest expert holding it (redux min):
+    // the order (logit desc, index asc), i.e. (score desc, index asc).
+    uint32_t key[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      const int ex = lane + 32 * q;
-      const uint32_t u = __float_as_uint(scores[warp * E + ex]);
-      const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-      key[q] = (uint64_t(ord) << 32) | uint32_t(E - 1 - ex);
+      const uint32_t u = __float_as_uint(scores[warp * E + lane + 32 * q]);
+      key[q] = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
     }
+    uint32_t own = 0;  // this lane's largest remaining key
+#pragma unroll
+    for (int q = 0; q < 8; ++q) own = key[q] > own ? key[q] : own;
     float sel_s[K];
     int sel_e[K];
 #pragma unroll
     for (int jj = 0; jj < K; ++jj) {
-      uint64_t best = 0;
+      const uint32_t best = __reduce_max_sync(0xffffffffu, own);
+      uint32_t mine = 0xffffffffu;  // this lane's lowest expert with the best key
 #pragma unroll
-      for (int q = 0; q < 8; ++q) best = key[q] > best ? key[q] : best;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
-        best = o > best ? o : best;
-      }
-      const int ex = E - 1 - int(best & 0xFFFFFFFFu);
+      for (int q = 7; q >= 0; --q)
+        if (key[q] == best) mine = uint32_t(lane + 32 * q);
+      const int ex = int(__reduce_min_sync(0xffffffffu, mine));
       sel_e[jj] = ex;
       sel_s[jj] = 1.0f / (1.0f + expf(-scores[warp * E + ex]));
+      if ((ex & 31) == lane) {
+        key[ex >> 5] = 0u;
+        own = 0;
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (lane + 32 * q == ex) key[q] = 0;  // a non-NaN logit keys above 0: an emptied slot never wins
+        for (int q = 0; q < 8; ++q) own = key[q] > own ? key[q] : own;
+      }
     }
     if (lane == 0) {
       float sum = 0.f;
