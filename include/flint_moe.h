@@ -18,7 +18,9 @@
  *   - bf16 tensors are passed as `const void*` (IEEE bfloat16, row-major, densely packed,
  *     16-byte aligned base).  Matrices use the math orientation y = x W.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = legacy default
- *     stream).  route / forward make no host synchronisation and no allocation.
+ *     stream).  route / forward make no host synchronisation and no allocation, so
+ *     flint_moe_forward and flint_moe_stack_forward can be captured in a CUDA graph and
+ *     replayed (each call leaves the workspace's counters at zero).
  *   - Argument errors are returned synchronously and nothing is enqueued.
  *   - Errors detected on the device (a bounded wait that ran out, an index out of range)
  *     are recorded in a status word inside the workspace; they are sticky until read by
