@@ -8,6 +8,7 @@ import torch
 
 import synth
 import sparse_moe_layer_15_b300 as fm
+from tests import parity
 
 pytestmark = pytest.mark.gpu
 
@@ -57,6 +58,32 @@ def test_stack_equals_layer_calls_prenorm_residual(layer_weights, T):
     torch.cuda.synchronize()
     assert torch.equal(x2.view(torch.int16), ref.view(torch.int16))
     stack.close()
+
+
+@pytest.mark.parametrize("T", [1, 64])
+def test_stack_with_a_router_bias_per_layer(T):
+    # each layer has its own N(0, 0.5) router bias (the prefill workload's kind): the stack must
+    # take layer l's bias from its table, so the routing and outputs equal the layer calls', and
+    # the last layer meets the parity rule against the oracle on the stack's own input to it
+    flags = fm.FLAG_PRE_RMSNORM | fm.FLAG_RESIDUAL
+    weights = [synth.flint_weights(seed=100 + l, device=DEV, bias="normal", bias_seed=300 + l)
+               for l in range(N_LAYERS)]
+    x0 = synth.torch_normal_bf16((T, fm.HIDDEN), 4300 + T, synth.TAG_X, 1.0, device=DEV)
+    ref, ref_idx, ref_gw = per_layer(weights, x0, flags, T)
+    prefix, _, _ = per_layer(weights[:-1], x0, flags, T)
+    stack = fm.FlintMoEStack(weights, max_tokens=T, flags=flags, rms_eps=EPS)
+    idx = torch.full((N_LAYERS, T, fm.TOP_K), -1, dtype=torch.int32, device=DEV)
+    gw = torch.zeros((N_LAYERS, T, fm.TOP_K), dtype=torch.float32, device=DEV)
+    x = x0.clone()
+    stack.forward(x, topk_idx=idx, topk_w=gw)
+    torch.cuda.synchronize()
+    assert stack.poll_device_status() == 0
+    assert torch.equal(idx, ref_idx)
+    assert torch.equal(x.view(torch.int16), ref.view(torch.int16))
+    stack.close()
+    rep = parity.compare(parity.oracle_reference(weights[-1], prefix, range(T), eps=EPS, residual=True), x,
+                         idx[-1], gw[-1])
+    assert rep["ok"], rep
 
 
 @pytest.mark.parametrize("T", [16, 64, 256])
