@@ -65,7 +65,7 @@ def test_decode_sweep(w0, layer0, T):
     assert_parity(parity.compare(ref, y, idx, gw))
 
 
-@pytest.mark.parametrize("T", [3, 37, 256])
+@pytest.mark.parametrize("T", [3, 37, 65, 100, 200, 256])  # 65..200: 16-row groups with a ragged last one
 def test_ragged_and_max_stream_sizes(w0, layer0, T):
     x = x_rows(T, 77 + T)
     y, idx, gw = run_forward(layer0, x)
